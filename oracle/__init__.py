@@ -1,0 +1,111 @@
+"""fp64 CPU oracle for GQA online-softmax attention -- TEST INFRASTRUCTURE.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg use this
+package.  The CUDA library never imports it and it imports nothing from the
+library.  The arithmetic lives in ``attn_oracle.c`` (plain C, fp64); this file
+only marshals numpy arrays through ctypes.
+
+Every function takes fp32 inputs (numpy, C-contiguous) and returns fp64
+results.  Layouts and window rules are those of the three shader pages:
+meganeura 0.2.0 src/shaders/attention.wgsl (forward), meganeura 0.2.0
+src/shaders/cached_attention.wgsl (decode) and cera
+src/backend/shaders/attention_prefill.wgsl (prefill).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+CAUSAL, FULL, CROSS = 0, 1, 2
+
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_c_int = ctypes.c_int
+
+
+def load(lib_path=None):
+    """Load (building first if needed) an oracle shared library."""
+    path = lib_path or _build.build()
+    lib = ctypes.CDLL(path)
+    lib.oracle_forward.restype = _c_int
+    lib.oracle_forward.argtypes = [_f32p, _f32p, _f32p, _f64p, ctypes.c_void_p,
+                                   _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                   ctypes.c_void_p, _c_int]
+    lib.oracle_decode.restype = _c_int
+    lib.oracle_decode.argtypes = [_f32p, _f32p, _f32p, ctypes.c_uint, _f64p,
+                                  _c_int, _c_int, _c_int, _c_int]
+    lib.oracle_prefill.restype = _c_int
+    lib.oracle_prefill.argtypes = [_f32p, _f32p, _f32p, _f64p] + [_c_int] * 6 + \
+        [ctypes.c_float] + [_c_int] * 4 + [ctypes.c_void_p, _c_int]
+    lib.oracle_num_threads.restype = _c_int
+    lib.oracle_num_threads.argtypes = []
+    return lib
+
+
+class Oracle:
+    """numpy front end over one oracle shared library."""
+
+    def __init__(self, lib_path=None):
+        self.lib = load(lib_path)
+
+    def num_threads(self):
+        return int(self.lib.oracle_num_threads())
+
+    @staticmethod
+    def _rows(rows):
+        if rows is None:
+            return None, 0, None
+        arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        return arr.ctypes.data_as(ctypes.c_void_p), int(arr.size), arr
+
+    def forward(self, q, k, v, q_seq, kv_seq, H, G, D, mask, rows=None, want_lse=True):
+        """Returns (out [q_seq, H*D], lse [q_seq, H, 2]); rows not listed stay NaN."""
+        q, k, v = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v))
+        out = np.full((max(q_seq, 0), H * D), np.nan)
+        lse = np.full((max(q_seq, 0), H, 2), np.nan)
+        rp, nr, keep = self._rows(rows)
+        rc = self.lib.oracle_forward(q.reshape(-1), k.reshape(-1), v.reshape(-1), out.reshape(-1),
+                                     lse.ctypes.data_as(ctypes.c_void_p) if want_lse else None,
+                                     q_seq, kv_seq, H, G, D, mask, rp, nr)
+        del keep
+        if rc != 0:
+            raise ValueError("oracle_forward rejected its arguments")
+        return out, lse
+
+    def decode(self, q, k_cache, v_cache, kv_pos, H, G, D, max_seq):
+        """Returns out [1, H*D]."""
+        q, k_cache, v_cache = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k_cache, v_cache))
+        out = np.full((1, H * D), np.nan)
+        rc = self.lib.oracle_decode(q.reshape(-1), k_cache.reshape(-1), v_cache.reshape(-1),
+                                    int(kv_pos), out.reshape(-1), H, G, D, max_seq)
+        if rc != 0:
+            raise ValueError("oracle_decode rejected its arguments")
+        return out
+
+    def prefill(self, q_batch, k_cache, v_cache, out_rows, n_queries, H, G, D, kv_dim, max_seq,
+                scale, start_pos, q_stride, out_stride, q_base, rows=None):
+        """Returns out_batch [out_rows, out_stride] (fp64, NaN where not written)."""
+        q_batch, k_cache, v_cache = (np.ascontiguousarray(x, dtype=np.float32)
+                                     for x in (q_batch, k_cache, v_cache))
+        out = np.full((out_rows, out_stride), np.nan)
+        rp, nr, keep = self._rows(rows)
+        rc = self.lib.oracle_prefill(q_batch.reshape(-1), k_cache.reshape(-1), v_cache.reshape(-1),
+                                     out.reshape(-1), n_queries, H, G, D, kv_dim, max_seq,
+                                     float(scale), start_pos, q_stride, out_stride, q_base, rp, nr)
+        del keep
+        if rc != 0:
+            raise ValueError("oracle_prefill rejected its arguments")
+        return out
+
+
+_default = None
+
+
+def default():
+    """Process-wide oracle instance (built on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default

@@ -1,0 +1,238 @@
+/*
+ * attn_oracle.c -- fp64 CPU oracle for grouped-query scaled-dot-product
+ * attention (forward + per-row max/log-sum, cached decode, batched prefill).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously-correct
+ * reference that the CUDA library is checked against.  Only the test suite,
+ * the smoke check and the CPU-baseline leg of the benchmark load it; the
+ * library itself never links, calls or reads anything here, and nothing here
+ * includes a header of the library.
+ *
+ * What it computes.  The three shader pages (meganeura 0.2.0
+ * src/shaders/attention.wgsl, meganeura 0.2.0 src/shaders/cached_attention.wgsl,
+ * cera src/backend/shaders/attention_prefill.wgsl) compute softmax attention
+ * with an online (streaming) softmax; the prefill page's header comment states
+ * the result equals a plain batched softmax up to floating-point roundoff.  So
+ * the oracle is that plain definition, one (query row, head) at a time:
+ *
+ *   g      = h / (H / G)                          (GQA head map, all pages)
+ *   s_t    = scale * sum_d q[d] * k[t][g][d]       t in [0, n)
+ *   m      = max_t s_t
+ *   l      = sum_t exp(s_t - m)
+ *   out[d] = sum_t exp(s_t - m) * v[t][g][d] / l
+ *   lse    = (m, log l)        (attention.wgsl, fn main, final store: the
+ *                               pair (max_score, log(sum_exp)))
+ *   n == 0 -> out = 0, lse = (-1e30, -1e30)   (attention.wgsl, fn main: the
+ *                               select() guards on sum_exp == 0 with the
+ *                               initial max of -1e30 left in place)
+ *
+ * Window length n per row (its first key is always 0):
+ *   forward causal  n = pos + 1        attention.wgsl header "Variants"
+ *   forward full    n = q_seq          (same)
+ *   forward cross   n = kv_seq         (same)
+ *   decode          n = min(kv_pos + 1, max_seq)
+ *                   cached_attention.wgsl, fn main (kv_len = kv_pos + 1);
+ *                   the max_seq clamp is the prefill page's defensive belt
+ *                   applied to decode as well.
+ *   prefill         n = min(start_pos + q_base + i + 1, max_seq)
+ *                   attention_prefill.wgsl, fn attention_prefill (pos_q,
+ *                   seq_len).
+ *
+ * Scores, exponentials and sums are fp64; the fp32 inputs are widened
+ * exactly.  scale is 1/sqrt(head_dim) in fp64 for forward and decode (both
+ * meganeura pages use inverseSqrt(head_dim)); prefill takes the fp32 scale
+ * argument (the cera page passes it as f32 bits) and widens it.
+ *
+ * Parallelism: rows are independent; with OpenMP the (row, head) loop is
+ * split across threads.  Nothing else is reordered: each score row is
+ * materialised in full and reduced in index order.
+ *
+ * Return value of every entry point: 0 on success, -1 on invalid arguments.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_EMPTY_LSE (-1e30)
+
+/* One (row, head): q points at head_dim query values; k and v point at key
+ * row 0 of this kv head, consecutive key rows kv_stride floats apart.
+ * s is caller scratch with room for n doubles. */
+static void attend_row(const float *q, const float *k, const float *v,
+                       size_t kv_stride, size_t n, int head_dim, double scale,
+                       double *s, double *out, double *m_out, double *logl_out)
+{
+    if (n == 0) {
+        for (int d = 0; d < head_dim; ++d) out[d] = 0.0;
+        *m_out = ORACLE_EMPTY_LSE;
+        *logl_out = ORACLE_EMPTY_LSE;
+        return;
+    }
+    double m = -INFINITY;
+    for (size_t t = 0; t < n; ++t) {
+        const float *kt = k + t * kv_stride;
+        double dot = 0.0;
+        for (int d = 0; d < head_dim; ++d) dot += (double)q[d] * (double)kt[d];
+        s[t] = dot * scale;
+        if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (size_t t = 0; t < n; ++t) {
+        s[t] = exp(s[t] - m);
+        l += s[t];
+    }
+    for (int d = 0; d < head_dim; ++d) {
+        double acc = 0.0;
+        for (size_t t = 0; t < n; ++t) acc += s[t] * (double)v[t * kv_stride + d];
+        out[d] = acc / l;
+    }
+    *m_out = m;
+    *logl_out = log(l);
+}
+
+static int bad_heads(int H, int G, int D)
+{
+    return H <= 0 || G <= 0 || D <= 0 || (H % G) != 0;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Forward attention (attention.wgsl, fn main).
+ *   q    [q_seq, H*D]        out [q_seq, H*D] (only the listed rows written)
+ *   k, v [kv_seq, G*D]       lse [q_seq, H, 2] or NULL
+ *   mask 0 causal (needs kv_seq == q_seq), 1 full (kv_seq == q_seq), 2 cross
+ *   rows: query positions to compute (NULL -> all q_seq of them)
+ */
+int oracle_forward(const float *q, const float *k, const float *v,
+                   double *out, double *lse, int q_seq, int kv_seq,
+                   int H, int G, int D, int mask, const int *rows, int n_rows)
+{
+    if (bad_heads(H, G, D) || q_seq < 0 || kv_seq < 0 || mask < 0 || mask > 2) return -1;
+    if (mask != 2 && kv_seq != q_seq) return -1;
+    if (rows == NULL) n_rows = q_seq;
+    for (int r = 0; r < n_rows; ++r) {
+        int pos = rows ? rows[r] : r;
+        if (pos < 0 || pos >= q_seq) return -1;
+    }
+    const int gs = H / G;
+    const size_t kv_dim = (size_t)G * D;
+    const double scale = 1.0 / sqrt((double)D);
+    int err = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(kv_seq > 0 ? kv_seq : 1));
+        if (s == NULL) {
+#pragma omp atomic write
+            err = -1;
+        } else {
+#pragma omp for collapse(2) schedule(dynamic, 4)
+            for (int r = 0; r < n_rows; ++r) {
+                for (int h = 0; h < H; ++h) {
+                    const int pos = rows ? rows[r] : r;
+                    const int g = h / gs;
+                    size_t n = (mask == 0) ? (size_t)pos + 1 : (size_t)kv_seq;
+                    const size_t qo = (size_t)pos * H * D + (size_t)h * D;
+                    double m, logl;
+                    attend_row(q + qo, k + (size_t)g * D, v + (size_t)g * D, kv_dim, n, D,
+                               scale, s, out + qo, &m, &logl);
+                    if (lse) {
+                        lse[((size_t)pos * H + h) * 2] = m;
+                        lse[((size_t)pos * H + h) * 2 + 1] = logl;
+                    }
+                }
+            }
+        }
+        free(s);
+    }
+    return err;
+}
+
+/*
+ * Cached single-token decode (cached_attention.wgsl, fn main).
+ *   q [1, H*D]; k_cache, v_cache [max_seq, G*D]; out [1, H*D]
+ *   attends to key positions 0..kv_pos inclusive, clamped to max_seq rows.
+ */
+int oracle_decode(const float *q, const float *k_cache, const float *v_cache,
+                  unsigned kv_pos, double *out, int H, int G, int D, int max_seq)
+{
+    if (bad_heads(H, G, D) || max_seq < 0) return -1;
+    const int gs = H / G;
+    const size_t kv_dim = (size_t)G * D;
+    const double scale = 1.0 / sqrt((double)D);
+    size_t n = (size_t)kv_pos + 1;
+    if (n > (size_t)max_seq) n = (size_t)max_seq;
+    double *s = (double *)malloc(sizeof(double) * (n > 0 ? n : 1));
+    if (s == NULL) return -1;
+    for (int h = 0; h < H; ++h) {
+        const int g = h / gs;
+        double m, logl;
+        attend_row(q + (size_t)h * D, k_cache + (size_t)g * D, v_cache + (size_t)g * D,
+                   kv_dim, n, D, scale, s, out + (size_t)h * D, &m, &logl);
+    }
+    free(s);
+    return 0;
+}
+
+/*
+ * Batched causal prefill (attention_prefill.wgsl, fn attention_prefill).
+ *   q_batch rows (q_base + i) * q_stride, head slice at h * D
+ *   out_batch rows (q_base + i) * out_stride, head slice at h * D
+ *   k_cache, v_cache [max_seq, kv_dim], kv head slice at g * D
+ *   window of local query i: min(start_pos + q_base + i + 1, max_seq)
+ *   rows: local query indices i to compute (NULL -> 0..n_queries-1)
+ */
+int oracle_prefill(const float *q_batch, const float *k_cache, const float *v_cache,
+                   double *out_batch, int n_queries, int H, int G, int D, int kv_dim,
+                   int max_seq, float scale, int start_pos, int q_stride, int out_stride,
+                   int q_base, const int *rows, int n_rows)
+{
+    if (bad_heads(H, G, D) || n_queries < 0 || max_seq < 0 || start_pos < 0 || q_base < 0)
+        return -1;
+    if (kv_dim < G * D || q_stride < H * D || out_stride < H * D) return -1;
+    if (rows == NULL) n_rows = n_queries;
+    for (int r = 0; r < n_rows; ++r) {
+        int i = rows ? rows[r] : r;
+        if (i < 0 || i >= n_queries) return -1;
+    }
+    const int gs = H / G;
+    const double sc = (double)scale;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(max_seq > 0 ? max_seq : 1));
+        if (s == NULL) {
+#pragma omp atomic write
+            err = -1;
+        } else {
+#pragma omp for collapse(2) schedule(dynamic, 4)
+            for (int r = 0; r < n_rows; ++r) {
+                for (int h = 0; h < H; ++h) {
+                    const int i = rows ? rows[r] : r;
+                    const size_t q_global = (size_t)q_base + (size_t)i;
+                    size_t n = (size_t)start_pos + q_global + 1;
+                    if (n > (size_t)max_seq) n = (size_t)max_seq;
+                    const int g = h / gs;
+                    double m, logl;
+                    attend_row(q_batch + q_global * q_stride + (size_t)h * D,
+                               k_cache + (size_t)g * D, v_cache + (size_t)g * D,
+                               (size_t)kv_dim, n, D, sc, s,
+                               out_batch + q_global * out_stride + (size_t)h * D, &m, &logl);
+                }
+            }
+        }
+        free(s);
+    }
+    return err;
+}

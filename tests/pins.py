@@ -1,0 +1,328 @@
+"""Pins for the fp64 oracle: facts fixed by the pages or by mathematics.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with something it must reproduce.  They are run on
+the real oracle (tests/test_oracle.py) and on deliberately broken copies of it
+(tests/test_oracle_mutants.py), which shows that a plausible slip in the
+oracle -- a dropped term, a wrong sign or index, a transposed operand --
+fails at least one of them.
+
+Nothing here re-types the oracle's materialised formula.  The pins are:
+  * PyTorch's own scaled_dot_product_attention (fp64, CPU) as an independent
+    library routine for the same definition, GQA head map included;
+  * the pages' own streaming recurrence (attention.wgsl, fn main: running
+    max, correction, weight; final (max_score, log(sum_exp)) store), run
+    element by element in pure Python on tiny shapes;
+  * closed forms (one-key window, constant V rows, Q = 0, a three-key case
+    worked by hand, the empty window);
+  * invariants (GQA == MHA with replicated K/V heads, softmax normalisation,
+    joint permutation of keys, causal prefix independence, shift of K along a
+    fixed vector, decode/prefill/forward window consistency, strides).
+"""
+import math
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from attention_gqa_online_gb300 import synthetic
+
+CAUSAL, FULL, CROSS = 0, 1, 2
+EMPTY_LSE = -1e30
+
+
+def _np(t):
+    return t.numpy() if isinstance(t, torch.Tensor) else t
+
+
+def _small(seed=0, q_seq=16, kv_seq=None, H=4, G=2, D=64, **kw):
+    kv = q_seq if kv_seq is None else kv_seq
+    q, k, v = synthetic.forward_inputs(q_seq, kv, H, G, D, seed=seed, **kw)
+    return _np(q), _np(k), _np(v)
+
+
+def _scores(q, k, H, G, D, pos, h, n):
+    """Score row of (pos, h) over keys [0, n), fp64 (used by invariants only)."""
+    g = h // (H // G)
+    qv = q[pos, h * D:(h + 1) * D].astype(np.float64)
+    kk = k[:n, g * D:(g + 1) * D].astype(np.float64)
+    return kk @ qv / math.sqrt(D)
+
+
+# ---------------------------------------------------------------- library routine
+def _sdpa(q, k, v, q_seq, kv_seq, H, G, D, causal):
+    qt = torch.from_numpy(q.astype(np.float64)).reshape(q_seq, H, D).transpose(0, 1)[None]
+    kt = torch.from_numpy(k.astype(np.float64)).reshape(kv_seq, G, D).transpose(0, 1)[None]
+    vt = torch.from_numpy(v.astype(np.float64)).reshape(kv_seq, G, D).transpose(0, 1)[None]
+    o = F.scaled_dot_product_attention(qt, kt, vt, is_causal=causal, enable_gqa=True)
+    return o[0].transpose(0, 1).reshape(q_seq, H * D).numpy()
+
+
+def pin_sdpa_causal(orc):
+    q, k, v = _small(seed=0)
+    out, _ = orc.forward(q, k, v, 16, 16, 4, 2, 64, CAUSAL)
+    ref = _sdpa(q, k, v, 16, 16, 4, 2, 64, True)
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def pin_sdpa_full(orc):
+    q, k, v = _small(seed=0)
+    out, _ = orc.forward(q, k, v, 16, 16, 4, 2, 64, FULL)
+    ref = _sdpa(q, k, v, 16, 16, 4, 2, 64, False)
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def pin_sdpa_cross(orc):
+    q, k, v = _small(seed=0, kv_seq=24)
+    out, _ = orc.forward(q, k, v, 16, 24, 4, 2, 64, CROSS)
+    ref = _sdpa(q, k, v, 16, 24, 4, 2, 64, False)
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def pin_sdpa_gqa_8_to_1(orc):
+    q, k, v = _small(seed=3, q_seq=9, H=8, G=1, D=16)
+    out, _ = orc.forward(q, k, v, 9, 9, 8, 1, 16, CAUSAL)
+    ref = _sdpa(q, k, v, 9, 9, 8, 1, 16, True)
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+# ---------------------------------------------------------------- the pages' recurrence
+def _streaming_row(qv, krows, vrows, scale):
+    """Per-key online softmax exactly as the forward page walks it, in fp64.
+
+    Running state starts at (max -1e30, sum 0, out 0); each key updates
+    new_max, correction = exp(max - new_max), weight = exp(score - new_max).
+    Returns (out / safe_sum, max, log(sum) or -1e30)."""
+    m, l = -1e30, 0.0
+    o = [0.0] * len(qv)
+    for kt, vt in zip(krows, vrows):
+        s = sum(float(a) * float(b) for a, b in zip(qv, kt)) * scale
+        nm = max(m, s)
+        corr = math.exp(m - nm)
+        w = math.exp(s - nm)
+        l = l * corr + w
+        o = [oi * corr + w * float(vi) for oi, vi in zip(o, vt)]
+        m = nm
+    safe = 1.0 if l == 0.0 else l
+    return [oi / safe for oi in o], m, (EMPTY_LSE if l == 0.0 else math.log(l))
+
+
+def _check_streaming(orc, q, k, v, q_seq, kv_seq, H, G, D, mask):
+    out, lse = orc.forward(q, k, v, q_seq, kv_seq, H, G, D, mask)
+    gs = H // G
+    for pos in range(q_seq):
+        n = pos + 1 if mask == CAUSAL else kv_seq
+        for h in range(H):
+            g = h // gs
+            ref, m, logl = _streaming_row(q[pos, h * D:(h + 1) * D],
+                                          k[:n, g * D:(g + 1) * D], v[:n, g * D:(g + 1) * D],
+                                          1.0 / math.sqrt(D))
+            assert np.max(np.abs(out[pos, h * D:(h + 1) * D] - np.array(ref))) < 1e-12
+            assert abs(lse[pos, h, 0] - m) < 1e-12
+            assert abs(lse[pos, h, 1] - logl) < 1e-12
+
+
+def pin_streaming_causal(orc):
+    q, k, v = _small(seed=1, q_seq=7, H=4, G=2, D=8)
+    _check_streaming(orc, q, k, v, 7, 7, 4, 2, 8, CAUSAL)
+
+
+def pin_streaming_cross(orc):
+    q, k, v = _small(seed=2, q_seq=3, kv_seq=11, H=6, G=3, D=4, qk_sigma=3.0)
+    _check_streaming(orc, q, k, v, 3, 11, 6, 3, 4, CROSS)
+
+
+def pin_streaming_full(orc):
+    q, k, v = _small(seed=4, q_seq=5, H=2, G=1, D=12, v_dist="uniform")
+    _check_streaming(orc, q, k, v, 5, 5, 2, 1, 12, FULL)
+
+
+# ---------------------------------------------------------------- closed forms
+def pin_window_one_is_v0(orc):
+    """Causal row 0 sees key 0 only: out = V[0] of its kv head, lse = (s_0, 0)."""
+    q, k, v = _small(seed=5)
+    out, lse = orc.forward(q, k, v, 16, 16, 4, 2, 64, CAUSAL)
+    for h in range(4):
+        g = h // 2
+        assert np.array_equal(out[0, h * 64:(h + 1) * 64], v[0, g * 64:(g + 1) * 64].astype(np.float64))
+        s0 = float(np.dot(q[0, h * 64:(h + 1) * 64].astype(np.float64),
+                          k[0, g * 64:(g + 1) * 64].astype(np.float64))) / 8.0
+        assert abs(lse[0, h, 0] - s0) < 1e-12 and lse[0, h, 1] == 0.0
+
+
+def pin_constant_v(orc):
+    """Every V row equal to c (per kv head): any convex combination is c."""
+    q, k, _ = _small(seed=6, kv_seq=24)
+    c = np.linspace(-2, 3, 2 * 64, dtype=np.float32)
+    v = np.tile(c, (24, 1))
+    for mask, kv in ((CROSS, 24),):
+        out, _ = orc.forward(q, k, v, 16, kv, 4, 2, 64, mask)
+        for h in range(4):
+            g = h // 2
+            assert np.max(np.abs(out[:, h * 64:(h + 1) * 64] - c[g * 64:(g + 1) * 64])) < 1e-12
+
+
+def pin_zero_query(orc):
+    """Q = 0: all scores are 0, so out = mean of V over the window, lse = (0, log n)."""
+    _, k, v = _small(seed=7)
+    q = np.zeros((16, 4 * 64), np.float32)
+    out, lse = orc.forward(q, k, v, 16, 16, 4, 2, 64, CAUSAL)
+    for pos in range(16):
+        for h in range(4):
+            g = h // 2
+            mean = v[:pos + 1, g * 64:(g + 1) * 64].astype(np.float64).mean(axis=0)
+            assert np.max(np.abs(out[pos, h * 64:(h + 1) * 64] - mean)) < 1e-13
+            assert lse[pos, h, 0] == 0.0 and abs(lse[pos, h, 1] - math.log(pos + 1)) < 1e-14
+
+
+def pin_hand_worked(orc):
+    """Three keys, D = 4 (scale 1/2), q = (2,0,0,0): scores are k_t[0] = 0, 1, 2.
+
+    Weights are e^0, e^1, e^2 over 1 + e + e^2; V rows are unit vectors, so
+    out = (1, e, e^2, 0) / (1 + e + e^2); lse = (2, log(1 + e^-1 + e^-2))."""
+    q = np.array([[2, 0, 0, 0]], np.float32)
+    k = np.array([[0, 5, -1, 2], [1, 0, 7, 0], [2, -3, 0, 1]], np.float32)
+    v = np.eye(3, 4, dtype=np.float32)
+    out, lse = orc.forward(q, k, v, 1, 3, 1, 1, 4, CROSS)
+    e = math.e
+    z = 1 + e + e * e
+    assert np.max(np.abs(out[0] - np.array([1 / z, e / z, e * e / z, 0.0]))) < 1e-15
+    assert lse[0, 0, 0] == 2.0 and abs(lse[0, 0, 1] - math.log(1 + 1 / e + 1 / (e * e))) < 1e-15
+
+
+def pin_empty_window(orc):
+    """Cross attention over zero keys writes zeros and lse = (-1e30, -1e30)."""
+    q, _, _ = _small(seed=8)
+    k = np.zeros((0, 128), np.float32)
+    out, lse = orc.forward(q, k, k, 16, 0, 4, 2, 64, CROSS)
+    assert np.all(out == 0.0) and np.all(lse == EMPTY_LSE)
+
+
+# ---------------------------------------------------------------- invariants
+def pin_gqa_equals_replicated_mha(orc):
+    q, k, v = _small(seed=9, q_seq=12, H=8, G=2, D=32)
+    out, lse = orc.forward(q, k, v, 12, 12, 8, 2, 32, CAUSAL)
+    kr = np.repeat(k.reshape(12, 2, 32), 4, axis=1).reshape(12, 8 * 32)
+    vr = np.repeat(v.reshape(12, 2, 32), 4, axis=1).reshape(12, 8 * 32)
+    out2, lse2 = orc.forward(q, kr, vr, 12, 12, 8, 8, 32, CAUSAL)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def pin_softmax_normalisation(orc):
+    """slot0 is the row max, and sum_t exp(s_t - slot0 - slot1) = 1."""
+    q, k, v = _small(seed=10, kv_seq=24, qk_sigma=3.0)
+    _, lse = orc.forward(q, k, v, 16, 24, 4, 2, 64, CROSS)
+    for pos in range(16):
+        for h in range(4):
+            s = _scores(q, k, 4, 2, 64, pos, h, 24)
+            assert abs(lse[pos, h, 0] - s.max()) < 1e-12
+            tot = np.exp(s - lse[pos, h, 0] - lse[pos, h, 1]).sum()
+            assert abs(tot - 1.0) < 1e-12
+
+
+def pin_key_permutation(orc):
+    """Full/cross attention does not depend on the order of the (K, V) pairs."""
+    q, k, v = _small(seed=11, kv_seq=24)
+    perm = np.random.default_rng(11).permutation(24)
+    out, lse = orc.forward(q, k, v, 16, 24, 4, 2, 64, CROSS)
+    out2, lse2 = orc.forward(q, k[perm].copy(), v[perm].copy(), 16, 24, 4, 2, 64, CROSS)
+    assert np.max(np.abs(out - out2)) < 1e-12 and np.max(np.abs(lse - lse2)) < 1e-12
+
+
+def pin_causal_prefix(orc):
+    """Causal row r is unchanged when K/V rows after r are overwritten."""
+    q, k, v = _small(seed=12)
+    out, lse = orc.forward(q, k, v, 16, 16, 4, 2, 64, CAUSAL)
+    for r in (0, 5, 14):
+        k2, v2 = k.copy(), v.copy()
+        k2[r + 1:] = 1e3
+        v2[r + 1:] = -7.0
+        o2, l2 = orc.forward(q, k2, v2, 16, 16, 4, 2, 64, CAUSAL)
+        assert np.array_equal(out[:r + 1], o2[:r + 1]) and np.array_equal(lse[:r + 1], l2[:r + 1])
+        assert not np.array_equal(out[r + 1:], o2[r + 1:])
+
+
+def pin_shift_invariance(orc):
+    """K_t += u shifts every score of a row by scale * q.u: out unchanged,
+    slot0 moves by that amount, slot1 unchanged."""
+    q, k, v = _small(seed=13, kv_seq=24)
+    k = (np.round(k * 1024.0) / 1024.0).astype(np.float32)   # k on a 2^-10 grid ...
+    u = np.zeros(2 * 64, np.float32)
+    u[:64] = 0.5        # ... so k + u is exact in fp32; kv head 0 only
+    k2 = k + u
+    assert np.array_equal(k2.astype(np.float64), k.astype(np.float64) + u.astype(np.float64))
+    out, lse = orc.forward(q, k, v, 16, 24, 4, 2, 64, CROSS)
+    out2, lse2 = orc.forward(q, k2, v, 16, 24, 4, 2, 64, CROSS)
+    assert np.max(np.abs(out - out2)) < 1e-10
+    for pos in range(16):
+        for h in range(4):
+            g = h // 2
+            d = float(np.dot(q[pos, h * 64:(h + 1) * 64].astype(np.float64),
+                             u[g * 64:(g + 1) * 64].astype(np.float64))) / 8.0
+            assert abs(lse2[pos, h, 0] - lse[pos, h, 0] - d) < 1e-10
+            assert abs(lse2[pos, h, 1] - lse[pos, h, 1]) < 1e-10
+
+
+def pin_decode_prefill_forward_agree(orc):
+    """Prefill row i == decode at kv_pos = start_pos + q_base + i, and a
+    prefill from position 0 == causal forward (window rules of the three pages)."""
+    H, G, D, max_seq = 4, 2, 16, 40
+    qb, kc, vc = (_np(x) for x in synthetic.prefill_inputs(10, 80, max_seq, G * D, seed=14))
+    start, qbase = 20, 3
+    scale = np.float32(1.0 / math.sqrt(D))
+    outp = orc.prefill(qb, kc, vc, 10, 7, H, G, D, G * D, max_seq, scale, start, 80, 80, qbase)
+    for i in range(7):
+        qrow = qb[qbase + i, :H * D].reshape(1, H * D)
+        od = orc.decode(qrow, kc, vc, start + qbase + i, H, G, D, max_seq)
+        assert np.max(np.abs(outp[qbase + i, :H * D] - od[0])) < 1e-12
+    qf, kf, vf = _small(seed=15, q_seq=9, H=H, G=G, D=D)
+    of, _ = orc.forward(qf, kf, vf, 9, 9, H, G, D, CAUSAL)
+    op = orc.prefill(qf, kf, vf, 9, 9, H, G, D, G * D, 9, scale, 0, H * D, H * D, 0)
+    assert np.max(np.abs(of - op)) < 1e-12
+
+
+def pin_prefill_strides_and_clamp(orc):
+    """Padding columns and rows before q_base stay untouched; a window that
+    would pass max_seq is cut at max_seq (attention over all max_seq keys)."""
+    H, G, D, max_seq = 2, 1, 16, 12
+    qb, kc, vc = (_np(x) for x in synthetic.prefill_inputs(9, 40, max_seq, 24, seed=16))
+    scale = np.float32(1.0 / math.sqrt(D))
+    out = orc.prefill(qb, kc, vc, 9, 6, H, G, D, 24, max_seq, scale, 8, 40, 36, 2)
+    assert np.all(np.isnan(out[:2])) and np.all(np.isnan(out[:, H * D:]))
+    assert np.all(np.isfinite(out[2:8, :H * D]))
+    # rows with start_pos + q_base + i + 1 >= max_seq see exactly max_seq keys
+    kx = np.ascontiguousarray(kc[:, :D])
+    vx = np.ascontiguousarray(vc[:, :D])
+    qx = np.ascontiguousarray(qb[:, :H * D])
+    ofull, _ = orc.forward(qx, kx, vx, 9, max_seq, H, 1, D, CROSS)
+    for i in (2, 3, 5):        # positions 12, 13, 15 -> clamped to 12 keys
+        assert np.max(np.abs(out[2 + i, :H * D] - ofull[2 + i])) < 1e-12
+
+
+def pin_decode_clamp(orc):
+    """kv_pos past the cache is cut at max_seq; kv_pos = 0 returns V[0]."""
+    H, G, D, max_seq = 4, 2, 16, 10
+    q, kc, vc = (_np(x) for x in synthetic.decode_inputs(max_seq, H, G, D, seed=17))
+    a = orc.decode(q, kc, vc, 9, H, G, D, max_seq)
+    b = orc.decode(q, kc, vc, 1000, H, G, D, max_seq)
+    assert np.array_equal(a, b)
+    z = orc.decode(q, kc, vc, 0, H, G, D, max_seq)
+    for h in range(H):
+        g = h // 2
+        assert np.array_equal(z[0, h * D:(h + 1) * D], vc[0, g * D:(g + 1) * D].astype(np.float64))
+
+
+def pin_prefill_scale_argument(orc):
+    """The prefill scale argument multiplies the scores: scale 2/sqrt(D) on Q
+    equals scale 1/sqrt(D) on 2Q (2Q is exact in fp32)."""
+    H, G, D, max_seq = 2, 1, 16, 8
+    qb, kc, vc = (_np(x) for x in synthetic.prefill_inputs(4, 32, max_seq, 16, seed=18))
+    s1 = np.float32(1.0 / math.sqrt(D))
+    a = orc.prefill(qb, kc, vc, 4, 4, H, G, D, 16, max_seq, np.float32(2.0 * s1), 4, 32, 32, 0)
+    b = orc.prefill((2 * qb).astype(np.float32), kc, vc, 4, 4, H, G, D, 16, max_seq, s1, 4, 32, 32, 0)
+    assert np.max(np.abs(a[:, :H * D] - b[:, :H * D])) < 1e-12
+    c = orc.prefill(qb, kc, vc, 4, 4, H, G, D, 16, max_seq, s1, 4, 32, 32, 0)
+    assert np.max(np.abs(a[:, :H * D] - c[:, :H * D])) > 1e-3
+
+
+ALL_PINS = [obj for name, obj in sorted(globals().items()) if name.startswith("pin_")]

@@ -1,0 +1,98 @@
+"""Mutation check of the oracle's pins (CPU only).
+
+Each case below plants one plausible mistake in a copy of the oracle's C
+source -- a wrong head map, a dropped scale, an off-by-one window, a
+transposed operand, a wrong LSE slot, a missed clamp -- compiles it into a
+temporary directory and runs every pin against it in a child process (a
+mutant may read out of bounds, so it must not share the test's process).
+The real oracle passes every pin; each mutant must fail at least one.
+"""
+import concurrent.futures
+import json
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "attn_oracle.c")
+
+# (name, text to replace, replacement, replace every occurrence?)
+MUTANTS = [
+    ("gqa_modulo", "const int g = h / gs;", "const int g = h % G;", True),
+    ("gqa_wrong_divisor", "const int g = h / gs;", "const int g = (h / G) % G;", True),
+    ("scale_dropped", "s[t] = dot * scale;", "s[t] = dot;", False),
+    ("scale_without_sqrt", "1.0 / sqrt((double)D)", "1.0 / (double)D", True),
+    ("causal_window_short", "(size_t)pos + 1 : (size_t)kv_seq", "(size_t)pos : (size_t)kv_seq", False),
+    ("causal_treated_as_full", "(mask == 0) ?", "(mask == 1) ?", False),
+    ("lse_slot1_is_total", "*logl_out = log(l);", "*logl_out = m + log(l);", False),
+    ("max_not_subtracted", "s[t] = exp(s[t] - m);", "s[t] = exp(s[t]);", False),
+    ("max_sign_flipped", "s[t] = exp(s[t] - m);", "s[t] = exp(s[t] + m);", False),
+    ("k_transposed", "(double)q[d] * (double)kt[d]", "(double)q[d] * (double)k[d * kv_stride + t]", False),
+    ("v_read_from_k", "(double)v[t * kv_stride + d]", "(double)k[t * kv_stride + d]", False),
+    ("not_normalised", "out[d] = acc / l;", "out[d] = acc;", False),
+    ("empty_lse_zero", "#define ORACLE_EMPTY_LSE (-1e30)", "#define ORACLE_EMPTY_LSE (0.0)", False),
+    ("empty_out_ones", "out[d] = 0.0;", "out[d] = 1.0;", False),
+    ("prefill_drops_q_base", "size_t n = (size_t)start_pos + q_global + 1;",
+     "size_t n = (size_t)start_pos + (size_t)i + 1;", False),
+    ("prefill_no_clamp", "if (n > (size_t)max_seq) n = (size_t)max_seq;\n                    const int g",
+     "const int g", False),
+    ("decode_no_clamp", "if (n > (size_t)max_seq) n = (size_t)max_seq;\n    double *s", "double *s", False),
+    ("decode_window_short", "size_t n = (size_t)kv_pos + 1;", "size_t n = (size_t)kv_pos;", False),
+    ("prefill_out_uses_q_stride", "out_batch + q_global * out_stride", "out_batch + q_global * q_stride", False),
+    ("prefill_scale_ignored", "const double sc = (double)scale;", "const double sc = 1.0 / sqrt((double)D);", False),
+    ("forward_kv_head_offset_dropped", "attend_row(q + qo, k + (size_t)g * D, v + (size_t)g * D,",
+     "attend_row(q + qo, k, v,", False),
+    ("query_head_is_kv_head", "(size_t)pos * H * D + (size_t)h * D;", "(size_t)pos * H * D + (size_t)(h / gs) * D;", False),
+    ("first_key_skipped", "for (size_t t = 0; t < n; ++t) {\n        const float *kt",
+     "for (size_t t = 1; t < n; ++t) {\n        const float *kt", False),
+    ("dot_in_fp32", "double dot = 0.0;", "float dot = 0.0f;", False),
+    ("sum_in_fp32", "double l = 0.0;", "float l = 0.0f;", False),
+]
+
+RUNNER = r"""
+import json, sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import oracle, pins
+orc = oracle.Oracle({lib!r})
+failed = []
+for pin in pins.ALL_PINS:
+    try:
+        pin(orc)
+    except Exception as e:
+        failed.append(pin.__name__)
+print(json.dumps(failed))
+"""
+
+
+def _run_mutant(name, old, new, every, tmp):
+    src = open(SRC).read()
+    assert old in src, "mutation site not found: " + name
+    mutated = src.replace(old, new) if every else src.replace(old, new, 1)
+    cfile = os.path.join(tmp, name + ".c")
+    lib = os.path.join(tmp, "lib" + name + ".so")
+    with open(cfile, "w") as f:
+        f.write(mutated)
+    r = subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", cfile, "-o", lib, "-lm"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    code = RUNNER.format(root=ROOT, tests=os.path.join(ROOT, "tests"), lib=lib)
+    p = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    if p.returncode != 0:
+        return ["<crashed: %d>" % p.returncode]
+    return json.loads(p.stdout.strip().splitlines()[-1])
+
+
+@pytest.fixture(scope="module")
+def mutant_results():
+    with tempfile.TemporaryDirectory() as tmp:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+            futs = {m[0]: ex.submit(_run_mutant, *m, tmp) for m in MUTANTS}
+            return {k: f.result() for k, f in futs.items()}
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_mutant_is_caught(mutant_results, name):
+    assert mutant_results[name], "no pin caught the planted mistake " + name
