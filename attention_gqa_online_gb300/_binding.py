@@ -1,0 +1,142 @@
+"""ctypes binding of libattn_gqa.so (declared in include/attn_gqa.h).
+
+Argument marshalling only: each function takes CUDA tensors (or raw device
+addresses as ints) and passes their addresses, sizes and the CUDA stream to
+the C entry point of the same name.  Every step of the computation runs in
+the library's CUDA kernels; there is no fallback.  If the library has not
+been built, loading fails with an error that says so.
+"""
+import ctypes
+import os
+
+ATTN_CAUSAL, ATTN_FULL, ATTN_CROSS = 0, 1, 2
+ATTN_FP32, ATTN_TF32, ATTN_BF16 = 0, 1, 2
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 0, 1, 2, 3, 4
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn_gqa.so")
+
+_lib = None
+_u32 = ctypes.c_uint32
+_vp = ctypes.c_void_p
+
+
+class AttnError(RuntimeError):
+    """A non-zero status returned by the library."""
+
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s: %s (status %d)" % (where, attn_status_string(code), code))
+
+
+def load_library(path=None):
+    """Load libattn_gqa.so (once).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError("libattn_gqa.so is not built (%s): run "
+                           "`python -m attention_gqa_online_gb300.build`" % p)
+    lib = ctypes.CDLL(p)
+    lib.attn_forward.restype = ctypes.c_int
+    lib.attn_forward.argtypes = [_vp, _vp, _vp, _vp, _vp, _u32, _u32, _u32, _u32, _u32,
+                                 ctypes.c_int, ctypes.c_int, _vp]
+    lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_decode_workspace_bytes.argtypes = [_u32, _u32, _u32, _u32]
+    lib.attn_decode_cached.restype = ctypes.c_int
+    lib.attn_decode_cached.argtypes = [_vp, _vp, _vp, _vp, _vp, _u32, _u32, _u32, _u32,
+                                       _vp, ctypes.c_size_t, _vp]
+    lib.attn_prefill.restype = ctypes.c_int
+    lib.attn_prefill.argtypes = [_vp, _vp, _vp, _vp] + [_u32] * 6 + [ctypes.c_float] + \
+        [_u32] * 4 + [ctypes.c_int, _vp]
+    lib.attn_get_status.restype = ctypes.c_int
+    lib.attn_get_status.argtypes = [_vp]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_status_string.argtypes = [ctypes.c_int]
+    _lib = lib
+    return lib
+
+
+def _addr(x, name, dtype=None):
+    """Device address of a tensor (checked to be CUDA and of `dtype`), an int, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    import torch
+    if not isinstance(x, torch.Tensor):
+        raise TypeError("%s must be a CUDA tensor, a device address or None" % name)
+    if not x.is_cuda:
+        raise ValueError("%s must be in device memory" % name)
+    if dtype is not None and x.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, x.dtype))
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code, where):
+    if code != ATTN_OK:
+        raise AttnError(code, where)
+
+
+def _f32():
+    import torch
+    return torch.float32
+
+
+def attn_forward(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask,
+                 prec=ATTN_FP32, stream=None):
+    """Self / cross attention forward with per-row (max, log-sum); see attn_gqa.h."""
+    f = _f32()
+    _check(load_library().attn_forward(
+        _addr(q, "q", f), _addr(k, "k", f), _addr(v, "v", f), _addr(out, "out", f), _addr(lse, "lse", f),
+        q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask, prec, _stream(stream)), "attn_forward")
+
+
+def attn_decode_workspace_bytes(num_heads, num_kv_heads, head_dim, max_seq):
+    return int(load_library().attn_decode_workspace_bytes(num_heads, num_kv_heads, head_dim, max_seq))
+
+
+def attn_decode_cached(q, k_cache, v_cache, kv_pos_dev, out, num_heads, num_kv_heads, head_dim, max_seq,
+                       workspace, workspace_bytes=None, stream=None):
+    """Cached single-token decode over positions 0..*kv_pos_dev; see attn_gqa.h."""
+    f = _f32()
+    if hasattr(kv_pos_dev, "element_size") and kv_pos_dev.element_size() != 4:
+        raise ValueError("kv_pos_dev must hold one 32-bit unsigned position")
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load_library().attn_decode_cached(
+        _addr(q, "q", f), _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f),
+        _addr(kv_pos_dev, "kv_pos_dev"),
+        _addr(out, "out", f), num_heads, num_kv_heads, head_dim, max_seq,
+        _addr(workspace, "workspace"), workspace_bytes, _stream(stream)), "attn_decode_cached")
+
+
+def attn_prefill(q_batch, k_cache, v_cache, out_batch, n_queries, n_heads, n_kv_heads, head_dim, kv_dim,
+                 max_seq, scale, start_pos, q_stride, out_stride, q_base, prec=ATTN_FP32, stream=None):
+    """Batched causal prefill against a KV cache; see attn_gqa.h."""
+    f = _f32()
+    _check(load_library().attn_prefill(
+        _addr(q_batch, "q_batch", f), _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f),
+        _addr(out_batch, "out_batch", f), n_queries, n_heads, n_kv_heads, head_dim, kv_dim, max_seq,
+        float(scale), start_pos, q_stride, out_stride, q_base, prec, _stream(stream)), "attn_prefill")
+
+
+def attn_get_status(stream=None):
+    """Synchronise `stream`, return and clear the device status word."""
+    return int(load_library().attn_get_status(_stream(stream)))
+
+
+def attn_status_string(code):
+    try:
+        return load_library().attn_status_string(code).decode()
+    except RuntimeError:
+        return "status %d" % code

@@ -1,0 +1,230 @@
+// api.cu -- the C ABI of libattn_gqa.so (declared in include/attn_gqa.h):
+// argument validation, kernel selection, and the device status word.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/attn_gqa.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+
+__device__ unsigned int g_status_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+std::mutex g_mu;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+// Device address of this device's status word (looked up once per device).
+unsigned* status_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+bool heads_ok(uint32_t H, uint32_t G, uint32_t D) {
+  return H >= 1 && G >= 1 && H % G == 0 && D >= 1 && D <= 128 && H <= (1u << 20);
+}
+
+bool valid_prec(int prec) { return prec == ATTN_FP32 || prec == ATTN_TF32 || prec == ATTN_BF16; }
+
+int run_flash(const FlashArgs& a, int prec, cudaStream_t s) {
+  if (prec == ATTN_FP32) return launch_flash_simt(a, s);
+  if (!flash_tc_supported(a, prec)) return ATTN_ERR_UNSUPPORTED;
+  return launch_flash_tc(a, prec, s);
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_forward(const float* q, const float* k, const float* v, float* out, float* lse,
+                            uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
+                            uint32_t head_dim, int mask, int prec, attn_stream_t stream) {
+  if (!heads_ok(num_heads, num_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
+  if (mask != ATTN_CAUSAL && mask != ATTN_FULL && mask != ATTN_CROSS) return ATTN_ERR_INVALID_ARG;
+  if (mask != ATTN_CROSS && kv_seq != q_seq) return ATTN_ERR_INVALID_ARG;
+  if (q_seq > 0x7fffffffu || kv_seq > 0x7fffffffu) return ATTN_ERR_INVALID_ARG;
+  if (q_seq == 0) return ATTN_OK;
+  if (q == nullptr || out == nullptr || (kv_seq > 0 && (k == nullptr || v == nullptr))) return ATTN_ERR_INVALID_ARG;
+  FlashArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.q_row_stride = (long long)num_heads * head_dim;
+  a.out_row_stride = a.q_row_stride;
+  a.kv_row_stride = (long long)num_kv_heads * head_dim;
+  a.n_q = (int)q_seq;
+  a.H = (int)num_heads;
+  a.G = (int)num_kv_heads;
+  a.D = (int)head_dim;
+  a.causal = (mask == ATTN_CAUSAL);
+  a.base_pos = 0;
+  a.cap = (int)kv_seq;
+  a.n_all = (int)kv_seq;
+  a.scale = 1.0f / sqrtf((float)head_dim);
+  a.kv_pos_dev = nullptr;
+  a.status = status_ptr();
+  if (a.status == nullptr) return ATTN_ERR_CUDA;
+  // An empty key set is handled by the same kernels (no tiles, zero rows).
+  return run_flash(a, prec, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t attn_decode_workspace_bytes(uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim,
+                                              uint32_t max_seq) {
+  if (!heads_ok(num_heads, num_kv_heads, head_dim) || max_seq == 0 || max_seq > 0x7fffffffu) return 0;
+  const int sms = sm_count();
+  if (sms <= 0) return 0;
+  const size_t b = decode_workspace_bytes((int)num_heads, (int)num_kv_heads, (int)head_dim, (int)max_seq, sms);
+  return b > 0 ? b : 256;  // the generic path needs none; report a token size
+}
+
+extern "C" int attn_decode_cached(const float* q, const float* k_cache, const float* v_cache,
+                                  const uint32_t* kv_pos_dev, float* out, uint32_t num_heads,
+                                  uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq, void* workspace,
+                                  size_t workspace_bytes, attn_stream_t stream) {
+  if (!heads_ok(num_heads, num_kv_heads, head_dim) || max_seq == 0 || max_seq > 0x7fffffffu)
+    return ATTN_ERR_INVALID_ARG;
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || kv_pos_dev == nullptr || out == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  const int H = (int)num_heads, G = (int)num_kv_heads, D = (int)head_dim, ms = (int)max_seq;
+  unsigned* st = status_ptr();
+  if (st == nullptr) return ATTN_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+                         reinterpret_cast<uintptr_t>(v_cache)) % 16) == 0;
+  if (decode_split_supported(H, G, D) && aligned) {
+    const int sms = sm_count();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    const size_t need = decode_workspace_bytes(H, G, D, ms, sms);
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % 16) != 0)
+      return ATTN_ERR_INVALID_ARG;
+    DecodeArgs d{};
+    d.q = q;
+    d.k_cache = k_cache;
+    d.v_cache = v_cache;
+    d.kv_pos_dev = kv_pos_dev;
+    d.out = out;
+    d.H = H;
+    d.G = G;
+    d.D = D;
+    d.max_seq = ms;
+    d.workspace = workspace;
+    d.status = st;
+    return launch_decode_split(d, decode_splits(G, ms, sms), s);
+  }
+  // Other shapes: the generic flash kernel with one query row whose causal
+  // position is read from kv_pos_dev.
+  FlashArgs a{};
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.out = out;
+  a.lse = nullptr;
+  a.q_row_stride = (long long)H * D;
+  a.out_row_stride = a.q_row_stride;
+  a.kv_row_stride = (long long)G * D;
+  a.n_q = 1;
+  a.H = H;
+  a.G = G;
+  a.D = D;
+  a.causal = 1;
+  a.base_pos = 0;
+  a.cap = ms;
+  a.n_all = ms;
+  a.scale = 1.0f / sqrtf((float)D);
+  a.kv_pos_dev = kv_pos_dev;
+  a.status = st;
+  return launch_flash_simt(a, s);
+}
+
+extern "C" int attn_prefill(const float* q_batch, const float* k_cache, const float* v_cache, float* out_batch,
+                            uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads, uint32_t head_dim,
+                            uint32_t kv_dim, uint32_t max_seq, float scale, uint32_t start_pos, uint32_t q_stride,
+                            uint32_t out_stride, uint32_t q_base, int prec, attn_stream_t stream) {
+  if (!heads_ok(n_heads, n_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
+  if ((uint64_t)kv_dim < (uint64_t)n_kv_heads * head_dim) return ATTN_ERR_INVALID_ARG;
+  if ((uint64_t)q_stride < (uint64_t)n_heads * head_dim || (uint64_t)out_stride < (uint64_t)n_heads * head_dim)
+    return ATTN_ERR_INVALID_ARG;
+  if ((uint64_t)start_pos + q_base + n_queries > max_seq || max_seq > 0x7fffffffu) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (n_queries == 0) return ATTN_OK;
+  if (q_batch == nullptr || k_cache == nullptr || v_cache == nullptr || out_batch == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  FlashArgs a{};
+  a.q = q_batch + (size_t)q_base * q_stride;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.out = out_batch + (size_t)q_base * out_stride;
+  a.lse = nullptr;
+  a.q_row_stride = q_stride;
+  a.out_row_stride = out_stride;
+  a.kv_row_stride = kv_dim;
+  a.n_q = (int)n_queries;
+  a.H = (int)n_heads;
+  a.G = (int)n_kv_heads;
+  a.D = (int)head_dim;
+  a.causal = 1;
+  a.base_pos = (long long)start_pos + q_base;
+  a.cap = (int)max_seq;
+  a.n_all = (int)max_seq;
+  a.scale = scale;
+  a.kv_pos_dev = nullptr;
+  a.status = status_ptr();
+  if (a.status == nullptr) return ATTN_ERR_CUDA;
+  return run_flash(a, prec, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_get_status(attn_stream_t stream) {
+  unsigned* st = status_ptr();
+  if (st == nullptr) return ATTN_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, st, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpy(st, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  return (int)v;
+}
+
+extern "C" const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape, precision or alignment";
+    case ATTN_ERR_CUDA: return "CUDA launch or runtime error";
+    case ATTN_ERR_TIMEOUT: return "a bounded device wait ran out";
+    default: return "unknown status";
+  }
+}

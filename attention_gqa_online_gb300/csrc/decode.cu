@@ -1,0 +1,344 @@
+// decode.cu -- split-KV single-token decode over a KV cache.
+//
+// Operation: meganeura cached_attention.wgsl, fn main -- one query token,
+// H heads, attends to cache positions 0..kv_pos (kv_pos read from device
+// memory).  Decode is bound by streaming the K/V cache from HBM, so the
+// design is about bytes, not flops:
+//
+//   * Grid (S, G): CTA (j, g) takes one contiguous range of cache positions
+//     of kv head g and serves all gs = H/G query heads that read it, so every
+//     K/V byte leaves HBM once per call (the shader reads each row once per
+//     query head).  S * G is about two CTAs per SM; the range length comes
+//     from kv_pos on the device, so the launch does not depend on it.
+//   * K and V rows of a stage (32 positions) are staged in shared memory with
+//     bulk asynchronous copies (TMA, one 256/512-byte row per copy) that
+//     complete on an mbarrier; three stages are in flight per CTA.
+//   * Each warp runs its own online softmax (tile max, one correction per
+//     stage, running sum and accumulator; the same recurrence as the pages)
+//     over its 8 positions of every stage; the 4 warps merge at the end.
+//   * Each CTA writes its partial (m, l, unnormalised o) to the workspace; the
+//     last CTA of kv head g to finish (atomic ticket) merges the S partials
+//     with the log-sum-exp rule: M = max m_j, L = sum l_j 2^(m_j - M),
+//     out = sum o_j 2^(m_j - M) / L, and resets the ticket for the next call.
+//
+// Scores are kept in the base-2 domain (scale * log2(e) folded into q).
+#include <cfloat>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kT = 32;         // positions per stage
+constexpr int kStages = 3;     // stages in flight
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kPpw = kT / kWarps;  // positions per warp per stage (8)
+constexpr int kMinChunk = 64;      // fewest positions a split is given
+
+template <int D, int GS>
+struct DecodeSmem {
+  float k[kStages][kT * D];
+  float v[kStages][kT * D];
+  float red_m[kWarps][GS];
+  float red_l[kWarps][GS];
+  float red_o[kWarps][GS][D];
+  uint64_t full[kStages];
+  int is_last;
+};
+
+struct WsLayout {
+  unsigned* tickets;  // [G]
+  float* ml;          // [H][S][2]
+  float* o;           // [H][S][D]
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline WsLayout ws_layout(void* ws, int H, int G, int D, int S) {
+  char* p = static_cast<char*>(ws);
+  WsLayout l;
+  l.tickets = reinterpret_cast<unsigned*>(p);
+  p += align256(sizeof(unsigned) * G);
+  l.ml = reinterpret_cast<float*>(p);
+  p += align256(sizeof(float) * 2 * (size_t)H * S);
+  l.o = reinterpret_cast<float*>(p);
+  return l;
+}
+
+// Lane layout for the scores: lane = 8 * p + c handles position p (0..3) of
+// the current group of four and the dims {4c + 32u : u < D/32} (float4 each),
+// so each 8-lane phase of a 16-byte shared load reads one contiguous row.
+template <int D, int GS>
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeArgs a, const int S, const float sl2) {
+  using Smem = DecodeSmem<D, GS>;
+  constexpr int U = D / 32;   // float4 groups per lane in the score phase
+  constexpr int VP = D / 32;  // output dims per lane in the PV phase
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j = blockIdx.x, g = blockIdx.y;
+
+  const unsigned kp = *a.kv_pos_dev;
+  if (j == 0 && g == 0 && tid == 0 && (long long)kp >= (long long)a.max_seq)
+    record_status(a.status, ATTN_ERR_INVALID_ARG);
+  const long long n_ll = (long long)kp + 1 < (long long)a.max_seq ? (long long)kp + 1 : (long long)a.max_seq;
+  const int n = (int)n_ll;
+  const int s_eff = min(S, (n + kMinChunk - 1) / kMinChunk);
+  if (j >= s_eff) return;
+  const int chunk = (n + s_eff - 1) / s_eff;
+  const int p_begin = min(n, j * chunk);
+  const int p_end = min(n, p_begin + chunk);
+  const int len = p_end - p_begin;
+  const int n_st = (len + kT - 1) / kT;
+
+  // Query registers: q[h][u] holds dims 4c + 32u .. +3 of head g*GS + h, pre-scaled.
+  const int qp = lane >> 3, qc = lane & 7;
+  float4 qr[GS][U];
+#pragma unroll
+  for (int h = 0; h < GS; ++h)
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float4 x = *reinterpret_cast<const float4*>(a.q + (size_t)(g * GS + h) * D + 4 * qc + 32 * u);
+      qr[h][u] = make_float4(x.x * sl2, x.y * sl2, x.z * sl2, x.w * sl2);
+    }
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const size_t row_stride = (size_t)a.G * D;
+  const float* kbase = a.k_cache + (size_t)g * D;
+  const float* vbase = a.v_cache + (size_t)g * D;
+  auto issue = [&](int st) {  // warp 0 only
+    const int slot = st % kStages;
+    const int t0 = p_begin + st * kT;
+    const int valid = min(kT, p_end - t0);
+    if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], (unsigned)(valid * D * 4 * 2));
+    __syncwarp();
+    if (lane < valid) {
+      const size_t off = (size_t)(t0 + lane) * row_stride;
+      bulk_g2s(&sm.k[slot][lane * D], kbase + off, D * 4, &sm.full[slot]);
+      bulk_g2s(&sm.v[slot][lane * D], vbase + off, D * 4, &sm.full[slot]);
+    }
+  };
+  if (warp == 0)
+    for (int st = 0; st < kStages && st < n_st; ++st) issue(st);
+
+  float m_run[GS], l_run[GS];
+  float acc[GS][VP];
+#pragma unroll
+  for (int h = 0; h < GS; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < VP; ++e) acc[h][e] = 0.f;
+  }
+
+  for (int st = 0; st < n_st; ++st) {
+    const int slot = st % kStages;
+    mbar_wait_bounded(&sm.full[slot], (st / kStages) & 1, a.status);
+    const int t0 = p_begin + st * kT;
+    const int valid = min(kT, p_end - t0);
+    const float* ks = sm.k[slot];
+    const float* vs = sm.v[slot];
+    const int wp0 = warp * kPpw;  // this warp's first position in the stage
+
+    // Scores of the warp's 8 positions, two groups of four.
+    float sc[2][GS];
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+      const int pos = wp0 + 4 * grp + qp;
+      float part[GS];
+#pragma unroll
+      for (int h = 0; h < GS; ++h) part[h] = 0.f;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float4 kv = *reinterpret_cast<const float4*>(&ks[pos * D + 4 * qc + 32 * u]);
+#pragma unroll
+        for (int h = 0; h < GS; ++h) {
+          part[h] = fmaf(qr[h][u].x, kv.x, part[h]);
+          part[h] = fmaf(qr[h][u].y, kv.y, part[h]);
+          part[h] = fmaf(qr[h][u].z, kv.z, part[h]);
+          part[h] = fmaf(qr[h][u].w, kv.w, part[h]);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < GS; ++h) {
+        float x = part[h];
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        sc[grp][h] = (pos < valid) ? x : -INFINITY;
+      }
+    }
+
+    // Online softmax over the 8 positions (per head).
+    float w[2][GS];
+#pragma unroll
+    for (int h = 0; h < GS; ++h) {
+      float mx = fmaxf(sc[0][h], sc[1][h]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_run[h], mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float corr = ex2(m_run[h] - m_use);
+      w[0][h] = ex2(sc[0][h] - m_use);
+      w[1][h] = ex2(sc[1][h] - m_use);
+      float sum = w[0][h] + w[1][h];
+      sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+      l_run[h] = l_run[h] * corr + sum;
+      m_run[h] = m_new;
+#pragma unroll
+      for (int e = 0; e < VP; ++e) acc[h][e] *= corr;
+    }
+
+    // acc += w * V for the warp's 8 positions; lane owns dims VP*lane ..
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const int pos = wp0 + 4 * grp + pp;
+        float wb[GS];
+#pragma unroll
+        for (int h = 0; h < GS; ++h) wb[h] = __shfl_sync(0xffffffffu, w[grp][h], 8 * pp);
+        if (pos < valid) {
+          if constexpr (VP == 4) {
+            const float4 vv = *reinterpret_cast<const float4*>(&vs[pos * D + 4 * lane]);
+#pragma unroll
+            for (int h = 0; h < GS; ++h) {
+              acc[h][0] = fmaf(wb[h], vv.x, acc[h][0]);
+              acc[h][1] = fmaf(wb[h], vv.y, acc[h][1]);
+              acc[h][2] = fmaf(wb[h], vv.z, acc[h][2]);
+              acc[h][3] = fmaf(wb[h], vv.w, acc[h][3]);
+            }
+          } else {
+            const float2 vv = *reinterpret_cast<const float2*>(&vs[pos * D + 2 * lane]);
+#pragma unroll
+            for (int h = 0; h < GS; ++h) {
+              acc[h][0] = fmaf(wb[h], vv.x, acc[h][0]);
+              acc[h][1] = fmaf(wb[h], vv.y, acc[h][1]);
+            }
+          }
+        }
+      }
+
+    __syncthreads();  // every warp is done with this slot
+    if (warp == 0 && st + kStages < n_st) issue(st + kStages);
+  }
+
+  // Merge the 4 warps' states, write this split's partial.
+#pragma unroll
+  for (int h = 0; h < GS; ++h) {
+    if (lane == 0) {
+      sm.red_m[warp][h] = m_run[h];
+      sm.red_l[warp][h] = l_run[h];
+    }
+#pragma unroll
+    for (int e = 0; e < VP; ++e) sm.red_o[warp][h][VP * lane + e] = acc[h][e];
+  }
+  __syncthreads();
+  const WsLayout ws = ws_layout(a.workspace, a.H, a.G, D, S);
+  for (int idx = tid; idx < GS * D; idx += kThreads) {
+    const int h = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) M = fmaxf(M, sm.red_m[w2][h]);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) {
+      const float f = ex2(sm.red_m[w2][h] - Mu);
+      L += sm.red_l[w2][h] * f;
+      O += sm.red_o[w2][h][d] * f;
+    }
+    const size_t hs = (size_t)(g * GS + h) * S + j;
+    ws.o[hs * D + d] = O;
+    if (d == 0) {
+      ws.ml[hs * 2] = M;
+      ws.ml[hs * 2 + 1] = L;
+    }
+  }
+
+  // Last split of this kv head merges every split.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(&ws.tickets[g], 1u);
+    sm.is_last = (prev == (unsigned)(s_eff - 1));
+  }
+  __syncthreads();
+  if (!sm.is_last) return;
+  __threadfence();
+  for (int idx = tid; idx < GS * D; idx += kThreads) {
+    const int h = idx / D, d = idx % D;
+    const size_t hb = (size_t)(g * GS + h) * S;
+    float M = -INFINITY;
+    for (int s = 0; s < s_eff; ++s) M = fmaxf(M, __ldcg(&ws.ml[(hb + s) * 2]));
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f, O = 0.f;
+    for (int s = 0; s < s_eff; ++s) {
+      const float f = ex2(__ldcg(&ws.ml[(hb + s) * 2]) - Mu);
+      L += __ldcg(&ws.ml[(hb + s) * 2 + 1]) * f;
+      O += __ldcg(&ws.o[(hb + s) * D + d]) * f;
+    }
+    a.out[(size_t)(g * GS + h) * D + d] = (L == 0.f) ? 0.f : O / L;
+  }
+  if (tid == 0) ws.tickets[g] = 0u;
+}
+
+template <int D, int GS>
+int launch_t(const DecodeArgs& a, int S, cudaStream_t s) {
+  const size_t smem = sizeof(DecodeSmem<D, GS>);
+  auto kern = decode_split_kernel<D, GS>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const float sl2 = (1.0f / sqrtf((float)D)) * kLog2e;
+  kern<<<dim3(S, a.G), kThreads, smem, s>>>(a, S, sl2);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+bool decode_split_supported(int H, int G, int D) {
+  if (G <= 0 || H % G != 0) return false;
+  const int gs = H / G;
+  if (D == 128) return gs == 1 || gs == 2 || gs == 4;
+  if (D == 64) return gs == 1 || gs == 2 || gs == 4 || gs == 8;
+  return false;
+}
+
+int decode_splits(int G, int max_seq, int sm_count) {
+  const int target = (2 * sm_count + G - 1) / G;
+  const int by_len = (max_seq + kMinChunk - 1) / kMinChunk;
+  return max(1, min(target, by_len));
+}
+
+size_t decode_workspace_bytes(int H, int G, int D, int max_seq, int sm_count) {
+  if (!decode_split_supported(H, G, D) || max_seq <= 0) return 0;
+  const int S = decode_splits(G, max_seq, sm_count);
+  return align256(sizeof(unsigned) * G) + align256(sizeof(float) * 2 * (size_t)H * S) +
+         sizeof(float) * (size_t)H * S * D;
+}
+
+int launch_decode_split(const DecodeArgs& a, int S, cudaStream_t s) {
+  const int gs = a.H / a.G;
+  if (a.D == 128) {
+    if (gs == 1) return launch_t<128, 1>(a, S, s);
+    if (gs == 2) return launch_t<128, 2>(a, S, s);
+    if (gs == 4) return launch_t<128, 4>(a, S, s);
+  } else if (a.D == 64) {
+    if (gs == 1) return launch_t<64, 1>(a, S, s);
+    if (gs == 2) return launch_t<64, 2>(a, S, s);
+    if (gs == 4) return launch_t<64, 4>(a, S, s);
+    if (gs == 8) return launch_t<64, 8>(a, S, s);
+  }
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace attn

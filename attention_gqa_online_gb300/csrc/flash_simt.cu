@@ -1,0 +1,294 @@
+// flash_simt.cu -- fp32 CUDA-core flash attention (forward, prefill, and the
+// generic decode path).
+//
+// One CTA owns 64 packed rows of one kv head g: row r of the block is the
+// pair (query i, head g*gs + j) with i*gs + j = 64*block + r, so every K/V
+// tile loaded into shared memory serves all gs query heads that read kv head
+// g (the GQA map kv_head = head / (n_heads / n_kv_heads) of all three shader
+// pages).  Keys are walked in tiles of 64 with a per-tile online softmax: the
+// tile max is taken first, then one correction factor per row per tile
+// (cera attention_prefill.wgsl, fn attention_prefill: tile max, correction
+// exp(m - m'), p = exp(s - m'), running sum and accumulator rescale).  The
+// exponentials are base 2 with scale*log2(e) folded into the scores, which is
+// the same function.  Per-row windows implement causal / full / cross /
+// prefill / decode masking; key tiles past the last row's window are never
+// loaded.
+//
+// Thread layout (256 threads): rg = tid / 16 owns rows 4rg..4rg+3; cl = tid %
+// 16 owns score columns cl + 16j (j < 4) and output columns 4cl + 64j.  Row
+// reductions stay inside a half-warp (xor shuffles 8, 4, 2, 1).
+#include <cfloat>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int BM = 64;   // packed rows per CTA
+constexpr int BN = 64;   // keys per tile
+constexpr int NT = 256;  // threads per CTA
+
+template <int DMAX>
+struct SimtSmem {
+  static constexpr int QS = DMAX + 4;  // padded row stride of the Q and K tiles (floats)
+  static constexpr int PS = BM + 4;    // padded row stride of the transposed P tile
+  float q[BM * QS];
+  float k[2][BN * QS];
+  float v[2][BN * DMAX];
+  float p[BN * PS];
+  int row_n[BM];
+};
+
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+  acc = fmaf(a.x, b.x, acc);
+  acc = fmaf(a.y, b.y, acc);
+  acc = fmaf(a.z, b.z, acc);
+  return fmaf(a.w, b.w, acc);
+}
+
+// Issues the async copies of one (rows x DMAX) tile into shared memory, with
+// zero fill for rows >= valid_rows and columns >= D.  src(r) is the global
+// address of row r's first element.
+template <int DMAX, int STRIDE, bool VEC, typename SrcFn>
+__device__ __forceinline__ void load_tile(float* dst, int rows, int valid_rows, int D, SrcFn src) {
+  if constexpr (VEC) {
+    constexpr int F = DMAX / 4;
+    for (int idx = threadIdx.x; idx < rows * F; idx += NT) {
+      const int r = idx / F, f = idx % F;
+      const bool ok = r < valid_rows && 4 * f < D;
+      const float* g = ok ? src(r) + 4 * f : src(0);
+      cp_async16(dst + r * STRIDE + 4 * f, g, ok ? 16u : 0u);
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < rows * DMAX; idx += NT) {
+      const int r = idx / DMAX, c = idx % DMAX;
+      const bool ok = r < valid_rows && c < D;
+      const float* g = ok ? src(r) + c : src(0);
+      cp_async4(dst + r * STRIDE + c, g, ok ? 4u : 0u);
+    }
+  }
+}
+
+template <int DMAX, bool VEC>
+__global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
+  using Smem = SimtSmem<DMAX>;
+  constexpr int QS = Smem::QS, PS = Smem::PS;
+  constexpr int OC = DMAX / 64 > 0 ? DMAX / 64 : 1;  // float4 output groups per thread
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+
+  const int tid = threadIdx.x;
+  const int rg = tid >> 4, cl = tid & 15;
+  const int r0 = 4 * rg;
+  const int g = blockIdx.y;
+  const int blk = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) causal rows first
+  const int gs = a.H / a.G;
+  const int D = a.D;
+
+  long long base_pos = a.base_pos;
+  if (a.kv_pos_dev != nullptr) {
+    const unsigned kp = *a.kv_pos_dev;
+    if (tid == 0 && blk == 0 && (long long)kp >= (long long)a.cap) record_status(a.status, ATTN_ERR_INVALID_ARG);
+    base_pos = kp;
+  }
+
+  // Window of every packed row of this block.
+  if (tid < BM) {
+    const long long packed = (long long)blk * BM + tid;
+    const long long i = packed / gs;
+    int n = 0;
+    if (i < a.n_q) {
+      if (a.causal) {
+        long long w = base_pos + i + 1;
+        n = (int)(w < a.cap ? w : a.cap);
+      } else {
+        n = a.n_all;
+      }
+    }
+    sm.row_n[tid] = n;
+  }
+  __syncthreads();
+  int n_max = 0;
+  for (int r = 0; r < BM; ++r) n_max = max(n_max, sm.row_n[r]);
+  int my_n[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) my_n[i] = sm.row_n[r0 + i];
+
+  // Q tile (rows past n_q are zero-filled and never stored).
+  const long long row_base = (long long)blk * BM;
+  const long long rows_left = (long long)a.n_q * gs - row_base;
+  const int q_valid = (int)(rows_left < BM ? rows_left : BM);
+  auto q_src = [&](int r) {
+    const long long packed = row_base + r;
+    const long long i = packed / gs;
+    const int h = g * gs + (int)(packed % gs);
+    return a.q + i * a.q_row_stride + (long long)h * D;
+  };
+  load_tile<DMAX, QS, VEC>(sm.q, BM, q_valid, D, q_src);
+
+  const int n_tiles = (n_max + BN - 1) / BN;
+  auto kv_src = [&](const float* base, int t0) {
+    return [=](int r) { return base + (long long)(t0 + r) * a.kv_row_stride + (long long)g * D; };
+  };
+  if (n_tiles > 0) {
+    load_tile<DMAX, QS, VEC>(sm.k[0], BN, min(BN, n_max), D, kv_src(a.k, 0));
+    load_tile<DMAX, DMAX, VEC>(sm.v[0], BN, min(BN, n_max), D, kv_src(a.v, 0));
+  }
+  cp_async_commit();
+
+  const float sl2 = a.scale * kLog2e;
+  float m_run[4], l_run[4];
+  float o[4][OC * 4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m_run[i] = -INFINITY;
+    l_run[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < OC * 4; ++c) o[i][c] = 0.f;
+  }
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const int buf = it & 1;
+    const int t0 = it * BN;
+    if (it + 1 < n_tiles) {
+      const int t1 = t0 + BN;
+      const int valid = min(BN, n_max - t1);
+      load_tile<DMAX, QS, VEC>(sm.k[buf ^ 1], BN, valid, D, kv_src(a.k, t1));
+      load_tile<DMAX, DMAX, VEC>(sm.v[buf ^ 1], BN, valid, D, kv_src(a.v, t1));
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+
+    // S = Q K^T for rows r0..r0+3, keys cl + 16j.
+    float s[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+    const float* kt = sm.k[buf];
+#pragma unroll 4
+    for (int d = 0; d < DMAX; d += 4) {
+      float4 qa[4], kb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qa[i] = *reinterpret_cast<const float4*>(&sm.q[(r0 + i) * QS + d]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) kb[j] = *reinterpret_cast<const float4*>(&kt[(cl + 16 * j) * QS + d]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[i][j] = dot4(qa[i], kb[j], s[i][j]);
+    }
+
+    // Mask, tile max, correction, exponentials, running sum.
+    float p[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int t = t0 + cl + 16 * j;
+        s[i][j] = (t < my_n[i]) ? s[i][j] * sl2 : -INFINITY;
+        mx = fmaxf(mx, s[i][j]);
+      }
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float m_new = fmaxf(m_run[i], mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float corr = ex2(m_run[i] - m_use);
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        p[i][j] = ex2(s[i][j] - m_use);
+        sum += p[i][j];
+      }
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      l_run[i] = l_run[i] * corr + sum;
+      m_run[i] = m_new;
+#pragma unroll
+      for (int c = 0; c < OC * 4; ++c) o[i][c] *= corr;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<float4*>(&sm.p[(cl + 16 * j) * PS + r0]) = make_float4(p[0][j], p[1][j], p[2][j], p[3][j]);
+    __syncthreads();
+
+    // O += P V.
+    const float* vt = sm.v[buf];
+#pragma unroll 4
+    for (int kk = 0; kk < BN; ++kk) {
+      const float4 pv = *reinterpret_cast<const float4*>(&sm.p[kk * PS + r0]);
+      const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+      for (int jj = 0; jj < OC; ++jj) {
+        const int col = (DMAX >= 64) ? (4 * cl + 64 * jj) : (4 * cl);
+        float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (DMAX >= 64 || col < DMAX) vv = *reinterpret_cast<const float4*>(&vt[kk * DMAX + col]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          o[i][4 * jj + 0] = fmaf(pr[i], vv.x, o[i][4 * jj + 0]);
+          o[i][4 * jj + 1] = fmaf(pr[i], vv.y, o[i][4 * jj + 1]);
+          o[i][4 * jj + 2] = fmaf(pr[i], vv.z, o[i][4 * jj + 2]);
+          o[i][4 * jj + 3] = fmaf(pr[i], vv.w, o[i][4 * jj + 3]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // Epilogue: normalise, store rows, store (max, log sum).
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = r0 + i;
+    if (r >= q_valid) continue;
+    const long long packed = row_base + r;
+    const long long qi = packed / gs;
+    const int h = g * gs + (int)(packed % gs);
+    const float inv = (l_run[i] == 0.f) ? 0.f : 1.f / l_run[i];
+    float* dst = a.out + qi * a.out_row_stride + (long long)h * D;
+#pragma unroll
+    for (int jj = 0; jj < OC; ++jj) {
+      const int col = (DMAX >= 64) ? (4 * cl + 64 * jj) : (4 * cl);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (col + c < D) dst[col + c] = o[i][4 * jj + c] * inv;
+    }
+    if (a.lse != nullptr && cl == 0) {
+      float* l2 = a.lse + (qi * a.H + h) * 2;
+      const bool empty = (l_run[i] == 0.f);
+      l2[0] = empty ? kEmptyLse : m_run[i] * kLn2;
+      l2[1] = empty ? kEmptyLse : logf(l_run[i]);
+    }
+  }
+}
+
+template <int DMAX, bool VEC>
+int launch_one(const FlashArgs& a, cudaStream_t s) {
+  const int gs = a.H / a.G;
+  const long long rows = (long long)a.n_q * gs;
+  const long long nb = (rows + BM - 1) / BM;
+  if (nb == 0) return 0;
+  if (nb > 0x7fffffffLL || a.G > 65535) return ATTN_ERR_UNSUPPORTED;
+  const size_t smem = sizeof(SimtSmem<DMAX>);
+  auto kern = flash_simt_kernel<DMAX, VEC>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  kern<<<dim3((unsigned)nb, (unsigned)a.G), NT, smem, s>>>(a);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_flash_simt(const FlashArgs& a, cudaStream_t s) {
+  const bool vec = (a.D % 4 == 0) && (a.q_row_stride % 4 == 0) && (a.kv_row_stride % 4 == 0) &&
+                   ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
+                     reinterpret_cast<uintptr_t>(a.v)) % 16 == 0);
+  if (a.D <= 64) return vec ? launch_one<64, true>(a, s) : launch_one<64, false>(a, s);
+  return vec ? launch_one<128, true>(a, s) : launch_one<128, false>(a, s);
+}
+
+}  // namespace attn

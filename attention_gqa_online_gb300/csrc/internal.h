@@ -1,0 +1,65 @@
+// internal.h -- launchers shared between the C-ABI layer (api.cu) and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// One flash-style attention launch.  Rows are (query i, head h) pairs; the
+// query, key and value pointers already include every batch offset (q_base),
+// so query 0 of the call is at q[0].
+struct FlashArgs {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* out;
+  float* lse;                 // [n_q, H, 2] or nullptr
+  long long q_row_stride;     // floats between consecutive query rows
+  long long out_row_stride;   // floats between consecutive output rows
+  long long kv_row_stride;    // floats between consecutive key/value rows
+  int n_q, H, G, D;
+  // Window of query i: keys [0, n_i) with
+  //   n_i = min(base_pos + i + 1, cap)  if causal
+  //   n_i = n_all                       otherwise
+  int causal;
+  long long base_pos;
+  int cap;
+  int n_all;
+  float scale;                // multiplies q . k
+  // Decode through the generic kernel: when set, base_pos is read from
+  // *kv_pos_dev on the device (n_q == 1, causal, cap = max_seq).
+  const uint32_t* kv_pos_dev;
+  unsigned* status;           // device status word
+};
+
+// fp32 CUDA-core flash kernel; any 1 <= D <= 128.
+int launch_flash_simt(const FlashArgs& a, cudaStream_t s);
+
+// tcgen05 tensor-core flash kernel (prec = ATTN_TF32 or ATTN_BF16).
+bool flash_tc_supported(const FlashArgs& a, int prec);
+int launch_flash_tc(const FlashArgs& a, int prec, cudaStream_t s);
+
+// Split-KV decode.
+struct DecodeArgs {
+  const float* q;
+  const float* k_cache;
+  const float* v_cache;
+  const uint32_t* kv_pos_dev;
+  float* out;
+  int H, G, D, max_seq;
+  void* workspace;
+  unsigned* status;
+};
+
+// Number of KV splits per kv head for these sizes on a device with sm_count SMs.
+int decode_splits(int G, int max_seq, int sm_count);
+// Workspace bytes the split decode needs (0 if the fast path does not apply).
+size_t decode_workspace_bytes(int H, int G, int D, int max_seq, int sm_count);
+// True if the split-KV kernels handle these sizes (else the generic kernel runs).
+bool decode_split_supported(int H, int G, int D);
+int launch_decode_split(const DecodeArgs& a, int splits, cudaStream_t s);
+
+}  // namespace attn

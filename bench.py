@@ -1,0 +1,464 @@
+"""Benchmark of the GQA attention hot path on GB300.
+
+Default line: cached single-token decode, Q [1, 32*128], K/V cache
+[16384, 8*128] fp32 at kv_pos = 16383 (the whole cache), 32 heads over 8 kv
+heads.  Metric: K/V-stream bandwidth in GB/s = algorithmic bytes per step
+(K and V window read once, Q read, out written) / device time per step.
+Three K/V caches are rotated so each step streams a cache that is not in L2
+(3 x 128 MiB > 2 x L2).
+
+The same JSON line carries the prefill (512 queries from start_pos 1536 into
+a 2048-row cache, 32 heads over 8, D=128) and long causal forward (q_seq 8192,
+32 heads over 8, D=128) results in TFLOP/s, each with its own roofline, and
+the CPU oracle baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+the method here) on the host cores for the same metric, on a bounded sample.
+Under torchrun each rank runs its own independent decode problem on its own
+GPU (no exchange); value = all ranks' bytes / slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+H, G, D, MAX_SEQ = 32, 8, 128, 16384
+KV_POS = 16383
+DECODE_WORKLOAD = "decode q[1,32x128] kv_cache[16384,8x128] fp32 kv_pos=16383"
+PREFILL = dict(n_queries=512, start_pos=1536, max_seq=2048, H=32, G=8, D=128, stride=4096)
+FORWARD = dict(q_seq=8192, H=32, G=8, D=128)
+
+
+def decode_bytes(kv_len):
+    return 2 * kv_len * G * D * 4 + 2 * H * D * 4
+
+
+def prefill_flops():
+    p = PREFILL
+    tri = sum(p["start_pos"] + i + 1 for i in range(p["n_queries"]))
+    return 4.0 * p["D"] * tri * p["H"]
+
+
+def forward_flops():
+    f = FORWARD
+    return 4.0 * f["D"] * (f["q_seq"] * (f["q_seq"] + 1) // 2) * f["H"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, \
+        "fallback"
+
+
+def fp32_alu_peak_tflops(sm_mhz, sms):
+    # 128 fp32 FMA lanes per SM, 2 flops per FMA.
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def profile_traffic(kernel_tag, src_file):
+    """DRAM bytes per launch from the committed ncu summary of `kernel_tag`,
+    or None when there is none or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", kernel_tag + ".md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(os.path.join(ROOT, src_file), "rb").read()).hexdigest()
+    return float(m.group(1)) if cur.startswith(h.group(1)) else None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, dev_uuid=None):
+        self.rows, self.proc, self.th = [], None, None
+        self.uuid = dev_uuid
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0=None, t1=None):
+        rows = [p for (t, p) in self.rows if (t0 is None or t >= t0) and (t1 is None or t <= t1)] or \
+            [p for (_, p) in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------- oracle timing
+_ORACLE_INPUTS = {}
+
+
+def time_oracle_decode(min_seconds, kv_pos=KV_POS):
+    """Oracle decode at the bench configuration (window 0..kv_pos), repeated
+    for ~min_seconds (at least one call).  Returns (calls, seconds)."""
+    import oracle
+    from attention_gqa_online_gb300 import synthetic
+    orc = oracle.default()
+    if not _ORACLE_INPUTS:
+        q, kc, vc = synthetic.decode_inputs(MAX_SEQ, H, G, D, seed=0)
+        _ORACLE_INPUTS["x"] = (q.numpy(), kc.numpy(), vc.numpy())
+    qn, kn, vn = _ORACLE_INPUTS["x"]
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        orc.decode(qn, kn, vn, kv_pos, H, G, D, MAX_SEQ)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    return calls, el
+
+
+def reference_arm(args, world, rank):
+    """The fp64 CPU oracle on the host cores, same metric and workload.  Each
+    step is a bounded sample: the decode over the first n' cache positions,
+    n' chosen so the whole run takes about args.ref_seconds."""
+    if rank != 0:
+        return
+    _, t_cal = time_oracle_decode(0.0, kv_pos=1023)          # calibration: 1024 keys
+    per_key = t_cal / 1024.0
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
+    n_sample = int(max(64, min(KV_POS + 1, budget / per_key)))
+    times = []
+    for i in range(args.warmup + args.steps):
+        _, el = time_oracle_decode(0.0, kv_pos=n_sample - 1)
+        if i >= args.warmup:
+            times.append(el)
+    per_step = sum(times) / len(times)
+    val = decode_bytes(n_sample) / per_step / 1e9
+    sample = "per step: oracle decode over cache positions 0..%d (%d of 16384 keys, all 32 heads)" % (
+        n_sample - 1, n_sample)
+    line = {
+        "impl": "reference", "metric": "decode K/V-stream bandwidth", "value": val, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DECODE_WORKLOAD, "l2": "n/a (host)"},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- GPU arm
+def run_ours(args, world, rank, local):
+    import torch
+    import attention_gqa_online_gb300 as A
+    from attention_gqa_online_gb300 import synthetic
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    lib = A.load_library()
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20)
+    sms = props.multi_processor_count
+    peaks, peak_src = load_peaks()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid if rank == 0 else None)
+    if rank == 0:
+        sampler.start()
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    # ------------------------------------------------------------------ decode
+    cache_bytes = MAX_SEQ * G * D * 4
+    n_rot = max(3, int(math.ceil(2.0 * l2 / (2 * cache_bytes))) + 1)
+    q, kc, vc = synthetic.decode_inputs(MAX_SEQ, H, G, D, seed=rank)
+    qd = q.to(dev)
+    caches = [(kc.to(dev), vc.to(dev))]
+    for _ in range(n_rot - 1):
+        caches.append((caches[0][0].clone(), caches[0][1].clone()))
+    out = torch.empty_like(qd)
+    ws_bytes = A.attn_decode_workspace_bytes(H, G, D, MAX_SEQ)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    pos = torch.full((1,), KV_POS, dtype=torch.int32, device=dev)
+    ptrs = [(k.data_ptr(), v.data_ptr()) for k, v in caches]
+
+    def decode_step(i):
+        kp, vp = ptrs[i % n_rot]
+        rc = lib.attn_decode_cached(qd.data_ptr(), kp, vp, pos.data_ptr(), out.data_ptr(), H, G, D, MAX_SEQ,
+                                    ws.data_ptr(), ws_bytes, sh)
+        if rc != 0:
+            raise RuntimeError("attn_decode_cached failed: %d" % rc)
+
+    for i in range(args.warmup):
+        decode_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        decode_step(i)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(ms_total, world)
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    status = A.attn_get_status(sh)
+    if status != 0:
+        raise RuntimeError("device status %d after the decode loop" % status)
+    ms_step = ms_total / args.steps
+    step_bytes = decode_bytes(KV_POS + 1)
+    value = step_bytes * world * args.steps / (ms_total * 1e-3) / 1e9
+    achieved = step_bytes / (kern_ms * 1e-3) / 1e9
+    clocks = sampler.summary(wall0, wall1) if rank == 0 else None
+
+    # e2e: a serving decode step through the public API from pinned host memory:
+    # H2D of the new token's q and its K/V rows (written into cache row kv_pos) and
+    # of kv_pos, the decode, D2H of out.
+    qh = q.pin_memory()
+    krow = caches[0][0][KV_POS].cpu().pin_memory()
+    vrow = caches[0][1][KV_POS].cpu().pin_memory()
+    posh = torch.full((1,), KV_POS, dtype=torch.int32).pin_memory()
+    outh = torch.empty_like(q).pin_memory()
+    h2d = qh.numel() * 4 + krow.numel() * 4 + vrow.numel() * 4 + 4
+    d2h = outh.numel() * 4
+
+    def e2e_step(i):
+        kd, vd = caches[i % n_rot]
+        qd.copy_(qh, non_blocking=True)
+        kd[KV_POS].copy_(krow, non_blocking=True)
+        vd[KV_POS].copy_(vrow, non_blocking=True)
+        pos.copy_(posh, non_blocking=True)
+        A.attn_decode_cached(qd, kd, vd, pos, out, H, G, D, MAX_SEQ, ws, ws_bytes, stream)
+        outh.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_val = step_bytes * world * args.steps / (e2e_ms * 1e-3) / 1e9
+    del caches
+
+    extras = {}
+    if rank == 0 and not args.decode_only:
+        extras = run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_src, clocks)
+
+    if rank == 0:
+        sampler.stop()
+        traffic = profile_traffic("decode_split_kernel", "attention_gqa_online_gb300/csrc/decode.cu")
+        line = {
+            "metric": "decode K/V-stream bandwidth", "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": DECODE_WORKLOAD, "heads": H, "kv_heads": G, "head_dim": D,
+                       "l2": "inputs rotate over %d K/V caches (%d MiB) > 2x L2" % (n_rot, n_rot * 2 * cache_bytes >> 20),
+                       "parallelism": "independent decode per GPU" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "kernel": "decode_split_kernel<128,4>", "kernel_us": kern_ms * 1e3,
+                         "bytes_per_launch": step_bytes, "peak_source": peak_src},
+            "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "what": "per step: H2D q + new K/V row + kv_pos, decode, D2H out",
+                    "us_per_step": e2e_ms * 1e3 / args.steps},
+            "gpu_launches": args.steps + extras.pop("_launches", 0),
+            "clocks": clocks,
+            "decode_us_per_token": ms_step * 1e3,
+        }
+        line.update(extras)
+        if not args.no_cpu_baseline:
+            calls, el = time_oracle_decode(args.cpu_seconds)
+            line["cpu_baseline"] = {"value": decode_bytes(KV_POS + 1) * calls / el / 1e9, "unit": "GB/s",
+                                    "cores": 1, "kind": "oracle",
+                                    "sample": "%d oracle decode calls at kv_pos=16383 in %.1f s" % (calls, el)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_src, clocks):
+    """Prefill and long causal forward on the fp32 CUDA-core path (TFLOP/s)."""
+    import torch
+    res, launches = {}, 0
+    sm_mhz = (clocks or {}).get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    alu_peak = fp32_alu_peak_tflops(sm_mhz, sms)
+    steps = max(3, min(args.steps, args.extra_steps))
+
+    def timed(fn, n):
+        for i in range(args.warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            evs[i][0].record(stream)
+            fn(i)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    p = PREFILL
+    qb, kc, vc = synthetic.prefill_inputs(p["n_queries"], p["stride"], p["max_seq"], p["G"] * p["D"], seed=0)
+    per = (qb.numel() + kc.numel() + vc.numel()) * 4
+    n_rot = max(2, int(math.ceil(2.0 * l2 / per)) + 1)
+    bufs = [(qb.to(dev), kc.to(dev), vc.to(dev)) for _ in range(n_rot)]
+    outp = torch.empty((p["n_queries"], p["stride"]), device=dev)
+    scale = 1.0 / math.sqrt(p["D"])
+
+    def prefill_step(i):
+        qd, kd, vd = bufs[i % n_rot]
+        rc = lib.attn_prefill(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outp.data_ptr(), p["n_queries"], p["H"],
+                              p["G"], p["D"], p["G"] * p["D"], p["max_seq"], scale, p["start_pos"], p["stride"],
+                              p["stride"], 0, A.ATTN_FP32, sh)
+        if rc != 0:
+            raise RuntimeError("attn_prefill failed: %d" % rc)
+
+    ms = timed(prefill_step, steps)
+    launches += steps
+    tf = prefill_flops() / (ms * 1e-3) / 1e12
+    res["prefill"] = {"workload": "prefill 512 queries start_pos=1536 max_seq=2048 32/8 heads D=128 fp32",
+                      "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "prec": "fp32",
+                      "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s",
+                                   "frac": tf / alu_peak, "traffic": None,
+                                   "kernel": "flash_simt_kernel<128,true>",
+                                   "peak_source": "fp32 FMA: %d SMs x 128 lanes x 2 x %.0f MHz" % (sms, sm_mhz)},
+                      "l2": "rotating %d input sets" % n_rot}
+    del bufs
+
+    f = FORWARD
+    q, k, v = synthetic.forward_inputs(f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], seed=5, qk_sigma=3.0)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    outf = torch.empty_like(qd)
+    lse = torch.empty((f["q_seq"], f["H"], 2), device=dev)
+
+    def fwd_step(i):
+        rc = lib.attn_forward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(), lse.data_ptr(),
+                              f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], A.ATTN_CAUSAL, A.ATTN_FP32, sh)
+        if rc != 0:
+            raise RuntimeError("attn_forward failed: %d" % rc)
+
+    ms = timed(fwd_step, steps)
+    launches += steps
+    tf = forward_flops() / (ms * 1e-3) / 1e12
+    res["forward"] = {"workload": "causal forward+LSE q_seq=8192 32/8 heads D=128 fp32", "value": tf,
+                      "unit": "TFLOP/s", "ms_per_step": ms, "prec": "fp32",
+                      "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s",
+                                   "frac": tf / alu_peak, "traffic": None,
+                                   "kernel": "flash_simt_kernel<128,true>"},
+                      "l2": "inputs 192 MiB > L2"}
+    res["_launches"] = launches
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--extra-steps", type=int, default=20)
+    ap.add_argument("--decode-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+        return
+    run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * attn_gqa.h -- C ABI of libattn_gqa.so: grouped-query scaled-dot-product
+ * attention computed in one tiled online-softmax pass on an NVIDIA GB300
+ * (sm_103a).  The score matrix is never materialised.
+ *
+ * The operations are those of three published WGSL compute shaders:
+ *   - meganeura 0.2.0, src/shaders/attention.wgsl         -> attn_forward
+ *   - meganeura 0.2.0, src/shaders/cached_attention.wgsl  -> attn_decode_cached
+ *   - cera, src/backend/shaders/attention_prefill.wgsl    -> attn_prefill
+ * Argument lists follow the shaders' parameter lists; shader templating and
+ * storage bindings become plain arguments.
+ *
+ * Common rules for every entry point
+ *   Notation   H = num_heads, G = num_kv_heads, D = head_dim, gs = H / G.
+ *   GQA map    query head h reads kv head g = h / gs (integer division); H
+ *              must be a multiple of G (all three shaders divide this way).
+ *   Scale      scores are scale * (q . k); forward and decode use
+ *              scale = 1 / sqrt(D) (the meganeura shaders' inverseSqrt), prefill
+ *              takes scale as an argument (the cera shader's params[5]).
+ *   Data       fp32 in, fp32 out, row-major, all pointers are DEVICE memory
+ *              owned by the caller.  The library keeps no pointer after a call
+ *              returns and allocates no device memory.
+ *   Streams    every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *              the legacy default stream).  Results are ready when the stream
+ *              has reached the call.
+ *   Errors     the return value is an attn status code.  Host-side checks run
+ *              before anything is launched: on ATTN_ERR_INVALID_ARG or
+ *              ATTN_ERR_UNSUPPORTED nothing is written.  ATTN_ERR_CUDA means a
+ *              launch failed (the CUDA error is left in place for
+ *              cudaGetLastError).  Conditions only the device can see (a
+ *              device-resident kv_pos past the cache, a bounded wait that ran
+ *              out) are recorded in a per-device status word; read it with
+ *              attn_get_status.
+ *   Empty      a window of zero keys writes zeros to the output rows and
+ *              (-1e30, -1e30) to their LSE pair (attention.wgsl, fn main: the
+ *              select() guards on sum_exp == 0).
+ *   Precision  ATTN_FP32: fp32 CUDA-core arithmetic throughout.
+ *              ATTN_TF32: QK^T and PV on tcgen05 tensor cores with TF32
+ *              operands and fp32 accumulation; softmax in fp32.
+ *              ATTN_BF16: as TF32 but with bf16 operands (inputs are rounded
+ *              to bf16 on the way in), fp32 accumulation.
+ *              Tensor-core precisions need D in {64, 128}, gs a power of two
+ *              <= 128, 16-byte aligned pointers and row strides that are
+ *              multiples of 4 floats; otherwise they return
+ *              ATTN_ERR_UNSUPPORTED.  ATTN_FP32 accepts any 1 <= D <= 128.
+ */
+#ifndef ATTN_GQA_H
+#define ATTN_GQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; declared here so the header needs no
+ * CUDA include. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+    ATTN_CAUSAL = 0, /* query at position p sees keys 0..p          (kv_seq == q_seq) */
+    ATTN_FULL = 1,   /* every query sees keys 0..q_seq-1             (kv_seq == q_seq) */
+    ATTN_CROSS = 2   /* every query sees keys 0..kv_seq-1 (any kv_seq, 0 allowed)      */
+} attn_mask_t;
+
+typedef enum { ATTN_FP32 = 0, ATTN_TF32 = 1, ATTN_BF16 = 2 } attn_prec_t;
+
+enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,
+    ATTN_ERR_UNSUPPORTED = 2,
+    ATTN_ERR_CUDA = 3,
+    ATTN_ERR_TIMEOUT = 4
+};
+
+/*
+ * Self / cross attention forward with per-row (max, log-sum) output.
+ * Source: meganeura attention.wgsl, fn main (variants causal kv_len = pos+1,
+ * full kv_len = q_seq, cross kv_len = kv_seq; final store of
+ * lse[(pos*H + head)*2 + {0,1}] = (max_score, log(sum_exp))).
+ *
+ *   q    [q_seq, H*D]     element (pos, h, d) at pos*H*D + h*D + d
+ *   k, v [kv_seq, G*D]    element (t, g, d)   at t*G*D + g*D + d
+ *   out  [q_seq, H*D]     same layout as q
+ *   lse  [q_seq, H, 2]    (m, log l) with m the row's largest scaled score and
+ *                         l = sum_t exp(s_t - m), so log-sum-exp = m + log l.
+ *                         May be NULL (not written).
+ *   mask ATTN_CAUSAL / ATTN_FULL need kv_seq == q_seq.
+ *   prec ATTN_FP32, ATTN_TF32 or ATTN_BF16.
+ * q_seq == 0 is a no-op (pointers may then be NULL).  Errors: INVALID_ARG for
+ * NULL q/k/v/out (or k/v with kv_seq > 0), H % G != 0, G == 0, D == 0 or
+ * D > 128, kv_seq != q_seq for causal/full, an unknown mask or precision;
+ * UNSUPPORTED as described under Precision.
+ */
+ATTN_API int attn_forward(const float *q, const float *k, const float *v, float *out, float *lse,
+                 uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
+                 uint32_t head_dim, int mask, int prec, attn_stream_t stream);
+
+/*
+ * Bytes of device workspace attn_decode_cached needs for these sizes on the
+ * current device (its SM count sets the number of KV splits).  Returns 0 for
+ * sizes attn_decode_cached would reject.
+ */
+ATTN_API size_t attn_decode_workspace_bytes(uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim,
+                                   uint32_t max_seq);
+
+/*
+ * Cached single-token decode.  Source: meganeura cached_attention.wgsl,
+ * fn main (Q = [1, H*D], K/V from a cache, kv_len = kv_pos_buf[0] + 1, so the
+ * token attends to positions 0..kv_pos inclusive).
+ *
+ *   q                  [1, H*D]
+ *   k_cache, v_cache   [max_seq, G*D]
+ *   kv_pos_dev         one uint32 in DEVICE memory, read by the kernels (so a
+ *                      CUDA graph can replay the call as the position grows)
+ *   out                [1, H*D]
+ *   max_seq            rows of the cache.  The window is cut at max_seq keys
+ *                      (the cera prefill shader's defensive clamp); a kv_pos
+ *                      >= max_seq also records ATTN_ERR_INVALID_ARG in the
+ *                      device status word.
+ *   workspace          device buffer of at least
+ *                      attn_decode_workspace_bytes(H, G, D, max_seq) bytes,
+ *                      16-byte aligned.  Zero it once (cudaMemset) before its
+ *                      first use; each completed call leaves it ready for the
+ *                      next.  Calls that share a workspace must not overlap on
+ *                      the GPU.
+ * The work is split over KV ranges; each split keeps its own (max, sum,
+ * weighted V) and the last split of each kv head to finish merges them with
+ * the log-sum-exp rule.  Errors: INVALID_ARG for NULL pointers, H % G != 0,
+ * G == 0, D == 0 or D > 128, max_seq == 0, or a workspace that is too small
+ * or misaligned.
+ */
+ATTN_API int attn_decode_cached(const float *q, const float *k_cache, const float *v_cache,
+                       const uint32_t *kv_pos_dev, float *out, uint32_t num_heads,
+                       uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq,
+                       void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * Batched causal prefill against a KV cache.  Source: cera
+ * attention_prefill.wgsl, fn attention_prefill (params n_heads, n_kv_heads,
+ * head_dim, kv_dim, max_seq, scale, start_pos, q_stride, out_stride, q_base;
+ * q_global = q_base + i; window min(start_pos + q_global + 1, max_seq)).
+ *
+ *   q_batch    query i of this call, head h, at (q_base+i)*q_stride + h*D
+ *   k_cache,
+ *   v_cache    [max_seq, kv_dim]; kv head g at column g*D
+ *   out_batch  (q_base+i)*out_stride + h*D; other columns are not written
+ *   n_queries  queries in this call (the shader's dispatch height)
+ * n_queries == 0 is a no-op.  Errors: INVALID_ARG for NULL pointers,
+ * H % G != 0, G == 0, D == 0 or D > 128, kv_dim < G*D, q_stride or
+ * out_stride < H*D, start_pos + q_base + n_queries > max_seq (the shader's
+ * host-side assertion), a non-finite scale or an unknown precision;
+ * UNSUPPORTED as described under Precision.
+ */
+ATTN_API int attn_prefill(const float *q_batch, const float *k_cache, const float *v_cache,
+                 float *out_batch, uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads,
+                 uint32_t head_dim, uint32_t kv_dim, uint32_t max_seq, float scale,
+                 uint32_t start_pos, uint32_t q_stride, uint32_t out_stride, uint32_t q_base,
+                 int prec, attn_stream_t stream);
+
+/*
+ * Waits for `stream`, then returns and clears the current device's status
+ * word: ATTN_OK, or the largest code a kernel recorded since the last read
+ * (ATTN_ERR_INVALID_ARG for a decode kv_pos past the cache, ATTN_ERR_TIMEOUT
+ * for a bounded device wait that gave up; its kernel returned early and its
+ * output is not valid).  Returns ATTN_ERR_CUDA if the stream or the read
+ * failed.
+ */
+ATTN_API int attn_get_status(attn_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+ATTN_API const char *attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GQA_H */

@@ -19,3 +19,16 @@ def pytest_configure(config):
 def orc():
     import oracle
     return oracle.default()
+
+
+@pytest.fixture(scope="session")
+def cuda_lib():
+    """The built CUDA library on a visible GPU (skips when there is no GPU)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from attention_gqa_online_gb300 import build as _b
+    _b.build()
+    import attention_gqa_online_gb300 as A
+    A.load_library()
+    return A

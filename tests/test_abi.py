@@ -1,0 +1,97 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects bad arguments on the host before touching the device."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_gqa_online_gb300 import build
+    build.build()
+    import attention_gqa_online_gb300 as A
+    return A.load_library()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"ATTN_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"attn_forward", "attn_decode_cached", "attn_prefill", "attn_decode_workspace_bytes",
+            "attn_get_status", "attn_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.attn_status_string(code)
+    assert lib.attn_status_string(99) == b"unknown status"
+
+
+def fwd(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=None, q_seq=16, kv_seq=16, H=4, G=2, D=64, mask=0, prec=0):
+    return lib.attn_forward(q, k, v, out, lse, q_seq, kv_seq, H, G, D, mask, prec, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(H=5, G=2), dict(G=0), dict(D=0), dict(D=129), dict(mask=3), dict(mask=-1), dict(prec=7),
+    dict(mask=0, kv_seq=17), dict(mask=1, kv_seq=8), dict(q=None), dict(out=None), dict(k=None),
+    dict(mask=2, kv_seq=5, v=None), dict(q_seq=2 ** 31),
+])
+def test_forward_rejects(lib, kw):
+    assert fwd(lib, **kw) == 1
+
+
+def test_forward_empty_query_is_noop(lib):
+    assert fwd(lib, q=None, k=None, v=None, out=None, q_seq=0, kv_seq=0) == 0
+    assert fwd(lib, q=None, k=None, v=None, out=None, q_seq=0, kv_seq=5, mask=2) == 0
+
+
+def pre(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, n=8, H=4, G=2, D=64, kv_dim=128, max_seq=64, scale=0.125,
+        start=0, q_stride=256, out_stride=256, q_base=0, prec=0):
+    return lib.attn_prefill(q, k, v, out, n, H, G, D, kv_dim, max_seq, scale, start, q_stride, out_stride,
+                            q_base, prec, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(H=6, G=4), dict(D=130), dict(kv_dim=127), dict(q_stride=255), dict(out_stride=100),
+    dict(start=50, n=15), dict(start=40, q_base=20, n=5), dict(scale=math.inf), dict(scale=math.nan),
+    dict(q=None), dict(k=None), dict(v=None), dict(out=None), dict(prec=3), dict(max_seq=2 ** 31, n=1),
+])
+def test_prefill_rejects(lib, kw):
+    assert pre(lib, **kw) == 1
+
+
+def test_prefill_empty_batch_is_noop(lib):
+    assert pre(lib, q=None, k=None, v=None, out=None, n=0) == 0
+
+
+def dec(lib, q=FAKE, k=FAKE, v=FAKE, pos=FAKE, out=FAKE, H=32, G=8, D=128, max_seq=100, ws=FAKE, nbytes=1 << 20):
+    return lib.attn_decode_cached(q, k, v, pos, out, H, G, D, max_seq, ws, nbytes, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(H=30), dict(G=0), dict(D=0), dict(D=200), dict(max_seq=0), dict(q=None), dict(k=None), dict(v=None),
+    dict(pos=None), dict(out=None),
+])
+def test_decode_rejects(lib, kw):
+    assert dec(lib, **kw) == 1
+
+
+def test_workspace_query_rejects_bad_sizes(lib):
+    assert lib.attn_decode_workspace_bytes(5, 2, 64, 100) == 0
+    assert lib.attn_decode_workspace_bytes(4, 2, 64, 0) == 0
+    assert lib.attn_decode_workspace_bytes(4, 2, 0, 10) == 0

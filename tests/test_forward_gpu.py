@@ -1,0 +1,92 @@
+"""attn_forward on the GPU against the fp64 oracle (same seeded inputs)."""
+import numpy as np
+import pytest
+import torch
+
+from attention_gqa_online_gb300 import synthetic
+from helpers import FP32, assert_lse_close, assert_out_close, dev
+
+pytestmark = pytest.mark.gpu
+CAUSAL, FULL, CROSS = 0, 1, 2
+PRECS = [FP32]
+
+
+def run_forward(A, q, k, v, q_seq, kv_seq, H, G, D, mask, prec):
+    out = torch.full((q_seq, H * D), float("nan"), device="cuda")
+    lse = torch.full((q_seq, H, 2), float("nan"), device="cuda")
+    A.attn_forward(dev(q) if q_seq else None, dev(k) if kv_seq else None, dev(v) if kv_seq else None,
+                   out, lse, q_seq, kv_seq, H, G, D, mask, prec)
+    torch.cuda.synchronize()
+    assert A.attn_get_status() == 0
+    return out.cpu().numpy(), lse.cpu().numpy()
+
+
+def check(A, orc, q_seq, kv_seq, H, G, D, mask, prec, seed=0, rows=None, **kw):
+    q, k, v = synthetic.forward_inputs(q_seq, kv_seq, H, G, D, seed=seed, **kw)
+    out, lse = run_forward(A, q, k, v, q_seq, kv_seq, H, G, D, mask, prec)
+    ro, rl = orc.forward(q.numpy(), k.numpy(), v.numpy(), q_seq, kv_seq, H, G, D, mask, rows=rows)
+    sel = slice(None) if rows is None else np.asarray(rows)
+    vmax = float(v.abs().max()) if kv_seq else 1.0
+    where = "q%d kv%d H%d G%d D%d mask%d prec%d" % (q_seq, kv_seq, H, G, D, mask, prec)
+    assert_out_close(out[sel], ro[sel], prec, vmax, where)
+    assert_lse_close(lse[sel], rl[sel], prec, float(np.abs(rl[sel][..., 0]).max()) if q_seq else 1.0, where)
+    return out, lse
+
+
+@pytest.mark.parametrize("prec", PRECS)
+@pytest.mark.parametrize("mask,kv", [(CAUSAL, 16), (FULL, 16), (CROSS, 24)])
+def test_small_config(cuda_lib, orc, prec, mask, kv):
+    """q_seq=16, 4 heads over 2 kv heads, D=64, N(0,1), seed 0."""
+    check(cuda_lib, orc, 16, kv, 4, 2, 64, mask, prec)
+
+
+@pytest.mark.parametrize("prec", PRECS)
+@pytest.mark.parametrize("q_seq,kv_seq,H,G,D,mask", [
+    (67, 67, 6, 2, 80, CAUSAL),      # gs = 3, several row tiles, ragged tail
+    (67, 67, 6, 2, 80, FULL),
+    (45, 131, 8, 8, 64, CROSS),      # MHA, ragged key tail
+    (130, 130, 16, 2, 128, CAUSAL),  # gs = 8
+    (33, 33, 4, 1, 32, CAUSAL),
+    (20, 20, 2, 1, 12, CAUSAL),      # head_dim not a multiple of 16
+    (9, 9, 3, 3, 1, FULL),           # head_dim 1
+    (5, 300, 2, 2, 100, CROSS),
+    (1, 1, 4, 2, 64, CAUSAL),        # single query: window of one key
+    (200, 200, 1, 1, 128, CAUSAL),
+])
+def test_shapes(cuda_lib, orc, prec, q_seq, kv_seq, H, G, D, mask):
+    check(cuda_lib, orc, q_seq, kv_seq, H, G, D, mask, prec, seed=q_seq + D)
+
+
+@pytest.mark.parametrize("prec", PRECS)
+def test_window_one_returns_v0(cuda_lib, prec):
+    q, k, v = synthetic.forward_inputs(3, 3, 4, 2, 64, seed=21)
+    out, lse = run_forward(cuda_lib, q, k, v, 3, 3, 4, 2, 64, CAUSAL, prec)
+    for h in range(4):
+        g = h // 2
+        np.testing.assert_allclose(out[0, h * 64:(h + 1) * 64], v[0, g * 64:(g + 1) * 64].numpy(), rtol=0,
+                                   atol=1e-6 if prec == FP32 else 1e-2)
+        assert abs(lse[0, h, 1]) < 1e-6
+
+
+@pytest.mark.parametrize("prec", PRECS)
+def test_empty_cross_window(cuda_lib, prec):
+    q, _, _ = synthetic.forward_inputs(7, 0, 4, 2, 64, seed=22)
+    out, lse = run_forward(cuda_lib, q, None, None, 7, 0, 4, 2, 64, CROSS, prec)
+    assert np.all(out == 0.0) and np.all(lse == np.float32(-1e30))
+
+
+@pytest.mark.parametrize("prec", PRECS)
+@pytest.mark.parametrize("mask,q_seq,kv_seq", [(FULL, 2048, 2048), (CROSS, 1024, 4096)])
+def test_mha_full_and_cross(cuda_lib, orc, prec, mask, q_seq, kv_seq):
+    """16 heads = 16 kv heads, D=64; Q,K N(0,1), V U(-1,1)."""
+    rows = None if mask == CROSS else list(range(0, 2048, 7)) + [2047]
+    check(cuda_lib, orc, q_seq, kv_seq, 16, 16, 64, mask, prec, seed=4, v_dist="uniform", rows=rows)
+
+
+@pytest.mark.parametrize("prec", PRECS)
+@pytest.mark.parametrize("q_seq", [8192, 8193])
+def test_long_causal_stress(cuda_lib, orc, prec, q_seq):
+    """q_seq 8192/8193, 32 heads over 8 kv heads, D=128, Q,K N(0,3^2): sampled rows."""
+    rng = np.random.default_rng(q_seq)
+    rows = sorted(set(range(16)) | set(range(q_seq - 16, q_seq)) | set(rng.integers(0, q_seq, 16).tolist()))
+    check(cuda_lib, orc, q_seq, q_seq, 32, 8, 128, CAUSAL, prec, seed=5, rows=rows, qk_sigma=3.0)
