@@ -169,22 +169,31 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+    // Each group of 8 products is summed on its own before it joins the
+    // running dot product: 16 roundings of the large partial sum instead of
+    // 128 keeps fp32 scores within a few ulp for widely spread inputs.
     const float* kt = sm.k[buf];
-#pragma unroll 4
-    for (int d = 0; d < DMAX; d += 4) {
-      float4 qa[4], kb[4];
+#pragma unroll 2
+    for (int d = 0; d < DMAX; d += 8) {
+      float4 qa[4][2], kb[4][2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) qa[i] = *reinterpret_cast<const float4*>(&sm.q[(r0 + i) * QS + d]);
+      for (int i = 0; i < 4; ++i) {
+        qa[i][0] = *reinterpret_cast<const float4*>(&sm.q[(r0 + i) * QS + d]);
+        qa[i][1] = *reinterpret_cast<const float4*>(&sm.q[(r0 + i) * QS + d + 4]);
+      }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) kb[j] = *reinterpret_cast<const float4*>(&kt[(cl + 16 * j) * QS + d]);
+      for (int j = 0; j < 4; ++j) {
+        kb[j][0] = *reinterpret_cast<const float4*>(&kt[(cl + 16 * j) * QS + d]);
+        kb[j][1] = *reinterpret_cast<const float4*>(&kt[(cl + 16 * j) * QS + d + 4]);
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) s[i][j] = dot4(qa[i], kb[j], s[i][j]);
+        for (int j = 0; j < 4; ++j) s[i][j] += dot4(qa[i][1], kb[j][1], dot4(qa[i][0], kb[j][0], 0.f));
     }
 
     // Mask, tile max, correction, exponentials, running sum.
-    float p[4][4];
+    float p[4][4], corr_row[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float mx = -INFINITY;
@@ -209,15 +218,20 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
       for (int off = 8; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
       l_run[i] = l_run[i] * corr + sum;
       m_run[i] = m_new;
-#pragma unroll
-      for (int c = 0; c < OC * 4; ++c) o[i][c] *= corr;
+      corr_row[i] = corr;
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       *reinterpret_cast<float4*>(&sm.p[(cl + 16 * j) * PS + r0]) = make_float4(p[0][j], p[1][j], p[2][j], p[3][j]);
     __syncthreads();
 
-    // O += P V.
+    // O = O * corr + P V, with P V of this tile summed on its own first (one
+    // rounding of the long-running accumulator per tile, not per key).
+    float t[4][OC * 4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < OC * 4; ++c) t[i][c] = 0.f;
     const float* vt = sm.v[buf];
 #pragma unroll 4
     for (int kk = 0; kk < BN; ++kk) {
@@ -230,13 +244,17 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
         if (DMAX >= 64 || col < DMAX) vv = *reinterpret_cast<const float4*>(&vt[kk * DMAX + col]);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          o[i][4 * jj + 0] = fmaf(pr[i], vv.x, o[i][4 * jj + 0]);
-          o[i][4 * jj + 1] = fmaf(pr[i], vv.y, o[i][4 * jj + 1]);
-          o[i][4 * jj + 2] = fmaf(pr[i], vv.z, o[i][4 * jj + 2]);
-          o[i][4 * jj + 3] = fmaf(pr[i], vv.w, o[i][4 * jj + 3]);
+          t[i][4 * jj + 0] = fmaf(pr[i], vv.x, t[i][4 * jj + 0]);
+          t[i][4 * jj + 1] = fmaf(pr[i], vv.y, t[i][4 * jj + 1]);
+          t[i][4 * jj + 2] = fmaf(pr[i], vv.z, t[i][4 * jj + 2]);
+          t[i][4 * jj + 3] = fmaf(pr[i], vv.w, t[i][4 * jj + 3]);
         }
       }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < OC * 4; ++c) o[i][c] = fmaf(o[i][c], corr_row[i], t[i][c]);
     __syncthreads();
   }
 
