@@ -130,6 +130,23 @@ def attn_prefill(q_batch, k_cache, v_cache, out_batch, n_queries, n_heads, n_kv_
         float(scale), start_pos, q_stride, out_stride, q_base, prec, _stream(stream)), "attn_prefill")
 
 
+def attn_decode_cached_noalloc(q, k_cache, v_cache, kv_pos_dev, out, num_heads, num_kv_heads, head_dim, max_seq,
+                               stream=None):
+    """Cached decode with no workspace argument: the library uses a fixed
+    4 MiB device array of its own instead (for callers that cannot allocate
+    device memory); see attn_gqa.h for its limits and sharing rules."""
+    lib = load_library()
+    fn = lib.attn_decode_cached_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [_vp, _vp, _vp, _vp, _vp, _u32, _u32, _u32, _u32, _vp]
+    f = _f32()
+    if hasattr(kv_pos_dev, "element_size") and kv_pos_dev.element_size() != 4:
+        raise ValueError("kv_pos_dev must hold one 32-bit unsigned position")
+    _check(fn(_addr(q, "q", f), _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f),
+              _addr(kv_pos_dev, "kv_pos_dev"), _addr(out, "out", f), num_heads, num_kv_heads, head_dim, max_seq,
+              _stream(stream)), "attn_decode_cached_noalloc")
+
+
 def attn_get_status(stream=None):
     """Synchronise `stream`, return and clear the device status word."""
     return int(load_library().attn_get_status(_stream(stream)))

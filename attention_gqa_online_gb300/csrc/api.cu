@@ -63,6 +63,9 @@ int run_flash(const FlashArgs& a, int prec, cudaStream_t s) {
 }
 
 }  // namespace
+
+unsigned* device_status_word() { return status_ptr(); }
+
 }  // namespace attn
 
 using namespace attn;

@@ -326,6 +326,8 @@ size_t decode_workspace_bytes(int H, int G, int D, int max_seq, int sm_count) {
          sizeof(float) * (size_t)H * S * D;
 }
 
+size_t decode_ticket_bytes(int G) { return align256(sizeof(unsigned) * G); }
+
 int launch_decode_split(const DecodeArgs& a, int S, cudaStream_t s) {
   const int gs = a.H / a.G;
   if (a.D == 128) {

@@ -61,5 +61,11 @@ size_t decode_workspace_bytes(int H, int G, int D, int max_seq, int sm_count);
 // True if the split-KV kernels handle these sizes (else the generic kernel runs).
 bool decode_split_supported(int H, int G, int D);
 int launch_decode_split(const DecodeArgs& a, int splits, cudaStream_t s);
+// Bytes at the start of a split-decode workspace that must be zero when a
+// call begins (the per-kv-head arrival counters).
+size_t decode_ticket_bytes(int G);
+
+// Device address of the current device's status word (nullptr on failure).
+unsigned* device_status_word();
 
 }  // namespace attn

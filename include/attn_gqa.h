@@ -166,6 +166,39 @@ ATTN_API int attn_prefill(const float *q_batch, const float *k_cache, const floa
                  int prec, attn_stream_t stream);
 
 /*
+ * Cached single-token decode that allocates nothing and takes no workspace.
+ * The shader pages have no counterpart to this entry point; it exists for
+ * callers that cannot provide device scratch memory -- a plugin inside a
+ * framework that owns every device allocation, or a serving loop that must
+ * never call cudaMalloc (an allocation may synchronise the device and has no
+ * latency bound).
+ *
+ * Arguments, layouts, the window rule and the result are those of
+ * attn_decode_cached, minus the workspace.  In its place the library uses a
+ * fixed 4 MiB array of device memory that is part of the library image: every
+ * GPU that loads libattn_gqa.so holds it until the process exits.
+ *   - Sizes whose split decode would need more than 4 MiB of scratch (about
+ *     H * 2 * SMs / G * D * 4 bytes), shapes the split kernels do not cover
+ *     (D = 128 with gs in {1, 2, 4}; D = 64 with gs in {1, 2, 4, 8}) and
+ *     pointers that are not 16-byte aligned return ATTN_ERR_UNSUPPORTED;
+ *     nothing is launched.
+ *   - All calls on a device share the one array, and it keeps what the last
+ *     call left there; each call first clears the counters that must start
+ *     at zero, on `stream`.  Calls that can overlap on the GPU (different
+ *     streams without ordering between them) race on the array and give
+ *     wrong results: order them on one stream.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ * Errors: as attn_decode_cached (INVALID_ARG for bad sizes or NULL pointers),
+ * plus the UNSUPPORTED cases above.
+ */
+ATTN_API int attn_decode_cached_noalloc(const float *q, const float *k_cache, const float *v_cache,
+                                        const uint32_t *kv_pos_dev, float *out, uint32_t num_heads,
+                                        uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq,
+                                        attn_stream_t stream);
+
+/*
  * Waits for `stream`, then returns and clears the current device's status
  * word: ATTN_OK, or the largest code a kernel recorded since the last read
  * (ATTN_ERR_INVALID_ARG for a decode kv_pos past the cache, ATTN_ERR_TIMEOUT
