@@ -30,21 +30,26 @@
 namespace attn {
 namespace {
 
-constexpr int kT = 32;         // positions per stage
-constexpr int kStages = 3;     // stages in flight
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kPpw = kT / kWarps;  // positions per warp per stage (8)
-constexpr int kMinChunk = 64;      // fewest positions a split is given
+constexpr int kT = 16;                    // positions per stage
+constexpr int kStages = 4;                // stages in flight
+constexpr int kCWarps = 4;                // consumer warps
+constexpr int kThreads = 32 * (kCWarps + 1);  // + one producer warp
+constexpr int kCtasPerSm = 3;
+constexpr int kMinChunk = 64;             // fewest positions a split is given
+// Most splits per kv head: the final merge keeps GS * splits floats twice in
+// the (then idle) stage buffers, at least kStages * kT * 64 floats per array.
+constexpr int kMaxSplits = 448;
+static_assert(8 * kMaxSplits <= kStages * kT * 64, "merge scratch too small");
 
 template <int D, int GS>
 struct DecodeSmem {
   float k[kStages][kT * D];
   float v[kStages][kT * D];
-  float red_m[kWarps][GS];
-  float red_l[kWarps][GS];
-  float red_o[kWarps][GS][D];
+  float red_m[kCWarps][GS];
+  float red_l[kCWarps][GS];
+  float red_o[kCWarps][GS][D];
   uint64_t full[kStages];
+  uint64_t empty[kStages];
   int is_last;
 };
 
@@ -67,11 +72,13 @@ __host__ __device__ inline WsLayout ws_layout(void* ws, int H, int G, int D, int
   return l;
 }
 
-// Lane layout for the scores: lane = 8 * p + c handles position p (0..3) of
-// the current group of four and the dims {4c + 32u : u < D/32} (float4 each),
-// so each 8-lane phase of a 16-byte shared load reads one contiguous row.
+// Warp roles: warps 0..3 consume, warp 4 issues the bulk copies.  Consumer
+// warp w owns positions 4w..4w+3 of every stage; within it lane = 8p + c
+// takes position p and dims {4c + 32u : u < D/32} (float4 each), so each
+// 8-lane phase of a 16-byte shared load reads one contiguous row.
 template <int D, int GS>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeArgs a, const int S, const float sl2) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    decode_split_kernel(const DecodeArgs a, const int S, const float sl2) {
   using Smem = DecodeSmem<D, GS>;
   constexpr int U = D / 32;   // float4 groups per lane in the score phase
   constexpr int VP = D / 32;  // output dims per lane in the PV phase
@@ -94,40 +101,14 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeArgs
   const int len = p_end - p_begin;
   const int n_st = (len + kT - 1) / kT;
 
-  // Query registers: q[h][u] holds dims 4c + 32u .. +3 of head g*GS + h, pre-scaled.
-  const int qp = lane >> 3, qc = lane & 7;
-  float4 qr[GS][U];
-#pragma unroll
-  for (int h = 0; h < GS; ++h)
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float4 x = *reinterpret_cast<const float4*>(a.q + (size_t)(g * GS + h) * D + 4 * qc + 32 * u);
-      qr[h][u] = make_float4(x.x * sl2, x.y * sl2, x.z * sl2, x.w * sl2);
-    }
-
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kCWarps);
+    }
     fence_mbar_init();
   }
   __syncthreads();
-
-  const size_t row_stride = (size_t)a.G * D;
-  const float* kbase = a.k_cache + (size_t)g * D;
-  const float* vbase = a.v_cache + (size_t)g * D;
-  auto issue = [&](int st) {  // warp 0 only
-    const int slot = st % kStages;
-    const int t0 = p_begin + st * kT;
-    const int valid = min(kT, p_end - t0);
-    if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], (unsigned)(valid * D * 4 * 2));
-    __syncwarp();
-    if (lane < valid) {
-      const size_t off = (size_t)(t0 + lane) * row_stride;
-      bulk_g2s(&sm.k[slot][lane * D], kbase + off, D * 4, &sm.full[slot]);
-      bulk_g2s(&sm.v[slot][lane * D], vbase + off, D * 4, &sm.full[slot]);
-    }
-  };
-  if (warp == 0)
-    for (int st = 0; st < kStages && st < n_st; ++st) issue(st);
 
   float m_run[GS], l_run[GS];
   float acc[GS][VP];
@@ -139,77 +120,100 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeArgs
     for (int e = 0; e < VP; ++e) acc[h][e] = 0.f;
   }
 
-  for (int st = 0; st < n_st; ++st) {
-    const int slot = st % kStages;
-    mbar_wait_bounded(&sm.full[slot], (st / kStages) & 1, a.status);
-    const int t0 = p_begin + st * kT;
-    const int valid = min(kT, p_end - t0);
-    const float* ks = sm.k[slot];
-    const float* vs = sm.v[slot];
-    const int wp0 = warp * kPpw;  // this warp's first position in the stage
-
-    // Scores of the warp's 8 positions, two groups of four.
-    float sc[2][GS];
+  if (warp == kCWarps) {
+    // ---------------- producer: one K row and one V row per lane per stage
+    const size_t row_stride = (size_t)a.G * D;
+    const float* kbase = a.k_cache + (size_t)g * D;
+    const float* vbase = a.v_cache + (size_t)g * D;
+    for (int st = 0; st < n_st; ++st) {
+      const int slot = st % kStages;
+      if (st >= kStages) mbar_wait_bounded(&sm.empty[slot], ((st / kStages) - 1) & 1, a.status);
+      const int t0 = p_begin + st * kT;
+      const int valid = min(kT, p_end - t0);
+      if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], (unsigned)(valid * D * 4 * 2));
+      __syncwarp();
+      if (lane < valid) {
+        const size_t off = (size_t)(t0 + lane) * row_stride;
+        bulk_g2s(&sm.k[slot][lane * D], kbase + off, D * 4, &sm.full[slot]);
+        bulk_g2s(&sm.v[slot][lane * D], vbase + off, D * 4, &sm.full[slot]);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ---------------- consumers
+    const int qp = lane >> 3, qc = lane & 7;
+    float4 qr[GS][U];
 #pragma unroll
-    for (int grp = 0; grp < 2; ++grp) {
-      const int pos = wp0 + 4 * grp + qp;
-      float part[GS];
-#pragma unroll
-      for (int h = 0; h < GS; ++h) part[h] = 0.f;
+    for (int h = 0; h < GS; ++h)
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const float4 kv = *reinterpret_cast<const float4*>(&ks[pos * D + 4 * qc + 32 * u]);
+        float4 x = *reinterpret_cast<const float4*>(a.q + (size_t)(g * GS + h) * D + 4 * qc + 32 * u);
+        qr[h][u] = make_float4(x.x * sl2, x.y * sl2, x.z * sl2, x.w * sl2);
+      }
+    const int pos = 4 * warp + qp;  // this lane's position within a stage
+    for (int st = 0; st < n_st; ++st) {
+      const int slot = st % kStages;
+      mbar_wait_bounded(&sm.full[slot], (st / kStages) & 1, a.status);
+      const int valid = min(kT, p_end - (p_begin + st * kT));
+      const float* ks = sm.k[slot];
+      const float* vs = sm.v[slot];
+
+      float sc[GS];
+      {
+        float part[GS];
+#pragma unroll
+        for (int h = 0; h < GS; ++h) part[h] = 0.f;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float4 kv = *reinterpret_cast<const float4*>(&ks[pos * D + 4 * qc + 32 * u]);
+#pragma unroll
+          for (int h = 0; h < GS; ++h) {
+            part[h] = fmaf(qr[h][u].x, kv.x, part[h]);
+            part[h] = fmaf(qr[h][u].y, kv.y, part[h]);
+            part[h] = fmaf(qr[h][u].z, kv.z, part[h]);
+            part[h] = fmaf(qr[h][u].w, kv.w, part[h]);
+          }
+        }
 #pragma unroll
         for (int h = 0; h < GS; ++h) {
-          part[h] = fmaf(qr[h][u].x, kv.x, part[h]);
-          part[h] = fmaf(qr[h][u].y, kv.y, part[h]);
-          part[h] = fmaf(qr[h][u].z, kv.z, part[h]);
-          part[h] = fmaf(qr[h][u].w, kv.w, part[h]);
+          float x = part[h];
+          x += __shfl_xor_sync(0xffffffffu, x, 1);
+          x += __shfl_xor_sync(0xffffffffu, x, 2);
+          x += __shfl_xor_sync(0xffffffffu, x, 4);
+          sc[h] = (pos < valid) ? x : -INFINITY;
         }
       }
+
+      // Online softmax over the warp's 4 positions, per head.
+      float w[GS];
 #pragma unroll
       for (int h = 0; h < GS; ++h) {
-        float x = part[h];
-        x += __shfl_xor_sync(0xffffffffu, x, 1);
-        x += __shfl_xor_sync(0xffffffffu, x, 2);
-        x += __shfl_xor_sync(0xffffffffu, x, 4);
-        sc[grp][h] = (pos < valid) ? x : -INFINITY;
+        float mx = sc[h];
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float m_new = fmaxf(m_run[h], mx);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float corr = ex2(m_run[h] - m_use);
+        w[h] = ex2(sc[h] - m_use);
+        float sum = w[h];
+        sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+        l_run[h] = l_run[h] * corr + sum;
+        m_run[h] = m_new;
+#pragma unroll
+        for (int e = 0; e < VP; ++e) acc[h][e] *= corr;
       }
-    }
 
-    // Online softmax over the 8 positions (per head).
-    float w[2][GS];
-#pragma unroll
-    for (int h = 0; h < GS; ++h) {
-      float mx = fmaxf(sc[0][h], sc[1][h]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const float m_new = fmaxf(m_run[h], mx);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float corr = ex2(m_run[h] - m_use);
-      w[0][h] = ex2(sc[0][h] - m_use);
-      w[1][h] = ex2(sc[1][h] - m_use);
-      float sum = w[0][h] + w[1][h];
-      sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-      l_run[h] = l_run[h] * corr + sum;
-      m_run[h] = m_new;
-#pragma unroll
-      for (int e = 0; e < VP; ++e) acc[h][e] *= corr;
-    }
-
-    // acc += w * V for the warp's 8 positions; lane owns dims VP*lane ..
-#pragma unroll
-    for (int grp = 0; grp < 2; ++grp)
+      // acc += w * V over the warp's 4 positions; lane owns dims VP*lane ..
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) {
-        const int pos = wp0 + 4 * grp + pp;
+        const int ppos = 4 * warp + pp;
         float wb[GS];
 #pragma unroll
-        for (int h = 0; h < GS; ++h) wb[h] = __shfl_sync(0xffffffffu, w[grp][h], 8 * pp);
-        if (pos < valid) {
+        for (int h = 0; h < GS; ++h) wb[h] = __shfl_sync(0xffffffffu, w[h], 8 * pp);
+        if (ppos < valid) {
           if constexpr (VP == 4) {
-            const float4 vv = *reinterpret_cast<const float4*>(&vs[pos * D + 4 * lane]);
+            const float4 vv = *reinterpret_cast<const float4*>(&vs[ppos * D + 4 * lane]);
 #pragma unroll
             for (int h = 0; h < GS; ++h) {
               acc[h][0] = fmaf(wb[h], vv.x, acc[h][0]);
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeArgs
               acc[h][3] = fmaf(wb[h], vv.w, acc[h][3]);
             }
           } else {
-            const float2 vv = *reinterpret_cast<const float2*>(&vs[pos * D + 2 * lane]);
+            const float2 vv = *reinterpret_cast<const float2*>(&vs[ppos * D + 2 * lane]);
 #pragma unroll
             for (int h = 0; h < GS; ++h) {
               acc[h][0] = fmaf(wb[h], vv.x, acc[h][0]);
@@ -227,32 +231,33 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeArgs
           }
         }
       }
-
-    __syncthreads();  // every warp is done with this slot
-    if (warp == 0 && st + kStages < n_st) issue(st + kStages);
-  }
-
-  // Merge the 4 warps' states, write this split's partial.
-#pragma unroll
-  for (int h = 0; h < GS; ++h) {
-    if (lane == 0) {
-      sm.red_m[warp][h] = m_run[h];
-      sm.red_l[warp][h] = l_run[h];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
+
 #pragma unroll
-    for (int e = 0; e < VP; ++e) sm.red_o[warp][h][VP * lane + e] = acc[h][e];
+    for (int h = 0; h < GS; ++h) {
+      if (lane == 0) {
+        sm.red_m[warp][h] = m_run[h];
+        sm.red_l[warp][h] = l_run[h];
+      }
+#pragma unroll
+      for (int e = 0; e < VP; ++e) sm.red_o[warp][h][VP * lane + e] = acc[h][e];
+    }
   }
   __syncthreads();
+
+  // Merge the consumer warps' states into this split's partial.
   const WsLayout ws = ws_layout(a.workspace, a.H, a.G, D, S);
   for (int idx = tid; idx < GS * D; idx += kThreads) {
     const int h = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w2 = 0; w2 < kWarps; ++w2) M = fmaxf(M, sm.red_m[w2][h]);
+    for (int w2 = 0; w2 < kCWarps; ++w2) M = fmaxf(M, sm.red_m[w2][h]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
     float L = 0.f, O = 0.f;
 #pragma unroll
-    for (int w2 = 0; w2 < kWarps; ++w2) {
+    for (int w2 = 0; w2 < kCWarps; ++w2) {
       const float f = ex2(sm.red_m[w2][h] - Mu);
       L += sm.red_l[w2][h] * f;
       O += sm.red_o[w2][h][d] * f;
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeArgs
     }
   }
 
-  // Last split of this kv head merges every split.
+  // The last split of this kv head to finish merges all of them.
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -275,19 +280,49 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeArgs
   __syncthreads();
   if (!sm.is_last) return;
   __threadfence();
-  for (int idx = tid; idx < GS * D; idx += kThreads) {
-    const int h = idx / D, d = idx % D;
-    const size_t hb = (size_t)(g * GS + h) * S;
+
+  // 1) (m, l) of every split into shared memory (the stage buffers are free).
+  float* fm = &sm.k[0][0];                 // [GS][s_eff] maxima, then weights
+  float* fl = &sm.v[0][0];                 // [GS][s_eff] sums
+  for (int i = tid; i < GS * s_eff; i += kThreads) {
+    const int h = i / s_eff, s = i % s_eff;
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(&ws.ml[((size_t)(g * GS + h) * S + s) * 2]));
+    fm[i] = ml.x;
+    fl[i] = ml.y;
+  }
+  __syncthreads();
+  // 2) per head: M = max m_s, L = sum l_s 2^(m_s - M); weights 2^(m_s - M) / L.
+  for (int h = warp; h < GS; h += kCWarps + 1) {
     float M = -INFINITY;
-    for (int s = 0; s < s_eff; ++s) M = fmaxf(M, __ldcg(&ws.ml[(hb + s) * 2]));
+    for (int s = lane; s < s_eff; s += 32) M = fmaxf(M, fm[h * s_eff + s]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f, O = 0.f;
+    float L = 0.f;
+    for (int s = lane; s < s_eff; s += 32) L += fl[h * s_eff + s] * ex2(fm[h * s_eff + s] - Mu);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    const float invL = (L == 0.f) ? 0.f : 1.f / L;
+    __syncwarp();
+    for (int s = lane; s < s_eff; s += 32) fm[h * s_eff + s] = ex2(fm[h * s_eff + s] - Mu) * invL;
+  }
+  __syncthreads();
+  // 3) out = sum_s weight_s * o_s, one float4 of one head per thread.
+  for (int idx = tid; idx < GS * (D / 4); idx += kThreads) {
+    const int h = idx / (D / 4), c = idx % (D / 4);
+    const float* op = ws.o + (size_t)(g * GS + h) * S * D + 4 * c;
+    const float* wt = fm + h * s_eff;
+    float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
     for (int s = 0; s < s_eff; ++s) {
-      const float f = ex2(__ldcg(&ws.ml[(hb + s) * 2]) - Mu);
-      L += __ldcg(&ws.ml[(hb + s) * 2 + 1]) * f;
-      O += __ldcg(&ws.o[(hb + s) * D + d]) * f;
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(op + (size_t)s * D));
+      const float wv = wt[s];
+      o4.x = fmaf(wv, x.x, o4.x);
+      o4.y = fmaf(wv, x.y, o4.y);
+      o4.z = fmaf(wv, x.z, o4.z);
+      o4.w = fmaf(wv, x.w, o4.w);
     }
-    a.out[(size_t)(g * GS + h) * D + d] = (L == 0.f) ? 0.f : O / L;
+    *reinterpret_cast<float4*>(a.out + (size_t)(g * GS + h) * D + 4 * c) = o4;
   }
   if (tid == 0) ws.tickets[g] = 0u;
 }
@@ -314,9 +349,9 @@ bool decode_split_supported(int H, int G, int D) {
 }
 
 int decode_splits(int G, int max_seq, int sm_count) {
-  const int target = (2 * sm_count + G - 1) / G;
+  const int target = (kCtasPerSm * sm_count + G - 1) / G;
   const int by_len = (max_seq + kMinChunk - 1) / kMinChunk;
-  return max(1, min(target, by_len));
+  return max(1, min(min(target, by_len), kMaxSplits));
 }
 
 size_t decode_workspace_bytes(int H, int G, int D, int max_seq, int sm_count) {
