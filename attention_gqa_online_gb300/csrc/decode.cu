@@ -30,19 +30,20 @@
 namespace attn {
 namespace {
 
-constexpr int kT = 16;                    // positions per stage
-constexpr int kStages = 4;                // stages in flight
+constexpr int kT = 32;                    // positions per stage
+constexpr int kStages = 3;                // stages in flight
 constexpr int kCWarps = 4;                // consumer warps
 constexpr int kThreads = 32 * (kCWarps + 1);  // + one producer warp
-constexpr int kCtasPerSm = 3;
+constexpr int kCtasPerSm = 2;
 constexpr int kMinChunk = 64;             // fewest positions a split is given
-// Most splits per kv head: the final merge keeps GS * splits floats twice in
-// the (then idle) stage buffers, at least kStages * kT * 64 floats per array.
-constexpr int kMaxSplits = 448;
-static_assert(8 * kMaxSplits <= kStages * kT * 64, "merge scratch too small");
+constexpr int kMaxSplits = 1024;          // most splits per kv head
+constexpr int kMergeBatch = 16;           // splits merged per batch of loads
+constexpr int kPpw = kT / kCWarps;        // positions per consumer warp per stage
+constexpr int kNg = kPpw / 4;             // groups of four positions per warp
+static_assert(kPpw % 4 == 0, "each consumer warp takes whole groups of four positions");
 
 template <int D, int GS>
-struct DecodeSmem {
+struct __align__(128) DecodeSmem {
   float k[kStages][kT * D];
   float v[kStages][kT * D];
   float red_m[kCWarps][GS];
@@ -78,7 +79,8 @@ __host__ __device__ inline WsLayout ws_layout(void* ws, int H, int G, int D, int
 // 8-lane phase of a 16-byte shared load reads one contiguous row.
 template <int D, int GS>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    decode_split_kernel(const DecodeArgs a, const int S, const float sl2) {
+    decode_split_kernel(const DecodeArgs a, const int S, const float sl2, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v) {
   using Smem = DecodeSmem<D, GS>;
   constexpr int U = D / 32;   // float4 groups per lane in the score phase
   constexpr int VP = D / 32;  // output dims per lane in the PV phase
@@ -93,14 +95,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     record_status(a.status, ATTN_ERR_INVALID_ARG);
   const long long n_ll = (long long)kp + 1 < (long long)a.max_seq ? (long long)kp + 1 : (long long)a.max_seq;
   const int n = (int)n_ll;
-  const int s_eff = min(S, (n + kMinChunk - 1) / kMinChunk);
+  // Splits start on stage boundaries, so no stage is read by two CTAs.
+  const int s0 = min(S, (n + kMinChunk - 1) / kMinChunk);
+  const int chunk = ((n + s0 - 1) / s0 + kT - 1) / kT * kT;
+  const int s_eff = (n + chunk - 1) / chunk;
   if (j >= s_eff) return;
-  const int chunk = (n + s_eff - 1) / s_eff;
   const int p_begin = min(n, j * chunk);
   const int p_end = min(n, p_begin + chunk);
   const int len = p_end - p_begin;
   const int n_st = (len + kT - 1) / kT;
 
+  if (tid == 32 * kCWarps) {
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -121,24 +129,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
 
   if (warp == kCWarps) {
-    // ---------------- producer: one K row and one V row per lane per stage
-    const size_t row_stride = (size_t)a.G * D;
-    const float* kbase = a.k_cache + (size_t)g * D;
-    const float* vbase = a.v_cache + (size_t)g * D;
-    for (int st = 0; st < n_st; ++st) {
-      const int slot = st % kStages;
-      if (st >= kStages) mbar_wait_bounded(&sm.empty[slot], ((st / kStages) - 1) & 1, a.status);
-      const int t0 = p_begin + st * kT;
-      const int valid = min(kT, p_end - t0);
-      if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], (unsigned)(valid * D * 4 * 2));
-      __syncwarp();
-      if (lane < valid) {
-        const size_t off = (size_t)(t0 + lane) * row_stride;
-        bulk_g2s(&sm.k[slot][lane * D], kbase + off, D * 4, &sm.full[slot]);
-        bulk_g2s(&sm.v[slot][lane * D], vbase + off, D * 4, &sm.full[slot]);
+    // ---------------- producer: one [kT x D] tile of K and of V per stage
+    if (lane == 0) {
+      for (int st = 0; st < n_st; ++st) {
+        const int slot = st % kStages;
+        if (st >= kStages) mbar_wait_bounded(&sm.empty[slot], ((st / kStages) - 1) & 1, a.status);
+        const int t0 = p_begin + st * kT;
+        mbar_arrive_expect_tx(&sm.full[slot], (unsigned)(kT * D * 4 * 2));
+        tma_load_2d(&sm.k[slot][0], &tm_k, g * D, t0, &sm.full[slot]);
+        tma_load_2d(&sm.v[slot][0], &tm_v, g * D, t0, &sm.full[slot]);
       }
-      __syncwarp();
     }
+    __syncwarp();
   } else {
     // ---------------- consumers
     const int qp = lane >> 3, qc = lane & 7;
@@ -150,7 +152,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         float4 x = *reinterpret_cast<const float4*>(a.q + (size_t)(g * GS + h) * D + 4 * qc + 32 * u);
         qr[h][u] = make_float4(x.x * sl2, x.y * sl2, x.z * sl2, x.w * sl2);
       }
-    const int pos = 4 * warp + qp;  // this lane's position within a stage
     for (int st = 0; st < n_st; ++st) {
       const int slot = st % kStages;
       mbar_wait_bounded(&sm.full[slot], (st / kStages) & 1, a.status);
@@ -158,8 +159,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const float* ks = sm.k[slot];
       const float* vs = sm.v[slot];
 
-      float sc[GS];
-      {
+      // Scores of this warp's kNg groups of four positions.
+      float sc[kNg][GS];
+#pragma unroll
+      for (int grp = 0; grp < kNg; ++grp) {
+        const int pos = kPpw * warp + 4 * grp + qp;
         float part[GS];
 #pragma unroll
         for (int h = 0; h < GS; ++h) part[h] = 0.f;
@@ -180,22 +184,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           x += __shfl_xor_sync(0xffffffffu, x, 1);
           x += __shfl_xor_sync(0xffffffffu, x, 2);
           x += __shfl_xor_sync(0xffffffffu, x, 4);
-          sc[h] = (pos < valid) ? x : -INFINITY;
+          sc[grp][h] = (pos < valid) ? x : -INFINITY;
         }
       }
 
-      // Online softmax over the warp's 4 positions, per head.
-      float w[GS];
+      // Online softmax over the warp's kPpw positions, per head.
+      float w[kNg][GS];
 #pragma unroll
       for (int h = 0; h < GS; ++h) {
-        float mx = sc[h];
+        float mx = sc[0][h];
+#pragma unroll
+        for (int grp = 1; grp < kNg; ++grp) mx = fmaxf(mx, sc[grp][h]);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float m_new = fmaxf(m_run[h], mx);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float corr = ex2(m_run[h] - m_use);
-        w[h] = ex2(sc[h] - m_use);
-        float sum = w[h];
+        float sum = 0.f;
+#pragma unroll
+        for (int grp = 0; grp < kNg; ++grp) {
+          w[grp][h] = ex2(sc[grp][h] - m_use);
+          sum += w[grp][h];
+        }
         sum += __shfl_xor_sync(0xffffffffu, sum, 8);
         sum += __shfl_xor_sync(0xffffffffu, sum, 16);
         l_run[h] = l_run[h] * corr + sum;
@@ -204,33 +214,35 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int e = 0; e < VP; ++e) acc[h][e] *= corr;
       }
 
-      // acc += w * V over the warp's 4 positions; lane owns dims VP*lane ..
+      // acc += w * V over the warp's positions; lane owns dims VP*lane ..
 #pragma unroll
-      for (int pp = 0; pp < 4; ++pp) {
-        const int ppos = 4 * warp + pp;
-        float wb[GS];
+      for (int grp = 0; grp < kNg; ++grp)
 #pragma unroll
-        for (int h = 0; h < GS; ++h) wb[h] = __shfl_sync(0xffffffffu, w[h], 8 * pp);
-        if (ppos < valid) {
-          if constexpr (VP == 4) {
-            const float4 vv = *reinterpret_cast<const float4*>(&vs[ppos * D + 4 * lane]);
+        for (int pp = 0; pp < 4; ++pp) {
+          const int ppos = kPpw * warp + 4 * grp + pp;
+          float wb[GS];
 #pragma unroll
-            for (int h = 0; h < GS; ++h) {
-              acc[h][0] = fmaf(wb[h], vv.x, acc[h][0]);
-              acc[h][1] = fmaf(wb[h], vv.y, acc[h][1]);
-              acc[h][2] = fmaf(wb[h], vv.z, acc[h][2]);
-              acc[h][3] = fmaf(wb[h], vv.w, acc[h][3]);
-            }
-          } else {
-            const float2 vv = *reinterpret_cast<const float2*>(&vs[ppos * D + 2 * lane]);
+          for (int h = 0; h < GS; ++h) wb[h] = __shfl_sync(0xffffffffu, w[grp][h], 8 * pp);
+          if (ppos < valid) {
+            if constexpr (VP == 4) {
+              const float4 vv = *reinterpret_cast<const float4*>(&vs[ppos * D + 4 * lane]);
 #pragma unroll
-            for (int h = 0; h < GS; ++h) {
-              acc[h][0] = fmaf(wb[h], vv.x, acc[h][0]);
-              acc[h][1] = fmaf(wb[h], vv.y, acc[h][1]);
+              for (int h = 0; h < GS; ++h) {
+                acc[h][0] = fmaf(wb[h], vv.x, acc[h][0]);
+                acc[h][1] = fmaf(wb[h], vv.y, acc[h][1]);
+                acc[h][2] = fmaf(wb[h], vv.z, acc[h][2]);
+                acc[h][3] = fmaf(wb[h], vv.w, acc[h][3]);
+              }
+            } else {
+              const float2 vv = *reinterpret_cast<const float2*>(&vs[ppos * D + 2 * lane]);
+#pragma unroll
+              for (int h = 0; h < GS; ++h) {
+                acc[h][0] = fmaf(wb[h], vv.x, acc[h][0]);
+                acc[h][1] = fmaf(wb[h], vv.y, acc[h][1]);
+              }
             }
           }
         }
-      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
@@ -281,48 +293,53 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (!sm.is_last) return;
   __threadfence();
 
-  // 1) (m, l) of every split into shared memory (the stage buffers are free).
-  float* fm = &sm.k[0][0];                 // [GS][s_eff] maxima, then weights
-  float* fl = &sm.v[0][0];                 // [GS][s_eff] sums
-  for (int i = tid; i < GS * s_eff; i += kThreads) {
-    const int h = i / s_eff, s = i % s_eff;
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(&ws.ml[((size_t)(g * GS + h) * S + s) * 2]));
-    fm[i] = ml.x;
-    fl[i] = ml.y;
-  }
-  __syncthreads();
-  // 2) per head: M = max m_s, L = sum l_s 2^(m_s - M); weights 2^(m_s - M) / L.
-  for (int h = warp; h < GS; h += kCWarps + 1) {
-    float M = -INFINITY;
-    for (int s = lane; s < s_eff; s += 32) M = fmaxf(M, fm[h * s_eff + s]);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f;
-    for (int s = lane; s < s_eff; s += 32) L += fl[h * s_eff + s] * ex2(fm[h * s_eff + s] - Mu);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    const float invL = (L == 0.f) ? 0.f : 1.f / L;
-    __syncwarp();
-    for (int s = lane; s < s_eff; s += 32) fm[h * s_eff + s] = ex2(fm[h * s_eff + s] - Mu) * invL;
-  }
-  __syncthreads();
-  // 3) out = sum_s weight_s * o_s, one float4 of one head per thread.
+  // One pass over the splits with the same online rule (running max,
+  // correction, sum), 16 splits' loads in flight at a time; one float4 of
+  // one head per thread.
   for (int idx = tid; idx < GS * (D / 4); idx += kThreads) {
     const int h = idx / (D / 4), c = idx % (D / 4);
-    const float* op = ws.o + (size_t)(g * GS + h) * S * D + 4 * c;
-    const float* wt = fm + h * s_eff;
-    float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int s = 0; s < s_eff; ++s) {
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(op + (size_t)s * D));
-      const float wv = wt[s];
-      o4.x = fmaf(wv, x.x, o4.x);
-      o4.y = fmaf(wv, x.y, o4.y);
-      o4.z = fmaf(wv, x.z, o4.z);
-      o4.w = fmaf(wv, x.w, o4.w);
+    const size_t hb = (size_t)(g * GS + h) * S;
+    const float* op = ws.o + hb * D + 4 * c;
+    const float2* mlp = reinterpret_cast<const float2*>(ws.ml + hb * 2);
+    float M = -INFINITY, L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < s_eff; s0 += kMergeBatch) {
+      float2 ml[kMergeBatch];
+      float4 ov[kMergeBatch];
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        if (s0 + u < s_eff) {
+          ml[u] = __ldcg(mlp + s0 + u);
+          ov[u] = __ldcg(reinterpret_cast<const float4*>(op + (size_t)(s0 + u) * D));
+        } else {
+          ml[u] = make_float2(-INFINITY, 0.f);
+          ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float m_new = M;
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) m_new = fmaxf(m_new, ml[u].x);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float corr = ex2(M - m_use);
+      L *= corr;
+      O.x *= corr;
+      O.y *= corr;
+      O.z *= corr;
+      O.w *= corr;
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const float f = ex2(ml[u].x - m_use);
+        L = fmaf(ml[u].y, f, L);
+        O.x = fmaf(ov[u].x, f, O.x);
+        O.y = fmaf(ov[u].y, f, O.y);
+        O.z = fmaf(ov[u].z, f, O.z);
+        O.w = fmaf(ov[u].w, f, O.w);
+      }
+      M = m_new;
     }
-    *reinterpret_cast<float4*>(a.out + (size_t)(g * GS + h) * D + 4 * c) = o4;
+    const float inv = (L == 0.f) ? 0.f : 1.f / L;
+    *reinterpret_cast<float4*>(a.out + (size_t)(g * GS + h) * D + 4 * c) =
+        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
   }
   if (tid == 0) ws.tickets[g] = 0u;
 }
@@ -331,10 +348,18 @@ template <int D, int GS>
 int launch_t(const DecodeArgs& a, int S, cudaStream_t s) {
   const size_t smem = sizeof(DecodeSmem<D, GS>);
   auto kern = decode_split_kernel<D, GS>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return ATTN_ERR_CUDA;
+  if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
+  // K and V caches as 2-D tensors [max_seq rows][G*D floats]; one request
+  // copies kT rows of one kv head's D columns.
+  CUtensorMap tm_k, tm_v;
+  const uint64_t dims[2] = {(uint64_t)a.G * D, (uint64_t)a.max_seq};
+  const uint64_t strides[1] = {(uint64_t)a.G * D * 4};
+  const uint32_t box[2] = {(uint32_t)D, (uint32_t)kT};
+  if (!make_tmap(&tm_k, a.k_cache, 2, dims, strides, box, false, false) ||
+      !make_tmap(&tm_v, a.v_cache, 2, dims, strides, box, false, false))
+    return ATTN_ERR_UNSUPPORTED;
   const float sl2 = (1.0f / sqrtf((float)D)) * kLog2e;
-  kern<<<dim3(S, a.G), kThreads, smem, s>>>(a, S, sl2);
+  kern<<<dim3(S, a.G), kThreads, smem, s>>>(a, S, sl2, tm_k, tm_v);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : ATTN_ERR_CUDA;
 }
 

@@ -293,8 +293,7 @@ int launch_one(const FlashArgs& a, cudaStream_t s) {
   if (nb > 0x7fffffffLL || a.G > 65535) return ATTN_ERR_UNSUPPORTED;
   const size_t smem = sizeof(SimtSmem<DMAX>);
   auto kern = flash_simt_kernel<DMAX, VEC>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return ATTN_ERR_CUDA;
+  if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
   kern<<<dim3((unsigned)nb, (unsigned)a.G), NT, smem, s>>>(a);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : ATTN_ERR_CUDA;
 }

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace attn {
@@ -34,6 +35,17 @@ struct FlashArgs {
   const uint32_t* kv_pos_dev;
   unsigned* status;           // device status word
 };
+
+// Raises a kernel's dynamic shared memory limit to `bytes` on the current
+// device; the attribute is set once per (kernel, device).
+bool set_smem_limit(const void* kernel, size_t bytes);
+
+// Encodes a tiled TMA tensor map.  dims[0] is the innermost (contiguous)
+// extent in elements; strides_bytes has rank-1 entries (dims 1..rank-1);
+// box is the tile copied per request.  fp32 or bf16 elements, no swizzle or
+// the 128-byte swizzle, out-of-bounds elements read as zero.
+bool make_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+               const uint32_t* box, bool bf16, bool swizzle128);
 
 // fp32 CUDA-core flash kernel; any 1 <= D <= 128.
 int launch_flash_simt(const FlashArgs& a, cudaStream_t s);

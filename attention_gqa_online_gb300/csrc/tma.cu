@@ -1,0 +1,67 @@
+// tma.cu -- host-side construction of TMA tensor maps (cuTensorMapEncodeTiled,
+// reached through the runtime's driver entry point so the library does not
+// link libcuda directly).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace attn {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+
+void resolve() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+}  // namespace
+
+bool make_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+               const uint32_t* box, bool bf16, bool swizzle128) {
+  std::call_once(g_once, resolve);
+  if (g_encode == nullptr || rank < 1 || rank > 5) return false;
+  uint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                              (cuuint32_t)rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+struct SmemAttr {
+  const void* kernel;
+  int device;
+  size_t bytes;
+};
+constexpr int kAttrSlots = 256;
+SmemAttr g_attr[kAttrSlots];
+int g_attr_n = 0;
+std::mutex g_attr_mu;
+}  // namespace
+
+bool set_smem_limit(const void* kernel, size_t bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  {
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    for (int i = 0; i < g_attr_n; ++i)
+      if (g_attr[i].kernel == kernel && g_attr[i].device == dev && g_attr[i].bytes >= bytes) return true;
+  }
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+    return false;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  if (g_attr_n < kAttrSlots) g_attr[g_attr_n++] = SmemAttr{kernel, dev, bytes};
+  return true;
+}
+
+}  // namespace attn
