@@ -58,14 +58,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
 }
 
 // Waits for phase `parity` of `bar` to complete, for at most kWaitLimitNs.
-// Returns false (and records ATTN_ERR_TIMEOUT in *status) if the limit ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity, unsigned* status) {
+// Returns false (and records ATTN_ERR_TIMEOUT in *status) if the limit ran
+// out.  `abort_flag` (shared memory, optional) is set on a timeout; once it
+// is set, later waits of the same CTA give up at once, so a CTA whose
+// pipeline broke finishes quickly instead of timing out wait after wait.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity, unsigned* status,
+                                                  volatile int* abort_flag = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag != 0) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       record_status(status, ATTN_ERR_TIMEOUT);
+      if (abort_flag != nullptr) *abort_flag = 1;
       return false;
     }
   }

@@ -52,6 +52,7 @@ struct __align__(128) DecodeSmem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   int is_last;
+  int abort;
 };
 
 struct WsLayout {
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kCWarps);
     }
+    sm.abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -133,11 +135,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (lane == 0) {
       for (int st = 0; st < n_st; ++st) {
         const int slot = st % kStages;
-        if (st >= kStages) mbar_wait_bounded(&sm.empty[slot], ((st / kStages) - 1) & 1, a.status);
+        if (st >= kStages) mbar_wait_bounded(&sm.empty[slot], ((st / kStages) - 1) & 1, a.status, &sm.abort);
         const int t0 = p_begin + st * kT;
         mbar_arrive_expect_tx(&sm.full[slot], (unsigned)(kT * D * 4 * 2));
         tma_load_2d(&sm.k[slot][0], &tm_k, g * D, t0, &sm.full[slot]);
         tma_load_2d(&sm.v[slot][0], &tm_v, g * D, t0, &sm.full[slot]);
+      }
+      // No copy may still be landing when the CTA exits (normally all were
+      // consumed already, so these return at once).
+      for (int s = 0; s < kStages && s < n_st; ++s) {
+        const int last = s + ((n_st - 1 - s) / kStages) * kStages;
+        mbar_wait_bounded(&sm.full[s], (unsigned)((last / kStages) & 1), a.status);
       }
     }
     __syncwarp();
@@ -154,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     for (int st = 0; st < n_st; ++st) {
       const int slot = st % kStages;
-      mbar_wait_bounded(&sm.full[slot], (st / kStages) & 1, a.status);
+      mbar_wait_bounded(&sm.full[slot], (st / kStages) & 1, a.status, &sm.abort);
       const int valid = min(kT, p_end - (p_begin + st * kT));
       const float* ks = sm.k[slot];
       const float* vs = sm.v[slot];
@@ -355,8 +363,8 @@ int launch_t(const DecodeArgs& a, int S, cudaStream_t s) {
   const uint64_t dims[2] = {(uint64_t)a.G * D, (uint64_t)a.max_seq};
   const uint64_t strides[1] = {(uint64_t)a.G * D * 4};
   const uint32_t box[2] = {(uint32_t)D, (uint32_t)kT};
-  if (!make_tmap(&tm_k, a.k_cache, 2, dims, strides, box, false, false) ||
-      !make_tmap(&tm_v, a.v_cache, 2, dims, strides, box, false, false))
+  if (!make_tmap(&tm_k, a.k_cache, 2, dims, strides, box, false, kSwizzleNone) ||
+      !make_tmap(&tm_v, a.v_cache, 2, dims, strides, box, false, kSwizzleNone))
     return ATTN_ERR_UNSUPPORTED;
   const float sl2 = (1.0f / sqrtf((float)D)) * kLog2e;
   kern<<<dim3(S, a.G), kThreads, smem, s>>>(a, S, sl2, tm_k, tm_v);

@@ -42,10 +42,12 @@ bool set_smem_limit(const void* kernel, size_t bytes);
 
 // Encodes a tiled TMA tensor map.  dims[0] is the innermost (contiguous)
 // extent in elements; strides_bytes has rank-1 entries (dims 1..rank-1);
-// box is the tile copied per request.  fp32 or bf16 elements, no swizzle or
-// the 128-byte swizzle, out-of-bounds elements read as zero.
+// box is the tile copied per request.  fp32 or bf16 elements; out-of-bounds
+// elements read as zero.  Swizzle: none, 128-byte rows with 16-byte chunks
+// permuted, or 128-byte rows with 32-byte chunks permuted.
+enum { kSwizzleNone = 0, kSwizzle128 = 1, kSwizzle128Atom32 = 2 };
 bool make_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-               const uint32_t* box, bool bf16, bool swizzle128);
+               const uint32_t* box, bool bf16, int swizzle);
 
 // fp32 CUDA-core flash kernel; any 1 <= D <= 128.
 int launch_flash_simt(const FlashArgs& a, cudaStream_t s);

@@ -25,14 +25,16 @@ void resolve() {
 }  // namespace
 
 bool make_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-               const uint32_t* box, bool bf16, bool swizzle128) {
+               const uint32_t* box, bool bf16, int swizzle) {
   std::call_once(g_once, resolve);
   if (g_encode == nullptr || rank < 1 || rank > 5) return false;
   uint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                               (cuuint32_t)rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              swizzle == kSwizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                              : swizzle == kSwizzle128Atom32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B
+                                                             : CU_TENSOR_MAP_SWIZZLE_NONE,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -366,12 +366,18 @@ def run_ours(args, world, rank, local):
         dist.destroy_process_group()
 
 
+def tf32_peak(peaks):
+    """TF32 dense peak: the measured bf16 peak times the nominal TF32 / bf16 ratio (1.1 / 2.25)."""
+    return peaks["bf16_tflops"] * 1.1 / 2.25
+
+
 def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_src, clocks):
-    """Prefill and long causal forward on the fp32 CUDA-core path (TFLOP/s)."""
+    """Prefill and long causal forward in TFLOP/s: TF32 tensor-core path and fp32 CUDA-core path."""
     import torch
     res, launches = {}, 0
     sm_mhz = (clocks or {}).get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
     alu_peak = fp32_alu_peak_tflops(sm_mhz, sms)
+    tc_peak = tf32_peak(peaks)
     steps = max(3, min(args.steps, args.extra_steps))
 
     def timed(fn, n):
@@ -386,6 +392,15 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
         torch.cuda.synchronize()
         return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
+    def roof(prec, tf, kernel):
+        if prec == A.ATTN_TF32:
+            return {"bound": "tensor", "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
+                    "traffic": None, "kernel": kernel,
+                    "peak_source": "%s bf16 %.0f TFLOP/s x 1.1/2.25 (nominal TF32/bf16)" % (peak_src, peaks["bf16_tflops"])}
+        return {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
+                "traffic": None, "kernel": kernel,
+                "peak_source": "fp32 FMA: %d SMs x 128 lanes x 2 x %.0f MHz" % (sms, sm_mhz)}
+
     p = PREFILL
     qb, kc, vc = synthetic.prefill_inputs(p["n_queries"], p["stride"], p["max_seq"], p["G"] * p["D"], seed=0)
     per = (qb.numel() + kc.numel() + vc.numel()) * 4
@@ -393,25 +408,22 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
     bufs = [(qb.to(dev), kc.to(dev), vc.to(dev)) for _ in range(n_rot)]
     outp = torch.empty((p["n_queries"], p["stride"]), device=dev)
     scale = 1.0 / math.sqrt(p["D"])
-
-    def prefill_step(i):
-        qd, kd, vd = bufs[i % n_rot]
-        rc = lib.attn_prefill(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outp.data_ptr(), p["n_queries"], p["H"],
-                              p["G"], p["D"], p["G"] * p["D"], p["max_seq"], scale, p["start_pos"], p["stride"],
-                              p["stride"], 0, A.ATTN_FP32, sh)
-        if rc != 0:
-            raise RuntimeError("attn_prefill failed: %d" % rc)
-
-    ms = timed(prefill_step, steps)
-    launches += steps
-    tf = prefill_flops() / (ms * 1e-3) / 1e12
-    res["prefill"] = {"workload": "prefill 512 queries start_pos=1536 max_seq=2048 32/8 heads D=128 fp32",
-                      "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "prec": "fp32",
-                      "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s",
-                                   "frac": tf / alu_peak, "traffic": None,
-                                   "kernel": "flash_simt_kernel<128,true>",
-                                   "peak_source": "fp32 FMA: %d SMs x 128 lanes x 2 x %.0f MHz" % (sms, sm_mhz)},
-                      "l2": "rotating %d input sets" % n_rot}
+    for prec, key, kern in ((A.ATTN_TF32, "prefill", "flash_tc_kernel<128> (tf32)"),
+                            (A.ATTN_FP32, "prefill_fp32", "flash_simt_kernel<128,true>")):
+        def prefill_step(i, prec=prec):
+            qd, kd, vd = bufs[i % n_rot]
+            rc = lib.attn_prefill(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outp.data_ptr(), p["n_queries"],
+                                  p["H"], p["G"], p["D"], p["G"] * p["D"], p["max_seq"], scale, p["start_pos"],
+                                  p["stride"], p["stride"], 0, prec, sh)
+            if rc != 0:
+                raise RuntimeError("attn_prefill failed: %d" % rc)
+        ms = timed(prefill_step, steps)
+        launches += steps + args.warmup
+        tf = prefill_flops() / (ms * 1e-3) / 1e12
+        res[key] = {"workload": "prefill 512 queries start_pos=1536 max_seq=2048 32/8 heads D=128",
+                    "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
+                    "prec": "tf32" if prec == A.ATTN_TF32 else "fp32", "roofline": roof(prec, tf, kern),
+                    "l2": "rotating %d input sets" % n_rot}
     del bufs
 
     f = FORWARD
@@ -419,22 +431,19 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     outf = torch.empty_like(qd)
     lse = torch.empty((f["q_seq"], f["H"], 2), device=dev)
-
-    def fwd_step(i):
-        rc = lib.attn_forward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(), lse.data_ptr(),
-                              f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], A.ATTN_CAUSAL, A.ATTN_FP32, sh)
-        if rc != 0:
-            raise RuntimeError("attn_forward failed: %d" % rc)
-
-    ms = timed(fwd_step, steps)
-    launches += steps
-    tf = forward_flops() / (ms * 1e-3) / 1e12
-    res["forward"] = {"workload": "causal forward+LSE q_seq=8192 32/8 heads D=128 fp32", "value": tf,
-                      "unit": "TFLOP/s", "ms_per_step": ms, "prec": "fp32",
-                      "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s",
-                                   "frac": tf / alu_peak, "traffic": None,
-                                   "kernel": "flash_simt_kernel<128,true>"},
-                      "l2": "inputs 192 MiB > L2"}
+    for prec, key, kern in ((A.ATTN_TF32, "forward", "flash_tc_kernel<128> (tf32)"),
+                            (A.ATTN_FP32, "forward_fp32", "flash_simt_kernel<128,true>")):
+        def fwd_step(i, prec=prec):
+            rc = lib.attn_forward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(), lse.data_ptr(),
+                                  f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], A.ATTN_CAUSAL, prec, sh)
+            if rc != 0:
+                raise RuntimeError("attn_forward failed: %d" % rc)
+        ms = timed(fwd_step, steps)
+        launches += steps + args.warmup
+        tf = forward_flops() / (ms * 1e-3) / 1e12
+        res[key] = {"workload": "causal forward+LSE q_seq=8192 32/8 heads D=128, Q,K N(0,9)", "value": tf,
+                    "unit": "TFLOP/s", "ms_per_step": ms, "prec": "tf32" if prec == A.ATTN_TF32 else "fp32",
+                    "roofline": roof(prec, tf, kern), "l2": "inputs 192 MiB > L2"}
     res["_launches"] = launches
     return res
 

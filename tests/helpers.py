@@ -41,3 +41,9 @@ def assert_lse_close(got, ref, prec, smax=1.0, where=""):
     err = np.abs(got - ref)
     tol = 1e-4 if prec == FP32 else LSE_TOL[prec] * max(1.0, smax)
     assert err.max() <= tol, "%s: LSE max err %.3g > %.3g" % (where, err.max(), tol)
+
+
+def tc_supported(H, G, D):
+    """Shapes the tensor-core precisions accept (contiguous, aligned tensors)."""
+    gs = H // G
+    return D in (64, 128) and gs > 0 and (gs & (gs - 1)) == 0 and gs <= 128

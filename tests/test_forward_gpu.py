@@ -4,11 +4,11 @@ import pytest
 import torch
 
 from attention_gqa_online_gb300 import synthetic
-from helpers import FP32, assert_lse_close, assert_out_close, dev
+from helpers import FP32, TF32, assert_lse_close, assert_out_close, dev, tc_supported
 
 pytestmark = pytest.mark.gpu
 CAUSAL, FULL, CROSS = 0, 1, 2
-PRECS = [FP32]
+PRECS = [FP32, TF32]
 
 
 def run_forward(A, q, k, v, q_seq, kv_seq, H, G, D, mask, prec):
@@ -54,6 +54,12 @@ def test_small_config(cuda_lib, orc, prec, mask, kv):
     (200, 200, 1, 1, 128, CAUSAL),
 ])
 def test_shapes(cuda_lib, orc, prec, q_seq, kv_seq, H, G, D, mask):
+    if prec != FP32 and not tc_supported(H, G, D):
+        q, k, v = synthetic.forward_inputs(q_seq, kv_seq, H, G, D, seed=1)
+        with pytest.raises(cuda_lib.AttnError) as e:
+            run_forward(cuda_lib, q, k, v, q_seq, kv_seq, H, G, D, mask, prec)
+        assert e.value.code == cuda_lib.ATTN_ERR_UNSUPPORTED
+        return
     check(cuda_lib, orc, q_seq, kv_seq, H, G, D, mask, prec, seed=q_seq + D)
 
 

@@ -6,10 +6,10 @@ import pytest
 import torch
 
 from attention_gqa_online_gb300 import synthetic
-from helpers import FP32, assert_out_close, dev
+from helpers import FP32, TF32, assert_out_close, dev, tc_supported
 
 pytestmark = pytest.mark.gpu
-PRECS = [FP32]
+PRECS = [FP32, TF32]
 
 
 def check(A, orc, n_queries, H, G, D, kv_dim, max_seq, start_pos, q_stride, out_stride, q_base, prec, seed,
@@ -50,6 +50,8 @@ def test_prefill_config(cuda_lib, orc, prec):
 ])
 def test_prefill_shapes(cuda_lib, orc, prec, n_queries, H, G, D, kv_dim, max_seq, start_pos, q_stride,
                         out_stride, q_base):
+    if prec != FP32 and not tc_supported(H, G, D):
+        pytest.skip("tensor-core precisions need D in {64, 128} and a power-of-two group size")
     check(cuda_lib, orc, n_queries, H, G, D, kv_dim, max_seq, start_pos, q_stride, out_stride, q_base, prec,
           seed=n_queries)
 
