@@ -5,29 +5,38 @@
 // (cera attention_prefill.wgsl, fn attention_prefill: per-tile max,
 // correction, exponentials, running sum; meganeura attention.wgsl, fn main:
 // the final (max, log sum) store).  Both contractions run on the 5th-generation
-// tensor cores with TF32 operands and fp32 accumulation in tensor memory.
+// tensor cores with fp32 accumulation in tensor memory, with TF32 operands
+// (K/V tiles straight from the fp32 inputs) or bf16 operands (K/V converted
+// once per call by a small pre-pass; Q and P rounded on their way into TMEM).
 //
 // One CTA owns 128 packed rows of one kv head g: row r is (query i, head
 // g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs
 // query heads that share it.  Keys are walked in tiles of 128.
 //
-// Warp roles (256 threads):
+// Warp roles (384 threads):
 //   warp 0      TMA producer: K tile (128 keys x D, 128-byte swizzle, K-major
-//               operand) and V tile (same box, 32-byte-atom swizzle, MN-major
-//               operand) into a ring of 64 KB shared-memory slots.
+//               operand) and V tile (MN-major operand; TF32 needs the
+//               32-byte-atom swizzle, bf16 the plain 128-byte one) into a
+//               192 KB shared-memory ring: 3 tiles deep for TF32, 6 for bf16.
 //   warp 1      tensor-memory allocation; one thread issues every MMA:
 //                 S_b = Q K_j^T      (A = Q in TMEM, B = K tile)      M=128 N=128
 //                 O  += P_j V_j      (A = P in TMEM over S_b, B = V)  M=128 N=D
-//   warps 4-7   softmax: thread t owns row t (TMEM lane t).  Loads S, masks
-//               the row's window, takes the tile max, writes P = 2^(S - m)
-//               (rounded to TF32) back over S, keeps the row sum, rescales O
-//               when the reference max moves, and finally writes O / l and
-//               (max, log sum).
-// Tensor memory (512 columns): Q [0, D), S0 [128, 256), S1 [256, 384),
-// O [384, 384 + D).  Scores are in base-2 units: Q is pre-multiplied by
-// scale * log2(e).  The reference max only moves when a row's tile max
-// exceeds it by more than 8 (so P <= 256), which leaves the result exact and
-// skips most O rescales; the true max is tracked separately for the LSE.
+//               The issuer is greedy: it issues whichever of the next Q K^T
+//               and the next P V has its inputs ready.
+//   warps 4-11  softmax, two warpgroups: warp w of group c handles rows
+//               32(w%4)..+31 (TMEM lanes) and score columns 64c..64c+63.  The
+//               two halves of a row swap their tile max through shared
+//               memory; each group writes its half of P = 2^(S - m) back into
+//               the score buffer, keeps its half of the row sum, rescales its
+//               half of O when the reference max moves, and finally writes its
+//               half of O / l; group 0 writes (max, log sum).
+// Tensor memory (512 columns): Q [0, 128), two 128-column score buffers
+// [128, 384), O [384, 384 + D).  Scores are in base-2 units: Q is
+// pre-multiplied by scale * log2(e).  The reference max only moves when a
+// row's tile max exceeds it by more than 8 (so P <= 256), which leaves the
+// result exact and skips most O rescales; the true max is tracked separately
+// for the LSE.  Every wait is bounded; a CTA whose pipeline breaks drains its
+// copies and MMAs before it releases tensor memory.
 #include <cfloat>
 
 #include "common.cuh"
@@ -37,23 +46,27 @@
 namespace attn {
 namespace {
 
-constexpr int kRows = 128;       // packed rows per CTA (MMA M)
-constexpr int kKeys = 128;       // keys per tile (MMA N of Q K^T, K of P V)
-constexpr int kThreads = 256;
+constexpr int kRows = 128;        // packed rows per CTA (MMA M)
+constexpr int kKeys = 128;        // keys per tile (MMA N of Q K^T, K of P V)
+constexpr int kSBuf = 2;          // score buffers in tensor memory
+constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 256;
 constexpr int kRingBytes = 3 * 65536;  // K/V tile ring in shared memory
-constexpr int kMaxRing = 6;
-constexpr int kColQ = 0, kColS0 = 128, kColO = 384;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMaxRing = 12;
+constexpr int kColQ = 0, kColS0 = 128, kColO = 384;  // S buffer b at kColS0 + kKeys * b
+constexpr float kRescaleThreshold = 8.0f;             // log2 units
 
 struct __align__(1024) TcSmem {
   unsigned char ring[kRingBytes];
   uint64_t kv_full[kMaxRing];
   uint64_t kv_empty[kMaxRing];
-  uint64_t s_full[2];
-  uint64_t p_ready[2];
-  uint64_t pv_done[2];
+  uint64_t s_full[kSBuf];
+  uint64_t p_ready[kSBuf];
+  uint64_t pv_done[kSBuf];
   uint64_t q_ready;
   uint64_t drain;
+  float red_max[2][2][kRows];  // [tile parity][group][row] partial tile maxima
+  float red_l[2][kRows];       // [group][row] partial row sums (epilogue)
   uint32_t tmem_base;
   int abort;
 };
@@ -64,15 +77,27 @@ __device__ __forceinline__ uint32_t tf32_round(float x) {
   return r;
 }
 
-template <int D>
+// Two floats as round-to-nearest bf16 in one word: lo in bits 0-15.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// BF = false: TF32 operands (fp32 K/V tiles straight from the inputs).
+// BF = true: bf16 operands (K/V already converted to bf16; Q and P rounded to
+// bf16 on their way into tensor memory, two values per 32-bit column).
+template <int D, bool BF>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_tc_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v) {
-  constexpr int kChunks = D / 32;              // 32-float column chunks of a row
+  constexpr int kEpr = BF ? 64 : 32;           // elements per 128-byte row
+  constexpr int kChunks = D / kEpr;            // 128-byte column chunks of a K/V row
   constexpr int kChunkBytes = kKeys * 128;     // one TMA box: 128 keys x 128 bytes
   constexpr int kTileBytes = kChunks * kChunkBytes;
-  constexpr int kRing = kRingBytes / kTileBytes;          // tiles in flight: 3 (D=128) or 6 (D=64)
+  constexpr int kRing = kRingBytes / kTileBytes;  // tiles in flight
   static_assert(kRing <= kMaxRing, "ring barriers");
+  constexpr int kKStep = BF ? 16 : 8;          // MMA K per instruction (32 bytes)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
@@ -99,12 +124,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kSBuf; ++b) {
       mbar_init(&sm.s_full[b], 1);
-      mbar_init(&sm.p_ready[b], 4);
+      mbar_init(&sm.p_ready[b], 8);
       mbar_init(&sm.pv_done[b], 1);
     }
-    mbar_init(&sm.q_ready, 4);
+    mbar_init(&sm.q_ready, 8);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbar_init();
@@ -129,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* tm = (idx & 1) ? &tm_v : &tm_k;
         const int y = kKeys * (idx >> 1);
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + 32 * c, y, &sm.kv_full[s]);
+        for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + kEpr * c, y, &sm.kv_full[s]);
       }
       // No copy may still be landing in shared memory when the CTA exits
       // (normally every fill was already consumed, so these return at once).
@@ -141,44 +166,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nt > 0) {
-      constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtTF32, false, kRows, kKeys);
-      constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtTF32, true, kRows, D);
+      constexpr uint32_t kFmt = BF ? tc::kFmtBF16 : tc::kFmtTF32;
+      constexpr uint32_t idesc_qk = tc::idesc_f32acc(kFmt, false, kRows, kKeys);
+      constexpr uint32_t idesc_pv = tc::idesc_f32acc(kFmt, true, kRows, D);
+      // V (MN-major B): TF32 needs the 32-byte-atom layout with 4-row K groups;
+      // bf16 uses the plain 128-byte swizzle with 8-row groups.
+      constexpr uint32_t kVLayout = BF ? tc::kLayoutSw128 : tc::kLayoutSw128Atom32;
+      constexpr uint32_t kVSbo = BF ? 1024 : 512;
+      constexpr uint32_t kVStep = kKStep * 128;  // bytes of V rows per K step
       const uint32_t ring0 = smem_u32(sm.ring);
       mbar_wait_bounded(&sm.q_ready, 0, a.status, &sm.abort);
       tc::fence_after_sync();
       auto tile_addr = [&](int idx) { return ring0 + (uint32_t)((idx % kRing) * kTileBytes); };
-      auto full_wait = [&](int idx) {
-        mbar_wait_bounded(&sm.kv_full[idx % kRing], (unsigned)((idx / kRing) & 1), a.status, &sm.abort);
+      auto full_ready = [&](int idx) {
+        return mbar_test_wait(&sm.kv_full[idx % kRing], (unsigned)((idx / kRing) & 1));
       };
       auto release = [&](int idx) { tc::commit(&sm.kv_empty[idx % kRing]); };
-      for (int j = 0; j <= nt; ++j) {
-        if (j < nt) {
-          const int b = j & 1;
-          if (j >= 2) mbar_wait_bounded(&sm.pv_done[b], (unsigned)(((j - 2) >> 1) & 1), a.status, &sm.abort);
-          full_wait(2 * j);
+      int nq = 0, np = 0;  // next Q K^T and next P V to issue
+      unsigned long long t_idle = 0;
+      while (np < nt) {
+        // Q K^T for tile nq writes S buffer nq % kSBuf, last read by P V of tile nq - kSBuf.
+        const bool qk_ok =
+            nq < nt && nq < np + kSBuf &&
+            (nq < kSBuf || mbar_test_wait(&sm.pv_done[nq % kSBuf], (unsigned)(((nq - kSBuf) / kSBuf) & 1))) &&
+            full_ready(2 * nq);
+        const bool pv_ok = !qk_ok && nq > np &&
+                           mbar_test_wait(&sm.p_ready[np % kSBuf], (unsigned)((np / kSBuf) & 1)) &&
+                           full_ready(2 * np + 1);
+        if (qk_ok) {
+          const int b = nq % kSBuf;
           tc::fence_after_sync();
-          const uint32_t kb = tile_addr(2 * j);
+          const uint32_t kb = tile_addr(2 * nq);
 #pragma unroll
-          for (int kk = 0; kk < D / 8; ++kk) {
+          for (int kk = 0; kk < D / kKStep; ++kk) {
             const uint64_t bdesc = tc::sdesc_sw128(kb + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
-            tc::mma_tf32_ts(tmem + kColS0 + 128 * b, tmem + kColQ + 8 * kk, bdesc, idesc_qk, kk > 0);
+            if constexpr (BF)
+              tc::mma_f16_ts(tmem + kColS0 + kKeys * b, tmem + kColQ + 8 * kk, bdesc, idesc_qk, kk > 0);
+            else
+              tc::mma_tf32_ts(tmem + kColS0 + kKeys * b, tmem + kColQ + 8 * kk, bdesc, idesc_qk, kk > 0);
           }
           tc::commit(&sm.s_full[b]);
-          release(2 * j);
-        }
-        if (j >= 1) {
-          const int jj = j - 1, b = jj & 1;
-          mbar_wait_bounded(&sm.p_ready[b], (unsigned)((jj >> 1) & 1), a.status, &sm.abort);
-          full_wait(2 * jj + 1);
+          release(2 * nq);
+          ++nq;
+          t_idle = 0;
+        } else if (pv_ok) {
+          const int b = np % kSBuf;
           tc::fence_after_sync();
-          const uint32_t vb = tile_addr(2 * jj + 1);
+          const uint32_t vb = tile_addr(2 * np + 1);
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 8; ++kk) {
-            const uint64_t bdesc = tc::sdesc_sw128(vb + kk * 1024, kChunkBytes, 512, tc::kLayoutSw128Atom32);
-            tc::mma_tf32_ts(tmem + kColO, tmem + kColS0 + 128 * b + 8 * kk, bdesc, idesc_pv, (jj > 0 || kk > 0));
+          for (int kk = 0; kk < kKeys / kKStep; ++kk) {
+            const uint64_t bdesc = tc::sdesc_sw128(vb + kk * kVStep, kChunkBytes, kVSbo, kVLayout);
+            if constexpr (BF)
+              tc::mma_f16_ts(tmem + kColO, tmem + kColS0 + kKeys * b + 8 * kk, bdesc, idesc_pv, (np > 0 || kk > 0));
+            else
+              tc::mma_tf32_ts(tmem + kColO, tmem + kColS0 + kKeys * b + 8 * kk, bdesc, idesc_pv, (np > 0 || kk > 0));
           }
           tc::commit(&sm.pv_done[b]);
-          release(2 * jj + 1);
+          release(2 * np + 1);
+          ++np;
+          t_idle = 0;
+        } else {
+          const unsigned long long now = globaltimer_ns();
+          if (t_idle == 0) t_idle = now;
+          if (*reinterpret_cast<volatile int*>(&sm.abort) != 0) break;
+          if (now - t_idle > kWaitLimitNs) {
+            record_status(a.status, ATTN_ERR_TIMEOUT);
+            *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+            break;
+          }
         }
       }
       // Every MMA has finished before tensor memory is released.
@@ -187,8 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
-    const int r = tid - 128;                       // row == TMEM lane
-    const uint32_t lane_base = (uint32_t)(32 * (warp - 4)) << 16;
+    constexpr int kHalfD = D / 2;              // O columns per group
+    const int grp = (warp - 4) >> 2;           // column group 0 or 1
+    const int r = 32 * (warp & 3) + lane;      // row == TMEM lane
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const long long packed = (long long)blk * kRows + r;
     const long long qi = packed / gs;
     const int h = g * gs + (int)(packed % gs);
@@ -196,21 +253,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = qi < a.n_q;
     const float sl2 = a.scale * kLog2e;
 
-    // Q row -> TMEM (pre-scaled); rows past n_q are zero.
+    // Q row -> TMEM (pre-scaled); rows past n_q are zero.  TF32: one value per
+    // column; bf16: two per column (lower index in the low half).  Each group
+    // stores half the row, unless half is under one 32-column store (bf16,
+    // D = 64): then group 0 stores the whole row.
     {
-      const float* qrow = a.q + qi * a.q_row_stride + (long long)h * D;
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
+      constexpr int kPer = BF ? 2 : 1;
+      constexpr int kQAll = D / kPer;          // TMEM columns of a Q row
+      constexpr bool kSplitQ = kQAll >= 64;
+      constexpr int kQCols = kSplitQ ? kQAll / 2 : kQAll;
+      const int q_grp = kSplitQ ? grp : 0;
+      const int n_chunks = (kSplitQ || grp == 0) ? kQCols / 32 : 0;
+      const float* qrow = a.q + qi * a.q_row_stride + (long long)h * D + q_grp * kQCols * kPer;
+      for (int c = 0; c < n_chunks; ++c) {
         uint32_t v[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          float4 x = row_ok ? *reinterpret_cast<const float4*>(qrow + 32 * c + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[e] = __float_as_uint(x.x * sl2);
-          v[e + 1] = __float_as_uint(x.y * sl2);
-          v[e + 2] = __float_as_uint(x.z * sl2);
-          v[e + 3] = __float_as_uint(x.w * sl2);
+        for (int e = 0; e < 32; e += 4 / kPer) {
+          const float* src = qrow + kPer * (32 * c + e);
+          const float4 x = row_ok ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if constexpr (BF) {
+            v[e] = pack_bf16(x.x * sl2, x.y * sl2);
+            v[e + 1] = pack_bf16(x.z * sl2, x.w * sl2);
+          } else {
+            v[e] = __float_as_uint(x.x * sl2);
+            v[e + 1] = __float_as_uint(x.y * sl2);
+            v[e + 2] = __float_as_uint(x.z * sl2);
+            v[e + 3] = __float_as_uint(x.w * sl2);
+          }
         }
-        tc::tmem_st32(tmem + lane_base + kColQ + 32 * c, v);
+        tc::tmem_st32(tmem + lane_base + kColQ + q_grp * kQCols + 32 * c, v);
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();
@@ -218,30 +289,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm.q_ready);
     }
 
+    constexpr int kCols = kKeys / 2;           // score columns per group per tile
+    constexpr int kCC = kCols / 32;            // 32-column TMEM loads per group per tile
     float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
     for (int j = 0; j < nt; ++j) {
-      const int b = j & 1;
-      const uint32_t s_col = tmem + lane_base + kColS0 + 128 * b;
-      mbar_wait_bounded(&sm.s_full[b], (unsigned)((j >> 1) & 1), a.status, &sm.abort);
+      const int b = j % kSBuf;
+      const uint32_t s_col = tmem + lane_base + kColS0 + kKeys * b + kCols * grp;
+      mbar_wait_bounded(&sm.s_full[b], (unsigned)((j / kSBuf) & 1), a.status, &sm.abort);
       tc::fence_after_sync();
-      uint32_t s[4][32];
+      uint32_t s[kCC][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_col + 32 * c, s[c]);
+      for (int c = 0; c < kCC; ++c) tc::tmem_ld32(s_col + 32 * c, s[c]);
       tc::tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::reg_fence(s[c]);
+      for (int c = 0; c < kCC; ++c) tc::reg_fence(s[c]);
 
+      // Mask and this half's max (four independent chains).
       const bool masked = (j + 1) * kKeys > n_min;
-      float tmax = -INFINITY;
+      const int col0 = j * kKeys + kCols * grp;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < kCC; ++c)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           float x = __uint_as_float(s[c][e]);
-          if (masked && (j * kKeys + 32 * c + e) >= n_r) x = -INFINITY;
+          if (masked && (col0 + 32 * c + e) >= n_r) x = -INFINITY;
           s[c][e] = __float_as_uint(x);
-          tmax = fmaxf(tmax, x);
+          mx[e & 3] = fmaxf(mx[e & 3], x);
         }
+      sm.red_max[j & 1][grp][r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      named_barrier(1, kSoftmaxThreads);
+      const float tmax = fmaxf(sm.red_max[j & 1][0][r], sm.red_max[j & 1][1][r]);
       m_true = fmaxf(m_true, tmax);
       float corr = 1.f;
       if (tmax > m_ref + kRescaleThreshold) {  // also true for the first finite tile max
@@ -249,35 +327,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = tmax;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float sum = 0.f;
+      float sm4[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (BF) {
+        // P as bf16 pairs into the first half of this buffer's columns: this
+        // group's 64 values become 32 columns at offset 32 * grp.  Both groups
+        // finished reading S before the max exchange above.
+        uint32_t pk[32];
+        static_assert(kCC * 16 == 32, "one 32-column P store per group");
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kCC; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const uint32_t p = tf32_round(ex2(__uint_as_float(s[c][e]) - m_use));
-          sum += __uint_as_float(p);
-          s[c][e] = p;
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = ex2(__uint_as_float(s[c][e]) - m_use);
+            const float p1 = ex2(__uint_as_float(s[c][e + 1]) - m_use);
+            const uint32_t w = pack_bf16(p0, p1);
+            sm4[e & 3] += __uint_as_float(w << 16);
+            sm4[(e + 1) & 3] += __uint_as_float(w & 0xffff0000u);
+            pk[16 * c + e / 2] = w;
+          }
+        tc::tmem_st32(tmem + lane_base + kColS0 + kKeys * b + 32 * grp, pk);
+      } else {
+#pragma unroll
+        for (int c = 0; c < kCC; ++c) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const uint32_t p = tf32_round(ex2(__uint_as_float(s[c][e]) - m_use));
+            sm4[e & 3] += __uint_as_float(p);
+            s[c][e] = p;
+          }
+          tc::tmem_st32(s_col + 32 * c, s[c]);
         }
-        tc::tmem_st32(s_col + 32 * c, s[c]);
       }
-      l = l * corr + sum;
+      l = l * corr + ((sm4[0] + sm4[1]) + (sm4[2] + sm4[3]));
       tc::tmem_st_wait();
 
-      // O was accumulated against the old reference: rescale it (after the
-      // previous P V has landed) when any row of this warp moved its reference.
+      // O was accumulated against the old reference: rescale this group's half
+      // (after the previous P V has landed) when any row of the warp moved.
       if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-        const int pb = (j - 1) & 1;
-        mbar_wait_bounded(&sm.pv_done[pb], (unsigned)(((j - 1) >> 1) & 1), a.status, &sm.abort);
+        const int pb = (j - 1) % kSBuf;
+        mbar_wait_bounded(&sm.pv_done[pb], (unsigned)(((j - 1) / kSBuf) & 1), a.status, &sm.abort);
         tc::fence_after_sync();
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
+        for (int c = 0; c < kHalfD / 32; ++c) {
           uint32_t o[32];
-          tc::tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
+          const uint32_t oc = tmem + lane_base + kColO + grp * kHalfD + 32 * c;
+          tc::tmem_ld32(oc, o);
           tc::tmem_ld_wait();
           tc::reg_fence(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-          tc::tmem_st32(tmem + lane_base + kColO + 32 * c, o);
+          tc::tmem_st32(oc, o);
         }
         tc::tmem_st_wait();
       }
@@ -287,18 +386,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // Epilogue: out = O / l, lse = (max, log sum).
+    sm.red_l[grp][r] = l;
     if (nt > 0) {
-      const int lb = (nt - 1) & 1;
-      mbar_wait_bounded(&sm.pv_done[lb], (unsigned)(((nt - 1) >> 1) & 1), a.status, &sm.abort);
+      const int lb = (nt - 1) % kSBuf;
+      mbar_wait_bounded(&sm.pv_done[lb], (unsigned)(((nt - 1) / kSBuf) & 1), a.status, &sm.abort);
       tc::fence_after_sync();
     }
-    const float inv = (l == 0.f) ? 0.f : 1.f / l;
-    float* orow = a.out + qi * a.out_row_stride + (long long)h * D;
+    named_barrier(1, kSoftmaxThreads);
+    const float l_row = sm.red_l[0][r] + sm.red_l[1][r];
+    const float inv = (l_row == 0.f) ? 0.f : 1.f / l_row;
+    float* orow = a.out + qi * a.out_row_stride + (long long)h * D + grp * kHalfD;
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
+    for (int c = 0; c < kHalfD / 32; ++c) {
       uint32_t o[32];
       if (nt > 0) {
-        tc::tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
+        tc::tmem_ld32(tmem + lane_base + kColO + grp * kHalfD + 32 * c, o);
         tc::tmem_ld_wait();
         tc::reg_fence(o);
       } else {
@@ -313,11 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                           __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
       }
     }
-    if (row_ok && a.lse != nullptr) {
+    if (grp == 0 && row_ok && a.lse != nullptr) {
       float* l2 = a.lse + (qi * a.H + h) * 2;
-      const bool empty = (l == 0.f);
+      const bool empty = (l_row == 0.f);
       l2[0] = empty ? kEmptyLse : m_true * kLn2;
-      l2[1] = empty ? kEmptyLse : logf(l) + (m_ref - m_true) * kLn2;
+      l2[1] = empty ? kEmptyLse : logf(l_row) + (m_ref - m_true) * kLn2;
     }
   }
 
@@ -330,9 +432,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// fp32 -> bf16, n4 groups of four values (the source is 16-byte aligned).
+__global__ void __launch_bounds__(256) to_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
+                                                      long long n4) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    const float4 x = src[i];
+    dst[i] = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+  }
+}
+
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
-template <int D>
+template <int D, bool BF>
 int launch_d(const FlashArgs& a, cudaStream_t s) {
   const int gs = a.H / a.G;
   const long long rows = (long long)a.n_q * gs;
@@ -342,41 +453,73 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   // it are outside the tensor map and arrive as zeros.
   long long kv_rows = a.causal ? a.base_pos + a.n_q : a.n_all;
   if (kv_rows > a.cap) kv_rows = a.cap;
+  const bool no_keys = kv_rows < 1 || a.k == nullptr || a.v == nullptr;
   if (kv_rows < 1) kv_rows = 1;
   CUtensorMap tm_k, tm_v;
   const uint64_t dims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
-  const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * 4};
-  const uint32_t box[2] = {32, (uint32_t)kKeys};
-  const float* kp = a.k != nullptr ? a.k : a.q;  // an empty key set never reads K/V
-  const float* vp = a.v != nullptr ? a.v : a.q;
-  if (!make_tmap(&tm_k, kp, 2, dims, strides, box, false, kSwizzle128) ||
-      !make_tmap(&tm_v, vp, 2, dims, strides, box, false, kSwizzle128Atom32))
-    return ATTN_ERR_UNSUPPORTED;
-  const size_t smem = sizeof(TcSmem) + 1024;
-  auto kern = flash_tc_kernel<D>;
-  if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
-  kern<<<dim3((unsigned)nb, (unsigned)a.G), kThreads, smem, s>>>(a, tm_k, tm_v);
-  return cudaPeekAtLastError() == cudaSuccess ? 0 : ATTN_ERR_CUDA;
+  const uint32_t box[2] = {(uint32_t)(BF ? 64 : 32), (uint32_t)kKeys};
+  void* scratch = nullptr;
+  const void* kp = a.q;  // an empty key set never reads K/V: any aligned base will do
+  const void* vp = a.q;
+  if (!no_keys) {
+    if constexpr (BF) {
+      // K and V as bf16 in stream-ordered temporary memory, released on the
+      // same stream once the attention kernel has run.
+      const long long elems = kv_rows * a.kv_row_stride;
+      if (cudaMallocAsync(&scratch, (size_t)elems * 2 * 2, s) != cudaSuccess) return ATTN_ERR_CUDA;
+      uint16_t* k16 = static_cast<uint16_t*>(scratch);
+      uint16_t* v16 = k16 + elems;
+      to_bf16_kernel<<<4 * 152, 256, 0, s>>>(reinterpret_cast<const float4*>(a.k), reinterpret_cast<uint2*>(k16),
+                                             elems / 4);
+      to_bf16_kernel<<<4 * 152, 256, 0, s>>>(reinterpret_cast<const float4*>(a.v), reinterpret_cast<uint2*>(v16),
+                                             elems / 4);
+      kp = k16;
+      vp = v16;
+    } else {
+      kp = a.k;
+      vp = a.v;
+    }
+  }
+  const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * (BF ? 2 : 4)};
+  int rc = ATTN_OK;
+  if (!make_tmap(&tm_k, kp, 2, dims, strides, box, BF, kSwizzle128) ||
+      !make_tmap(&tm_v, vp, 2, dims, strides, box, BF, BF ? kSwizzle128 : kSwizzle128Atom32)) {
+    rc = ATTN_ERR_UNSUPPORTED;
+  } else {
+    const size_t smem = sizeof(TcSmem) + 1024;
+    auto kern = flash_tc_kernel<D, BF>;
+    if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) {
+      rc = ATTN_ERR_CUDA;
+    } else {
+      kern<<<dim3((unsigned)nb, (unsigned)a.G), kThreads, smem, s>>>(a, tm_k, tm_v);
+      if (cudaPeekAtLastError() != cudaSuccess) rc = ATTN_ERR_CUDA;
+    }
+  }
+  if (scratch != nullptr && cudaFreeAsync(scratch, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+  return rc;
 }
 
 }  // namespace
 
 bool flash_tc_supported(const FlashArgs& a, int prec) {
-  if (prec != ATTN_TF32) return false;
+  if (prec != ATTN_TF32 && prec != ATTN_BF16) return false;
   if (a.kv_pos_dev != nullptr) return false;
   if (a.D != 64 && a.D != 128) return false;
+  if (a.G > 65535) return false;
   const int gs = a.H / a.G;
   if (!is_pow2(gs) || gs > kRows) return false;
   const uintptr_t al = reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.out) |
                        reinterpret_cast<uintptr_t>(a.k) | reinterpret_cast<uintptr_t>(a.v);
   if (al % 16 != 0) return false;
   if (a.q_row_stride % 4 != 0 || a.out_row_stride % 4 != 0 || a.kv_row_stride % 4 != 0) return false;
+  if (prec == ATTN_BF16 && a.kv_row_stride % 8 != 0) return false;  // bf16 rows in 16-byte units
   return true;
 }
 
 int launch_flash_tc(const FlashArgs& a, int prec, cudaStream_t s) {
   if (!flash_tc_supported(a, prec)) return ATTN_ERR_UNSUPPORTED;
-  return a.D == 128 ? launch_d<128>(a, s) : launch_d<64>(a, s);
+  if (prec == ATTN_BF16) return a.D == 128 ? launch_d<128, true>(a, s) : launch_d<64, true>(a, s);
+  return a.D == 128 ? launch_d<128, false>(a, s) : launch_d<64, false>(a, s);
 }
 
 }  // namespace attn

@@ -371,13 +371,13 @@ def tf32_peak(peaks):
     return peaks["bf16_tflops"] * 1.1 / 2.25
 
 
-def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_src, clocks):
-    """Prefill and long causal forward in TFLOP/s: TF32 tensor-core path and fp32 CUDA-core path."""
+def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_src, clocks, only="all"):
+    """Prefill and long causal forward in TFLOP/s on the TF32 and bf16
+    tensor-core paths and the fp32 CUDA-core path."""
     import torch
-    res, launches = {}, 0
+    res = {"_launches": 0}
     sm_mhz = (clocks or {}).get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
     alu_peak = fp32_alu_peak_tflops(sm_mhz, sms)
-    tc_peak = tf32_peak(peaks)
     steps = max(3, min(args.steps, args.extra_steps))
 
     def timed(fn, n):
@@ -390,62 +390,88 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
             fn(i)
             evs[i][1].record(stream)
         torch.cuda.synchronize()
+        res["_launches"] += n + args.warmup
         return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
     def roof(prec, tf, kernel):
+        if prec == A.ATTN_BF16:
+            pk = peaks["bf16_tflops"]
+            return {"bound": "tensor", "achieved": tf, "peak": pk, "unit": "TFLOP/s", "frac": tf / pk,
+                    "traffic": None, "kernel": kernel, "peak_source": "%s bf16 dense, burst" % peak_src}
         if prec == A.ATTN_TF32:
-            return {"bound": "tensor", "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
+            pk = tf32_peak(peaks)
+            return {"bound": "tensor", "achieved": tf, "peak": pk, "unit": "TFLOP/s", "frac": tf / pk,
                     "traffic": None, "kernel": kernel,
                     "peak_source": "%s bf16 %.0f TFLOP/s x 1.1/2.25 (nominal TF32/bf16)" % (peak_src, peaks["bf16_tflops"])}
         return {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
                 "traffic": None, "kernel": kernel,
                 "peak_source": "fp32 FMA: %d SMs x 128 lanes x 2 x %.0f MHz" % (sms, sm_mhz)}
 
-    p = PREFILL
-    qb, kc, vc = synthetic.prefill_inputs(p["n_queries"], p["stride"], p["max_seq"], p["G"] * p["D"], seed=0)
-    per = (qb.numel() + kc.numel() + vc.numel()) * 4
-    n_rot = max(2, int(math.ceil(2.0 * l2 / per)) + 1)
-    bufs = [(qb.to(dev), kc.to(dev), vc.to(dev)) for _ in range(n_rot)]
-    outp = torch.empty((p["n_queries"], p["stride"]), device=dev)
-    scale = 1.0 / math.sqrt(p["D"])
-    for prec, key, kern in ((A.ATTN_TF32, "prefill", "flash_tc_kernel<128> (tf32)"),
-                            (A.ATTN_FP32, "prefill_fp32", "flash_simt_kernel<128,true>")):
-        def prefill_step(i, prec=prec):
-            qd, kd, vd = bufs[i % n_rot]
-            rc = lib.attn_prefill(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outp.data_ptr(), p["n_queries"],
-                                  p["H"], p["G"], p["D"], p["G"] * p["D"], p["max_seq"], scale, p["start_pos"],
-                                  p["stride"], p["stride"], 0, prec, sh)
-            if rc != 0:
-                raise RuntimeError("attn_prefill failed: %d" % rc)
-        ms = timed(prefill_step, steps)
-        launches += steps + args.warmup
-        tf = prefill_flops() / (ms * 1e-3) / 1e12
-        res[key] = {"workload": "prefill 512 queries start_pos=1536 max_seq=2048 32/8 heads D=128",
-                    "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
-                    "prec": "tf32" if prec == A.ATTN_TF32 else "fp32", "roofline": roof(prec, tf, kern),
-                    "l2": "rotating %d input sets" % n_rot}
-    del bufs
+    variants = ((A.ATTN_TF32, "tf32", "flash_tc_kernel<128,false> (tf32)"),
+                (A.ATTN_BF16, "bf16", "flash_tc_kernel<128,true> (bf16) + to_bf16 pre-pass"),
+                (A.ATTN_FP32, "fp32", "flash_simt_kernel<128,true>"))
 
-    f = FORWARD
-    q, k, v = synthetic.forward_inputs(f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], seed=5, qk_sigma=3.0)
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    outf = torch.empty_like(qd)
-    lse = torch.empty((f["q_seq"], f["H"], 2), device=dev)
-    for prec, key, kern in ((A.ATTN_TF32, "forward", "flash_tc_kernel<128> (tf32)"),
-                            (A.ATTN_FP32, "forward_fp32", "flash_simt_kernel<128,true>")):
-        def fwd_step(i, prec=prec):
-            rc = lib.attn_forward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(), lse.data_ptr(),
-                                  f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], A.ATTN_CAUSAL, prec, sh)
-            if rc != 0:
-                raise RuntimeError("attn_forward failed: %d" % rc)
-        ms = timed(fwd_step, steps)
-        launches += steps + args.warmup
-        tf = forward_flops() / (ms * 1e-3) / 1e12
-        res[key] = {"workload": "causal forward+LSE q_seq=8192 32/8 heads D=128, Q,K N(0,9)", "value": tf,
-                    "unit": "TFLOP/s", "ms_per_step": ms, "prec": "tf32" if prec == A.ATTN_TF32 else "fp32",
-                    "roofline": roof(prec, tf, kern), "l2": "inputs 192 MiB > L2"}
-    res["_launches"] = launches
+    if only in ("all", "prefill"):
+        p = PREFILL
+        qb, kc, vc = synthetic.prefill_inputs(p["n_queries"], p["stride"], p["max_seq"], p["G"] * p["D"], seed=0)
+        per = (qb.numel() + kc.numel() + vc.numel()) * 4
+        n_rot = max(2, int(math.ceil(2.0 * l2 / per)) + 1)
+        bufs = [(qb.to(dev), kc.to(dev), vc.to(dev)) for _ in range(n_rot)]
+        outp = torch.empty((p["n_queries"], p["stride"]), device=dev)
+        scale = 1.0 / math.sqrt(p["D"])
+        for prec, name, kern in variants:
+            def prefill_step(i, prec=prec):
+                qd, kd, vd = bufs[i % n_rot]
+                rc = lib.attn_prefill(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outp.data_ptr(), p["n_queries"],
+                                      p["H"], p["G"], p["D"], p["G"] * p["D"], p["max_seq"], scale, p["start_pos"],
+                                      p["stride"], p["stride"], 0, prec, sh)
+                if rc != 0:
+                    raise RuntimeError("attn_prefill failed: %d" % rc)
+            ms = timed(prefill_step, steps)
+            tf = prefill_flops() / (ms * 1e-3) / 1e12
+            res["prefill_" + name] = {
+                "workload": "prefill 512 queries start_pos=1536 max_seq=2048 32/8 heads D=128",
+                "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "prec": name,
+                "roofline": roof(prec, tf, kern), "l2": "rotating %d input sets" % n_rot}
+        del bufs
+
+    if only in ("all", "forward"):
+        f = FORWARD
+        q, k, v = synthetic.forward_inputs(f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], seed=5, qk_sigma=3.0)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        outf = torch.empty_like(qd)
+        lse = torch.empty((f["q_seq"], f["H"], 2), device=dev)
+        for prec, name, kern in variants:
+            def fwd_step(i, prec=prec):
+                rc = lib.attn_forward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(), lse.data_ptr(),
+                                      f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], A.ATTN_CAUSAL, prec, sh)
+                if rc != 0:
+                    raise RuntimeError("attn_forward failed: %d" % rc)
+            ms = timed(fwd_step, steps)
+            tf = forward_flops() / (ms * 1e-3) / 1e12
+            res["forward_" + name] = {
+                "workload": "causal forward+LSE q_seq=8192 32/8 heads D=128, Q,K N(0,9)", "value": tf,
+                "unit": "TFLOP/s", "ms_per_step": ms, "prec": name, "roofline": roof(prec, tf, kern),
+                "l2": "inputs 192 MiB > L2"}
     return res
+
+
+def run_single(args, local):
+    """Prefill or forward workloads only (for profiling)."""
+    import torch
+    import attention_gqa_online_gb300 as A
+    from attention_gqa_online_gb300 import synthetic
+    torch.cuda.set_device(local)
+    lib = A.load_library()
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    res = run_extras(args, A, lib, synthetic, dev, stream, stream.cuda_stream,
+                     getattr(props, "L2_cache_size", 128 << 20), props.multi_processor_count, peaks, peak_src,
+                     None, only=args.only)
+    res.pop("_launches", None)
+    print(json.dumps(res), flush=True)
 
 
 def main():
@@ -458,6 +484,8 @@ def main():
     ap.add_argument("--decode-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "forward"], default="all",
+                    help="run one workload (for profiling); the default runs all of them")
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -466,6 +494,11 @@ def main():
     if args.impl == "reference":
         reference_arm(args, world, rank)
         return
+    if args.only in ("prefill", "forward"):
+        run_single(args, local)
+        return
+    if args.only == "decode":
+        args.decode_only = True
     run_ours(args, world, rank, local)
 
 

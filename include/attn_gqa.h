@@ -19,7 +19,9 @@
  *              takes scale as an argument (the cera shader's params[5]).
  *   Data       fp32 in, fp32 out, row-major, all pointers are DEVICE memory
  *              owned by the caller.  The library keeps no pointer after a call
- *              returns and allocates no device memory.
+ *              returns.  The only device memory it allocates is the ATTN_BF16
+ *              path's temporary bf16 copy of K and V (stream-ordered:
+ *              cudaMallocAsync and cudaFreeAsync on the call's stream).
  *   Streams    every call is asynchronous on `stream` (a cudaStream_t; NULL is
  *              the legacy default stream).  Results are ready when the stream
  *              has reached the call.
@@ -37,12 +39,14 @@
  *   Precision  ATTN_FP32: fp32 CUDA-core arithmetic throughout.
  *              ATTN_TF32: QK^T and PV on tcgen05 tensor cores with TF32
  *              operands and fp32 accumulation; softmax in fp32.
- *              ATTN_BF16: as TF32 but with bf16 operands (inputs are rounded
- *              to bf16 on the way in), fp32 accumulation.
+ *              ATTN_BF16: as TF32 but with bf16 operands (K and V rounded to
+ *              bf16 by a pre-pass, Q and the probabilities P on their way
+ *              into tensor memory), fp32 accumulation and softmax.
  *              Tensor-core precisions need D in {64, 128}, gs a power of two
  *              <= 128, 16-byte aligned pointers and row strides that are
- *              multiples of 4 floats; otherwise they return
- *              ATTN_ERR_UNSUPPORTED.  ATTN_FP32 accepts any 1 <= D <= 128.
+ *              multiples of 4 floats (K/V rows a multiple of 8 floats for
+ *              ATTN_BF16); otherwise they return ATTN_ERR_UNSUPPORTED.
+ *              ATTN_FP32 accepts any 1 <= D <= 128.
  */
 #ifndef ATTN_GQA_H
 #define ATTN_GQA_H

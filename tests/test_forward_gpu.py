@@ -4,11 +4,11 @@ import pytest
 import torch
 
 from attention_gqa_online_gb300 import synthetic
-from helpers import FP32, TF32, assert_lse_close, assert_out_close, dev, tc_supported
+from helpers import BF16, FP32, TF32, assert_lse_close, assert_out_close, dev, tc_supported
 
 pytestmark = pytest.mark.gpu
 CAUSAL, FULL, CROSS = 0, 1, 2
-PRECS = [FP32, TF32]
+PRECS = [FP32, TF32, BF16]
 
 
 def run_forward(A, q, k, v, q_seq, kv_seq, H, G, D, mask, prec):

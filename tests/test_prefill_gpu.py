@@ -6,10 +6,10 @@ import pytest
 import torch
 
 from attention_gqa_online_gb300 import synthetic
-from helpers import FP32, TF32, assert_out_close, dev, tc_supported
+from helpers import BF16, FP32, TF32, assert_out_close, dev, tc_supported
 
 pytestmark = pytest.mark.gpu
-PRECS = [FP32, TF32]
+PRECS = [FP32, TF32, BF16]
 
 
 def check(A, orc, n_queries, H, G, D, kv_dim, max_seq, start_pos, q_stride, out_stride, q_base, prec, seed,
