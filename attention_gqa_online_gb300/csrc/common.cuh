@@ -143,6 +143,16 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels launched with programmatic stream serialization may start while the
+// previous kernel in the stream is finishing.  grid_dependency_wait() blocks
+// until that kernel has completed and its memory is visible: call it before
+// the first global read or write.  allow_dependent_launch() lets the next
+// such kernel start launching (its CTAs then wait in their own
+// grid_dependency_wait()).  Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ---------------------------------------------------------------- math
 // 2^x with the hardware's approximate exp2 (MUFU.EX2); 2^-inf = 0.
 __device__ __forceinline__ float ex2(float x) {

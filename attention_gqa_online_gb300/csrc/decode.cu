@@ -20,6 +20,9 @@
 //     last CTA of kv head g to finish (atomic ticket) merges the S partials
 //     with the log-sum-exp rule: M = max m_j, L = sum l_j 2^(m_j - M),
 //     out = sum o_j 2^(m_j - M) / L, and resets the ticket for the next call.
+//   * Launched with programmatic dependent launch: a decode step's launch and
+//     set-up overlap the previous step's merge tail; nothing touches global
+//     memory before the previous kernel has completed.
 //
 // Scores are kept in the base-2 domain (scale * log2(e) folded into q).
 #include <cfloat>
@@ -51,6 +54,7 @@ struct __align__(128) DecodeSmem {
   float red_o[kCWarps][GS][D];
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t merge_bar;
   int is_last;
   int abort;
 };
@@ -63,13 +67,17 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// (m, l) pairs of one head are kEvenS(S) pairs apart, so every head's pairs
+// start on a 16-byte boundary (the final merge bulk-copies them).
+__host__ __device__ inline int even_splits(int S) { return (S + 1) & ~1; }
+
 __host__ __device__ inline WsLayout ws_layout(void* ws, int H, int G, int D, int S) {
   char* p = static_cast<char*>(ws);
   WsLayout l;
   l.tickets = reinterpret_cast<unsigned*>(p);
   p += align256(sizeof(unsigned) * G);
   l.ml = reinterpret_cast<float*>(p);
-  p += align256(sizeof(float) * 2 * (size_t)H * S);
+  p += align256(sizeof(float) * 2 * (size_t)H * even_splits(S));
   l.o = reinterpret_cast<float*>(p);
   return l;
 }
@@ -91,6 +99,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int j = blockIdx.x, g = blockIdx.y;
 
+  // Launched with programmatic serialization: let the next decode start
+  // launching now, and wait for the previous kernel before any global access.
+  allow_dependent_launch();
+  grid_dependency_wait();
   const unsigned kp = *a.kv_pos_dev;
   if (j == 0 && g == 0 && tid == 0 && (long long)kp >= (long long)a.max_seq)
     record_status(a.status, ATTN_ERR_INVALID_ARG);
@@ -115,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kCWarps);
     }
+    mbar_init(&sm.merge_bar, 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -285,8 +298,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const size_t hs = (size_t)(g * GS + h) * S + j;
     ws.o[hs * D + d] = O;
     if (d == 0) {
-      ws.ml[hs * 2] = M;
-      ws.ml[hs * 2 + 1] = L;
+      const size_t ms = ((size_t)(g * GS + h) * even_splits(S) + j) * 2;
+      ws.ml[ms] = M;
+      ws.ml[ms + 1] = L;
     }
   }
 
@@ -301,6 +315,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (!sm.is_last) return;
   __threadfence();
 
+  // Fast path: every split's partials of this kv head fit in the (now idle)
+  // stage buffers: one round of bulk copies brings them all in, then the
+  // merge runs from shared memory.
+  const int S2 = even_splits(S);
+  const unsigned ml_head_bytes = ((unsigned)s_eff * 8u + 15u) & ~15u;
+  const size_t merge_bytes = (size_t)GS * s_eff * D * 4 + (size_t)GS * ml_head_bytes;
+  if (merge_bytes <= sizeof(sm.k) + sizeof(sm.v)) {
+    float* so = &sm.k[0][0];                       // [GS][s_eff][D]
+    float* sml = so + (size_t)GS * s_eff * D;      // [GS][ml_head_bytes / 4]
+    if (tid == 0) {
+      asm volatile("fence.proxy.async;" ::: "memory");
+      mbar_arrive_expect_tx(&sm.merge_bar, (unsigned)merge_bytes);
+      for (int h = 0; h < GS; ++h) {
+        bulk_g2s(so + (size_t)h * s_eff * D, ws.o + (size_t)(g * GS + h) * S * D, (unsigned)(s_eff * D * 4),
+                 &sm.merge_bar);
+        bulk_g2s(sml + (size_t)h * (ml_head_bytes / 4), ws.ml + (size_t)(g * GS + h) * S2 * 2, ml_head_bytes,
+                 &sm.merge_bar);
+      }
+    }
+    mbar_wait_bounded(&sm.merge_bar, 0, a.status);
+    for (int idx = tid; idx < GS * (D / 4); idx += kThreads) {
+      const int h = idx / (D / 4), c = idx % (D / 4);
+      const float* mlh = sml + (size_t)h * (ml_head_bytes / 4);
+      float M = -INFINITY;
+      for (int s = 0; s < s_eff; ++s) M = fmaxf(M, mlh[2 * s]);
+      const float Mu = (M == -INFINITY) ? 0.f : M;
+      float L = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int s = 0; s < s_eff; ++s) {
+        const float f = ex2(mlh[2 * s] - Mu);
+        const float4 x = *reinterpret_cast<const float4*>(so + ((size_t)h * s_eff + s) * D + 4 * c);
+        L = fmaf(mlh[2 * s + 1], f, L);
+        O.x = fmaf(x.x, f, O.x);
+        O.y = fmaf(x.y, f, O.y);
+        O.z = fmaf(x.z, f, O.z);
+        O.w = fmaf(x.w, f, O.w);
+      }
+      const float inv = (L == 0.f) ? 0.f : 1.f / L;
+      *reinterpret_cast<float4*>(a.out + (size_t)(g * GS + h) * D + 4 * c) =
+          make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    }
+    if (tid == 0) ws.tickets[g] = 0u;
+    return;
+  }
+
   // One pass over the splits with the same online rule (running max,
   // correction, sum), 16 splits' loads in flight at a time; one float4 of
   // one head per thread.
@@ -308,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int h = idx / (D / 4), c = idx % (D / 4);
     const size_t hb = (size_t)(g * GS + h) * S;
     const float* op = ws.o + hb * D + 4 * c;
-    const float2* mlp = reinterpret_cast<const float2*>(ws.ml + hb * 2);
+    const float2* mlp = reinterpret_cast<const float2*>(ws.ml + (size_t)(g * GS + h) * S2 * 2);
     float M = -INFINITY, L = 0.f;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < s_eff; s0 += kMergeBatch) {
@@ -367,8 +427,13 @@ int launch_t(const DecodeArgs& a, int S, cudaStream_t s) {
       !make_tmap(&tm_v, a.v_cache, 2, dims, strides, box, false, kSwizzleNone))
     return ATTN_ERR_UNSUPPORTED;
   const float sl2 = (1.0f / sqrtf((float)D)) * kLog2e;
-  kern<<<dim3(S, a.G), kThreads, smem, s>>>(a, S, sl2, tm_k, tm_v);
-  return cudaPeekAtLastError() == cudaSuccess ? 0 : ATTN_ERR_CUDA;
+  DecodeArgs aa = a;
+  int SS = S;
+  float sl = sl2;
+  void* args[] = {&aa, &SS, &sl, &tm_k, &tm_v};
+  return launch_pdl(reinterpret_cast<const void*>(kern), dim3(S, a.G), dim3(kThreads), smem, s, args) == cudaSuccess
+             ? 0
+             : ATTN_ERR_CUDA;
 }
 
 }  // namespace
@@ -390,7 +455,7 @@ int decode_splits(int G, int max_seq, int sm_count) {
 size_t decode_workspace_bytes(int H, int G, int D, int max_seq, int sm_count) {
   if (!decode_split_supported(H, G, D) || max_seq <= 0) return 0;
   const int S = decode_splits(G, max_seq, sm_count);
-  return align256(sizeof(unsigned) * G) + align256(sizeof(float) * 2 * (size_t)H * S) +
+  return align256(sizeof(unsigned) * G) + align256(sizeof(float) * 2 * (size_t)H * even_splits(S)) +
          sizeof(float) * (size_t)H * S * D;
 }
 

@@ -98,6 +98,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kRing = kRingBytes / kTileBytes;  // tiles in flight
   static_assert(kRing <= kMaxRing, "ring barriers");
   constexpr int kKStep = BF ? 16 : 8;          // MMA K per instruction (32 bytes)
+  // V operand form.  The bf16 path reads V^T (keys contiguous), written by the
+  // pre-pass, as a K-major operand: an MN-major V measured about twice as slow
+  // in P V as the same-size K-major Q K^T.
+  constexpr bool kVT = BF;
+  constexpr int kVtChunkBytes = D * 128;       // one V^T box: D rows x 128 bytes of keys
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
@@ -151,10 +156,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned char* dst = sm.ring + s * kTileBytes;
         if (use >= 1) mbar_wait_bounded(&sm.kv_empty[s], (unsigned)((use - 1) & 1), a.status, &sm.abort);
         mbar_arrive_expect_tx(&sm.kv_full[s], (unsigned)kTileBytes);
-        const CUtensorMap* tm = (idx & 1) ? &tm_v : &tm_k;
-        const int y = kKeys * (idx >> 1);
+        const int t0 = kKeys * (idx >> 1);
+        if ((idx & 1) && kVT) {
+          // V^T tile: kKeys / kEpr boxes of [D rows (d) x 128 bytes of keys].
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + kEpr * c, y, &sm.kv_full[s]);
+          for (int c = 0; c < kKeys / kEpr; ++c)
+            tma_load_2d(dst + c * kVtChunkBytes, &tm_v, t0 + kEpr * c, g * D, &sm.kv_full[s]);
+        } else {
+          const CUtensorMap* tm = (idx & 1) ? &tm_v : &tm_k;
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + kEpr * c, t0, &sm.kv_full[s]);
+        }
       }
       // No copy may still be landing in shared memory when the CTA exits
       // (normally every fill was already consumed, so these return at once).
@@ -168,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && nt > 0) {
       constexpr uint32_t kFmt = BF ? tc::kFmtBF16 : tc::kFmtTF32;
       constexpr uint32_t idesc_qk = tc::idesc_f32acc(kFmt, false, kRows, kKeys);
-      constexpr uint32_t idesc_pv = tc::idesc_f32acc(kFmt, true, kRows, D);
+      constexpr uint32_t idesc_pv = tc::idesc_f32acc(kFmt, !kVT, kRows, D);
       // V (MN-major B): TF32 needs the 32-byte-atom layout with 4-row K groups;
       // bf16 uses the plain 128-byte swizzle with 8-row groups.
       constexpr uint32_t kVLayout = BF ? tc::kLayoutSw128 : tc::kLayoutSw128Atom32;
@@ -215,7 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t vb = tile_addr(2 * np + 1);
 #pragma unroll
           for (int kk = 0; kk < kKeys / kKStep; ++kk) {
-            const uint64_t bdesc = tc::sdesc_sw128(vb + kk * kVStep, kChunkBytes, kVSbo, kVLayout);
+            const uint64_t bdesc =
+                kVT ? tc::sdesc_sw128(vb + (kk >> 2) * kVtChunkBytes + (kk & 3) * 32, 16, 1024)
+                    : tc::sdesc_sw128(vb + kk * kVStep, kChunkBytes, kVSbo, kVLayout);
             if constexpr (BF)
               tc::mma_f16_ts(tmem + kColO, tmem + kColS0 + kKeys * b + 8 * kk, bdesc, idesc_pv, (np > 0 || kk > 0));
             else
@@ -441,6 +455,30 @@ __global__ void __launch_bounds__(256) to_bf16_kernel(const float4* __restrict__
   }
 }
 
+// V [rows][row_stride] fp32 -> V^T [cols][pad] bf16 (cols = G*D), zero for
+// rows >= rows.  32 x 32 tiles through shared memory; block (32, 8).
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const float* __restrict__ v, uint16_t* __restrict__ vt,
+                                                             long long rows, long long pad, long long row_stride,
+                                                             int cols) {
+  __shared__ float tile[32][33];
+  const long long t0 = (long long)blockIdx.x * 32;
+  const int c0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const long long t = t0 + i;
+    const int c = c0 + threadIdx.x;
+    tile[i][threadIdx.x] = (t < rows && c < cols) ? v[t * row_stride + c] : 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i;
+    const long long t = t0 + threadIdx.x;
+    if (c < cols && t < pad) {
+      const uint32_t w = pack_bf16(tile[threadIdx.x][i], 0.f);
+      vt[(long long)c * pad + t] = (uint16_t)(w & 0xffffu);
+    }
+  }
+}
+
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 template <int D, bool BF>
@@ -459,31 +497,45 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const uint64_t dims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
   const uint32_t box[2] = {(uint32_t)(BF ? 64 : 32), (uint32_t)kKeys};
   void* scratch = nullptr;
+  long long kv_pad = 64;
   const void* kp = a.q;  // an empty key set never reads K/V: any aligned base will do
   const void* vp = a.q;
   if (!no_keys) {
     if constexpr (BF) {
       // K and V as bf16 in stream-ordered temporary memory, released on the
       // same stream once the attention kernel has run.
+      // K keeps its layout; V is written transposed, V^T [G*D][kv_pad] with
+      // keys contiguous and the pad columns zero.
       const long long elems = kv_rows * a.kv_row_stride;
-      if (cudaMallocAsync(&scratch, (size_t)elems * 2 * 2, s) != cudaSuccess) return ATTN_ERR_CUDA;
+      kv_pad = (kv_rows + 63) / 64 * 64;
+      const long long vt_elems = (long long)a.G * D * kv_pad;
+      if (cudaMallocAsync(&scratch, (size_t)(elems + vt_elems) * 2, s) != cudaSuccess) return ATTN_ERR_CUDA;
       uint16_t* k16 = static_cast<uint16_t*>(scratch);
-      uint16_t* v16 = k16 + elems;
+      uint16_t* vt16 = k16 + elems;
       to_bf16_kernel<<<4 * 152, 256, 0, s>>>(reinterpret_cast<const float4*>(a.k), reinterpret_cast<uint2*>(k16),
                                              elems / 4);
-      to_bf16_kernel<<<4 * 152, 256, 0, s>>>(reinterpret_cast<const float4*>(a.v), reinterpret_cast<uint2*>(v16),
-                                             elems / 4);
+      const dim3 tgrid((unsigned)(kv_pad / 32), (unsigned)((a.G * D + 31) / 32));
+      transpose_bf16_kernel<<<tgrid, dim3(32, 8), 0, s>>>(a.v, vt16, kv_rows, kv_pad, a.kv_row_stride, a.G * D);
       kp = k16;
-      vp = v16;
+      vp = vt16;
     } else {
       kp = a.k;
       vp = a.v;
     }
   }
   const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * (BF ? 2 : 4)};
+  bool maps_ok = make_tmap(&tm_k, kp, 2, dims, strides, box, BF, kSwizzle128);
+  if (BF) {
+    // V^T: [G*D rows][kv_pad keys], boxes of 64 keys x D rows.
+    const uint64_t vdims[2] = {(uint64_t)kv_pad, (uint64_t)a.G * D};
+    const uint64_t vstrides[1] = {(uint64_t)kv_pad * 2};
+    const uint32_t vbox[2] = {64, (uint32_t)D};
+    maps_ok = maps_ok && make_tmap(&tm_v, vp, 2, vdims, vstrides, vbox, true, kSwizzle128);
+  } else {
+    maps_ok = maps_ok && make_tmap(&tm_v, vp, 2, dims, strides, box, false, kSwizzle128Atom32);
+  }
   int rc = ATTN_OK;
-  if (!make_tmap(&tm_k, kp, 2, dims, strides, box, BF, kSwizzle128) ||
-      !make_tmap(&tm_v, vp, 2, dims, strides, box, BF, BF ? kSwizzle128 : kSwizzle128Atom32)) {
+  if (!maps_ok) {
     rc = ATTN_ERR_UNSUPPORTED;
   } else {
     const size_t smem = sizeof(TcSmem) + 1024;

@@ -36,6 +36,11 @@ struct FlashArgs {
   unsigned* status;           // device status word
 };
 
+// Launches `kernel` with programmatic stream serialization allowed, so it may
+// start while the previous kernel in `s` finishes (the kernel itself waits
+// for that kernel before touching global memory).
+cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args);
+
 // Raises a kernel's dynamic shared memory limit to `bytes` on the current
 // device; the attribute is set once per (kernel, device).
 bool set_smem_limit(const void* kernel, size_t bytes);
