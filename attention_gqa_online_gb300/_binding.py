@@ -147,6 +147,16 @@ def attn_decode_cached_noalloc(q, k_cache, v_cache, kv_pos_dev, out, num_heads, 
               _stream(stream)), "attn_decode_cached_noalloc")
 
 
+def attn_selftest_wait_timeout(timeout_us=10000, stream=None):
+    """Run the bounded-wait failure path once (see attn_gqa.h); read the
+    outcome with attn_get_status()."""
+    lib = load_library()
+    fn = lib.attn_selftest_wait_timeout
+    fn.restype = ctypes.c_int
+    fn.argtypes = [_u32, _vp]
+    _check(fn(timeout_us, _stream(stream)), "attn_selftest_wait_timeout")
+
+
 def attn_get_status(stream=None):
     """Synchronise `stream`, return and clear the device status word."""
     return int(load_library().attn_get_status(_stream(stream)))

@@ -81,13 +81,14 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 // is set, later waits of the same CTA give up at once, so a CTA whose
 // pipeline broke finishes quickly instead of timing out wait after wait.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity, unsigned* status,
-                                                  volatile int* abort_flag = nullptr) {
+                                                  volatile int* abort_flag = nullptr,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort_flag != nullptr && *abort_flag != 0) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       record_status(status, ATTN_ERR_TIMEOUT);
       if (abort_flag != nullptr) *abort_flag = 1;
       return false;

@@ -78,6 +78,10 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
 
+  // Programmatic dependent launch (see common.cuh): no global access before
+  // the previous kernel in the stream has completed.
+  allow_dependent_launch();
+  grid_dependency_wait();
   const int tid = threadIdx.x;
   const int rg = tid >> 4, cl = tid & 15;
   const int r0 = 4 * rg;
@@ -294,8 +298,12 @@ int launch_one(const FlashArgs& a, cudaStream_t s) {
   const size_t smem = sizeof(SimtSmem<DMAX>);
   auto kern = flash_simt_kernel<DMAX, VEC>;
   if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
-  kern<<<dim3((unsigned)nb, (unsigned)a.G), NT, smem, s>>>(a);
-  return cudaPeekAtLastError() == cudaSuccess ? 0 : ATTN_ERR_CUDA;
+  FlashArgs aa = a;
+  void* args[] = {&aa};
+  return launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(NT), smem, s, args) ==
+                 cudaSuccess
+             ? 0
+             : ATTN_ERR_CUDA;
 }
 
 }  // namespace

@@ -107,6 +107,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
 
+  // Programmatic dependent launch: the next kernel may start launching; this
+  // one touches no global memory before the previous kernel has completed.
+  allow_dependent_launch();
+  grid_dependency_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y;
   const int blk = gridDim.x - 1 - blockIdx.x;  // heaviest causal blocks first
@@ -543,8 +547,11 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
     if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) {
       rc = ATTN_ERR_CUDA;
     } else {
-      kern<<<dim3((unsigned)nb, (unsigned)a.G), kThreads, smem, s>>>(a, tm_k, tm_v);
-      if (cudaPeekAtLastError() != cudaSuccess) rc = ATTN_ERR_CUDA;
+      FlashArgs aa = a;
+      void* args[] = {&aa, &tm_k, &tm_v};
+      if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s,
+                     args) != cudaSuccess)
+        rc = ATTN_ERR_CUDA;
     }
   }
   if (scratch != nullptr && cudaFreeAsync(scratch, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;

@@ -155,13 +155,20 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Largest x over all ranks (x is a host float; the time of the slowest rank)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def weak_scaling_value(bytes_per_step, world, steps, ms_total_max):
+    """Whole-job bandwidth in GB/s: every rank's bytes over the slowest rank's time."""
+    return bytes_per_step * world * steps / (ms_total_max * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------- oracle timing
@@ -301,7 +308,7 @@ def run_ours(args, world, rank, local):
         raise RuntimeError("device status %d after the decode loop" % status)
     ms_step = ms_total / args.steps
     step_bytes = decode_bytes(KV_POS + 1)
-    value = step_bytes * world * args.steps / (ms_total * 1e-3) / 1e9
+    value = weak_scaling_value(step_bytes, world, args.steps, ms_total)
     achieved = step_bytes / (kern_ms * 1e-3) / 1e9
     clocks = sampler.summary(wall0, wall1) if rank == 0 else None
 

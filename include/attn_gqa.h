@@ -212,6 +212,17 @@ ATTN_API int attn_decode_cached_noalloc(const float *q, const float *k_cache, co
  */
 ATTN_API int attn_get_status(attn_stream_t stream);
 
+/*
+ * Failure-path self test.  Launches one CTA that waits, with the bounded wait
+ * every kernel of this library uses, on a barrier that nothing completes, but
+ * with a limit of timeout_us microseconds (1 .. 1000000) instead of the usual
+ * one second.  The wait gives up, the kernel records ATTN_ERR_TIMEOUT in the
+ * device status word and returns normally: no fault, no hang, and the CUDA
+ * context stays usable.  Read the outcome with attn_get_status.  Errors:
+ * INVALID_ARG for a timeout outside the range.
+ */
+ATTN_API int attn_selftest_wait_timeout(uint32_t timeout_us, attn_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 ATTN_API const char *attn_status_string(int status);
 
