@@ -1,0 +1,523 @@
+// flash_bf16.cu -- tcgen05 flash attention with bf16 operands (forward and
+// prefill).
+//
+// Operation: softmax(scale * Q K^T) V over per-row causal / full / cross /
+// prefill windows with the online softmax's running max and sum (cera
+// attention_prefill.wgsl, fn attention_prefill: per-tile max, correction,
+// exponentials, running sum; meganeura attention.wgsl, fn main: the final
+// (max, log sum) store).  A pre-pass converts K to bf16 in place order and V to
+// bf16 transposed (keys contiguous); Q and P are rounded to bf16 inside the
+// kernel; both products accumulate in fp32 in tensor memory.
+//
+// One CTA owns 128 packed rows of one kv head g: row r is (query i, head
+// g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs query
+// heads that share it.  Keys are walked in tiles of 128, dealt alternately to
+// two independent online-softmax streams: stream 0 takes the even tiles,
+// stream 1 the odd ones.  Each stream has its own score buffer, O accumulator,
+// running max and running sum, and its own softmax warpgroup in which one
+// thread owns one whole row, so the two warpgroups never wait for each other
+// inside the loop, and while one of them turns scores into probabilities the
+// tensor core runs the other stream's products.  The two partial results are
+// merged once at the end with log-sum-exp weights, the way two KV splits are.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: K tile (128 keys x D, 128-byte swizzle, K-major)
+//               and V^T tile (D x 128 keys, K-major) into a shared-memory ring.
+//   warps 1, 2  MMA issue, one thread per stream s (warp 1 also allocates
+//               tensor memory), for the tiles j of that stream in order:
+//                 S_s  = Q K_j^T   (A = Q in shared memory, B = K tile)
+//                 O_s += P_j V_j   (A = P in TMEM over S_s, B = V^T tile)
+//   warps 4-7   softmax of stream 0; warps 8-11 of stream 1.  Warp w covers
+//               rows 32(w%4)..+31 (its TMEM lanes); a thread owns one row.
+// Tensor memory (512 columns): S_0 [0, 128), S_1 [128, 256), O_0 [256, 256+D),
+// O_1 [256+D, 256+2D).  Scores are in base-2 units (Q is pre-multiplied by
+// scale * log2(e)).  A stream's reference max only moves when its tile max
+// exceeds it by more than 8 (so P <= 256); the true max is tracked apart for
+// the LSE.  Every wait is bounded; a CTA whose pipeline breaks drains its
+// copies and MMAs before it releases tensor memory.
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kRows = 128;              // packed rows per CTA (MMA M)
+constexpr int kKeys = 128;              // keys per tile
+constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kOperandBytes = 192 * 1024;  // Q tile + K/V ring
+constexpr int kMaxRing = 12;
+constexpr int kColS = 0, kColO = 256;   // S_s at kColS + 128 s; O_s at kColO + D s
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct __align__(1024) PpSmem {
+  unsigned char operands[kOperandBytes];  // [Q tile][ring slots]
+  uint64_t kv_full[kMaxRing];
+  uint64_t kv_empty[kMaxRing];
+  uint64_t s_full[2];
+  uint64_t p_ready[2];
+  uint64_t pv_done[2];
+  uint64_t q_ready;
+  uint64_t drain[2];
+  float part[2][3][kRows];  // [stream][m_ref, m_true, l][row], for the final merge
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Three-way max (one instruction on this architecture).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (a0, a1) += (b0, b1) as one paired fp32 add.
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+      "add.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    flash_bf16_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_vt) {
+  constexpr int kChunks = D / 64;                // 128-byte (64-element) column chunks of a K row
+  constexpr int kChunkBytes = kKeys * 128;       // one K box: 128 keys x 128 bytes
+  constexpr int kVtChunkBytes = D * 128;         // one V^T box: D rows x 128 bytes of keys
+  constexpr int kTileBytes = kChunks * kChunkBytes;  // == 2 * kVtChunkBytes
+  constexpr int kQBytes = kRows * D * 2;
+  constexpr int kRing = (kOperandBytes - kQBytes) / kTileBytes;
+  static_assert(kRing <= kMaxRing && kRing >= 4, "ring depth");
+  static_assert(kTileBytes == (kKeys / 64) * kVtChunkBytes, "K and V^T tiles fill a slot alike");
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  PpSmem& sm = *reinterpret_cast<PpSmem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
+  unsigned char* const qtile = sm.operands;
+  unsigned char* const ring = sm.operands + kQBytes;
+
+  allow_dependent_launch();
+  grid_dependency_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.y;
+  const int blk = gridDim.x - 1 - blockIdx.x;  // heaviest causal blocks first
+  const int gs = a.H / a.G;
+  const int qpb = kRows / gs;
+  const long long i0 = (long long)blk * qpb;
+  auto window = [&](long long i) -> int {
+    if (i < 0 || i >= a.n_q) return 0;
+    if (!a.causal) return a.n_all;
+    const long long w = a.base_pos + i + 1;
+    return (int)(w < a.cap ? w : a.cap);
+  };
+  const int n_min = window(i0);
+  const int n_max = window(min((long long)a.n_q, i0 + qpb) - 1);
+  const int nt = (n_max + kKeys - 1) / kKeys;
+
+  if (tid == 0) {
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.s_full[b], 1);
+      mbar_init(&sm.p_ready[b], 4);
+      mbar_init(&sm.pv_done[b], 1);
+    }
+    mbar_init(&sm.q_ready, 8);
+    mbar_init(&sm.drain[0], 1);
+    mbar_init(&sm.drain[1], 1);
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tc::tmem_alloc(&sm.tmem_base, 512);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && nt > 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_vt);
+      // Copies are issued in the order the two streams need the tiles:
+      // K_0, K_1, V_0, K_2, V_1, ..., K_(nt-1), V_(nt-2), V_(nt-1), so each
+      // ring slot is released roughly in the order it was filled and the ring
+      // runs kRing copies ahead of the tensor core.
+      for (int p = 0; p < 2 * nt; ++p) {
+        const int s = p % kRing, use = p / kRing;
+        unsigned char* dst = ring + s * kTileBytes;
+        if (use >= 1) mbar_wait_bounded(&sm.kv_empty[s], (unsigned)((use - 1) & 1), a.status, &sm.abort);
+        mbar_arrive_expect_tx(&sm.kv_full[s], (unsigned)kTileBytes);
+        const bool is_v = (p == 2 * nt - 1) || (p > 0 && (p & 1) == 0);
+        const int j = is_v ? (p == 2 * nt - 1 ? nt - 1 : p / 2 - 1) : (p + 1) / 2;
+        const int t0 = kKeys * j;
+        if (is_v) {
+#pragma unroll
+          for (int c = 0; c < kKeys / 64; ++c)
+            tma_load_2d(dst + c * kVtChunkBytes, &tm_vt, t0 + 64 * c, g * D, &sm.kv_full[s]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, &tm_k, g * D + 64 * c, t0, &sm.kv_full[s]);
+        }
+      }
+      // No copy may still be landing in shared memory when the CTA exits.
+      for (int s = 0; s < kRing && s < 2 * nt; ++s) {
+        const int last = s + ((2 * nt - 1 - s) / kRing) * kRing;
+        mbar_wait_bounded(&sm.kv_full[s], (unsigned)((last / kRing) & 1), a.status);
+      }
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues stream 0's products, warp 2 stream 1's.  An issuing
+    // thread blocks in tcgen05.mma while the tensor core's queue is full, so
+    // one thread alone leaves the tensor core idle for every wait and every
+    // bookkeeping step between its groups; with one issuer per stream, one
+    // stream's products run while the other's issuer waits.
+    const int st = warp - 1;
+    if (lane == 0 && nt > st) {
+      constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, kKeys);
+      constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, D);
+      // Every operand here is K-major with the 128-byte swizzle and 1024-byte
+      // row groups, so one descriptor serves each base and an operand at byte
+      // offset off is that descriptor plus off >> 4 (the start-address field;
+      // shared-memory offsets stay far below its 14-bit range).
+      const uint64_t dq = tc::sdesc_sw128(smem_u32(qtile), 16, 1024);
+      const uint64_t dring = tc::sdesc_sw128(smem_u32(ring), 16, 1024);
+      const uint32_t ds = tmem + kColS + kKeys * st;  // S_st (P_st in its first 64 columns)
+      const uint32_t d_o = tmem + kColO + D * st;      // O_st
+      auto tile_desc = [&](int p) { return dring + (uint64_t)(((p % kRing) * kTileBytes) >> 4); };
+      auto wait = [&](uint64_t* bar, int phase) {
+        return mbar_wait_bounded(bar, (unsigned)(phase & 1), a.status, &sm.abort);
+      };
+      bool ok = wait(&sm.q_ready, 0);
+      tc::fence_after_sync();
+      for (int j = st; ok && j < nt; j += 2) {
+        // S_st = Q K_j^T.  It overwrites the P that P V of tile j-2 reads, so
+        // that product must have completed.
+        const int pk = j == 0 ? 0 : 2 * j - 1;            // ring position of K_j
+        const int pv = j == nt - 1 ? 2 * nt - 1 : 2 * j + 2;  // and of V_j
+        ok = wait(&sm.kv_full[pk % kRing], pk / kRing) && (j < 2 || wait(&sm.pv_done[st], (j - 2) >> 1));
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint64_t dk = tile_desc(pk);
+        // Four K steps (16 elements, 32 bytes each) per 128-byte chunk.
+#pragma unroll
+        for (int c4 = 0; c4 < kChunks; ++c4) {
+          const uint64_t c = (uint64_t)((c4 * kChunkBytes) >> 4);
+          tc::mma4_f16_ss(ds, dq + c, dq + c + 2, dq + c + 4, dq + c + 6, dk + c, dk + c + 2, dk + c + 4, dk + c + 6,
+                          idesc_qk, c4 > 0 ? 1u : 0u);
+        }
+        tc::commit(&sm.s_full[st]);
+        tc::commit(&sm.kv_empty[pk % kRing]);
+        // O_st += P_j V_j once the softmax group has written P_j.
+        ok = wait(&sm.p_ready[st], j >> 1) && wait(&sm.kv_full[pv % kRing], pv / kRing);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint64_t dv = tile_desc(pv);
+        const uint32_t acc0 = j >= 2 ? 1u : 0u;
+#pragma unroll
+        for (int c4 = 0; c4 < kKeys / 64; ++c4) {
+          const uint64_t c = (uint64_t)((c4 * kVtChunkBytes) >> 4);
+          const uint32_t pa = ds + 32 * c4;  // P: 8 columns (16 keys) per K step
+          tc::mma4_f16_ts(d_o, pa, pa + 8, pa + 16, pa + 24, dv + c, dv + c + 2, dv + c + 4, dv + c + 6, idesc_pv,
+                          c4 > 0 ? 1u : acc0);
+        }
+        tc::commit(&sm.pv_done[st]);
+        tc::commit(&sm.kv_empty[pv % kRing]);
+      }
+      // Every MMA has finished before tensor memory is released.
+      tc::commit(&sm.drain[st]);
+      mbar_wait_bounded(&sm.drain[st], 0, a.status);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int st = (warp - 4) >> 2;            // stream 0 or 1
+    const int r = 32 * (warp & 3) + lane;      // row == TMEM lane
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const long long packed = (long long)blk * kRows + r;
+    const long long qi = packed / gs;
+    const int h = g * gs + (int)(packed % gs);
+    const int n_r = window(qi);
+    const bool row_ok = qi < a.n_q;
+    const float sl2 = a.scale * kLog2e;
+
+    // Q row, pre-scaled, as bf16 into the K-major operand tile: 64-element
+    // chunk c holds 128 rows of 128 bytes, 16-byte unit u of row r at unit
+    // u ^ (r & 7) (the 128-byte swizzle).  Stream c's warps write chunk c.
+    if (st < kChunks) {
+      unsigned char* qdst = qtile + st * kChunkBytes + r * 128;
+      const float* qrow = a.q + qi * a.q_row_stride + (long long)h * D + 64 * st;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+        if (row_ok) {
+          x0 = *reinterpret_cast<const float4*>(qrow + 8 * u);
+          x1 = *reinterpret_cast<const float4*>(qrow + 8 * u + 4);
+        }
+        const uint4 w = make_uint4(tc::pack_bf16(x0.x * sl2, x0.y * sl2), tc::pack_bf16(x0.z * sl2, x0.w * sl2),
+                                   tc::pack_bf16(x1.x * sl2, x1.y * sl2), tc::pack_bf16(x1.z * sl2, x1.w * sl2));
+        *reinterpret_cast<uint4*>(qdst + 16 * (u ^ (r & 7))) = w;
+      }
+    }
+    // The tensor core reads the tile through the async proxy.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.q_ready);
+
+    const uint32_t s_col = tmem + lane_base + kColS + kKeys * st;
+    const uint32_t o_col = tmem + lane_base + kColO + D * st;
+    float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
+    for (int j = st; j < nt; j += 2) {
+      mbar_wait_bounded(&sm.s_full[st], (unsigned)((j >> 1) & 1), a.status, &sm.abort);
+      tc::fence_after_sync();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_col + 32 * c, s[c]);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::reg_fence(s[c]);
+
+      if ((j + 1) * kKeys > n_min) {  // the tile crosses some row's window end
+        const int lim = n_r - j * kKeys;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
+      }
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < kKeys; i += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mx[k] = max3(mx[k], __uint_as_float(s[i >> 5][(i & 31) + 2 * k]), __uint_as_float(s[i >> 5][(i & 31) + 2 * k + 1]));
+      const float tmax = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      m_true = fmaxf(m_true, tmax);
+      float corr = 1.f;
+      if (tmax > m_ref + kRescaleThreshold) {  // also true for the first finite tile max
+        corr = ex2(m_ref - tmax);              // m_ref = -inf gives 0
+        m_ref = tmax;
+      }
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+
+      // P = 2^(S - m) as bf16 pairs over the first 64 columns of S_s (every
+      // column of this row was read above): the 32 values of chunk c become
+      // 16 words, packed in place into s[c] and stored at column 16 c.  The
+      // row sum is taken in fp32.
+      float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float x0 = __uint_as_float(s[c][e]), x1 = __uint_as_float(s[c][e + 1]);
+          add2(x0, x1, neg_m, neg_m);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          const int k = (e >> 1) & 3;
+          add2(sum[2 * k], sum[2 * k + 1], p0, p1);
+          s[c][e >> 1] = tc::pack_bf16(p0, p1);
+        }
+        tc::tmem_st16(s_col + 16 * c, s[c]);
+      }
+      const float tsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+      l = l * corr + tsum;
+
+      // O_s holds this stream's earlier tiles and is idle here: P V of tile
+      // j-2 finished before Q K^T of tile j was issued, and P V of tile j
+      // waits for p_ready.  Rescale it when any row of the warp moved.
+      if (j >= 2 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(o_col + 32 * c, o);
+          tc::tmem_ld_wait();
+          tc::reg_fence(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+          tc::tmem_st32(o_col + 32 * c, o);
+        }
+      }
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_ready[st]);
+    }
+
+    // Epilogue: merge the two streams, out = O / l, lse = (max, log sum).
+    // Each warpgroup waits for its own stream's last P V (one phase at most is
+    // outstanding: the one before it finished before this group's last Q K^T
+    // was issued); after the barrier both accumulators are final.
+    if (nt > st) {
+      const int last = st + 2 * ((nt - 1 - st) >> 1);
+      mbar_wait_bounded(&sm.pv_done[st], (unsigned)((last >> 1) & 1), a.status, &sm.abort);
+    }
+    sm.part[st][0][r] = m_ref;
+    sm.part[st][1][r] = m_true;
+    sm.part[st][2][r] = l;
+    tc::fence_before_sync();
+    named_barrier(1, kSoftmaxThreads);
+    tc::fence_after_sync();
+    const float m0 = sm.part[0][0][r], m1 = sm.part[1][0][r];
+    const float l0 = sm.part[0][2][r], l1 = sm.part[1][2][r];
+    const float mm = fmaxf(m0, m1);
+    const float c0 = (l0 > 0.f) ? ex2(m0 - mm) : 0.f;
+    const float c1 = (l1 > 0.f) ? ex2(m1 - mm) : 0.f;
+    const float l_row = l0 * c0 + l1 * c1;
+    const float inv = (l_row == 0.f) ? 0.f : 1.f / l_row;
+    const float w0 = c0 * inv, w1 = c1 * inv;
+    constexpr int kHalfD = D / 2;  // output columns per stream warpgroup
+    float* orow = a.out + qi * a.out_row_stride + (long long)h * D + st * kHalfD;
+#pragma unroll
+    for (int c = 0; c < kHalfD / 32; ++c) {
+      const int col = st * kHalfD + 32 * c;
+      uint32_t o0[32], o1[32];
+      if (nt > 0) {
+        tc::tmem_ld32(tmem + lane_base + kColO + col, o0);
+      }
+      if (nt > 1) {
+        tc::tmem_ld32(tmem + lane_base + kColO + D + col, o1);
+      }
+      tc::tmem_ld_wait();
+      if (nt > 0) tc::reg_fence(o0);
+      if (nt > 1) tc::reg_fence(o1);
+      if (row_ok) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          float v[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float x0 = nt > 0 ? __uint_as_float(o0[e + k]) * w0 : 0.f;
+            const float x1 = nt > 1 ? __uint_as_float(o1[e + k]) * w1 : 0.f;
+            v[k] = x0 + x1;
+          }
+          *reinterpret_cast<float4*>(orow + 32 * c + e) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+      }
+    }
+    if (st == 0 && row_ok && a.lse != nullptr) {
+      const float mt = fmaxf(sm.part[0][1][r], sm.part[1][1][r]);
+      float* l2 = a.lse + (qi * a.H + h) * 2;
+      const bool empty = (l_row == 0.f);
+      l2[0] = empty ? kEmptyLse : mt * kLn2;
+      l2[1] = empty ? kEmptyLse : logf(l_row) + (mm - mt) * kLn2;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+    tc::tmem_relinquish();
+  }
+}
+
+// fp32 -> bf16, n4 groups of four values (the source is 16-byte aligned).
+__global__ void __launch_bounds__(256) to_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
+                                                      long long n4) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    const float4 x = src[i];
+    dst[i] = make_uint2(tc::pack_bf16(x.x, x.y), tc::pack_bf16(x.z, x.w));
+  }
+}
+
+// V [rows][row_stride] fp32 -> V^T [cols][pad] bf16 (cols = G*D), zero for
+// rows >= rows.  32 x 32 tiles through shared memory; block (32, 8).
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const float* __restrict__ v, uint16_t* __restrict__ vt,
+                                                             long long rows, long long pad, long long row_stride,
+                                                             int cols) {
+  __shared__ float tile[32][33];
+  const long long t0 = (long long)blockIdx.x * 32;
+  const int c0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const long long t = t0 + i;
+    const int c = c0 + threadIdx.x;
+    tile[i][threadIdx.x] = (t < rows && c < cols) ? v[t * row_stride + c] : 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i;
+    const long long t = t0 + threadIdx.x;
+    if (c < cols && t < pad) {
+      const uint32_t w = tc::pack_bf16(tile[threadIdx.x][i], 0.f);
+      vt[(long long)c * pad + t] = (uint16_t)(w & 0xffffu);
+    }
+  }
+}
+
+template <int D>
+int launch_d(const FlashArgs& a, cudaStream_t s) {
+  const int gs = a.H / a.G;
+  const long long rows = (long long)a.n_q * gs;
+  const long long nb = (rows + kRows - 1) / kRows;
+  if (nb == 0) return 0;
+  // Rows of K/V any CTA may read: the largest window of the call.  Rows past
+  // it are outside the tensor maps and arrive as zeros.
+  long long kv_rows = a.causal ? a.base_pos + a.n_q : a.n_all;
+  if (kv_rows > a.cap) kv_rows = a.cap;
+  const bool no_keys = kv_rows < 1 || a.k == nullptr || a.v == nullptr;
+  if (kv_rows < 1) kv_rows = 1;
+  void* scratch = nullptr;
+  long long kv_pad = 64;
+  const void* kp = a.q;  // an empty key set never reads K/V: any aligned base will do
+  const void* vp = a.q;
+  if (!no_keys) {
+    // K and V as bf16 in stream-ordered temporary memory, released on the
+    // same stream once the attention kernel has run.  K keeps its layout; V
+    // is written transposed, V^T [G*D][kv_pad] with keys contiguous and the
+    // pad columns zero.
+    const long long elems = kv_rows * a.kv_row_stride;
+    kv_pad = (kv_rows + 63) / 64 * 64;
+    const long long vt_elems = (long long)a.G * D * kv_pad;
+    if (cudaMallocAsync(&scratch, (size_t)(elems + vt_elems) * 2, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    uint16_t* k16 = static_cast<uint16_t*>(scratch);
+    uint16_t* vt16 = k16 + elems;
+    to_bf16_kernel<<<4 * 152, 256, 0, s>>>(reinterpret_cast<const float4*>(a.k), reinterpret_cast<uint2*>(k16),
+                                           elems / 4);
+    const dim3 tgrid((unsigned)(kv_pad / 32), (unsigned)((a.G * D + 31) / 32));
+    transpose_bf16_kernel<<<tgrid, dim3(32, 8), 0, s>>>(a.v, vt16, kv_rows, kv_pad, a.kv_row_stride, a.G * D);
+    kp = k16;
+    vp = vt16;
+  }
+  CUtensorMap tm_k, tm_vt;
+  // K: [kv_rows][kv_row_stride] bf16, boxes of 64 elements x 128 keys.
+  const uint64_t kdims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
+  const uint64_t kstrides[1] = {(uint64_t)a.kv_row_stride * 2};
+  const uint32_t kbox[2] = {64, (uint32_t)kKeys};
+  // V^T: [G*D rows][kv_pad keys] bf16, boxes of 64 keys x D rows.
+  const uint64_t vdims[2] = {(uint64_t)kv_pad, (uint64_t)a.G * D};
+  const uint64_t vstrides[1] = {(uint64_t)kv_pad * 2};
+  const uint32_t vbox[2] = {64, (uint32_t)D};
+  const bool maps_ok = make_tmap(&tm_k, kp, 2, kdims, kstrides, kbox, true, kSwizzle128) &&
+                       make_tmap(&tm_vt, vp, 2, vdims, vstrides, vbox, true, kSwizzle128);
+  int rc = ATTN_OK;
+  if (!maps_ok) {
+    rc = ATTN_ERR_UNSUPPORTED;
+  } else {
+    const size_t smem = sizeof(PpSmem) + 1024;
+    auto kern = flash_bf16_kernel<D>;
+    if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) {
+      rc = ATTN_ERR_CUDA;
+    } else {
+      FlashArgs aa = a;
+      void* args[] = {&aa, &tm_k, &tm_vt};
+      if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s,
+                     args) != cudaSuccess)
+        rc = ATTN_ERR_CUDA;
+    }
+  }
+  if (scratch != nullptr && cudaFreeAsync(scratch, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+  return rc;
+}
+
+}  // namespace
+
+// Callers check flash_tc_supported(a, ATTN_BF16) first.
+int launch_flash_bf16(const FlashArgs& a, cudaStream_t s) {
+  return a.D == 128 ? launch_d<128>(a, s) : launch_d<64>(a, s);
+}
+
+}  // namespace attn

@@ -1,13 +1,14 @@
-// flash_tc.cu -- tcgen05 tensor-core flash attention (forward and prefill).
+// flash_tc.cu -- tcgen05 tensor-core flash attention with TF32 operands
+// (forward and prefill).
 //
 // Operation: softmax(scale * Q K^T) V over per-row causal / full / cross /
 // prefill windows, with the running max / sum of the pages' online softmax
 // (cera attention_prefill.wgsl, fn attention_prefill: per-tile max,
 // correction, exponentials, running sum; meganeura attention.wgsl, fn main:
 // the final (max, log sum) store).  Both contractions run on the 5th-generation
-// tensor cores with fp32 accumulation in tensor memory, with TF32 operands
-// (K/V tiles straight from the fp32 inputs) or bf16 operands (K/V converted
-// once per call by a small pre-pass; Q and P rounded on their way into TMEM).
+// tensor cores with fp32 accumulation in tensor memory and TF32 operands: the
+// K/V tiles come straight from the fp32 inputs.  (The bf16-operand kernel is
+// flash_bf16.cu.)
 //
 // One CTA owns 128 packed rows of one kv head g: row r is (query i, head
 // g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs
@@ -15,14 +16,14 @@
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: K tile (128 keys x D, 128-byte swizzle, K-major
-//               operand) and V tile (MN-major operand; TF32 needs the
-//               32-byte-atom swizzle, bf16 the plain 128-byte one) into a
-//               192 KB shared-memory ring: 3 tiles deep for TF32, 6 for bf16.
+//               operand) and V tile (MN-major operand, which for 32-bit
+//               elements needs the 128-byte swizzle of 32-byte atoms) into a
+//               192 KB shared-memory ring three tiles deep, in the order the
+//               MMAs consume them.
 //   warp 1      tensor-memory allocation; one thread issues every MMA:
 //                 S_b = Q K_j^T      (A = Q in TMEM, B = K tile)      M=128 N=128
 //                 O  += P_j V_j      (A = P in TMEM over S_b, B = V)  M=128 N=D
-//               The issuer is greedy: it issues whichever of the next Q K^T
-//               and the next P V has its inputs ready.
+//               in the fixed order Q K_0, Q K_1, P V_0, Q K_2, P V_1, ...
 //   warps 4-11  softmax, two warpgroups: warp w of group c handles rows
 //               32(w%4)..+31 (TMEM lanes) and score columns 64c..64c+63.  The
 //               two halves of a row swap their tile max through shared
@@ -77,32 +78,17 @@ __device__ __forceinline__ uint32_t tf32_round(float x) {
   return r;
 }
 
-// Two floats as round-to-nearest bf16 in one word: lo in bits 0-15.
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// BF = false: TF32 operands (fp32 K/V tiles straight from the inputs).
-// BF = true: bf16 operands (K/V already converted to bf16; Q and P rounded to
-// bf16 on their way into tensor memory, two values per 32-bit column).
-template <int D, bool BF>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_tc_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v) {
-  constexpr int kEpr = BF ? 64 : 32;           // elements per 128-byte row
+  constexpr int kEpr = 32;                     // elements per 128-byte row
   constexpr int kChunks = D / kEpr;            // 128-byte column chunks of a K/V row
   constexpr int kChunkBytes = kKeys * 128;     // one TMA box: 128 keys x 128 bytes
   constexpr int kTileBytes = kChunks * kChunkBytes;
   constexpr int kRing = kRingBytes / kTileBytes;  // tiles in flight
   static_assert(kRing <= kMaxRing, "ring barriers");
-  constexpr int kKStep = BF ? 16 : 8;          // MMA K per instruction (32 bytes)
-  // V operand form.  The bf16 path reads V^T (keys contiguous), written by the
-  // pre-pass, as a K-major operand: an MN-major V measured about twice as slow
-  // in P V as the same-size K-major Q K^T.
-  constexpr bool kVT = BF;
-  constexpr int kVtChunkBytes = D * 128;       // one V^T box: D rows x 128 bytes of keys
+  constexpr int kKStep = 8;                    // MMA K per instruction (32 bytes)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
@@ -154,23 +140,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && nt > 0) {
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      // Tile idx: K_(idx/2) for even idx, V_(idx/2) for odd; ring slot idx % kRing.
-      for (int idx = 0; idx < 2 * nt; ++idx) {
-        const int s = idx % kRing, use = idx / kRing;
+      // Copies go out in the order the MMA issuer consumes the tiles: K_0,
+      // K_1, V_0, K_2, V_1, ..., K_(nt-1), V_(nt-2), V_(nt-1).  Ring slot
+      // p % kRing holds copy p; it is refilled once its consumer completes.
+      for (int p = 0; p < 2 * nt; ++p) {
+        const int s = p % kRing, use = p / kRing;
         unsigned char* dst = sm.ring + s * kTileBytes;
         if (use >= 1) mbar_wait_bounded(&sm.kv_empty[s], (unsigned)((use - 1) & 1), a.status, &sm.abort);
         mbar_arrive_expect_tx(&sm.kv_full[s], (unsigned)kTileBytes);
-        const int t0 = kKeys * (idx >> 1);
-        if ((idx & 1) && kVT) {
-          // V^T tile: kKeys / kEpr boxes of [D rows (d) x 128 bytes of keys].
+        const bool is_v = (p == 2 * nt - 1) || (p > 0 && (p & 1) == 0);
+        const int t0 = kKeys * (is_v ? (p == 2 * nt - 1 ? nt - 1 : p / 2 - 1) : (p + 1) / 2);
+        const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
 #pragma unroll
-          for (int c = 0; c < kKeys / kEpr; ++c)
-            tma_load_2d(dst + c * kVtChunkBytes, &tm_v, t0 + kEpr * c, g * D, &sm.kv_full[s]);
-        } else {
-          const CUtensorMap* tm = (idx & 1) ? &tm_v : &tm_k;
-#pragma unroll
-          for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + kEpr * c, t0, &sm.kv_full[s]);
-        }
+        for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + kEpr * c, t0, &sm.kv_full[s]);
       }
       // No copy may still be landing in shared memory when the CTA exits
       // (normally every fill was already consumed, so these return at once).
@@ -182,77 +164,76 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nt > 0) {
-      constexpr uint32_t kFmt = BF ? tc::kFmtBF16 : tc::kFmtTF32;
-      constexpr uint32_t idesc_qk = tc::idesc_f32acc(kFmt, false, kRows, kKeys);
-      constexpr uint32_t idesc_pv = tc::idesc_f32acc(kFmt, !kVT, kRows, D);
-      // V (MN-major B): TF32 needs the 32-byte-atom layout with 4-row K groups;
-      // bf16 uses the plain 128-byte swizzle with 8-row groups.
-      constexpr uint32_t kVLayout = BF ? tc::kLayoutSw128 : tc::kLayoutSw128Atom32;
-      constexpr uint32_t kVSbo = BF ? 1024 : 512;
+      constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtTF32, false, kRows, kKeys);
+      constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtTF32, true, kRows, D);
+      // V (MN-major B): the 32-byte-atom layout, 4-row K groups 512 bytes apart.
       constexpr uint32_t kVStep = kKStep * 128;  // bytes of V rows per K step
+      // One descriptor per operand form at the ring's base; an operand at byte
+      // offset off is that descriptor plus off >> 4 (the start-address field;
+      // shared-memory offsets stay far below its 14-bit range).
       const uint32_t ring0 = smem_u32(sm.ring);
-      mbar_wait_bounded(&sm.q_ready, 0, a.status, &sm.abort);
-      tc::fence_after_sync();
-      auto tile_addr = [&](int idx) { return ring0 + (uint32_t)((idx % kRing) * kTileBytes); };
-      auto full_ready = [&](int idx) {
-        return mbar_test_wait(&sm.kv_full[idx % kRing], (unsigned)((idx / kRing) & 1));
+      const uint64_t dk0 = tc::sdesc_sw128(ring0, 16, 1024);
+      const uint64_t dv0 = tc::sdesc_sw128(ring0, kChunkBytes, 512, tc::kLayoutSw128Atom32);
+      auto slot_off = [&](int p) { return (uint64_t)(((p % kRing) * kTileBytes) >> 4); };
+      auto wait = [&](uint64_t* bar, int phase) {
+        return mbar_wait_bounded(bar, (unsigned)(phase & 1), a.status, &sm.abort);
       };
-      auto release = [&](int idx) { tc::commit(&sm.kv_empty[idx % kRing]); };
-      int nq = 0, np = 0;  // next Q K^T and next P V to issue
-      unsigned long long t_idle = 0;
-      while (np < nt) {
-        // Q K^T for tile nq writes S buffer nq % kSBuf, last read by P V of tile nq - kSBuf.
-        const bool qk_ok =
-            nq < nt && nq < np + kSBuf &&
-            (nq < kSBuf || mbar_test_wait(&sm.pv_done[nq % kSBuf], (unsigned)(((nq - kSBuf) / kSBuf) & 1))) &&
-            full_ready(2 * nq);
-        const bool pv_ok = !qk_ok && nq > np &&
-                           mbar_test_wait(&sm.p_ready[np % kSBuf], (unsigned)((np / kSBuf) & 1)) &&
-                           full_ready(2 * np + 1);
-        if (qk_ok) {
-          const int b = nq % kSBuf;
-          tc::fence_after_sync();
-          const uint32_t kb = tile_addr(2 * nq);
+      // Ring positions of K_j and V_j (the copy order above).
+      auto k_pos = [&](int j) { return j == 0 ? 0 : 2 * j - 1; };
+      auto v_pos = [&](int j) { return j == nt - 1 ? 2 * nt - 1 : 2 * j + 2; };
+      // S_(j%2) = Q K_j^T; it overwrites the P that P V of tile j-2 reads.
+      auto issue_qk = [&](int j) {
+        const int p = k_pos(j), b = j % kSBuf;
+        if (!wait(&sm.kv_full[p % kRing], p / kRing)) return false;
+        if (j >= kSBuf && !wait(&sm.pv_done[b], (j - kSBuf) / kSBuf)) return false;
+        tc::fence_after_sync();
+        const uint64_t dk = dk0 + slot_off(p);
+        const uint32_t ds = tmem + kColS0 + kKeys * b;
+        // Four K steps (32 bytes each) per 128-byte chunk of the K tile; Q
+        // takes 8 TMEM columns per step.
 #pragma unroll
-          for (int kk = 0; kk < D / kKStep; ++kk) {
-            const uint64_t bdesc = tc::sdesc_sw128(kb + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
-            if constexpr (BF)
-              tc::mma_f16_ts(tmem + kColS0 + kKeys * b, tmem + kColQ + 8 * kk, bdesc, idesc_qk, kk > 0);
-            else
-              tc::mma_tf32_ts(tmem + kColS0 + kKeys * b, tmem + kColQ + 8 * kk, bdesc, idesc_qk, kk > 0);
-          }
-          tc::commit(&sm.s_full[b]);
-          release(2 * nq);
-          ++nq;
-          t_idle = 0;
-        } else if (pv_ok) {
-          const int b = np % kSBuf;
-          tc::fence_after_sync();
-          const uint32_t vb = tile_addr(2 * np + 1);
-#pragma unroll
-          for (int kk = 0; kk < kKeys / kKStep; ++kk) {
-            const uint64_t bdesc =
-                kVT ? tc::sdesc_sw128(vb + (kk >> 2) * kVtChunkBytes + (kk & 3) * 32, 16, 1024)
-                    : tc::sdesc_sw128(vb + kk * kVStep, kChunkBytes, kVSbo, kVLayout);
-            if constexpr (BF)
-              tc::mma_f16_ts(tmem + kColO, tmem + kColS0 + kKeys * b + 8 * kk, bdesc, idesc_pv, (np > 0 || kk > 0));
-            else
-              tc::mma_tf32_ts(tmem + kColO, tmem + kColS0 + kKeys * b + 8 * kk, bdesc, idesc_pv, (np > 0 || kk > 0));
-          }
-          tc::commit(&sm.pv_done[b]);
-          release(2 * np + 1);
-          ++np;
-          t_idle = 0;
-        } else {
-          const unsigned long long now = globaltimer_ns();
-          if (t_idle == 0) t_idle = now;
-          if (*reinterpret_cast<volatile int*>(&sm.abort) != 0) break;
-          if (now - t_idle > kWaitLimitNs) {
-            record_status(a.status, ATTN_ERR_TIMEOUT);
-            *reinterpret_cast<volatile int*>(&sm.abort) = 1;
-            break;
-          }
+        for (int c4 = 0; c4 < kChunks; ++c4) {
+          const uint64_t c = (uint64_t)((c4 * kChunkBytes) >> 4);
+          const uint32_t qa = tmem + kColQ + 32 * c4;
+          tc::mma4_tf32_ts(ds, qa, qa + 8, qa + 16, qa + 24, dk + c, dk + c + 2, dk + c + 4, dk + c + 6, idesc_qk,
+                           c4 > 0 ? 1u : 0u);
         }
+        tc::commit(&sm.s_full[b]);
+        tc::commit(&sm.kv_empty[p % kRing]);
+        return true;
+      };
+      // O += P_j V_j once both softmax groups have written P_j.
+      auto issue_pv = [&](int j) {
+        const int p = v_pos(j), b = j % kSBuf;
+        if (!wait(&sm.kv_full[p % kRing], p / kRing)) return false;
+        if (!wait(&sm.p_ready[b], j / kSBuf)) return false;
+        tc::fence_after_sync();
+        const uint64_t dv = dv0 + slot_off(p);
+        const uint32_t dp = tmem + kColS0 + kKeys * b;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+        for (int c4 = 0; c4 < kKeys / kKStep / 4; ++c4) {
+          // K steps 4 c4 .. 4 c4 + 3; P takes 8 TMEM columns per step.
+          const uint32_t pa = dp + 32 * c4;
+          constexpr uint64_t st = kVStep >> 4;  // V rows of one K step
+          const uint64_t c = 4 * st * c4;
+          tc::mma4_tf32_ts(tmem + kColO, pa, pa + 8, pa + 16, pa + 24, dv + c, dv + c + st, dv + c + 2 * st,
+                           dv + c + 3 * st, idesc_pv, c4 > 0 ? 1u : acc0);
+        }
+        tc::commit(&sm.pv_done[b]);
+        tc::commit(&sm.kv_empty[p % kRing]);
+        return true;
+      };
+      // Fixed order Q K_0, Q K_1, P V_0, Q K_2, P V_1, ...: Q K of the next
+      // tile runs while the softmax of the current one does.  Every wait
+      // blocks in hardware (a loop of test-waits competes with the tensor
+      // core for shared memory and notices completions late).
+      bool ok = wait(&sm.q_ready, 0);
+      tc::fence_after_sync();
+      ok = ok && issue_qk(0) && (nt < 2 || issue_qk(1));
+      for (int j = 0; ok && j < nt; ++j) {
+        ok = issue_pv(j);
+        if (ok && j + 2 < nt) ok = issue_qk(j + 2);
       }
       // Every MMA has finished before tensor memory is released.
       tc::commit(&sm.drain);
@@ -271,35 +252,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = qi < a.n_q;
     const float sl2 = a.scale * kLog2e;
 
-    // Q row -> TMEM (pre-scaled); rows past n_q are zero.  TF32: one value per
-    // column; bf16: two per column (lower index in the low half).  Each group
-    // stores half the row, unless half is under one 32-column store (bf16,
-    // D = 64): then group 0 stores the whole row.
+    // Q row -> TMEM (pre-scaled), one value per column; each group stores half
+    // the row.  Rows past n_q are zero.
     {
-      constexpr int kPer = BF ? 2 : 1;
-      constexpr int kQAll = D / kPer;          // TMEM columns of a Q row
-      constexpr bool kSplitQ = kQAll >= 64;
-      constexpr int kQCols = kSplitQ ? kQAll / 2 : kQAll;
-      const int q_grp = kSplitQ ? grp : 0;
-      const int n_chunks = (kSplitQ || grp == 0) ? kQCols / 32 : 0;
-      const float* qrow = a.q + qi * a.q_row_stride + (long long)h * D + q_grp * kQCols * kPer;
-      for (int c = 0; c < n_chunks; ++c) {
+      constexpr int kQCols = D / 2;
+      const float* qrow = a.q + qi * a.q_row_stride + (long long)h * D + grp * kQCols;
+#pragma unroll
+      for (int c = 0; c < kQCols / 32; ++c) {
         uint32_t v[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4 / kPer) {
-          const float* src = qrow + kPer * (32 * c + e);
-          const float4 x = row_ok ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
-          if constexpr (BF) {
-            v[e] = pack_bf16(x.x * sl2, x.y * sl2);
-            v[e + 1] = pack_bf16(x.z * sl2, x.w * sl2);
-          } else {
-            v[e] = __float_as_uint(x.x * sl2);
-            v[e + 1] = __float_as_uint(x.y * sl2);
-            v[e + 2] = __float_as_uint(x.z * sl2);
-            v[e + 3] = __float_as_uint(x.w * sl2);
-          }
+        for (int e = 0; e < 32; e += 4) {
+          const float4 x = row_ok ? *reinterpret_cast<const float4*>(qrow + 32 * c + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[e] = __float_as_uint(x.x * sl2);
+          v[e + 1] = __float_as_uint(x.y * sl2);
+          v[e + 2] = __float_as_uint(x.z * sl2);
+          v[e + 3] = __float_as_uint(x.w * sl2);
         }
-        tc::tmem_st32(tmem + lane_base + kColQ + q_grp * kQCols + 32 * c, v);
+        tc::tmem_st32(tmem + lane_base + kColQ + grp * kQCols + 32 * c, v);
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();
@@ -346,35 +315,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       float sm4[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (BF) {
-        // P as bf16 pairs into the first half of this buffer's columns: this
-        // group's 64 values become 32 columns at offset 32 * grp.  Both groups
-        // finished reading S before the max exchange above.
-        uint32_t pk[32];
-        static_assert(kCC * 16 == 32, "one 32-column P store per group");
 #pragma unroll
-        for (int c = 0; c < kCC; ++c)
+      for (int c = 0; c < kCC; ++c) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float p0 = ex2(__uint_as_float(s[c][e]) - m_use);
-            const float p1 = ex2(__uint_as_float(s[c][e + 1]) - m_use);
-            const uint32_t w = pack_bf16(p0, p1);
-            sm4[e & 3] += __uint_as_float(w << 16);
-            sm4[(e + 1) & 3] += __uint_as_float(w & 0xffff0000u);
-            pk[16 * c + e / 2] = w;
-          }
-        tc::tmem_st32(tmem + lane_base + kColS0 + kKeys * b + 32 * grp, pk);
-      } else {
-#pragma unroll
-        for (int c = 0; c < kCC; ++c) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const uint32_t p = tf32_round(ex2(__uint_as_float(s[c][e]) - m_use));
-            sm4[e & 3] += __uint_as_float(p);
-            s[c][e] = p;
-          }
-          tc::tmem_st32(s_col + 32 * c, s[c]);
+        for (int e = 0; e < 32; ++e) {
+          const uint32_t p = tf32_round(ex2(__uint_as_float(s[c][e]) - m_use));
+          sm4[e & 3] += __uint_as_float(p);
+          s[c][e] = p;
         }
+        tc::tmem_st32(s_col + 32 * c, s[c]);
       }
       l = l * corr + ((sm4[0] + sm4[1]) + (sm4[2] + sm4[3]));
       tc::tmem_st_wait();
@@ -450,42 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// fp32 -> bf16, n4 groups of four values (the source is 16-byte aligned).
-__global__ void __launch_bounds__(256) to_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
-                                                      long long n4) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
-    const float4 x = src[i];
-    dst[i] = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
-  }
-}
-
-// V [rows][row_stride] fp32 -> V^T [cols][pad] bf16 (cols = G*D), zero for
-// rows >= rows.  32 x 32 tiles through shared memory; block (32, 8).
-__global__ void __launch_bounds__(256) transpose_bf16_kernel(const float* __restrict__ v, uint16_t* __restrict__ vt,
-                                                             long long rows, long long pad, long long row_stride,
-                                                             int cols) {
-  __shared__ float tile[32][33];
-  const long long t0 = (long long)blockIdx.x * 32;
-  const int c0 = blockIdx.y * 32;
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const long long t = t0 + i;
-    const int c = c0 + threadIdx.x;
-    tile[i][threadIdx.x] = (t < rows && c < cols) ? v[t * row_stride + c] : 0.f;
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int c = c0 + i;
-    const long long t = t0 + threadIdx.x;
-    if (c < cols && t < pad) {
-      const uint32_t w = pack_bf16(tile[threadIdx.x][i], 0.f);
-      vt[(long long)c * pad + t] = (uint16_t)(w & 0xffffu);
-    }
-  }
-}
-
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
-template <int D, bool BF>
+template <int D>
 int launch_d(const FlashArgs& a, cudaStream_t s) {
   const int gs = a.H / a.G;
   const long long rows = (long long)a.n_q * gs;
@@ -497,65 +413,25 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   if (kv_rows > a.cap) kv_rows = a.cap;
   const bool no_keys = kv_rows < 1 || a.k == nullptr || a.v == nullptr;
   if (kv_rows < 1) kv_rows = 1;
+  // An empty key set never reads K/V: any aligned base will do.
+  const void* kp = no_keys ? static_cast<const void*>(a.q) : a.k;
+  const void* vp = no_keys ? static_cast<const void*>(a.q) : a.v;
   CUtensorMap tm_k, tm_v;
   const uint64_t dims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
-  const uint32_t box[2] = {(uint32_t)(BF ? 64 : 32), (uint32_t)kKeys};
-  void* scratch = nullptr;
-  long long kv_pad = 64;
-  const void* kp = a.q;  // an empty key set never reads K/V: any aligned base will do
-  const void* vp = a.q;
-  if (!no_keys) {
-    if constexpr (BF) {
-      // K and V as bf16 in stream-ordered temporary memory, released on the
-      // same stream once the attention kernel has run.
-      // K keeps its layout; V is written transposed, V^T [G*D][kv_pad] with
-      // keys contiguous and the pad columns zero.
-      const long long elems = kv_rows * a.kv_row_stride;
-      kv_pad = (kv_rows + 63) / 64 * 64;
-      const long long vt_elems = (long long)a.G * D * kv_pad;
-      if (cudaMallocAsync(&scratch, (size_t)(elems + vt_elems) * 2, s) != cudaSuccess) return ATTN_ERR_CUDA;
-      uint16_t* k16 = static_cast<uint16_t*>(scratch);
-      uint16_t* vt16 = k16 + elems;
-      to_bf16_kernel<<<4 * 152, 256, 0, s>>>(reinterpret_cast<const float4*>(a.k), reinterpret_cast<uint2*>(k16),
-                                             elems / 4);
-      const dim3 tgrid((unsigned)(kv_pad / 32), (unsigned)((a.G * D + 31) / 32));
-      transpose_bf16_kernel<<<tgrid, dim3(32, 8), 0, s>>>(a.v, vt16, kv_rows, kv_pad, a.kv_row_stride, a.G * D);
-      kp = k16;
-      vp = vt16;
-    } else {
-      kp = a.k;
-      vp = a.v;
-    }
-  }
-  const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * (BF ? 2 : 4)};
-  bool maps_ok = make_tmap(&tm_k, kp, 2, dims, strides, box, BF, kSwizzle128);
-  if (BF) {
-    // V^T: [G*D rows][kv_pad keys], boxes of 64 keys x D rows.
-    const uint64_t vdims[2] = {(uint64_t)kv_pad, (uint64_t)a.G * D};
-    const uint64_t vstrides[1] = {(uint64_t)kv_pad * 2};
-    const uint32_t vbox[2] = {64, (uint32_t)D};
-    maps_ok = maps_ok && make_tmap(&tm_v, vp, 2, vdims, vstrides, vbox, true, kSwizzle128);
-  } else {
-    maps_ok = maps_ok && make_tmap(&tm_v, vp, 2, dims, strides, box, false, kSwizzle128Atom32);
-  }
-  int rc = ATTN_OK;
-  if (!maps_ok) {
-    rc = ATTN_ERR_UNSUPPORTED;
-  } else {
-    const size_t smem = sizeof(TcSmem) + 1024;
-    auto kern = flash_tc_kernel<D, BF>;
-    if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) {
-      rc = ATTN_ERR_CUDA;
-    } else {
-      FlashArgs aa = a;
-      void* args[] = {&aa, &tm_k, &tm_v};
-      if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s,
-                     args) != cudaSuccess)
-        rc = ATTN_ERR_CUDA;
-    }
-  }
-  if (scratch != nullptr && cudaFreeAsync(scratch, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
-  return rc;
+  const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * 4};
+  const uint32_t box[2] = {32, (uint32_t)kKeys};
+  if (!make_tmap(&tm_k, kp, 2, dims, strides, box, false, kSwizzle128) ||
+      !make_tmap(&tm_v, vp, 2, dims, strides, box, false, kSwizzle128Atom32))
+    return ATTN_ERR_UNSUPPORTED;
+  const size_t smem = sizeof(TcSmem) + 1024;
+  auto kern = flash_tc_kernel<D>;
+  if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
+  FlashArgs aa = a;
+  void* args[] = {&aa, &tm_k, &tm_v};
+  if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s, args) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
 }
 
 }  // namespace
@@ -577,8 +453,8 @@ bool flash_tc_supported(const FlashArgs& a, int prec) {
 
 int launch_flash_tc(const FlashArgs& a, int prec, cudaStream_t s) {
   if (!flash_tc_supported(a, prec)) return ATTN_ERR_UNSUPPORTED;
-  if (prec == ATTN_BF16) return a.D == 128 ? launch_d<128, true>(a, s) : launch_d<64, true>(a, s);
-  return a.D == 128 ? launch_d<128, false>(a, s) : launch_d<64, false>(a, s);
+  if (prec == ATTN_BF16) return launch_flash_bf16(a, s);
+  return a.D == 128 ? launch_d<128>(a, s) : launch_d<64>(a, s);
 }
 
 }  // namespace attn

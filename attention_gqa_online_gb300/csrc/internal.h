@@ -60,6 +60,9 @@ int launch_flash_simt(const FlashArgs& a, cudaStream_t s);
 // tcgen05 tensor-core flash kernel (prec = ATTN_TF32 or ATTN_BF16).
 bool flash_tc_supported(const FlashArgs& a, int prec);
 int launch_flash_tc(const FlashArgs& a, int prec, cudaStream_t s);
+// bf16-operand kernel (flash_bf16.cu); the caller has checked
+// flash_tc_supported(a, ATTN_BF16).
+int launch_flash_bf16(const FlashArgs& a, cudaStream_t s);
 
 // Split-KV decode.
 struct DecodeArgs {

@@ -97,6 +97,42 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Four MMAs into one accumulator in a single block: D (+)= A_i * B_i^T for
+// i = 0..3, the first accumulating iff `accumulate` != 0, the others always.
+// An issuing thread that shares its SM sub-partition with busy warps gets few
+// issue slots, so the instructions between MMAs are kept to a minimum (the
+// descriptors arrive precomputed).
+#define ATTN_MMA4(KIND, AFORM)                                                                              \
+  asm volatile(                                                                                             \
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, %10, %10;\n\t"                  \
+      "tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(1) ", %5, %9, p;\n\t"                           \
+      "tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(2) ", %6, %9, t;\n\t"                           \
+      "tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(3) ", %7, %9, t;\n\t"                           \
+      "tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(4) ", %8, %9, t;\n\t}"
+#define ATTN_A_DESC(i) "%" #i
+#define ATTN_A_TMEM(i) "[%" #i "]"
+__device__ __forceinline__ void mma4_f16_ss(uint32_t d, uint64_t a0, uint64_t a1, uint64_t a2, uint64_t a3, uint64_t b0,
+                                            uint64_t b1, uint64_t b2, uint64_t b3, uint32_t idesc, uint32_t accumulate) {
+  ATTN_MMA4("f16", ATTN_A_DESC)::"r"(d), "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3),
+      "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma4_f16_ts(uint32_t d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint64_t b0,
+                                            uint64_t b1, uint64_t b2, uint64_t b3, uint32_t idesc, uint32_t accumulate) {
+  ATTN_MMA4("f16", ATTN_A_TMEM)::"r"(d), "r"(a0), "r"(a1), "r"(a2), "r"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3),
+      "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma4_tf32_ts(uint32_t d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint64_t b0,
+                                             uint64_t b1, uint64_t b2, uint64_t b3, uint32_t idesc, uint32_t accumulate) {
+  ATTN_MMA4("tf32", ATTN_A_TMEM)::"r"(d), "r"(a0), "r"(a1), "r"(a2), "r"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3),
+      "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+#undef ATTN_A_TMEM
+#undef ATTN_A_DESC
+#undef ATTN_MMA4
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
@@ -126,6 +162,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       ATTN_W8(0), ATTN_W8(8), ATTN_W8(16), ATTN_W8(24)
       : "memory");
 }
+// The first 16 of v into 16 consecutive columns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      ATTN_W8(0), ATTN_W8(8)
+      : "memory");
+}
 #undef ATTN_W8
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // After tmem_ld_wait(): ties the loaded registers to that point, so no use of
@@ -137,6 +181,14 @@ __device__ __forceinline__ void reg_fence(uint32_t (&v)[32]) {
 }
 #undef ATTN_F8
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- bf16 packing
+// Two floats as round-to-nearest-even bf16 in one word: lo in bits 0-15.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
 }  // namespace tc
 }  // namespace attn
