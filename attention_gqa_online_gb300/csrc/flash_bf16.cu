@@ -65,21 +65,6 @@ struct __align__(1024) PpSmem {
   int abort;
 };
 
-// Three-way max (one instruction on this architecture).
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// (a0, a1) += (b0, b1) as one paired fp32 add.
-__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 x, y;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
-      "add.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
-      : "+f"(a0), "+f"(a1)
-      : "f"(b0), "f"(b1));
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_bf16_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
@@ -177,8 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one thread alone leaves the tensor core idle for every wait and every
     // bookkeeping step between its groups; with one issuer per stream, one
     // stream's products run while the other's issuer waits.
+    // The whole warp runs the issue loop (warp-uniform values); one elected
+    // lane issues each MMA and commit.
     const int st = warp - 1;
-    if (lane == 0 && nt > st) {
+    if (nt > st) {
       constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, kKeys);
       constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, D);
       // Every operand here is K-major with the 128-byte swizzle and 1024-byte
@@ -191,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t d_o = tmem + kColO + D * st;      // O_st
       auto tile_desc = [&](int p) { return dring + (uint64_t)(((p % kRing) * kTileBytes) >> 4); };
       auto wait = [&](uint64_t* bar, int phase) {
-        return mbar_wait_bounded(bar, (unsigned)(phase & 1), a.status, &sm.abort);
+        return __all_sync(0xffffffffu, mbar_wait_bounded(bar, (unsigned)(phase & 1), a.status, &sm.abort));
       };
       bool ok = wait(&sm.q_ready, 0);
       tc::fence_after_sync();
@@ -211,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma4_f16_ss(ds, dq + c, dq + c + 2, dq + c + 4, dq + c + 6, dk + c, dk + c + 2, dk + c + 4, dk + c + 6,
                           idesc_qk, c4 > 0 ? 1u : 0u);
         }
-        tc::commit(&sm.s_full[st]);
-        tc::commit(&sm.kv_empty[pk % kRing]);
+        tc::commit_elect(&sm.s_full[st]);
+        tc::commit_elect(&sm.kv_empty[pk % kRing]);
         // O_st += P_j V_j once the softmax group has written P_j.
         ok = wait(&sm.p_ready[st], j >> 1) && wait(&sm.kv_full[pv % kRing], pv / kRing);
         if (!ok) break;
@@ -226,11 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma4_f16_ts(d_o, pa, pa + 8, pa + 16, pa + 24, dv + c, dv + c + 2, dv + c + 4, dv + c + 6, idesc_pv,
                           c4 > 0 ? 1u : acc0);
         }
-        tc::commit(&sm.pv_done[st]);
-        tc::commit(&sm.kv_empty[pv % kRing]);
+        tc::commit_elect(&sm.pv_done[st]);
+        tc::commit_elect(&sm.kv_empty[pv % kRing]);
       }
       // Every MMA has finished before tensor memory is released.
-      tc::commit(&sm.drain[st]);
+      tc::commit_elect(&sm.drain[st]);
       mbar_wait_bounded(&sm.drain[st], 0, a.status);
     }
   } else if (warp >= 4) {

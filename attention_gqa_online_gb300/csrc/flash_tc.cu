@@ -72,12 +72,6 @@ struct __align__(1024) TcSmem {
   int abort;
 };
 
-__device__ __forceinline__ uint32_t tf32_round(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_tc_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
@@ -163,7 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nt > 0) {
+    // The whole warp runs the issue loop (warp-uniform values); one elected
+    // lane issues each MMA and commit.
+    if (nt > 0) {
       constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtTF32, false, kRows, kKeys);
       constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtTF32, true, kRows, D);
       // V (MN-major B): the 32-byte-atom layout, 4-row K groups 512 bytes apart.
@@ -176,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv0 = tc::sdesc_sw128(ring0, kChunkBytes, 512, tc::kLayoutSw128Atom32);
       auto slot_off = [&](int p) { return (uint64_t)(((p % kRing) * kTileBytes) >> 4); };
       auto wait = [&](uint64_t* bar, int phase) {
-        return mbar_wait_bounded(bar, (unsigned)(phase & 1), a.status, &sm.abort);
+        return __all_sync(0xffffffffu, mbar_wait_bounded(bar, (unsigned)(phase & 1), a.status, &sm.abort));
       };
       // Ring positions of K_j and V_j (the copy order above).
       auto k_pos = [&](int j) { return j == 0 ? 0 : 2 * j - 1; };
@@ -198,8 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma4_tf32_ts(ds, qa, qa + 8, qa + 16, qa + 24, dk + c, dk + c + 2, dk + c + 4, dk + c + 6, idesc_qk,
                            c4 > 0 ? 1u : 0u);
         }
-        tc::commit(&sm.s_full[b]);
-        tc::commit(&sm.kv_empty[p % kRing]);
+        tc::commit_elect(&sm.s_full[b]);
+        tc::commit_elect(&sm.kv_empty[p % kRing]);
         return true;
       };
       // O += P_j V_j once both softmax groups have written P_j.
@@ -220,8 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma4_tf32_ts(tmem + kColO, pa, pa + 8, pa + 16, pa + 24, dv + c, dv + c + st, dv + c + 2 * st,
                            dv + c + 3 * st, idesc_pv, c4 > 0 ? 1u : acc0);
         }
-        tc::commit(&sm.pv_done[b]);
-        tc::commit(&sm.kv_empty[p % kRing]);
+        tc::commit_elect(&sm.pv_done[b]);
+        tc::commit_elect(&sm.kv_empty[p % kRing]);
         return true;
       };
       // Fixed order Q K_0, Q K_1, P V_0, Q K_2, P V_1, ...: Q K of the next
@@ -236,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && j + 2 < nt) ok = issue_qk(j + 2);
       }
       // Every MMA has finished before tensor memory is released.
-      tc::commit(&sm.drain);
+      tc::commit_elect(&sm.drain);
       mbar_wait_bounded(&sm.drain, 0, a.status);
     }
   } else if (warp >= 4) {
@@ -291,20 +287,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kCC; ++c) tc::reg_fence(s[c]);
 
-      // Mask and this half's max (four independent chains).
-      const bool masked = (j + 1) * kKeys > n_min;
-      const int col0 = j * kKeys + kCols * grp;
+      // Mask (only a tile that crosses some row's window end) and this
+      // half's max.
+      if ((j + 1) * kKeys > n_min) {
+        const int lim = n_r - (j * kKeys + kCols * grp);
+#pragma unroll
+        for (int c = 0; c < kCC; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
+      }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < kCC; ++c)
+      for (int i = 0; i < kCols; i += 8)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(s[c][e]);
-          if (masked && (col0 + 32 * c + e) >= n_r) x = -INFINITY;
-          s[c][e] = __float_as_uint(x);
-          mx[e & 3] = fmaxf(mx[e & 3], x);
-        }
-      sm.red_max[j & 1][grp][r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        for (int k = 0; k < 4; ++k)
+          mx[k] = max3(mx[k], __uint_as_float(s[i >> 5][(i & 31) + 2 * k]), __uint_as_float(s[i >> 5][(i & 31) + 2 * k + 1]));
+      sm.red_max[j & 1][grp][r] = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       named_barrier(1, kSoftmaxThreads);
       const float tmax = fmaxf(sm.red_max[j & 1][0][r], sm.red_max[j & 1][1][r]);
       m_true = fmaxf(m_true, tmax);
@@ -313,19 +312,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         corr = ex2(m_ref - tmax);              // m_ref = -inf gives 0
         m_ref = tmax;
       }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float sm4[4] = {0.f, 0.f, 0.f, 0.f};
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      // P = 2^(S - m) in place.  The tensor core reads its 32-bit operands as
+      // TF32 (the low 13 mantissa bits dropped), so P is stored unrounded; the
+      // row sum is taken over the unrounded values.
+      float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kCC; ++c) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const uint32_t p = tf32_round(ex2(__uint_as_float(s[c][e]) - m_use));
-          sm4[e & 3] += __uint_as_float(p);
-          s[c][e] = p;
+        for (int e = 0; e < 32; e += 2) {
+          float x0 = __uint_as_float(s[c][e]), x1 = __uint_as_float(s[c][e + 1]);
+          add2(x0, x1, neg_m, neg_m);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          const int k = (e >> 1) & 3;
+          add2(sum[2 * k], sum[2 * k + 1], p0, p1);
+          s[c][e] = __float_as_uint(p0);
+          s[c][e + 1] = __float_as_uint(p1);
         }
         tc::tmem_st32(s_col + 32 * c, s[c]);
       }
-      l = l * corr + ((sm4[0] + sm4[1]) + (sm4[2] + sm4[3]));
+      l = l * corr + (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
       tc::tmem_st_wait();
 
       // O was accumulated against the old reference: rescale this group's half

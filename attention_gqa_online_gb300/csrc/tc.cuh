@@ -99,16 +99,18 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
 }
 // Four MMAs into one accumulator in a single block: D (+)= A_i * B_i^T for
 // i = 0..3, the first accumulating iff `accumulate` != 0, the others always.
-// An issuing thread that shares its SM sub-partition with busy warps gets few
-// issue slots, so the instructions between MMAs are kept to a minimum (the
-// descriptors arrive precomputed).
+// The whole warp executes the block with warp-uniform operands and one
+// elected lane issues the MMAs.  An issuing warp that shares its SM
+// sub-partition with busy warps gets few issue slots, so the instructions
+// around each MMA are kept to a minimum.
 #define ATTN_MMA4(KIND, AFORM)                                                                              \
   asm volatile(                                                                                             \
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, %10, %10;\n\t"                  \
-      "tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(1) ", %5, %9, p;\n\t"                           \
-      "tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(2) ", %6, %9, t;\n\t"                           \
-      "tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(3) ", %7, %9, t;\n\t"                           \
-      "tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(4) ", %8, %9, t;\n\t}"
+      "{\n\t.reg .pred p, t, e;\n\telect.sync _|e, 0xffffffff;\n\t"                                          \
+      "setp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, %10, %10;\n\t"                                                 \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(1) ", %5, %9, p;\n\t"                        \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(2) ", %6, %9, t;\n\t"                        \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(3) ", %7, %9, t;\n\t"                        \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], " AFORM(4) ", %8, %9, t;\n\t}"
 #define ATTN_A_DESC(i) "%" #i
 #define ATTN_A_TMEM(i) "[%" #i "]"
 __device__ __forceinline__ void mma4_f16_ss(uint32_t d, uint64_t a0, uint64_t a1, uint64_t a2, uint64_t a3, uint64_t b0,
@@ -132,6 +134,15 @@ __device__ __forceinline__ void mma4_tf32_ts(uint32_t d, uint32_t a0, uint32_t a
 #undef ATTN_A_TMEM
 #undef ATTN_A_DESC
 #undef ATTN_MMA4
+
+// Warp-uniform form of commit(): one elected lane of the (converged) warp
+// commits, so the barrier gets exactly one arrival.
+__device__ __forceinline__ void commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
 
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
