@@ -75,6 +75,12 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrives on named barrier `id` without waiting (the other `count` - 32*k
+// threads wait with named_barrier()).
+__device__ __forceinline__ void named_barrier_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Waits for phase `parity` of `bar` to complete, for at most kWaitLimitNs.
 // Returns false (and records ATTN_ERR_TIMEOUT in *status) if the limit ran
 // out.  `abort_flag` (shared memory, optional) is set on a timeout; once it

@@ -11,30 +11,35 @@
 //
 // One CTA owns 128 packed rows of one kv head g: row r is (query i, head
 // g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs query
-// heads that share it.  Keys are walked in tiles of 128, dealt alternately to
-// two independent online-softmax streams: stream 0 takes the even tiles,
-// stream 1 the odd ones.  Each stream has its own score buffer, O accumulator,
-// running max and running sum, and its own softmax warpgroup in which one
-// thread owns one whole row, so the two warpgroups never wait for each other
-// inside the loop, and while one of them turns scores into probabilities the
-// tensor core runs the other stream's products.  The two partial results are
-// merged once at the end with log-sum-exp weights, the way two KV splits are.
+// heads that share it.  Keys are walked in tiles of 128.  Three score buffers
+// in tensor memory let Q K^T run up to three tiles ahead of P V, and the two
+// softmax warpgroups take the tiles in turn (even / odd), one thread per row,
+// so one group's exponentials overlap the other's and both overlap the
+// products.  The reference max of the online softmax is shared: the group
+// working on tile j takes the value after tile j-1 from shared memory (an
+// mbarrier per tile parity orders the hand-over), moves it only when the tile
+// max exceeds it by more than 8 (so P <= 256), publishes it, and when it moved
+// rescales the single O accumulator once P V of tile j-1 has landed.  Each
+// group keeps the row sum of its own tiles against the reference it last
+// used; the two are combined at the end.
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: K tile (128 keys x D, 128-byte swizzle, K-major)
-//               and V^T tile (D x 128 keys, K-major) into a shared-memory ring.
-//   warps 1, 2  MMA issue, one thread per stream s (warp 1 also allocates
-//               tensor memory), for the tiles j of that stream in order:
-//                 S_s  = Q K_j^T   (A = Q in shared memory, B = K tile)
-//                 O_s += P_j V_j   (A = P in TMEM over S_s, B = V^T tile)
-//   warps 4-7   softmax of stream 0; warps 8-11 of stream 1.  Warp w covers
-//               rows 32(w%4)..+31 (its TMEM lanes); a thread owns one row.
-// Tensor memory (512 columns): S_0 [0, 128), S_1 [128, 256), O_0 [256, 256+D),
-// O_1 [256+D, 256+2D).  Scores are in base-2 units (Q is pre-multiplied by
-// scale * log2(e)).  A stream's reference max only moves when its tile max
-// exceeds it by more than 8 (so P <= 256); the true max is tracked apart for
-// the LSE.  Every wait is bounded; a CTA whose pipeline breaks drains its
-// copies and MMAs before it releases tensor memory.
+//               and V^T tile (D x 128 keys, K-major) into a shared-memory ring,
+//               in the order they are consumed.
+//   warp 1      tensor-memory allocation; issues S_(j%3) = Q K_j^T
+//               (A = Q in shared memory, B = K tile) once P V of tile j-3
+//               has released that buffer.
+//   warp 2      issues O += P_j V_j (A = P in TMEM over S_(j%3), B = V^T
+//               tile) in tile order once P_j is written.
+//   warps 4-7   softmax of the even tiles, warps 8-11 of the odd ones; warp
+//               w covers rows 32(w%4)..+31 (its TMEM lanes).
+// The issuing warps run their loops warp-uniformly; one elected lane issues.
+// Tensor memory (512 columns): S_b [128 b, 128 b + 128) for b = 0..2, O
+// [384, 384 + D).  Scores are in base-2 units (Q is pre-multiplied by
+// scale * log2(e)).  The true max is tracked apart for the LSE.  Every wait is
+// bounded; a CTA whose pipeline breaks drains its copies and MMAs before it
+// releases tensor memory.
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -42,25 +47,29 @@
 namespace attn {
 namespace {
 
-constexpr int kRows = 128;              // packed rows per CTA (MMA M)
-constexpr int kKeys = 128;              // keys per tile
+constexpr int kRows = 128;                 // packed rows per CTA (MMA M)
+constexpr int kKeys = 128;                 // keys per tile
 constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kOperandBytes = 192 * 1024;  // Q tile + K/V ring
 constexpr int kMaxRing = 12;
-constexpr int kColS = 0, kColO = 256;   // S_s at kColS + 128 s; O_s at kColO + D s
+constexpr int kSBuf = 3;                   // score buffers
+constexpr int kColO = 384;                 // S_b at 128 b; O at 384
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-struct __align__(1024) PpSmem {
+struct __align__(1024) Bf16Smem {
   unsigned char operands[kOperandBytes];  // [Q tile][ring slots]
   uint64_t kv_full[kMaxRing];
   uint64_t kv_empty[kMaxRing];
-  uint64_t s_full[2];
-  uint64_t p_ready[2];
-  uint64_t pv_done[2];
+  uint64_t s_full[kSBuf];
+  uint64_t p_ready[kSBuf];
+  uint64_t pv_done[2];     // P V of tile j completes phase j/2 of pv_done[j & 1]
+  uint64_t m_ready[2];     // reference max after tile j published: phase j/2 of m_ready[j & 1]
   uint64_t q_ready;
+  uint64_t o_final;        // every P V has completed
   uint64_t drain[2];
-  float part[2][3][kRows];  // [stream][m_ref, m_true, l][row], for the final merge
+  float m_pub[2][kRows];   // reference max after tile j, slot j & 1
+  float part[2][3][kRows];  // [group][reference of l, true max, l][row], for the epilogue
   uint32_t tmem_base;
   int abort;
 };
@@ -79,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(kTileBytes == (kKeys / 64) * kVtChunkBytes, "K and V^T tiles fill a slot alike");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
-  PpSmem& sm = *reinterpret_cast<PpSmem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
+  Bf16Smem& sm = *reinterpret_cast<Bf16Smem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
   unsigned char* const qtile = sm.operands;
   unsigned char* const ring = sm.operands + kQBytes;
 
@@ -100,20 +109,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_min = window(i0);
   const int n_max = window(min((long long)a.n_q, i0 + qpb) - 1);
   const int nt = (n_max + kKeys - 1) / kKeys;
+  // Ring positions (copy order): K_0, K_1, K_2, then V_j followed by K_(j+3).
+  auto k_pos = [&](int j) { return j < 3 ? j : 2 * j - 2; };
+  auto v_pos = [&](int j) { return min(2 * j + 3, j + nt); };
 
   if (tid == 0) {
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kSBuf; ++b) {
       mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.p_ready[b], 4);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.pv_done[b], 1);
+      mbar_init(&sm.m_ready[b], 4);
+      mbar_init(&sm.drain[b], 1);
     }
     mbar_init(&sm.q_ready, 8);
-    mbar_init(&sm.drain[0], 1);
-    mbar_init(&sm.drain[1], 1);
+    mbar_init(&sm.o_final, 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -128,17 +143,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && nt > 0) {
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_vt);
-      // Copies are issued in the order the two streams need the tiles:
-      // K_0, K_1, V_0, K_2, V_1, ..., K_(nt-1), V_(nt-2), V_(nt-1), so each
-      // ring slot is released roughly in the order it was filled and the ring
-      // runs kRing copies ahead of the tensor core.
-      for (int p = 0; p < 2 * nt; ++p) {
+      int p = 0;  // copies issued; copy p goes to ring slot p % kRing
+      auto load = [&](bool is_v, int j) {
         const int s = p % kRing, use = p / kRing;
         unsigned char* dst = ring + s * kTileBytes;
         if (use >= 1) mbar_wait_bounded(&sm.kv_empty[s], (unsigned)((use - 1) & 1), a.status, &sm.abort);
         mbar_arrive_expect_tx(&sm.kv_full[s], (unsigned)kTileBytes);
-        const bool is_v = (p == 2 * nt - 1) || (p > 0 && (p & 1) == 0);
-        const int j = is_v ? (p == 2 * nt - 1 ? nt - 1 : p / 2 - 1) : (p + 1) / 2;
         const int t0 = kKeys * j;
         if (is_v) {
 #pragma unroll
@@ -148,81 +158,84 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, &tm_k, g * D + 64 * c, t0, &sm.kv_full[s]);
         }
+        ++p;
+      };
+      for (int t = 0; t < 3 && t < nt; ++t) load(false, t);
+      for (int j = 0; j < nt; ++j) {
+        load(true, j);
+        if (j + 3 < nt) load(false, j + 3);
       }
       // No copy may still be landing in shared memory when the CTA exits.
-      for (int s = 0; s < kRing && s < 2 * nt; ++s) {
-        const int last = s + ((2 * nt - 1 - s) / kRing) * kRing;
+      for (int s = 0; s < kRing && s < p; ++s) {
+        const int last = s + ((p - 1 - s) / kRing) * kRing;
         mbar_wait_bounded(&sm.kv_full[s], (unsigned)((last / kRing) & 1), a.status);
       }
     }
   } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------ MMA issuers
-    // Warp 1 issues stream 0's products, warp 2 stream 1's.  An issuing
-    // thread blocks in tcgen05.mma while the tensor core's queue is full, so
-    // one thread alone leaves the tensor core idle for every wait and every
-    // bookkeeping step between its groups; with one issuer per stream, one
-    // stream's products run while the other's issuer waits.
-    // The whole warp runs the issue loop (warp-uniform values); one elected
-    // lane issues each MMA and commit.
-    const int st = warp - 1;
-    if (nt > st) {
-      constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, kKeys);
-      constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, D);
-      // Every operand here is K-major with the 128-byte swizzle and 1024-byte
-      // row groups, so one descriptor serves each base and an operand at byte
-      // offset off is that descriptor plus off >> 4 (the start-address field;
-      // shared-memory offsets stay far below its 14-bit range).
-      const uint64_t dq = tc::sdesc_sw128(smem_u32(qtile), 16, 1024);
+    // ------------------------------------------------------------ MMA issue
+    // Warp-uniform loops; one elected lane issues each MMA and commit.
+    if (nt > 0) {
+      // Every operand is K-major with the 128-byte swizzle and 1024-byte row
+      // groups, so an operand at byte offset off from a base is the base's
+      // descriptor plus off >> 4 (the start-address field).
       const uint64_t dring = tc::sdesc_sw128(smem_u32(ring), 16, 1024);
-      const uint32_t ds = tmem + kColS + kKeys * st;  // S_st (P_st in its first 64 columns)
-      const uint32_t d_o = tmem + kColO + D * st;      // O_st
       auto tile_desc = [&](int p) { return dring + (uint64_t)(((p % kRing) * kTileBytes) >> 4); };
       auto wait = [&](uint64_t* bar, int phase) {
         return __all_sync(0xffffffffu, mbar_wait_bounded(bar, (unsigned)(phase & 1), a.status, &sm.abort));
       };
-      bool ok = wait(&sm.q_ready, 0);
-      tc::fence_after_sync();
-      for (int j = st; ok && j < nt; j += 2) {
-        // S_st = Q K_j^T.  It overwrites the P that P V of tile j-2 reads, so
-        // that product must have completed.
-        const int pk = j == 0 ? 0 : 2 * j - 1;            // ring position of K_j
-        const int pv = j == nt - 1 ? 2 * nt - 1 : 2 * j + 2;  // and of V_j
-        ok = wait(&sm.kv_full[pk % kRing], pk / kRing) && (j < 2 || wait(&sm.pv_done[st], (j - 2) >> 1));
-        if (!ok) break;
+      if (warp == 1) {
+        // S_b = Q K_j^T, b = j % 3.  It overwrites the P that P V of tile
+        // j-3 reads, so that product must have completed.
+        constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, kKeys);
+        const uint64_t dq = tc::sdesc_sw128(smem_u32(qtile), 16, 1024);
+        bool ok = wait(&sm.q_ready, 0);
         tc::fence_after_sync();
-        const uint64_t dk = tile_desc(pk);
-        // Four K steps (16 elements, 32 bytes each) per 128-byte chunk.
+        for (int j = 0; ok && j < nt; ++j) {
+          const int pk = k_pos(j), b = j % kSBuf;
+          ok = wait(&sm.kv_full[pk % kRing], pk / kRing) && (j < kSBuf || wait(&sm.pv_done[(j - 3) & 1], (j - 3) >> 1));
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint64_t dk = tile_desc(pk);
+          const uint32_t ds = tmem + kKeys * b;
 #pragma unroll
-        for (int c4 = 0; c4 < kChunks; ++c4) {
-          const uint64_t c = (uint64_t)((c4 * kChunkBytes) >> 4);
-          tc::mma4_f16_ss(ds, dq + c, dq + c + 2, dq + c + 4, dq + c + 6, dk + c, dk + c + 2, dk + c + 4, dk + c + 6,
-                          idesc_qk, c4 > 0 ? 1u : 0u);
+          for (int c4 = 0; c4 < kChunks; ++c4) {  // four 16-element K steps per 64-element chunk
+            const uint64_t c = (uint64_t)((c4 * kChunkBytes) >> 4);
+            tc::mma4_f16_ss(ds, dq + c, dq + c + 2, dq + c + 4, dq + c + 6, dk + c, dk + c + 2, dk + c + 4,
+                            dk + c + 6, idesc_qk, c4 > 0 ? 1u : 0u);
+          }
+          tc::commit_elect(&sm.s_full[b]);
+          tc::commit_elect(&sm.kv_empty[pk % kRing]);
         }
-        tc::commit_elect(&sm.s_full[st]);
-        tc::commit_elect(&sm.kv_empty[pk % kRing]);
-        // O_st += P_j V_j once the softmax group has written P_j.
-        ok = wait(&sm.p_ready[st], j >> 1) && wait(&sm.kv_full[pv % kRing], pv / kRing);
-        if (!ok) break;
-        tc::fence_after_sync();
-        const uint64_t dv = tile_desc(pv);
-        const uint32_t acc0 = j >= 2 ? 1u : 0u;
+        tc::commit_elect(&sm.drain[0]);
+        mbar_wait_bounded(&sm.drain[0], 0, a.status);
+      } else {
+        // O += P_j V_j in tile order.
+        constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, D);
+        bool ok = true;
+        for (int j = 0; ok && j < nt; ++j) {
+          const int pv = v_pos(j), b = j % kSBuf;
+          ok = wait(&sm.p_ready[b], j / kSBuf) && wait(&sm.kv_full[pv % kRing], pv / kRing);
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint64_t dv = tile_desc(pv);
 #pragma unroll
-        for (int c4 = 0; c4 < kKeys / 64; ++c4) {
-          const uint64_t c = (uint64_t)((c4 * kVtChunkBytes) >> 4);
-          const uint32_t pa = ds + 32 * c4;  // P: 8 columns (16 keys) per K step
-          tc::mma4_f16_ts(d_o, pa, pa + 8, pa + 16, pa + 24, dv + c, dv + c + 2, dv + c + 4, dv + c + 6, idesc_pv,
-                          c4 > 0 ? 1u : acc0);
+          for (int c4 = 0; c4 < kKeys / 64; ++c4) {
+            const uint64_t c = (uint64_t)((c4 * kVtChunkBytes) >> 4);
+            const uint32_t pa = tmem + kKeys * b + 32 * c4;  // P: 8 columns (16 keys) per K step
+            tc::mma4_f16_ts(tmem + kColO, pa, pa + 8, pa + 16, pa + 24, dv + c, dv + c + 2, dv + c + 4, dv + c + 6,
+                            idesc_pv, (j > 0 || c4 > 0) ? 1u : 0u);
+          }
+          tc::commit_elect(&sm.pv_done[j & 1]);
+          tc::commit_elect(&sm.kv_empty[pv % kRing]);
         }
-        tc::commit_elect(&sm.pv_done[st]);
-        tc::commit_elect(&sm.kv_empty[pv % kRing]);
+        tc::commit_elect(&sm.o_final);
+        tc::commit_elect(&sm.drain[1]);
+        mbar_wait_bounded(&sm.drain[1], 0, a.status);
       }
-      // Every MMA has finished before tensor memory is released.
-      tc::commit_elect(&sm.drain[st]);
-      mbar_wait_bounded(&sm.drain[st], 0, a.status);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
-    const int st = (warp - 4) >> 2;            // stream 0 or 1
+    const int grp = (warp - 4) >> 2;           // group 0: even tiles, 1: odd tiles
     const int r = 32 * (warp & 3) + lane;      // row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const long long packed = (long long)blk * kRows + r;
@@ -234,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Q row, pre-scaled, as bf16 into the K-major operand tile: 64-element
     // chunk c holds 128 rows of 128 bytes, 16-byte unit u of row r at unit
-    // u ^ (r & 7) (the 128-byte swizzle).  Stream c's warps write chunk c.
-    if (st < kChunks) {
-      unsigned char* qdst = qtile + st * kChunkBytes + r * 128;
-      const float* qrow = a.q + qi * a.q_row_stride + (long long)h * D + 64 * st;
+    // u ^ (r & 7) (the 128-byte swizzle).  Group c writes chunk c.
+    if (grp < kChunks) {
+      unsigned char* qdst = qtile + grp * kChunkBytes + r * 128;
+      const float* qrow = a.q + qi * a.q_row_stride + (long long)h * D + 64 * grp;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
@@ -255,11 +268,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.q_ready);
 
-    const uint32_t s_col = tmem + lane_base + kColS + kKeys * st;
-    const uint32_t o_col = tmem + lane_base + kColO + D * st;
-    float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
-    for (int j = st; j < nt; j += 2) {
-      mbar_wait_bounded(&sm.s_full[st], (unsigned)((j >> 1) & 1), a.status, &sm.abort);
+    const uint32_t o_col = tmem + lane_base + kColO;
+    float m_l = -INFINITY;   // reference of l (the shared reference at this group's last tile)
+    float m_true = -INFINITY, l = 0.f;
+    for (int j = grp; j < nt; j += 2) {
+      const int b = j % kSBuf;
+      const uint32_t s_col = tmem + lane_base + kKeys * b;
+      mbar_wait_bounded(&sm.s_full[b], (unsigned)((j / kSBuf) & 1), a.status, &sm.abort);
       tc::fence_after_sync();
       uint32_t s[4][32];
 #pragma unroll
@@ -284,14 +299,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx[k] = max3(mx[k], __uint_as_float(s[i >> 5][(i & 31) + 2 * k]), __uint_as_float(s[i >> 5][(i & 31) + 2 * k + 1]));
       const float tmax = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       m_true = fmaxf(m_true, tmax);
-      float corr = 1.f;
-      if (tmax > m_ref + kRescaleThreshold) {  // also true for the first finite tile max
-        corr = ex2(m_ref - tmax);              // m_ref = -inf gives 0
-        m_ref = tmax;
-      }
-      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
-      // P = 2^(S - m) as bf16 pairs over the first 64 columns of S_s (every
+      // Shared reference: the value after tile j-1, moved if this tile's max
+      // exceeds it by more than the threshold (also for the first finite max).
+      float m_prev = -INFINITY;
+      if (j >= 1) {
+        mbar_wait_bounded(&sm.m_ready[(j - 1) & 1], (unsigned)(((j - 1) >> 1) & 1), a.status, &sm.abort);
+        m_prev = sm.m_pub[(j - 1) & 1][r];
+      }
+      const float m_new = (tmax > m_prev + kRescaleThreshold) ? tmax : m_prev;
+      sm.m_pub[j & 1][r] = m_new;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.m_ready[j & 1]);
+      const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
+
+      // P = 2^(S - m) as bf16 pairs over the first 64 columns of S_b (every
       // column of this row was read above): the 32 values of chunk c become
       // 16 words, packed in place into s[c] and stored at column 16 c.  The
       // row sum is taken in fp32.
@@ -310,12 +332,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_st16(s_col + 16 * c, s[c]);
       }
       const float tsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-      l = l * corr + tsum;
+      // This group's row sum, moved to the new reference (m_l <= m_new).
+      l = (l == 0.f ? 0.f : l * ex2(m_l - m_new)) + tsum;
+      m_l = m_new;
 
-      // O_s holds this stream's earlier tiles and is idle here: P V of tile
-      // j-2 finished before Q K^T of tile j was issued, and P V of tile j
-      // waits for p_ready.  Rescale it when any row of the warp moved.
-      if (j >= 2 && __any_sync(0xffffffffu, corr != 1.f)) {
+      // O holds tiles 0..j-1 against m_prev once P V of tile j-1 has landed;
+      // P V of tile j waits for p_ready.  Rescale when any row of the warp
+      // moved its reference.
+      if (j >= 1 && __any_sync(0xffffffffu, m_new != m_prev)) {
+        const float corr = (m_new != m_prev) ? ex2(m_prev - m_new) : 1.f;  // m_prev = -inf gives 0
+        mbar_wait_bounded(&sm.pv_done[(j - 1) & 1], (unsigned)(((j - 1) >> 1) & 1), a.status, &sm.abort);
+        tc::fence_after_sync();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -330,66 +357,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_ready[st]);
+      if (lane == 0) mbar_arrive(&sm.p_ready[b]);
     }
 
-    // Epilogue: merge the two streams, out = O / l, lse = (max, log sum).
-    // Each warpgroup waits for its own stream's last P V (one phase at most is
-    // outstanding: the one before it finished before this group's last Q K^T
-    // was issued); after the barrier both accumulators are final.
-    if (nt > st) {
-      const int last = st + 2 * ((nt - 1 - st) >> 1);
-      mbar_wait_bounded(&sm.pv_done[st], (unsigned)((last >> 1) & 1), a.status, &sm.abort);
-    }
-    sm.part[st][0][r] = m_ref;
-    sm.part[st][1][r] = m_true;
-    sm.part[st][2][r] = l;
+    // Epilogue: out = O / l, lse = (max, log sum).
+    sm.part[grp][0][r] = m_l;
+    sm.part[grp][1][r] = m_true;
+    sm.part[grp][2][r] = l;
+    if (nt > 0) mbar_wait_bounded(&sm.o_final, 0, a.status, &sm.abort);
     tc::fence_before_sync();
     named_barrier(1, kSoftmaxThreads);
     tc::fence_after_sync();
-    const float m0 = sm.part[0][0][r], m1 = sm.part[1][0][r];
-    const float l0 = sm.part[0][2][r], l1 = sm.part[1][2][r];
-    const float mm = fmaxf(m0, m1);
-    const float c0 = (l0 > 0.f) ? ex2(m0 - mm) : 0.f;
-    const float c1 = (l1 > 0.f) ? ex2(m1 - mm) : 0.f;
-    const float l_row = l0 * c0 + l1 * c1;
+    const float m_fin = nt > 0 ? sm.m_pub[(nt - 1) & 1][r] : -INFINITY;
+    float l_row = 0.f;
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const float lw = sm.part[w][2][r];
+      if (lw > 0.f) l_row += lw * ex2(sm.part[w][0][r] - m_fin);
+    }
     const float inv = (l_row == 0.f) ? 0.f : 1.f / l_row;
-    const float w0 = c0 * inv, w1 = c1 * inv;
-    constexpr int kHalfD = D / 2;  // output columns per stream warpgroup
-    float* orow = a.out + qi * a.out_row_stride + (long long)h * D + st * kHalfD;
+    constexpr int kHalfD = D / 2;  // output columns per group
+    float* orow = a.out + qi * a.out_row_stride + (long long)h * D + grp * kHalfD;
 #pragma unroll
     for (int c = 0; c < kHalfD / 32; ++c) {
-      const int col = st * kHalfD + 32 * c;
-      uint32_t o0[32], o1[32];
+      uint32_t o[32];
       if (nt > 0) {
-        tc::tmem_ld32(tmem + lane_base + kColO + col, o0);
+        tc::tmem_ld32(o_col + grp * kHalfD + 32 * c, o);
+        tc::tmem_ld_wait();
+        tc::reg_fence(o);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
-      if (nt > 1) {
-        tc::tmem_ld32(tmem + lane_base + kColO + D + col, o1);
-      }
-      tc::tmem_ld_wait();
-      if (nt > 0) tc::reg_fence(o0);
-      if (nt > 1) tc::reg_fence(o1);
       if (row_ok) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          float v[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float x0 = nt > 0 ? __uint_as_float(o0[e + k]) * w0 : 0.f;
-            const float x1 = nt > 1 ? __uint_as_float(o1[e + k]) * w1 : 0.f;
-            v[k] = x0 + x1;
-          }
-          *reinterpret_cast<float4*>(orow + 32 * c + e) = make_float4(v[0], v[1], v[2], v[3]);
-        }
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(orow + 32 * c + e) =
+              make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                          __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
       }
     }
-    if (st == 0 && row_ok && a.lse != nullptr) {
+    if (grp == 0 && row_ok && a.lse != nullptr) {
       const float mt = fmaxf(sm.part[0][1][r], sm.part[1][1][r]);
       float* l2 = a.lse + (qi * a.H + h) * 2;
       const bool empty = (l_row == 0.f);
       l2[0] = empty ? kEmptyLse : mt * kLn2;
-      l2[1] = empty ? kEmptyLse : logf(l_row) + (mm - mt) * kLn2;
+      l2[1] = empty ? kEmptyLse : logf(l_row) + (m_fin - mt) * kLn2;
     }
   }
 
@@ -484,7 +497,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   if (!maps_ok) {
     rc = ATTN_ERR_UNSUPPORTED;
   } else {
-    const size_t smem = sizeof(PpSmem) + 1024;
+    const size_t smem = sizeof(Bf16Smem) + 1024;
     auto kern = flash_bf16_kernel<D>;
     if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) {
       rc = ATTN_ERR_CUDA;
