@@ -5,9 +5,9 @@
 // prefill windows with the online softmax's running max and sum (cera
 // attention_prefill.wgsl, fn attention_prefill: per-tile max, correction,
 // exponentials, running sum; meganeura attention.wgsl, fn main: the final
-// (max, log sum) store).  A pre-pass converts K to bf16 in place order and V to
-// bf16 transposed (keys contiguous); Q and P are rounded to bf16 inside the
-// kernel; both products accumulate in fp32 in tensor memory.
+// (max, log sum) store).  A pre-pass converts K and V to bf16 (same layout);
+// Q and P are rounded to bf16 inside the kernel; both products accumulate in
+// fp32 in tensor memory.
 //
 // One CTA owns 128 packed rows of one kv head g: row r is (query i, head
 // g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs query
@@ -25,12 +25,12 @@
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: K tile (128 keys x D, 128-byte swizzle, K-major)
-//               and V^T tile (D x 128 keys, K-major) into a shared-memory ring,
-//               in the order they are consumed.
+//               and V tile (the same boxes; read as the MN-major operand of
+//               P V) into a shared-memory ring, in the order they are consumed.
 //   warp 1      tensor-memory allocation; issues S_(j%3) = Q K_j^T
 //               (A = Q in shared memory, B = K tile) once P V of tile j-3
 //               has released that buffer.
-//   warp 2      issues O += P_j V_j (A = P in TMEM over S_(j%3), B = V^T
+//   warp 2      issues O += P_j V_j (A = P in TMEM over S_(j%3), B = V
 //               tile) in tile order once P_j is written.
 //   warps 4-7   softmax of the even tiles, warps 8-11 of the odd ones; warp
 //               w covers rows 32(w%4)..+31 (its TMEM lanes).
@@ -65,7 +65,8 @@ struct __align__(1024) Bf16Smem {
   uint64_t p_ready[kSBuf];
   uint64_t pv_done[2];     // P V of tile j completes phase j/2 of pv_done[j & 1]
   uint64_t m_ready[2];     // reference max after tile j published: phase j/2 of m_ready[j & 1]
-  uint64_t q_ready;
+  uint64_t q_full;         // the fp32 Q block has landed in the staging area
+  uint64_t q_ready;        // the bf16 Q tile is written
   uint64_t o_final;        // every P V has completed
   uint64_t drain[2];
   float m_pub[2][kRows];   // reference max after tile j, slot j & 1
@@ -77,20 +78,23 @@ struct __align__(1024) Bf16Smem {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_bf16_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_vt) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q) {
   constexpr int kChunks = D / 64;                // 128-byte (64-element) column chunks of a K row
   constexpr int kChunkBytes = kKeys * 128;       // one K box: 128 keys x 128 bytes
-  constexpr int kVtChunkBytes = D * 128;         // one V^T box: D rows x 128 bytes of keys
-  constexpr int kTileBytes = kChunks * kChunkBytes;  // == 2 * kVtChunkBytes
+  constexpr int kTileBytes = kChunks * kChunkBytes;
   constexpr int kQBytes = kRows * D * 2;
   constexpr int kRing = (kOperandBytes - kQBytes) / kTileBytes;
   static_assert(kRing <= kMaxRing && kRing >= 4, "ring depth");
-  static_assert(kTileBytes == (kKeys / 64) * kVtChunkBytes, "K and V^T tiles fill a slot alike");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   Bf16Smem& sm = *reinterpret_cast<Bf16Smem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
   unsigned char* const qtile = sm.operands;
   unsigned char* const ring = sm.operands + kQBytes;
+  // The CTA's fp32 Q block ([queries][gs heads][D], 128 rows of D floats)
+  // lands by TMA in ring slots 3 and 4, which hold no K/V copy until the Q
+  // tile has been converted.
+  static_assert(2 * kTileBytes == kRows * D * 4, "Q staging fills two ring slots");
+  const float* const qstage = reinterpret_cast<const float*>(ring + 3 * kTileBytes);
 
   allow_dependent_launch();
   grid_dependency_wait();
@@ -127,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.m_ready[b], 4);
       mbar_init(&sm.drain[b], 1);
     }
+    mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_ready, 8);
     mbar_init(&sm.o_final, 1);
     sm.abort = 0;
@@ -141,23 +146,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nt > 0) {
+      prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_vt);
+      prefetch_tmap(&tm_v);
+      mbar_arrive_expect_tx(&sm.q_full, (unsigned)(kRows * D * 4));
+      tma_load_3d(ring + 3 * kTileBytes, &tm_q, 0, g * gs, (int)i0, &sm.q_full);
       int p = 0;  // copies issued; copy p goes to ring slot p % kRing
       auto load = [&](bool is_v, int j) {
         const int s = p % kRing, use = p / kRing;
+        if (p == 3) mbar_wait_bounded(&sm.q_ready, 0, a.status, &sm.abort);  // slots 3-4 free again
         unsigned char* dst = ring + s * kTileBytes;
         if (use >= 1) mbar_wait_bounded(&sm.kv_empty[s], (unsigned)((use - 1) & 1), a.status, &sm.abort);
         mbar_arrive_expect_tx(&sm.kv_full[s], (unsigned)kTileBytes);
         const int t0 = kKeys * j;
-        if (is_v) {
+        const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
 #pragma unroll
-          for (int c = 0; c < kKeys / 64; ++c)
-            tma_load_2d(dst + c * kVtChunkBytes, &tm_vt, t0 + 64 * c, g * D, &sm.kv_full[s]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, &tm_k, g * D + 64 * c, t0, &sm.kv_full[s]);
-        }
+        for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + 64 * c, t0, &sm.kv_full[s]);
         ++p;
       };
       for (int t = 0; t < 3 && t < nt; ++t) load(false, t);
@@ -175,11 +179,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issue
     // Warp-uniform loops; one elected lane issues each MMA and commit.
     if (nt > 0) {
-      // Every operand is K-major with the 128-byte swizzle and 1024-byte row
-      // groups, so an operand at byte offset off from a base is the base's
-      // descriptor plus off >> 4 (the start-address field).
-      const uint64_t dring = tc::sdesc_sw128(smem_u32(ring), 16, 1024);
-      auto tile_desc = [&](int p) { return dring + (uint64_t)(((p % kRing) * kTileBytes) >> 4); };
+      // Operands use the 128-byte swizzle with 1024-byte groups of 8 rows; an
+      // operand at byte offset off from a base is the base's descriptor plus
+      // off >> 4 (the start-address field).  K (and Q) are K-major; V is read
+      // MN-major: each key row holds 64 elements of D per 128-byte chunk,
+      // chunks kChunkBytes apart.
+      const uint64_t dk0 = tc::sdesc_sw128(smem_u32(ring), 16, 1024);
+      const uint64_t dv0 = tc::sdesc_sw128(smem_u32(ring), kChunkBytes, 1024);
+      auto slot_off = [&](int p) { return (uint64_t)(((p % kRing) * kTileBytes) >> 4); };
       auto wait = [&](uint64_t* bar, int phase) {
         return __all_sync(0xffffffffu, mbar_wait_bounded(bar, (unsigned)(phase & 1), a.status, &sm.abort));
       };
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait(&sm.kv_full[pk % kRing], pk / kRing) && (j < kSBuf || wait(&sm.pv_done[(j - 3) & 1], (j - 3) >> 1));
           if (!ok) break;
           tc::fence_after_sync();
-          const uint64_t dk = tile_desc(pk);
+          const uint64_t dk = dk0 + slot_off(pk);
           const uint32_t ds = tmem + kKeys * b;
 #pragma unroll
           for (int c4 = 0; c4 < kChunks; ++c4) {  // four 16-element K steps per 64-element chunk
@@ -210,20 +217,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(&sm.drain[0], 0, a.status);
       } else {
         // O += P_j V_j in tile order.
-        constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, D);
+        constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtBF16, true, kRows, D);
         bool ok = true;
         for (int j = 0; ok && j < nt; ++j) {
           const int pv = v_pos(j), b = j % kSBuf;
           ok = wait(&sm.p_ready[b], j / kSBuf) && wait(&sm.kv_full[pv % kRing], pv / kRing);
           if (!ok) break;
           tc::fence_after_sync();
-          const uint64_t dv = tile_desc(pv);
+          const uint64_t dv = dv0 + slot_off(pv);
+          constexpr uint64_t st = (16 * 128) >> 4;  // one K step: 16 key rows of 128 bytes
 #pragma unroll
           for (int c4 = 0; c4 < kKeys / 64; ++c4) {
-            const uint64_t c = (uint64_t)((c4 * kVtChunkBytes) >> 4);
+            const uint64_t c = 4 * st * c4;
             const uint32_t pa = tmem + kKeys * b + 32 * c4;  // P: 8 columns (16 keys) per K step
-            tc::mma4_f16_ts(tmem + kColO, pa, pa + 8, pa + 16, pa + 24, dv + c, dv + c + 2, dv + c + 4, dv + c + 6,
-                            idesc_pv, (j > 0 || c4 > 0) ? 1u : 0u);
+            tc::mma4_f16_ts(tmem + kColO, pa, pa + 8, pa + 16, pa + 24, dv + c, dv + c + st, dv + c + 2 * st,
+                            dv + c + 3 * st, idesc_pv, (j > 0 || c4 > 0) ? 1u : 0u);
           }
           tc::commit_elect(&sm.pv_done[j & 1]);
           tc::commit_elect(&sm.kv_empty[pv % kRing]);
@@ -247,20 +255,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Q row, pre-scaled, as bf16 into the K-major operand tile: 64-element
     // chunk c holds 128 rows of 128 bytes, 16-byte unit u of row r at unit
-    // u ^ (r & 7) (the 128-byte swizzle).  Group c writes chunk c.
-    if (grp < kChunks) {
+    // u ^ (r & 7) (the 128-byte swizzle).  Group c converts chunk c from the
+    // staging rows; each thread starts at float4 r % 16 of its row, which
+    // spreads both the staging reads and the tile writes over the banks.
+    if (nt > 0 && grp < kChunks) {
+      mbar_wait_bounded(&sm.q_full, 0, a.status, &sm.abort);
+      const float4* src = reinterpret_cast<const float4*>(qstage + r * D + 64 * grp);
       unsigned char* qdst = qtile + grp * kChunkBytes + r * 128;
-      const float* qrow = a.q + qi * a.q_row_stride + (long long)h * D + 64 * grp;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-        if (row_ok) {
-          x0 = *reinterpret_cast<const float4*>(qrow + 8 * u);
-          x1 = *reinterpret_cast<const float4*>(qrow + 8 * u + 4);
-        }
-        const uint4 w = make_uint4(tc::pack_bf16(x0.x * sl2, x0.y * sl2), tc::pack_bf16(x0.z * sl2, x0.w * sl2),
-                                   tc::pack_bf16(x1.x * sl2, x1.y * sl2), tc::pack_bf16(x1.z * sl2, x1.w * sl2));
-        *reinterpret_cast<uint4*>(qdst + 16 * (u ^ (r & 7))) = w;
+      for (int i = 0; i < 16; ++i) {
+        const int f = (i + r) & 15;
+        const float4 x = src[f];
+        *reinterpret_cast<uint2*>(qdst + 16 * ((f >> 1) ^ (r & 7)) + 8 * (f & 1)) =
+            make_uint2(tc::pack_bf16(x.x * sl2, x.y * sl2), tc::pack_bf16(x.z * sl2, x.w * sl2));
       }
     }
     // The tensor core reads the tile through the async proxy.
@@ -415,36 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// fp32 -> bf16, n4 groups of four values (the source is 16-byte aligned).
-__global__ void __launch_bounds__(256) to_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
-                                                      long long n4) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
-    const float4 x = src[i];
-    dst[i] = make_uint2(tc::pack_bf16(x.x, x.y), tc::pack_bf16(x.z, x.w));
-  }
-}
-
-// V [rows][row_stride] fp32 -> V^T [cols][pad] bf16 (cols = G*D), zero for
-// rows >= rows.  32 x 32 tiles through shared memory; block (32, 8).
-__global__ void __launch_bounds__(256) transpose_bf16_kernel(const float* __restrict__ v, uint16_t* __restrict__ vt,
-                                                             long long rows, long long pad, long long row_stride,
-                                                             int cols) {
-  __shared__ float tile[32][33];
-  const long long t0 = (long long)blockIdx.x * 32;
-  const int c0 = blockIdx.y * 32;
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const long long t = t0 + i;
-    const int c = c0 + threadIdx.x;
-    tile[i][threadIdx.x] = (t < rows && c < cols) ? v[t * row_stride + c] : 0.f;
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int c = c0 + i;
-    const long long t = t0 + threadIdx.x;
-    if (c < cols && t < pad) {
-      const uint32_t w = tc::pack_bf16(tile[threadIdx.x][i], 0.f);
-      vt[(long long)c * pad + t] = (uint16_t)(w & 0xffffu);
-    }
+// K and V fp32 -> bf16 in one pass: n4 groups of four values from each (both
+// sources 16-byte aligned).
+__global__ void __launch_bounds__(256) kv_to_bf16_kernel(const float4* __restrict__ k, const float4* __restrict__ v,
+                                                         uint2* __restrict__ k16, uint2* __restrict__ v16, long long n4) {
+  allow_dependent_launch();
+  grid_dependency_wait();
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 x = k[i], y = v[i];
+    k16[i] = make_uint2(tc::pack_bf16(x.x, x.y), tc::pack_bf16(x.z, x.w));
+    v16[i] = make_uint2(tc::pack_bf16(y.x, y.y), tc::pack_bf16(y.z, y.w));
   }
 }
 
@@ -461,38 +449,43 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const bool no_keys = kv_rows < 1 || a.k == nullptr || a.v == nullptr;
   if (kv_rows < 1) kv_rows = 1;
   void* scratch = nullptr;
-  long long kv_pad = 64;
   const void* kp = a.q;  // an empty key set never reads K/V: any aligned base will do
   const void* vp = a.q;
   if (!no_keys) {
     // K and V as bf16 in stream-ordered temporary memory, released on the
-    // same stream once the attention kernel has run.  K keeps its layout; V
-    // is written transposed, V^T [G*D][kv_pad] with keys contiguous and the
-    // pad columns zero.
+    // same stream once the attention kernel has run.
     const long long elems = kv_rows * a.kv_row_stride;
-    kv_pad = (kv_rows + 63) / 64 * 64;
-    const long long vt_elems = (long long)a.G * D * kv_pad;
-    if (cudaMallocAsync(&scratch, (size_t)(elems + vt_elems) * 2, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMallocAsync(&scratch, (size_t)elems * 4, s) != cudaSuccess) return ATTN_ERR_CUDA;
     uint16_t* k16 = static_cast<uint16_t*>(scratch);
-    uint16_t* vt16 = k16 + elems;
-    to_bf16_kernel<<<4 * 152, 256, 0, s>>>(reinterpret_cast<const float4*>(a.k), reinterpret_cast<uint2*>(k16),
-                                           elems / 4);
-    const dim3 tgrid((unsigned)(kv_pad / 32), (unsigned)((a.G * D + 31) / 32));
-    transpose_bf16_kernel<<<tgrid, dim3(32, 8), 0, s>>>(a.v, vt16, kv_rows, kv_pad, a.kv_row_stride, a.G * D);
+    uint16_t* v16 = k16 + elems;
+    const float4* k4 = reinterpret_cast<const float4*>(a.k);
+    const float4* v4 = reinterpret_cast<const float4*>(a.v);
+    uint2* k2 = reinterpret_cast<uint2*>(k16);
+    uint2* v2 = reinterpret_cast<uint2*>(v16);
+    long long n4 = elems / 4;
+    void* cargs[] = {&k4, &v4, &k2, &v2, &n4};
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 152;
+    if (launch_pdl(reinterpret_cast<const void*>(kv_to_bf16_kernel), dim3(4 * sms), dim3(256), 0, s, cargs) !=
+        cudaSuccess) {
+      cudaFreeAsync(scratch, s);
+      return ATTN_ERR_CUDA;
+    }
     kp = k16;
-    vp = vt16;
+    vp = v16;
   }
-  CUtensorMap tm_k, tm_vt;
-  // K: [kv_rows][kv_row_stride] bf16, boxes of 64 elements x 128 keys.
-  const uint64_t kdims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
-  const uint64_t kstrides[1] = {(uint64_t)a.kv_row_stride * 2};
-  const uint32_t kbox[2] = {64, (uint32_t)kKeys};
-  // V^T: [G*D rows][kv_pad keys] bf16, boxes of 64 keys x D rows.
-  const uint64_t vdims[2] = {(uint64_t)kv_pad, (uint64_t)a.G * D};
-  const uint64_t vstrides[1] = {(uint64_t)kv_pad * 2};
-  const uint32_t vbox[2] = {64, (uint32_t)D};
-  const bool maps_ok = make_tmap(&tm_k, kp, 2, kdims, kstrides, kbox, true, kSwizzle128) &&
-                       make_tmap(&tm_vt, vp, 2, vdims, vstrides, vbox, true, kSwizzle128);
+  CUtensorMap tm_k, tm_v, tm_q;
+  // Q: fp32 [n_q][H][D] (query rows q_row_stride floats apart); the box is
+  // one CTA's block, D x gs heads x 128/gs queries; rows past n_q read as 0.
+  const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)a.H, (uint64_t)a.n_q};
+  const uint64_t qstrides[2] = {(uint64_t)D * 4, (uint64_t)a.q_row_stride * 4};
+  const uint32_t qbox[3] = {(uint32_t)D, (uint32_t)gs, (uint32_t)(kRows / gs)};
+  // K and V: [kv_rows][kv_row_stride] bf16, boxes of 64 elements x 128 keys.
+  const uint64_t dims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
+  const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * 2};
+  const uint32_t box[2] = {64, (uint32_t)kKeys};
+  const bool maps_ok = make_tmap(&tm_k, kp, 2, dims, strides, box, true, kSwizzle128) &&
+                       make_tmap(&tm_v, vp, 2, dims, strides, box, true, kSwizzle128) &&
+                       make_tmap(&tm_q, a.q, 3, qdims, qstrides, qbox, false, kSwizzleNone);
   int rc = ATTN_OK;
   if (!maps_ok) {
     rc = ATTN_ERR_UNSUPPORTED;
@@ -503,7 +496,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
       rc = ATTN_ERR_CUDA;
     } else {
       FlashArgs aa = a;
-      void* args[] = {&aa, &tm_k, &tm_vt};
+      void* args[] = {&aa, &tm_k, &tm_v, &tm_q};
       if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s,
                      args) != cudaSuccess)
         rc = ATTN_ERR_CUDA;

@@ -64,7 +64,8 @@ struct __align__(1024) TcSmem {
   uint64_t s_full[kSBuf];
   uint64_t p_ready[kSBuf];
   uint64_t pv_done[kSBuf];
-  uint64_t q_ready;
+  uint64_t q_full;   // the fp32 Q block has landed in the staging slot
+  uint64_t q_ready;  // Q is in tensor memory
   uint64_t drain;
   float red_max[2][2][kRows];  // [tile parity][group][row] partial tile maxima
   float red_l[2][kRows];       // [group][row] partial row sums (epilogue)
@@ -75,7 +76,7 @@ struct __align__(1024) TcSmem {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_tc_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q) {
   constexpr int kEpr = 32;                     // elements per 128-byte row
   constexpr int kChunks = D / kEpr;            // 128-byte column chunks of a K/V row
   constexpr int kChunkBytes = kKeys * 128;     // one TMA box: 128 keys x 128 bytes
@@ -86,6 +87,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
+  // The CTA's fp32 Q block lands by TMA in ring slot 2 (which holds no K/V
+  // copy until Q is in tensor memory): D/32 chunks of 128 rows x 128 bytes,
+  // 128-byte swizzle (16-byte unit u of row r at unit u ^ (r & 7)).
+  static_assert(kTileBytes == kRows * D * 4, "Q staging fills one ring slot");
+  unsigned char* const qstage = sm.ring + 2 * kTileBytes;
 
   // Programmatic dependent launch: the next kernel may start launching; this
   // one touches no global memory before the previous kernel has completed.
@@ -118,6 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.p_ready[b], 8);
       mbar_init(&sm.pv_done[b], 1);
     }
+    mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_ready, 8);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
@@ -132,14 +139,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nt > 0) {
+      prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
+      mbar_arrive_expect_tx(&sm.q_full, (unsigned)kTileBytes);
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) tma_load_3d(qstage + c * kChunkBytes, &tm_q, kEpr * c, g * gs, (int)i0, &sm.q_full);
       // Copies go out in the order the MMA issuer consumes the tiles: K_0,
       // K_1, V_0, K_2, V_1, ..., K_(nt-1), V_(nt-2), V_(nt-1).  Ring slot
       // p % kRing holds copy p; it is refilled once its consumer completes.
       for (int p = 0; p < 2 * nt; ++p) {
         const int s = p % kRing, use = p / kRing;
         unsigned char* dst = sm.ring + s * kTileBytes;
+        if (p == 2) mbar_wait_bounded(&sm.q_ready, 0, a.status, &sm.abort);  // the staging slot is free again
         if (use >= 1) mbar_wait_bounded(&sm.kv_empty[s], (unsigned)((use - 1) & 1), a.status, &sm.abort);
         mbar_arrive_expect_tx(&sm.kv_full[s], (unsigned)kTileBytes);
         const bool is_v = (p == 2 * nt - 1) || (p > 0 && (p & 1) == 0);
@@ -249,24 +261,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = a.scale * kLog2e;
 
     // Q row -> TMEM (pre-scaled), one value per column; each group stores half
-    // the row.  Rows past n_q are zero.
-    {
+    // the row, read from the staging slot (rows past n_q arrived as zeros).
+    if (nt > 0) {
       constexpr int kQCols = D / 2;
-      const float* qrow = a.q + qi * a.q_row_stride + (long long)h * D + grp * kQCols;
+      mbar_wait_bounded(&sm.q_full, 0, a.status, &sm.abort);
 #pragma unroll
       for (int c = 0; c < kQCols / 32; ++c) {
+        const unsigned char* src = qstage + (grp * (kQCols / 32) + c) * kChunkBytes + r * 128;
         uint32_t v[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 x = row_ok ? *reinterpret_cast<const float4*>(qrow + 32 * c + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[e] = __float_as_uint(x.x * sl2);
-          v[e + 1] = __float_as_uint(x.y * sl2);
-          v[e + 2] = __float_as_uint(x.z * sl2);
-          v[e + 3] = __float_as_uint(x.w * sl2);
+        for (int u = 0; u < 8; ++u) {
+          const float4 x = *reinterpret_cast<const float4*>(src + 16 * (u ^ (r & 7)));
+          v[4 * u] = __float_as_uint(x.x * sl2);
+          v[4 * u + 1] = __float_as_uint(x.y * sl2);
+          v[4 * u + 2] = __float_as_uint(x.z * sl2);
+          v[4 * u + 3] = __float_as_uint(x.w * sl2);
         }
         tc::tmem_st32(tmem + lane_base + kColQ + grp * kQCols + 32 * c, v);
       }
       tc::tmem_st_wait();
+    }
+    {
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.q_ready);
@@ -422,18 +437,25 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   // An empty key set never reads K/V: any aligned base will do.
   const void* kp = no_keys ? static_cast<const void*>(a.q) : a.k;
   const void* vp = no_keys ? static_cast<const void*>(a.q) : a.v;
-  CUtensorMap tm_k, tm_v;
+  CUtensorMap tm_k, tm_v, tm_q;
+  // Q: fp32 [n_q][H][D] (query rows q_row_stride floats apart); one CTA's
+  // block is D/32 boxes of 32 floats x gs heads x 128/gs queries, rows past
+  // n_q read as 0.
+  const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)a.H, (uint64_t)a.n_q};
+  const uint64_t qstrides[2] = {(uint64_t)D * 4, (uint64_t)a.q_row_stride * 4};
+  const uint32_t qbox[3] = {32, (uint32_t)gs, (uint32_t)(kRows / gs)};
   const uint64_t dims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
   const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * 4};
   const uint32_t box[2] = {32, (uint32_t)kKeys};
   if (!make_tmap(&tm_k, kp, 2, dims, strides, box, false, kSwizzle128) ||
-      !make_tmap(&tm_v, vp, 2, dims, strides, box, false, kSwizzle128Atom32))
+      !make_tmap(&tm_v, vp, 2, dims, strides, box, false, kSwizzle128Atom32) ||
+      !make_tmap(&tm_q, a.q, 3, qdims, qstrides, qbox, false, kSwizzle128))
     return ATTN_ERR_UNSUPPORTED;
   const size_t smem = sizeof(TcSmem) + 1024;
   auto kern = flash_tc_kernel<D>;
   if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
   FlashArgs aa = a;
-  void* args[] = {&aa, &tm_k, &tm_v};
+  void* args[] = {&aa, &tm_k, &tm_v, &tm_q};
   if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s, args) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;

@@ -90,4 +90,7 @@ size_t decode_ticket_bytes(int G);
 // Device address of the current device's status word (nullptr on failure).
 unsigned* device_status_word();
 
+// SM count of the current device (0 on failure).
+int device_sm_count();
+
 }  // namespace attn
