@@ -383,8 +383,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lw > 0.f) l_row += lw * ex2(sm.part[w][0][r] - m_fin);
     }
     const float inv = (l_row == 0.f) ? 0.f : 1.f / l_row;
+    // O / l leaves through a per-warp staging area in the (now idle) K/V
+    // ring so that the global stores are whole row runs: each thread writes
+    // its row's kHalfD values (16-byte unit u at u ^ (row & 7), which spreads
+    // a warp's writes over all banks), then the warp stores rows out.
     constexpr int kHalfD = D / 2;  // output columns per group
-    float* orow = a.out + qi * a.out_row_stride + (long long)h * D + grp * kHalfD;
+    float* stage = reinterpret_cast<float*>(ring) + (warp - 4) * 32 * kHalfD;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the ring was last written by TMA
 #pragma unroll
     for (int c = 0; c < kHalfD / 32; ++c) {
       uint32_t o[32];
@@ -396,12 +401,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
-      if (row_ok) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(orow + 32 * c + e) =
-              make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                          __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+      for (int e = 0; e < 32; e += 4) {
+        const int u = (32 * c + e) / 4;
+        *reinterpret_cast<float4*>(stage + lane * kHalfD + 4 * (u ^ (lane & 7))) =
+            make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv, __uint_as_float(o[e + 2]) * inv,
+                        __uint_as_float(o[e + 3]) * inv);
+      }
+    }
+    __syncwarp();
+    {
+      constexpr int kLanesPerRow = kHalfD / 4;
+      constexpr int kRowsPerStore = 32 / kLanesPerRow;
+      const int lg = __ffs(gs) - 1;  // gs is a power of two
+      const int u = lane % kLanesPerRow;
+#pragma unroll 4
+      for (int i = 0; i < 32 / kRowsPerStore; ++i) {
+        const int t = kRowsPerStore * i + lane / kLanesPerRow;  // row within the warp
+        const long long pk = (long long)blk * kRows + 32 * (warp & 3) + t;
+        const long long qq = pk >> lg;
+        if (qq < a.n_q) {
+          const float4 v = *reinterpret_cast<const float4*>(stage + t * kHalfD + 4 * (u ^ (t & 7)));
+          *reinterpret_cast<float4*>(a.out + qq * a.out_row_stride + (long long)(g * gs + (int)(pk & (gs - 1))) * D +
+                                     grp * kHalfD + 4 * u) = v;
+        }
       }
     }
     if (grp == 0 && row_ok && a.lse != nullptr) {
@@ -452,10 +475,10 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const void* kp = a.q;  // an empty key set never reads K/V: any aligned base will do
   const void* vp = a.q;
   if (!no_keys) {
-    // K and V as bf16 in stream-ordered temporary memory, released on the
-    // same stream once the attention kernel has run.
+    // K and V as bf16 in stream-ordered scratch memory (library pool),
+    // released on the same stream once the attention kernel has run.
     const long long elems = kv_rows * a.kv_row_stride;
-    if (cudaMallocAsync(&scratch, (size_t)elems * 4, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (scratch_alloc(&scratch, (size_t)elems * 4, s) != cudaSuccess) return ATTN_ERR_CUDA;
     uint16_t* k16 = static_cast<uint16_t*>(scratch);
     uint16_t* v16 = k16 + elems;
     const float4* k4 = reinterpret_cast<const float4*>(a.k);
@@ -467,7 +490,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
     const int sms = device_sm_count() > 0 ? device_sm_count() : 152;
     if (launch_pdl(reinterpret_cast<const void*>(kv_to_bf16_kernel), dim3(4 * sms), dim3(256), 0, s, cargs) !=
         cudaSuccess) {
-      cudaFreeAsync(scratch, s);
+      scratch_free(scratch, s);
       return ATTN_ERR_CUDA;
     }
     kp = k16;
@@ -502,7 +525,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
         rc = ATTN_ERR_CUDA;
     }
   }
-  if (scratch != nullptr && cudaFreeAsync(scratch, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+  if (scratch != nullptr && scratch_free(scratch, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
   return rc;
 }
 

@@ -383,7 +383,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_barrier(1, kSoftmaxThreads);
     const float l_row = sm.red_l[0][r] + sm.red_l[1][r];
     const float inv = (l_row == 0.f) ? 0.f : 1.f / l_row;
-    float* orow = a.out + qi * a.out_row_stride + (long long)h * D + grp * kHalfD;
+    // O / l leaves through a per-warp staging area in the (now idle) K/V
+    // ring so that the global stores are whole row runs: each thread writes
+    // its row's kHalfD values (16-byte unit u at u ^ (row & 7), which spreads
+    // a warp's writes over all banks), then the warp stores rows out.
+    float* stage = reinterpret_cast<float*>(sm.ring) + (warp - 4) * 32 * kHalfD;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the ring was last written by TMA
 #pragma unroll
     for (int c = 0; c < kHalfD / 32; ++c) {
       uint32_t o[32];
@@ -395,12 +400,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
-      if (row_ok) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(orow + 32 * c + e) =
-              make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                          __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+      for (int e = 0; e < 32; e += 4) {
+        const int u = (32 * c + e) / 4;
+        *reinterpret_cast<float4*>(stage + lane * kHalfD + 4 * (u ^ (lane & 7))) =
+            make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv, __uint_as_float(o[e + 2]) * inv,
+                        __uint_as_float(o[e + 3]) * inv);
+      }
+    }
+    __syncwarp();
+    {
+      constexpr int kLanesPerRow = kHalfD / 4;
+      constexpr int kRowsPerStore = 32 / kLanesPerRow;
+      const int lg = __ffs(gs) - 1;  // gs is a power of two
+      const int u = lane % kLanesPerRow;
+#pragma unroll 4
+      for (int i = 0; i < 32 / kRowsPerStore; ++i) {
+        const int t = kRowsPerStore * i + lane / kLanesPerRow;  // row within the warp
+        const long long pk = (long long)blk * kRows + 32 * (warp & 3) + t;
+        const long long qq = pk >> lg;
+        if (qq < a.n_q) {
+          const float4 v = *reinterpret_cast<const float4*>(stage + t * kHalfD + 4 * (u ^ (t & 7)));
+          *reinterpret_cast<float4*>(a.out + qq * a.out_row_stride + (long long)(g * gs + (int)(pk & (gs - 1))) * D +
+                                     grp * kHalfD + 4 * u) = v;
+        }
       }
     }
     if (grp == 0 && row_ok && a.lse != nullptr) {

@@ -90,6 +90,11 @@ size_t decode_ticket_bytes(int G);
 // Device address of the current device's status word (nullptr on failure).
 unsigned* device_status_word();
 
+// Stream-ordered scratch memory from a library-owned pool on the current
+// device that keeps freed memory reserved between calls.
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);
+cudaError_t scratch_free(void* p, cudaStream_t s);
+
 // SM count of the current device (0 on failure).
 int device_sm_count();
 

@@ -65,6 +65,45 @@ cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, c
   return cudaLaunchKernelExC(&cfg, kernel, args);
 }
 
+namespace {
+// One stream-ordered memory pool per device for kernel scratch.  Its release
+// threshold is unbounded, so memory freed at the end of a call stays
+// reserved for the next one instead of being returned (and re-mapped) at
+// every synchronisation.
+constexpr int kMaxDevices = 64;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+std::mutex g_pool_mu;
+
+cudaMemPool_t scratch_pool() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  if (g_pool[dev] == nullptr) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = ~0ull;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return nullptr;
+    }
+    g_pool[dev] = pool;
+  }
+  return g_pool[dev];
+}
+}  // namespace
+
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s) {
+  cudaMemPool_t pool = scratch_pool();
+  if (pool == nullptr) return cudaErrorMemoryAllocation;
+  return cudaMallocFromPoolAsync(p, bytes, pool, s);
+}
+
+cudaError_t scratch_free(void* p, cudaStream_t s) { return cudaFreeAsync(p, s); }
+
 bool set_smem_limit(const void* kernel, size_t bytes) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;

@@ -20,8 +20,9 @@
  *   Data       fp32 in, fp32 out, row-major, all pointers are DEVICE memory
  *              owned by the caller.  The library keeps no pointer after a call
  *              returns.  The only device memory it allocates is the ATTN_BF16
- *              path's temporary bf16 copy of K and V (stream-ordered:
- *              cudaMallocAsync and cudaFreeAsync on the call's stream).
+ *              path's temporary bf16 copy of K and V: stream-ordered on the
+ *              call's stream, from a memory pool the library creates per
+ *              device and keeps (freed blocks stay reserved for later calls).
  *   Streams    every call is asynchronous on `stream` (a cudaStream_t; NULL is
  *              the legacy default stream).  Results are ready when the stream
  *              has reached the call.
