@@ -65,7 +65,6 @@ int run_flash(const FlashArgs& a, int prec, cudaStream_t s) {
 }  // namespace
 
 unsigned* device_status_word() { return status_ptr(); }
-int device_sm_count() { return sm_count(); }
 
 }  // namespace attn
 

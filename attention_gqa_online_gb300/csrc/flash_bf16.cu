@@ -445,17 +445,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// K and V fp32 -> bf16 in one pass: n4 groups of four values from each (both
-// sources 16-byte aligned).
+// K and V fp32 -> bf16 in one pass.  A block converts kConvPer * 256
+// consecutive float4 groups of each tensor; thread t takes groups t, t+256,
+// ... (coalesced), all loads issued before the first store; n4 groups of four
+// values per tensor, both sources 16-byte aligned.
+constexpr int kConvPer = 4;
 __global__ void __launch_bounds__(256) kv_to_bf16_kernel(const float4* __restrict__ k, const float4* __restrict__ v,
                                                          uint2* __restrict__ k16, uint2* __restrict__ v16, long long n4) {
   allow_dependent_launch();
   grid_dependency_wait();
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
-    const float4 x = k[i], y = v[i];
-    k16[i] = make_uint2(tc::pack_bf16(x.x, x.y), tc::pack_bf16(x.z, x.w));
-    v16[i] = make_uint2(tc::pack_bf16(y.x, y.y), tc::pack_bf16(y.z, y.w));
+  const long long base = (long long)blockIdx.x * (kConvPer * 256) + threadIdx.x;
+  float4 x[kConvPer], y[kConvPer];
+#pragma unroll
+  for (int t = 0; t < kConvPer; ++t) {
+    const long long i = base + 256 * t;
+    if (i < n4) {
+      x[t] = k[i];
+      y[t] = v[i];
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kConvPer; ++t) {
+    const long long i = base + 256 * t;
+    if (i < n4) {
+      k16[i] = make_uint2(tc::pack_bf16(x[t].x, x[t].y), tc::pack_bf16(x[t].z, x[t].w));
+      v16[i] = make_uint2(tc::pack_bf16(y[t].x, y[t].y), tc::pack_bf16(y[t].z, y[t].w));
+    }
   }
 }
 
@@ -487,8 +502,8 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
     uint2* v2 = reinterpret_cast<uint2*>(v16);
     long long n4 = elems / 4;
     void* cargs[] = {&k4, &v4, &k2, &v2, &n4};
-    const int sms = device_sm_count() > 0 ? device_sm_count() : 152;
-    if (launch_pdl(reinterpret_cast<const void*>(kv_to_bf16_kernel), dim3(4 * sms), dim3(256), 0, s, cargs) !=
+    const long long blocks = (n4 + kConvPer * 256 - 1) / (kConvPer * 256);
+    if (launch_pdl(reinterpret_cast<const void*>(kv_to_bf16_kernel), dim3((unsigned)blocks), dim3(256), 0, s, cargs) !=
         cudaSuccess) {
       scratch_free(scratch, s);
       return ATTN_ERR_CUDA;

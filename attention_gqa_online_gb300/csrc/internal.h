@@ -95,7 +95,4 @@ unsigned* device_status_word();
 cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);
 cudaError_t scratch_free(void* p, cudaStream_t s);
 
-// SM count of the current device (0 on failure).
-int device_sm_count();
-
 }  // namespace attn

@@ -425,8 +425,8 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
                 "traffic": None, "kernel": kernel,
                 "peak_source": "fp32 FMA: %d SMs x 128 lanes x 2 x %.0f MHz" % (sms, sm_mhz)}
 
-    variants = ((A.ATTN_TF32, "tf32", "flash_tc_kernel<128,false> (tf32)"),
-                (A.ATTN_BF16, "bf16", "flash_tc_kernel<128,true> (bf16) + to_bf16 pre-pass"),
+    variants = ((A.ATTN_TF32, "tf32", "flash_tc_kernel<128> (tf32)"),
+                (A.ATTN_BF16, "bf16", "flash_bf16_kernel<128> (bf16) + kv_to_bf16 pre-pass"),
                 (A.ATTN_FP32, "fp32", "flash_simt_kernel<128,true>"))
 
     if only in ("all", "prefill"):
