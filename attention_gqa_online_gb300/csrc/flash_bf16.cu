@@ -12,16 +12,13 @@
 // One CTA owns 128 packed rows of one kv head g: row r is (query i, head
 // g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs query
 // heads that share it.  Keys are walked in tiles of 128.  Three score buffers
-// in tensor memory let Q K^T run up to three tiles ahead of P V, and the two
-// softmax warpgroups take the tiles in turn (even / odd), one thread per row,
-// so one group's exponentials overlap the other's and both overlap the
-// products.  The reference max of the online softmax is shared: the group
-// working on tile j takes the value after tile j-1 from shared memory (an
-// mbarrier per tile parity orders the hand-over), moves it only when the tile
-// max exceeds it by more than 8 (so P <= 256), publishes it, and when it moved
-// rescales the single O accumulator once P V of tile j-1 has landed.  Each
-// group keeps the row sum of its own tiles against the reference it last
-// used; the two are combined at the end.
+// in tensor memory let Q K^T run up to three tiles ahead of P V, so the
+// softmax of one tile overlaps the products of the others.  The two softmax
+// warpgroups split every tile's columns (64 each) and swap their partial row
+// maxima through shared memory, so both hold the same reference max; it only
+// moves when a row's tile max exceeds it by more than 8 (so P <= 256), and
+// when it moves each group rescales its half of the single O accumulator
+// once P V of the previous tile has landed.
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: K tile (128 keys x D, 128-byte swizzle, K-major)
@@ -32,8 +29,8 @@
 //               has released that buffer.
 //   warp 2      issues O += P_j V_j (A = P in TMEM over S_(j%3), B = V
 //               tile) in tile order once P_j is written.
-//   warps 4-7   softmax of the even tiles, warps 8-11 of the odd ones; warp
-//               w covers rows 32(w%4)..+31 (its TMEM lanes).
+//   warps 4-11  softmax, two warpgroups: warp w of group c covers rows
+//               32(w%4)..+31 (its TMEM lanes) and score columns 64c..64c+63.
 // The issuing warps run their loops warp-uniformly; one elected lane issues.
 // Tensor memory (512 columns): S_b [128 b, 128 b + 128) for b = 0..2, O
 // [384, 384 + D).  Scores are in base-2 units (Q is pre-multiplied by
@@ -64,13 +61,12 @@ struct __align__(1024) Bf16Smem {
   uint64_t s_full[kSBuf];
   uint64_t p_ready[kSBuf];
   uint64_t pv_done[2];     // P V of tile j completes phase j/2 of pv_done[j & 1]
-  uint64_t m_ready[2];     // reference max after tile j published: phase j/2 of m_ready[j & 1]
   uint64_t q_full;         // the fp32 Q block has landed in the staging area
   uint64_t q_ready;        // the bf16 Q tile is written
   uint64_t o_final;        // every P V has completed
   uint64_t drain[2];
-  float m_pub[2][kRows];   // reference max after tile j, slot j & 1
-  float part[2][3][kRows];  // [group][reference of l, true max, l][row], for the epilogue
+  float red_max[2][2][kRows];  // [tile parity][group][row] partial tile maxima
+  float red_l[2][kRows];       // [group][row] partial row sums (epilogue)
   uint32_t tmem_base;
   int abort;
 };
@@ -124,11 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < kSBuf; ++b) {
       mbar_init(&sm.s_full[b], 1);
-      mbar_init(&sm.p_ready[b], 4);
+      mbar_init(&sm.p_ready[b], 8);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.pv_done[b], 1);
-      mbar_init(&sm.m_ready[b], 4);
       mbar_init(&sm.drain[b], 1);
     }
     mbar_init(&sm.q_full, 1);
@@ -243,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
-    const int grp = (warp - 4) >> 2;           // group 0: even tiles, 1: odd tiles
+    const int grp = (warp - 4) >> 2;           // column group 0 or 1
     const int r = 32 * (warp & 3) + lane;      // row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const long long packed = (long long)blk * kRows + r;
@@ -276,57 +271,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(&sm.q_ready);
 
     const uint32_t o_col = tmem + lane_base + kColO;
-    float m_l = -INFINITY;   // reference of l (the shared reference at this group's last tile)
-    float m_true = -INFINITY, l = 0.f;
-    for (int j = grp; j < nt; j += 2) {
+    constexpr int kHalfD = D / 2;  // O columns per group
+    float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
+    for (int j = 0; j < nt; ++j) {
       const int b = j % kSBuf;
-      const uint32_t s_col = tmem + lane_base + kKeys * b;
+      const uint32_t s_col = tmem + lane_base + kKeys * b + 64 * grp;
       mbar_wait_bounded(&sm.s_full[b], (unsigned)((j / kSBuf) & 1), a.status, &sm.abort);
       tc::fence_after_sync();
-      uint32_t s[4][32];
+      uint32_t s[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_col + 32 * c, s[c]);
+      for (int c = 0; c < 2; ++c) tc::tmem_ld32(s_col + 32 * c, s[c]);
       tc::tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::reg_fence(s[c]);
+      for (int c = 0; c < 2; ++c) tc::reg_fence(s[c]);
 
       if ((j + 1) * kKeys > n_min) {  // the tile crosses some row's window end
-        const int lim = n_r - j * kKeys;
+        const int lim = n_r - (j * kKeys + 64 * grp);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (32 * c + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < kKeys; i += 8)
+      for (int i = 0; i < 64; i += 8)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mx[k] = max3(mx[k], __uint_as_float(s[i >> 5][(i & 31) + 2 * k]), __uint_as_float(s[i >> 5][(i & 31) + 2 * k + 1]));
-      const float tmax = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      sm.red_max[j & 1][grp][r] = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      named_barrier(1, kSoftmaxThreads);  // both halves of every row are read and maxed
+      const float tmax = fmaxf(sm.red_max[j & 1][0][r], sm.red_max[j & 1][1][r]);
       m_true = fmaxf(m_true, tmax);
+      const float m_prev = m_ref;
+      if (tmax > m_ref + kRescaleThreshold) m_ref = tmax;  // also for the first finite tile max
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
-      // Shared reference: the value after tile j-1, moved if this tile's max
-      // exceeds it by more than the threshold (also for the first finite max).
-      float m_prev = -INFINITY;
-      if (j >= 1) {
-        mbar_wait_bounded(&sm.m_ready[(j - 1) & 1], (unsigned)(((j - 1) >> 1) & 1), a.status, &sm.abort);
-        m_prev = sm.m_pub[(j - 1) & 1][r];
-      }
-      const float m_new = (tmax > m_prev + kRescaleThreshold) ? tmax : m_prev;
-      sm.m_pub[j & 1][r] = m_new;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.m_ready[j & 1]);
-      const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
-
-      // P = 2^(S - m) as bf16 pairs over the first 64 columns of S_b (every
-      // column of this row was read above): the 32 values of chunk c become
-      // 16 words, packed in place into s[c] and stored at column 16 c.  The
-      // row sum is taken in fp32.
+      // P = 2^(S - m) as bf16 pairs: this group's 64 values become 32
+      // columns at 32 grp of S_b (the other group has read its scores: the
+      // barrier above).  Chunk c's 32 values are packed in place into s[c]
+      // and stored at column 32 grp + 16 c.  The row sum is taken in fp32.
       float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float x0 = __uint_as_float(s[c][e]), x1 = __uint_as_float(s[c][e + 1]);
@@ -336,29 +323,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           add2(sum[2 * k], sum[2 * k + 1], p0, p1);
           s[c][e >> 1] = tc::pack_bf16(p0, p1);
         }
-        tc::tmem_st16(s_col + 16 * c, s[c]);
+        tc::tmem_st16(tmem + lane_base + kKeys * b + 32 * grp + 16 * c, s[c]);
       }
       const float tsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-      // This group's row sum, moved to the new reference (m_l <= m_new).
-      l = (l == 0.f ? 0.f : l * ex2(m_l - m_new)) + tsum;
-      m_l = m_new;
+      const float corr = (m_ref != m_prev) ? ex2(m_prev - m_ref) : 1.f;  // m_prev = -inf gives 0
+      l = l * corr + tsum;
 
       // O holds tiles 0..j-1 against m_prev once P V of tile j-1 has landed;
-      // P V of tile j waits for p_ready.  Rescale when any row of the warp
-      // moved its reference.
-      if (j >= 1 && __any_sync(0xffffffffu, m_new != m_prev)) {
-        const float corr = (m_new != m_prev) ? ex2(m_prev - m_new) : 1.f;  // m_prev = -inf gives 0
+      // P V of tile j waits for p_ready.  Rescale this group's half of O when
+      // any row of the warp moved its reference.
+      if (j >= 1 && __any_sync(0xffffffffu, m_ref != m_prev)) {
         mbar_wait_bounded(&sm.pv_done[(j - 1) & 1], (unsigned)(((j - 1) >> 1) & 1), a.status, &sm.abort);
         tc::fence_after_sync();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < kHalfD / 32; ++c) {
           uint32_t o[32];
-          tc::tmem_ld32(o_col + 32 * c, o);
+          tc::tmem_ld32(o_col + grp * kHalfD + 32 * c, o);
           tc::tmem_ld_wait();
           tc::reg_fence(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-          tc::tmem_st32(o_col + 32 * c, o);
+          tc::tmem_st32(o_col + grp * kHalfD + 32 * c, o);
         }
       }
       tc::tmem_st_wait();
@@ -368,26 +353,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // Epilogue: out = O / l, lse = (max, log sum).
-    sm.part[grp][0][r] = m_l;
-    sm.part[grp][1][r] = m_true;
-    sm.part[grp][2][r] = l;
+    sm.red_l[grp][r] = l;
     if (nt > 0) mbar_wait_bounded(&sm.o_final, 0, a.status, &sm.abort);
     tc::fence_before_sync();
     named_barrier(1, kSoftmaxThreads);
     tc::fence_after_sync();
-    const float m_fin = nt > 0 ? sm.m_pub[(nt - 1) & 1][r] : -INFINITY;
-    float l_row = 0.f;
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      const float lw = sm.part[w][2][r];
-      if (lw > 0.f) l_row += lw * ex2(sm.part[w][0][r] - m_fin);
-    }
+    const float l_row = sm.red_l[0][r] + sm.red_l[1][r];
     const float inv = (l_row == 0.f) ? 0.f : 1.f / l_row;
     // O / l leaves through a per-warp staging area in the (now idle) K/V
     // ring so that the global stores are whole row runs: each thread writes
     // its row's kHalfD values (16-byte unit u at u ^ (row & 7), which spreads
     // a warp's writes over all banks), then the warp stores rows out.
-    constexpr int kHalfD = D / 2;  // output columns per group
     float* stage = reinterpret_cast<float*>(ring) + (warp - 4) * 32 * kHalfD;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the ring was last written by TMA
 #pragma unroll
@@ -428,11 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (grp == 0 && row_ok && a.lse != nullptr) {
-      const float mt = fmaxf(sm.part[0][1][r], sm.part[1][1][r]);
       float* l2 = a.lse + (qi * a.H + h) * 2;
       const bool empty = (l_row == 0.f);
-      l2[0] = empty ? kEmptyLse : mt * kLn2;
-      l2[1] = empty ? kEmptyLse : logf(l_row) + (m_fin - mt) * kLn2;
+      l2[0] = empty ? kEmptyLse : m_true * kLn2;
+      l2[1] = empty ? kEmptyLse : logf(l_row) + (m_ref - m_true) * kLn2;
     }
   }
 
