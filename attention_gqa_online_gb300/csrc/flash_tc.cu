@@ -20,10 +20,13 @@
 //               elements needs the 128-byte swizzle of 32-byte atoms) into a
 //               192 KB shared-memory ring three tiles deep, in the order the
 //               MMAs consume them.
-//   warp 1      tensor-memory allocation; one thread issues every MMA:
-//                 S_b = Q K_j^T      (A = Q in TMEM, B = K tile)      M=128 N=128
-//                 O  += P_j V_j      (A = P in TMEM over S_b, B = V)  M=128 N=D
-//               in the fixed order Q K_0, Q K_1, P V_0, Q K_2, P V_1, ...
+//   warp 1      tensor-memory allocation; issues S_(j%2) = Q K_j^T
+//               (A = Q in TMEM, B = K tile, M=128 N=128) once P V of tile
+//               j-2 has released that buffer.
+//   warp 2      issues O += P_j V_j (A = P in TMEM over S_(j%2), B = V,
+//               M=128 N=D) in tile order once both softmax groups wrote P_j.
+//               The issuing warps run their loops warp-uniformly; one elected
+//               lane issues.
 //   warps 4-11  softmax, two warpgroups: warp w of group c handles rows
 //               32(w%4)..+31 (TMEM lanes) and score columns 64c..64c+63.  The
 //               two halves of a row swap their tile max through shared
@@ -66,7 +69,7 @@ struct __align__(1024) TcSmem {
   uint64_t pv_done[kSBuf];
   uint64_t q_full;   // the fp32 Q block has landed in the staging slot
   uint64_t q_ready;  // Q is in tensor memory
-  uint64_t drain;
+  uint64_t drain[2];
   float red_max[2][2][kRows];  // [tile parity][group][row] partial tile maxima
   float red_l[2][kRows];       // [group][row] partial row sums (epilogue)
   uint32_t tmem_base;
@@ -126,7 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_ready, 8);
-    mbar_init(&sm.drain, 1);
+    mbar_init(&sm.drain[0], 1);
+    mbar_init(&sm.drain[1], 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -167,10 +171,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(&sm.kv_full[s], (unsigned)((last / kRing) & 1), a.status);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the issue loop (warp-uniform values); one elected
-    // lane issues each MMA and commit.
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issue
+    // Warp 1 issues Q K^T, warp 2 P V, each in tile order.  The whole warp
+    // runs its loop (warp-uniform values); one elected lane issues each MMA
+    // and commit.
     if (nt > 0) {
       constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtTF32, false, kRows, kKeys);
       constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtTF32, true, kRows, D);
@@ -232,20 +237,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit_elect(&sm.kv_empty[p % kRing]);
         return true;
       };
-      // Fixed order Q K_0, Q K_1, P V_0, Q K_2, P V_1, ...: Q K of the next
-      // tile runs while the softmax of the current one does.  Every wait
-      // blocks in hardware (a loop of test-waits competes with the tensor
-      // core for shared memory and notices completions late).
-      bool ok = wait(&sm.q_ready, 0);
-      tc::fence_after_sync();
-      ok = ok && issue_qk(0) && (nt < 2 || issue_qk(1));
-      for (int j = 0; ok && j < nt; ++j) {
-        ok = issue_pv(j);
-        if (ok && j + 2 < nt) ok = issue_qk(j + 2);
+      // Every wait blocks in hardware (a loop of test-waits competes with
+      // the tensor core for shared memory and notices completions late).
+      if (warp == 1) {
+        bool ok = wait(&sm.q_ready, 0);
+        tc::fence_after_sync();
+        for (int j = 0; ok && j < nt; ++j) ok = issue_qk(j);
+      } else {
+        bool ok = true;
+        for (int j = 0; ok && j < nt; ++j) ok = issue_pv(j);
       }
       // Every MMA has finished before tensor memory is released.
-      tc::commit_elect(&sm.drain);
-      mbar_wait_bounded(&sm.drain, 0, a.status);
+      tc::commit_elect(&sm.drain[warp - 1]);
+      mbar_wait_bounded(&sm.drain[warp - 1], 0, a.status);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
