@@ -32,13 +32,13 @@ def load(lib_path=None):
     lib.oracle_forward.restype = _c_int
     lib.oracle_forward.argtypes = [_f32p, _f32p, _f32p, _f64p, ctypes.c_void_p,
                                    _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
-                                   ctypes.c_void_p, _c_int]
+                                   ctypes.c_void_p, _c_int, _c_int]
     lib.oracle_decode.restype = _c_int
     lib.oracle_decode.argtypes = [_f32p, _f32p, _f32p, ctypes.c_uint, _f64p,
-                                  _c_int, _c_int, _c_int, _c_int]
+                                  _c_int, _c_int, _c_int, _c_int, _c_int]
     lib.oracle_prefill.restype = _c_int
     lib.oracle_prefill.argtypes = [_f32p, _f32p, _f32p, _f64p] + [_c_int] * 6 + \
-        [ctypes.c_float] + [_c_int] * 4 + [ctypes.c_void_p, _c_int]
+        [ctypes.c_float] + [_c_int] * 4 + [ctypes.c_void_p, _c_int, _c_int]
     lib.oracle_num_threads.restype = _c_int
     lib.oracle_num_threads.argtypes = []
     return lib
@@ -60,32 +60,33 @@ class Oracle:
         arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
         return arr.ctypes.data_as(ctypes.c_void_p), int(arr.size), arr
 
-    def forward(self, q, k, v, q_seq, kv_seq, H, G, D, mask, rows=None, want_lse=True):
-        """Returns (out [q_seq, H*D], lse [q_seq, H, 2]); rows not listed stay NaN."""
+    def forward(self, q, k, v, q_seq, kv_seq, H, G, D, mask, rows=None, want_lse=True, window=0):
+        """Returns (out [q_seq, H*D], lse [q_seq, H, 2]); rows not listed stay NaN.
+        window > 0 keeps the last `window` keys of every row's window."""
         q, k, v = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v))
         out = np.full((max(q_seq, 0), H * D), np.nan)
         lse = np.full((max(q_seq, 0), H, 2), np.nan)
         rp, nr, keep = self._rows(rows)
         rc = self.lib.oracle_forward(q.reshape(-1), k.reshape(-1), v.reshape(-1), out.reshape(-1),
                                      lse.ctypes.data_as(ctypes.c_void_p) if want_lse else None,
-                                     q_seq, kv_seq, H, G, D, mask, rp, nr)
+                                     q_seq, kv_seq, H, G, D, mask, rp, nr, int(window))
         del keep
         if rc != 0:
             raise ValueError("oracle_forward rejected its arguments")
         return out, lse
 
-    def decode(self, q, k_cache, v_cache, kv_pos, H, G, D, max_seq):
+    def decode(self, q, k_cache, v_cache, kv_pos, H, G, D, max_seq, window=0):
         """Returns out [1, H*D]."""
         q, k_cache, v_cache = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k_cache, v_cache))
         out = np.full((1, H * D), np.nan)
         rc = self.lib.oracle_decode(q.reshape(-1), k_cache.reshape(-1), v_cache.reshape(-1),
-                                    int(kv_pos), out.reshape(-1), H, G, D, max_seq)
+                                    int(kv_pos), out.reshape(-1), H, G, D, max_seq, int(window))
         if rc != 0:
             raise ValueError("oracle_decode rejected its arguments")
         return out
 
     def prefill(self, q_batch, k_cache, v_cache, out_rows, n_queries, H, G, D, kv_dim, max_seq,
-                scale, start_pos, q_stride, out_stride, q_base, rows=None):
+                scale, start_pos, q_stride, out_stride, q_base, rows=None, window=0):
         """Returns out_batch [out_rows, out_stride] (fp64, NaN where not written)."""
         q_batch, k_cache, v_cache = (np.ascontiguousarray(x, dtype=np.float32)
                                      for x in (q_batch, k_cache, v_cache))
@@ -93,7 +94,7 @@ class Oracle:
         rp, nr, keep = self._rows(rows)
         rc = self.lib.oracle_prefill(q_batch.reshape(-1), k_cache.reshape(-1), v_cache.reshape(-1),
                                      out.reshape(-1), n_queries, H, G, D, kv_dim, max_seq,
-                                     float(scale), start_pos, q_stride, out_stride, q_base, rp, nr)
+                                     float(scale), start_pos, q_stride, out_stride, q_base, rp, nr, int(window))
         del keep
         if rc != 0:
             raise ValueError("oracle_prefill rejected its arguments")

@@ -37,6 +37,11 @@
  *   prefill         n = min(start_pos + q_base + i + 1, max_seq)
  *                   attention_prefill.wgsl, fn attention_prefill (pos_q,
  *                   seq_len).
+ * Sliding window (every entry point's last argument, 0 = none): the window
+ * becomes keys [lo, n) with lo = max(0, n - window).  attention.wgsl's key
+ * loop starts at a $KV_START placeholder whose body the page leaves open; the
+ * plainest reading, taken here, is a per-row lower bound that keeps the last
+ * `window` positions of the row's window.
  *
  * Scores, exponentials and sums are fp64; the fp32 inputs are widened
  * exactly.  scale is 1/sqrt(head_dim) in fp64 for forward and decode (both
@@ -94,6 +99,13 @@ static void attend_row(const float *q, const float *k, const float *v,
     *logl_out = log(l);
 }
 
+/* First key of a row whose window ends at n (exclusive), under a sliding
+ * window of `window` keys (0 = no limit). */
+static size_t window_start(size_t n, int window)
+{
+    return (window > 0 && n > (size_t)window) ? n - (size_t)window : 0;
+}
+
 static int bad_heads(int H, int G, int D)
 {
     return H <= 0 || G <= 0 || D <= 0 || (H % G) != 0;
@@ -117,9 +129,9 @@ int oracle_num_threads(void)
  */
 int oracle_forward(const float *q, const float *k, const float *v,
                    double *out, double *lse, int q_seq, int kv_seq,
-                   int H, int G, int D, int mask, const int *rows, int n_rows)
+                   int H, int G, int D, int mask, const int *rows, int n_rows, int window)
 {
-    if (bad_heads(H, G, D) || q_seq < 0 || kv_seq < 0 || mask < 0 || mask > 2) return -1;
+    if (bad_heads(H, G, D) || q_seq < 0 || kv_seq < 0 || mask < 0 || mask > 2 || window < 0) return -1;
     if (mask != 2 && kv_seq != q_seq) return -1;
     if (rows == NULL) n_rows = q_seq;
     for (int r = 0; r < n_rows; ++r) {
@@ -143,10 +155,11 @@ int oracle_forward(const float *q, const float *k, const float *v,
                     const int pos = rows ? rows[r] : r;
                     const int g = h / gs;
                     size_t n = (mask == 0) ? (size_t)pos + 1 : (size_t)kv_seq;
+                    const size_t lo = window_start(n, window);
                     const size_t qo = (size_t)pos * H * D + (size_t)h * D;
                     double m, logl;
-                    attend_row(q + qo, k + (size_t)g * D, v + (size_t)g * D, kv_dim, n, D,
-                               scale, s, out + qo, &m, &logl);
+                    attend_row(q + qo, k + lo * kv_dim + (size_t)g * D, v + lo * kv_dim + (size_t)g * D, kv_dim,
+                               n - lo, D, scale, s, out + qo, &m, &logl);
                     if (lse) {
                         lse[((size_t)pos * H + h) * 2] = m;
                         lse[((size_t)pos * H + h) * 2 + 1] = logl;
@@ -165,9 +178,9 @@ int oracle_forward(const float *q, const float *k, const float *v,
  *   attends to key positions 0..kv_pos inclusive, clamped to max_seq rows.
  */
 int oracle_decode(const float *q, const float *k_cache, const float *v_cache,
-                  unsigned kv_pos, double *out, int H, int G, int D, int max_seq)
+                  unsigned kv_pos, double *out, int H, int G, int D, int max_seq, int window)
 {
-    if (bad_heads(H, G, D) || max_seq < 0) return -1;
+    if (bad_heads(H, G, D) || max_seq < 0 || window < 0) return -1;
     const int gs = H / G;
     const size_t kv_dim = (size_t)G * D;
     const double scale = 1.0 / sqrt((double)D);
@@ -175,11 +188,12 @@ int oracle_decode(const float *q, const float *k_cache, const float *v_cache,
     if (n > (size_t)max_seq) n = (size_t)max_seq;
     double *s = (double *)malloc(sizeof(double) * (n > 0 ? n : 1));
     if (s == NULL) return -1;
+    const size_t lo = window_start(n, window);
     for (int h = 0; h < H; ++h) {
         const int g = h / gs;
         double m, logl;
-        attend_row(q + (size_t)h * D, k_cache + (size_t)g * D, v_cache + (size_t)g * D,
-                   kv_dim, n, D, scale, s, out + (size_t)h * D, &m, &logl);
+        attend_row(q + (size_t)h * D, k_cache + lo * kv_dim + (size_t)g * D, v_cache + lo * kv_dim + (size_t)g * D,
+                   kv_dim, n - lo, D, scale, s, out + (size_t)h * D, &m, &logl);
     }
     free(s);
     return 0;
@@ -196,9 +210,9 @@ int oracle_decode(const float *q, const float *k_cache, const float *v_cache,
 int oracle_prefill(const float *q_batch, const float *k_cache, const float *v_cache,
                    double *out_batch, int n_queries, int H, int G, int D, int kv_dim,
                    int max_seq, float scale, int start_pos, int q_stride, int out_stride,
-                   int q_base, const int *rows, int n_rows)
+                   int q_base, const int *rows, int n_rows, int window)
 {
-    if (bad_heads(H, G, D) || n_queries < 0 || max_seq < 0 || start_pos < 0 || q_base < 0)
+    if (bad_heads(H, G, D) || n_queries < 0 || max_seq < 0 || start_pos < 0 || q_base < 0 || window < 0)
         return -1;
     if (kv_dim < G * D || q_stride < H * D || out_stride < H * D) return -1;
     if (rows == NULL) n_rows = n_queries;
@@ -224,10 +238,11 @@ int oracle_prefill(const float *q_batch, const float *k_cache, const float *v_ca
                     size_t n = (size_t)start_pos + q_global + 1;
                     if (n > (size_t)max_seq) n = (size_t)max_seq;
                     const int g = h / gs;
+                    const size_t lo = window_start(n, window);
                     double m, logl;
                     attend_row(q_batch + q_global * q_stride + (size_t)h * D,
-                               k_cache + (size_t)g * D, v_cache + (size_t)g * D,
-                               (size_t)kv_dim, n, D, sc, s,
+                               k_cache + lo * kv_dim + (size_t)g * D, v_cache + lo * kv_dim + (size_t)g * D,
+                               (size_t)kv_dim, n - lo, D, sc, s,
                                out_batch + q_global * out_stride + (size_t)h * D, &m, &logl);
                 }
             }

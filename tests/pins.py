@@ -325,4 +325,105 @@ def pin_prefill_scale_argument(orc):
     assert np.max(np.abs(a[:, :H * D] - c[:, :H * D])) > 1e-3
 
 
+
+# ---------------------------------------------------------------- sliding window
+def _sdpa_banded(q, k, v, q_seq, kv_seq, H, G, D, ends, window):
+    """SDPA with an explicit boolean mask: row i attends keys [lo_i, ends[i]),
+    lo_i = max(0, ends[i] - window) (window 0 = no lower bound)."""
+    allow = np.zeros((q_seq, kv_seq), dtype=bool)
+    for i, n in enumerate(ends):
+        lo = max(0, n - window) if window > 0 else 0
+        allow[i, lo:n] = True
+    qt = torch.from_numpy(q.astype(np.float64)).reshape(q_seq, H, D).transpose(0, 1)[None]
+    kt = torch.from_numpy(k.astype(np.float64)).reshape(kv_seq, G, D).transpose(0, 1)[None]
+    vt = torch.from_numpy(v.astype(np.float64)).reshape(kv_seq, G, D).transpose(0, 1)[None]
+    o = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=torch.from_numpy(allow), enable_gqa=True)
+    return o[0].transpose(0, 1).reshape(q_seq, H * D).numpy()
+
+
+def pin_window_sdpa_forward(orc):
+    """Sliding window on all three masks against SDPA with a banded mask."""
+    q, k, v = _small(seed=20, q_seq=13, kv_seq=13, H=4, G=2, D=16)
+    for w in (1, 3, 5):
+        out, _ = orc.forward(q, k, v, 13, 13, 4, 2, 16, CAUSAL, window=w)
+        ref = _sdpa_banded(q, k, v, 13, 13, 4, 2, 16, [i + 1 for i in range(13)], w)
+        assert np.max(np.abs(out - ref)) < 1e-12
+        out, _ = orc.forward(q, k, v, 13, 13, 4, 2, 16, FULL, window=w)
+        ref = _sdpa_banded(q, k, v, 13, 13, 4, 2, 16, [13] * 13, w)
+        assert np.max(np.abs(out - ref)) < 1e-12
+    q, k, v = _small(seed=21, q_seq=5, kv_seq=19, H=6, G=3, D=8)
+    out, _ = orc.forward(q, k, v, 5, 19, 6, 3, 8, CROSS, window=7)
+    ref = _sdpa_banded(q, k, v, 5, 19, 6, 3, 8, [19] * 5, 7)
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def pin_window_streaming_lse(orc):
+    """The (max, log-sum) pair under a window follows the pages' recurrence run
+    over the kept keys only."""
+    q, k, v = _small(seed=22, q_seq=9, H=2, G=1, D=4, qk_sigma=3.0)
+    w = 4
+    out, lse = orc.forward(q, k, v, 9, 9, 2, 1, 4, CAUSAL, window=w)
+    for pos in range(9):
+        lo = max(0, pos + 1 - w)
+        for h in range(2):
+            ref, m, logl = _streaming_row(q[pos, h * 4:(h + 1) * 4], k[lo:pos + 1, :4], v[lo:pos + 1, :4], 0.5)
+            assert np.max(np.abs(out[pos, h * 4:(h + 1) * 4] - np.array(ref))) < 1e-12
+            assert abs(lse[pos, h, 0] - m) < 1e-12 and abs(lse[pos, h, 1] - logl) < 1e-12
+
+
+def pin_window_one_is_last_v(orc):
+    """window = 1 keeps only key n - 1: out = V[n-1] of the kv head, lse = (s, 0)."""
+    q, k, v = _small(seed=23, q_seq=6, kv_seq=10, H=2, G=1, D=8)
+    for mask, kv, ends in ((CAUSAL, 6, list(range(1, 7))), (CROSS, 10, [10] * 6)):
+        kk, vv = k[:kv], v[:kv]
+        out, lse = orc.forward(q, kk, vv, 6, kv, 2, 1, 8, mask, window=1)
+        for pos, n in enumerate(ends):
+            for h in range(2):
+                assert np.array_equal(out[pos, h * 8:(h + 1) * 8], vv[n - 1, :8].astype(np.float64))
+                s = float(np.dot(q[pos, h * 8:(h + 1) * 8].astype(np.float64),
+                                 kk[n - 1, :8].astype(np.float64))) / math.sqrt(8)
+                assert abs(lse[pos, h, 0] - s) < 1e-12 and lse[pos, h, 1] == 0.0
+
+
+def pin_window_wide_is_no_window(orc):
+    """A window at least as long as every row's window changes nothing."""
+    q, k, v = _small(seed=24, q_seq=11, H=4, G=2, D=16)
+    a = orc.forward(q, k, v, 11, 11, 4, 2, 16, CAUSAL)
+    for w in (11, 12, 1000):
+        b = orc.forward(q, k, v, 11, 11, 4, 2, 16, CAUSAL, window=w)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    c = orc.forward(q, k, v, 11, 11, 4, 2, 16, CAUSAL, window=10)
+    assert np.array_equal(a[0][:10], c[0][:10]) and not np.array_equal(a[0][10], c[0][10])
+
+
+def pin_window_decode_shifted_cache(orc):
+    """Decode with window W at kv_pos p equals decode without one on the cache
+    cut to start at p + 1 - W (the kept keys moved to the front)."""
+    H, G, D, max_seq = 4, 2, 16, 30
+    q, kc, vc = (_np(x) for x in synthetic.decode_inputs(max_seq, H, G, D, seed=25))
+    for p, w in ((20, 6), (5, 6), (29, 1), (40, 4)):
+        n = min(p + 1, max_seq)
+        lo = max(0, n - w)
+        a = orc.decode(q, kc, vc, p, H, G, D, max_seq, window=w)
+        b = orc.decode(q, np.ascontiguousarray(kc[lo:]), np.ascontiguousarray(vc[lo:]),
+                       n - 1 - lo, H, G, D, max_seq - lo)
+        assert np.max(np.abs(a - b)) < 1e-15
+
+
+def pin_window_prefill_matches_decode(orc):
+    """Prefill row i with a window equals decode at kv_pos = start_pos + q_base + i
+    with the same window, and differs from the unwindowed prefill."""
+    H, G, D, max_seq = 4, 2, 16, 40
+    qb, kc, vc = (_np(x) for x in synthetic.prefill_inputs(10, 80, max_seq, G * D, seed=26))
+    start, qbase, w = 20, 3, 5
+    scale = np.float32(1.0 / math.sqrt(D))
+    outp = orc.prefill(qb, kc, vc, 10, 7, H, G, D, G * D, max_seq, scale, start, 80, 80, qbase, window=w)
+    full = orc.prefill(qb, kc, vc, 10, 7, H, G, D, G * D, max_seq, scale, start, 80, 80, qbase)
+    for i in range(7):
+        qrow = qb[qbase + i, :H * D].reshape(1, H * D)
+        od = orc.decode(qrow, kc, vc, start + qbase + i, H, G, D, max_seq, window=w)
+        assert np.max(np.abs(outp[qbase + i, :H * D] - od[0])) < 1e-12
+    assert np.max(np.abs(outp[qbase:qbase + 7, :H * D] - full[qbase:qbase + 7, :H * D])) > 1e-3
+
+
 ALL_PINS = [obj for name, obj in sorted(globals().items()) if name.startswith("pin_")]

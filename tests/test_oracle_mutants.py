@@ -39,12 +39,17 @@ MUTANTS = [
      "size_t n = (size_t)start_pos + (size_t)i + 1;", False),
     ("prefill_no_clamp", "if (n > (size_t)max_seq) n = (size_t)max_seq;\n                    const int g",
      "const int g", False),
+    ("window_one_short", "return (window > 0 && n > (size_t)window) ? n - (size_t)window : 0;",
+     "return (window > 0 && n > (size_t)window) ? n - (size_t)window + 1 : 0;", False),
+    ("window_ignored", "return (window > 0 && n > (size_t)window) ? n - (size_t)window : 0;", "return 0;", False),
+    ("window_from_start", "attend_row(q + qo, k + lo * kv_dim + (size_t)g * D, v + lo * kv_dim + (size_t)g * D, kv_dim,\n                               n - lo,",
+     "attend_row(q + qo, k + (size_t)g * D, v + (size_t)g * D, kv_dim,\n                               n - lo,", False),
     ("decode_no_clamp", "if (n > (size_t)max_seq) n = (size_t)max_seq;\n    double *s", "double *s", False),
     ("decode_window_short", "size_t n = (size_t)kv_pos + 1;", "size_t n = (size_t)kv_pos;", False),
     ("prefill_out_uses_q_stride", "out_batch + q_global * out_stride", "out_batch + q_global * q_stride", False),
     ("prefill_scale_ignored", "const double sc = (double)scale;", "const double sc = 1.0 / sqrt((double)D);", False),
-    ("forward_kv_head_offset_dropped", "attend_row(q + qo, k + (size_t)g * D, v + (size_t)g * D,",
-     "attend_row(q + qo, k, v,", False),
+    ("forward_kv_head_offset_dropped", "attend_row(q + qo, k + lo * kv_dim + (size_t)g * D, v + lo * kv_dim + (size_t)g * D,",
+     "attend_row(q + qo, k + lo * kv_dim, v + lo * kv_dim,", False),
     ("query_head_is_kv_head", "(size_t)pos * H * D + (size_t)h * D;", "(size_t)pos * H * D + (size_t)(h / gs) * D;", False),
     ("first_key_skipped", "for (size_t t = 0; t < n; ++t) {\n        const float *kt",
      "for (size_t t = 1; t < n; ++t) {\n        const float *kt", False),
