@@ -49,6 +49,12 @@ def load_library(path=None):
     lib.attn_prefill.restype = ctypes.c_int
     lib.attn_prefill.argtypes = [_vp, _vp, _vp, _vp] + [_u32] * 6 + [ctypes.c_float] + \
         [_u32] * 4 + [ctypes.c_int, _vp]
+    lib.attn_forward_window.restype = ctypes.c_int
+    lib.attn_forward_window.argtypes = lib.attn_forward.argtypes[:-1] + [_u32, _vp]
+    lib.attn_decode_cached_window.restype = ctypes.c_int
+    lib.attn_decode_cached_window.argtypes = lib.attn_decode_cached.argtypes[:-1] + [_u32, _vp]
+    lib.attn_prefill_window.restype = ctypes.c_int
+    lib.attn_prefill_window.argtypes = lib.attn_prefill.argtypes[:-1] + [_u32, _vp]
     lib.attn_get_status.restype = ctypes.c_int
     lib.attn_get_status.argtypes = [_vp]
     lib.attn_status_string.restype = ctypes.c_char_p
@@ -101,6 +107,16 @@ def attn_forward(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads, head
         q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask, prec, _stream(stream)), "attn_forward")
 
 
+def attn_forward_window(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask, prec,
+                        window, stream=None):
+    """attn_forward restricted to each row's last `window` keys (0 = all); see attn_gqa.h."""
+    f = _f32()
+    _check(load_library().attn_forward_window(
+        _addr(q, "q", f), _addr(k, "k", f), _addr(v, "v", f), _addr(out, "out", f), _addr(lse, "lse", f),
+        q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask, prec, window, _stream(stream)),
+        "attn_forward_window")
+
+
 def attn_decode_workspace_bytes(num_heads, num_kv_heads, head_dim, max_seq):
     return int(load_library().attn_decode_workspace_bytes(num_heads, num_kv_heads, head_dim, max_seq))
 
@@ -120,6 +136,21 @@ def attn_decode_cached(q, k_cache, v_cache, kv_pos_dev, out, num_heads, num_kv_h
         _addr(workspace, "workspace"), workspace_bytes, _stream(stream)), "attn_decode_cached")
 
 
+def attn_decode_cached_window(q, k_cache, v_cache, kv_pos_dev, out, num_heads, num_kv_heads, head_dim, max_seq,
+                              workspace, workspace_bytes, window, stream=None):
+    """attn_decode_cached over the last `window` positions up to *kv_pos_dev (0 = all); see attn_gqa.h."""
+    f = _f32()
+    if hasattr(kv_pos_dev, "element_size") and kv_pos_dev.element_size() != 4:
+        raise ValueError("kv_pos_dev must hold one 32-bit unsigned position")
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load_library().attn_decode_cached_window(
+        _addr(q, "q", f), _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f),
+        _addr(kv_pos_dev, "kv_pos_dev"),
+        _addr(out, "out", f), num_heads, num_kv_heads, head_dim, max_seq,
+        _addr(workspace, "workspace"), workspace_bytes, window, _stream(stream)), "attn_decode_cached_window")
+
+
 def attn_prefill(q_batch, k_cache, v_cache, out_batch, n_queries, n_heads, n_kv_heads, head_dim, kv_dim,
                  max_seq, scale, start_pos, q_stride, out_stride, q_base, prec=ATTN_FP32, stream=None):
     """Batched causal prefill against a KV cache; see attn_gqa.h."""
@@ -128,6 +159,16 @@ def attn_prefill(q_batch, k_cache, v_cache, out_batch, n_queries, n_heads, n_kv_
         _addr(q_batch, "q_batch", f), _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f),
         _addr(out_batch, "out_batch", f), n_queries, n_heads, n_kv_heads, head_dim, kv_dim, max_seq,
         float(scale), start_pos, q_stride, out_stride, q_base, prec, _stream(stream)), "attn_prefill")
+
+
+def attn_prefill_window(q_batch, k_cache, v_cache, out_batch, n_queries, n_heads, n_kv_heads, head_dim, kv_dim,
+                        max_seq, scale, start_pos, q_stride, out_stride, q_base, prec, window, stream=None):
+    """attn_prefill restricted to each row's last `window` keys (0 = all); see attn_gqa.h."""
+    f = _f32()
+    _check(load_library().attn_prefill_window(
+        _addr(q_batch, "q_batch", f), _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f),
+        _addr(out_batch, "out_batch", f), n_queries, n_heads, n_kv_heads, head_dim, kv_dim, max_seq,
+        float(scale), start_pos, q_stride, out_stride, q_base, prec, window, _stream(stream)), "attn_prefill_window")
 
 
 def attn_decode_cached_noalloc(q, k_cache, v_cache, kv_pos_dev, out, num_heads, num_kv_heads, head_dim, max_seq,

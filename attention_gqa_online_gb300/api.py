@@ -7,26 +7,35 @@ from . import _binding as B
 
 
 def forward(q, k, v, num_heads, num_kv_heads, mask=B.ATTN_CAUSAL, prec=B.ATTN_FP32, want_lse=True,
-            stream=None):
-    """q [q_seq, H*D], k/v [kv_seq, G*D] (CUDA fp32) -> (out [q_seq, H*D], lse [q_seq, H, 2] or None)."""
+            stream=None, window=0):
+    """q [q_seq, H*D], k/v [kv_seq, G*D] (CUDA fp32) -> (out [q_seq, H*D], lse [q_seq, H, 2] or None).
+    window > 0 keeps each row's last `window` keys."""
     q_seq, kv_seq = q.shape[0], k.shape[0]
     D = q.shape[1] // num_heads
     out = torch.empty_like(q)
     lse = torch.empty((q_seq, num_heads, 2), device=q.device, dtype=torch.float32) if want_lse else None
-    B.attn_forward(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads, D, mask, prec, stream)
+    if window:
+        B.attn_forward_window(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads, D, mask, prec, window,
+                              stream)
+    else:
+        B.attn_forward(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads, D, mask, prec, stream)
     return out, lse
 
 
 def prefill(q_batch, k_cache, v_cache, n_queries, n_heads, n_kv_heads, head_dim, start_pos, q_base=0,
-            scale=None, out=None, prec=B.ATTN_FP32, stream=None):
+            scale=None, out=None, prec=B.ATTN_FP32, stream=None, window=0):
     """Causal prefill of rows q_base .. q_base+n_queries-1 of q_batch (row stride = its width)."""
     max_seq, kv_dim = k_cache.shape
     if out is None:
         out = torch.zeros((q_batch.shape[0], n_heads * head_dim), device=q_batch.device, dtype=torch.float32)
     if scale is None:
         scale = 1.0 / math.sqrt(head_dim)
-    B.attn_prefill(q_batch, k_cache, v_cache, out, n_queries, n_heads, n_kv_heads, head_dim, kv_dim, max_seq,
-                   scale, start_pos, q_batch.shape[1], out.shape[1], q_base, prec, stream)
+    if window:
+        B.attn_prefill_window(q_batch, k_cache, v_cache, out, n_queries, n_heads, n_kv_heads, head_dim, kv_dim,
+                              max_seq, scale, start_pos, q_batch.shape[1], out.shape[1], q_base, prec, window, stream)
+    else:
+        B.attn_prefill(q_batch, k_cache, v_cache, out, n_queries, n_heads, n_kv_heads, head_dim, kv_dim, max_seq,
+                       scale, start_pos, q_batch.shape[1], out.shape[1], q_base, prec, stream)
     return out
 
 
@@ -45,10 +54,15 @@ class DecodeState:
         self.kv_pos.fill_(int(kv_pos))
 
 
-def decode(state, q, k_cache, v_cache, out=None, stream=None):
-    """One decode step at the position held in state.kv_pos."""
+def decode(state, q, k_cache, v_cache, out=None, stream=None, window=0):
+    """One decode step at the position held in state.kv_pos (over its last
+    `window` positions when window > 0)."""
     if out is None:
         out = torch.empty_like(q)
-    B.attn_decode_cached(q, k_cache, v_cache, state.kv_pos, out, state.num_heads, state.num_kv_heads,
-                         state.head_dim, state.max_seq, state.workspace, None, stream)
+    if window:
+        B.attn_decode_cached_window(q, k_cache, v_cache, state.kv_pos, out, state.num_heads, state.num_kv_heads,
+                                    state.head_dim, state.max_seq, state.workspace, None, window, stream)
+    else:
+        B.attn_decode_cached(q, k_cache, v_cache, state.kv_pos, out, state.num_heads, state.num_kv_heads,
+                             state.head_dim, state.max_seq, state.workspace, None, stream)
     return out

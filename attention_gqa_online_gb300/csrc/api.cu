@@ -54,6 +54,9 @@ bool heads_ok(uint32_t H, uint32_t G, uint32_t D) {
   return H >= 1 && G >= 1 && H % G == 0 && D >= 1 && D <= 128 && H <= (1u << 20);
 }
 
+// A window longer than any key range is no limit at all.
+int window_arg(uint32_t window) { return window > 0x7fffffffu ? 0x7fffffff : (int)window; }
+
 bool valid_prec(int prec) { return prec == ATTN_FP32 || prec == ATTN_TF32 || prec == ATTN_BF16; }
 
 int run_flash(const FlashArgs& a, int prec, cudaStream_t s) {
@@ -70,9 +73,9 @@ unsigned* device_status_word() { return status_ptr(); }
 
 using namespace attn;
 
-extern "C" int attn_forward(const float* q, const float* k, const float* v, float* out, float* lse,
-                            uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
-                            uint32_t head_dim, int mask, int prec, attn_stream_t stream) {
+extern "C" int attn_forward_window(const float* q, const float* k, const float* v, float* out, float* lse,
+                                   uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
+                                   uint32_t head_dim, int mask, int prec, uint32_t window, attn_stream_t stream) {
   if (!heads_ok(num_heads, num_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
   if (mask != ATTN_CAUSAL && mask != ATTN_FULL && mask != ATTN_CROSS) return ATTN_ERR_INVALID_ARG;
   if (mask != ATTN_CROSS && kv_seq != q_seq) return ATTN_ERR_INVALID_ARG;
@@ -96,12 +99,20 @@ extern "C" int attn_forward(const float* q, const float* k, const float* v, floa
   a.base_pos = 0;
   a.cap = (int)kv_seq;
   a.n_all = (int)kv_seq;
+  a.window = window_arg(window);
   a.scale = 1.0f / sqrtf((float)head_dim);
   a.kv_pos_dev = nullptr;
   a.status = status_ptr();
   if (a.status == nullptr) return ATTN_ERR_CUDA;
   // An empty key set is handled by the same kernels (no tiles, zero rows).
   return run_flash(a, prec, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_forward(const float* q, const float* k, const float* v, float* out, float* lse,
+                            uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
+                            uint32_t head_dim, int mask, int prec, attn_stream_t stream) {
+  return attn_forward_window(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask, prec, 0,
+                             stream);
 }
 
 extern "C" size_t attn_decode_workspace_bytes(uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim,
@@ -113,10 +124,11 @@ extern "C" size_t attn_decode_workspace_bytes(uint32_t num_heads, uint32_t num_k
   return b > 0 ? b : 256;  // the generic path needs none; report a token size
 }
 
-extern "C" int attn_decode_cached(const float* q, const float* k_cache, const float* v_cache,
-                                  const uint32_t* kv_pos_dev, float* out, uint32_t num_heads,
-                                  uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq, void* workspace,
-                                  size_t workspace_bytes, attn_stream_t stream) {
+extern "C" int attn_decode_cached_window(const float* q, const float* k_cache, const float* v_cache,
+                                         const uint32_t* kv_pos_dev, float* out, uint32_t num_heads,
+                                         uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq,
+                                         void* workspace, size_t workspace_bytes, uint32_t window,
+                                         attn_stream_t stream) {
   if (!heads_ok(num_heads, num_kv_heads, head_dim) || max_seq == 0 || max_seq > 0x7fffffffu)
     return ATTN_ERR_INVALID_ARG;
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || kv_pos_dev == nullptr || out == nullptr)
@@ -143,6 +155,7 @@ extern "C" int attn_decode_cached(const float* q, const float* k_cache, const fl
     d.G = G;
     d.D = D;
     d.max_seq = ms;
+    d.window = window_arg(window);
     d.workspace = workspace;
     d.status = st;
     return launch_decode_split(d, decode_splits(G, ms, sms), s);
@@ -166,16 +179,26 @@ extern "C" int attn_decode_cached(const float* q, const float* k_cache, const fl
   a.base_pos = 0;
   a.cap = ms;
   a.n_all = ms;
+  a.window = window_arg(window);
   a.scale = 1.0f / sqrtf((float)D);
   a.kv_pos_dev = kv_pos_dev;
   a.status = st;
   return launch_flash_simt(a, s);
 }
 
-extern "C" int attn_prefill(const float* q_batch, const float* k_cache, const float* v_cache, float* out_batch,
-                            uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads, uint32_t head_dim,
-                            uint32_t kv_dim, uint32_t max_seq, float scale, uint32_t start_pos, uint32_t q_stride,
-                            uint32_t out_stride, uint32_t q_base, int prec, attn_stream_t stream) {
+extern "C" int attn_decode_cached(const float* q, const float* k_cache, const float* v_cache,
+                                  const uint32_t* kv_pos_dev, float* out, uint32_t num_heads,
+                                  uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq, void* workspace,
+                                  size_t workspace_bytes, attn_stream_t stream) {
+  return attn_decode_cached_window(q, k_cache, v_cache, kv_pos_dev, out, num_heads, num_kv_heads, head_dim, max_seq,
+                                   workspace, workspace_bytes, 0, stream);
+}
+
+extern "C" int attn_prefill_window(const float* q_batch, const float* k_cache, const float* v_cache,
+                                   float* out_batch, uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads,
+                                   uint32_t head_dim, uint32_t kv_dim, uint32_t max_seq, float scale,
+                                   uint32_t start_pos, uint32_t q_stride, uint32_t out_stride, uint32_t q_base,
+                                   int prec, uint32_t window, attn_stream_t stream) {
   if (!heads_ok(n_heads, n_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
   if ((uint64_t)kv_dim < (uint64_t)n_kv_heads * head_dim) return ATTN_ERR_INVALID_ARG;
   if ((uint64_t)q_stride < (uint64_t)n_heads * head_dim || (uint64_t)out_stride < (uint64_t)n_heads * head_dim)
@@ -202,11 +225,20 @@ extern "C" int attn_prefill(const float* q_batch, const float* k_cache, const fl
   a.base_pos = (long long)start_pos + q_base;
   a.cap = (int)max_seq;
   a.n_all = (int)max_seq;
+  a.window = window_arg(window);
   a.scale = scale;
   a.kv_pos_dev = nullptr;
   a.status = status_ptr();
   if (a.status == nullptr) return ATTN_ERR_CUDA;
   return run_flash(a, prec, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_prefill(const float* q_batch, const float* k_cache, const float* v_cache, float* out_batch,
+                            uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads, uint32_t head_dim,
+                            uint32_t kv_dim, uint32_t max_seq, float scale, uint32_t start_pos, uint32_t q_stride,
+                            uint32_t out_stride, uint32_t q_base, int prec, attn_stream_t stream) {
+  return attn_prefill_window(q_batch, k_cache, v_cache, out_batch, n_queries, n_heads, n_kv_heads, head_dim, kv_dim,
+                             max_seq, scale, start_pos, q_stride, out_stride, q_base, prec, 0, stream);
 }
 
 extern "C" int attn_get_status(attn_stream_t stream) {

@@ -2,7 +2,7 @@
 //
 // Operation: meganeura cached_attention.wgsl, fn main -- one query token,
 // H heads, attends to cache positions 0..kv_pos (kv_pos read from device
-// memory).  Decode is bound by streaming the K/V cache from HBM, so the
+// memory), or to the last `window` of them under a sliding window.  Decode is bound by streaming the K/V cache from HBM, so the
 // design is about bytes, not flops:
 //
 //   * Grid (S, G): CTA (j, g) takes one contiguous range of cache positions
@@ -107,14 +107,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (j == 0 && g == 0 && tid == 0 && (long long)kp >= (long long)a.max_seq)
     record_status(a.status, ATTN_ERR_INVALID_ARG);
   const long long n_ll = (long long)kp + 1 < (long long)a.max_seq ? (long long)kp + 1 : (long long)a.max_seq;
-  const int n = (int)n_ll;
-  // Splits start on stage boundaries, so no stage is read by two CTAs.
+  // Positions [lo, lo + n) are attended.  Splits start on stage boundaries
+  // (relative to lo), so no stage is read by two CTAs.
+  const int lo = first_key((int)n_ll, a.window);
+  const int n = (int)n_ll - lo;
   const int s0 = min(S, (n + kMinChunk - 1) / kMinChunk);
   const int chunk = ((n + s0 - 1) / s0 + kT - 1) / kT * kT;
   const int s_eff = (n + chunk - 1) / chunk;
   if (j >= s_eff) return;
-  const int p_begin = min(n, j * chunk);
-  const int p_end = min(n, p_begin + chunk);
+  const int p_begin = lo + min(n, j * chunk);
+  const int p_end = lo + min(n, j * chunk + chunk);
   const int len = p_end - p_begin;
   const int n_st = (len + kT - 1) / kT;
 

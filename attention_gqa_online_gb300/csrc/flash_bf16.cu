@@ -2,7 +2,7 @@
 // prefill).
 //
 // Operation: softmax(scale * Q K^T) V over per-row causal / full / cross /
-// prefill windows with the online softmax's running max and sum (cera
+// prefill windows (optionally cut to their last `window` keys) with the online softmax's running max and sum (cera
 // attention_prefill.wgsl, fn attention_prefill: per-tile max, correction,
 // exponentials, running sum; meganeura attention.wgsl, fn main: the final
 // (max, log sum) store).  A pre-pass converts K and V to bf16 (same layout);
@@ -11,7 +11,8 @@
 //
 // One CTA owns 128 packed rows of one kv head g: row r is (query i, head
 // g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs query
-// heads that share it.  Keys are walked in tiles of 128.  Three score buffers
+// heads that share it.  Keys are walked in tiles of 128, from the tile holding
+// the block's first kept key to the one holding its last.  Three score buffers
 // in tensor memory let Q K^T run up to three tiles ahead of P V, so the
 // softmax of one tile overlaps the products of the others.  The two softmax
 // warpgroups split every tile's columns (64 each) and swap their partial row
@@ -108,7 +109,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   const int n_min = window(i0);
   const int n_max = window(min((long long)a.n_q, i0 + qpb) - 1);
-  const int nt = (n_max + kKeys - 1) / kKeys;
+  const int lo_max = first_key(n_max, a.window);
+  const int jt0 = first_key(n_min, a.window) / kKeys;  // first key tile of the block
+  const int nt = (n_max + kKeys - 1) / kKeys - jt0;    // key tiles the block walks
   // Ring positions (copy order): K_0, K_1, K_2, then V_j followed by K_(j+3).
   auto k_pos = [&](int j) { return j < 3 ? j : 2 * j - 2; };
   auto v_pos = [&](int j) { return min(2 * j + 3, j + nt); };
@@ -153,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned char* dst = ring + s * kTileBytes;
         if (use >= 1) mbar_wait_bounded(&sm.kv_empty[s], (unsigned)((use - 1) & 1), a.status, &sm.abort);
         mbar_arrive_expect_tx(&sm.kv_full[s], (unsigned)kTileBytes);
-        const int t0 = kKeys * j;
+        const int t0 = kKeys * (jt0 + j);
         const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + 64 * c, t0, &sm.kv_full[s]);
@@ -245,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long qi = packed / gs;
     const int h = g * gs + (int)(packed % gs);
     const int n_r = window(qi);
+    const int lo_r = first_key(n_r, a.window);
     const bool row_ok = qi < a.n_q;
     const float sl2 = a.scale * kLog2e;
 
@@ -285,13 +289,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) tc::reg_fence(s[c]);
 
-      if ((j + 1) * kKeys > n_min) {  // the tile crosses some row's window end
-        const int lim = n_r - (j * kKeys + 64 * grp);
+      const int key0 = (jt0 + j) * kKeys + 64 * grp;  // key of this half's first column
+      if (key0 - 64 * grp + kKeys > n_min) {  // the tile crosses some row's window end
+        const int lim = n_r - key0;
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (32 * c + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
+      }
+      if (key0 - 64 * grp < lo_max) {  // ... or some row's window start
+        const int lim = lo_r - key0;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e < lim) s[c][e] = __float_as_uint(-INFINITY);
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -466,16 +479,21 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const void* vp = a.q;
   if (!no_keys) {
     // K and V as bf16 in stream-ordered scratch memory (library pool),
-    // released on the same stream once the attention kernel has run.
+    // released on the same stream once the attention kernel has run.  Only
+    // rows from the first key tile any CTA reads are converted (under a
+    // sliding window the earlier rows are never read).
     const long long elems = kv_rows * a.kv_row_stride;
+    const int n_first = a.causal ? (int)min((long long)a.cap, a.base_pos + 1) : a.n_all;  // window of query 0
+    const long long row0 = first_key(n_first, a.window) / kKeys * kKeys;
+    const long long skip = row0 * a.kv_row_stride;  // a multiple of 4 (row stride % 8 == 0)
     if (scratch_alloc(&scratch, (size_t)elems * 4, s) != cudaSuccess) return ATTN_ERR_CUDA;
     uint16_t* k16 = static_cast<uint16_t*>(scratch);
     uint16_t* v16 = k16 + elems;
-    const float4* k4 = reinterpret_cast<const float4*>(a.k);
-    const float4* v4 = reinterpret_cast<const float4*>(a.v);
-    uint2* k2 = reinterpret_cast<uint2*>(k16);
-    uint2* v2 = reinterpret_cast<uint2*>(v16);
-    long long n4 = elems / 4;
+    const float4* k4 = reinterpret_cast<const float4*>(a.k + skip);
+    const float4* v4 = reinterpret_cast<const float4*>(a.v + skip);
+    uint2* k2 = reinterpret_cast<uint2*>(k16 + skip);
+    uint2* v2 = reinterpret_cast<uint2*>(v16 + skip);
+    long long n4 = (elems - skip) / 4;
     void* cargs[] = {&k4, &v4, &k2, &v2, &n4};
     const long long blocks = (n4 + kConvPer * 256 - 1) / (kConvPer * 256);
     if (launch_pdl(reinterpret_cast<const void*>(kv_to_bf16_kernel), dim3((unsigned)blocks), dim3(256), 0, s, cargs) !=

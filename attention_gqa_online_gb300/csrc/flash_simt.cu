@@ -11,13 +11,15 @@
 // exp(m - m'), p = exp(s - m'), running sum and accumulator rescale).  The
 // exponentials are base 2 with scale*log2(e) folded into the scores, which is
 // the same function.  Per-row windows implement causal / full / cross /
-// prefill / decode masking; key tiles past the last row's window are never
-// loaded.
+// prefill / decode masking, and a sliding window keeps the last `window` keys
+// of each row's window; key tiles outside every row's window of the block
+// are never loaded.
 //
 // Thread layout (256 threads): rg = tid / 16 owns rows 4rg..4rg+3; cl = tid %
 // 16 owns score columns cl + 16j (j < 4) and output columns 4cl + 64j.  Row
 // reductions stay inside a half-warp (xor shuffles 8, 4, 2, 1).
 #include <cfloat>
+#include <climits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -38,6 +40,7 @@ struct SimtSmem {
   float v[2][BN * DMAX];
   float p[BN * PS];
   int row_n[BM];
+  int row_lo[BM];
 };
 
 __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
@@ -111,13 +114,22 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
       }
     }
     sm.row_n[tid] = n;
+    sm.row_lo[tid] = first_key(n, a.window);
   }
   __syncthreads();
-  int n_max = 0;
-  for (int r = 0; r < BM; ++r) n_max = max(n_max, sm.row_n[r]);
-  int my_n[4];
+  // Keys [t_begin, n_max) cover every row's window; t_begin is tile-aligned.
+  int n_max = 0, lo_min = INT_MAX;
+  for (int r = 0; r < BM; ++r) {
+    n_max = max(n_max, sm.row_n[r]);
+    if (sm.row_n[r] > 0) lo_min = min(lo_min, sm.row_lo[r]);
+  }
+  const int t_begin = n_max > 0 ? lo_min / BN * BN : 0;
+  int my_n[4], my_lo[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) my_n[i] = sm.row_n[r0 + i];
+  for (int i = 0; i < 4; ++i) {
+    my_n[i] = sm.row_n[r0 + i];
+    my_lo[i] = sm.row_lo[r0 + i];
+  }
 
   // Q tile (rows past n_q are zero-filled and never stored).
   const long long row_base = (long long)blk * BM;
@@ -131,13 +143,13 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
   };
   load_tile<DMAX, QS, VEC>(sm.q, BM, q_valid, D, q_src);
 
-  const int n_tiles = (n_max + BN - 1) / BN;
+  const int n_tiles = (n_max - t_begin + BN - 1) / BN;
   auto kv_src = [&](const float* base, int t0) {
     return [=](int r) { return base + (long long)(t0 + r) * a.kv_row_stride + (long long)g * D; };
   };
   if (n_tiles > 0) {
-    load_tile<DMAX, QS, VEC>(sm.k[0], BN, min(BN, n_max), D, kv_src(a.k, 0));
-    load_tile<DMAX, DMAX, VEC>(sm.v[0], BN, min(BN, n_max), D, kv_src(a.v, 0));
+    load_tile<DMAX, QS, VEC>(sm.k[0], BN, min(BN, n_max - t_begin), D, kv_src(a.k, t_begin));
+    load_tile<DMAX, DMAX, VEC>(sm.v[0], BN, min(BN, n_max - t_begin), D, kv_src(a.v, t_begin));
   }
   cp_async_commit();
 
@@ -154,7 +166,7 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
 
   for (int it = 0; it < n_tiles; ++it) {
     const int buf = it & 1;
-    const int t0 = it * BN;
+    const int t0 = t_begin + it * BN;
     if (it + 1 < n_tiles) {
       const int t1 = t0 + BN;
       const int valid = min(BN, n_max - t1);
@@ -204,7 +216,7 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int t = t0 + cl + 16 * j;
-        s[i][j] = (t < my_n[i]) ? s[i][j] * sl2 : -INFINITY;
+        s[i][j] = (t >= my_lo[i] && t < my_n[i]) ? s[i][j] * sl2 : -INFINITY;
         mx = fmaxf(mx, s[i][j]);
       }
 #pragma unroll

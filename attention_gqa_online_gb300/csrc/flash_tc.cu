@@ -2,7 +2,7 @@
 // (forward and prefill).
 //
 // Operation: softmax(scale * Q K^T) V over per-row causal / full / cross /
-// prefill windows, with the running max / sum of the pages' online softmax
+// prefill windows (optionally cut to their last `window` keys), with the running max / sum of the pages' online softmax
 // (cera attention_prefill.wgsl, fn attention_prefill: per-tile max,
 // correction, exponentials, running sum; meganeura attention.wgsl, fn main:
 // the final (max, log sum) store).  Both contractions run on the 5th-generation
@@ -12,7 +12,8 @@
 //
 // One CTA owns 128 packed rows of one kv head g: row r is (query i, head
 // g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs
-// query heads that share it.  Keys are walked in tiles of 128.
+// query heads that share it.  Keys are walked in tiles of 128, from the tile
+// holding the block's first kept key to the one holding its last.
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: K tile (128 keys x D, 128-byte swizzle, K-major
@@ -115,7 +116,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   const int n_max = window(i1);
   const int n_min = window(i0);
-  const int nt = (n_max + kKeys - 1) / kKeys;
+  const int lo_max = first_key(n_max, a.window);
+  const int jt0 = first_key(n_min, a.window) / kKeys;  // first key tile of the block
+  const int nt = (n_max + kKeys - 1) / kKeys - jt0;    // key tiles the block walks
 
   if (tid == 0) {
     for (int s = 0; s < kRing; ++s) {
@@ -159,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (use >= 1) mbar_wait_bounded(&sm.kv_empty[s], (unsigned)((use - 1) & 1), a.status, &sm.abort);
         mbar_arrive_expect_tx(&sm.kv_full[s], (unsigned)kTileBytes);
         const bool is_v = (p == 2 * nt - 1) || (p > 0 && (p & 1) == 0);
-        const int t0 = kKeys * (is_v ? (p == 2 * nt - 1 ? nt - 1 : p / 2 - 1) : (p + 1) / 2);
+        const int t0 = kKeys * (jt0 + (is_v ? (p == 2 * nt - 1 ? nt - 1 : p / 2 - 1) : (p + 1) / 2));
         const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + kEpr * c, t0, &sm.kv_full[s]);
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long qi = packed / gs;
     const int h = g * gs + (int)(packed % gs);
     const int n_r = window(qi);
+    const int lo_r = first_key(n_r, a.window);
     const bool row_ok = qi < a.n_q;
     const float sl2 = a.scale * kLog2e;
 
@@ -306,15 +310,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kCC; ++c) tc::reg_fence(s[c]);
 
-      // Mask (only a tile that crosses some row's window end) and this
-      // half's max.
-      if ((j + 1) * kKeys > n_min) {
-        const int lim = n_r - (j * kKeys + kCols * grp);
+      // Mask (only a tile that crosses some row's window end or start) and
+      // this half's max.
+      const int key0 = (jt0 + j) * kKeys + kCols * grp;  // key of this half's first column
+      if (key0 - kCols * grp + kKeys > n_min) {
+        const int lim = n_r - key0;
 #pragma unroll
         for (int c = 0; c < kCC; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (32 * c + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
+      }
+      if (key0 - kCols * grp < lo_max) {
+        const int lim = lo_r - key0;
+#pragma unroll
+        for (int c = 0; c < kCC; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e < lim) s[c][e] = __float_as_uint(-INFINITY);
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll

@@ -22,19 +22,27 @@ struct FlashArgs {
   long long out_row_stride;   // floats between consecutive output rows
   long long kv_row_stride;    // floats between consecutive key/value rows
   int n_q, H, G, D;
-  // Window of query i: keys [0, n_i) with
+  // Window of query i: keys [lo_i, n_i) with
   //   n_i = min(base_pos + i + 1, cap)  if causal
   //   n_i = n_all                       otherwise
+  //   lo_i = first_key(n_i, window)
   int causal;
   long long base_pos;
   int cap;
   int n_all;
+  int window;                 // sliding window length, 0 = none
   float scale;                // multiplies q . k
   // Decode through the generic kernel: when set, base_pos is read from
   // *kv_pos_dev on the device (n_q == 1, causal, cap = max_seq).
   const uint32_t* kv_pos_dev;
   unsigned* status;           // device status word
 };
+
+// First key of a window that ends at n (exclusive) under a sliding window of
+// `window` keys (0 = unlimited): the window keeps the last `window` positions.
+// Both bounds are non-decreasing in n, so over a block of consecutive queries
+// the first query has the smallest bounds and the last the largest.
+__host__ __device__ inline int first_key(int n, int window) { return (window > 0 && n > window) ? n - window : 0; }
 
 // Launches `kernel` with programmatic stream serialization allowed, so it may
 // start while the previous kernel in `s` finishes (the kernel itself waits
@@ -72,6 +80,7 @@ struct DecodeArgs {
   const uint32_t* kv_pos_dev;
   float* out;
   int H, G, D, max_seq;
+  int window;  // sliding window length, 0 = none: keys [first_key(n, window), n)
   void* workspace;
   unsigned* status;
 };

@@ -40,6 +40,7 @@ KV_POS = 16383
 DECODE_WORKLOAD = "decode q[1,32x128] kv_cache[16384,8x128] fp32 kv_pos=16383"
 PREFILL = dict(n_queries=512, start_pos=1536, max_seq=2048, H=32, G=8, D=128, stride=4096)
 FORWARD = dict(q_seq=8192, H=32, G=8, D=128)
+WINDOW = 4096  # sliding-window workloads: each row keeps its last 4096 keys
 
 
 def decode_bytes(kv_len):
@@ -52,9 +53,15 @@ def prefill_flops():
     return 4.0 * p["D"] * tri * p["H"]
 
 
-def forward_flops():
+def forward_flops(window=0):
+    """Algorithmic FLOPs of the causal forward: 4 D per (row, head, kept key)."""
     f = FORWARD
-    return 4.0 * f["D"] * (f["q_seq"] * (f["q_seq"] + 1) // 2) * f["H"]
+    n = f["q_seq"]
+    keys = n * (n + 1) // 2
+    if window:
+        w = min(window, n)
+        keys = w * (w + 1) // 2 + (n - w) * w
+    return 4.0 * f["D"] * keys * f["H"]
 
 
 def load_peaks():
@@ -425,6 +432,25 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
                 "traffic": None, "kernel": kernel,
                 "peak_source": "fp32 FMA: %d SMs x 128 lanes x 2 x %.0f MHz" % (sms, sm_mhz)}
 
+    def forward_lines(prefix, window, what):
+        f = FORWARD
+        q, k, v = synthetic.forward_inputs(f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], seed=5, qk_sigma=3.0)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        outf = torch.empty_like(qd)
+        lse = torch.empty((f["q_seq"], f["H"], 2), device=dev)
+        for prec, name, kern in variants:
+            def fwd_step(i, prec=prec):
+                rc = lib.attn_forward_window(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(),
+                                             lse.data_ptr(), f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"],
+                                             A.ATTN_CAUSAL, prec, window, sh)
+                if rc != 0:
+                    raise RuntimeError("attn_forward_window failed: %d" % rc)
+            ms = timed(fwd_step, steps)
+            tf = forward_flops(window) / (ms * 1e-3) / 1e12
+            res[prefix + name] = {
+                "workload": what, "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "prec": name,
+                "roofline": roof(prec, tf, kern), "l2": "inputs 192 MiB > L2"}
+
     variants = ((A.ATTN_TF32, "tf32", "flash_tc_kernel<128> (tf32)"),
                 (A.ATTN_BF16, "bf16", "flash_bf16_kernel<128> (bf16) + kv_to_bf16 pre-pass"),
                 (A.ATTN_FP32, "fp32", "flash_simt_kernel<128,true>"))
@@ -454,23 +480,52 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
         del bufs
 
     if only in ("all", "forward"):
-        f = FORWARD
-        q, k, v = synthetic.forward_inputs(f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], seed=5, qk_sigma=3.0)
-        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-        outf = torch.empty_like(qd)
-        lse = torch.empty((f["q_seq"], f["H"], 2), device=dev)
-        for prec, name, kern in variants:
-            def fwd_step(i, prec=prec):
-                rc = lib.attn_forward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(), lse.data_ptr(),
-                                      f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], A.ATTN_CAUSAL, prec, sh)
-                if rc != 0:
-                    raise RuntimeError("attn_forward failed: %d" % rc)
-            ms = timed(fwd_step, steps)
-            tf = forward_flops() / (ms * 1e-3) / 1e12
-            res["forward_" + name] = {
-                "workload": "causal forward+LSE q_seq=8192 32/8 heads D=128, Q,K N(0,9)", "value": tf,
-                "unit": "TFLOP/s", "ms_per_step": ms, "prec": name, "roofline": roof(prec, tf, kern),
-                "l2": "inputs 192 MiB > L2"}
+        forward_lines("forward_", 0, "causal forward+LSE q_seq=8192 32/8 heads D=128, Q,K N(0,9)")
+
+    if only in ("all", "window"):
+        forward_lines("forward_window_", WINDOW, "sliding-window causal forward+LSE q_seq=8192 window=%d 32/8 heads "
+                      "D=128, Q,K N(0,9)" % WINDOW)
+        # Windowed decode: the last WINDOW positions of a 16384-row cache.
+        win_bytes = decode_bytes(WINDOW)
+        n_rot = max(3, int(math.ceil(2.0 * l2 / (win_bytes - 2 * H * D * 4))) + 1)
+        q, kc, vc = synthetic.decode_inputs(MAX_SEQ, H, G, D, seed=1)
+        qd = q.to(dev)
+        caches = [(kc.to(dev), vc.to(dev)) for _ in range(n_rot)]
+        out = torch.empty_like(qd)
+        ws_bytes = A.attn_decode_workspace_bytes(H, G, D, MAX_SEQ)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        pos = torch.full((1,), KV_POS, dtype=torch.int32, device=dev)
+
+        def dec_step(i):
+            kd, vd = caches[i % n_rot]
+            rc = lib.attn_decode_cached_window(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), pos.data_ptr(),
+                                               out.data_ptr(), H, G, D, MAX_SEQ, ws.data_ptr(), ws_bytes, WINDOW, sh)
+            if rc != 0:
+                raise RuntimeError("attn_decode_cached_window failed: %d" % rc)
+        # Back-to-back launches between one event pair, as for the main
+        # decode line (each launch overlaps the previous one's tail by PDL).
+        for i in range(args.warmup):
+            dec_step(i)
+        torch.cuda.synchronize()
+        n_dec = max(steps, 200)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n_dec):
+            dec_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res["_launches"] += n_dec + args.warmup
+        ms = e0.elapsed_time(e1) / n_dec
+        gbs = win_bytes / (ms * 1e-3) / 1e9
+        res["decode_window"] = {
+            "workload": "decode kv_pos=16383 window=%d (positions 12288..16383), cache [16384, 8x128] fp32" % WINDOW,
+            "value": gbs, "unit": "GB/s", "us_per_step": ms * 1e3,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "decode_split_kernel<128,4>",
+                         "bytes_per_launch": win_bytes, "peak_source": peak_src},
+            "l2": "rotating %d caches (%d MiB of windows) > 2x L2" % (n_rot, n_rot * (win_bytes >> 20)),
+            "timing": "%d back-to-back launches between one event pair" % n_dec}
+        del caches
     return res
 
 
@@ -502,7 +557,7 @@ def main():
     ap.add_argument("--decode-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "forward"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "forward", "window"], default="all",
                     help="run one workload (for profiling); the default runs all of them")
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     args = ap.parse_args()
@@ -512,7 +567,7 @@ def main():
     if args.impl == "reference":
         reference_arm(args, world, rank)
         return
-    if args.only in ("prefill", "forward"):
+    if args.only in ("prefill", "forward", "window"):
         run_single(args, local)
         return
     if args.only == "decode":

@@ -171,6 +171,36 @@ ATTN_API int attn_prefill(const float *q_batch, const float *k_cache, const floa
                  int prec, attn_stream_t stream);
 
 /*
+ * Sliding-window (local) attention: the three calls above with one more
+ * argument, `window`, placed just before `stream`.  Every other argument,
+ * layout, error and result is that of the call without the suffix.
+ * Source: meganeura attention.wgsl, fn main -- the key loop of every variant
+ * starts at a $KV_START placeholder that the page leaves to the host
+ * framework.  This library reads it as a per-row lower bound: a row whose
+ * window is keys [0, n) under the rules above attends keys
+ *     [max(0, n - window), n)
+ * i.e. its last `window` keys (window == 0: no lower bound, the call without
+ * the suffix).  A window of 1 returns the V row of the last key; a window at
+ * least n changes nothing.  The LSE pair of attn_forward_window describes
+ * the kept keys only.  Key tiles that lie wholly before every row's window
+ * are neither read nor computed, so the cost follows the window, not the
+ * position.  No further errors.
+ */
+ATTN_API int attn_forward_window(const float *q, const float *k, const float *v, float *out, float *lse,
+                                 uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
+                                 uint32_t head_dim, int mask, int prec, uint32_t window, attn_stream_t stream);
+ATTN_API int attn_decode_cached_window(const float *q, const float *k_cache, const float *v_cache,
+                                       const uint32_t *kv_pos_dev, float *out, uint32_t num_heads,
+                                       uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq,
+                                       void *workspace, size_t workspace_bytes, uint32_t window,
+                                       attn_stream_t stream);
+ATTN_API int attn_prefill_window(const float *q_batch, const float *k_cache, const float *v_cache,
+                                 float *out_batch, uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads,
+                                 uint32_t head_dim, uint32_t kv_dim, uint32_t max_seq, float scale,
+                                 uint32_t start_pos, uint32_t q_stride, uint32_t out_stride, uint32_t q_base,
+                                 int prec, uint32_t window, attn_stream_t stream);
+
+/*
  * Cached single-token decode that allocates nothing and takes no workspace.
  * The shader pages have no counterpart to this entry point; it exists for
  * callers that cannot provide device scratch memory -- a plugin inside a

@@ -426,4 +426,105 @@ def pin_window_prefill_matches_decode(orc):
     assert np.max(np.abs(outp[qbase:qbase + 7, :H * D] - full[qbase:qbase + 7, :H * D])) > 1e-3
 
 
+
+# ---------------------------------------------------------------- backward
+def _grad_inputs(seed, q_seq, kv_seq, H, G, D):
+    """Q, K, V and an upstream gradient dout, all N(0,1) fp32."""
+    rng = np.random.default_rng(seed)
+    f = lambda *sh: rng.standard_normal(sh).astype(np.float32)  # noqa: E731
+    return f(q_seq, H * D), f(kv_seq, G * D), f(kv_seq, G * D), f(q_seq, H * D)
+
+
+def _autograd(q, k, v, dout, q_seq, kv_seq, H, G, D, ends, window):
+    """Gradients from PyTorch autograd through fp64 SDPA with a banded boolean mask."""
+    allow = np.zeros((q_seq, kv_seq), dtype=bool)
+    for i, n in enumerate(ends):
+        allow[i, (max(0, n - window) if window > 0 else 0):n] = True
+    qt = torch.from_numpy(q.astype(np.float64)).reshape(q_seq, H, D).transpose(0, 1)[None].requires_grad_()
+    kt = torch.from_numpy(k.astype(np.float64)).reshape(kv_seq, G, D).transpose(0, 1)[None].requires_grad_()
+    vt = torch.from_numpy(v.astype(np.float64)).reshape(kv_seq, G, D).transpose(0, 1)[None].requires_grad_()
+    o = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=torch.from_numpy(allow), enable_gqa=True)
+    go = torch.from_numpy(dout.astype(np.float64)).reshape(q_seq, H, D).transpose(0, 1)[None]
+    o.backward(go)
+    flat = lambda t, n, c: t.grad[0].transpose(0, 1).reshape(n, c).numpy()  # noqa: E731
+    return flat(qt, q_seq, H * D), flat(kt, kv_seq, G * D), flat(vt, kv_seq, G * D)
+
+
+def pin_backward_autograd(orc):
+    """The three masks, with and without a sliding window, against autograd of SDPA."""
+    for mask, q_seq, kv_seq, w in ((CAUSAL, 11, 11, 0), (FULL, 9, 9, 0), (CROSS, 6, 13, 0),
+                                   (CAUSAL, 11, 11, 4), (CROSS, 6, 13, 5)):
+        H, G, D = 6, 2, 8
+        q, k, v, do = _grad_inputs(30 + mask + w, q_seq, kv_seq, H, G, D)
+        got = orc.backward(q, k, v, do, q_seq, kv_seq, H, G, D, mask, window=w)
+        ends = [i + 1 for i in range(q_seq)] if mask == CAUSAL else [kv_seq] * q_seq
+        ref = _autograd(q, k, v, do, q_seq, kv_seq, H, G, D, ends, w)
+        for a, b in zip(got, ref):
+            assert np.max(np.abs(a - b)) < 1e-12
+
+
+def pin_backward_finite_difference(orc):
+    """Central differences of L = sum(dout * out) through the forward oracle.
+
+    Inputs sit on a 2^-10 grid and the step is 2^-12, so x +- h is exact in
+    fp32 and the difference quotient is accurate to O(h^2)."""
+    H, G, D, n = 4, 2, 4, 7
+    q, k, v, do = _grad_inputs(40, n, n, H, G, D)
+    q, k, v = (np.round(x * 1024.0) / 1024.0 for x in (q, k, v))
+    q, k, v = (x.astype(np.float32) for x in (q, k, v))
+    dq, dk, dv = orc.backward(q, k, v, do, n, n, H, G, D, CAUSAL)
+    h = 2.0 ** -12
+
+    def loss(qq, kk, vv):
+        out, _ = orc.forward(qq, kk, vv, n, n, H, G, D, CAUSAL)
+        return float(np.sum(out * do.astype(np.float64)))
+
+    for arr, grad, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        for idx in ((0, 0), (3, 5), (6, 7), (2, 3)):
+            plus, minus = [x.copy() for x in (q, k, v)], [x.copy() for x in (q, k, v)]
+            plus[which][idx] += np.float32(h)
+            minus[which][idx] -= np.float32(h)
+            assert plus[which][idx] - arr[idx] == np.float32(h)
+            fd = (loss(*plus) - loss(*minus)) / (2 * h)
+            assert abs(fd - grad[idx]) < 2e-6, (which, idx, fd, grad[idx])
+
+
+def pin_backward_sums(orc):
+    """Each row's softmax sums to 1 and its score gradient sums to 0, so over all
+    keys of a kv head: sum_t dv_t = sum of dout over that head's query rows, and
+    sum_t dk_t = 0 (any mask, any window)."""
+    H, G, D = 8, 2, 16
+    for mask, q_seq, kv_seq, w in ((CAUSAL, 20, 20, 0), (CROSS, 9, 30, 7), (FULL, 12, 12, 3)):
+        q, k, v, do = _grad_inputs(50 + mask, q_seq, kv_seq, H, G, D)
+        _, dk, dv = orc.backward(q, k, v, do, q_seq, kv_seq, H, G, D, mask, window=w)
+        dsum = do.astype(np.float64).reshape(q_seq, G, H // G, D).sum(axis=(0, 2)).reshape(G * D)
+        assert np.max(np.abs(dv.sum(axis=0) - dsum)) < 1e-11
+        assert np.max(np.abs(dk.sum(axis=0))) < 1e-11
+
+
+def pin_backward_window_one(orc):
+    """window 1: each row copies one V row, so dq = dk = 0 and dv_t collects the
+    dout of every query head of the group at the row that keeps key t."""
+    H, G, D, n = 4, 2, 8, 6
+    q, k, v, do = _grad_inputs(60, n, n, H, G, D)
+    dq, dk, dv = orc.backward(q, k, v, do, n, n, H, G, D, CAUSAL, window=1)
+    assert np.all(dq == 0.0) and np.all(dk == 0.0)
+    ref = do.astype(np.float64).reshape(n, G, H // G, D).sum(axis=2).reshape(n, G * D)
+    assert np.max(np.abs(dv - ref)) < 1e-15
+
+
+def pin_backward_gqa_is_summed_mha(orc):
+    """GQA gradients of a shared kv head are the sums over its query heads of the
+    MHA gradients with that head's K/V replicated."""
+    H, G, D, n = 6, 2, 8, 10
+    q, k, v, do = _grad_inputs(70, n, n, H, G, D)
+    kr = np.repeat(k.reshape(n, G, D), H // G, axis=1).reshape(n, H * D)
+    vr = np.repeat(v.reshape(n, G, D), H // G, axis=1).reshape(n, H * D)
+    dq, dk, dv = orc.backward(q, k, v, do, n, n, H, G, D, CAUSAL)
+    dq2, dk2, dv2 = orc.backward(q, kr, vr, do, n, n, H, H, D, CAUSAL)
+    assert np.max(np.abs(dq - dq2)) < 1e-13
+    assert np.max(np.abs(dk - dk2.reshape(n, G, H // G, D).sum(axis=2).reshape(n, G * D))) < 1e-13
+    assert np.max(np.abs(dv - dv2.reshape(n, G, H // G, D).sum(axis=2).reshape(n, G * D))) < 1e-13
+
+
 ALL_PINS = [obj for name, obj in sorted(globals().items()) if name.startswith("pin_")]

@@ -95,3 +95,37 @@ def test_workspace_query_rejects_bad_sizes(lib):
     assert lib.attn_decode_workspace_bytes(5, 2, 64, 100) == 0
     assert lib.attn_decode_workspace_bytes(4, 2, 64, 0) == 0
     assert lib.attn_decode_workspace_bytes(4, 2, 0, 10) == 0
+
+
+# ---------------------------------------------------------------- windowed entry points
+@pytest.mark.parametrize("kw", [
+    dict(H=5, G=2), dict(D=129), dict(mask=3), dict(mask=0, kv_seq=17), dict(q=None), dict(prec=7),
+])
+@pytest.mark.parametrize("window", [0, 1, 2 ** 32 - 1])
+def test_forward_window_rejects(lib, kw, window):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=None, q_seq=16, kv_seq=16, H=4, G=2, D=64, mask=0, prec=0)
+    a.update(kw)
+    assert lib.attn_forward_window(a["q"], a["k"], a["v"], a["out"], a["lse"], a["q_seq"], a["kv_seq"], a["H"],
+                                   a["G"], a["D"], a["mask"], a["prec"], window, None) == 1
+
+
+def test_forward_window_empty_query_is_noop(lib):
+    assert lib.attn_forward_window(None, None, None, None, None, 0, 0, 4, 2, 64, 0, 0, 7, None) == 0
+
+
+@pytest.mark.parametrize("kw", [dict(kv_dim=127), dict(start=50, n=15), dict(scale=math.nan), dict(out=None)])
+def test_prefill_window_rejects(lib, kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, n=8, H=4, G=2, D=64, kv_dim=128, max_seq=64, scale=0.125,
+             start=0, q_stride=256, out_stride=256, q_base=0, prec=0)
+    a.update(kw)
+    assert lib.attn_prefill_window(a["q"], a["k"], a["v"], a["out"], a["n"], a["H"], a["G"], a["D"], a["kv_dim"],
+                                   a["max_seq"], a["scale"], a["start"], a["q_stride"], a["out_stride"],
+                                   a["q_base"], a["prec"], 16, None) == 1
+
+
+@pytest.mark.parametrize("kw", [dict(H=30), dict(max_seq=0), dict(pos=None)])
+def test_decode_window_rejects(lib, kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, pos=FAKE, out=FAKE, H=32, G=8, D=128, max_seq=100)
+    a.update(kw)
+    assert lib.attn_decode_cached_window(a["q"], a["k"], a["v"], a["pos"], a["out"], a["H"], a["G"], a["D"],
+                                         a["max_seq"], FAKE, 1 << 20, 16, None) == 1

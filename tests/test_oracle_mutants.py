@@ -55,6 +55,20 @@ MUTANTS = [
      "for (size_t t = 1; t < n; ++t) {\n        const float *kt", False),
     ("dot_in_fp32", "double dot = 0.0;", "float dot = 0.0f;", False),
     ("sum_in_fp32", "double l = 0.0;", "float l = 0.0f;", False),
+    # backward
+    ("bwd_mean_dropped", "const double ds = p[t] * (dp[t] - mean);", "const double ds = p[t] * dp[t];", False),
+    ("bwd_dk_unscaled", "dkt[d] += scale * ds * (double)qr[d];", "dkt[d] += ds * (double)qr[d];", False),
+    ("bwd_dq_reads_v", "dqr[d] += scale * ds * (double)kt[d];",
+     "dqr[d] += scale * ds * (double)v[t * kv_dim + (size_t)g * D + d];", False),
+    ("bwd_dv_unweighted", "dvt[d] += p[t] * (double)dor[d];", "dvt[d] += (double)dor[d];", False),
+    ("bwd_p_not_normalised", "for (size_t t = lo; t < n; ++t) p[t] /= l;", "", False),
+    ("bwd_dp_reads_k", "(double)dor[d] * (double)vt[d]", "(double)dor[d] * (double)k[t * kv_dim + (size_t)g * D + d]",
+     False),
+    ("bwd_window_ignored", "const size_t lo = window_start(n, window);\n                        if (n == lo)",
+     "const size_t lo = 0;\n                        if (n == lo)", False),
+    ("bwd_causal_short", "const size_t n = (mask == 0) ? (size_t)pos + 1", "const size_t n = (mask == 0) ? (size_t)pos",
+     False),
+    ("bwd_head_map_interleaved", "const int h = g * gs + hh;", "const int h = hh * G + g;", False),
 ]
 
 RUNNER = r"""
