@@ -39,6 +39,8 @@ def load(lib_path=None):
     lib.oracle_prefill.restype = _c_int
     lib.oracle_prefill.argtypes = [_f32p, _f32p, _f32p, _f64p] + [_c_int] * 6 + \
         [ctypes.c_float] + [_c_int] * 4 + [ctypes.c_void_p, _c_int, _c_int]
+    lib.oracle_backward.restype = _c_int
+    lib.oracle_backward.argtypes = [_f32p, _f32p, _f32p, _f32p, _f64p, _f64p, _f64p] + [_c_int] * 7
     lib.oracle_num_threads.restype = _c_int
     lib.oracle_num_threads.argtypes = []
     return lib
@@ -84,6 +86,19 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_decode rejected its arguments")
         return out
+
+    def backward(self, q, k, v, dout, q_seq, kv_seq, H, G, D, mask, window=0):
+        """Gradients of out for upstream dout: returns (dq [q_seq, H*D], dk, dv [kv_seq, G*D])."""
+        q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v, dout))
+        dq = np.full((max(q_seq, 0), H * D), np.nan)
+        dk = np.full((max(kv_seq, 0), G * D), np.nan)
+        dv = np.full((max(kv_seq, 0), G * D), np.nan)
+        rc = self.lib.oracle_backward(q.reshape(-1), k.reshape(-1), v.reshape(-1), dout.reshape(-1),
+                                      dq.reshape(-1), dk.reshape(-1), dv.reshape(-1), q_seq, kv_seq, H, G, D,
+                                      mask, int(window))
+        if rc != 0:
+            raise ValueError("oracle_backward rejected its arguments")
+        return dq, dk, dv
 
     def prefill(self, q_batch, k_cache, v_cache, out_rows, n_queries, H, G, D, kv_dim, max_seq,
                 scale, start_pos, q_stride, out_stride, q_base, rows=None, window=0):

@@ -251,3 +251,102 @@ int oracle_prefill(const float *q_batch, const float *k_cache, const float *v_ca
     }
     return err;
 }
+
+/*
+ * Backward of the forward attention (the pages emit the per-row (max,
+ * log-sum) pair for a backward pass -- attention.wgsl header and final LSE
+ * store -- but print no backward; this is the plain gradient of the forward
+ * definition above).  For a loss L with dL/dout = dout, one (row, head) with
+ * kept keys t in [lo, n):
+ *
+ *   p_t   = softmax_t(s_t),  s_t = scale * q . k_t
+ *   dv_t += p_t * dout                       (out = sum_t p_t v_t)
+ *   dp_t  = dout . v_t
+ *   ds_t  = p_t * (dp_t - sum_u p_u dp_u)    (Jacobian of softmax)
+ *   dq    = scale * sum_t ds_t k_t
+ *   dk_t += scale * ds_t q
+ *
+ * dk and dv of kv head g collect every row of every query head h with
+ * h / (H/G) == g.  The LSE output itself is not differentiated (its
+ * gradient is taken as zero).  Empty windows contribute nothing.
+ *   q, dout [q_seq, H*D]; k, v [kv_seq, G*D]
+ *   dq [q_seq, H*D]; dk, dv [kv_seq, G*D]  (all written in full)
+ *   mask, window: as oracle_forward.
+ * Parallel over kv heads only; within a kv head rows are taken in order.
+ */
+int oracle_backward(const float *q, const float *k, const float *v, const float *dout,
+                    double *dq, double *dk, double *dv, int q_seq, int kv_seq,
+                    int H, int G, int D, int mask, int window)
+{
+    if (bad_heads(H, G, D) || q_seq < 0 || kv_seq < 0 || mask < 0 || mask > 2 || window < 0) return -1;
+    if (mask != 2 && kv_seq != q_seq) return -1;
+    const int gs = H / G;
+    const size_t kv_dim = (size_t)G * D;
+    const double scale = 1.0 / sqrt((double)D);
+    for (size_t i = 0; i < (size_t)q_seq * H * D; ++i) dq[i] = 0.0;
+    for (size_t i = 0; i < (size_t)kv_seq * kv_dim; ++i) dk[i] = dv[i] = 0.0;
+    int err = 0;
+#pragma omp parallel
+    {
+        const size_t cap = (size_t)(kv_seq > 0 ? kv_seq : 1);
+        double *p = (double *)malloc(sizeof(double) * cap);
+        double *dp = (double *)malloc(sizeof(double) * cap);
+        if (p == NULL || dp == NULL) {
+#pragma omp atomic write
+            err = -1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int g = 0; g < G; ++g) {
+                for (int hh = 0; hh < gs; ++hh) {
+                    const int h = g * gs + hh;
+                    for (int pos = 0; pos < q_seq; ++pos) {
+                        const size_t n = (mask == 0) ? (size_t)pos + 1 : (size_t)kv_seq;
+                        const size_t lo = window_start(n, window);
+                        if (n == lo) continue;
+                        const float *qr = q + (size_t)pos * H * D + (size_t)h * D;
+                        const float *dor = dout + (size_t)pos * H * D + (size_t)h * D;
+                        double *dqr = dq + (size_t)pos * H * D + (size_t)h * D;
+                        /* p = softmax of the scores over the kept keys */
+                        double m = -INFINITY;
+                        for (size_t t = lo; t < n; ++t) {
+                            const float *kt = k + t * kv_dim + (size_t)g * D;
+                            double dot = 0.0;
+                            for (int d = 0; d < D; ++d) dot += (double)qr[d] * (double)kt[d];
+                            p[t] = dot * scale;
+                            if (p[t] > m) m = p[t];
+                        }
+                        double l = 0.0;
+                        for (size_t t = lo; t < n; ++t) {
+                            p[t] = exp(p[t] - m);
+                            l += p[t];
+                        }
+                        for (size_t t = lo; t < n; ++t) p[t] /= l;
+                        /* dp_t = dout . v_t and its p-weighted mean */
+                        double mean = 0.0;
+                        for (size_t t = lo; t < n; ++t) {
+                            const float *vt = v + t * kv_dim + (size_t)g * D;
+                            double dot = 0.0;
+                            for (int d = 0; d < D; ++d) dot += (double)dor[d] * (double)vt[d];
+                            dp[t] = dot;
+                            mean += p[t] * dot;
+                        }
+                        for (size_t t = lo; t < n; ++t) {
+                            const double ds = p[t] * (dp[t] - mean);
+                            const float *kt = k + t * kv_dim + (size_t)g * D;
+                            double *dkt = dk + t * kv_dim + (size_t)g * D;
+                            double *dvt = dv + t * kv_dim + (size_t)g * D;
+                            for (int d = 0; d < D; ++d) {
+                                dqr[d] += scale * ds * (double)kt[d];
+                                dkt[d] += scale * ds * (double)qr[d];
+                                dvt[d] += p[t] * (double)dor[d];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return err;
+}
