@@ -55,6 +55,8 @@ def load_library(path=None):
     lib.attn_decode_cached_window.argtypes = lib.attn_decode_cached.argtypes[:-1] + [_u32, _vp]
     lib.attn_prefill_window.restype = ctypes.c_int
     lib.attn_prefill_window.argtypes = lib.attn_prefill.argtypes[:-1] + [_u32, _vp]
+    lib.attn_backward.restype = ctypes.c_int
+    lib.attn_backward.argtypes = [_vp] * 9 + [_u32] * 5 + [ctypes.c_int, ctypes.c_int, _u32, _vp]
     lib.attn_get_status.restype = ctypes.c_int
     lib.attn_get_status.argtypes = [_vp]
     lib.attn_status_string.restype = ctypes.c_char_p
@@ -115,6 +117,16 @@ def attn_forward_window(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_head
         _addr(q, "q", f), _addr(k, "k", f), _addr(v, "v", f), _addr(out, "out", f), _addr(lse, "lse", f),
         q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask, prec, window, _stream(stream)),
         "attn_forward_window")
+
+
+def attn_backward(q, k, v, out, dout, lse, dq, dk, dv, q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask,
+                  prec=ATTN_FP32, window=0, stream=None):
+    """Gradients of the forward's out for upstream dout (out and lse from the forward); see attn_gqa.h."""
+    f = _f32()
+    _check(load_library().attn_backward(
+        _addr(q, "q", f), _addr(k, "k", f), _addr(v, "v", f), _addr(out, "out", f), _addr(dout, "dout", f),
+        _addr(lse, "lse", f), _addr(dq, "dq", f), _addr(dk, "dk", f), _addr(dv, "dv", f), q_seq, kv_seq,
+        num_heads, num_kv_heads, head_dim, mask, prec, window, _stream(stream)), "attn_backward")
 
 
 def attn_decode_workspace_bytes(num_heads, num_kv_heads, head_dim, max_seq):

@@ -22,6 +22,16 @@ def forward(q, k, v, num_heads, num_kv_heads, mask=B.ATTN_CAUSAL, prec=B.ATTN_FP
     return out, lse
 
 
+def backward(q, k, v, out, lse, dout, num_heads, num_kv_heads, mask=B.ATTN_CAUSAL, window=0, stream=None):
+    """Gradients (dq, dk, dv) of forward(q, k, v, ...)'s out for upstream dout, given its out and lse."""
+    q_seq, kv_seq = q.shape[0], k.shape[0]
+    D = q.shape[1] // num_heads
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    B.attn_backward(q, k, v, out, dout, lse, dq, dk, dv, q_seq, kv_seq, num_heads, num_kv_heads, D, mask,
+                    B.ATTN_FP32, window, stream)
+    return dq, dk, dv
+
+
 def prefill(q_batch, k_cache, v_cache, n_queries, n_heads, n_kv_heads, head_dim, start_pos, q_base=0,
             scale=None, out=None, prec=B.ATTN_FP32, stream=None, window=0):
     """Causal prefill of rows q_base .. q_base+n_queries-1 of q_batch (row stride = its width)."""

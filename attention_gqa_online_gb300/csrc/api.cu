@@ -241,6 +241,49 @@ extern "C" int attn_prefill(const float* q_batch, const float* k_cache, const fl
                              max_seq, scale, start_pos, q_stride, out_stride, q_base, prec, 0, stream);
 }
 
+extern "C" int attn_backward(const float* q, const float* k, const float* v, const float* out, const float* dout,
+                             const float* lse, float* dq, float* dk, float* dv, uint32_t q_seq, uint32_t kv_seq,
+                             uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,
+                             uint32_t window, attn_stream_t stream) {
+  if (!heads_ok(num_heads, num_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
+  if (mask != ATTN_CAUSAL && mask != ATTN_FULL && mask != ATTN_CROSS) return ATTN_ERR_INVALID_ARG;
+  if (mask != ATTN_CROSS && kv_seq != q_seq) return ATTN_ERR_INVALID_ARG;
+  if (q_seq > 0x7fffffffu || kv_seq > 0x7fffffffu) return ATTN_ERR_INVALID_ARG;
+  if (q_seq == 0) return ATTN_OK;
+  if (q == nullptr || dout == nullptr || dq == nullptr || out == nullptr || lse == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (kv_seq > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (prec != ATTN_FP32) return ATTN_ERR_UNSUPPORTED;
+  const uintptr_t al = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
+                       reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
+                       reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv);
+  if (head_dim % 4 != 0 || al % 16 != 0) return ATTN_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (kv_seq == 0)  // no keys: out was all zeros and every gradient is zero
+    return cudaMemsetAsync(dq, 0, (size_t)q_seq * num_heads * head_dim * sizeof(float), s) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
+  BwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.n_q = (int)q_seq;
+  a.n_kv = (int)kv_seq;
+  a.H = (int)num_heads;
+  a.G = (int)num_kv_heads;
+  a.D = (int)head_dim;
+  a.causal = (mask == ATTN_CAUSAL);
+  a.window = window_arg(window);
+  a.scale = 1.0f / sqrtf((float)head_dim);
+  return launch_backward_simt(a, s);
+}
+
 extern "C" int attn_get_status(attn_stream_t stream) {
   unsigned* st = status_ptr();
   if (st == nullptr) return ATTN_ERR_CUDA;

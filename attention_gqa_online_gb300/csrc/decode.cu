@@ -41,6 +41,7 @@ constexpr int kCtasPerSm = 2;
 constexpr int kMinChunk = 64;             // fewest positions a split is given
 constexpr int kMaxSplits = 1024;          // most splits per kv head
 constexpr int kMergeBatch = 16;           // splits merged per batch of loads
+constexpr int kPrefetchStages = 4;        // stages per CTA pulled into L2 before the launch wait
 constexpr int kPpw = kT / kCWarps;        // positions per consumer warp per stage
 constexpr int kNg = kPpw / 4;             // groups of four positions per warp
 static_assert(kPpw % 4 == 0, "each consumer warp takes whole groups of four positions");
@@ -82,6 +83,26 @@ __host__ __device__ inline WsLayout ws_layout(void* ws, int H, int G, int D, int
   return l;
 }
 
+// Positions [p_begin, p_end) of split j of kv head g, out of S splits, for a
+// cache position kv_pos; s_eff = splits that get any position.  Positions
+// [lo, lo + n) are attended; splits start on stage boundaries (relative to
+// lo), so no stage is read by two CTAs.
+struct SplitRange {
+  int p_begin, p_end, s_eff;
+};
+__device__ __forceinline__ SplitRange split_range(unsigned kp, int max_seq, int window, int S, int j) {
+  const long long n_ll = (long long)kp + 1 < (long long)max_seq ? (long long)kp + 1 : (long long)max_seq;
+  const int lo = first_key((int)n_ll, window);
+  const int n = (int)n_ll - lo;
+  const int s0 = min(S, (n + kMinChunk - 1) / kMinChunk);
+  const int chunk = ((n + s0 - 1) / s0 + kT - 1) / kT * kT;
+  SplitRange r;
+  r.s_eff = (n + chunk - 1) / chunk;
+  r.p_begin = lo + min(n, j * chunk);
+  r.p_end = lo + min(n, j * chunk + chunk);
+  return r;
+}
+
 // Warp roles: warps 0..3 consume, warp 4 issues the bulk copies.  Consumer
 // warp w owns positions 4w..4w+3 of every stage; within it lane = 8p + c
 // takes position p and dims {4c + 32u : u < D/32} (float4 each), so each
@@ -100,30 +121,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int j = blockIdx.x, g = blockIdx.y;
 
   // Launched with programmatic serialization: let the next decode start
-  // launching now, and wait for the previous kernel before any global access.
+  // launching now.  While the previous kernel in the stream drains, the
+  // producer thread pulls this CTA's first stages into L2, steered by a read
+  // of kv_pos that may predate the previous kernel's writes: these are only
+  // hints (a wrong range costs bandwidth, never a result), and nothing read
+  // before the wait below is used afterwards.
   allow_dependent_launch();
+  if (tid == 32 * kCWarps) {
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    const unsigned kp_hint = *static_cast<const volatile uint32_t*>(a.kv_pos_dev);
+    const SplitRange h = split_range(kp_hint, a.max_seq, a.window, S, j);
+    for (int st = 0; st < kPrefetchStages && j < h.s_eff && h.p_begin + st * kT < h.p_end; ++st) {
+      tma_prefetch_l2_2d(&tm_k, g * D, h.p_begin + st * kT);
+      tma_prefetch_l2_2d(&tm_v, g * D, h.p_begin + st * kT);
+    }
+  }
   grid_dependency_wait();
   const unsigned kp = *a.kv_pos_dev;
   if (j == 0 && g == 0 && tid == 0 && (long long)kp >= (long long)a.max_seq)
     record_status(a.status, ATTN_ERR_INVALID_ARG);
-  const long long n_ll = (long long)kp + 1 < (long long)a.max_seq ? (long long)kp + 1 : (long long)a.max_seq;
-  // Positions [lo, lo + n) are attended.  Splits start on stage boundaries
-  // (relative to lo), so no stage is read by two CTAs.
-  const int lo = first_key((int)n_ll, a.window);
-  const int n = (int)n_ll - lo;
-  const int s0 = min(S, (n + kMinChunk - 1) / kMinChunk);
-  const int chunk = ((n + s0 - 1) / s0 + kT - 1) / kT * kT;
-  const int s_eff = (n + chunk - 1) / chunk;
+  const SplitRange range = split_range(kp, a.max_seq, a.window, S, j);
+  const int s_eff = range.s_eff;
   if (j >= s_eff) return;
-  const int p_begin = lo + min(n, j * chunk);
-  const int p_end = lo + min(n, j * chunk + chunk);
+  const int p_begin = range.p_begin;
+  const int p_end = range.p_end;
   const int len = p_end - p_begin;
   const int n_st = (len + kT - 1) / kT;
 
-  if (tid == 32 * kCWarps) {
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
-  }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);

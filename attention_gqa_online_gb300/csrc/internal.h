@@ -72,6 +72,29 @@ int launch_flash_tc(const FlashArgs& a, int prec, cudaStream_t s);
 // flash_tc_supported(a, ATTN_BF16).
 int launch_flash_bf16(const FlashArgs& a, cudaStream_t s);
 
+// Backward of the forward attention (fp32, CUDA cores).  Contiguous
+// layouts: q, out, dout, dq [n_q][H*D]; k, v, dk, dv [n_kv][G*D]; lse
+// [n_q][H][2] as the forward wrote it.  Windows follow the forward: query i
+// sees keys [first_key(n_i, window), n_i) with n_i = min(i + 1, n_kv) if
+// causal, else n_kv.  Needs n_kv >= 1, D % 4 == 0, 1 <= D <= 128 and
+// 16-byte-aligned pointers (the caller checks).
+struct BwdArgs {
+  const float* q;
+  const float* k;
+  const float* v;
+  const float* out;
+  const float* dout;
+  const float* lse;
+  float* dq;
+  float* dk;
+  float* dv;
+  int n_q, n_kv, H, G, D;
+  int causal;
+  int window;
+  float scale;
+};
+int launch_backward_simt(const BwdArgs& a, cudaStream_t s);
+
 // Split-KV decode.
 struct DecodeArgs {
   const float* q;

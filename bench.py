@@ -482,6 +482,36 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
     if only in ("all", "forward"):
         forward_lines("forward_", 0, "causal forward+LSE q_seq=8192 32/8 heads D=128, Q,K N(0,9)")
 
+    if only in ("all", "backward"):
+        # fp32 backward of the long causal forward (dq, dk, dv from out, lse, dout).
+        f = FORWARD
+        q, k, v = synthetic.forward_inputs(f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], seed=5, qk_sigma=3.0)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        outf = torch.empty_like(qd)
+        lse = torch.empty((f["q_seq"], f["H"], 2), device=dev)
+        rc = lib.attn_forward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(), lse.data_ptr(),
+                              f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], A.ATTN_CAUSAL, A.ATTN_FP32, sh)
+        if rc != 0:
+            raise RuntimeError("attn_forward failed: %d" % rc)
+        gout = torch.randn(qd.shape, device=dev, generator=torch.Generator(device=dev).manual_seed(3))
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+
+        def bwd_step(i):
+            rc = lib.attn_backward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(), gout.data_ptr(),
+                                   lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), f["q_seq"],
+                                   f["q_seq"], f["H"], f["G"], f["D"], A.ATTN_CAUSAL, A.ATTN_FP32, 0, sh)
+            if rc != 0:
+                raise RuntimeError("attn_backward failed: %d" % rc)
+        ms = timed(bwd_step, max(3, steps // 4))
+        tf = 2.5 * forward_flops() / (ms * 1e-3) / 1e12
+        res["backward_fp32"] = {
+            "workload": "causal backward (dq, dk, dv) q_seq=8192 32/8 heads D=128, Q,K N(0,9)", "value": tf,
+            "unit": "TFLOP/s", "ms_per_step": ms, "prec": "fp32",
+            "flops": "2.5x the forward's: 10 D per (row, head, kept key), the five products of the gradient",
+            "roofline": roof(A.ATTN_FP32, tf, "bwd_dkdv_kernel<128> + bwd_dq_kernel<128> (+ bwd_prep_kernel)"),
+            "l2": "inputs 320 MiB > L2"}
+        del qd, kd, vd, outf, gout, dq, dk, dv
+
     if only in ("all", "window"):
         forward_lines("forward_window_", WINDOW, "sliding-window causal forward+LSE q_seq=8192 window=%d 32/8 heads "
                       "D=128, Q,K N(0,9)" % WINDOW)
@@ -557,7 +587,7 @@ def main():
     ap.add_argument("--decode-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "forward", "window"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "forward", "window", "backward"], default="all",
                     help="run one workload (for profiling); the default runs all of them")
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     args = ap.parse_args()
@@ -567,7 +597,7 @@ def main():
     if args.impl == "reference":
         reference_arm(args, world, rank)
         return
-    if args.only in ("prefill", "forward", "window"):
+    if args.only in ("prefill", "forward", "window", "backward"):
         run_single(args, local)
         return
     if args.only == "decode":

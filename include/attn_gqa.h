@@ -201,6 +201,38 @@ ATTN_API int attn_prefill_window(const float *q_batch, const float *k_cache, con
                                  int prec, uint32_t window, attn_stream_t stream);
 
 /*
+ * Backward of attn_forward / attn_forward_window: the gradients of `out` with
+ * respect to q, k and v for an upstream gradient dout.  The pages emit the
+ * per-row (max, log-sum) pair for a backward pass (meganeura attention.wgsl:
+ * header comment and the final LSE store) but print none; this is the plain
+ * gradient of the forward definition, rebuilt from that pair:
+ *   p_t  = exp(scale q.k_t - lse0 - lse1)      over the row's kept keys
+ *   ds_t = p_t (dout.v_t - dout.out)
+ *   dq   = scale sum_t ds_t k_t
+ *   dk_t = scale sum over rows of ds_t q      (every query head of the kv head)
+ *   dv_t = sum over rows of p_t dout
+ * The LSE output is not differentiated (its gradient is taken as zero).
+ *
+ *   q, out, dout, dq   [q_seq, H*D]  (out and lse exactly as the forward wrote
+ *   k, v, dk, dv       [kv_seq, G*D]  them for these q, k, v, mask, window)
+ *   lse                [q_seq, H, 2]
+ *   mask, window       as attn_forward_window (window 0 = none)
+ *   prec               ATTN_FP32 (CUDA cores, fp32 arithmetic); the
+ *                      tensor-core precisions return ATTN_ERR_UNSUPPORTED.
+ * dq, dk and dv are written in full (keys no row attends get zero).  Each
+ * element is computed by one thread block, without atomics, so repeated
+ * calls give identical bits.  Needs D % 4 == 0 and 16-byte-aligned pointers,
+ * else ATTN_ERR_UNSUPPORTED.  Scratch (8 bytes per (row, head)) comes from
+ * the library's per-device pool.  q_seq == 0 is a no-op; kv_seq == 0 zeroes
+ * dq.  Errors otherwise as attn_forward, plus NULL out, dout, lse or
+ * gradient pointers.
+ */
+ATTN_API int attn_backward(const float *q, const float *k, const float *v, const float *out, const float *dout,
+                           const float *lse, float *dq, float *dk, float *dv, uint32_t q_seq, uint32_t kv_seq,
+                           uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,
+                           uint32_t window, attn_stream_t stream);
+
+/*
  * Cached single-token decode that allocates nothing and takes no workspace.
  * The shader pages have no counterpart to this entry point; it exists for
  * callers that cannot provide device scratch memory -- a plugin inside a

@@ -129,3 +129,20 @@ def test_decode_window_rejects(lib, kw):
     a.update(kw)
     assert lib.attn_decode_cached_window(a["q"], a["k"], a["v"], a["pos"], a["out"], a["H"], a["G"], a["D"],
                                          a["max_seq"], FAKE, 1 << 20, 16, None) == 1
+
+
+@pytest.mark.parametrize("kw", [
+    dict(H=5, G=2), dict(D=129), dict(mask=3), dict(mask=0, kv_seq=17), dict(q=None), dict(dout=None),
+    dict(lse=None), dict(out=None), dict(dq=None), dict(dk=None), dict(dv=None), dict(prec=7),
+])
+def test_backward_rejects(lib, kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, dout=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, q_seq=16, kv_seq=16,
+             H=4, G=2, D=64, mask=0, prec=0)
+    a.update(kw)
+    assert lib.attn_backward(a["q"], a["k"], a["v"], a["out"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"],
+                             a["q_seq"], a["kv_seq"], a["H"], a["G"], a["D"], a["mask"], a["prec"], 0, None) == 1
+
+
+def test_backward_empty_query_is_noop(lib):
+    assert lib.attn_backward(None, None, None, None, None, None, None, None, None, 0, 0, 4, 2, 64, 0, 0, 0,
+                             None) == 0
