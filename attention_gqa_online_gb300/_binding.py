@@ -55,6 +55,11 @@ def load_library(path=None):
     lib.attn_decode_cached_window.argtypes = lib.attn_decode_cached.argtypes[:-1] + [_u32, _vp]
     lib.attn_prefill_window.restype = ctypes.c_int
     lib.attn_prefill_window.argtypes = lib.attn_prefill.argtypes[:-1] + [_u32, _vp]
+    lib.attn_decode_paged.restype = ctypes.c_int
+    lib.attn_decode_paged.argtypes = [_vp] * 6 + [_u32] * 6 + [_vp, ctypes.c_size_t, _u32, _vp]
+    lib.attn_prefill_paged.restype = ctypes.c_int
+    lib.attn_prefill_paged.argtypes = [_vp] * 5 + [_u32] * 8 + [ctypes.c_float] + [_u32] * 4 + \
+        [ctypes.c_int, _u32, _vp]
     lib.attn_backward.restype = ctypes.c_int
     lib.attn_backward.argtypes = [_vp] * 9 + [_u32] * 5 + [ctypes.c_int, ctypes.c_int, _u32, _vp]
     lib.attn_get_status.restype = ctypes.c_int
@@ -181,6 +186,31 @@ def attn_prefill_window(q_batch, k_cache, v_cache, out_batch, n_queries, n_heads
         _addr(q_batch, "q_batch", f), _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f),
         _addr(out_batch, "out_batch", f), n_queries, n_heads, n_kv_heads, head_dim, kv_dim, max_seq,
         float(scale), start_pos, q_stride, out_stride, q_base, prec, window, _stream(stream)), "attn_prefill_window")
+
+
+def attn_decode_paged(q, k_pages, v_pages, block_table, kv_pos_dev, out, num_heads, num_kv_heads, head_dim,
+                      page_rows, num_pages, max_blocks, workspace, workspace_bytes=None, window=0, stream=None):
+    """Cached decode against a paged cache (block_table: device uint32); see attn_gqa.h."""
+    f = _f32()
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load_library().attn_decode_paged(
+        _addr(q, "q", f), _addr(k_pages, "k_pages", f), _addr(v_pages, "v_pages", f),
+        _addr(block_table, "block_table"), _addr(kv_pos_dev, "kv_pos_dev"), _addr(out, "out", f), num_heads,
+        num_kv_heads, head_dim, page_rows, num_pages, max_blocks, _addr(workspace, "workspace"), workspace_bytes,
+        window, _stream(stream)), "attn_decode_paged")
+
+
+def attn_prefill_paged(q_batch, k_pages, v_pages, block_table, out_batch, n_queries, n_heads, n_kv_heads, head_dim,
+                       kv_dim, page_rows, num_pages, max_blocks, scale, start_pos, q_stride, out_stride, q_base,
+                       prec=ATTN_FP32, window=0, stream=None):
+    """Batched causal prefill against a paged cache; see attn_gqa.h."""
+    f = _f32()
+    _check(load_library().attn_prefill_paged(
+        _addr(q_batch, "q_batch", f), _addr(k_pages, "k_pages", f), _addr(v_pages, "v_pages", f),
+        _addr(block_table, "block_table"), _addr(out_batch, "out_batch", f), n_queries, n_heads, n_kv_heads,
+        head_dim, kv_dim, page_rows, num_pages, max_blocks, float(scale), start_pos, q_stride, out_stride, q_base,
+        prec, window, _stream(stream)), "attn_prefill_paged")
 
 
 def attn_decode_cached_noalloc(q, k_cache, v_cache, kv_pos_dev, out, num_heads, num_kv_heads, head_dim, max_seq,

@@ -241,6 +241,127 @@ extern "C" int attn_prefill(const float* q_batch, const float* k_cache, const fl
                              max_seq, scale, start_pos, q_stride, out_stride, q_base, prec, 0, stream);
 }
 
+// Paged-cache checks shared by the two paged entry points: the logical
+// capacity page_rows * max_blocks and the pool page_rows * num_pages rows must
+// fit in an int.
+static bool paged_sizes_ok(uint32_t page_rows, uint32_t num_pages, uint32_t max_blocks) {
+  return page_rows >= 1 && num_pages >= 1 && max_blocks >= 1 &&
+         (uint64_t)page_rows * max_blocks <= 0x7fffffffu && (uint64_t)page_rows * num_pages <= 0x7fffffffu;
+}
+
+extern "C" int attn_decode_paged(const float* q, const float* k_pages, const float* v_pages,
+                                 const uint32_t* block_table, const uint32_t* kv_pos_dev, float* out,
+                                 uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, uint32_t page_rows,
+                                 uint32_t num_pages, uint32_t max_blocks, void* workspace, size_t workspace_bytes,
+                                 uint32_t window, attn_stream_t stream) {
+  if (!heads_ok(num_heads, num_kv_heads, head_dim) || !paged_sizes_ok(page_rows, num_pages, max_blocks))
+    return ATTN_ERR_INVALID_ARG;
+  if (q == nullptr || k_pages == nullptr || v_pages == nullptr || block_table == nullptr || kv_pos_dev == nullptr ||
+      out == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  const int H = (int)num_heads, G = (int)num_kv_heads, D = (int)head_dim;
+  const int ms = (int)(page_rows * max_blocks);
+  unsigned* st = status_ptr();
+  if (st == nullptr) return ATTN_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_pages) |
+                         reinterpret_cast<uintptr_t>(v_pages)) % 16) == 0;
+  if (decode_split_supported(H, G, D) && aligned && page_rows % 32 == 0) {
+    const int sms = sm_count();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    const size_t need = decode_workspace_bytes(H, G, D, ms, sms);
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % 16) != 0)
+      return ATTN_ERR_INVALID_ARG;
+    DecodeArgs d{};
+    d.q = q;
+    d.k_cache = k_pages;
+    d.v_cache = v_pages;
+    d.kv_pos_dev = kv_pos_dev;
+    d.out = out;
+    d.H = H;
+    d.G = G;
+    d.D = D;
+    d.max_seq = ms;
+    d.window = window_arg(window);
+    d.block_table = block_table;
+    d.page_rows = (int)page_rows;
+    d.num_pages = (int)num_pages;
+    d.workspace = workspace;
+    d.status = st;
+    return launch_decode_split(d, decode_splits(G, ms, sms), s);
+  }
+  FlashArgs a{};
+  a.q = q;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.out = out;
+  a.lse = nullptr;
+  a.q_row_stride = (long long)H * D;
+  a.out_row_stride = a.q_row_stride;
+  a.kv_row_stride = (long long)G * D;
+  a.n_q = 1;
+  a.H = H;
+  a.G = G;
+  a.D = D;
+  a.causal = 1;
+  a.base_pos = 0;
+  a.cap = ms;
+  a.n_all = ms;
+  a.window = window_arg(window);
+  a.scale = 1.0f / sqrtf((float)D);
+  a.kv_pos_dev = kv_pos_dev;
+  a.status = st;
+  a.block_table = block_table;
+  a.page_rows = (int)page_rows;
+  a.num_pages = (int)num_pages;
+  return launch_flash_simt(a, s);
+}
+
+extern "C" int attn_prefill_paged(const float* q_batch, const float* k_pages, const float* v_pages,
+                                  const uint32_t* block_table, float* out_batch, uint32_t n_queries, uint32_t n_heads,
+                                  uint32_t n_kv_heads, uint32_t head_dim, uint32_t kv_dim, uint32_t page_rows,
+                                  uint32_t num_pages, uint32_t max_blocks, float scale, uint32_t start_pos,
+                                  uint32_t q_stride, uint32_t out_stride, uint32_t q_base, int prec, uint32_t window,
+                                  attn_stream_t stream) {
+  if (!heads_ok(n_heads, n_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
+  if (!paged_sizes_ok(page_rows, num_pages, max_blocks)) return ATTN_ERR_INVALID_ARG;
+  const uint64_t max_seq = (uint64_t)page_rows * max_blocks;
+  if ((uint64_t)kv_dim < (uint64_t)n_kv_heads * head_dim) return ATTN_ERR_INVALID_ARG;
+  if ((uint64_t)q_stride < (uint64_t)n_heads * head_dim || (uint64_t)out_stride < (uint64_t)n_heads * head_dim)
+    return ATTN_ERR_INVALID_ARG;
+  if ((uint64_t)start_pos + q_base + n_queries > max_seq) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (n_queries == 0) return ATTN_OK;
+  if (q_batch == nullptr || k_pages == nullptr || v_pages == nullptr || block_table == nullptr || out_batch == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  FlashArgs a{};
+  a.q = q_batch + (size_t)q_base * q_stride;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.out = out_batch + (size_t)q_base * out_stride;
+  a.lse = nullptr;
+  a.q_row_stride = q_stride;
+  a.out_row_stride = out_stride;
+  a.kv_row_stride = kv_dim;
+  a.n_q = (int)n_queries;
+  a.H = (int)n_heads;
+  a.G = (int)n_kv_heads;
+  a.D = (int)head_dim;
+  a.causal = 1;
+  a.base_pos = (long long)start_pos + q_base;
+  a.cap = (int)max_seq;
+  a.n_all = (int)max_seq;
+  a.window = window_arg(window);
+  a.scale = scale;
+  a.kv_pos_dev = nullptr;
+  a.status = status_ptr();
+  if (a.status == nullptr) return ATTN_ERR_CUDA;
+  a.block_table = block_table;
+  a.page_rows = (int)page_rows;
+  a.num_pages = (int)num_pages;
+  return run_flash(a, prec, reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" int attn_backward(const float* q, const float* k, const float* v, const float* out, const float* dout,
                              const float* lse, float* dq, float* dk, float* dv, uint32_t q_seq, uint32_t kv_seq,
                              uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,

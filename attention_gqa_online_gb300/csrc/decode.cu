@@ -85,22 +85,36 @@ __host__ __device__ inline WsLayout ws_layout(void* ws, int H, int G, int D, int
 
 // Positions [p_begin, p_end) of split j of kv head g, out of S splits, for a
 // cache position kv_pos; s_eff = splits that get any position.  Positions
-// [lo, lo + n) are attended; splits start on stage boundaries (relative to
-// lo), so no stage is read by two CTAs.
+// [lo, end) are attended.  Splits cover [lo rounded down to a stage, end) and
+// start on absolute stage boundaries, so no stage is read by two CTAs and no
+// stage crosses a page of a paged cache; positions below lo are masked.
 struct SplitRange {
-  int p_begin, p_end, s_eff;
+  int p_begin, p_end, s_eff, lo;
 };
 __device__ __forceinline__ SplitRange split_range(unsigned kp, int max_seq, int window, int S, int j) {
   const long long n_ll = (long long)kp + 1 < (long long)max_seq ? (long long)kp + 1 : (long long)max_seq;
   const int lo = first_key((int)n_ll, window);
-  const int n = (int)n_ll - lo;
+  const int base = lo / kT * kT;
+  const int n = (int)n_ll - base;
   const int s0 = min(S, (n + kMinChunk - 1) / kMinChunk);
   const int chunk = ((n + s0 - 1) / s0 + kT - 1) / kT * kT;
   SplitRange r;
   r.s_eff = (n + chunk - 1) / chunk;
-  r.p_begin = lo + min(n, j * chunk);
-  r.p_end = lo + min(n, j * chunk + chunk);
+  r.p_begin = base + min(n, j * chunk);
+  r.p_end = base + min(n, j * chunk + chunk);
+  r.lo = lo;
   return r;
+}
+
+// Cache row of position t: t itself, or its pool row through the block table
+// (a page outside the pool gives a row past the pool: zeros, and the status
+// word records ATTN_ERR_INVALID_ARG unless `hint`).
+__device__ __forceinline__ int cache_row(const DecodeArgs& a, int t, bool hint) {
+  if (a.block_table == nullptr) return t;
+  const uint32_t page = a.block_table[t / a.page_rows];
+  if (page < (uint32_t)a.num_pages) return (int)page * a.page_rows + t % a.page_rows;
+  if (!hint) record_status(a.status, ATTN_ERR_INVALID_ARG);
+  return a.num_pages * a.page_rows;
 }
 
 // Warp roles: warps 0..3 consume, warp 4 issues the bulk copies.  Consumer
@@ -133,8 +147,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const unsigned kp_hint = *static_cast<const volatile uint32_t*>(a.kv_pos_dev);
     const SplitRange h = split_range(kp_hint, a.max_seq, a.window, S, j);
     for (int st = 0; st < kPrefetchStages && j < h.s_eff && h.p_begin + st * kT < h.p_end; ++st) {
-      tma_prefetch_l2_2d(&tm_k, g * D, h.p_begin + st * kT);
-      tma_prefetch_l2_2d(&tm_v, g * D, h.p_begin + st * kT);
+      const int row = cache_row(a, h.p_begin + st * kT, true);
+      tma_prefetch_l2_2d(&tm_k, g * D, row);
+      tma_prefetch_l2_2d(&tm_v, g * D, row);
     }
   }
   grid_dependency_wait();
@@ -146,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (j >= s_eff) return;
   const int p_begin = range.p_begin;
   const int p_end = range.p_end;
+  const int lo = range.lo;
   const int len = p_end - p_begin;
   const int n_st = (len + kT - 1) / kT;
 
@@ -176,10 +192,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       for (int st = 0; st < n_st; ++st) {
         const int slot = st % kStages;
         if (st >= kStages) mbar_wait_bounded(&sm.empty[slot], ((st / kStages) - 1) & 1, a.status, &sm.abort);
-        const int t0 = p_begin + st * kT;
+        const int row = cache_row(a, p_begin + st * kT, false);
         mbar_arrive_expect_tx(&sm.full[slot], (unsigned)(kT * D * 4 * 2));
-        tma_load_2d(&sm.k[slot][0], &tm_k, g * D, t0, &sm.full[slot]);
-        tma_load_2d(&sm.v[slot][0], &tm_v, g * D, t0, &sm.full[slot]);
+        tma_load_2d(&sm.k[slot][0], &tm_k, g * D, row, &sm.full[slot]);
+        tma_load_2d(&sm.v[slot][0], &tm_v, g * D, row, &sm.full[slot]);
       }
       // No copy may still be landing when the CTA exits (normally all were
       // consumed already, so these return at once).
@@ -204,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int slot = st % kStages;
       mbar_wait_bounded(&sm.full[slot], (st / kStages) & 1, a.status, &sm.abort);
       const int valid = min(kT, p_end - (p_begin + st * kT));
+      const int first = lo - (p_begin + st * kT);  // positions below this one are outside the window
       const float* ks = sm.k[slot];
       const float* vs = sm.v[slot];
 
@@ -232,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           x += __shfl_xor_sync(0xffffffffu, x, 1);
           x += __shfl_xor_sync(0xffffffffu, x, 2);
           x += __shfl_xor_sync(0xffffffffu, x, 4);
-          sc[grp][h] = (pos < valid) ? x : -INFINITY;
+          sc[grp][h] = (pos < valid && pos >= first) ? x : -INFINITY;
         }
       }
 
@@ -271,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           float wb[GS];
 #pragma unroll
           for (int h = 0; h < GS; ++h) wb[h] = __shfl_sync(0xffffffffu, w[grp][h], 8 * pp);
-          if (ppos < valid) {
+          if (ppos < valid && ppos >= first) {
             if constexpr (VP == 4) {
               const float4 vv = *reinterpret_cast<const float4*>(&vs[ppos * D + 4 * lane]);
 #pragma unroll
@@ -447,7 +464,9 @@ int launch_t(const DecodeArgs& a, int S, cudaStream_t s) {
   // K and V caches as 2-D tensors [max_seq rows][G*D floats]; one request
   // copies kT rows of one kv head's D columns.
   CUtensorMap tm_k, tm_v;
-  const uint64_t dims[2] = {(uint64_t)a.G * D, (uint64_t)a.max_seq};
+  // (A paged cache: the whole pool.)
+  const uint64_t rows = a.block_table != nullptr ? (uint64_t)a.num_pages * a.page_rows : (uint64_t)a.max_seq;
+  const uint64_t dims[2] = {(uint64_t)a.G * D, rows};
   const uint64_t strides[1] = {(uint64_t)a.G * D * 4};
   const uint32_t box[2] = {(uint32_t)D, (uint32_t)kT};
   if (!make_tmap(&tm_k, a.k_cache, 2, dims, strides, box, false, kSwizzleNone) ||

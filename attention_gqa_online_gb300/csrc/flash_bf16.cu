@@ -462,6 +462,34 @@ __global__ void __launch_bounds__(256) kv_to_bf16_kernel(const float4* __restric
   }
 }
 
+// The same conversion from a paged pool: logical rows [row0, row0 + rows) of
+// K and V (rows of n4 float4 groups) are gathered through the block table
+// into the contiguous bf16 copies (logical row t at t * n4).  A page outside
+// the pool gives zeros and ATTN_ERR_INVALID_ARG in the status word.
+__global__ void __launch_bounds__(256) kv_pages_to_bf16_kernel(const float4* __restrict__ k, const float4* __restrict__ v,
+                                                               uint2* __restrict__ k16, uint2* __restrict__ v16,
+                                                               const uint32_t* __restrict__ table, int page_rows,
+                                                               int num_pages, long long row0, long long rows, int n4,
+                                                               unsigned* status) {
+  allow_dependent_launch();
+  grid_dependency_wait();
+  const long long idx = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (idx >= rows * n4) return;
+  const long long t = row0 + idx / n4;
+  const int c = (int)(idx % n4);
+  const uint32_t page = table[t / page_rows];
+  float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+  if (page < (uint32_t)num_pages) {
+    const long long src = ((long long)page * page_rows + t % page_rows) * n4 + c;
+    x = k[src];
+    y = v[src];
+  } else if (c == 0) {
+    record_status(status, ATTN_ERR_INVALID_ARG);
+  }
+  k16[t * n4 + c] = make_uint2(tc::pack_bf16(x.x, x.y), tc::pack_bf16(x.z, x.w));
+  v16[t * n4 + c] = make_uint2(tc::pack_bf16(y.x, y.y), tc::pack_bf16(y.z, y.w));
+}
+
 template <int D>
 int launch_d(const FlashArgs& a, cudaStream_t s) {
   const int gs = a.H / a.G;
@@ -494,10 +522,28 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
     uint2* k2 = reinterpret_cast<uint2*>(k16 + skip);
     uint2* v2 = reinterpret_cast<uint2*>(v16 + skip);
     long long n4 = (elems - skip) / 4;
-    void* cargs[] = {&k4, &v4, &k2, &v2, &n4};
-    const long long blocks = (n4 + kConvPer * 256 - 1) / (kConvPer * 256);
-    if (launch_pdl(reinterpret_cast<const void*>(kv_to_bf16_kernel), dim3((unsigned)blocks), dim3(256), 0, s, cargs) !=
-        cudaSuccess) {
+    cudaError_t e;
+    if (a.block_table == nullptr) {
+      void* cargs[] = {&k4, &v4, &k2, &v2, &n4};
+      const long long blocks = (n4 + kConvPer * 256 - 1) / (kConvPer * 256);
+      e = launch_pdl(reinterpret_cast<const void*>(kv_to_bf16_kernel), dim3((unsigned)blocks), dim3(256), 0, s, cargs);
+    } else {
+      // Paged pool: gather the logical rows [row0, kv_rows) (same addresses
+      // in the copies as for a contiguous cache).
+      const float4* kpool = reinterpret_cast<const float4*>(a.k);
+      const float4* vpool = reinterpret_cast<const float4*>(a.v);
+      uint2* k0 = reinterpret_cast<uint2*>(k16);
+      uint2* v0 = reinterpret_cast<uint2*>(v16);
+      const uint32_t* table = a.block_table;
+      int pr = a.page_rows, np = a.num_pages, row_n4 = (int)(a.kv_row_stride / 4);
+      long long r0 = row0, rows = kv_rows - row0;
+      unsigned* st = a.status;
+      void* gargs[] = {&kpool, &vpool, &k0, &v0, &table, &pr, &np, &r0, &rows, &row_n4, &st};
+      const long long blocks = (rows * row_n4 + 255) / 256;
+      e = launch_pdl(reinterpret_cast<const void*>(kv_pages_to_bf16_kernel), dim3((unsigned)blocks), dim3(256), 0, s,
+                     gargs);
+    }
+    if (e != cudaSuccess) {
       scratch_free(scratch, s);
       return ATTN_ERR_CUDA;
     }

@@ -51,24 +51,23 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
 }
 
 // Issues the async copies of one (rows x DMAX) tile into shared memory, with
-// zero fill for rows >= valid_rows and columns >= D.  src(r) is the global
-// address of row r's first element.
+// zero fill for rows >= valid_rows, columns >= D and rows whose src(r) is
+// nullptr.  src(r) is the global address of row r's first element; `any` is
+// a valid address used for the zero-fill copies.
 template <int DMAX, int STRIDE, bool VEC, typename SrcFn>
-__device__ __forceinline__ void load_tile(float* dst, int rows, int valid_rows, int D, SrcFn src) {
+__device__ __forceinline__ void load_tile(float* dst, int rows, int valid_rows, int D, SrcFn src, const float* any) {
   if constexpr (VEC) {
     constexpr int F = DMAX / 4;
     for (int idx = threadIdx.x; idx < rows * F; idx += NT) {
       const int r = idx / F, f = idx % F;
-      const bool ok = r < valid_rows && 4 * f < D;
-      const float* g = ok ? src(r) + 4 * f : src(0);
-      cp_async16(dst + r * STRIDE + 4 * f, g, ok ? 16u : 0u);
+      const float* row = r < valid_rows && 4 * f < D ? src(r) : nullptr;
+      cp_async16(dst + r * STRIDE + 4 * f, row ? row + 4 * f : any, row ? 16u : 0u);
     }
   } else {
     for (int idx = threadIdx.x; idx < rows * DMAX; idx += NT) {
       const int r = idx / DMAX, c = idx % DMAX;
-      const bool ok = r < valid_rows && c < D;
-      const float* g = ok ? src(r) + c : src(0);
-      cp_async4(dst + r * STRIDE + c, g, ok ? 4u : 0u);
+      const float* row = r < valid_rows && c < D ? src(r) : nullptr;
+      cp_async4(dst + r * STRIDE + c, row ? row + c : any, row ? 4u : 0u);
     }
   }
 }
@@ -141,15 +140,24 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
     const int h = g * gs + (int)(packed % gs);
     return a.q + i * a.q_row_stride + (long long)h * D;
   };
-  load_tile<DMAX, QS, VEC>(sm.q, BM, q_valid, D, q_src);
+  load_tile<DMAX, QS, VEC>(sm.q, BM, q_valid, D, q_src, a.q);
 
   const int n_tiles = (n_max - t_begin + BN - 1) / BN;
+  // Row t of K or V (through the block table for a paged cache; nullptr for
+  // a page outside the pool, which then reads as zeros).
   auto kv_src = [&](const float* base, int t0) {
-    return [=](int r) { return base + (long long)(t0 + r) * a.kv_row_stride + (long long)g * D; };
+    return [=](int r) -> const float* {
+      long long row = t0 + r;
+      if (a.block_table != nullptr) {
+        row = paged_row(a.block_table, a.page_rows, a.num_pages, t0 + r, a.status);
+        if (row < 0) return nullptr;
+      }
+      return base + row * a.kv_row_stride + (long long)g * D;
+    };
   };
   if (n_tiles > 0) {
-    load_tile<DMAX, QS, VEC>(sm.k[0], BN, min(BN, n_max - t_begin), D, kv_src(a.k, t_begin));
-    load_tile<DMAX, DMAX, VEC>(sm.v[0], BN, min(BN, n_max - t_begin), D, kv_src(a.v, t_begin));
+    load_tile<DMAX, QS, VEC>(sm.k[0], BN, min(BN, n_max - t_begin), D, kv_src(a.k, t_begin), a.q);
+    load_tile<DMAX, DMAX, VEC>(sm.v[0], BN, min(BN, n_max - t_begin), D, kv_src(a.v, t_begin), a.q);
   }
   cp_async_commit();
 
@@ -170,8 +178,8 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
     if (it + 1 < n_tiles) {
       const int t1 = t0 + BN;
       const int valid = min(BN, n_max - t1);
-      load_tile<DMAX, QS, VEC>(sm.k[buf ^ 1], BN, valid, D, kv_src(a.k, t1));
-      load_tile<DMAX, DMAX, VEC>(sm.v[buf ^ 1], BN, valid, D, kv_src(a.v, t1));
+      load_tile<DMAX, QS, VEC>(sm.k[buf ^ 1], BN, valid, D, kv_src(a.k, t1), a.q);
+      load_tile<DMAX, DMAX, VEC>(sm.v[buf ^ 1], BN, valid, D, kv_src(a.v, t1), a.q);
       cp_async_commit();
       cp_async_wait<1>();
     } else {

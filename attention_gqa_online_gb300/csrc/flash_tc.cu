@@ -60,6 +60,8 @@ constexpr int kRingBytes = 3 * 65536;  // K/V tile ring in shared memory
 constexpr int kMaxRing = 12;
 constexpr int kColQ = 0, kColS0 = 128, kColO = 384;  // S buffer b at kColS0 + kKeys * b
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
+constexpr int kPageBox = 32;     // key rows per TMA box of a paged cache (page_rows % 32 == 0)
+constexpr int kPageCache = 1024;  // block-table entries a CTA keeps in shared memory
 
 struct __align__(1024) TcSmem {
   unsigned char ring[kRingBytes];
@@ -73,6 +75,7 @@ struct __align__(1024) TcSmem {
   uint64_t drain[2];
   float red_max[2][2][kRows];  // [tile parity][group][row] partial tile maxima
   float red_l[2][kRows];       // [group][row] partial row sums (epilogue)
+  uint32_t pages[kPageCache];  // block-table entries of the CTA's key range (paged caches)
   uint32_t tmem_base;
   int abort;
 };
@@ -137,6 +140,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.abort = 0;
     fence_mbar_init();
   }
+  // Paged cache: the block-table entries of pages [page0, page0 + n_pages)
+  // (the CTA's key range) are read once into shared memory.
+  const int pr = a.page_rows;
+  int page0 = 0, n_pages = 0;
+  if (a.block_table != nullptr && nt > 0) {
+    page0 = jt0 * kKeys / pr;
+    n_pages = min(kPageCache, (n_max - 1) / pr - page0 + 1);
+    for (int i = tid; i < n_pages; i += kThreads) sm.pages[i] = a.block_table[page0 + i];
+  }
   if (warp == 1) tc::tmem_alloc(&sm.tmem_base, 512);
   tc::fence_before_sync();
   __syncthreads();
@@ -164,8 +176,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool is_v = (p == 2 * nt - 1) || (p > 0 && (p & 1) == 0);
         const int t0 = kKeys * (jt0 + (is_v ? (p == 2 * nt - 1 ? nt - 1 : p / 2 - 1) : (p + 1) / 2));
         const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
+        if (a.block_table == nullptr) {
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + kEpr * c, t0, &sm.kv_full[s]);
+          for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + kEpr * c, t0, &sm.kv_full[s]);
+        } else {
+          // Paged: 32-row boxes, each inside one page.  Rows no query of the
+          // CTA reads, and pages outside the pool, come from a row past the
+          // pool's end (zeros).
+          for (int sub = 0; sub < kKeys / kPageBox; ++sub) {
+            const int t = t0 + kPageBox * sub;
+            int y = a.num_pages * pr;
+            if (t < n_max) {
+              const int pi = t / pr;
+              const uint32_t page = pi - page0 < n_pages ? sm.pages[pi - page0] : a.block_table[pi];
+              if (page < (uint32_t)a.num_pages)
+                y = (int)page * pr + t % pr;
+              else
+                record_status(a.status, ATTN_ERR_INVALID_ARG);
+            }
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_2d(dst + c * kChunkBytes + sub * kPageBox * 128, tm, g * D + kEpr * c, y, &sm.kv_full[s]);
+          }
+        }
       }
       // No copy may still be landing in shared memory when the CTA exits
       // (normally every fill was already consumed, so these return at once).
@@ -468,10 +501,13 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.n_q * gs;
   const long long nb = (rows + kRows - 1) / kRows;
   if (nb == 0) return 0;
-  // Rows of K/V any CTA may read: the largest window of the call.  Rows past
-  // it are outside the tensor map and arrive as zeros.
+  // Rows of K/V any CTA may read: the largest window of the call (a paged
+  // cache: the whole pool).  Rows past it are outside the tensor map and
+  // arrive as zeros.
   long long kv_rows = a.causal ? a.base_pos + a.n_q : a.n_all;
   if (kv_rows > a.cap) kv_rows = a.cap;
+  const bool paged = a.block_table != nullptr;
+  if (paged && kv_rows > 0) kv_rows = (long long)a.num_pages * a.page_rows;
   const bool no_keys = kv_rows < 1 || a.k == nullptr || a.v == nullptr;
   if (kv_rows < 1) kv_rows = 1;
   // An empty key set never reads K/V: any aligned base will do.
@@ -486,7 +522,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const uint32_t qbox[3] = {32, (uint32_t)gs, (uint32_t)(kRows / gs)};
   const uint64_t dims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
   const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * 4};
-  const uint32_t box[2] = {32, (uint32_t)kKeys};
+  const uint32_t box[2] = {32, (uint32_t)(paged ? kPageBox : kKeys)};
   if (!make_tmap(&tm_k, kp, 2, dims, strides, box, false, kSwizzle128) ||
       !make_tmap(&tm_v, vp, 2, dims, strides, box, false, kSwizzle128Atom32) ||
       !make_tmap(&tm_q, a.q, 3, qdims, qstrides, qbox, false, kSwizzle128))
@@ -516,6 +552,8 @@ bool flash_tc_supported(const FlashArgs& a, int prec) {
   if (al % 16 != 0) return false;
   if (a.q_row_stride % 4 != 0 || a.out_row_stride % 4 != 0 || a.kv_row_stride % 4 != 0) return false;
   if (prec == ATTN_BF16 && a.kv_row_stride % 8 != 0) return false;  // bf16 rows in 16-byte units
+  if (a.block_table != nullptr && (a.page_rows % kPageBox != 0 || (long long)a.num_pages * a.page_rows > 0x7fffffffLL))
+    return false;
   return true;
 }
 

@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/attn_gqa.h"
+
 namespace attn {
 
 // One flash-style attention launch.  Rows are (query i, head h) pairs; the
@@ -36,7 +38,25 @@ struct FlashArgs {
   // *kv_pos_dev on the device (n_q == 1, causal, cap = max_seq).
   const uint32_t* kv_pos_dev;
   unsigned* status;           // device status word
+  // Paged K/V when block_table != nullptr: k and v are pools of num_pages
+  // pages of page_rows rows, and key row t is pool row
+  // block_table[t / page_rows] * page_rows + t % page_rows (see paged_row).
+  const uint32_t* block_table;
+  int page_rows;
+  int num_pages;
 };
+
+// Pool row of logical key row t in a paged cache, or -1 (and ATTN_ERR_INVALID_ARG
+// in the status word) when the block table names a page outside the pool.
+__device__ __forceinline__ long long paged_row(const uint32_t* table, int page_rows, int num_pages, int t,
+                                               unsigned* status) {
+  const uint32_t page = table[t / page_rows];
+  if (page >= (uint32_t)num_pages) {
+    atomicMax(status, (unsigned)ATTN_ERR_INVALID_ARG);
+    return -1;
+  }
+  return (long long)page * page_rows + t % page_rows;
+}
 
 // First key of a window that ends at n (exclusive) under a sliding window of
 // `window` keys (0 = unlimited): the window keeps the last `window` positions.
@@ -104,6 +124,10 @@ struct DecodeArgs {
   float* out;
   int H, G, D, max_seq;
   int window;  // sliding window length, 0 = none: keys [first_key(n, window), n)
+  // Paged caches (block_table != nullptr): as FlashArgs; page_rows % 32 == 0.
+  const uint32_t* block_table;
+  int page_rows;
+  int num_pages;
   void* workspace;
   unsigned* status;
 };

@@ -201,6 +201,45 @@ ATTN_API int attn_prefill_window(const float *q_batch, const float *k_cache, con
                                  int prec, uint32_t window, attn_stream_t stream);
 
 /*
+ * Paged KV cache: decode and prefill against a cache held in pages.  The
+ * pages name paged KV only as future work for caches that overflow one buffer
+ * (cera attention_prefill.wgsl, header comment); the layout here:
+ *   k_pages, v_pages  pools of num_pages pages; page p holds page_rows
+ *                     consecutive cache positions as rows
+ *                     [p * page_rows, (p + 1) * page_rows) of a
+ *                     [num_pages * page_rows, kv_dim] array (decode:
+ *                     kv_dim = G*D)
+ *   block_table       max_blocks uint32 in DEVICE memory: cache position t
+ *                     is in pool page block_table[t / page_rows] at row
+ *                     t % page_rows.  Entries may repeat (shared pages).
+ * The cache's capacity is max_seq = page_rows * max_blocks; every other
+ * argument, the window rule (with `window` as in the *_window calls), the
+ * result and the errors are those of attn_decode_cached_window /
+ * attn_prefill_window with that max_seq (decode's workspace:
+ * attn_decode_workspace_bytes(H, G, D, max_seq)).  Only the block-table
+ * entries of pages inside a row's window are read; an entry >= num_pages
+ * reads as zeros and records ATTN_ERR_INVALID_ARG in the status word.  The
+ * split decode and the tensor-core precisions need page_rows % 32 == 0
+ * (decode otherwise runs the fp32 CUDA-core kernel; the tensor-core prefill
+ * returns ATTN_ERR_UNSUPPORTED).  The TF32 prefill reads named pages in
+ * 32-row groups, so rows of such a group past the last attended position
+ * must hold finite values.  Further errors: INVALID_ARG for a NULL
+ * block_table, page_rows, num_pages or max_blocks of 0, or a capacity or
+ * pool of 2^31 rows or more.
+ */
+ATTN_API int attn_decode_paged(const float *q, const float *k_pages, const float *v_pages,
+                               const uint32_t *block_table, const uint32_t *kv_pos_dev, float *out,
+                               uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, uint32_t page_rows,
+                               uint32_t num_pages, uint32_t max_blocks, void *workspace, size_t workspace_bytes,
+                               uint32_t window, attn_stream_t stream);
+ATTN_API int attn_prefill_paged(const float *q_batch, const float *k_pages, const float *v_pages,
+                                const uint32_t *block_table, float *out_batch, uint32_t n_queries, uint32_t n_heads,
+                                uint32_t n_kv_heads, uint32_t head_dim, uint32_t kv_dim, uint32_t page_rows,
+                                uint32_t num_pages, uint32_t max_blocks, float scale, uint32_t start_pos,
+                                uint32_t q_stride, uint32_t out_stride, uint32_t q_base, int prec, uint32_t window,
+                                attn_stream_t stream);
+
+/*
  * Backward of attn_forward / attn_forward_window: the gradients of `out` with
  * respect to q, k and v for an upstream gradient dout.  The pages emit the
  * per-row (max, log-sum) pair for a backward pass (meganeura attention.wgsl:

@@ -87,6 +87,38 @@ class Oracle:
             raise ValueError("oracle_decode rejected its arguments")
         return out
 
+    # Paged KV cache.  The pages name paged KV only as future work for caches
+    # that overflow one buffer; the layout read here: the cache is cut into
+    # pages of page_rows consecutive positions, the pool holds num_pages pages
+    # [num_pages, page_rows, kv_dim], and logical position t lives in pool page
+    # block_table[t // page_rows] at row t % page_rows.  The oracle gathers the
+    # logical cache [len(block_table) * page_rows, kv_dim] from the pool and
+    # runs the contiguous computation on it.
+    @staticmethod
+    def gather_pages(pool, block_table, page_rows):
+        pool = np.asarray(pool, dtype=np.float32)
+        table = np.asarray(block_table, dtype=np.int64)
+        num_pages = pool.shape[0] // page_rows
+        if pool.shape[0] != num_pages * page_rows or table.min(initial=0) < 0 or \
+                table.max(initial=0) >= num_pages:
+            raise ValueError("bad page pool or block table")
+        pages = pool.reshape(num_pages, page_rows, pool.shape[1])
+        return np.ascontiguousarray(pages[table].reshape(len(table) * page_rows, pool.shape[1]))
+
+    def decode_paged(self, q, k_pool, v_pool, block_table, kv_pos, H, G, D, page_rows, window=0):
+        """Decode over a paged cache (capacity len(block_table) * page_rows rows); returns out [1, H*D]."""
+        kc = self.gather_pages(k_pool, block_table, page_rows)
+        vc = self.gather_pages(v_pool, block_table, page_rows)
+        return self.decode(q, kc, vc, kv_pos, H, G, D, kc.shape[0], window=window)
+
+    def prefill_paged(self, q_batch, k_pool, v_pool, block_table, out_rows, n_queries, H, G, D, kv_dim, page_rows,
+                      scale, start_pos, q_stride, out_stride, q_base, rows=None, window=0):
+        """Prefill against a paged cache (max_seq = len(block_table) * page_rows)."""
+        kc = self.gather_pages(k_pool, block_table, page_rows)
+        vc = self.gather_pages(v_pool, block_table, page_rows)
+        return self.prefill(q_batch, kc, vc, out_rows, n_queries, H, G, D, kv_dim, kc.shape[0], scale, start_pos,
+                            q_stride, out_stride, q_base, rows=rows, window=window)
+
     def backward(self, q, k, v, dout, q_seq, kv_seq, H, G, D, mask, window=0):
         """Gradients of out for upstream dout: returns (dq [q_seq, H*D], dk, dv [kv_seq, G*D])."""
         q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v, dout))

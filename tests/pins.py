@@ -527,4 +527,60 @@ def pin_backward_gqa_is_summed_mha(orc):
     assert np.max(np.abs(dv - dv2.reshape(n, G, H // G, D).sum(axis=2).reshape(n, G * D))) < 1e-13
 
 
+
+# ---------------------------------------------------------------- paged KV cache
+def _paged_case(seed, max_blocks, page_rows, kv_dim, spare=3):
+    """A contiguous cache, and a pool holding its pages shuffled among `spare`
+    extra NaN pages, with the block table that maps them back."""
+    rng = np.random.default_rng(seed)
+    kc = rng.standard_normal((max_blocks * page_rows, kv_dim)).astype(np.float32)
+    vc = rng.standard_normal((max_blocks * page_rows, kv_dim)).astype(np.float32)
+    num_pages = max_blocks + spare
+    where = rng.permutation(num_pages)[:max_blocks]  # pool page of logical page b
+    kp = np.full((num_pages * page_rows, kv_dim), np.nan, np.float32)
+    vp = np.full((num_pages * page_rows, kv_dim), np.nan, np.float32)
+    for b in range(max_blocks):
+        kp[where[b] * page_rows:(where[b] + 1) * page_rows] = kc[b * page_rows:(b + 1) * page_rows]
+        vp[where[b] * page_rows:(where[b] + 1) * page_rows] = vc[b * page_rows:(b + 1) * page_rows]
+    return kc, vc, kp, vp, where.astype(np.uint32)
+
+
+def pin_paged_decode_equals_contiguous(orc):
+    """Shuffled pages (with unused NaN pages in the pool) give the contiguous cache's bits,
+    with and without a window."""
+    H, G, D, P, nb = 4, 2, 16, 8, 5
+    kc, vc, kp, vp, table = _paged_case(80, nb, P, G * D)
+    q = np.random.default_rng(81).standard_normal((1, H * D)).astype(np.float32)
+    for pos, w in ((0, 0), (17, 0), (39, 0), (39, 9), (100, 0)):
+        a = orc.decode(q, kc, vc, pos, H, G, D, nb * P, window=w)
+        b = orc.decode_paged(q, kp, vp, table, pos, H, G, D, P, window=w)
+        assert np.array_equal(a, b)
+
+
+def pin_paged_prefill_equals_contiguous(orc):
+    H, G, D, P, nb = 4, 2, 16, 16, 4
+    kc, vc, kp, vp, table = _paged_case(82, nb, P, G * D)
+    qb = np.random.default_rng(83).standard_normal((12, H * D)).astype(np.float32)
+    sc = np.float32(0.25)
+    a = orc.prefill(qb, kc, vc, 12, 10, H, G, D, G * D, nb * P, sc, 30, H * D, H * D, 2)
+    b = orc.prefill_paged(qb, kp, vp, table, 12, 10, H, G, D, G * D, P, sc, 30, H * D, H * D, 2)
+    assert np.array_equal(a, b, equal_nan=True)
+
+
+def pin_paged_shared_page(orc):
+    """Two logical pages may map to one pool page (a shared prefix page): the
+    result is that of the contiguous cache holding the page twice."""
+    H, G, D, P = 2, 1, 8, 4
+    rng = np.random.default_rng(84)
+    kp = rng.standard_normal((2 * P, G * D)).astype(np.float32)
+    vp = rng.standard_normal((2 * P, G * D)).astype(np.float32)
+    table = np.array([1, 1, 0], np.uint32)
+    kc = np.concatenate([kp[P:], kp[P:], kp[:P]])
+    vc = np.concatenate([vp[P:], vp[P:], vp[:P]])
+    q = rng.standard_normal((1, H * D)).astype(np.float32)
+    a = orc.decode(q, kc, vc, 10, H, G, D, 3 * P)
+    b = orc.decode_paged(q, kp, vp, table, 10, H, G, D, P)
+    assert np.array_equal(a, b)
+
+
 ALL_PINS = [obj for name, obj in sorted(globals().items()) if name.startswith("pin_")]

@@ -146,3 +146,20 @@ def test_backward_rejects(lib, kw):
 def test_backward_empty_query_is_noop(lib):
     assert lib.attn_backward(None, None, None, None, None, None, None, None, None, 0, 0, 4, 2, 64, 0, 0, 0,
                              None) == 0
+
+
+@pytest.mark.parametrize("kw", [dict(page_rows=0), dict(num_pages=0), dict(max_blocks=0), dict(table=None),
+                                dict(H=5), dict(page_rows=2 ** 20, max_blocks=2 ** 12)])
+def test_decode_paged_rejects(lib, kw):
+    a = dict(table=FAKE, H=32, G=8, D=128, page_rows=32, num_pages=10, max_blocks=8)
+    a.update(kw)
+    assert lib.attn_decode_paged(FAKE, FAKE, FAKE, a["table"], FAKE, FAKE, a["H"], a["G"], a["D"], a["page_rows"],
+                                 a["num_pages"], a["max_blocks"], FAKE, 1 << 20, 0, None) == 1
+
+
+@pytest.mark.parametrize("kw", [dict(page_rows=0), dict(table=None), dict(start=60, n=10), dict(kv_dim=100)])
+def test_prefill_paged_rejects(lib, kw):
+    a = dict(table=FAKE, page_rows=32, num_pages=4, max_blocks=2, start=0, n=8, kv_dim=128)
+    a.update(kw)
+    assert lib.attn_prefill_paged(FAKE, FAKE, FAKE, a["table"], FAKE, a["n"], 4, 2, 64, a["kv_dim"], a["page_rows"],
+                                  a["num_pages"], a["max_blocks"], 0.125, a["start"], 256, 256, 0, 0, 0, None) == 1
