@@ -39,6 +39,9 @@ def load(lib_path=None):
     lib.oracle_prefill.restype = _c_int
     lib.oracle_prefill.argtypes = [_f32p, _f32p, _f32p, _f64p] + [_c_int] * 6 + \
         [ctypes.c_float] + [_c_int] * 4 + [ctypes.c_void_p, _c_int, _c_int]
+    lib.oracle_forward_rope.restype = _c_int
+    lib.oracle_forward_rope.argtypes = [_f32p, _f32p, _f32p, _f64p, ctypes.c_void_p] + [_c_int] * 6 + \
+        [ctypes.c_void_p, _c_int, _c_int, ctypes.c_double]
     lib.oracle_backward.restype = _c_int
     lib.oracle_backward.argtypes = [_f32p, _f32p, _f32p, _f32p, _f64p, _f64p, _f64p] + [_c_int] * 7
     lib.oracle_num_threads.restype = _c_int
@@ -75,6 +78,20 @@ class Oracle:
         del keep
         if rc != 0:
             raise ValueError("oracle_forward rejected its arguments")
+        return out, lse
+
+    def forward_rope(self, q, k, v, q_seq, kv_seq, H, G, D, mask, rope_base, rows=None, want_lse=True, window=0):
+        """forward() with RoPE on q (row i at position i) and k (row t at position t)."""
+        q, k, v = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v))
+        out = np.full((max(q_seq, 0), H * D), np.nan)
+        lse = np.full((max(q_seq, 0), H, 2), np.nan)
+        rp, nr, keep = self._rows(rows)
+        rc = self.lib.oracle_forward_rope(q.reshape(-1), k.reshape(-1), v.reshape(-1), out.reshape(-1),
+                                          lse.ctypes.data_as(ctypes.c_void_p) if want_lse else None,
+                                          q_seq, kv_seq, H, G, D, mask, rp, nr, int(window), float(rope_base))
+        del keep
+        if rc != 0:
+            raise ValueError("oracle_forward_rope rejected its arguments")
         return out, lse
 
     def decode(self, q, k_cache, v_cache, kv_pos, H, G, D, max_seq, window=0):

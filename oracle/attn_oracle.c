@@ -350,3 +350,105 @@ int oracle_backward(const float *q, const float *k, const float *v, const float 
     }
     return err;
 }
+
+/*
+ * Forward with rotary position embedding (RoPE) applied to q and k.  The
+ * forward page leaves its RoPE hooks ($ROPE_DECL, $ROPE_Q_APPLY on the query
+ * value, $K_VAL_EXPR on each key value) to the host framework, so the
+ * convention is this library's reading: pairs (d, d + D/2) for d < D/2
+ * rotated by the angle pos * base^(-2d/D),
+ *   x'[d]       = x[d] cos(a) - x[d + D/2] sin(a)
+ *   x'[d + D/2] = x[d + D/2] cos(a) + x[d] sin(a),
+ * with query row i at position i and key row t at position t.  The rotated
+ * q and k (fp64) then go through the plain definition above.  D even.
+ */
+static void rope_rotate(const float *x, double *y, int D, size_t pos, double base)
+{
+    const int half = D / 2;
+    for (int d = 0; d < half; ++d) {
+        const double a = (double)pos * pow(base, -2.0 * (double)d / (double)D);
+        const double c = cos(a), s = sin(a);
+        y[d] = (double)x[d] * c - (double)x[d + half] * s;
+        y[d + half] = (double)x[d + half] * c + (double)x[d] * s;
+    }
+}
+
+int oracle_forward_rope(const float *q, const float *k, const float *v,
+                        double *out, double *lse, int q_seq, int kv_seq,
+                        int H, int G, int D, int mask, const int *rows, int n_rows, int window,
+                        double rope_base)
+{
+    if (bad_heads(H, G, D) || (D % 2) != 0 || q_seq < 0 || kv_seq < 0 || mask < 0 || mask > 2 || window < 0 ||
+        !(rope_base > 1.0))
+        return -1;
+    if (mask != 2 && kv_seq != q_seq) return -1;
+    if (rows == NULL) n_rows = q_seq;
+    for (int r = 0; r < n_rows; ++r) {
+        int pos = rows ? rows[r] : r;
+        if (pos < 0 || pos >= q_seq) return -1;
+    }
+    const int gs = H / G;
+    const size_t kv_dim = (size_t)G * D;
+    const double scale = 1.0 / sqrt((double)D);
+    /* every key row of every kv head, rotated at its position */
+    double *kr = (double *)malloc(sizeof(double) * (kv_seq > 0 ? (size_t)kv_seq * kv_dim : 1));
+    if (kr == NULL) return -1;
+    for (size_t t = 0; t < (size_t)kv_seq; ++t)
+        for (int g = 0; g < G; ++g) rope_rotate(k + t * kv_dim + (size_t)g * D, kr + t * kv_dim + (size_t)g * D, D, t,
+                                               rope_base);
+    int err = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(kv_seq > 0 ? kv_seq : 1));
+        double *qr = (double *)malloc(sizeof(double) * (size_t)D);
+        if (s == NULL || qr == NULL) {
+#pragma omp atomic write
+            err = -1;
+        } else {
+#pragma omp for collapse(2) schedule(dynamic, 4)
+            for (int r = 0; r < n_rows; ++r) {
+                for (int h = 0; h < H; ++h) {
+                    const int pos = rows ? rows[r] : r;
+                    const int g = h / gs;
+                    const size_t n = (mask == 0) ? (size_t)pos + 1 : (size_t)kv_seq;
+                    const size_t lo = window_start(n, window);
+                    const size_t qo = (size_t)pos * H * D + (size_t)h * D;
+                    double *o = out + qo;
+                    double m = ORACLE_EMPTY_LSE, logl = ORACLE_EMPTY_LSE;
+                    if (n == lo) {
+                        for (int d = 0; d < D; ++d) o[d] = 0.0;
+                    } else {
+                        rope_rotate(q + qo, qr, D, (size_t)pos, rope_base);
+                        m = -INFINITY;
+                        for (size_t t = lo; t < n; ++t) {
+                            const double *kt = kr + t * kv_dim + (size_t)g * D;
+                            double dot = 0.0;
+                            for (int d = 0; d < D; ++d) dot += qr[d] * kt[d];
+                            s[t - lo] = dot * scale;
+                            if (s[t - lo] > m) m = s[t - lo];
+                        }
+                        double l = 0.0;
+                        for (size_t t = lo; t < n; ++t) {
+                            s[t - lo] = exp(s[t - lo] - m);
+                            l += s[t - lo];
+                        }
+                        for (int d = 0; d < D; ++d) {
+                            double acc = 0.0;
+                            for (size_t t = lo; t < n; ++t) acc += s[t - lo] * (double)v[t * kv_dim + (size_t)g * D + d];
+                            o[d] = acc / l;
+                        }
+                        logl = log(l);
+                    }
+                    if (lse) {
+                        lse[((size_t)pos * H + h) * 2] = m;
+                        lse[((size_t)pos * H + h) * 2 + 1] = logl;
+                    }
+                }
+            }
+        }
+        free(s);
+        free(qr);
+    }
+    free(kr);
+    return err;
+}

@@ -583,4 +583,57 @@ def pin_paged_shared_page(orc):
     assert np.array_equal(a, b)
 
 
+
+# ---------------------------------------------------------------- RoPE forward
+def pin_rope_hand_worked(orc):
+    """D = 4, base 100 (so the pair (1, 3) turns by 100^(-1/2) = 0.1 rad per
+    position, the pair (0, 2) by 1 rad).  Query row 2 (position 2) is
+    e0 + e1; key row 0 (position 0) is e2, key row 1 (position 1) is e0 + e3.
+    Rotated: q' = (cos 2, cos 0.2, sin 2, sin 0.2), k0' = e2,
+    k1' = (cos 1, -sin 0.1, sin 1, cos 0.1), so the scores (scale 1/2) are
+    sin(2)/2 and (cos(1) + sin(0.1))/2; V rows are e0 and e1."""
+    q = np.zeros((3, 4), np.float32)
+    q[2] = [1, 1, 0, 0]
+    k = np.array([[0, 0, 1, 0], [1, 0, 0, 1]], np.float32)
+    v = np.eye(2, 4, dtype=np.float32)
+    out, lse = orc.forward_rope(q, k, v, 3, 2, 1, 1, 4, CROSS, 100.0)
+    s = np.array([math.sin(2.0), math.cos(1.0) + math.sin(0.1)]) / 2
+    w = np.exp(s - s.max())
+    assert np.max(np.abs(out[2] - np.array([w[0], w[1], 0, 0]) / w.sum())) < 1e-15
+    assert abs(lse[2, 0, 0] - s.max()) < 1e-15 and abs(lse[2, 0, 1] - math.log(w.sum())) < 1e-15
+
+
+def _rope_complex(x, H, D, base):
+    """Rotate [rows, H*D] with row r at position r, pairs (i, i + D/2) as the
+    complex numbers x_i + i x_(i+D/2) multiplied by exp(i r base^(-2i/D))."""
+    rows = x.shape[0]
+    xt = torch.from_numpy(x.astype(np.float64)).reshape(rows, H, D)
+    z = torch.complex(xt[..., :D // 2], xt[..., D // 2:])
+    ang = torch.arange(rows, dtype=torch.float64)[:, None] * \
+        torch.pow(torch.tensor(base, dtype=torch.float64), -2.0 * torch.arange(D // 2, dtype=torch.float64) / D)
+    z = z * torch.polar(torch.ones_like(ang), ang)[:, None, :]
+    return torch.cat([z.real, z.imag], dim=-1).reshape(rows, H * D).numpy()
+
+
+def pin_rope_complex_sdpa(orc):
+    """Causal and cross RoPE forwards against SDPA on q, k rotated as complex pairs."""
+    for mask, q_seq, kv_seq, w in ((CAUSAL, 12, 12, 0), (CROSS, 7, 15, 0), (CAUSAL, 12, 12, 5)):
+        H, G, D = 6, 2, 8
+        q, k, v = _small(seed=90 + mask + w, q_seq=q_seq, kv_seq=kv_seq, H=H, G=G, D=D)
+        out, _ = orc.forward_rope(q, k, v, q_seq, kv_seq, H, G, D, mask, 10000.0, window=w)
+        qr, kr = _rope_complex(q, H, D, 10000.0), _rope_complex(k, G, D, 10000.0)
+        ends = [i + 1 for i in range(q_seq)] if mask == CAUSAL else [kv_seq] * q_seq
+        ref = _sdpa_banded(qr, kr, v, q_seq, kv_seq, H, G, D, ends, w)
+        assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def pin_rope_gqa_equals_replicated_mha(orc):
+    q, k, v = _small(seed=95, q_seq=10, H=8, G=2, D=16)
+    out, lse = orc.forward_rope(q, k, v, 10, 10, 8, 2, 16, CAUSAL, 500.0)
+    kr = np.repeat(k.reshape(10, 2, 16), 4, axis=1).reshape(10, 8 * 16)
+    vr = np.repeat(v.reshape(10, 2, 16), 4, axis=1).reshape(10, 8 * 16)
+    out2, lse2 = orc.forward_rope(q, kr, vr, 10, 10, 8, 8, 16, CAUSAL, 500.0)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
 ALL_PINS = [obj for name, obj in sorted(globals().items()) if name.startswith("pin_")]

@@ -68,6 +68,17 @@ MUTANTS = [
      "const size_t lo = 0;\n                        if (n == lo)", False),
     ("bwd_causal_short", "const size_t n = (mask == 0) ? (size_t)pos + 1", "const size_t n = (mask == 0) ? (size_t)pos",
      False),
+    # RoPE forward
+    ("rope_sign_flipped", "y[d] = (double)x[d] * c - (double)x[d + half] * s;",
+     "y[d] = (double)x[d] * c + (double)x[d + half] * s;", False),
+    ("rope_pairs_interleaved", "y[d + half] = (double)x[d + half] * c + (double)x[d] * s;",
+     "y[d + half] = (double)x[d + half] * c + (double)x[d] * s; if (D > 2 && d < half) { y[d] = (double)x[d] * c - (double)x[d ^ 1] * s; }",
+     False),
+    ("rope_exponent_halved", "pow(base, -2.0 * (double)d / (double)D)", "pow(base, -1.0 * (double)d / (double)D)", False),
+    ("rope_key_position_shifted", "D, t,\n                                               rope_base);",
+     "D, t + 1,\n                                               rope_base);", False),
+    ("rope_query_unrotated", "rope_rotate(q + qo, qr, D, (size_t)pos, rope_base);",
+     "rope_rotate(q + qo, qr, D, 0, rope_base);", False),
     ("bwd_head_map_interleaved", "const int h = g * gs + hh;", "const int h = hh * G + g;", False),
 ]
 
