@@ -60,8 +60,13 @@ constexpr int kRingBytes = 3 * 65536;  // K/V tile ring in shared memory
 constexpr int kMaxRing = 12;
 constexpr int kColQ = 0, kColS0 = 128, kColO = 384;  // S buffer b at kColS0 + kKeys * b
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
-constexpr int kPageBox = 32;     // key rows per TMA box of a paged cache (page_rows % 32 == 0)
+constexpr int kPageBox = 32;     // fewest key rows per TMA box of a paged cache (page_rows % 32 == 0)
 constexpr int kPageCache = 1024;  // block-table entries a CTA keeps in shared memory
+
+// Key rows per TMA box of a paged cache with pages of page_rows rows.
+__host__ __device__ inline int page_box(int page_rows) {
+  return page_rows % kKeys == 0 ? kKeys : page_rows % 64 == 0 ? 64 : kPageBox;
+}
 
 struct __align__(1024) TcSmem {
   unsigned char ring[kRingBytes];
@@ -180,11 +185,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + kEpr * c, t0, &sm.kv_full[s]);
         } else {
-          // Paged: 32-row boxes, each inside one page.  Rows no query of the
+          // Paged: boxes of page_box rows (128, 64 or 32: the largest that
+          // divides page_rows), each inside one page.  Rows no query of the
           // CTA reads, and pages outside the pool, come from a row past the
           // pool's end (zeros).
-          for (int sub = 0; sub < kKeys / kPageBox; ++sub) {
-            const int t = t0 + kPageBox * sub;
+          const int box = page_box(pr);
+          for (int sub = 0; sub < kKeys / box; ++sub) {
+            const int t = t0 + box * sub;
             int y = a.num_pages * pr;
             if (t < n_max) {
               const int pi = t / pr;
@@ -196,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
-              tma_load_2d(dst + c * kChunkBytes + sub * kPageBox * 128, tm, g * D + kEpr * c, y, &sm.kv_full[s]);
+              tma_load_2d(dst + c * kChunkBytes + sub * box * 128, tm, g * D + kEpr * c, y, &sm.kv_full[s]);
           }
         }
       }
@@ -522,7 +529,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const uint32_t qbox[3] = {32, (uint32_t)gs, (uint32_t)(kRows / gs)};
   const uint64_t dims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
   const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * 4};
-  const uint32_t box[2] = {32, (uint32_t)(paged ? kPageBox : kKeys)};
+  const uint32_t box[2] = {32, (uint32_t)(paged ? page_box(a.page_rows) : kKeys)};
   if (!make_tmap(&tm_k, kp, 2, dims, strides, box, false, kSwizzle128) ||
       !make_tmap(&tm_v, vp, 2, dims, strides, box, false, kSwizzle128Atom32) ||
       !make_tmap(&tm_q, a.q, 3, qdims, qstrides, qbox, false, kSwizzle128))

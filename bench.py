@@ -512,6 +512,86 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
             "l2": "inputs 320 MiB > L2"}
         del qd, kd, vd, outf, gout, dq, dk, dv
 
+    if only in ("all", "paged"):
+        # Paged cache: the decode and prefill workloads with their caches cut
+        # into pages placed in shuffled order in a pool.
+        P_DEC, P_PRE = 64, 128
+        nb = MAX_SEQ // P_DEC
+        rng = torch.Generator().manual_seed(11)
+        q, kc, vc = synthetic.decode_inputs(MAX_SEQ, H, G, D, seed=1)
+        qd = q.to(dev)
+        cache_bytes = 2 * MAX_SEQ * G * D * 4
+        n_rot = max(3, int(math.ceil(2.0 * l2 / cache_bytes)) + 1)
+        pools, tables = [], []
+        for r in range(n_rot):
+            perm = torch.randperm(nb, generator=rng)
+            pools.append((kc.view(nb, P_DEC, G * D)[perm].reshape(MAX_SEQ, G * D).to(dev),
+                          vc.view(nb, P_DEC, G * D)[perm].reshape(MAX_SEQ, G * D).to(dev)))
+            tables.append(torch.argsort(perm).to(torch.int32).to(dev))  # logical page b -> pool page
+        out = torch.empty_like(qd)
+        ws_bytes = A.attn_decode_workspace_bytes(H, G, D, MAX_SEQ)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        pos = torch.full((1,), KV_POS, dtype=torch.int32, device=dev)
+
+        def pdec_step(i):
+            kd, vd = pools[i % n_rot]
+            rc = lib.attn_decode_paged(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), tables[i % n_rot].data_ptr(),
+                                       pos.data_ptr(), out.data_ptr(), H, G, D, P_DEC, nb, nb, ws.data_ptr(),
+                                       ws_bytes, 0, sh)
+            if rc != 0:
+                raise RuntimeError("attn_decode_paged failed: %d" % rc)
+        for i in range(args.warmup):
+            pdec_step(i)
+        torch.cuda.synchronize()
+        n_dec = max(steps, 200)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n_dec):
+            pdec_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res["_launches"] += n_dec + args.warmup
+        ms = e0.elapsed_time(e1) / n_dec
+        by = decode_bytes(KV_POS + 1)
+        gbs = by / (ms * 1e-3) / 1e9
+        res["decode_paged"] = {
+            "workload": "decode kv_pos=16383, cache of 256 pages x 64 rows in shuffled pool order, [16384, 8x128] fp32",
+            "value": gbs, "unit": "GB/s", "us_per_step": ms * 1e3,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "decode_split_kernel<128,4>",
+                         "bytes_per_launch": by, "peak_source": peak_src},
+            "l2": "rotating %d pools > 2x L2" % n_rot, "timing": "%d back-to-back launches" % n_dec}
+        del pools
+        pp = PREFILL
+        nbp = pp["max_seq"] // P_PRE
+        qb, kc2, vc2 = synthetic.prefill_inputs(pp["n_queries"], pp["stride"], pp["max_seq"], pp["G"] * pp["D"], seed=0)
+        per = (qb.numel() + kc2.numel() + vc2.numel()) * 4
+        n_rot2 = max(2, int(math.ceil(2.0 * l2 / per)) + 1)
+        bufs = []
+        for r in range(n_rot2):
+            perm = torch.randperm(nbp, generator=rng)
+            bufs.append((qb.to(dev), kc2.view(nbp, P_PRE, -1)[perm].reshape(pp["max_seq"], -1).to(dev),
+                         vc2.view(nbp, P_PRE, -1)[perm].reshape(pp["max_seq"], -1).to(dev),
+                         torch.argsort(perm).to(torch.int32).to(dev)))
+        outp = torch.empty((pp["n_queries"], pp["stride"]), device=dev)
+        scale = 1.0 / math.sqrt(pp["D"])
+        for prec, name, kern in variants[:2]:
+            def pprefill_step(i, prec=prec):
+                qd2, kd, vd, td = bufs[i % n_rot2]
+                rc = lib.attn_prefill_paged(qd2.data_ptr(), kd.data_ptr(), vd.data_ptr(), td.data_ptr(), outp.data_ptr(),
+                                            pp["n_queries"], pp["H"], pp["G"], pp["D"], pp["G"] * pp["D"], P_PRE, nbp,
+                                            nbp, scale, pp["start_pos"], pp["stride"], pp["stride"], 0, prec, 0, sh)
+                if rc != 0:
+                    raise RuntimeError("attn_prefill_paged failed: %d" % rc)
+            ms = timed(pprefill_step, steps)
+            tf = prefill_flops() / (ms * 1e-3) / 1e12
+            res["prefill_paged_" + name] = {
+                "workload": "prefill 512 queries start_pos=1536, cache of 16 pages x 128 rows in shuffled pool order, "
+                            "32/8 heads D=128", "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "prec": name,
+                "roofline": roof(prec, tf, kern + (" (paged gather pre-pass)" if prec == A.ATTN_BF16 else "")),
+                "l2": "rotating %d input sets" % n_rot2}
+        del bufs
+
     if only in ("all", "window"):
         forward_lines("forward_window_", WINDOW, "sliding-window causal forward+LSE q_seq=8192 window=%d 32/8 heads "
                       "D=128, Q,K N(0,9)" % WINDOW)
@@ -587,7 +667,8 @@ def main():
     ap.add_argument("--decode-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "forward", "window", "backward"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "forward", "window", "backward", "paged"],
+                    default="all",
                     help="run one workload (for profiling); the default runs all of them")
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     args = ap.parse_args()
@@ -597,7 +678,7 @@ def main():
     if args.impl == "reference":
         reference_arm(args, world, rank)
         return
-    if args.only in ("prefill", "forward", "window", "backward"):
+    if args.only in ("prefill", "forward", "window", "backward", "paged"):
         run_single(args, local)
         return
     if args.only == "decode":
