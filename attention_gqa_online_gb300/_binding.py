@@ -60,6 +60,10 @@ def load_library(path=None):
     lib.attn_prefill_paged.restype = ctypes.c_int
     lib.attn_prefill_paged.argtypes = [_vp] * 5 + [_u32] * 8 + [ctypes.c_float] + [_u32] * 4 + \
         [ctypes.c_int, _u32, _vp]
+    lib.attn_rope_table.restype = ctypes.c_int
+    lib.attn_rope_table.argtypes = [_vp, _u32, _u32, ctypes.c_double, _vp]
+    lib.attn_forward_rope.restype = ctypes.c_int
+    lib.attn_forward_rope.argtypes = [_vp] * 5 + [_u32] * 5 + [ctypes.c_int, ctypes.c_int, _u32, _vp, _u32, _vp]
     lib.attn_backward.restype = ctypes.c_int
     lib.attn_backward.argtypes = [_vp] * 9 + [_u32] * 5 + [ctypes.c_int, ctypes.c_int, _u32, _vp]
     lib.attn_get_status.restype = ctypes.c_int
@@ -132,6 +136,24 @@ def attn_backward(q, k, v, out, dout, lse, dq, dk, dv, q_seq, kv_seq, num_heads,
         _addr(q, "q", f), _addr(k, "k", f), _addr(v, "v", f), _addr(out, "out", f), _addr(dout, "dout", f),
         _addr(lse, "lse", f), _addr(dq, "dq", f), _addr(dk, "dk", f), _addr(dv, "dv", f), q_seq, kv_seq,
         num_heads, num_kv_heads, head_dim, mask, prec, window, _stream(stream)), "attn_backward")
+
+
+def attn_rope_table(table, max_pos, head_dim, base=10000.0, stream=None):
+    """Fill a device [max_pos, head_dim] fp32 RoPE table (cos | sin per position); see attn_gqa.h."""
+    _check(load_library().attn_rope_table(_addr(table, "table", _f32()), max_pos, head_dim, float(base),
+                                          _stream(stream)), "attn_rope_table")
+
+
+def attn_forward_rope(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask, prec, window,
+                      rope_table, table_rows=None, stream=None):
+    """attn_forward_window with RoPE on q and k (table from attn_rope_table); see attn_gqa.h."""
+    f = _f32()
+    if table_rows is None:
+        table_rows = rope_table.shape[0]
+    _check(load_library().attn_forward_rope(
+        _addr(q, "q", f), _addr(k, "k", f), _addr(v, "v", f), _addr(out, "out", f), _addr(lse, "lse", f),
+        q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask, prec, window, _addr(rope_table, "rope_table", f),
+        table_rows, _stream(stream)), "attn_forward_rope")
 
 
 def attn_decode_workspace_bytes(num_heads, num_kv_heads, head_dim, max_seq):

@@ -108,6 +108,55 @@ extern "C" int attn_forward_window(const float* q, const float* k, const float* 
   return run_flash(a, prec, reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" int attn_rope_table(float* table, uint32_t max_pos, uint32_t head_dim, double base, attn_stream_t stream) {
+  if (head_dim == 0 || head_dim > 128 || head_dim % 2 != 0 || !(base > 1.0) || !std::isfinite(base))
+    return ATTN_ERR_INVALID_ARG;
+  if ((uint64_t)max_pos * head_dim > 0x7fffffffu) return ATTN_ERR_INVALID_ARG;
+  if (max_pos == 0) return ATTN_OK;
+  if (table == nullptr) return ATTN_ERR_INVALID_ARG;
+  return launch_rope_table(table, (int)max_pos, (int)head_dim, base, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_forward_rope(const float* q, const float* k, const float* v, float* out, float* lse,
+                                 uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
+                                 uint32_t head_dim, int mask, int prec, uint32_t window, const float* rope_table,
+                                 uint32_t table_rows, attn_stream_t stream) {
+  if (!heads_ok(num_heads, num_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
+  if (mask != ATTN_CAUSAL && mask != ATTN_FULL && mask != ATTN_CROSS) return ATTN_ERR_INVALID_ARG;
+  if (mask != ATTN_CROSS && kv_seq != q_seq) return ATTN_ERR_INVALID_ARG;
+  if (q_seq > 0x7fffffffu || kv_seq > 0x7fffffffu) return ATTN_ERR_INVALID_ARG;
+  if (head_dim % 2 != 0 || table_rows < q_seq || table_rows < kv_seq) return ATTN_ERR_INVALID_ARG;
+  if (q_seq == 0) return ATTN_OK;
+  if (q == nullptr || out == nullptr || rope_table == nullptr || (kv_seq > 0 && (k == nullptr || v == nullptr)))
+    return ATTN_ERR_INVALID_ARG;
+  // The table is read as float4 groups of pairs on every path.
+  if (head_dim % 8 != 0 || (reinterpret_cast<uintptr_t>(rope_table) % 16) != 0) return ATTN_ERR_UNSUPPORTED;
+  FlashArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.q_row_stride = (long long)num_heads * head_dim;
+  a.out_row_stride = a.q_row_stride;
+  a.kv_row_stride = (long long)num_kv_heads * head_dim;
+  a.n_q = (int)q_seq;
+  a.H = (int)num_heads;
+  a.G = (int)num_kv_heads;
+  a.D = (int)head_dim;
+  a.causal = (mask == ATTN_CAUSAL);
+  a.base_pos = 0;
+  a.cap = (int)kv_seq;
+  a.n_all = (int)kv_seq;
+  a.window = window_arg(window);
+  a.scale = 1.0f / sqrtf((float)head_dim);
+  a.kv_pos_dev = nullptr;
+  a.rope = rope_table;
+  a.status = status_ptr();
+  if (a.status == nullptr) return ATTN_ERR_CUDA;
+  return run_flash(a, prec, reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" int attn_forward(const float* q, const float* k, const float* v, float* out, float* lse,
                             uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
                             uint32_t head_dim, int mask, int prec, attn_stream_t stream) {

@@ -261,10 +261,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_bounded(&sm.q_full, 0, a.status, &sm.abort);
       const float4* src = reinterpret_cast<const float4*>(qstage + r * D + 64 * grp);
       unsigned char* qdst = qtile + grp * kChunkBytes + r * 128;
+      // RoPE: element e pairs with e +- D/2 (query qi at position base_pos + qi).
+      const float* cs = (a.rope != nullptr && row_ok) ? a.rope + (a.base_pos + qi) * D : nullptr;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int f = (i + r) & 15;
-        const float4 x = src[f];
+        float4 x = src[f];
+        if (cs != nullptr) {
+          const int e = 64 * grp + 4 * f;                 // first element of this float4
+          const bool first = e < D / 2;
+          const int dd = first ? e : e - D / 2;          // pair index
+          const float4 y = *reinterpret_cast<const float4*>(qstage + r * D + (first ? e + D / 2 : dd));
+          const float4 cv = *reinterpret_cast<const float4*>(cs + dd);
+          const float4 sv = *reinterpret_cast<const float4*>(cs + D / 2 + dd);
+          const float sg = first ? -1.f : 1.f;
+          x = make_float4(fmaf(sg * y.x, sv.x, x.x * cv.x), fmaf(sg * y.y, sv.y, x.y * cv.y),
+                          fmaf(sg * y.z, sv.z, x.z * cv.z), fmaf(sg * y.w, sv.w, x.w * cv.w));
+        }
         *reinterpret_cast<uint2*>(qdst + 16 * ((f >> 1) ^ (r & 7)) + 8 * (f & 1)) =
             make_uint2(tc::pack_bf16(x.x * sl2, x.y * sl2), tc::pack_bf16(x.z * sl2, x.w * sl2));
       }
@@ -490,6 +503,34 @@ __global__ void __launch_bounds__(256) kv_pages_to_bf16_kernel(const float4* __r
   v16[t * n4 + c] = make_uint2(tc::pack_bf16(y.x, y.y), tc::pack_bf16(y.z, y.w));
 }
 
+// kv_to_bf16_kernel with RoPE on K: float4 group i (of rows of `stride`
+// floats, kv head g at g*D) pairs with the group D/2 further (or back) in its
+// head; key row t turns at position t.  V is converted as is.
+__global__ void __launch_bounds__(256) kv_rope_to_bf16_kernel(const float4* __restrict__ k, const float4* __restrict__ v,
+                                                              uint2* __restrict__ k16, uint2* __restrict__ v16,
+                                                              const float* __restrict__ table, long long first4,
+                                                              long long n4, int stride4, int D) {
+  allow_dependent_launch();
+  grid_dependency_wait();
+  const long long i = first4 + (long long)blockIdx.x * 256 + threadIdx.x;
+  if (i >= n4) return;
+  const long long t = i / stride4;
+  const int col = 4 * (int)(i % stride4);  // float index within the row
+  const int e = col % D;                   // within the head
+  const bool first = e < D / 2;
+  const int dd = first ? e : e - D / 2;
+  const float4 x = k[i];
+  const float4 y = k[i + (first ? D / 8 : -D / 8)];
+  const float4 cv = *reinterpret_cast<const float4*>(table + t * D + dd);
+  const float4 sv = *reinterpret_cast<const float4*>(table + t * D + D / 2 + dd);
+  const float sg = first ? -1.f : 1.f;
+  const float4 r = make_float4(fmaf(sg * y.x, sv.x, x.x * cv.x), fmaf(sg * y.y, sv.y, x.y * cv.y),
+                               fmaf(sg * y.z, sv.z, x.z * cv.z), fmaf(sg * y.w, sv.w, x.w * cv.w));
+  const float4 w = v[i];
+  k16[i] = make_uint2(tc::pack_bf16(r.x, r.y), tc::pack_bf16(r.z, r.w));
+  v16[i] = make_uint2(tc::pack_bf16(w.x, w.y), tc::pack_bf16(w.z, w.w));
+}
+
 template <int D>
 int launch_d(const FlashArgs& a, cudaStream_t s) {
   const int gs = a.H / a.G;
@@ -523,7 +564,20 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
     uint2* v2 = reinterpret_cast<uint2*>(v16 + skip);
     long long n4 = (elems - skip) / 4;
     cudaError_t e;
-    if (a.block_table == nullptr) {
+    if (a.rope != nullptr) {
+      // RoPE (contiguous K/V rows of G*D floats; the caller checks).
+      const float4* kb = reinterpret_cast<const float4*>(a.k);
+      const float4* vb = reinterpret_cast<const float4*>(a.v);
+      uint2* kd = reinterpret_cast<uint2*>(k16);
+      uint2* vd = reinterpret_cast<uint2*>(v16);
+      const float* table = a.rope;
+      long long first4 = skip / 4, all4 = elems / 4;
+      int stride4 = (int)(a.kv_row_stride / 4), dh = D;
+      void* rargs[] = {&kb, &vb, &kd, &vd, &table, &first4, &all4, &stride4, &dh};
+      const long long blocks = (all4 - first4 + 255) / 256;
+      e = launch_pdl(reinterpret_cast<const void*>(kv_rope_to_bf16_kernel), dim3((unsigned)blocks), dim3(256), 0, s,
+                     rargs);
+    } else if (a.block_table == nullptr) {
       void* cargs[] = {&k4, &v4, &k2, &v2, &n4};
       const long long blocks = (n4 + kConvPer * 256 - 1) / (kConvPer * 256);
       e = launch_pdl(reinterpret_cast<const void*>(kv_to_bf16_kernel), dim3((unsigned)blocks), dim3(256), 0, s, cargs);

@@ -172,6 +172,20 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
     for (int c = 0; c < OC * 4; ++c) o[i][c] = 0.f;
   }
 
+  // Turns the pairs (d, d + D/2) of `rows` rows of a shared-memory tile, row
+  // r at position pos(r), by the RoPE table.
+  auto rope_rows = [&](float* tile, int rows, auto pos) {
+    const int half = D / 2;
+    for (int idx = tid; idx < rows * half; idx += NT) {
+      const int r = idx / half, d = idx % half;
+      const float* cs = a.rope + pos(r) * D;
+      const float c = cs[d], s = cs[half + d];
+      const float x = tile[r * QS + d], y = tile[r * QS + half + d];
+      tile[r * QS + d] = x * c - y * s;
+      tile[r * QS + half + d] = y * c + x * s;
+    }
+  };
+
   for (int it = 0; it < n_tiles; ++it) {
     const int buf = it & 1;
     const int t0 = t_begin + it * BN;
@@ -186,6 +200,13 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
       cp_async_wait<0>();
     }
     __syncthreads();
+    if (a.rope != nullptr) {
+      // RoPE: Q once (query i at base_pos + i), then every K tile (row t at t).
+      if (it == 0)
+        rope_rows(sm.q, q_valid, [&](int r) { return base_pos + (row_base + r) / gs; });
+      rope_rows(sm.k[buf], min(BN, n_max - t0), [&](int r) { return (long long)(t0 + r); });
+      __syncthreads();
+    }
 
     // S = Q K^T for rows r0..r0+3, keys cl + 16j.
     float s[4][4];

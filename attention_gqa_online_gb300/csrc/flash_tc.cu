@@ -313,13 +313,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (nt > 0) {
       constexpr int kQCols = D / 2;
       mbar_wait_bounded(&sm.q_full, 0, a.status, &sm.abort);
+      // RoPE: the group's half pairs with the other half of the row (query
+      // qi at position base_pos + qi; rows past n_q are zeros and stay so).
+      const float* cs = (a.rope != nullptr && row_ok) ? a.rope + (a.base_pos + qi) * D : nullptr;
+      const float sgn = grp == 0 ? -1.f : 1.f;
 #pragma unroll
       for (int c = 0; c < kQCols / 32; ++c) {
         const unsigned char* src = qstage + (grp * (kQCols / 32) + c) * kChunkBytes + r * 128;
+        const unsigned char* other = qstage + ((1 - grp) * (kQCols / 32) + c) * kChunkBytes + r * 128;
         uint32_t v[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const float4 x = *reinterpret_cast<const float4*>(src + 16 * (u ^ (r & 7)));
+          float4 x = *reinterpret_cast<const float4*>(src + 16 * (u ^ (r & 7)));
+          if (cs != nullptr) {
+            const float4 y = *reinterpret_cast<const float4*>(other + 16 * (u ^ (r & 7)));
+            const float4 cv = *reinterpret_cast<const float4*>(cs + 32 * c + 4 * u);
+            const float4 sv = *reinterpret_cast<const float4*>(cs + kQCols + 32 * c + 4 * u);
+            x = make_float4(fmaf(sgn * y.x, sv.x, x.x * cv.x), fmaf(sgn * y.y, sv.y, x.y * cv.y),
+                            fmaf(sgn * y.z, sv.z, x.z * cv.z), fmaf(sgn * y.w, sv.w, x.w * cv.w));
+          }
           v[4 * u] = __float_as_uint(x.x * sl2);
           v[4 * u + 1] = __float_as_uint(x.y * sl2);
           v[4 * u + 2] = __float_as_uint(x.z * sl2);
@@ -520,6 +532,18 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   // An empty key set never reads K/V: any aligned base will do.
   const void* kp = no_keys ? static_cast<const void*>(a.q) : a.k;
   const void* vp = no_keys ? static_cast<const void*>(a.q) : a.v;
+  // RoPE: K turned at its positions into stream-ordered scratch first (rows
+  // of exactly G*D floats; the caller checks).
+  void* scratch = nullptr;
+  if (a.rope != nullptr && !no_keys) {
+    if (scratch_alloc(&scratch, (size_t)kv_rows * a.kv_row_stride * sizeof(float), s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (launch_rope_k(a.k, static_cast<float*>(scratch), a.rope, kv_rows, a.G, D, s) != cudaSuccess) {
+      scratch_free(scratch, s);
+      return ATTN_ERR_CUDA;
+    }
+    kp = scratch;
+  }
   CUtensorMap tm_k, tm_v, tm_q;
   // Q: fp32 [n_q][H][D] (query rows q_row_stride floats apart); one CTA's
   // block is D/32 boxes of 32 floats x gs heads x 128/gs queries, rows past
@@ -530,19 +554,26 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const uint64_t dims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
   const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * 4};
   const uint32_t box[2] = {32, (uint32_t)(paged ? page_box(a.page_rows) : kKeys)};
+  int rc = ATTN_OK;
   if (!make_tmap(&tm_k, kp, 2, dims, strides, box, false, kSwizzle128) ||
       !make_tmap(&tm_v, vp, 2, dims, strides, box, false, kSwizzle128Atom32) ||
-      !make_tmap(&tm_q, a.q, 3, qdims, qstrides, qbox, false, kSwizzle128))
-    return ATTN_ERR_UNSUPPORTED;
-  const size_t smem = sizeof(TcSmem) + 1024;
-  auto kern = flash_tc_kernel<D>;
-  if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
-  FlashArgs aa = a;
-  void* args[] = {&aa, &tm_k, &tm_v, &tm_q};
-  if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s, args) !=
-      cudaSuccess)
-    return ATTN_ERR_CUDA;
-  return ATTN_OK;
+      !make_tmap(&tm_q, a.q, 3, qdims, qstrides, qbox, false, kSwizzle128)) {
+    rc = ATTN_ERR_UNSUPPORTED;
+  } else {
+    const size_t smem = sizeof(TcSmem) + 1024;
+    auto kern = flash_tc_kernel<D>;
+    if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) {
+      rc = ATTN_ERR_CUDA;
+    } else {
+      FlashArgs aa = a;
+      void* args[] = {&aa, &tm_k, &tm_v, &tm_q};
+      if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s,
+                     args) != cudaSuccess)
+        rc = ATTN_ERR_CUDA;
+    }
+  }
+  if (scratch != nullptr && scratch_free(scratch, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+  return rc;
 }
 
 }  // namespace

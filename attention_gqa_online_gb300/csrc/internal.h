@@ -44,6 +44,10 @@ struct FlashArgs {
   const uint32_t* block_table;
   int page_rows;
   int num_pages;
+  // Rotary position embedding when rope != nullptr: the [positions][D]
+  // cos | sin table of launch_rope_table; q of query i is turned at position
+  // base_pos + i and k of key row t at position t before the scores.
+  const float* rope;
 };
 
 // Pool row of logical key row t in a paged cache, or -1 (and ATTN_ERR_INVALID_ARG
@@ -114,6 +118,13 @@ struct BwdArgs {
   float scale;
 };
 int launch_backward_simt(const BwdArgs& a, cudaStream_t s);
+
+// RoPE helpers (rope.cu): fill table[max_pos][D] (cos of the D/2 pairs, then
+// their sin; angles p * base^(-2d/D) in fp64), and write K ([rows][G*D],
+// row t at position t) turned by the table into out.  D % 8 == 0 for
+// launch_rope_k; 16-byte-aligned pointers.
+int launch_rope_table(float* table, int max_pos, int D, double base, cudaStream_t s);
+cudaError_t launch_rope_k(const float* k, float* out, const float* table, long long rows, int G, int D, cudaStream_t s);
 
 // Split-KV decode.
 struct DecodeArgs {

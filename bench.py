@@ -432,19 +432,27 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
                 "traffic": None, "kernel": kernel,
                 "peak_source": "fp32 FMA: %d SMs x 128 lanes x 2 x %.0f MHz" % (sms, sm_mhz)}
 
-    def forward_lines(prefix, window, what):
+    def forward_lines(prefix, window, what, rope=False):
         f = FORWARD
         q, k, v = synthetic.forward_inputs(f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], seed=5, qk_sigma=3.0)
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
         outf = torch.empty_like(qd)
         lse = torch.empty((f["q_seq"], f["H"], 2), device=dev)
+        tab = torch.empty((f["q_seq"], f["D"]), device=dev)
+        if rope:
+            A.attn_rope_table(tab, f["q_seq"], f["D"], 10000.0, stream)
         for prec, name, kern in variants:
             def fwd_step(i, prec=prec):
-                rc = lib.attn_forward_window(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(),
-                                             lse.data_ptr(), f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"],
-                                             A.ATTN_CAUSAL, prec, window, sh)
+                if rope:
+                    rc = lib.attn_forward_rope(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(),
+                                               lse.data_ptr(), f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"],
+                                               A.ATTN_CAUSAL, prec, window, tab.data_ptr(), f["q_seq"], sh)
+                else:
+                    rc = lib.attn_forward_window(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(),
+                                                 lse.data_ptr(), f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"],
+                                                 A.ATTN_CAUSAL, prec, window, sh)
                 if rc != 0:
-                    raise RuntimeError("attn_forward_window failed: %d" % rc)
+                    raise RuntimeError("forward failed: %d" % rc)
             ms = timed(fwd_step, steps)
             tf = forward_flops(window) / (ms * 1e-3) / 1e12
             res[prefix + name] = {
@@ -481,6 +489,10 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
 
     if only in ("all", "forward"):
         forward_lines("forward_", 0, "causal forward+LSE q_seq=8192 32/8 heads D=128, Q,K N(0,9)")
+
+    if only in ("all", "rope"):
+        forward_lines("forward_rope_", 0, "causal forward+LSE with RoPE on q and k (base 10000), q_seq=8192 32/8 "
+                      "heads D=128, Q,K N(0,9)", rope=True)
 
     if only in ("all", "backward"):
         # fp32 backward of the long causal forward (dq, dk, dv from out, lse, dout).
@@ -667,7 +679,7 @@ def main():
     ap.add_argument("--decode-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "forward", "window", "backward", "paged"],
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "forward", "window", "backward", "paged", "rope"],
                     default="all",
                     help="run one workload (for profiling); the default runs all of them")
     ap.add_argument("--ref-seconds", type=float, default=60.0)
@@ -678,7 +690,7 @@ def main():
     if args.impl == "reference":
         reference_arm(args, world, rank)
         return
-    if args.only in ("prefill", "forward", "window", "backward", "paged"):
+    if args.only in ("prefill", "forward", "window", "backward", "paged", "rope"):
         run_single(args, local)
         return
     if args.only == "decode":

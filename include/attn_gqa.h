@@ -201,6 +201,33 @@ ATTN_API int attn_prefill_window(const float *q_batch, const float *k_cache, con
                                  int prec, uint32_t window, attn_stream_t stream);
 
 /*
+ * Rotary position embedding (RoPE) fused into the forward.  The forward page
+ * has hooks for it ($ROPE_DECL; $ROPE_Q_APPLY on the query value, and the key
+ * expression $K_VAL_EXPR) whose bodies it leaves to the host framework.  This
+ * library's convention: the pairs (d, d + D/2), d < D/2, of a row at position
+ * p turn by the angle p * base^(-2d/D),
+ *   x'[d]       = x[d] cos - x[d + D/2] sin
+ *   x'[d + D/2] = x[d + D/2] cos + x[d] sin,
+ * query row i at position i and key row t at position t; V is not turned.
+ *
+ * attn_rope_table fills a caller-owned DEVICE table [max_pos, head_dim] of
+ * fp32: row p holds the cosines of the D/2 pair angles, then their sines,
+ * computed in fp64 (base > 1, head_dim even and <= 128).
+ *
+ * attn_forward_rope is attn_forward_window with q and k turned first (inside
+ * the kernels: the inputs are not modified); rope_table has table_rows >=
+ * max(q_seq, kv_seq) rows from attn_rope_table for this head_dim.  Errors as
+ * attn_forward_window, plus INVALID_ARG for an odd head_dim, a NULL or short
+ * table, and UNSUPPORTED for head_dim % 8 != 0 or a table that is not
+ * 16-byte aligned.
+ */
+ATTN_API int attn_rope_table(float *table, uint32_t max_pos, uint32_t head_dim, double base, attn_stream_t stream);
+ATTN_API int attn_forward_rope(const float *q, const float *k, const float *v, float *out, float *lse,
+                               uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
+                               uint32_t head_dim, int mask, int prec, uint32_t window, const float *rope_table,
+                               uint32_t table_rows, attn_stream_t stream);
+
+/*
  * Paged KV cache: decode and prefill against a cache held in pages.  The
  * pages name paged KV only as future work for caches that overflow one buffer
  * (cera attention_prefill.wgsl, header comment); the layout here:

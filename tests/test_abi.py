@@ -163,3 +163,15 @@ def test_prefill_paged_rejects(lib, kw):
     a.update(kw)
     assert lib.attn_prefill_paged(FAKE, FAKE, FAKE, a["table"], FAKE, a["n"], 4, 2, 64, a["kv_dim"], a["page_rows"],
                                   a["num_pages"], a["max_blocks"], 0.125, a["start"], 256, 256, 0, 0, 0, None) == 1
+
+
+@pytest.mark.parametrize("D,base,rows", [(0, 1e4, 8), (7, 1e4, 8), (130, 1e4, 8), (64, 1.0, 8), (64, math.inf, 8),
+                                         (64, math.nan, 8)])
+def test_rope_table_rejects(lib, D, base, rows):
+    assert lib.attn_rope_table(FAKE, rows, D, base, None) == 1
+
+
+def test_forward_rope_rejects_odd_and_short(lib):
+    assert lib.attn_forward_rope(FAKE, FAKE, FAKE, FAKE, None, 8, 8, 2, 1, 63, 0, 0, 0, FAKE, 8, None) == 1
+    assert lib.attn_forward_rope(FAKE, FAKE, FAKE, FAKE, None, 8, 8, 2, 1, 64, 0, 0, 0, FAKE, 7, None) == 1
+    assert lib.attn_forward_rope(FAKE, FAKE, FAKE, FAKE, None, 8, 8, 2, 1, 64, 0, 0, 0, None, 8, None) == 1
