@@ -25,6 +25,9 @@
 #include "internal.h"
 
 namespace attn {
+
+int launch_flash_simt_plain(const FlashArgs& a, cudaStream_t s);
+
 namespace {
 
 constexpr int BM = 64;   // packed rows per CTA
@@ -200,11 +203,9 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
       cp_async_wait<0>();
     }
     __syncthreads();
-    if (a.rope != nullptr) {
-      // RoPE: Q once (query i at base_pos + i), then every K tile (row t at t).
-      if (it == 0)
-        rope_rows(sm.q, q_valid, [&](int r) { return base_pos + (row_base + r) / gs; });
-      rope_rows(sm.k[buf], min(BN, n_max - t0), [&](int r) { return (long long)(t0 + r); });
+    if (a.rope != nullptr && it == 0) {
+      // RoPE: Q once (query i at base_pos + i); K arrives turned (pre-pass).
+      rope_rows(sm.q, q_valid, [&](int r) { return base_pos + (row_base + r) / gs; });
       __syncthreads();
     }
 
@@ -349,7 +350,27 @@ int launch_one(const FlashArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-int launch_flash_simt(const FlashArgs& a, cudaStream_t s) {
+int launch_flash_simt(const FlashArgs& a0, cudaStream_t s) {
+  // RoPE: K is turned once into stream-ordered scratch (rows of G*D floats,
+  // row t at position t) and the kernel turns Q.
+  FlashArgs a = a0;
+  void* scratch = nullptr;
+  const long long kv_rows = a.causal ? min((long long)a.cap, a.base_pos + a.n_q) : a.n_all;
+  if (a.rope != nullptr && kv_rows > 0) {
+    if (scratch_alloc(&scratch, (size_t)kv_rows * a.kv_row_stride * sizeof(float), s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (launch_rope_k(a.k, static_cast<float*>(scratch), a.rope, kv_rows, a.G, a.D, s) != cudaSuccess) {
+      scratch_free(scratch, s);
+      return ATTN_ERR_CUDA;
+    }
+    a.k = static_cast<const float*>(scratch);
+  }
+  int rc = launch_flash_simt_plain(a, s);
+  if (scratch != nullptr && scratch_free(scratch, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+  return rc;
+}
+
+int launch_flash_simt_plain(const FlashArgs& a, cudaStream_t s) {
   const bool vec = (a.D % 4 == 0) && (a.q_row_stride % 4 == 0) && (a.kv_row_stride % 4 == 0) &&
                    ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
                      reinterpret_cast<uintptr_t>(a.v)) % 16 == 0);
