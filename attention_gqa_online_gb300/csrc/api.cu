@@ -422,7 +422,7 @@ extern "C" int attn_backward(const float* q, const float* k, const float* v, con
   if (q_seq == 0) return ATTN_OK;
   if (q == nullptr || dout == nullptr || dq == nullptr || out == nullptr || lse == nullptr) return ATTN_ERR_INVALID_ARG;
   if (kv_seq > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr)) return ATTN_ERR_INVALID_ARG;
-  if (prec != ATTN_FP32) return ATTN_ERR_UNSUPPORTED;
+  if (prec == ATTN_TF32) return ATTN_ERR_UNSUPPORTED;
   const uintptr_t al = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
                        reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
@@ -451,6 +451,9 @@ extern "C" int attn_backward(const float* q, const float* k, const float* v, con
   a.causal = (mask == ATTN_CAUSAL);
   a.window = window_arg(window);
   a.scale = 1.0f / sqrtf((float)head_dim);
+  a.status = status_ptr();
+  if (a.status == nullptr) return ATTN_ERR_CUDA;
+  if (prec == ATTN_BF16) return backward_bf16_supported(a) ? launch_backward_bf16(a, s) : ATTN_ERR_UNSUPPORTED;
   return launch_backward_simt(a, s);
 }
 

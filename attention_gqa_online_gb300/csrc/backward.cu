@@ -424,6 +424,14 @@ int launch_d(const BwdArgs& a, float* delta, float* l2, cudaStream_t s) {
 
 }  // namespace
 
+cudaError_t launch_bwd_prep(const BwdArgs& a, float* delta, float* l2, cudaStream_t s) {
+  const long long pairs = (long long)a.n_q * a.H;
+  BwdArgs aa = a;
+  void* pargs[] = {&aa, &delta, &l2};
+  return launch_pdl(reinterpret_cast<const void*>(bwd_prep_kernel), dim3((unsigned)((pairs + 7) / 8)), dim3(256), 0, s,
+                    pargs);
+}
+
 int launch_backward_simt(const BwdArgs& a, cudaStream_t s) {
   const long long pairs = (long long)a.n_q * a.H;
   if (pairs == 0) return ATTN_OK;
@@ -432,12 +440,7 @@ int launch_backward_simt(const BwdArgs& a, cudaStream_t s) {
   if (scratch_alloc(&scratch, (size_t)pairs * 2 * sizeof(float), s) != cudaSuccess) return ATTN_ERR_CUDA;
   float* delta = static_cast<float*>(scratch);
   float* l2 = delta + pairs;
-  BwdArgs aa = a;
-  void* pargs[] = {&aa, &delta, &l2};
-  int rc = ATTN_OK;
-  if (launch_pdl(reinterpret_cast<const void*>(bwd_prep_kernel), dim3((unsigned)((pairs + 7) / 8)), dim3(256), 0, s,
-                 pargs) != cudaSuccess)
-    rc = ATTN_ERR_CUDA;
+  int rc = launch_bwd_prep(a, delta, l2, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   if (rc == ATTN_OK) rc = a.D <= 64 ? launch_d<64>(a, delta, l2, s) : launch_d<128>(a, delta, l2, s);
   if (scratch_free(scratch, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
   return rc;

@@ -116,8 +116,16 @@ struct BwdArgs {
   int causal;
   int window;
   float scale;
+  unsigned* status;  // device status word (bounded waits of the tensor-core kernels)
 };
 int launch_backward_simt(const BwdArgs& a, cudaStream_t s);
+// The backward's first pass: delta[i*H + h] = dout . out and l2[i*H + h] =
+// (lse0 + lse1) * log2(e) for every (row, head).
+cudaError_t launch_bwd_prep(const BwdArgs& a, float* delta, float* l2, cudaStream_t s);
+// tcgen05 backward with bf16 operands (bwd_tc.cu): D in {64, 128}, H/G a
+// power of two up to 128, 16-byte-aligned pointers.
+bool backward_bf16_supported(const BwdArgs& a);
+int launch_backward_bf16(const BwdArgs& a, cudaStream_t s);
 
 // RoPE helpers (rope.cu): fill table[max_pos][D] (cos of the D/2 pairs, then
 // their sin; angles p * base^(-2d/D) in fp64), and write K ([rows][G*D],

@@ -507,21 +507,24 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
             raise RuntimeError("attn_forward failed: %d" % rc)
         gout = torch.randn(qd.shape, device=dev, generator=torch.Generator(device=dev).manual_seed(3))
         dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-
-        def bwd_step(i):
-            rc = lib.attn_backward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(), gout.data_ptr(),
-                                   lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), f["q_seq"],
-                                   f["q_seq"], f["H"], f["G"], f["D"], A.ATTN_CAUSAL, A.ATTN_FP32, 0, sh)
-            if rc != 0:
-                raise RuntimeError("attn_backward failed: %d" % rc)
-        ms = timed(bwd_step, max(3, steps // 4))
-        tf = 2.5 * forward_flops() / (ms * 1e-3) / 1e12
-        res["backward_fp32"] = {
-            "workload": "causal backward (dq, dk, dv) q_seq=8192 32/8 heads D=128, Q,K N(0,9)", "value": tf,
-            "unit": "TFLOP/s", "ms_per_step": ms, "prec": "fp32",
-            "flops": "2.5x the forward's: 10 D per (row, head, kept key), the five products of the gradient",
-            "roofline": roof(A.ATTN_FP32, tf, "bwd_dkdv_kernel<128> + bwd_dq_kernel<128> (+ bwd_prep_kernel)"),
-            "l2": "inputs 320 MiB > L2"}
+        for prec, name, kern, nsteps in (
+                (A.ATTN_BF16, "bf16", "bwd_dkdv_tc_kernel<128> + bwd_dq_tc_kernel<128> (+ prep, bf16 pre-passes)",
+                 steps),
+                (A.ATTN_FP32, "fp32", "bwd_dkdv_kernel<128> + bwd_dq_kernel<128> (+ bwd_prep_kernel)",
+                 max(3, steps // 4))):
+            def bwd_step(i, prec=prec):
+                rc = lib.attn_backward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outf.data_ptr(), gout.data_ptr(),
+                                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), f["q_seq"],
+                                       f["q_seq"], f["H"], f["G"], f["D"], A.ATTN_CAUSAL, prec, 0, sh)
+                if rc != 0:
+                    raise RuntimeError("attn_backward failed: %d" % rc)
+            ms = timed(bwd_step, nsteps)
+            tf = 2.5 * forward_flops() / (ms * 1e-3) / 1e12
+            res["backward_" + name] = {
+                "workload": "causal backward (dq, dk, dv) q_seq=8192 32/8 heads D=128, Q,K N(0,9)", "value": tf,
+                "unit": "TFLOP/s", "ms_per_step": ms, "prec": name,
+                "flops": "2.5x the forward's: 10 D per (row, head, kept key), the five products of the gradient",
+                "roofline": roof(prec, tf, kern), "l2": "inputs 320 MiB > L2"}
         del qd, kd, vd, outf, gout, dq, dk, dv
 
     if only in ("all", "paged"):

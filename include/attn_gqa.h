@@ -283,13 +283,17 @@ ATTN_API int attn_prefill_paged(const float *q_batch, const float *k_pages, cons
  *   k, v, dk, dv       [kv_seq, G*D]  them for these q, k, v, mask, window)
  *   lse                [q_seq, H, 2]
  *   mask, window       as attn_forward_window (window 0 = none)
- *   prec               ATTN_FP32 (CUDA cores, fp32 arithmetic); the
- *                      tensor-core precisions return ATTN_ERR_UNSUPPORTED.
+ *   prec               ATTN_FP32: CUDA cores, fp32 arithmetic.
+ *                      ATTN_BF16: tensor cores; q, k, v, dout and the
+ *                      P and dS tiles rounded to bf16, fp32 accumulation
+ *                      (D in {64, 128}, H/G a power of two up to 128).
+ *                      ATTN_TF32 returns ATTN_ERR_UNSUPPORTED.
  * dq, dk and dv are written in full (keys no row attends get zero).  Each
  * element is computed by one thread block, without atomics, so repeated
  * calls give identical bits.  Needs D % 4 == 0 and 16-byte-aligned pointers,
- * else ATTN_ERR_UNSUPPORTED.  Scratch (8 bytes per (row, head)) comes from
- * the library's per-device pool.  q_seq == 0 is a no-op; kv_seq == 0 zeroes
+ * else ATTN_ERR_UNSUPPORTED.  Scratch (8 bytes per (row, head); with
+ * ATTN_BF16 also bf16 copies of q, dout, k and v) comes from the library's
+ * per-device pool.  q_seq == 0 is a no-op; kv_seq == 0 zeroes
  * dq.  Errors otherwise as attn_forward, plus NULL out, dout, lse or
  * gradient pointers.
  */

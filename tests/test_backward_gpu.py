@@ -139,3 +139,64 @@ def test_long_causal_properties_and_sampled_rows(cuda_lib, orc, window):
         lo = max(0, n - window) if window else 0
         dq1, _, _ = orc.backward(qn[i:i + 1], kn[lo:n], vn[lo:n], dn[i:i + 1], 1, n - lo, H, G, D, CROSS)
         assert_grad_close(gq[i:i + 1], dq1, "dq row %d window %d" % (i, window))
+
+
+# ---------------------------------------------------------------- bf16 operands (tensor cores)
+BF16_TOL = 2e-2  # per gradient tensor: max|gpu - ref| <= 2e-2 * max|ref| (the forward's bf16 bound)
+
+
+def gpu_backward_bf16(A, q, k, v, dout, q_seq, kv_seq, H, G, D, mask, window=0):
+    dq_, dk_, dv_, do_ = dev(q), dev(k), dev(v), dev(dout)
+    out = torch.empty((q_seq, H * D), device="cuda")
+    lse = torch.empty((q_seq, H, 2), device="cuda")
+    A.attn_forward_window(dq_, dk_, dv_, out, lse, q_seq, kv_seq, H, G, D, mask, A.ATTN_FP32, window)
+    gq = torch.full((q_seq, H * D), float("nan"), device="cuda")
+    gk = torch.full((kv_seq, G * D), float("nan"), device="cuda")
+    gv = torch.full((kv_seq, G * D), float("nan"), device="cuda")
+    A.attn_backward(dq_, dk_, dv_, out, do_, lse, gq, gk, gv, q_seq, kv_seq, H, G, D, mask, A.ATTN_BF16, window)
+    torch.cuda.synchronize()
+    assert A.attn_get_status() == 0
+    return gq.cpu().numpy(), gk.cpu().numpy(), gv.cpu().numpy()
+
+
+@pytest.mark.parametrize("q_seq,kv_seq,H,G,D,mask,window", [
+    (16, 16, 4, 2, 64, CAUSAL, 0),
+    (16, 24, 4, 2, 64, CROSS, 0),
+    (300, 300, 8, 2, 64, CAUSAL, 0),    # 3 row blocks (gs = 4: 32 queries each), ragged tail
+    (300, 300, 8, 2, 64, FULL, 0),
+    (130, 130, 16, 2, 128, CAUSAL, 0),  # gs = 8
+    (200, 200, 1, 1, 128, CAUSAL, 0),   # MHA, one head
+    (90, 421, 8, 8, 128, CROSS, 0),     # ragged key tail
+    (300, 300, 8, 2, 64, CAUSAL, 100),  # sliding windows
+    (90, 421, 8, 2, 64, CROSS, 129),
+    (1024, 1024, 8, 2, 128, CAUSAL, 0),
+])
+def test_bf16_shapes(cuda_lib, orc, q_seq, kv_seq, H, G, D, mask, window):
+    q, k, v = (x.numpy() for x in synthetic.forward_inputs(q_seq, kv_seq, H, G, D, seed=q_seq + window))
+    dout = np.random.default_rng(q_seq).standard_normal((q_seq, H * D)).astype(np.float32)
+    got = gpu_backward_bf16(cuda_lib, *(torch.from_numpy(x) for x in (q, k, v, dout)), q_seq, kv_seq, H, G, D, mask,
+                            window)
+    ref = orc.backward(q, k, v, dout, q_seq, kv_seq, H, G, D, mask, window=window)
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        assert np.all(np.isfinite(a)), name
+        err = float(np.abs(a - b).max()) / float(np.abs(b).max())
+        assert err <= BF16_TOL, "bf16 backward q%d kv%d mask%d window%d %s: %.3g" % (q_seq, kv_seq, mask, window,
+                                                                                     name, err)
+
+
+def test_bf16_long_causal_properties(cuda_lib, orc):
+    """q_seq 8192, 32 / 8 heads, D=128: key sums of dv and dk, and sampled dq rows (oracle,
+    one row over its own window as cross attention)."""
+    q_seq, H, G, D = 8192, 32, 8, 128
+    q, k, v = synthetic.forward_inputs(q_seq, q_seq, H, G, D, seed=5)
+    dout = torch.from_numpy(np.random.default_rng(78).standard_normal((q_seq, H * D)).astype(np.float32))
+    gq, gk, gv = gpu_backward_bf16(cuda_lib, q, k, v, dout, q_seq, q_seq, H, G, D, CAUSAL)
+    dsum = dout.double().numpy().reshape(q_seq, G, H // G, D).sum(axis=(0, 2)).reshape(G * D)
+    assert np.abs(gv.astype(np.float64).sum(axis=0) - dsum).max() <= BF16_TOL * np.abs(dsum).max()
+    assert np.abs(gk.astype(np.float64).sum(axis=0)).max() <= BF16_TOL * np.abs(gk).sum(axis=0).max()
+    qn, kn, vn, dn = q.numpy(), k.numpy(), v.numpy(), dout.numpy()
+    rows = (0, 1, 127, 4096, 8191)  # row 0 has one key: its exact dq is 0
+    refs = [orc.backward(qn[i:i + 1], kn[:i + 1], vn[:i + 1], dn[i:i + 1], 1, i + 1, H, G, D, CROSS)[0] for i in rows]
+    scale = max(float(np.abs(r).max()) for r in refs)
+    for i, r in zip(rows, refs):
+        assert np.abs(gq[i:i + 1] - r).max() <= BF16_TOL * scale, i
