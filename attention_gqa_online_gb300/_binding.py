@@ -55,6 +55,8 @@ def load_library(path=None):
     lib.attn_decode_cached_window.argtypes = lib.attn_decode_cached.argtypes[:-1] + [_u32, _vp]
     lib.attn_prefill_window.restype = ctypes.c_int
     lib.attn_prefill_window.argtypes = lib.attn_prefill.argtypes[:-1] + [_u32, _vp]
+    lib.attn_decode_append.restype = ctypes.c_int
+    lib.attn_decode_append.argtypes = [_vp] * 7 + [_u32] * 4 + [_vp, ctypes.c_size_t, _vp]
     lib.attn_decode_paged.restype = ctypes.c_int
     lib.attn_decode_paged.argtypes = [_vp] * 6 + [_u32] * 6 + [_vp, ctypes.c_size_t, _u32, _vp]
     lib.attn_prefill_paged.restype = ctypes.c_int
@@ -208,6 +210,19 @@ def attn_prefill_window(q_batch, k_cache, v_cache, out_batch, n_queries, n_heads
         _addr(q_batch, "q_batch", f), _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f),
         _addr(out_batch, "out_batch", f), n_queries, n_heads, n_kv_heads, head_dim, kv_dim, max_seq,
         float(scale), start_pos, q_stride, out_stride, q_base, prec, window, _stream(stream)), "attn_prefill_window")
+
+
+def attn_decode_append(q, k_new, v_new, k_cache, v_cache, kv_pos_dev, out, num_heads, num_kv_heads, head_dim,
+                       max_seq, workspace, workspace_bytes=None, stream=None):
+    """Write the new token's K/V row at *kv_pos_dev, then decode over 0..kv_pos; see attn_gqa.h."""
+    f = _f32()
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load_library().attn_decode_append(
+        _addr(q, "q", f), _addr(k_new, "k_new", f), _addr(v_new, "v_new", f), _addr(k_cache, "k_cache", f),
+        _addr(v_cache, "v_cache", f), _addr(kv_pos_dev, "kv_pos_dev"), _addr(out, "out", f), num_heads,
+        num_kv_heads, head_dim, max_seq, _addr(workspace, "workspace"), workspace_bytes, _stream(stream)),
+        "attn_decode_append")
 
 
 def attn_decode_paged(q, k_pages, v_pages, block_table, kv_pos_dev, out, num_heads, num_kv_heads, head_dim,

@@ -235,6 +235,51 @@ extern "C" int attn_decode_cached_window(const float* q, const float* k_cache, c
   return launch_flash_simt(a, s);
 }
 
+extern "C" int attn_decode_append(const float* q, const float* k_new, const float* v_new, float* k_cache,
+                                  float* v_cache, const uint32_t* kv_pos_dev, float* out, uint32_t num_heads,
+                                  uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq, void* workspace,
+                                  size_t workspace_bytes, attn_stream_t stream) {
+  if (!heads_ok(num_heads, num_kv_heads, head_dim) || max_seq == 0 || max_seq > 0x7fffffffu)
+    return ATTN_ERR_INVALID_ARG;
+  if (q == nullptr || k_new == nullptr || v_new == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      kv_pos_dev == nullptr || out == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  const int H = (int)num_heads, G = (int)num_kv_heads, D = (int)head_dim, ms = (int)max_seq;
+  unsigned* st = status_ptr();
+  if (st == nullptr) return ATTN_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+                         reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(k_new) |
+                         reinterpret_cast<uintptr_t>(v_new)) % 16) == 0;
+  if (decode_split_supported(H, G, D) && aligned) {
+    // The split decode writes the row itself (the split ending at kv_pos).
+    const int sms = sm_count();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    const size_t need = decode_workspace_bytes(H, G, D, ms, sms);
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) % 16) != 0)
+      return ATTN_ERR_INVALID_ARG;
+    DecodeArgs d{};
+    d.q = q;
+    d.k_cache = k_cache;
+    d.v_cache = v_cache;
+    d.kv_pos_dev = kv_pos_dev;
+    d.out = out;
+    d.H = H;
+    d.G = G;
+    d.D = D;
+    d.max_seq = ms;
+    d.k_new = k_new;
+    d.v_new = v_new;
+    d.workspace = workspace;
+    d.status = st;
+    return launch_decode_split(d, decode_splits(G, ms, sms), s);
+  }
+  if (launch_cache_append(k_new, v_new, k_cache, v_cache, kv_pos_dev, G * D, ms, st, s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return attn_decode_cached(q, k_cache, v_cache, kv_pos_dev, out, num_heads, num_kv_heads, head_dim, max_seq,
+                            workspace, workspace_bytes, stream);
+}
+
 extern "C" int attn_decode_cached(const float* q, const float* k_cache, const float* v_cache,
                                   const uint32_t* kv_pos_dev, float* out, uint32_t num_heads,
                                   uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq, void* workspace,

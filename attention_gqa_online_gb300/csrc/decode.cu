@@ -165,6 +165,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int len = p_end - p_begin;
   const int n_st = (len + kT - 1) / kT;
 
+  // Append: the split that ends at kv_pos first writes the new token's K and
+  // V row of kv head g into cache row kv_pos (no other CTA reads that row),
+  // then makes the writes visible to its own bulk copies.
+  if (a.k_new != nullptr && j == s_eff - 1 && (long long)kp < (long long)a.max_seq) {
+    const long long row = cache_row(a, (int)kp, false);
+    if (row < (long long)a.num_pages * a.page_rows || a.block_table == nullptr) {
+      const long long off = row * a.G * D + (long long)g * D;
+      for (int d = 4 * tid; d < D; d += 4 * kThreads) {
+        *reinterpret_cast<float4*>(const_cast<float*>(a.k_cache) + off + d) =
+            *reinterpret_cast<const float4*>(a.k_new + (long long)g * D + d);
+        *reinterpret_cast<float4*>(const_cast<float*>(a.v_cache) + off + d) =
+            *reinterpret_cast<const float4*>(a.v_new + (long long)g * D + d);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+  }
+
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -482,7 +499,31 @@ int launch_t(const DecodeArgs& a, int S, cudaStream_t s) {
              : ATTN_ERR_CUDA;
 }
 
+__global__ void __launch_bounds__(256) cache_append_kernel(const float* __restrict__ k_new,
+                                                           const float* __restrict__ v_new, float* k_cache,
+                                                           float* v_cache, const uint32_t* kv_pos_dev, int kv_dim,
+                                                           int max_seq, unsigned* status) {
+  allow_dependent_launch();
+  grid_dependency_wait();
+  const unsigned kp = *kv_pos_dev;
+  if ((long long)kp >= (long long)max_seq) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) record_status(status, ATTN_ERR_INVALID_ARG);
+    return;
+  }
+  for (int d = blockIdx.x * 256 + threadIdx.x; d < kv_dim; d += gridDim.x * 256) {
+    k_cache[(long long)kp * kv_dim + d] = k_new[d];
+    v_cache[(long long)kp * kv_dim + d] = v_new[d];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_cache_append(const float* k_new, const float* v_new, float* k_cache, float* v_cache,
+                                const uint32_t* kv_pos_dev, int kv_dim, int max_seq, unsigned* status, cudaStream_t s) {
+  void* args[] = {&k_new, &v_new, &k_cache, &v_cache, &kv_pos_dev, &kv_dim, &max_seq, &status};
+  return launch_pdl(reinterpret_cast<const void*>(cache_append_kernel), dim3((unsigned)((kv_dim + 255) / 256)),
+                    dim3(256), 0, s, args);
+}
 
 bool decode_split_supported(int H, int G, int D) {
   if (G <= 0 || H % G != 0) return false;

@@ -75,7 +75,7 @@ __device__ __forceinline__ void load_tile(float* dst, int rows, int valid_rows, 
   }
 }
 
-template <int DMAX, bool VEC>
+template <int DMAX, bool VEC, bool PAGED>
 __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
   using Smem = SimtSmem<DMAX>;
   constexpr int QS = Smem::QS, PS = Smem::PS;
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
   auto kv_src = [&](const float* base, int t0) {
     return [=](int r) -> const float* {
       long long row = t0 + r;
-      if (a.block_table != nullptr) {
+      if constexpr (PAGED) {
         row = paged_row(a.block_table, a.page_rows, a.num_pages, t0 + r, a.status);
         if (row < 0) return nullptr;
       }
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
   }
 }
 
-template <int DMAX, bool VEC>
+template <int DMAX, bool VEC, bool PAGED>
 int launch_one(const FlashArgs& a, cudaStream_t s) {
   const int gs = a.H / a.G;
   const long long rows = (long long)a.n_q * gs;
@@ -338,7 +338,7 @@ int launch_one(const FlashArgs& a, cudaStream_t s) {
   if (nb == 0) return 0;
   if (nb > 0x7fffffffLL || a.G > 65535) return ATTN_ERR_UNSUPPORTED;
   const size_t smem = sizeof(SimtSmem<DMAX>);
-  auto kern = flash_simt_kernel<DMAX, VEC>;
+  auto kern = flash_simt_kernel<DMAX, VEC, PAGED>;
   if (!set_smem_limit(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
   FlashArgs aa = a;
   void* args[] = {&aa};
@@ -374,8 +374,14 @@ int launch_flash_simt_plain(const FlashArgs& a, cudaStream_t s) {
   const bool vec = (a.D % 4 == 0) && (a.q_row_stride % 4 == 0) && (a.kv_row_stride % 4 == 0) &&
                    ((reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
                      reinterpret_cast<uintptr_t>(a.v)) % 16 == 0);
-  if (a.D <= 64) return vec ? launch_one<64, true>(a, s) : launch_one<64, false>(a, s);
-  return vec ? launch_one<128, true>(a, s) : launch_one<128, false>(a, s);
+  // Paged caches get their own instances (the row mapping stays out of the
+  // contiguous kernels' load loops).
+  if (a.block_table != nullptr) {
+    if (a.D <= 64) return vec ? launch_one<64, true, true>(a, s) : launch_one<64, false, true>(a, s);
+    return vec ? launch_one<128, true, true>(a, s) : launch_one<128, false, true>(a, s);
+  }
+  if (a.D <= 64) return vec ? launch_one<64, true, false>(a, s) : launch_one<64, false, false>(a, s);
+  return vec ? launch_one<128, true, false>(a, s) : launch_one<128, false, false>(a, s);
 }
 
 }  // namespace attn

@@ -143,6 +143,10 @@ struct DecodeArgs {
   float* out;
   int H, G, D, max_seq;
   int window;  // sliding window length, 0 = none: keys [first_key(n, window), n)
+  // Append (k_new != nullptr): the new token's K and V rows ([G*D] each) are
+  // written into cache row kv_pos before it is attended.
+  const float* k_new;
+  const float* v_new;
   // Paged caches (block_table != nullptr): as FlashArgs; page_rows % 32 == 0.
   const uint32_t* block_table;
   int page_rows;
@@ -158,6 +162,11 @@ size_t decode_workspace_bytes(int H, int G, int D, int max_seq, int sm_count);
 // True if the split-KV kernels handle these sizes (else the generic kernel runs).
 bool decode_split_supported(int H, int G, int D);
 int launch_decode_split(const DecodeArgs& a, int splits, cudaStream_t s);
+// Writes k_new / v_new ([G*D] each) into row *kv_pos_dev of [max_seq][G*D]
+// caches (nothing, and ATTN_ERR_INVALID_ARG in the status word, when the
+// position is past the cache).
+cudaError_t launch_cache_append(const float* k_new, const float* v_new, float* k_cache, float* v_cache,
+                                const uint32_t* kv_pos_dev, int kv_dim, int max_seq, unsigned* status, cudaStream_t s);
 // Bytes at the start of a split-decode workspace that must be zero when a
 // call begins (the per-kv-head arrival counters).
 size_t decode_ticket_bytes(int G);

@@ -320,23 +320,30 @@ def run_ours(args, world, rank, local):
     clocks = sampler.summary(wall0, wall1) if rank == 0 else None
 
     # e2e: a serving decode step through the public API from pinned host memory:
-    # H2D of the new token's q and its K/V rows (written into cache row kv_pos) and
-    # of kv_pos, the decode, D2H of out.
-    qh = q.pin_memory()
-    krow = caches[0][0][KV_POS].cpu().pin_memory()
-    vrow = caches[0][1][KV_POS].cpu().pin_memory()
-    posh = torch.full((1,), KV_POS, dtype=torch.int32).pin_memory()
+    # one H2D copy of the step's inputs packed as [q | k_new | v_new | kv_pos],
+    # attn_decode_append (writes the new K/V row at kv_pos, then attends 0..kv_pos),
+    # D2H of out.
+    n_q, n_kv = H * D, G * D
+    n_stage = n_q + 2 * n_kv + 4  # kv_pos in the first of four trailing words (16-byte multiple)
+    stage_h = torch.zeros(n_stage, dtype=torch.float32).pin_memory()
+    stage_h[:n_q] = q.reshape(-1)
+    stage_h[n_q:n_q + n_kv] = caches[0][0][KV_POS].cpu()
+    stage_h[n_q + n_kv:n_q + 2 * n_kv] = caches[0][1][KV_POS].cpu()
+    stage_h.view(torch.int32)[n_q + 2 * n_kv] = KV_POS
+    stage_d = torch.empty(n_stage, dtype=torch.float32, device=dev)
+    sp = stage_d.data_ptr()
     outh = torch.empty_like(q).pin_memory()
-    h2d = qh.numel() * 4 + krow.numel() * 4 + vrow.numel() * 4 + 4
+    h2d = n_stage * 4
     d2h = outh.numel() * 4
 
     def e2e_step(i):
         kd, vd = caches[i % n_rot]
-        qd.copy_(qh, non_blocking=True)
-        kd[KV_POS].copy_(krow, non_blocking=True)
-        vd[KV_POS].copy_(vrow, non_blocking=True)
-        pos.copy_(posh, non_blocking=True)
-        A.attn_decode_cached(qd, kd, vd, pos, out, H, G, D, MAX_SEQ, ws, ws_bytes, stream)
+        stage_d.copy_(stage_h, non_blocking=True)
+        rc = lib.attn_decode_append(sp, sp + 4 * n_q, sp + 4 * (n_q + n_kv), kd.data_ptr(), vd.data_ptr(),
+                                    sp + 4 * (n_q + 2 * n_kv), out.data_ptr(), H, G, D, MAX_SEQ, ws.data_ptr(),
+                                    ws_bytes, sh)
+        if rc != 0:
+            raise RuntimeError("attn_decode_append failed: %d" % rc)
         outh.copy_(out, non_blocking=True)
 
     for i in range(args.warmup):
@@ -373,7 +380,8 @@ def run_ours(args, world, rank, local):
                          "isolated_launch_us": iso_ms * 1e3,
                          "bytes_per_launch": step_bytes, "peak_source": peak_src},
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "what": "per step: H2D q + new K/V row + kv_pos, decode, D2H out",
+                    "what": "per step: one H2D of [q | new K row | new V row | kv_pos], attn_decode_append "
+                            "(writes the row at kv_pos, attends 0..kv_pos), D2H out",
                     "us_per_step": e2e_ms * 1e3 / args.steps},
             "gpu_launches": args.steps,
             "clocks": clocks,

@@ -148,6 +148,23 @@ ATTN_API int attn_decode_cached(const float *q, const float *k_cache, const floa
                        void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * Cached decode of a new token that first appends its own K and V row: the
+ * [G*D] rows k_new and v_new (DEVICE memory) are written into row *kv_pos_dev
+ * of k_cache and v_cache, then the call is attn_decode_cached over positions
+ * 0..kv_pos (the new row included).  The pages leave filling the cache to
+ * the host framework; this entry point saves a serving step the separate
+ * copies into the cache (the split decode writes the row itself, in the
+ * split that ends at kv_pos, before that split reads it).  A kv_pos >=
+ * max_seq writes nothing and records ATTN_ERR_INVALID_ARG, as in
+ * attn_decode_cached.  Arguments, workspace and errors otherwise as
+ * attn_decode_cached, plus NULL k_new / v_new.
+ */
+ATTN_API int attn_decode_append(const float *q, const float *k_new, const float *v_new, float *k_cache,
+                                float *v_cache, const uint32_t *kv_pos_dev, float *out, uint32_t num_heads,
+                                uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq, void *workspace,
+                                size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * Batched causal prefill against a KV cache.  Source: cera
  * attention_prefill.wgsl, fn attention_prefill (params n_heads, n_kv_heads,
  * head_dim, kv_dim, max_seq, scale, start_pos, q_stride, out_stride, q_base;

@@ -175,3 +175,11 @@ def test_forward_rope_rejects_odd_and_short(lib):
     assert lib.attn_forward_rope(FAKE, FAKE, FAKE, FAKE, None, 8, 8, 2, 1, 63, 0, 0, 0, FAKE, 8, None) == 1
     assert lib.attn_forward_rope(FAKE, FAKE, FAKE, FAKE, None, 8, 8, 2, 1, 64, 0, 0, 0, FAKE, 7, None) == 1
     assert lib.attn_forward_rope(FAKE, FAKE, FAKE, FAKE, None, 8, 8, 2, 1, 64, 0, 0, 0, None, 8, None) == 1
+
+
+@pytest.mark.parametrize("kw", [dict(H=30), dict(max_seq=0), dict(kn=None), dict(vn=None), dict(pos=None)])
+def test_decode_append_rejects(lib, kw):
+    a = dict(kn=FAKE, vn=FAKE, pos=FAKE, H=32, G=8, D=128, max_seq=100)
+    a.update(kw)
+    assert lib.attn_decode_append(FAKE, a["kn"], a["vn"], FAKE, FAKE, a["pos"], FAKE, a["H"], a["G"], a["D"],
+                                  a["max_seq"], FAKE, 1 << 20, None) == 1

@@ -81,3 +81,36 @@ def test_decode_kv_pos_past_cache_is_clamped_and_flagged(cuda_lib, orc, H, G, D)
         ref = orc.decode(q.numpy(), kc.numpy(), vc.numpy(), max_seq - 1, H, G, D, max_seq)
         assert_out_close(out, ref, FP32, float(vc.abs().max()), "clamped kv_pos=%d" % kp)
     assert cuda_lib.attn_get_status() == 0
+
+
+@pytest.mark.parametrize("H,G,D,max_seq", [(32, 8, 128, 4096), (16, 2, 64, 700), (6, 2, 80, 300)])
+def test_decode_append(cuda_lib, orc, H, G, D, max_seq):
+    """attn_decode_append writes the new row at kv_pos (and nothing else), then
+    decodes over 0..kv_pos: a serving loop of steps against the oracle."""
+    q, kc, vc = synthetic.decode_inputs(max_seq, H, G, D, seed=max_seq + 3)
+    rng = np.random.default_rng(max_seq)
+    kh, vh = kc.numpy().copy(), vc.numpy().copy()
+    dk, dv = dev(kc), dev(vc)
+    ws, pos = make_state(cuda_lib, H, G, D, max_seq)
+    for kv_pos in (0, 1, 2, 63, max_seq // 2, max_seq - 1):
+        kn = rng.standard_normal(G * D).astype(np.float32)
+        vn = rng.standard_normal(G * D).astype(np.float32)
+        qn = rng.standard_normal((1, H * D)).astype(np.float32)
+        pos.fill_(kv_pos)
+        out = torch.full((1, H * D), float("nan"), device="cuda")
+        cuda_lib.attn_decode_append(dev(torch.from_numpy(qn)), dev(torch.from_numpy(kn)), dev(torch.from_numpy(vn)),
+                                    dk, dv, pos, out, H, G, D, max_seq, ws)
+        torch.cuda.synchronize()
+        assert cuda_lib.attn_get_status() == 0
+        kh[kv_pos], vh[kv_pos] = kn, vn
+        assert np.array_equal(dk.cpu().numpy(), kh) and np.array_equal(dv.cpu().numpy(), vh)
+        ref = orc.decode(qn, kh, vh, kv_pos, H, G, D, max_seq)
+        assert_out_close(out.cpu().numpy(), ref, FP32, float(np.abs(vh).max()), "append kv_pos=%d" % kv_pos)
+    # past the cache: nothing written, status flagged
+    before = dk.cpu().numpy().copy()
+    pos.fill_(max_seq)
+    out = torch.empty((1, H * D), device="cuda")
+    cuda_lib.attn_decode_append(dev(q), dev(torch.zeros(G * D)), dev(torch.zeros(G * D)), dk, dv, pos, out, H, G, D,
+                                max_seq, ws)
+    assert cuda_lib.attn_get_status() == cuda_lib.ATTN_ERR_INVALID_ARG
+    assert np.array_equal(dk.cpu().numpy(), before)
