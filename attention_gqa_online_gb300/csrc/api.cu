@@ -207,7 +207,7 @@ extern "C" int attn_decode_cached_window(const float* q, const float* k_cache, c
     d.window = window_arg(window);
     d.workspace = workspace;
     d.status = st;
-    return launch_decode_split(d, decode_splits(G, ms, sms), s);
+    return launch_decode_split(d, decode_splits(decode_groups(H, G, D), ms, sms), s);
   }
   // Other shapes: the generic flash kernel with one query row whose causal
   // position is read from kv_pos_dev.
@@ -272,7 +272,7 @@ extern "C" int attn_decode_append(const float* q, const float* k_new, const floa
     d.v_new = v_new;
     d.workspace = workspace;
     d.status = st;
-    return launch_decode_split(d, decode_splits(G, ms, sms), s);
+    return launch_decode_split(d, decode_splits(decode_groups(H, G, D), ms, sms), s);
   }
   if (launch_cache_append(k_new, v_new, k_cache, v_cache, kv_pos_dev, G * D, ms, st, s) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -382,7 +382,7 @@ extern "C" int attn_decode_paged(const float* q, const float* k_pages, const flo
     d.num_pages = (int)num_pages;
     d.workspace = workspace;
     d.status = st;
-    return launch_decode_split(d, decode_splits(G, ms, sms), s);
+    return launch_decode_split(d, decode_splits(decode_groups(H, G, D), ms, sms), s);
   }
   FlashArgs a{};
   a.q = q;

@@ -5,8 +5,11 @@
 // memory), or to the last `window` of them under a sliding window.  Decode is bound by streaming the K/V cache from HBM, so the
 // design is about bytes, not flops:
 //
-//   * Grid (S, G): CTA (j, g) takes one contiguous range of cache positions
-//     of kv head g and serves all gs = H/G query heads that read it, so every
+//   * Grid (S, G'): CTA (j, g) takes one contiguous range of cache positions
+//     of a kv head and serves a group of GS query heads that read it (G' = G
+//     and GS = gs = H/G up to 4 heads at D = 128, 8 at D = 64; larger groups
+//     are split into G' = G * gs/GS head groups whose CTAs read the same K/V
+//     rows at about the same time, the second read mostly from L2), so every
 //     K/V byte leaves HBM once per call (the shader reads each row once per
 //     query head).  S * G is about two CTAs per SM; the range length comes
 //     from kv_pos on the device, so the launch does not depend on it.
@@ -132,7 +135,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int j = blockIdx.x, g = blockIdx.y;
+  // Grid (S * kv_div, G): the kv_div head groups of one split are adjacent
+  // CTAs, so they stream the same K/V rows at about the same time.
+  const int j = blockIdx.x / a.kv_div;                  // split
+  const int kvh = blockIdx.y;                           // kv head
+  const int g = kvh * a.kv_div + blockIdx.x % a.kv_div;  // head group (query heads g*GS ..)
 
   // Launched with programmatic serialization: let the next decode start
   // launching now.  While the previous kernel in the stream drains, the
@@ -148,13 +155,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const SplitRange h = split_range(kp_hint, a.max_seq, a.window, S, j);
     for (int st = 0; st < kPrefetchStages && j < h.s_eff && h.p_begin + st * kT < h.p_end; ++st) {
       const int row = cache_row(a, h.p_begin + st * kT, true);
-      tma_prefetch_l2_2d(&tm_k, g * D, row);
-      tma_prefetch_l2_2d(&tm_v, g * D, row);
+      tma_prefetch_l2_2d(&tm_k, kvh * D, row);
+      tma_prefetch_l2_2d(&tm_v, kvh * D, row);
     }
   }
   grid_dependency_wait();
   const unsigned kp = *a.kv_pos_dev;
-  if (j == 0 && g == 0 && tid == 0 && (long long)kp >= (long long)a.max_seq)
+  if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0 && (long long)kp >= (long long)a.max_seq)
     record_status(a.status, ATTN_ERR_INVALID_ARG);
   const SplitRange range = split_range(kp, a.max_seq, a.window, S, j);
   const int s_eff = range.s_eff;
@@ -166,17 +173,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int n_st = (len + kT - 1) / kT;
 
   // Append: the split that ends at kv_pos first writes the new token's K and
-  // V row of kv head g into cache row kv_pos (no other CTA reads that row),
-  // then makes the writes visible to its own bulk copies.
+  // V row of its kv head into cache row kv_pos (only the CTAs of that split
+  // read the row; head groups of one kv head write the same values), then
+  // makes the writes visible to its own bulk copies.
   if (a.k_new != nullptr && j == s_eff - 1 && (long long)kp < (long long)a.max_seq) {
     const long long row = cache_row(a, (int)kp, false);
     if (row < (long long)a.num_pages * a.page_rows || a.block_table == nullptr) {
-      const long long off = row * a.G * D + (long long)g * D;
+      const long long off = row * a.G * D + (long long)kvh * D;
       for (int d = 4 * tid; d < D; d += 4 * kThreads) {
         *reinterpret_cast<float4*>(const_cast<float*>(a.k_cache) + off + d) =
-            *reinterpret_cast<const float4*>(a.k_new + (long long)g * D + d);
+            *reinterpret_cast<const float4*>(a.k_new + (long long)kvh * D + d);
         *reinterpret_cast<float4*>(const_cast<float*>(a.v_cache) + off + d) =
-            *reinterpret_cast<const float4*>(a.v_new + (long long)g * D + d);
+            *reinterpret_cast<const float4*>(a.v_new + (long long)kvh * D + d);
       }
       asm volatile("fence.proxy.async.global;" ::: "memory");
     }
@@ -211,8 +219,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (st >= kStages) mbar_wait_bounded(&sm.empty[slot], ((st / kStages) - 1) & 1, a.status, &sm.abort);
         const int row = cache_row(a, p_begin + st * kT, false);
         mbar_arrive_expect_tx(&sm.full[slot], (unsigned)(kT * D * 4 * 2));
-        tma_load_2d(&sm.k[slot][0], &tm_k, g * D, row, &sm.full[slot]);
-        tma_load_2d(&sm.v[slot][0], &tm_v, g * D, row, &sm.full[slot]);
+        tma_load_2d(&sm.k[slot][0], &tm_k, kvh * D, row, &sm.full[slot]);
+        tma_load_2d(&sm.v[slot][0], &tm_v, kvh * D, row, &sm.full[slot]);
       }
       // No copy may still be landing when the CTA exits (normally all were
       // consumed already, so these return at once).
@@ -342,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   __syncthreads();
 
   // Merge the consumer warps' states into this split's partial.
-  const WsLayout ws = ws_layout(a.workspace, a.H, a.G, D, S);
+  const WsLayout ws = ws_layout(a.workspace, a.H, a.G * a.kv_div, D, S);
   for (int idx = tid; idx < GS * D; idx += kThreads) {
     const int h = idx / D, d = idx % D;
     float M = -INFINITY;
@@ -494,7 +502,7 @@ int launch_t(const DecodeArgs& a, int S, cudaStream_t s) {
   int SS = S;
   float sl = sl2;
   void* args[] = {&aa, &SS, &sl, &tm_k, &tm_v};
-  return launch_pdl(reinterpret_cast<const void*>(kern), dim3(S, a.G), dim3(kThreads), smem, s, args) == cudaSuccess
+  return launch_pdl(reinterpret_cast<const void*>(kern), dim3(S * a.kv_div, a.G), dim3(kThreads), smem, s, args) == cudaSuccess
              ? 0
              : ATTN_ERR_CUDA;
 }
@@ -525,13 +533,18 @@ cudaError_t launch_cache_append(const float* k_new, const float* v_new, float* k
                     dim3(256), 0, s, args);
 }
 
+// Query heads per CTA: the group size gs up to 4 (D = 128) or 8 (D = 64);
+// larger power-of-two groups split into gs / GS head groups.
+int heads_per_cta(int gs, int D) { return min(gs, D == 128 ? 4 : 8); }
+
 bool decode_split_supported(int H, int G, int D) {
   if (G <= 0 || H % G != 0) return false;
   const int gs = H / G;
-  if (D == 128) return gs == 1 || gs == 2 || gs == 4;
-  if (D == 64) return gs == 1 || gs == 2 || gs == 4 || gs == 8;
-  return false;
+  if (D != 64 && D != 128) return false;
+  return gs >= 1 && gs <= 32 && (gs & (gs - 1)) == 0;
 }
+
+int decode_groups(int H, int G, int D) { return G * ((H / G) / heads_per_cta(H / G, D)); }
 
 int decode_splits(int G, int max_seq, int sm_count) {
   const int target = (kCtasPerSm * sm_count + G - 1) / G;
@@ -541,24 +554,27 @@ int decode_splits(int G, int max_seq, int sm_count) {
 
 size_t decode_workspace_bytes(int H, int G, int D, int max_seq, int sm_count) {
   if (!decode_split_supported(H, G, D) || max_seq <= 0) return 0;
-  const int S = decode_splits(G, max_seq, sm_count);
-  return align256(sizeof(unsigned) * G) + align256(sizeof(float) * 2 * (size_t)H * even_splits(S)) +
+  const int groups = decode_groups(H, G, D);
+  const int S = decode_splits(groups, max_seq, sm_count);
+  return align256(sizeof(unsigned) * groups) + align256(sizeof(float) * 2 * (size_t)H * even_splits(S)) +
          sizeof(float) * (size_t)H * S * D;
 }
 
 size_t decode_ticket_bytes(int G) { return align256(sizeof(unsigned) * G); }
 
-int launch_decode_split(const DecodeArgs& a, int S, cudaStream_t s) {
-  const int gs = a.H / a.G;
+int launch_decode_split(const DecodeArgs& a0, int S, cudaStream_t s) {
+  DecodeArgs a = a0;
+  const int gs = a.H / a.G, hp = heads_per_cta(gs, a.D);
+  a.kv_div = gs / hp;
   if (a.D == 128) {
-    if (gs == 1) return launch_t<128, 1>(a, S, s);
-    if (gs == 2) return launch_t<128, 2>(a, S, s);
-    if (gs == 4) return launch_t<128, 4>(a, S, s);
+    if (hp == 1) return launch_t<128, 1>(a, S, s);
+    if (hp == 2) return launch_t<128, 2>(a, S, s);
+    if (hp == 4) return launch_t<128, 4>(a, S, s);
   } else if (a.D == 64) {
-    if (gs == 1) return launch_t<64, 1>(a, S, s);
-    if (gs == 2) return launch_t<64, 2>(a, S, s);
-    if (gs == 4) return launch_t<64, 4>(a, S, s);
-    if (gs == 8) return launch_t<64, 8>(a, S, s);
+    if (hp == 1) return launch_t<64, 1>(a, S, s);
+    if (hp == 2) return launch_t<64, 2>(a, S, s);
+    if (hp == 4) return launch_t<64, 4>(a, S, s);
+    if (hp == 8) return launch_t<64, 8>(a, S, s);
   }
   return ATTN_ERR_UNSUPPORTED;
 }

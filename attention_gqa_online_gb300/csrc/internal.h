@@ -143,6 +143,7 @@ struct DecodeArgs {
   float* out;
   int H, G, D, max_seq;
   int window;  // sliding window length, 0 = none: keys [first_key(n, window), n)
+  int kv_div;  // head groups per kv head (set by launch_decode_split)
   // Append (k_new != nullptr): the new token's K and V rows ([G*D] each) are
   // written into cache row kv_pos before it is attended.
   const float* k_new;
@@ -155,8 +156,12 @@ struct DecodeArgs {
   unsigned* status;
 };
 
-// Number of KV splits per kv head for these sizes on a device with sm_count SMs.
-int decode_splits(int G, int max_seq, int sm_count);
+// Head groups of the split decode (one CTA column each): G, or more when a kv
+// head's query heads are split over several CTAs.
+int decode_groups(int H, int G, int D);
+// Number of KV splits per head group for `groups` groups on a device with
+// sm_count SMs.
+int decode_splits(int groups, int max_seq, int sm_count);
 // Workspace bytes the split decode needs (0 if the fast path does not apply).
 size_t decode_workspace_bytes(int H, int G, int D, int max_seq, int sm_count);
 // True if the split-KV kernels handle these sizes (else the generic kernel runs).
@@ -168,8 +173,8 @@ int launch_decode_split(const DecodeArgs& a, int splits, cudaStream_t s);
 cudaError_t launch_cache_append(const float* k_new, const float* v_new, float* k_cache, float* v_cache,
                                 const uint32_t* kv_pos_dev, int kv_dim, int max_seq, unsigned* status, cudaStream_t s);
 // Bytes at the start of a split-decode workspace that must be zero when a
-// call begins (the per-kv-head arrival counters).
-size_t decode_ticket_bytes(int G);
+// call begins (the per-head-group arrival counters).
+size_t decode_ticket_bytes(int groups);
 
 // Device address of the current device's status word (nullptr on failure).
 unsigned* device_status_word();

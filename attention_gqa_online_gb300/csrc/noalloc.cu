@@ -81,7 +81,7 @@ extern "C" int attn_decode_cached_noalloc(const float* q, const float* k_cache, 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // The scratch keeps whatever the previous call left; the per-kv-head
   // arrival counters at its start must read zero when the kernel begins.
-  if (cudaMemsetAsync(scratch, 0, decode_ticket_bytes(G), s) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, decode_ticket_bytes(decode_groups(H, G, D)), s) != cudaSuccess) return ATTN_ERR_CUDA;
   DecodeArgs d{};
   d.q = q;
   d.k_cache = k_cache;
@@ -94,5 +94,5 @@ extern "C" int attn_decode_cached_noalloc(const float* q, const float* k_cache, 
   d.max_seq = ms;
   d.workspace = scratch;
   d.status = status;
-  return launch_decode_split(d, decode_splits(G, ms, sms), s);
+  return launch_decode_split(d, decode_splits(decode_groups(H, G, D), ms, sms), s);
 }

@@ -615,6 +615,48 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
                 "l2": "rotating %d input sets" % n_rot2}
         del bufs
 
+    if only in ("all", "decode_gqa8"):
+        # 64 query heads over 8 kv heads at D = 128 (two head groups per kv head).
+        H8 = 64
+        q8, kc8, vc8 = synthetic.decode_inputs(MAX_SEQ, H8, G, D, seed=2)
+        q8d = q8.to(dev)
+        n_rot8 = max(3, int(math.ceil(2.0 * l2 / (2 * MAX_SEQ * G * D * 4))) + 1)
+        caches8 = [(kc8.to(dev), vc8.to(dev)) for _ in range(n_rot8)]
+        out8 = torch.empty_like(q8d)
+        ws8_bytes = A.attn_decode_workspace_bytes(H8, G, D, MAX_SEQ)
+        ws8 = torch.zeros(ws8_bytes, dtype=torch.uint8, device=dev)
+        pos8 = torch.full((1,), KV_POS, dtype=torch.int32, device=dev)
+
+        def dec8_step(i):
+            kd, vd = caches8[i % n_rot8]
+            rc = lib.attn_decode_cached(q8d.data_ptr(), kd.data_ptr(), vd.data_ptr(), pos8.data_ptr(), out8.data_ptr(),
+                                        H8, G, D, MAX_SEQ, ws8.data_ptr(), ws8_bytes, sh)
+            if rc != 0:
+                raise RuntimeError("attn_decode_cached failed: %d" % rc)
+        for i in range(args.warmup):
+            dec8_step(i)
+        torch.cuda.synchronize()
+        n_dec = max(steps, 200)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n_dec):
+            dec8_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res["_launches"] += n_dec + args.warmup
+        ms = e0.elapsed_time(e1) / n_dec
+        by = 2 * (KV_POS + 1) * G * D * 4 + 2 * H8 * D * 4
+        gbs = by / (ms * 1e-3) / 1e9
+        res["decode_gqa8"] = {
+            "workload": "decode q[1,64x128] kv_cache[16384,8x128] fp32 kv_pos=16383 (8 query heads per kv head)",
+            "value": gbs, "unit": "GB/s", "us_per_step": ms * 1e3,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": "decode_split_kernel<128,4> x 2 head groups per kv head",
+                         "bytes_per_launch": by, "peak_source": peak_src},
+            "l2": "rotating %d caches > 2x L2" % n_rot8, "timing": "%d back-to-back launches" % n_dec}
+        del caches8
+
     if only in ("all", "window"):
         forward_lines("forward_window_", WINDOW, "sliding-window causal forward+LSE q_seq=8192 window=%d 32/8 heads "
                       "D=128, Q,K N(0,9)" % WINDOW)
@@ -690,7 +732,8 @@ def main():
     ap.add_argument("--decode-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["all", "decode", "prefill", "forward", "window", "backward", "paged", "rope"],
+    ap.add_argument("--only", choices=["all", "decode", "prefill", "forward", "window", "backward", "paged", "rope",
+                                       "decode_gqa8"],
                     default="all",
                     help="run one workload (for profiling); the default runs all of them")
     ap.add_argument("--ref-seconds", type=float, default=60.0)
@@ -701,7 +744,7 @@ def main():
     if args.impl == "reference":
         reference_arm(args, world, rank)
         return
-    if args.only in ("prefill", "forward", "window", "backward", "paged", "rope"):
+    if args.only in ("prefill", "forward", "window", "backward", "paged", "rope", "decode_gqa8"):
         run_single(args, local)
         return
     if args.only == "decode":

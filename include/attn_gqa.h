@@ -333,7 +333,7 @@ ATTN_API int attn_backward(const float *q, const float *k, const float *v, const
  * GPU that loads libattn_gqa.so holds it until the process exits.
  *   - Sizes whose split decode would need more than 4 MiB of scratch (about
  *     H * 2 * SMs / G * D * 4 bytes), shapes the split kernels do not cover
- *     (D = 128 with gs in {1, 2, 4}; D = 64 with gs in {1, 2, 4, 8}) and
+ *     (they take D in {64, 128} with gs = H/G a power of two up to 32) and
  *     pointers that are not 16-byte aligned return ATTN_ERR_UNSUPPORTED;
  *     nothing is launched.
  *   - All calls on a device share the one array, and it keeps what the last

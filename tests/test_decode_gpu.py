@@ -44,7 +44,10 @@ def test_decode_config_sweep(cuda_lib, orc, kv_pos):
     (8, 8, 128, 700, [0, 1, 699]),              # split kernel, MHA
     (4, 2, 64, 1, [0]),                         # one-row cache
     (6, 2, 80, 513, [0, 200, 512]),             # generic kernel (D = 80, gs = 3)
-    (64, 4, 128, 260, [5, 259]),                # generic kernel (gs = 16)
+    (64, 4, 128, 260, [5, 259]),                # split kernel, gs = 16: four head groups per kv head
+    (64, 8, 128, 4096, [0, 31, 32, 4095]),      # split kernel, gs = 8 at D = 128: two head groups
+    (32, 2, 64, 1000, [0, 999]),                # split kernel, gs = 16 at D = 64: two head groups
+    (96, 3, 128, 500, [100, 499]),              # gs = 32: eight head groups
     (2, 1, 12, 40, [0, 39]),                    # generic kernel, small D
 ])
 def test_decode_shapes(cuda_lib, orc, H, G, D, max_seq, positions):
@@ -83,7 +86,8 @@ def test_decode_kv_pos_past_cache_is_clamped_and_flagged(cuda_lib, orc, H, G, D)
     assert cuda_lib.attn_get_status() == 0
 
 
-@pytest.mark.parametrize("H,G,D,max_seq", [(32, 8, 128, 4096), (16, 2, 64, 700), (6, 2, 80, 300)])
+@pytest.mark.parametrize("H,G,D,max_seq", [(32, 8, 128, 4096), (16, 2, 64, 700), (6, 2, 80, 300),
+                                            (64, 8, 128, 600)])
 def test_decode_append(cuda_lib, orc, H, G, D, max_seq):
     """attn_decode_append writes the new row at kv_pos (and nothing else), then
     decodes over 0..kv_pos: a serving loop of steps against the oracle."""

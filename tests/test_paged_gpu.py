@@ -41,6 +41,7 @@ def table_dev(table):
     (32, 8, 128, 256, 16),   # split kernel, 256-row pages
     (16, 2, 64, 64, 40),     # split kernel, gs = 8
     (6, 2, 80, 16, 30),      # generic kernel (D = 80, 16-row pages)
+    (64, 8, 128, 64, 20),    # split kernel, gs = 8 at D = 128 (two head groups)
 ])
 def test_decode_paged(cuda_lib, orc, H, G, D, page_rows, max_blocks):
     kp, vp, table, num_pages = paged_pool(H + page_rows, max_blocks, page_rows, G * D)

@@ -191,6 +191,7 @@ def run_decode_window(A, dq, dk, dv, pos_t, ws, kv_pos, H, G, D, max_seq, window
     (32, 8, 128, 16384, [(16383, 4096), (16383, 1), (4095, 4096), (4096, 4096), (9000, 31), (511, 64)]),
     (16, 2, 64, 3000, [(2999, 65), (2999, 3000), (100, 7)]),   # split kernel, gs = 8
     (6, 2, 80, 513, [(512, 100), (5, 3), (300, 1)]),           # generic kernel (D = 80)
+    (64, 8, 128, 2048, [(2047, 300), (1000, 1)]),              # split kernel, two head groups per kv head
 ])
 def test_decode_window(cuda_lib, orc, H, G, D, max_seq, cases):
     q, kc, vc = synthetic.decode_inputs(max_seq, H, G, D, seed=max_seq + 1)
