@@ -11,4 +11,4 @@ from ._binding import (ATTN_BF16, ATTN_CAUSAL, ATTN_CROSS, ATTN_ERR_CUDA, ATTN_E
                        attn_decode_cached_window, attn_decode_paged, attn_decode_workspace_bytes, attn_forward, attn_forward_rope, attn_forward_window,
                        attn_get_status, attn_prefill, attn_prefill_paged, attn_prefill_window, attn_rope_table, attn_selftest_wait_timeout,
                        attn_status_string, load_library)
-from .api import backward, decode, forward, prefill, DecodeState  # noqa: F401
+from .api import backward, decode, forward, prefill, rope_table, DecodeState  # noqa: F401

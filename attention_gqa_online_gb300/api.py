@@ -6,15 +6,26 @@ import torch
 from . import _binding as B
 
 
+def rope_table(max_pos, head_dim, base=10000.0, device="cuda", stream=None):
+    """[max_pos, head_dim] RoPE table (cos of the head_dim/2 pair angles, then their sin)."""
+    t = torch.empty((max_pos, head_dim), device=device, dtype=torch.float32)
+    B.attn_rope_table(t, max_pos, head_dim, base, stream)
+    return t
+
+
 def forward(q, k, v, num_heads, num_kv_heads, mask=B.ATTN_CAUSAL, prec=B.ATTN_FP32, want_lse=True,
-            stream=None, window=0):
+            stream=None, window=0, rope=None):
     """q [q_seq, H*D], k/v [kv_seq, G*D] (CUDA fp32) -> (out [q_seq, H*D], lse [q_seq, H, 2] or None).
-    window > 0 keeps each row's last `window` keys."""
+    window > 0 keeps each row's last `window` keys; rope (a table from rope_table) turns q and k
+    by their row positions first."""
     q_seq, kv_seq = q.shape[0], k.shape[0]
     D = q.shape[1] // num_heads
     out = torch.empty_like(q)
     lse = torch.empty((q_seq, num_heads, 2), device=q.device, dtype=torch.float32) if want_lse else None
-    if window:
+    if rope is not None:
+        B.attn_forward_rope(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads, D, mask, prec, window, rope,
+                            None, stream)
+    elif window:
         B.attn_forward_window(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads, D, mask, prec, window,
                               stream)
     else:
