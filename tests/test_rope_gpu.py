@@ -89,3 +89,17 @@ def test_rope_rejects(cuda_lib):
     with pytest.raises(cuda_lib.AttnError) as e:  # table one row short
         cuda_lib.attn_forward_rope(dev(q), dev(k), dev(v), out, None, 8, 8, 2, 1, 64, CAUSAL, FP32, 0, tab)
     assert e.value.code == cuda_lib.ATTN_ERR_INVALID_ARG
+
+
+def test_python_helpers_match_the_entry_point(cuda_lib, orc):
+    """forward(..., rope=rope_table(...)) is attn_forward_rope (same bits)."""
+    q, k, v = synthetic.forward_inputs(100, 100, 4, 2, 64, seed=12)
+    tab = cuda_lib.rope_table(100, 64)
+    out, lse = cuda_lib.forward(dev(q), dev(k), dev(v), 4, 2, mask=CAUSAL, prec=FP32, rope=tab)
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    cuda_lib.attn_forward_rope(dev(q), dev(k), dev(v), out2, lse2, 100, 100, 4, 2, 64, CAUSAL, FP32, 0, tab)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    ro, _ = orc.forward_rope(q.numpy(), k.numpy(), v.numpy(), 100, 100, 4, 2, 64, CAUSAL, 10000.0)
+    assert_out_close(out.cpu().numpy(), ro, FP32, float(v.abs().max()), "rope helper")
