@@ -413,13 +413,10 @@ int launch_d(const BwdArgs& a, float* delta, float* l2, cudaStream_t s) {
   void* args[] = {&aa, &d, &l};
   const long long kb = (a.n_kv + BN - 1) / BN;
   const long long qb = ((long long)a.n_q * gs + BM - 1) / BM;
-  if (kb > 0 && launch_pdl(reinterpret_cast<const void*>(kv_kern), dim3((unsigned)kb, (unsigned)a.G), dim3(NT),
-                           kv_smem, s, args) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  if (launch_pdl(reinterpret_cast<const void*>(q_kern), dim3((unsigned)qb, (unsigned)a.G), dim3(NT), q_smem, s,
-                 args) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  return ATTN_OK;
+  // dK/dV and dQ are independent: they run concurrently (dQ on a side stream).
+  return launch_forked(s, reinterpret_cast<const void*>(kv_kern), dim3((unsigned)kb, (unsigned)a.G), kv_smem,
+                       reinterpret_cast<const void*>(q_kern), dim3((unsigned)qb, (unsigned)a.G), q_smem, dim3(NT),
+                       args);
 }
 
 }  // namespace

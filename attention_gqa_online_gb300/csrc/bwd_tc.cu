@@ -536,12 +536,12 @@ int launch_d(const BwdArgs& a, const float* delta, const float* l2, const uint16
   void* args[] = {&aa, &d, &l, &tm_k, &tm_v, &tm_q, &tm_g};
   const long long kb = (a.n_kv + kR - 1) / kR;
   const long long qb = ((long long)a.n_q * gs + kR - 1) / kR;
-  if (launch_pdl(reinterpret_cast<const void*>(kv_kern), dim3((unsigned)kb, (unsigned)a.G), dim3(kThreads), kv_smem, s,
-                 args) != cudaSuccess ||
-      launch_pdl(reinterpret_cast<const void*>(q_kern), dim3((unsigned)qb, (unsigned)a.G), dim3(kThreads), q_smem, s,
-                 args) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  return ATTN_OK;
+  // The two kernels are independent: dQ runs on a side stream forked after
+  // the pre-passes and joined before the caller's stream moves on, so its
+  // CTAs fill the SMs that the dK/dV grid's uneven causal tail leaves idle.
+  return launch_forked(s, reinterpret_cast<const void*>(kv_kern), dim3((unsigned)kb, (unsigned)a.G), kv_smem,
+                       reinterpret_cast<const void*>(q_kern), dim3((unsigned)qb, (unsigned)a.G), q_smem,
+                       dim3(kThreads), args);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

@@ -73,6 +73,15 @@ __host__ __device__ inline int first_key(int n, int window) { return (window > 0
 // for that kernel before touching global memory).
 cudaError_t launch_pdl(const void* kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args);
 
+// A non-blocking stream per device, created once, for work the library runs
+// beside the caller's stream.
+cudaStream_t side_stream();
+// Runs two independent kernels with the same arguments concurrently: k1 on
+// `s`, k2 on the side stream forked from `s` and joined back into it, so
+// that work queued on `s` afterwards follows both.  Returns an ATTN_ status.
+int launch_forked(cudaStream_t s, const void* k1, dim3 g1, size_t smem1, const void* k2, dim3 g2, size_t smem2,
+                  dim3 block, void** args);
+
 // Raises a kernel's dynamic shared memory limit to `bytes` on the current
 // device; the attribute is set once per (kernel, device).
 bool set_smem_limit(const void* kernel, size_t bytes);

@@ -104,6 +104,36 @@ cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s) {
 
 cudaError_t scratch_free(void* p, cudaStream_t s) { return cudaFreeAsync(p, s); }
 
+cudaStream_t side_stream() {
+  static cudaStream_t streams[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (streams[dev] == nullptr && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+    streams[dev] = nullptr;
+  return streams[dev];
+}
+
+int launch_forked(cudaStream_t s, const void* k1, dim3 g1, size_t smem1, const void* k2, dim3 g2, size_t smem2,
+                  dim3 block, void** args) {
+  cudaStream_t side = side_stream();
+  cudaEvent_t fork = nullptr, join = nullptr;
+  if (side == nullptr || cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+    if (fork != nullptr) cudaEventDestroy(fork);
+    return ATTN_ERR_CUDA;
+  }
+  int rc = ATTN_OK;
+  if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess ||
+      launch_pdl(k2, g2, block, smem2, side, args) != cudaSuccess || launch_pdl(k1, g1, block, smem1, s, args) != cudaSuccess ||
+      cudaEventRecord(join, side) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
+    rc = ATTN_ERR_CUDA;
+  cudaEventDestroy(fork);  // released once the recorded work has completed
+  cudaEventDestroy(join);
+  return rc;
+}
+
 bool set_smem_limit(const void* kernel, size_t bytes) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
