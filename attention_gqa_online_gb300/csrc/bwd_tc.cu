@@ -56,7 +56,7 @@ struct __align__(1024) KvTcSmem {
   unsigned char q[2][Tile<D>::kBytes];
   unsigned char g[2][Tile<D>::kBytes];  // dout
   RowInfo rows[2][kR];
-  uint64_t kv_full, q_full[2], q_empty[2], s_full, p_ready, pv_done, drain;
+  uint64_t kv_full, q_full[2], q_empty[2], s_full, p_ready[2], pv_done, drain;  // p_ready: rows 0-63, 64-127
   uint32_t tmem_base;
   int abort;
 };
@@ -67,7 +67,7 @@ struct __align__(1024) QTcSmem {
   unsigned char g[Tile<D>::kBytes];
   unsigned char k[2][Tile<D>::kBytes];
   unsigned char v[2][Tile<D>::kBytes];
-  uint64_t q_full, kv_full[2], kv_empty[2], s_full, p_ready, pv_done, drain;
+  uint64_t q_full, kv_full[2], kv_empty[2], s_full, p_ready[2], pv_done, drain;  // p_ready: keys 0-63, 64-127
   uint32_t tmem_base;
   int abort;
 };
@@ -79,10 +79,17 @@ __device__ __forceinline__ int query_n(const BwdArgs& a, long long i) {
 // The elementwise step for one thread's TMEM lane: 128 columns of S and dP
 // (at kColS / kColP) become bf16 P (over S, if write_p) and dS (over dP).
 // info(c) gives the column's l2, delta and whether it is inside the window.
-template <typename InfoFn>
-__device__ __forceinline__ void elementwise(uint32_t lane_tmem, float sl2, bool write_p, InfoFn info) {
+// half_done() runs once the first 64 columns are written (the products that
+// read them may start while the other 64 are worked on).
+template <typename InfoFn, typename HalfFn>
+__device__ __forceinline__ void elementwise(uint32_t lane_tmem, float sl2, bool write_p, InfoFn info,
+                                            HalfFn half_done) {
 #pragma unroll 1
   for (int cc = 0; cc < kR / 32; ++cc) {
+    if (cc == 2) {
+      tc::tmem_st_wait();
+      half_done();
+    }
     uint32_t s[32], dp[32];
     tc::tmem_ld32(lane_tmem + kColS + 32 * cc, s);
     tc::tmem_ld32(lane_tmem + kColP + 32 * cc, dp);
@@ -164,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.q_empty[b], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_ready, 4);
+    mbar_init(&sm.p_ready[0], 4);
+    mbar_init(&sm.p_ready[1], 4);
     mbar_init(&sm.pv_done, 1);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
@@ -257,14 +265,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                           dg + c + 6, idesc_ss, c4 > 0 ? 1u : 0u);
         }
         tc::commit_elect(&sm.s_full);
-        ok = wait(&sm.p_ready, j);
-        if (!ok) break;
-        tc::fence_after_sync();
         // dV += P^T dout and dK += dS^T Q (M = 128 keys, N = D, K = 128 rows;
-        // A bf16 in TMEM, 8 columns per 16-row step; B MN-major).
+        // A bf16 in TMEM, 8 columns per 16-row step; B MN-major), in two
+        // halves of 64 rows, each as soon as its P and dS are written.
         const uint64_t gm = tc::sdesc_sw128(ga, kChunkBytes, 1024), qm = tc::sdesc_sw128(qa, kChunkBytes, 1024);
-#pragma unroll
+#pragma unroll 1
         for (int c4 = 0; c4 < kR / 64; ++c4) {
+          ok = wait(&sm.p_ready[c4], j);
+          if (!ok) break;
+          tc::fence_after_sync();
           const uint64_t c = 4 * st * c4;
           const uint32_t pa = tmem + kColS + 32 * c4, sa = tmem + kColP + 32 * c4;
           const uint32_t acc = (j > 0 || c4 > 0) ? 1u : 0u;
@@ -273,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma4_f16_ts(tmem + kColAcc + D, sa, sa + 8, sa + 16, sa + 24, qm + c, qm + c + st, qm + c + 2 * st,
                           qm + c + 3 * st, idesc_ts, acc);
         }
+        if (!ok) break;
         tc::commit_elect(&sm.pv_done);
         tc::commit_elect(&sm.q_empty[b]);
       }
@@ -290,15 +300,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = j & 1;
       mbar_wait_bounded(&sm.s_full, (unsigned)(j & 1), a.status, &sm.abort);
       tc::fence_after_sync();
-      elementwise(lane_tmem, sl2, true, [&](int c, float* lv, float* dv) {
-        const RowInfo ri = sm.rows[b][c];
-        *lv = ri.l2;
-        *dv = ri.delta;
-        return key >= ri.lo && key < ri.n;
-      });
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_ready);
+      auto ready = [&](int half) {
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_ready[half]);
+      };
+      elementwise(
+          lane_tmem, sl2, true,
+          [&](int c, float* lv, float* dv) {
+            const RowInfo ri = sm.rows[b][c];
+            *lv = ri.l2;
+            *dv = ri.delta;
+            return key >= ri.lo && key < ri.n;
+          },
+          [&] { ready(0); });
+      ready(1);
     }
     if (nqb > 0) mbar_wait_bounded(&sm.pv_done, (unsigned)((nqb - 1) & 1), a.status, &sm.abort);
     tc::fence_after_sync();
@@ -352,7 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.kv_empty[b], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_ready, 4);
+    mbar_init(&sm.p_ready[0], 4);
+    mbar_init(&sm.p_ready[1], 4);
     mbar_init(&sm.pv_done, 1);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
@@ -420,18 +437,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                           dv + c + 6, idesc_ss, c4 > 0 ? 1u : 0u);
         }
         tc::commit_elect(&sm.s_full);
-        ok = wait(&sm.p_ready, t);
-        if (!ok) break;
-        tc::fence_after_sync();
-        // dQ += dS K (M = 128 rows, N = D, K = 128 keys; B = K tile MN-major).
+        // dQ += dS K (M = 128 rows, N = D, K = 128 keys; B = K tile MN-major),
+        // in two halves of 64 keys, each as soon as its dS is written.
         const uint64_t km = tc::sdesc_sw128(ka, kChunkBytes, 1024);
-#pragma unroll
+#pragma unroll 1
         for (int c4 = 0; c4 < kR / 64; ++c4) {
+          ok = wait(&sm.p_ready[c4], t);
+          if (!ok) break;
+          tc::fence_after_sync();
           const uint64_t c = 4 * st * c4;
           const uint32_t sa = tmem + kColP + 32 * c4;
           tc::mma4_f16_ts(tmem + kColAcc, sa, sa + 8, sa + 16, sa + 24, km + c, km + c + st, km + c + 2 * st,
                           km + c + 3 * st, idesc_ts, (t > 0 || c4 > 0) ? 1u : 0u);
         }
+        if (!ok) break;
         tc::commit_elect(&sm.pv_done);
         tc::commit_elect(&sm.kv_empty[b]);
       }
@@ -454,14 +473,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_bounded(&sm.s_full, (unsigned)(t & 1), a.status, &sm.abort);
       tc::fence_after_sync();
       const int key0 = (jt0 + t) * kR;
-      elementwise(lane_tmem, sl2, false, [&](int c, float* lv, float* dv) {
-        *lv = lr;
-        *dv = dr;
-        return key0 + c >= lo_r && key0 + c < n_r;
-      });
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_ready);
+      auto ready = [&](int half) {
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_ready[half]);
+      };
+      elementwise(
+          lane_tmem, sl2, false,
+          [&](int c, float* lv, float* dv) {
+            *lv = lr;
+            *dv = dr;
+            return key0 + c >= lo_r && key0 + c < n_r;
+          },
+          [&] { ready(0); });
+      ready(1);
     }
     if (nt > 0) mbar_wait_bounded(&sm.pv_done, (unsigned)((nt - 1) & 1), a.status, &sm.abort);
     tc::fence_after_sync();
