@@ -44,6 +44,9 @@ def load(lib_path=None):
         [ctypes.c_void_p, _c_int, _c_int, ctypes.c_double]
     lib.oracle_backward.restype = _c_int
     lib.oracle_backward.argtypes = [_f32p, _f32p, _f32p, _f32p, _f64p, _f64p, _f64p] + [_c_int] * 7
+    lib.oracle_backward_rope.restype = _c_int
+    lib.oracle_backward_rope.argtypes = [_f32p, _f32p, _f32p, _f32p, _f64p, _f64p, _f64p] + [_c_int] * 7 + \
+        [ctypes.c_double]
     lib.oracle_num_threads.restype = _c_int
     lib.oracle_num_threads.argtypes = []
     return lib
@@ -103,6 +106,19 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_decode rejected its arguments")
         return out
+
+    def backward_rope(self, q, k, v, dout, q_seq, kv_seq, H, G, D, mask, rope_base, window=0):
+        """backward() of forward_rope(): returns (dq, dk, dv) with respect to the unturned q, k."""
+        q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v, dout))
+        dq = np.full((max(q_seq, 0), H * D), np.nan)
+        dk = np.full((max(kv_seq, 0), G * D), np.nan)
+        dv = np.full((max(kv_seq, 0), G * D), np.nan)
+        rc = self.lib.oracle_backward_rope(q.reshape(-1), k.reshape(-1), v.reshape(-1), dout.reshape(-1),
+                                           dq.reshape(-1), dk.reshape(-1), dv.reshape(-1), q_seq, kv_seq, H, G, D,
+                                           mask, int(window), float(rope_base))
+        if rc != 0:
+            raise ValueError("oracle_backward_rope rejected its arguments")
+        return dq, dk, dv
 
     # Paged KV cache.  The pages name paged KV only as future work for caches
     # that overflow one buffer; the layout read here: the cache is cut into

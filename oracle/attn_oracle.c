@@ -452,3 +452,102 @@ int oracle_forward_rope(const float *q, const float *k, const float *v,
     free(kr);
     return err;
 }
+
+/*
+ * Backward of the RoPE forward (oracle_forward_rope).  With q' and k' the
+ * turned rows (rotations are orthogonal), the gradient is the plain one of
+ * the forward at (q', k', v), turned back: dq = R_q^T dq', dk = R_k^T dk',
+ * dv unchanged.  The steps below are those of oracle_backward on fp64 rows.
+ */
+static void rope_unrotate(double *x, int D, size_t pos, double base)
+{
+    const int half = D / 2;
+    for (int d = 0; d < half; ++d) {
+        const double a = (double)pos * pow(base, -2.0 * (double)d / (double)D);
+        const double c = cos(a), s = sin(a);
+        const double x0 = x[d], x1 = x[d + half];
+        x[d] = x0 * c + x1 * s;
+        x[d + half] = x1 * c - x0 * s;
+    }
+}
+
+int oracle_backward_rope(const float *q, const float *k, const float *v, const float *dout,
+                         double *dq, double *dk, double *dv, int q_seq, int kv_seq,
+                         int H, int G, int D, int mask, int window, double rope_base)
+{
+    if (bad_heads(H, G, D) || (D % 2) != 0 || q_seq < 0 || kv_seq < 0 || mask < 0 || mask > 2 || window < 0 ||
+        !(rope_base > 1.0))
+        return -1;
+    if (mask != 2 && kv_seq != q_seq) return -1;
+    const int gs = H / G;
+    const size_t kv_dim = (size_t)G * D;
+    const double scale = 1.0 / sqrt((double)D);
+    double *qr = (double *)malloc(sizeof(double) * ((size_t)q_seq * H * D + 1));
+    double *kr = (double *)malloc(sizeof(double) * ((size_t)kv_seq * kv_dim + 1));
+    double *p = (double *)malloc(sizeof(double) * (size_t)(kv_seq > 0 ? kv_seq : 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(kv_seq > 0 ? kv_seq : 1));
+    if (qr == NULL || kr == NULL || p == NULL || dp == NULL) {
+        free(qr); free(kr); free(p); free(dp);
+        return -1;
+    }
+    for (size_t i = 0; i < (size_t)q_seq; ++i)
+        for (int h = 0; h < H; ++h) rope_rotate(q + (i * H + h) * D, qr + (i * H + h) * D, D, i, rope_base);
+    for (size_t t = 0; t < (size_t)kv_seq; ++t)
+        for (int g = 0; g < G; ++g) rope_rotate(k + t * kv_dim + (size_t)g * D, kr + t * kv_dim + (size_t)g * D, D, t,
+                                               rope_base);
+    for (size_t i = 0; i < (size_t)q_seq * H * D; ++i) dq[i] = 0.0;
+    for (size_t i = 0; i < (size_t)kv_seq * kv_dim; ++i) dk[i] = dv[i] = 0.0;
+    for (int g = 0; g < G; ++g) {
+        for (int hh = 0; hh < gs; ++hh) {
+            const int h = g * gs + hh;
+            for (int pos = 0; pos < q_seq; ++pos) {
+                const size_t n = (mask == 0) ? (size_t)pos + 1 : (size_t)kv_seq;
+                const size_t lo = window_start(n, window);
+                if (n == lo) continue;
+                const double *qrow = qr + (size_t)pos * H * D + (size_t)h * D;
+                const float *dor = dout + (size_t)pos * H * D + (size_t)h * D;
+                double *dqr = dq + (size_t)pos * H * D + (size_t)h * D;
+                double m = -INFINITY;
+                for (size_t t = lo; t < n; ++t) {
+                    const double *kt = kr + t * kv_dim + (size_t)g * D;
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += qrow[d] * kt[d];
+                    p[t] = dot * scale;
+                    if (p[t] > m) m = p[t];
+                }
+                double l = 0.0;
+                for (size_t t = lo; t < n; ++t) {
+                    p[t] = exp(p[t] - m);
+                    l += p[t];
+                }
+                for (size_t t = lo; t < n; ++t) p[t] /= l;
+                double mean = 0.0;
+                for (size_t t = lo; t < n; ++t) {
+                    const float *vt = v + t * kv_dim + (size_t)g * D;
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += (double)dor[d] * (double)vt[d];
+                    dp[t] = dot;
+                    mean += p[t] * dot;
+                }
+                for (size_t t = lo; t < n; ++t) {
+                    const double ds = p[t] * (dp[t] - mean);
+                    const double *kt = kr + t * kv_dim + (size_t)g * D;
+                    double *dkt = dk + t * kv_dim + (size_t)g * D;
+                    double *dvt = dv + t * kv_dim + (size_t)g * D;
+                    for (int d = 0; d < D; ++d) {
+                        dqr[d] += scale * ds * kt[d];
+                        dkt[d] += scale * ds * qrow[d];
+                        dvt[d] += p[t] * (double)dor[d];
+                    }
+                }
+            }
+        }
+    }
+    /* back from the turned frame */
+    for (size_t i = 0; i < (size_t)q_seq; ++i)
+        for (int h = 0; h < H; ++h) rope_unrotate(dq + (i * H + h) * D, D, i, rope_base);
+    for (size_t t = 0; t < (size_t)kv_seq; ++t)
+        for (int g = 0; g < G; ++g) rope_unrotate(dk + t * kv_dim + (size_t)g * D, D, t, rope_base);
+    free(qr); free(kr); free(p); free(dp);
+    return 0;
+}

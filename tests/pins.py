@@ -636,4 +636,38 @@ def pin_rope_gqa_equals_replicated_mha(orc):
     assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
 
 
+
+def pin_rope_backward_autograd(orc):
+    """The RoPE backward against autograd through the complex-pair rotation and
+    fp64 SDPA (causal, cross with a window)."""
+    for mask, q_seq, kv_seq, w in ((CAUSAL, 10, 10, 0), (CROSS, 6, 11, 4)):
+        H, G, D = 4, 2, 8
+        q, k, v, do = _grad_inputs(110 + mask, q_seq, kv_seq, H, G, D)
+        got = orc.backward_rope(q, k, v, do, q_seq, kv_seq, H, G, D, mask, 500.0, window=w)
+
+        def turned(x, heads):
+            rows = x.shape[0]
+            xt = x.reshape(rows, heads, D)
+            z = torch.complex(xt[..., :D // 2], xt[..., D // 2:])
+            ang = torch.arange(rows, dtype=torch.float64)[:, None] * torch.pow(
+                torch.tensor(500.0, dtype=torch.float64), -2.0 * torch.arange(D // 2, dtype=torch.float64) / D)
+            z = z * torch.polar(torch.ones_like(ang), ang)[:, None, :]
+            return torch.cat([z.real, z.imag], dim=-1).reshape(rows, heads * D)
+
+        qt = torch.from_numpy(q.astype(np.float64)).requires_grad_()
+        kt = torch.from_numpy(k.astype(np.float64)).requires_grad_()
+        vt = torch.from_numpy(v.astype(np.float64)).requires_grad_()
+        allow = np.zeros((q_seq, kv_seq), dtype=bool)
+        for i in range(q_seq):
+            n = i + 1 if mask == CAUSAL else kv_seq
+            allow[i, (max(0, n - w) if w else 0):n] = True
+        qs = turned(qt, H).reshape(q_seq, H, D).transpose(0, 1)[None]
+        ks = turned(kt, G).reshape(kv_seq, G, D).transpose(0, 1)[None]
+        vs = vt.reshape(kv_seq, G, D).transpose(0, 1)[None]
+        o = F.scaled_dot_product_attention(qs, ks, vs, attn_mask=torch.from_numpy(allow), enable_gqa=True)
+        o.backward(torch.from_numpy(do.astype(np.float64)).reshape(q_seq, H, D).transpose(0, 1)[None])
+        for a, b in zip(got, (qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy())):
+            assert np.max(np.abs(a - b)) < 1e-12
+
+
 ALL_PINS = [obj for name, obj in sorted(globals().items()) if name.startswith("pin_")]

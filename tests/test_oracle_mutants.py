@@ -79,6 +79,7 @@ MUTANTS = [
      "D, t + 1,\n                                               rope_base);", False),
     ("rope_query_unrotated", "rope_rotate(q + qo, qr, D, (size_t)pos, rope_base);",
      "rope_rotate(q + qo, qr, D, 0, rope_base);", False),
+    ("rope_bwd_not_turned_back", "x[d] = x0 * c + x1 * s;", "x[d] = x0 * c - x1 * s;", False),
     ("bwd_head_map_interleaved", "const int h = g * gs + hh;", "const int h = hh * G + g;", False),
 ]
 
