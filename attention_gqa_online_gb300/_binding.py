@@ -68,6 +68,8 @@ def load_library(path=None):
     lib.attn_forward_rope.argtypes = [_vp] * 5 + [_u32] * 5 + [ctypes.c_int, ctypes.c_int, _u32, _vp, _u32, _vp]
     lib.attn_backward.restype = ctypes.c_int
     lib.attn_backward.argtypes = [_vp] * 9 + [_u32] * 5 + [ctypes.c_int, ctypes.c_int, _u32, _vp]
+    lib.attn_backward_rope.restype = ctypes.c_int
+    lib.attn_backward_rope.argtypes = [_vp] * 9 + [_u32] * 5 + [ctypes.c_int, ctypes.c_int, _u32, _vp, _u32, _vp]
     lib.attn_get_status.restype = ctypes.c_int
     lib.attn_get_status.argtypes = [_vp]
     lib.attn_status_string.restype = ctypes.c_char_p
@@ -156,6 +158,19 @@ def attn_forward_rope(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads,
         _addr(q, "q", f), _addr(k, "k", f), _addr(v, "v", f), _addr(out, "out", f), _addr(lse, "lse", f),
         q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask, prec, window, _addr(rope_table, "rope_table", f),
         table_rows, _stream(stream)), "attn_forward_rope")
+
+
+def attn_backward_rope(q, k, v, out, dout, lse, dq, dk, dv, q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask,
+                       prec, window, rope_table, table_rows=None, stream=None):
+    """Backward of attn_forward_rope (gradients for the unturned q, k); see attn_gqa.h."""
+    f = _f32()
+    if table_rows is None:
+        table_rows = rope_table.shape[0]
+    _check(load_library().attn_backward_rope(
+        _addr(q, "q", f), _addr(k, "k", f), _addr(v, "v", f), _addr(out, "out", f), _addr(dout, "dout", f),
+        _addr(lse, "lse", f), _addr(dq, "dq", f), _addr(dk, "dk", f), _addr(dv, "dv", f), q_seq, kv_seq,
+        num_heads, num_kv_heads, head_dim, mask, prec, window, _addr(rope_table, "rope_table", f), table_rows,
+        _stream(stream)), "attn_backward_rope")
 
 
 def attn_decode_workspace_bytes(num_heads, num_kv_heads, head_dim, max_seq):

@@ -456,14 +456,18 @@ extern "C" int attn_prefill_paged(const float* q_batch, const float* k_pages, co
   return run_flash(a, prec, reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" int attn_backward(const float* q, const float* k, const float* v, const float* out, const float* dout,
-                             const float* lse, float* dq, float* dk, float* dv, uint32_t q_seq, uint32_t kv_seq,
-                             uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,
-                             uint32_t window, attn_stream_t stream) {
+// The backward behind attn_backward and attn_backward_rope; rope_table (or
+// nullptr) turns q and k first and the gradients back afterwards.
+static int backward_impl(const float* q, const float* k, const float* v, const float* out, const float* dout,
+                         const float* lse, float* dq, float* dk, float* dv, uint32_t q_seq, uint32_t kv_seq,
+                         uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,
+                         uint32_t window, const float* rope_table, uint32_t table_rows, attn_stream_t stream) {
   if (!heads_ok(num_heads, num_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
   if (mask != ATTN_CAUSAL && mask != ATTN_FULL && mask != ATTN_CROSS) return ATTN_ERR_INVALID_ARG;
   if (mask != ATTN_CROSS && kv_seq != q_seq) return ATTN_ERR_INVALID_ARG;
   if (q_seq > 0x7fffffffu || kv_seq > 0x7fffffffu) return ATTN_ERR_INVALID_ARG;
+  const bool rope = rope_table != nullptr;
+  if (rope && (head_dim % 2 != 0 || table_rows < q_seq || table_rows < kv_seq)) return ATTN_ERR_INVALID_ARG;
   if (q_seq == 0) return ATTN_OK;
   if (q == nullptr || dout == nullptr || dq == nullptr || out == nullptr || lse == nullptr) return ATTN_ERR_INVALID_ARG;
   if (kv_seq > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr)) return ATTN_ERR_INVALID_ARG;
@@ -471,8 +475,9 @@ extern "C" int attn_backward(const float* q, const float* k, const float* v, con
   const uintptr_t al = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
                        reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
-                       reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv);
-  if (head_dim % 4 != 0 || al % 16 != 0) return ATTN_ERR_UNSUPPORTED;
+                       reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv) |
+                       reinterpret_cast<uintptr_t>(rope_table);
+  if (head_dim % 4 != 0 || al % 16 != 0 || (rope && head_dim % 8 != 0)) return ATTN_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kv_seq == 0)  // no keys: out was all zeros and every gradient is zero
     return cudaMemsetAsync(dq, 0, (size_t)q_seq * num_heads * head_dim * sizeof(float), s) == cudaSuccess
@@ -498,8 +503,48 @@ extern "C" int attn_backward(const float* q, const float* k, const float* v, con
   a.scale = 1.0f / sqrtf((float)head_dim);
   a.status = status_ptr();
   if (a.status == nullptr) return ATTN_ERR_CUDA;
-  if (prec == ATTN_BF16) return backward_bf16_supported(a) ? launch_backward_bf16(a, s) : ATTN_ERR_UNSUPPORTED;
-  return launch_backward_simt(a, s);
+  if (prec == ATTN_BF16 && !backward_bf16_supported(a)) return ATTN_ERR_UNSUPPORTED;
+  // RoPE: the gradient of the plain attention at the turned q and k, turned
+  // back (the rotations are orthogonal); q and k are turned into scratch.
+  void* scratch = nullptr;
+  const size_t qe = (size_t)q_seq * num_heads * head_dim, ke = (size_t)kv_seq * num_kv_heads * head_dim;
+  if (rope) {
+    if (scratch_alloc(&scratch, (qe + ke) * sizeof(float), s) != cudaSuccess) return ATTN_ERR_CUDA;
+    float* qt = static_cast<float*>(scratch);
+    float* kt = qt + qe;  // qe is a multiple of 8 floats: 32-byte aligned
+    if (launch_rope_k(q, qt, rope_table, q_seq, a.H, a.D, s) != cudaSuccess ||
+        launch_rope_k(k, kt, rope_table, kv_seq, a.G, a.D, s) != cudaSuccess) {
+      scratch_free(scratch, s);
+      return ATTN_ERR_CUDA;
+    }
+    a.q = qt;
+    a.k = kt;
+  }
+  int rc = prec == ATTN_BF16 ? launch_backward_bf16(a, s) : launch_backward_simt(a, s);
+  if (rope && rc == ATTN_OK &&
+      (launch_rope_k(dq, dq, rope_table, q_seq, a.H, a.D, s, -1.f) != cudaSuccess ||
+       launch_rope_k(dk, dk, rope_table, kv_seq, a.G, a.D, s, -1.f) != cudaSuccess))
+    rc = ATTN_ERR_CUDA;
+  if (scratch != nullptr && scratch_free(scratch, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+  return rc;
+}
+
+extern "C" int attn_backward(const float* q, const float* k, const float* v, const float* out, const float* dout,
+                             const float* lse, float* dq, float* dk, float* dv, uint32_t q_seq, uint32_t kv_seq,
+                             uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,
+                             uint32_t window, attn_stream_t stream) {
+  return backward_impl(q, k, v, out, dout, lse, dq, dk, dv, q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask,
+                       prec, window, nullptr, 0, stream);
+}
+
+extern "C" int attn_backward_rope(const float* q, const float* k, const float* v, const float* out, const float* dout,
+                                  const float* lse, float* dq, float* dk, float* dv, uint32_t q_seq, uint32_t kv_seq,
+                                  uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,
+                                  uint32_t window, const float* rope_table, uint32_t table_rows,
+                                  attn_stream_t stream) {
+  if (rope_table == nullptr) return ATTN_ERR_INVALID_ARG;
+  return backward_impl(q, k, v, out, dout, lse, dq, dk, dv, q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask,
+                       prec, window, rope_table, table_rows, stream);
 }
 
 extern "C" int attn_get_status(attn_stream_t stream) {

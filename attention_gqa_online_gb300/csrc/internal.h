@@ -137,11 +137,13 @@ bool backward_bf16_supported(const BwdArgs& a);
 int launch_backward_bf16(const BwdArgs& a, cudaStream_t s);
 
 // RoPE helpers (rope.cu): fill table[max_pos][D] (cos of the D/2 pairs, then
-// their sin; angles p * base^(-2d/D) in fp64), and write K ([rows][G*D],
-// row t at position t) turned by the table into out.  D % 8 == 0 for
-// launch_rope_k; 16-byte-aligned pointers.
+// their sin; angles p * base^(-2d/D) in fp64), and write x ([rows][G*D], G
+// heads, row t at position t) turned by the table (sgn = 1) or turned back
+// (sgn = -1) into out (which may be x).  D % 8 == 0 for launch_rope_k;
+// 16-byte-aligned pointers.
 int launch_rope_table(float* table, int max_pos, int D, double base, cudaStream_t s);
-cudaError_t launch_rope_k(const float* k, float* out, const float* table, long long rows, int G, int D, cudaStream_t s);
+cudaError_t launch_rope_k(const float* k, float* out, const float* table, long long rows, int G, int D, cudaStream_t s,
+                          float sgn = 1.f);
 
 // Split-KV decode.
 struct DecodeArgs {

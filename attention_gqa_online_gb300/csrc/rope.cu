@@ -27,10 +27,11 @@ __global__ void __launch_bounds__(256) rope_table_kernel(float* table, int max_p
   table[(long long)p * D + half + d] = (float)s;
 }
 
-// Rows [0, rows) of K ([rows][G*D]): each thread turns one float4 pair
-// (4 dims d..d+3 and d+D/2..d+D/2+3) of one kv head of one row.
-__global__ void __launch_bounds__(256) rope_k_kernel(const float* __restrict__ k, float* __restrict__ out,
-                                                     const float* __restrict__ table, long long rows, int G, int D) {
+// Rows [0, rows) of x ([rows][G*D], G heads): each thread turns one float4
+// pair (4 dims d..d+3 and d+D/2..d+D/2+3) of one head of one row, by the
+// angle (sgn = 1) or back (sgn = -1).  out may be x itself.
+__global__ void __launch_bounds__(256) rope_k_kernel(const float* k, float* out, const float* __restrict__ table,
+                                                     long long rows, int G, int D, float sgn) {
   allow_dependent_launch();
   grid_dependency_wait();
   const int half4 = D / 8;  // float4 groups per half row of one head
@@ -43,7 +44,8 @@ __global__ void __launch_bounds__(256) rope_k_kernel(const float* __restrict__ k
   const float4 lo = *reinterpret_cast<const float4*>(k + base + d);
   const float4 hi = *reinterpret_cast<const float4*>(k + base + D / 2 + d);
   const float4 c = *reinterpret_cast<const float4*>(table + t * D + d);
-  const float4 s = *reinterpret_cast<const float4*>(table + t * D + D / 2 + d);
+  float4 s = *reinterpret_cast<const float4*>(table + t * D + D / 2 + d);
+  s = make_float4(sgn * s.x, sgn * s.y, sgn * s.z, sgn * s.w);
   *reinterpret_cast<float4*>(out + base + d) =
       make_float4(lo.x * c.x - hi.x * s.x, lo.y * c.y - hi.y * s.y, lo.z * c.z - hi.z * s.z, lo.w * c.w - hi.w * s.w);
   *reinterpret_cast<float4*>(out + base + D / 2 + d) =
@@ -60,10 +62,10 @@ int launch_rope_table(float* table, int max_pos, int D, double base, cudaStream_
 }
 
 cudaError_t launch_rope_k(const float* k, float* out, const float* table, long long rows, int G, int D,
-                          cudaStream_t s) {
+                          cudaStream_t s, float sgn) {
   const long long n = rows * G * (D / 8);
   if (n == 0) return cudaSuccess;
-  void* args[] = {&k, &out, &table, &rows, &G, &D};
+  void* args[] = {&k, &out, &table, &rows, &G, &D, &sgn};
   return launch_pdl(reinterpret_cast<const void*>(rope_k_kernel), dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
                     args);
 }

@@ -320,6 +320,20 @@ ATTN_API int attn_backward(const float *q, const float *k, const float *v, const
                            uint32_t window, attn_stream_t stream);
 
 /*
+ * Backward of attn_forward_rope: attn_backward's arguments plus the RoPE
+ * table of that forward (rope_table, table_rows as there).  The gradients
+ * are with respect to the unturned q and k: the plain gradient at the turned
+ * q, k (turned into library scratch) is turned back.  out and lse are those
+ * attn_forward_rope wrote.  Errors as attn_backward plus those of
+ * attn_forward_rope's table checks.
+ */
+ATTN_API int attn_backward_rope(const float *q, const float *k, const float *v, const float *out, const float *dout,
+                                const float *lse, float *dq, float *dk, float *dv, uint32_t q_seq, uint32_t kv_seq,
+                                uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,
+                                uint32_t window, const float *rope_table, uint32_t table_rows,
+                                attn_stream_t stream);
+
+/*
  * Cached single-token decode that allocates nothing and takes no workspace.
  * The shader pages have no counterpart to this entry point; it exists for
  * callers that cannot provide device scratch memory -- a plugin inside a

@@ -183,3 +183,11 @@ def test_decode_append_rejects(lib, kw):
     a.update(kw)
     assert lib.attn_decode_append(FAKE, a["kn"], a["vn"], FAKE, FAKE, a["pos"], FAKE, a["H"], a["G"], a["D"],
                                   a["max_seq"], FAKE, 1 << 20, None) == 1
+
+
+def test_backward_rope_rejects(lib):
+    args = [FAKE] * 9 + [8, 8, 2, 1, 64, 0, 0, 0]
+    assert lib.attn_backward_rope(*args, None, 8, None) == 1          # no table
+    assert lib.attn_backward_rope(*args, FAKE, 7, None) == 1          # table one row short
+    odd = [FAKE] * 9 + [8, 8, 2, 1, 63, 0, 0, 0]
+    assert lib.attn_backward_rope(*odd, FAKE, 8, None) == 1           # odd head_dim

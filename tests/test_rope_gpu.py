@@ -103,3 +103,31 @@ def test_python_helpers_match_the_entry_point(cuda_lib, orc):
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
     ro, _ = orc.forward_rope(q.numpy(), k.numpy(), v.numpy(), 100, 100, 4, 2, 64, CAUSAL, 10000.0)
     assert_out_close(out.cpu().numpy(), ro, FP32, float(v.abs().max()), "rope helper")
+
+
+@pytest.mark.parametrize("prec,tol", [(FP32, None), (BF16, 2e-2)])
+@pytest.mark.parametrize("q_seq,kv_seq,H,G,D,mask,window", [
+    (130, 130, 8, 2, 64, CAUSAL, 0),
+    (300, 300, 4, 2, 128, CAUSAL, 77),
+    (45, 131, 8, 8, 64, CROSS, 0),
+])
+def test_rope_backward(cuda_lib, orc, prec, tol, q_seq, kv_seq, H, G, D, mask, window):
+    """attn_backward_rope after attn_forward_rope against the oracle's RoPE backward
+    (fp32: 1e-5 + 1e-4 max|ref| per gradient; bf16 operands: 2e-2 max|ref|)."""
+    q, k, v = synthetic.forward_inputs(q_seq, kv_seq, H, G, D, seed=q_seq + D)
+    do = np.random.default_rng(q_seq).standard_normal((q_seq, H * D)).astype(np.float32)
+    tab = table(cuda_lib, max(q_seq, kv_seq), D, 10000.0)
+    out = torch.empty((q_seq, H * D), device="cuda")
+    lse = torch.empty((q_seq, H, 2), device="cuda")
+    cuda_lib.attn_forward_rope(dev(q), dev(k), dev(v), out, lse, q_seq, kv_seq, H, G, D, mask, FP32, window, tab)
+    grads = [torch.full(x.shape, float("nan"), device="cuda") for x in (q, k, v)]
+    cuda_lib.attn_backward_rope(dev(q), dev(k), dev(v), out, dev(torch.from_numpy(do)), lse, *grads, q_seq, kv_seq,
+                                H, G, D, mask, prec, window, tab)
+    torch.cuda.synchronize()
+    assert cuda_lib.attn_get_status() == 0
+    refs = orc.backward_rope(q.numpy(), k.numpy(), v.numpy(), do, q_seq, kv_seq, H, G, D, mask, 10000.0,
+                             window=window)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, refs):
+        g = g.cpu().numpy()
+        bound = (1e-5 + 1e-4 * np.abs(r).max()) if tol is None else tol * np.abs(r).max()
+        assert np.abs(g - r).max() <= bound, (name, float(np.abs(g - r).max()), bound)
