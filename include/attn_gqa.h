@@ -8,7 +8,10 @@
  *   - meganeura 0.2.0, src/shaders/cached_attention.wgsl  -> attn_decode_cached
  *   - cera, src/backend/shaders/attention_prefill.wgsl    -> attn_prefill
  * Argument lists follow the shaders' parameter lists; shader templating and
- * storage bindings become plain arguments.
+ * storage bindings become plain arguments.  Further entry points fill the
+ * shaders' open hooks and named future work: sliding windows (*_window),
+ * paged caches (*_paged), rotary embedding (*_rope), the backward pass,
+ * and an append-and-decode step; each states its reading below.
  *
  * Common rules for every entry point
  *   Notation   H = num_heads, G = num_kv_heads, D = head_dim, gs = H / G.
@@ -19,10 +22,13 @@
  *              takes scale as an argument (the cera shader's params[5]).
  *   Data       fp32 in, fp32 out, row-major, all pointers are DEVICE memory
  *              owned by the caller.  The library keeps no pointer after a call
- *              returns.  The only device memory it allocates is the ATTN_BF16
- *              path's temporary bf16 copy of K and V: stream-ordered on the
- *              call's stream, from a memory pool the library creates per
- *              device and keeps (freed blocks stay reserved for later calls).
+ *              returns.  The device memory it allocates is temporary scratch
+ *              (the bf16 copies of the ATTN_BF16 paths, K turned for RoPE,
+ *              the backward's per-row values): stream-ordered on the call's
+ *              stream, from a memory pool the library creates per device and
+ *              keeps (freed blocks stay reserved for later calls).  The
+ *              backward also runs one of its kernels on a library-owned
+ *              stream per device, forked from and joined back into `stream`.
  *   Streams    every call is asynchronous on `stream` (a cudaStream_t; NULL is
  *              the legacy default stream).  Results are ready when the stream
  *              has reached the call.
