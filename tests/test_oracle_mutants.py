@@ -14,6 +14,7 @@ import subprocess
 import sys
 import tempfile
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -127,3 +128,42 @@ def mutant_results():
 @pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
 def test_mutant_is_caught(mutant_results, name):
     assert mutant_results[name], "no pin caught the planted mistake " + name
+
+
+# The paged oracle is a numpy gather (oracle/__init__.py), outside the C file:
+# its plausible mistakes are planted by swapping the gather for a wrong one.
+def _gather_identity(pool, table, page_rows):          # table ignored
+    n = len(table) * page_rows
+    return np.ascontiguousarray(np.asarray(pool, np.float32)[:n])
+
+
+def _gather_inverse(pool, table, page_rows):           # table read backwards (pool page -> logical page)
+    pool = np.asarray(pool, np.float32)
+    pages = pool.reshape(-1, page_rows, pool.shape[1])
+    inv = np.argsort(np.asarray(table, np.int64))
+    inv = inv[inv < pages.shape[0]][:len(table)]
+    return np.ascontiguousarray(pages[inv].reshape(-1, pool.shape[1]))
+
+
+def _gather_rows_transposed(pool, table, page_rows):   # rows within a page reversed
+    pool = np.asarray(pool, np.float32)
+    pages = pool.reshape(-1, page_rows, pool.shape[1])
+    return np.ascontiguousarray(pages[np.asarray(table, np.int64)][:, ::-1].reshape(-1, pool.shape[1]))
+
+
+@pytest.mark.parametrize("wrong", [_gather_identity, _gather_inverse, _gather_rows_transposed])
+def test_paged_gather_mistake_is_caught(wrong, monkeypatch):
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    import pins
+    orc = oracle.default()
+    monkeypatch.setattr(oracle.Oracle, "gather_pages", staticmethod(wrong))
+    failed = 0
+    for pin in (pins.pin_paged_decode_equals_contiguous, pins.pin_paged_prefill_equals_contiguous,
+                pins.pin_paged_shared_page):
+        try:
+            pin(orc)
+        except Exception:
+            failed += 1
+    assert failed > 0
