@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -188,6 +189,34 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
       "add.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
       : "+f"(a0), "+f"(a1)
       : "f"(b0), "f"(b1));
+}
+
+// (a0, a1) = (a0 * b0 + c0, a1 * b1 + c1) as one paired fp32 fma.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float b0, float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\tmov.b64 z, {%4, %5};\n\t"
+      "fma.rn.f32x2 x, x, y, z;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// Power-of-two range scaling of 16-bit tensor-core operands.  For the
+// largest magnitude m of a set of values, pow2_scale_exp gives E such that
+// m * 2^(14 - E) lies in [2^14, 2^15) (exactly representable range of fp16,
+// whose largest finite value is 65504), with E clamped to [-100, 127] so both
+// 2^(14 - E) and 2^(E - 14) are normal fp32 numbers.  A zero or subnormal m
+// gives -100; an infinite or NaN m gives 127 (inf and NaN then stay so).
+__host__ __device__ __forceinline__ int pow2_scale_exp(float m) {
+  uint32_t bits;
+  memcpy(&bits, &m, 4);
+  int e = (int)((bits >> 23) & 0xffu) - 127;
+  return e < -100 ? -100 : (e > 127 ? 127 : e);
+}
+// 2^k for -126 <= k <= 127, exact.
+__host__ __device__ __forceinline__ float pow2f(int k) {
+  const uint32_t bits = (uint32_t)(127 + k) << 23;
+  float f;
+  memcpy(&f, &bits, 4);
+  return f;
 }
 
 constexpr float kLog2e = 1.4426950408889634f;

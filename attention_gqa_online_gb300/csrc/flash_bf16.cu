@@ -1,13 +1,27 @@
-// flash_bf16.cu -- tcgen05 flash attention with bf16 operands (forward and
-// prefill).
+// flash_bf16.cu -- tcgen05 flash attention with 16-bit operands (forward and
+// prefill): Q K^T in fp16, P V in bf16, both accumulated in fp32.
 //
 // Operation: softmax(scale * Q K^T) V over per-row causal / full / cross /
-// prefill windows (optionally cut to their last `window` keys) with the online softmax's running max and sum (cera
-// attention_prefill.wgsl, fn attention_prefill: per-tile max, correction,
-// exponentials, running sum; meganeura attention.wgsl, fn main: the final
-// (max, log sum) store).  A pre-pass converts K and V to bf16 (same layout);
-// Q and P are rounded to bf16 inside the kernel; both products accumulate in
-// fp32 in tensor memory.
+// prefill windows (optionally cut to their last `window` keys) with the
+// online softmax's running max and sum (cera attention_prefill.wgsl, fn
+// attention_prefill: per-tile max, correction, exponentials, running sum;
+// meganeura attention.wgsl, fn main: the final (max, log sum) store).
+//
+// Operand precision.  The scores decide the softmax weights exponentially,
+// so their operands carry 11 significant bits (fp16) instead of bf16's 8:
+// with scores of standard deviation 9 (Q, K ~ N(0, 3^2), D = 128) bf16 Q and
+// K move the output by up to about 2.2e-2 max|V|, fp16 ones by about 3e-3.
+// fp16 has a narrow exponent range, so every operand set carries a power of
+// two: each query row r is stored as q * scale * log2(e) * 2^(14 - E_r) and
+// each 128-key tile T of a kv head as k * 2^(14 - E_T), where E is the
+// binary exponent of the set's largest magnitude (so its values lie below
+// 2^15, inside fp16's range, whatever the fp32 inputs).  The product of the
+// two powers of two, 2^(E_r + E_T - 28), turns a raw score back into base-2
+// units in the softmax, at no extra instruction (it is the multiplier of the
+// fma that subtracts the running max).  P (<= 256) and V keep bf16 operands:
+// their rounding enters the output linearly, not through an exponential.
+// A pre-pass writes K as fp16 (with the tile factors) and V as bf16, in
+// their own layout; Q is converted inside the kernel.
 //
 // One CTA owns 128 packed rows of one kv head g: row r is (query i, head
 // g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs query
@@ -34,10 +48,12 @@
 //               32(w%4)..+31 (its TMEM lanes) and score columns 64c..64c+63.
 // The issuing warps run their loops warp-uniformly; one elected lane issues.
 // Tensor memory (512 columns): S_b [128 b, 128 b + 128) for b = 0..2, O
-// [384, 384 + D).  Scores are in base-2 units (Q is pre-multiplied by
+// [384, 384 + D).  Scores are in base-2 units once scaled (Q carries
 // scale * log2(e)).  The true max is tracked apart for the LSE.  Every wait is
 // bounded; a CTA whose pipeline breaks drains its copies and MMAs before it
 // releases tensor memory.
+#include <cfloat>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -75,7 +91,8 @@ struct __align__(1024) Bf16Smem {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_bf16_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
+                      const float* __restrict__ kfac) {
   constexpr int kChunks = D / 64;                // 128-byte (64-element) column chunks of a K row
   constexpr int kChunkBytes = kKeys * 128;       // one K box: 128 keys x 128 bytes
   constexpr int kTileBytes = kChunks * kChunkBytes;
@@ -191,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == 1) {
         // S_b = Q K_j^T, b = j % 3.  It overwrites the P that P V of tile
         // j-3 reads, so that product must have completed.
-        constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, kKeys);
+        constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtF16, false, kRows, kKeys);
         const uint64_t dq = tc::sdesc_sw128(smem_u32(qtile), 16, 1024);
         bool ok = wait(&sm.q_ready, 0);
         tc::fence_after_sync();
@@ -252,34 +269,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = qi < a.n_q;
     const float sl2 = a.scale * kLog2e;
 
-    // Q row, pre-scaled, as bf16 into the K-major operand tile: 64-element
-    // chunk c holds 128 rows of 128 bytes, 16-byte unit u of row r at unit
-    // u ^ (r & 7) (the 128-byte swizzle).  Group c converts chunk c from the
-    // staging rows; each thread starts at float4 r % 16 of its row, which
-    // spreads both the staging reads and the tile writes over the banks.
-    if (nt > 0 && grp < kChunks) {
+    // Q row, pre-scaled by scale * log2(e), as fp16 into the K-major operand
+    // tile: 64-element chunk c holds 128 rows of 128 bytes, 16-byte unit u of
+    // row r at unit u ^ (r & 7) (the 128-byte swizzle).  Group c converts
+    // elements [c D/2, (c + 1) D/2) of its row; the two halves agree on the
+    // row's power of two through shared memory.  Each thread starts at float4
+    // r % (D/8) of its half, which spreads both the staging reads and the
+    // tile writes over the banks.
+    constexpr int kQF4 = D / 8;  // float4 groups per half row
+    float f_row = 1.f;           // 2^(E_r - 14): turns this row's raw scores back
+    if (nt > 0) {
       mbar_wait_bounded(&sm.q_full, 0, a.status, &sm.abort);
-      const float4* src = reinterpret_cast<const float4*>(qstage + r * D + 64 * grp);
-      unsigned char* qdst = qtile + grp * kChunkBytes + r * 128;
+      const float* qrow = qstage + r * D;
       // RoPE: element e pairs with e +- D/2 (query qi at position base_pos + qi).
       const float* cs = (a.rope != nullptr && row_ok) ? a.rope + (a.base_pos + qi) * D : nullptr;
+      float4 xq[kQF4];
+      float qmax = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int f = (i + r) & 15;
-        float4 x = src[f];
+      for (int i = 0; i < kQF4; ++i) {
+        const int f = (i + r) % kQF4;
+        const int e = grp * (D / 2) + 4 * f;  // first element of this float4
+        float4 x = *reinterpret_cast<const float4*>(qrow + e);
         if (cs != nullptr) {
-          const int e = 64 * grp + 4 * f;                 // first element of this float4
-          const bool first = e < D / 2;
-          const int dd = first ? e : e - D / 2;          // pair index
-          const float4 y = *reinterpret_cast<const float4*>(qstage + r * D + (first ? e + D / 2 : dd));
+          const int dd = grp == 0 ? e : e - D / 2;  // pair index
+          const float4 y = *reinterpret_cast<const float4*>(qrow + (grp == 0 ? e + D / 2 : dd));
           const float4 cv = *reinterpret_cast<const float4*>(cs + dd);
           const float4 sv = *reinterpret_cast<const float4*>(cs + D / 2 + dd);
-          const float sg = first ? -1.f : 1.f;
+          const float sg = grp == 0 ? -1.f : 1.f;
           x = make_float4(fmaf(sg * y.x, sv.x, x.x * cv.x), fmaf(sg * y.y, sv.y, x.y * cv.y),
                           fmaf(sg * y.z, sv.z, x.z * cv.z), fmaf(sg * y.w, sv.w, x.w * cv.w));
         }
-        *reinterpret_cast<uint2*>(qdst + 16 * ((f >> 1) ^ (r & 7)) + 8 * (f & 1)) =
-            make_uint2(tc::pack_bf16(x.x * sl2, x.y * sl2), tc::pack_bf16(x.z * sl2, x.w * sl2));
+        x = make_float4(x.x * sl2, x.y * sl2, x.z * sl2, x.w * sl2);
+        xq[i] = x;
+        qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+      }
+      sm.red_l[grp][r] = qmax;
+      named_barrier(1, kSoftmaxThreads);
+      const int er = pow2_scale_exp(fmaxf(sm.red_l[0][r], sm.red_l[1][r]));
+      const float up = pow2f(14 - er);
+      f_row = pow2f(er - 14);
+#pragma unroll
+      for (int i = 0; i < kQF4; ++i) {
+        const int f = (i + r) % kQF4;
+        const int e = grp * (D / 2) + 4 * f;
+        const int u = (e & 63) >> 3;
+        unsigned char* qdst = qtile + (e >> 6) * kChunkBytes + r * 128 + 16 * (u ^ (r & 7)) + 8 * ((e >> 2) & 1);
+        const float4 x = xq[i];
+        *reinterpret_cast<uint2*>(qdst) = make_uint2(tc::pack_f16(x.x * up, x.y * up), tc::pack_f16(x.z * up, x.w * up));
       }
     }
     // The tensor core reads the tile through the async proxy.
@@ -290,9 +326,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_col = tmem + lane_base + kColO;
     constexpr int kHalfD = D / 2;  // O columns per group
     float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
+    // Power of two of K tile jt0 + j of this kv head, read one tile ahead.
+    float f_next = nt > 0 ? __ldg(kfac + (long long)jt0 * a.G + g) : 1.f;
     for (int j = 0; j < nt; ++j) {
       const int b = j % kSBuf;
       const uint32_t s_col = tmem + lane_base + kKeys * b + 64 * grp;
+      // Raw score -> base-2 units (at least FLT_MIN, so a masked -inf stays -inf).
+      const float cf = fmaxf(f_row * f_next, FLT_MIN);
+      if (j + 1 < nt) f_next = __ldg(kfac + (long long)(jt0 + j + 1) * a.G + g);
       mbar_wait_bounded(&sm.s_full[b], (unsigned)((j / kSBuf) & 1), a.status, &sm.abort);
       tc::fence_after_sync();
       uint32_t s[2][32];
@@ -327,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx[k] = max3(mx[k], __uint_as_float(s[i >> 5][(i & 31) + 2 * k]), __uint_as_float(s[i >> 5][(i & 31) + 2 * k + 1]));
       sm.red_max[j & 1][grp][r] = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       named_barrier(1, kSoftmaxThreads);  // both halves of every row are read and maxed
-      const float tmax = fmaxf(sm.red_max[j & 1][0][r], sm.red_max[j & 1][1][r]);
+      const float tmax = cf * fmaxf(sm.red_max[j & 1][0][r], sm.red_max[j & 1][1][r]);
       m_true = fmaxf(m_true, tmax);
       const float m_prev = m_ref;
       if (tmax > m_ref + kRescaleThreshold) m_ref = tmax;  // also for the first finite tile max
@@ -343,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float x0 = __uint_as_float(s[c][e]), x1 = __uint_as_float(s[c][e + 1]);
-          add2(x0, x1, neg_m, neg_m);
+          fma2(x0, x1, cf, cf, neg_m, neg_m);
           const float p0 = ex2(x0), p1 = ex2(x1);
           const int k = (e >> 1) & 3;
           add2(sum[2 * k], sum[2 * k + 1], p0, p1);
@@ -446,91 +487,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// K and V fp32 -> bf16 in one pass.  A block converts kConvPer * 256
-// consecutive float4 groups of each tensor; thread t takes groups t, t+256,
-// ... (coalesced), all loads issued before the first store; n4 groups of four
-// values per tensor, both sources 16-byte aligned.
-constexpr int kConvPer = 4;
-__global__ void __launch_bounds__(256) kv_to_bf16_kernel(const float4* __restrict__ k, const float4* __restrict__ v,
-                                                         uint2* __restrict__ k16, uint2* __restrict__ v16, long long n4) {
-  allow_dependent_launch();
-  grid_dependency_wait();
-  const long long base = (long long)blockIdx.x * (kConvPer * 256) + threadIdx.x;
-  float4 x[kConvPer], y[kConvPer];
-#pragma unroll
-  for (int t = 0; t < kConvPer; ++t) {
-    const long long i = base + 256 * t;
-    if (i < n4) {
-      x[t] = k[i];
-      y[t] = v[i];
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < kConvPer; ++t) {
-    const long long i = base + 256 * t;
-    if (i < n4) {
-      k16[i] = make_uint2(tc::pack_bf16(x[t].x, x[t].y), tc::pack_bf16(x[t].z, x[t].w));
-      v16[i] = make_uint2(tc::pack_bf16(y[t].x, y[t].y), tc::pack_bf16(y[t].z, y[t].w));
-    }
-  }
-}
-
-// The same conversion from a paged pool: logical rows [row0, row0 + rows) of
-// K and V (rows of n4 float4 groups) are gathered through the block table
-// into the contiguous bf16 copies (logical row t at t * n4).  A page outside
-// the pool gives zeros and ATTN_ERR_INVALID_ARG in the status word.
-__global__ void __launch_bounds__(256) kv_pages_to_bf16_kernel(const float4* __restrict__ k, const float4* __restrict__ v,
-                                                               uint2* __restrict__ k16, uint2* __restrict__ v16,
-                                                               const uint32_t* __restrict__ table, int page_rows,
-                                                               int num_pages, long long row0, long long rows, int n4,
-                                                               unsigned* status) {
-  allow_dependent_launch();
-  grid_dependency_wait();
-  const long long idx = (long long)blockIdx.x * 256 + threadIdx.x;
-  if (idx >= rows * n4) return;
-  const long long t = row0 + idx / n4;
-  const int c = (int)(idx % n4);
-  const uint32_t page = table[t / page_rows];
-  float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
-  if (page < (uint32_t)num_pages) {
-    const long long src = ((long long)page * page_rows + t % page_rows) * n4 + c;
-    x = k[src];
-    y = v[src];
-  } else if (c == 0) {
-    record_status(status, ATTN_ERR_INVALID_ARG);
-  }
-  k16[t * n4 + c] = make_uint2(tc::pack_bf16(x.x, x.y), tc::pack_bf16(x.z, x.w));
-  v16[t * n4 + c] = make_uint2(tc::pack_bf16(y.x, y.y), tc::pack_bf16(y.z, y.w));
-}
-
-// kv_to_bf16_kernel with RoPE on K: float4 group i (of rows of `stride`
-// floats, kv head g at g*D) pairs with the group D/2 further (or back) in its
-// head; key row t turns at position t.  V is converted as is.
-__global__ void __launch_bounds__(256) kv_rope_to_bf16_kernel(const float4* __restrict__ k, const float4* __restrict__ v,
-                                                              uint2* __restrict__ k16, uint2* __restrict__ v16,
-                                                              const float* __restrict__ table, long long first4,
-                                                              long long n4, int stride4, int D) {
-  allow_dependent_launch();
-  grid_dependency_wait();
-  const long long i = first4 + (long long)blockIdx.x * 256 + threadIdx.x;
-  if (i >= n4) return;
-  const long long t = i / stride4;
-  const int col = 4 * (int)(i % stride4);  // float index within the row
-  const int e = col % D;                   // within the head
-  const bool first = e < D / 2;
-  const int dd = first ? e : e - D / 2;
-  const float4 x = k[i];
-  const float4 y = k[i + (first ? D / 8 : -D / 8)];
-  const float4 cv = *reinterpret_cast<const float4*>(table + t * D + dd);
-  const float4 sv = *reinterpret_cast<const float4*>(table + t * D + D / 2 + dd);
-  const float sg = first ? -1.f : 1.f;
-  const float4 r = make_float4(fmaf(sg * y.x, sv.x, x.x * cv.x), fmaf(sg * y.y, sv.y, x.y * cv.y),
-                               fmaf(sg * y.z, sv.z, x.z * cv.z), fmaf(sg * y.w, sv.w, x.w * cv.w));
-  const float4 w = v[i];
-  k16[i] = make_uint2(tc::pack_bf16(r.x, r.y), tc::pack_bf16(r.z, r.w));
-  v16[i] = make_uint2(tc::pack_bf16(w.x, w.y), tc::pack_bf16(w.z, w.w));
-}
-
 template <int D>
 int launch_d(const FlashArgs& a, cudaStream_t s) {
   const int gs = a.H / a.G;
@@ -546,63 +502,49 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   void* scratch = nullptr;
   const void* kp = a.q;  // an empty key set never reads K/V: any aligned base will do
   const void* vp = a.q;
+  const float* kfac = nullptr;
   if (!no_keys) {
-    // K and V as bf16 in stream-ordered scratch memory (library pool),
-    // released on the same stream once the attention kernel has run.  Only
-    // rows from the first key tile any CTA reads are converted (under a
-    // sliding window the earlier rows are never read).
+    // K as fp16 with one power of two per (tile, kv head), V as bf16, in
+    // stream-ordered scratch memory (library pool), released on the same
+    // stream once the attention kernel has run.  Only tiles from the first
+    // one any CTA reads are converted (under a sliding window the earlier
+    // rows are never read).
     const long long elems = kv_rows * a.kv_row_stride;
+    const int n_tiles = (int)((kv_rows + kKeys - 1) / kKeys);
     const int n_first = a.causal ? (int)min((long long)a.cap, a.base_pos + 1) : a.n_all;  // window of query 0
-    const long long row0 = first_key(n_first, a.window) / kKeys * kKeys;
-    const long long skip = row0 * a.kv_row_stride;  // a multiple of 4 (row stride % 8 == 0)
-    if (scratch_alloc(&scratch, (size_t)elems * 4, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    const int tile0 = first_key(n_first, a.window) / kKeys;
+    const size_t fac_off = ((size_t)elems * 4 + 255) / 256 * 256;
+    if (scratch_alloc(&scratch, fac_off + (size_t)n_tiles * a.G * sizeof(float), s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
     uint16_t* k16 = static_cast<uint16_t*>(scratch);
     uint16_t* v16 = k16 + elems;
-    const float4* k4 = reinterpret_cast<const float4*>(a.k + skip);
-    const float4* v4 = reinterpret_cast<const float4*>(a.v + skip);
-    uint2* k2 = reinterpret_cast<uint2*>(k16 + skip);
-    uint2* v2 = reinterpret_cast<uint2*>(v16 + skip);
-    long long n4 = (elems - skip) / 4;
-    cudaError_t e;
-    if (a.rope != nullptr) {
-      // RoPE (contiguous K/V rows of G*D floats; the caller checks).
-      const float4* kb = reinterpret_cast<const float4*>(a.k);
-      const float4* vb = reinterpret_cast<const float4*>(a.v);
-      uint2* kd = reinterpret_cast<uint2*>(k16);
-      uint2* vd = reinterpret_cast<uint2*>(v16);
-      const float* table = a.rope;
-      long long first4 = skip / 4, all4 = elems / 4;
-      int stride4 = (int)(a.kv_row_stride / 4), dh = D;
-      void* rargs[] = {&kb, &vb, &kd, &vd, &table, &first4, &all4, &stride4, &dh};
-      const long long blocks = (all4 - first4 + 255) / 256;
-      e = launch_pdl(reinterpret_cast<const void*>(kv_rope_to_bf16_kernel), dim3((unsigned)blocks), dim3(256), 0, s,
-                     rargs);
-    } else if (a.block_table == nullptr) {
-      void* cargs[] = {&k4, &v4, &k2, &v2, &n4};
-      const long long blocks = (n4 + kConvPer * 256 - 1) / (kConvPer * 256);
-      e = launch_pdl(reinterpret_cast<const void*>(kv_to_bf16_kernel), dim3((unsigned)blocks), dim3(256), 0, s, cargs);
-    } else {
-      // Paged pool: gather the logical rows [row0, kv_rows) (same addresses
-      // in the copies as for a contiguous cache).
-      const float4* kpool = reinterpret_cast<const float4*>(a.k);
-      const float4* vpool = reinterpret_cast<const float4*>(a.v);
-      uint2* k0 = reinterpret_cast<uint2*>(k16);
-      uint2* v0 = reinterpret_cast<uint2*>(v16);
-      const uint32_t* table = a.block_table;
-      int pr = a.page_rows, np = a.num_pages, row_n4 = (int)(a.kv_row_stride / 4);
-      long long r0 = row0, rows = kv_rows - row0;
-      unsigned* st = a.status;
-      void* gargs[] = {&kpool, &vpool, &k0, &v0, &table, &pr, &np, &r0, &rows, &row_n4, &st};
-      const long long blocks = (rows * row_n4 + 255) / 256;
-      e = launch_pdl(reinterpret_cast<const void*>(kv_pages_to_bf16_kernel), dim3((unsigned)blocks), dim3(256), 0, s,
-                     gargs);
-    }
+    float* fac = reinterpret_cast<float*>(static_cast<char*>(scratch) + fac_off);
+    PrepArgs pa{};
+    pa.k = a.k;
+    pa.v = a.v;
+    pa.out0 = k16;
+    pa.out1 = v16;
+    pa.kfac = fac;
+    pa.stride = a.kv_row_stride;
+    pa.G = a.G;
+    pa.D = D;
+    pa.tile0 = tile0;
+    pa.n_tiles = n_tiles;
+    pa.rows_end = kv_rows;
+    pa.rope = a.rope;
+    pa.table = a.block_table;
+    pa.page_rows = a.page_rows;
+    pa.num_pages = a.num_pages;
+    pa.status = a.status;
+    pa.mode = kPrepF16Scaled;
+    const cudaError_t e = launch_kv_prep(pa, s);
     if (e != cudaSuccess) {
       scratch_free(scratch, s);
       return ATTN_ERR_CUDA;
     }
     kp = k16;
     vp = v16;
+    kfac = fac;
   }
   CUtensorMap tm_k, tm_v, tm_q;
   // Q: fp32 [n_q][H][D] (query rows q_row_stride floats apart); the box is
@@ -610,7 +552,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)a.H, (uint64_t)a.n_q};
   const uint64_t qstrides[2] = {(uint64_t)D * 4, (uint64_t)a.q_row_stride * 4};
   const uint32_t qbox[3] = {(uint32_t)D, (uint32_t)gs, (uint32_t)(kRows / gs)};
-  // K and V: [kv_rows][kv_row_stride] bf16, boxes of 64 elements x 128 keys.
+  // K and V: [kv_rows][kv_row_stride] 16-bit, boxes of 64 elements x 128 keys.
   const uint64_t dims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
   const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * 2};
   const uint32_t box[2] = {64, (uint32_t)kKeys};
@@ -627,7 +569,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
       rc = ATTN_ERR_CUDA;
     } else {
       FlashArgs aa = a;
-      void* args[] = {&aa, &tm_k, &tm_v, &tm_q};
+      void* args[] = {&aa, &tm_k, &tm_v, &tm_q, &kfac};
       if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s,
                      args) != cudaSuccess)
         rc = ATTN_ERR_CUDA;

@@ -1,14 +1,26 @@
-// flash_tc.cu -- tcgen05 tensor-core flash attention with TF32 operands
-// (forward and prefill).
+// flash_tc.cu -- tcgen05 tensor-core flash attention with TF32-class
+// accuracy (forward and prefill).
 //
 // Operation: softmax(scale * Q K^T) V over per-row causal / full / cross /
-// prefill windows (optionally cut to their last `window` keys), with the running max / sum of the pages' online softmax
-// (cera attention_prefill.wgsl, fn attention_prefill: per-tile max,
-// correction, exponentials, running sum; meganeura attention.wgsl, fn main:
-// the final (max, log sum) store).  Both contractions run on the 5th-generation
-// tensor cores with fp32 accumulation in tensor memory and TF32 operands: the
-// K/V tiles come straight from the fp32 inputs.  (The bf16-operand kernel is
-// flash_bf16.cu.)
+// prefill windows (optionally cut to their last `window` keys), with the
+// running max / sum of the pages' online softmax (cera attention_prefill.wgsl,
+// fn attention_prefill: per-tile max, correction, exponentials, running sum;
+// meganeura attention.wgsl, fn main: the final (max, log sum) store).  Both
+// contractions run on the 5th-generation tensor cores with fp32 accumulation
+// in tensor memory.  (The 16-bit-operand kernel is flash_bf16.cu.)
+//
+// Precision.  The scores enter the softmax through an exponential, so their
+// operand rounding dominates the error: with scores of standard deviation 9
+// (Q, K ~ N(0, 3^2), D = 128), TF32 Q and K (11 significant bits) move the
+// output by up to about 3.5e-3 max|V|.  Q K^T is therefore computed from a
+// split of both operands into bf16 pairs, x = hi + lo with hi = bf16(x) and
+// lo = bf16(x - hi) (16 or more significant bits), as the three products
+// Qhi Khi^T + Qhi Klo^T + Qlo Khi^T (the dropped Qlo Klo^T is below 2^-16 of
+// the score): about 1.5 times the tensor time of one TF32 product, and an
+// error near 5e-4 max|V|, set by P V.  P V uses TF32 operands: P (fp32 in
+// tensor memory) and the V tiles straight from the fp32 input.  A pre-pass
+// writes K's hi and lo parts (bf16, K's own layout); Q is split inside the
+// kernel.
 //
 // One CTA owns 128 packed rows of one kv head g: row r is (query i, head
 // g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs
@@ -16,14 +28,14 @@
 // holding the block's first kept key to the one holding its last.
 //
 // Warp roles (384 threads):
-//   warp 0      TMA producer: K tile (128 keys x D, 128-byte swizzle, K-major
-//               operand) and V tile (MN-major operand, which for 32-bit
-//               elements needs the 128-byte swizzle of 32-byte atoms) into a
-//               192 KB shared-memory ring three tiles deep, in the order the
-//               MMAs consume them.
+//   warp 0      TMA producer: K tile (hi then lo part, each 128 keys x D bf16,
+//               128-byte swizzle, K-major operand) and V tile (fp32, MN-major
+//               operand, which for 32-bit elements needs the 128-byte swizzle
+//               of 32-byte atoms) into a 192 KB shared-memory ring three tiles
+//               deep, in the order the MMAs consume them.
 //   warp 1      tensor-memory allocation; issues S_(j%2) = Q K_j^T
-//               (A = Q in TMEM, B = K tile, M=128 N=128) once P V of tile
-//               j-2 has released that buffer.
+//               (A = Q hi / lo in TMEM, B = K hi / lo tile, M=128 N=128) once
+//               P V of tile j-2 has released that buffer.
 //   warp 2      issues O += P_j V_j (A = P in TMEM over S_(j%2), B = V,
 //               M=128 N=D) in tile order once both softmax groups wrote P_j.
 //               The issuing warps run their loops warp-uniformly; one elected
@@ -35,13 +47,14 @@
 //               the score buffer, keeps its half of the row sum, rescales its
 //               half of O when the reference max moves, and finally writes its
 //               half of O / l; group 0 writes (max, log sum).
-// Tensor memory (512 columns): Q [0, 128), two 128-column score buffers
-// [128, 384), O [384, 384 + D).  Scores are in base-2 units: Q is
-// pre-multiplied by scale * log2(e).  The reference max only moves when a
-// row's tile max exceeds it by more than 8 (so P <= 256), which leaves the
-// result exact and skips most O rescales; the true max is tracked separately
-// for the LSE.  Every wait is bounded; a CTA whose pipeline breaks drains its
-// copies and MMAs before it releases tensor memory.
+// Tensor memory (512 columns): Q hi [0, D/2) and Q lo [D/2, D) as packed
+// bf16 pairs, two 128-column score buffers [128, 384), O [384, 384 + D).
+// Scores are in base-2 units: Q is pre-multiplied by scale * log2(e) before
+// it is split.  The reference max only moves when a row's tile max exceeds it
+// by more than 8 (so P <= 256), which leaves the result exact and skips most
+// O rescales; the true max is tracked separately for the LSE.  Every wait is
+// bounded; a CTA whose pipeline breaks drains its copies and MMAs before it
+// releases tensor memory.
 #include <cfloat>
 
 #include "common.cuh"
@@ -58,7 +71,7 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kRingBytes = 3 * 65536;  // K/V tile ring in shared memory
 constexpr int kMaxRing = 12;
-constexpr int kColQ = 0, kColS0 = 128, kColO = 384;  // S buffer b at kColS0 + kKeys * b
+constexpr int kColQ = 0, kColS0 = 128, kColO = 384;  // Q hi / lo in [0, 128); S buffer b at kColS0 + kKeys * b
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 constexpr int kPageBox = 32;     // fewest key rows per TMA box of a paged cache (page_rows % 32 == 0)
 constexpr int kPageCache = 1024;  // block-table entries a CTA keeps in shared memory
@@ -87,12 +100,17 @@ struct __align__(1024) TcSmem {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    flash_tc_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q) {
-  constexpr int kEpr = 32;                     // elements per 128-byte row
-  constexpr int kChunks = D / kEpr;            // 128-byte column chunks of a K/V row
+    flash_tc_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_kh,
+                    const __grid_constant__ CUtensorMap tm_kl, const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_q) {
+  constexpr int kEpr = 32;                     // fp32 elements per 128-byte row
+  constexpr int kChunks = D / kEpr;            // 128-byte column chunks of an fp32 V (or Q) row
   constexpr int kChunkBytes = kKeys * 128;     // one TMA box: 128 keys x 128 bytes
   constexpr int kTileBytes = kChunks * kChunkBytes;
+  constexpr int kKChunks = D / 64;             // 128-byte column chunks of a bf16 K row
+  constexpr int kKHalf = kKChunks * kChunkBytes;  // the hi (then the lo) part of a K tile
+  static_assert(2 * kKHalf == kTileBytes, "a K tile (hi + lo) fills one ring slot");
+  constexpr int kColQl = D / 2;                // Q lo after the D/2 columns of Q hi pairs
   constexpr int kRing = kRingBytes / kTileBytes;  // tiles in flight
   static_assert(kRing <= kMaxRing, "ring barriers");
   constexpr int kKStep = 8;                    // MMA K per instruction (32 bytes)
@@ -164,7 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nt > 0) {
       prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_kh);
+      prefetch_tmap(&tm_kl);
       prefetch_tmap(&tm_v);
       mbar_arrive_expect_tx(&sm.q_full, (unsigned)kTileBytes);
 #pragma unroll
@@ -180,10 +199,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&sm.kv_full[s], (unsigned)kTileBytes);
         const bool is_v = (p == 2 * nt - 1) || (p > 0 && (p & 1) == 0);
         const int t0 = kKeys * (jt0 + (is_v ? (p == 2 * nt - 1 ? nt - 1 : p / 2 - 1) : (p + 1) / 2));
-        const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
-        if (a.block_table == nullptr) {
+        if (!is_v) {
+          // K: the pre-pass's hi and lo parts (bf16, logical rows, also for a
+          // paged cache), 64-element column chunks.
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, tm, g * D + kEpr * c, t0, &sm.kv_full[s]);
+          for (int c = 0; c < kKChunks; ++c) {
+            tma_load_2d(dst + c * kChunkBytes, &tm_kh, g * D + 64 * c, t0, &sm.kv_full[s]);
+            tma_load_2d(dst + kKHalf + c * kChunkBytes, &tm_kl, g * D + 64 * c, t0, &sm.kv_full[s]);
+          }
+        } else if (a.block_table == nullptr) {
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, &tm_v, g * D + kEpr * c, t0, &sm.kv_full[s]);
         } else {
           // Paged: boxes of page_box rows (128, 64 or 32: the largest that
           // divides page_rows), each inside one page.  Rows no query of the
@@ -203,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
-              tma_load_2d(dst + c * kChunkBytes + sub * box * 128, tm, g * D + kEpr * c, y, &sm.kv_full[s]);
+              tma_load_2d(dst + c * kChunkBytes + sub * box * 128, &tm_v, g * D + kEpr * c, y, &sm.kv_full[s]);
           }
         }
       }
@@ -220,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // runs its loop (warp-uniform values); one elected lane issues each MMA
     // and commit.
     if (nt > 0) {
-      constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtTF32, false, kRows, kKeys);
+      constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, kKeys);
       constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtTF32, true, kRows, D);
       // V (MN-major B): the 32-byte-atom layout, 4-row K groups 512 bytes apart.
       constexpr uint32_t kVStep = kKStep * 128;  // bytes of V rows per K step
@@ -243,16 +269,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(&sm.kv_full[p % kRing], p / kRing)) return false;
         if (j >= kSBuf && !wait(&sm.pv_done[b], (j - kSBuf) / kSBuf)) return false;
         tc::fence_after_sync();
-        const uint64_t dk = dk0 + slot_off(p);
+        const uint64_t dkh = dk0 + slot_off(p);
+        const uint64_t dkl = dkh + (uint64_t)(kKHalf >> 4);
         const uint32_t ds = tmem + kColS0 + kKeys * b;
-        // Four K steps (32 bytes each) per 128-byte chunk of the K tile; Q
-        // takes 8 TMEM columns per step.
+        // Four K steps (16 bf16, 32 bytes each) per 128-byte chunk of the K
+        // tile; Q takes 8 TMEM columns (16 packed bf16) per step.  Per chunk:
+        // Qhi Khi, Qhi Klo, Qlo Khi, all accumulating into S.
 #pragma unroll
-        for (int c4 = 0; c4 < kChunks; ++c4) {
+        for (int c4 = 0; c4 < kKChunks; ++c4) {
           const uint64_t c = (uint64_t)((c4 * kChunkBytes) >> 4);
-          const uint32_t qa = tmem + kColQ + 32 * c4;
-          tc::mma4_tf32_ts(ds, qa, qa + 8, qa + 16, qa + 24, dk + c, dk + c + 2, dk + c + 4, dk + c + 6, idesc_qk,
-                           c4 > 0 ? 1u : 0u);
+          const uint32_t qh = tmem + kColQ + 32 * c4, ql = qh + kColQl;
+          tc::mma4_f16_ts(ds, qh, qh + 8, qh + 16, qh + 24, dkh + c, dkh + c + 2, dkh + c + 4, dkh + c + 6, idesc_qk,
+                          c4 > 0 ? 1u : 0u);
+          tc::mma4_f16_ts(ds, qh, qh + 8, qh + 16, qh + 24, dkl + c, dkl + c + 2, dkl + c + 4, dkl + c + 6, idesc_qk,
+                          1u);
+          tc::mma4_f16_ts(ds, ql, ql + 8, ql + 16, ql + 24, dkh + c, dkh + c + 2, dkh + c + 4, dkh + c + 6, idesc_qk,
+                          1u);
         }
         tc::commit_elect(&sm.s_full[b]);
         tc::commit_elect(&sm.kv_empty[p % kRing]);
@@ -308,8 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = qi < a.n_q;
     const float sl2 = a.scale * kLog2e;
 
-    // Q row -> TMEM (pre-scaled), one value per column; each group stores half
-    // the row, read from the staging slot (rows past n_q arrived as zeros).
+    // Q row -> TMEM (pre-scaled, then split into bf16 hi and lo parts), two
+    // values per column; each group stores half the row, read from the
+    // staging slot (rows past n_q arrived as zeros).
     if (nt > 0) {
       constexpr int kQCols = D / 2;
       mbar_wait_bounded(&sm.q_full, 0, a.status, &sm.abort);
@@ -337,7 +370,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           v[4 * u + 2] = __float_as_uint(x.z * sl2);
           v[4 * u + 3] = __float_as_uint(x.w * sl2);
         }
-        tc::tmem_st32(tmem + lane_base + kColQ + grp * kQCols + 32 * c, v);
+        // Element pairs (2i, 2i+1) of the chunk: hi = bf16 of each, lo = bf16
+        // of what hi leaves (exact in fp32).  Pair i goes to column i.
+        uint32_t hi[32], lo[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float x0 = __uint_as_float(v[2 * i]), x1 = __uint_as_float(v[2 * i + 1]);
+          const uint32_t h = tc::pack_bf16(x0, x1);
+          hi[i] = h;
+          lo[i] = tc::pack_bf16(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xffff0000u));
+        }
+        const uint32_t qcol = tmem + lane_base + kColQ + (grp * kQCols + 32 * c) / 2;
+        tc::tmem_st16(qcol, hi);
+        tc::tmem_st16(qcol + kColQl, lo);
       }
       tc::tmem_st_wait();
     }
@@ -520,43 +565,72 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.n_q * gs;
   const long long nb = (rows + kRows - 1) / kRows;
   if (nb == 0) return 0;
-  // Rows of K/V any CTA may read: the largest window of the call (a paged
-  // cache: the whole pool).  Rows past it are outside the tensor map and
-  // arrive as zeros.
+  // Logical K/V rows any CTA may read: the largest window of the call.  Rows
+  // past it are outside the tensor maps and arrive as zeros.  A paged V is
+  // read from its pool (the whole pool is mapped).
   long long kv_rows = a.causal ? a.base_pos + a.n_q : a.n_all;
   if (kv_rows > a.cap) kv_rows = a.cap;
   const bool paged = a.block_table != nullptr;
-  if (paged && kv_rows > 0) kv_rows = (long long)a.num_pages * a.page_rows;
   const bool no_keys = kv_rows < 1 || a.k == nullptr || a.v == nullptr;
   if (kv_rows < 1) kv_rows = 1;
+  const long long v_rows = (paged && !no_keys) ? (long long)a.num_pages * a.page_rows : kv_rows;
   // An empty key set never reads K/V: any aligned base will do.
-  const void* kp = no_keys ? static_cast<const void*>(a.q) : a.k;
+  const void* khp = a.q;
+  const void* klp = a.q;
   const void* vp = no_keys ? static_cast<const void*>(a.q) : a.v;
-  // RoPE: K turned at its positions into stream-ordered scratch first (rows
-  // of exactly G*D floats; the caller checks).
   void* scratch = nullptr;
-  if (a.rope != nullptr && !no_keys) {
-    if (scratch_alloc(&scratch, (size_t)kv_rows * a.kv_row_stride * sizeof(float), s) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    if (launch_rope_k(a.k, static_cast<float*>(scratch), a.rope, kv_rows, a.G, D, s) != cudaSuccess) {
+  if (!no_keys) {
+    // K's bf16 hi and lo parts (turned by RoPE, gathered from pages) in
+    // stream-ordered scratch memory (library pool), released on the same
+    // stream once the attention kernel has run.  Only tiles from the first
+    // one any CTA reads are written.
+    const long long elems = kv_rows * a.kv_row_stride;
+    const int n_first = a.causal ? (int)min((long long)a.cap, a.base_pos + 1) : a.n_all;  // window of query 0
+    if (scratch_alloc(&scratch, (size_t)elems * 4, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    uint16_t* kh = static_cast<uint16_t*>(scratch);
+    PrepArgs pa{};
+    pa.k = a.k;
+    pa.v = a.v;
+    pa.out0 = kh;
+    pa.out1 = kh + elems;
+    pa.stride = a.kv_row_stride;
+    pa.G = a.G;
+    pa.D = D;
+    pa.tile0 = first_key(n_first, a.window) / kKeys;
+    pa.n_tiles = (int)((kv_rows + kKeys - 1) / kKeys);
+    pa.rows_end = kv_rows;
+    pa.rope = a.rope;
+    pa.table = a.block_table;
+    pa.page_rows = a.page_rows;
+    pa.num_pages = a.num_pages;
+    pa.status = a.status;
+    pa.mode = kPrepBf16Split;
+    if (launch_kv_prep(pa, s) != cudaSuccess) {
       scratch_free(scratch, s);
       return ATTN_ERR_CUDA;
     }
-    kp = scratch;
+    khp = pa.out0;
+    klp = pa.out1;
   }
-  CUtensorMap tm_k, tm_v, tm_q;
+  CUtensorMap tm_kh, tm_kl, tm_v, tm_q;
   // Q: fp32 [n_q][H][D] (query rows q_row_stride floats apart); one CTA's
   // block is D/32 boxes of 32 floats x gs heads x 128/gs queries, rows past
   // n_q read as 0.
   const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)a.H, (uint64_t)a.n_q};
   const uint64_t qstrides[2] = {(uint64_t)D * 4, (uint64_t)a.q_row_stride * 4};
   const uint32_t qbox[3] = {32, (uint32_t)gs, (uint32_t)(kRows / gs)};
-  const uint64_t dims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
-  const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * 4};
-  const uint32_t box[2] = {32, (uint32_t)(paged ? page_box(a.page_rows) : kKeys)};
+  // K hi / lo: [kv_rows][kv_row_stride] bf16, boxes of 64 elements x 128 keys.
+  const uint64_t kdims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
+  const uint64_t kstrides[1] = {(uint64_t)a.kv_row_stride * 2};
+  const uint32_t kbox[2] = {64, (uint32_t)kKeys};
+  // V: fp32 rows (a paged pool: boxes inside one page).
+  const uint64_t vdims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)v_rows};
+  const uint64_t vstrides[1] = {(uint64_t)a.kv_row_stride * 4};
+  const uint32_t vbox[2] = {32, (uint32_t)(paged ? page_box(a.page_rows) : kKeys)};
   int rc = ATTN_OK;
-  if (!make_tmap(&tm_k, kp, 2, dims, strides, box, false, kSwizzle128) ||
-      !make_tmap(&tm_v, vp, 2, dims, strides, box, false, kSwizzle128Atom32) ||
+  if (!make_tmap(&tm_kh, khp, 2, kdims, kstrides, kbox, true, kSwizzle128) ||
+      !make_tmap(&tm_kl, klp, 2, kdims, kstrides, kbox, true, kSwizzle128) ||
+      !make_tmap(&tm_v, vp, 2, vdims, vstrides, vbox, false, kSwizzle128Atom32) ||
       !make_tmap(&tm_q, a.q, 3, qdims, qstrides, qbox, false, kSwizzle128)) {
     rc = ATTN_ERR_UNSUPPORTED;
   } else {
@@ -566,7 +640,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
       rc = ATTN_ERR_CUDA;
     } else {
       FlashArgs aa = a;
-      void* args[] = {&aa, &tm_k, &tm_v, &tm_q};
+      void* args[] = {&aa, &tm_kh, &tm_kl, &tm_v, &tm_q};
       if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s,
                      args) != cudaSuccess)
         rc = ATTN_ERR_CUDA;
@@ -589,7 +663,7 @@ bool flash_tc_supported(const FlashArgs& a, int prec) {
                        reinterpret_cast<uintptr_t>(a.k) | reinterpret_cast<uintptr_t>(a.v);
   if (al % 16 != 0) return false;
   if (a.q_row_stride % 4 != 0 || a.out_row_stride % 4 != 0 || a.kv_row_stride % 4 != 0) return false;
-  if (prec == ATTN_BF16 && a.kv_row_stride % 8 != 0) return false;  // bf16 rows in 16-byte units
+  if (a.kv_row_stride % 8 != 0) return false;  // the 16-bit K (and V) copies: rows in 16-byte units
   if (a.block_table != nullptr && (a.page_rows % kPageBox != 0 || (long long)a.num_pages * a.page_rows > 0x7fffffffLL))
     return false;
   return true;

@@ -1,0 +1,143 @@
+// kv_prep.cu -- K/V operand pre-pass of the tensor-core flash kernels.
+//
+// One block per (128-key tile T, kv head g, tensor z), 512 threads; a row of
+// one head is D/4 consecutive threads' float4 groups, so every load and store
+// is a coalesced row run.  Rows [128 T, 128 T + 128) at or past `rows_end`
+// are not written (the attention kernels' tensor maps end there).  Paged
+// caches (table != nullptr): logical row t is read from its pool row; a page
+// outside the pool reads as zeros and records ATTN_ERR_INVALID_ARG.  RoPE
+// (rope != nullptr): K row t is turned at position t first.  Outputs keep the
+// inputs' layout (rows of `stride` elements, head g at column g * D).
+//
+// kPrepF16Scaled (the 16-bit kernel's operands):
+//   z = 0  K as fp16 times 2^(14 - E_T), E_T the binary exponent of the
+//          tile's (this head's) largest magnitude, so its values lie below
+//          2^15, inside fp16's range; kfac[T * G + g] = 2^(E_T - 14).
+//   z = 1  V as bf16.
+// kPrepBf16Split (the TF32 kernel's exact Q K^T):
+//   z = 0  K = hi + lo with hi = bf16(K) and lo = bf16(K - hi), 16 or more
+//          significant bits between them (K - hi is exact in fp32).
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kPrepThreads = 512;
+
+template <int D, int Mode>
+__global__ void __launch_bounds__(kPrepThreads, 2) kv_prep_kernel(const PrepArgs p) {
+  constexpr int kPerRow = D / 4;                       // float4 groups per row of one head
+  constexpr int kRowsPerPass = kPrepThreads / kPerRow;  // rows of the tile per pass of the block
+  constexpr int kPasses = 128 / kRowsPerPass;
+  allow_dependent_launch();
+  grid_dependency_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = blockIdx.y;
+  const bool is_k = blockIdx.z == 0;
+  const long long t_first = (long long)(p.tile0 + blockIdx.x) * 128;
+  const int c4 = tid % kPerRow;  // float4 group within the row
+  const int rsub = tid / kPerRow;
+  const float* src = is_k ? p.k : p.v;
+  const long long col = (long long)g * D + 4 * c4;
+  float4 x[kPasses];
+  float mx = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {
+    const long long t = t_first + i * kRowsPerPass + rsub;
+    x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < p.rows_end) {
+      long long row = t;
+      if (p.table != nullptr) row = paged_row(p.table, p.page_rows, p.num_pages, (int)t, p.status);
+      if (row >= 0) x[i] = *reinterpret_cast<const float4*>(src + row * p.stride + col);
+    }
+  }
+  if (!is_k) {  // V as bf16 (kPrepF16Scaled only)
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      const long long t = t_first + i * kRowsPerPass + rsub;
+      if (t < p.rows_end)
+        *reinterpret_cast<uint2*>(p.out1 + t * p.stride + col) =
+            make_uint2(tc::pack_bf16(x[i].x, x[i].y), tc::pack_bf16(x[i].z, x[i].w));
+    }
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {
+    if (p.rope != nullptr) {
+      // Pair (d, d + D/2): the partner float4 is D/8 lanes away in the same row.
+      const float4 y =
+          make_float4(__shfl_xor_sync(0xffffffffu, x[i].x, D / 8), __shfl_xor_sync(0xffffffffu, x[i].y, D / 8),
+                      __shfl_xor_sync(0xffffffffu, x[i].z, D / 8), __shfl_xor_sync(0xffffffffu, x[i].w, D / 8));
+      const long long t = t_first + i * kRowsPerPass + rsub;
+      if (t < p.rows_end) {
+        const int e = 4 * c4;
+        const bool first = e < D / 2;
+        const int dd = first ? e : e - D / 2;
+        const float4 cv = *reinterpret_cast<const float4*>(p.rope + t * D + dd);
+        const float4 sv = *reinterpret_cast<const float4*>(p.rope + t * D + D / 2 + dd);
+        const float sg = first ? -1.f : 1.f;
+        x[i] = make_float4(fmaf(sg * y.x, sv.x, x[i].x * cv.x), fmaf(sg * y.y, sv.y, x[i].y * cv.y),
+                           fmaf(sg * y.z, sv.z, x[i].z * cv.z), fmaf(sg * y.w, sv.w, x[i].w * cv.w));
+      }
+    }
+    if (Mode == kPrepF16Scaled)
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x[i].x), fabsf(x[i].y)), fmaxf(fabsf(x[i].z), fabsf(x[i].w))));
+  }
+  if (Mode == kPrepBf16Split) {
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      const long long t = t_first + i * kRowsPerPass + rsub;
+      if (t < p.rows_end) {
+        const uint32_t h01 = tc::pack_bf16(x[i].x, x[i].y), h23 = tc::pack_bf16(x[i].z, x[i].w);
+        const float4 h = make_float4(__uint_as_float(h01 << 16), __uint_as_float(h01 & 0xffff0000u),
+                                     __uint_as_float(h23 << 16), __uint_as_float(h23 & 0xffff0000u));
+        *reinterpret_cast<uint2*>(p.out0 + t * p.stride + col) = make_uint2(h01, h23);
+        *reinterpret_cast<uint2*>(p.out1 + t * p.stride + col) =
+            make_uint2(tc::pack_bf16(x[i].x - h.x, x[i].y - h.y), tc::pack_bf16(x[i].z - h.z, x[i].w - h.w));
+      }
+    }
+    return;
+  }
+  // Largest magnitude of the tile: warp maxima, then the block's.
+  __shared__ float wmax[kPrepThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) wmax[warp] = mx;
+  __syncthreads();
+  mx = 0.f;
+#pragma unroll
+  for (int w = 0; w < kPrepThreads / 32; ++w) mx = fmaxf(mx, wmax[w]);
+  const int et = pow2_scale_exp(mx);
+  const float up = pow2f(14 - et);
+  if (tid == 0) p.kfac[(long long)(p.tile0 + blockIdx.x) * p.G + g] = pow2f(et - 14);
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {
+    const long long t = t_first + i * kRowsPerPass + rsub;
+    if (t < p.rows_end)
+      *reinterpret_cast<uint2*>(p.out0 + t * p.stride + col) =
+          make_uint2(tc::pack_f16(x[i].x * up, x[i].y * up), tc::pack_f16(x[i].z * up, x[i].w * up));
+  }
+}
+
+template <int D, int Mode>
+cudaError_t launch_mode(const PrepArgs& p, cudaStream_t s) {
+  PrepArgs pp = p;
+  void* args[] = {&pp};
+  const dim3 grid((unsigned)(p.n_tiles - p.tile0), (unsigned)p.G, Mode == kPrepF16Scaled ? 2u : 1u);
+  return launch_pdl(reinterpret_cast<const void*>(kv_prep_kernel<D, Mode>), grid, dim3(kPrepThreads), 0, s, args);
+}
+
+}  // namespace
+
+cudaError_t launch_kv_prep(const PrepArgs& p, cudaStream_t s) {
+  if (p.n_tiles <= p.tile0) return cudaSuccess;
+  if (p.D == 128)
+    return p.mode == kPrepF16Scaled ? launch_mode<128, kPrepF16Scaled>(p, s) : launch_mode<128, kPrepBf16Split>(p, s);
+  if (p.D == 64)
+    return p.mode == kPrepF16Scaled ? launch_mode<64, kPrepF16Scaled>(p, s) : launch_mode<64, kPrepBf16Split>(p, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

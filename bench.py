@@ -40,6 +40,8 @@ KV_POS = 16383
 DECODE_WORKLOAD = "decode q[1,32x128] kv_cache[16384,8x128] fp32 kv_pos=16383"
 PREFILL = dict(n_queries=512, start_pos=1536, max_seq=2048, H=32, G=8, D=128, stride=4096)
 FORWARD = dict(q_seq=8192, H=32, G=8, D=128)
+MHA = dict(H=16, D=64, q_full=2048, q_cross=1024, kv_cross=4096)
+SWEEP = (0, 7, 511, 4095, 16383)
 WINDOW = 4096  # sliding-window workloads: each row keeps its last 4096 keys
 
 
@@ -53,10 +55,10 @@ def prefill_flops():
     return 4.0 * p["D"] * tri * p["H"]
 
 
-def forward_flops(window=0):
+def forward_flops(window=0, q_seq=None):
     """Algorithmic FLOPs of the causal forward: 4 D per (row, head, kept key)."""
     f = FORWARD
-    n = f["q_seq"]
+    n = q_seq or f["q_seq"]
     keys = n * (n + 1) // 2
     if window:
         w = min(window, n)
@@ -387,16 +389,43 @@ def run_ours(args, world, rank, local):
             "clocks": clocks,
             "decode_us_per_token": ms_step * 1e3,
         }
-        line.update(extras)
         if not args.no_cpu_baseline:
             calls, el = time_oracle_decode(args.cpu_seconds)
             line["cpu_baseline"] = {"value": decode_bytes(KV_POS + 1) * calls / el / 1e9, "unit": "GB/s",
                                     "cores": 1, "kind": "oracle",
                                     "sample": "%d oracle decode calls at kv_pos=16383 in %.1f s" % (calls, el)}
+        line.update(extras)
+        line["summary"] = summary(line, extras)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+# Order of the compact summary that closes the JSON line (last = most
+# important: a reader that keeps only the line's tail still sees them).
+SUMMARY_ORDER = ("backward_fp32", "backward_bf16", "forward_rope_fp32", "forward_rope_tf32", "forward_rope_bf16",
+                 "forward_window_fp32", "forward_window_tf32", "forward_window_bf16", "decode_window", "decode_gqa8",
+                 "decode_paged", "prefill_paged_tf32", "prefill_paged_bf16", "mha_cross_fp32", "mha_cross_tf32",
+                 "mha_cross_bf16", "mha_full_fp32", "mha_full_tf32", "mha_full_bf16", "forward_8193_fp32",
+                 "forward_8193_tf32", "forward_8193_bf16", "forward_fp32", "forward_tf32", "forward_bf16",
+                 "prefill_fp32", "prefill_tf32", "prefill_bf16")
+
+
+def summary(line, extras):
+    """Compact {workload: [value, unit, roofline fraction]} of every line, the
+    decode sweep as {kv_pos: [us/token, GB/s]}, and the headline decode last."""
+    out = {}
+    for k in SUMMARY_ORDER:
+        e = extras.get(k)
+        if e:
+            out[k] = [round(e["value"], 1), e["unit"], round(e["roofline"]["frac"], 3)]
+    sw = extras.get("decode_sweep")
+    if sw:
+        out["decode_sweep_us_GBs"] = {p: [round(x["us_per_token"], 2), round(x["GB/s"], 0)]
+                                      for p, x in sw["points"].items()}
+    out["decode"] = [round(line["value"], 1), line["unit"], round(line["roofline"]["frac"], 3)]
+    return out
 
 
 def tf32_peak(peaks):
@@ -440,8 +469,10 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
                 "traffic": None, "kernel": kernel,
                 "peak_source": "fp32 FMA: %d SMs x 128 lanes x 2 x %.0f MHz" % (sms, sm_mhz)}
 
-    def forward_lines(prefix, window, what, rope=False):
-        f = FORWARD
+    def forward_lines(prefix, window, what, rope=False, q_seq=None):
+        f = dict(FORWARD)
+        if q_seq is not None:
+            f["q_seq"] = q_seq
         q, k, v = synthetic.forward_inputs(f["q_seq"], f["q_seq"], f["H"], f["G"], f["D"], seed=5, qk_sigma=3.0)
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
         outf = torch.empty_like(qd)
@@ -462,13 +493,13 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
                 if rc != 0:
                     raise RuntimeError("forward failed: %d" % rc)
             ms = timed(fwd_step, steps)
-            tf = forward_flops(window) / (ms * 1e-3) / 1e12
+            tf = forward_flops(window, f["q_seq"]) / (ms * 1e-3) / 1e12
             res[prefix + name] = {
                 "workload": what, "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "prec": name,
                 "roofline": roof(prec, tf, kern), "l2": "inputs 192 MiB > L2"}
 
     variants = ((A.ATTN_TF32, "tf32", "flash_tc_kernel<128> (tf32)"),
-                (A.ATTN_BF16, "bf16", "flash_bf16_kernel<128> (bf16) + kv_to_bf16 pre-pass"),
+                (A.ATTN_BF16, "bf16", "flash_bf16_kernel<128> (fp16 QK, bf16 PV) + kv_prep16 pre-pass"),
                 (A.ATTN_FP32, "fp32", "flash_simt_kernel<128,true>"))
 
     if only in ("all", "prefill"):
@@ -611,7 +642,7 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
             res["prefill_paged_" + name] = {
                 "workload": "prefill 512 queries start_pos=1536, cache of 16 pages x 128 rows in shuffled pool order, "
                             "32/8 heads D=128", "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "prec": name,
-                "roofline": roof(prec, tf, kern + (" (paged gather pre-pass)" if prec == A.ATTN_BF16 else "")),
+                "roofline": roof(prec, tf, kern + (" (gathering the pages)" if prec == A.ATTN_BF16 else "")),
                 "l2": "rotating %d input sets" % n_rot2}
         del bufs
 
@@ -701,6 +732,83 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
             "l2": "rotating %d caches (%d MiB of windows) > 2x L2" % (n_rot, n_rot * (win_bytes >> 20)),
             "timing": "%d back-to-back launches between one event pair" % n_dec}
         del caches
+
+    if only in ("all", "forward"):
+        # The long causal stress workload's ragged length.
+        forward_lines("forward_8193_", 0, "causal forward+LSE q_seq=8193 (ragged last tile) 32/8 heads D=128, "
+                      "Q,K N(0,9)", q_seq=8193)
+
+    if only in ("all", "mha"):
+        # Full and cross attention, 16 heads = 16 kv heads, D=64, Q,K N(0,1), V U(-1,1).
+        for name, mask, qs, ks in (("mha_full_", A.ATTN_FULL, MHA["q_full"], MHA["q_full"]),
+                                   ("mha_cross_", A.ATTN_CROSS, MHA["q_cross"], MHA["kv_cross"])):
+            q, k, v = synthetic.forward_inputs(qs, ks, MHA["H"], MHA["H"], MHA["D"], seed=4, v_dist="uniform")
+            per = (q.numel() + k.numel() + v.numel()) * 4 * 2
+            n_rot = max(2, int(math.ceil(2.0 * l2 / per)) + 1)
+            bufs = [(q.to(dev), k.to(dev), v.to(dev)) for _ in range(n_rot)]
+            outm = torch.empty_like(bufs[0][0])
+            lsem = torch.empty((qs, MHA["H"], 2), device=dev)
+            flops = 4.0 * MHA["D"] * qs * ks * MHA["H"]
+            what = "%s forward+LSE q=%d kv=%d, 16/16 heads D=64, Q,K N(0,1), V U(-1,1)" % (
+                "full" if mask == A.ATTN_FULL else "cross", qs, ks)
+            kern = {A.ATTN_TF32: "flash_tc_kernel<64> (tf32)", A.ATTN_BF16: "flash_bf16_kernel<64> + kv_prep16",
+                    A.ATTN_FP32: "flash_simt_kernel<64>"}
+            for prec, pname in ((A.ATTN_TF32, "tf32"), (A.ATTN_BF16, "bf16"), (A.ATTN_FP32, "fp32")):
+                def mha_step(i, prec=prec, mask=mask, qs=qs, ks=ks):
+                    qd, kd, vd = bufs[i % n_rot]
+                    rc = lib.attn_forward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), outm.data_ptr(),
+                                          lsem.data_ptr(), qs, ks, MHA["H"], MHA["H"], MHA["D"], mask, prec, sh)
+                    if rc != 0:
+                        raise RuntimeError("attn_forward failed: %d" % rc)
+                ms = timed(mha_step, steps)
+                tf = flops / (ms * 1e-3) / 1e12
+                res[name + pname] = {"workload": what, "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
+                                     "prec": pname, "roofline": roof(prec, tf, kern[prec]),
+                                     "l2": "rotating %d input sets" % n_rot}
+            del bufs
+
+    if only in ("all", "sweep"):
+        # Decode at every kv_pos of the sweep: microseconds per token and K/V GB/s.
+        q, kc, vc = synthetic.decode_inputs(MAX_SEQ, H, G, D, seed=3)
+        qd = q.to(dev)
+        n_rot = max(3, int(math.ceil(2.0 * l2 / (2 * MAX_SEQ * G * D * 4))) + 1)
+        caches = [(kc.to(dev), vc.to(dev)) for _ in range(n_rot)]
+        out = torch.empty_like(qd)
+        ws_bytes = A.attn_decode_workspace_bytes(H, G, D, MAX_SEQ)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        pos = torch.zeros((1,), dtype=torch.int32, device=dev)
+        sweep = {}
+        for kv_pos in SWEEP:
+            pos.fill_(kv_pos)
+
+            def sw_step(i):
+                kd, vd = caches[i % n_rot]
+                rc = lib.attn_decode_cached(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), pos.data_ptr(),
+                                            out.data_ptr(), H, G, D, MAX_SEQ, ws.data_ptr(), ws_bytes, sh)
+                if rc != 0:
+                    raise RuntimeError("attn_decode_cached failed: %d" % rc)
+            for i in range(args.warmup):
+                sw_step(i)
+            torch.cuda.synchronize()
+            n_dec = max(steps, 200)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(n_dec):
+                sw_step(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res["_launches"] += n_dec + args.warmup
+            ms = e0.elapsed_time(e1) / n_dec
+            by = decode_bytes(kv_pos + 1)
+            gbs = by / (ms * 1e-3) / 1e9
+            sweep[str(kv_pos)] = {"us_per_token": ms * 1e3, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"],
+                                  "bytes": by}
+        res["decode_sweep"] = {
+            "workload": "decode q[1,32x128] kv_cache[16384,8x128] fp32 at kv_pos in %s" % (list(SWEEP),),
+            "points": sweep, "unit": "us/token and GB/s", "kernel": "decode_split_kernel<128,4>",
+            "peak": peaks["hbm_gbs"], "peak_source": peak_src, "l2": "rotating %d caches > 2x L2" % n_rot,
+            "timing": "%d back-to-back launches per point" % max(steps, 200)}
+        del caches
     return res
 
 
@@ -733,7 +841,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only", choices=["all", "decode", "prefill", "forward", "window", "backward", "paged", "rope",
-                                       "decode_gqa8"],
+                                       "decode_gqa8", "mha", "sweep"],
                     default="all",
                     help="run one workload (for profiling); the default runs all of them")
     ap.add_argument("--ref-seconds", type=float, default=60.0)
@@ -744,7 +852,7 @@ def main():
     if args.impl == "reference":
         reference_arm(args, world, rank)
         return
-    if args.only in ("prefill", "forward", "window", "backward", "paged", "rope", "decode_gqa8"):
+    if args.only in ("prefill", "forward", "window", "backward", "paged", "rope", "decode_gqa8", "mha", "sweep"):
         run_single(args, local)
         return
     if args.only == "decode":

@@ -1,5 +1,12 @@
 """The C ABI without a GPU: the library loads, exports every declared entry
-point, and rejects bad arguments on the host before touching the device."""
+point, and rejects bad arguments on the host before touching the device.
+
+The calls below pass made-up device addresses, which host validation must
+refuse before anything is launched.  They therefore never run where a GPU is
+visible: there, test_abi_device_hidden.py runs this module in a child process
+with CUDA_VISIBLE_DEVICES="" instead, so that a validation regression shows
+as a wrong status code (no device to launch on) and never as a kernel
+reading a made-up address on a shared GPU."""
 import ctypes
 import math
 import os
@@ -9,6 +16,21 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def gpu_visible():
+    """True when this process can see a CUDA device."""
+    if os.environ.get("CUDA_VISIBLE_DEVICES") == "":
+        return False
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+pytestmark = pytest.mark.skipif(gpu_visible(), reason="a GPU is visible: test_abi_device_hidden.py runs this "
+                                                      "module in a child process with the device hidden")
 
 
 @pytest.fixture(scope="module")

@@ -1,4 +1,6 @@
 """attn_forward on the GPU against the fp64 oracle (same seeded inputs)."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -96,3 +98,44 @@ def test_long_causal_stress(cuda_lib, orc, prec, q_seq):
     rng = np.random.default_rng(q_seq)
     rows = sorted(set(range(16)) | set(range(q_seq - 16, q_seq)) | set(rng.integers(0, q_seq, 16).tolist()))
     check(cuda_lib, orc, q_seq, q_seq, 32, 8, 128, CAUSAL, prec, seed=5, rows=rows, qk_sigma=3.0)
+
+
+@pytest.mark.parametrize("prec", [TF32, BF16])
+@pytest.mark.parametrize("seed", [11, 12, 13])
+def test_long_causal_stress_seeds(cuda_lib, orc, prec, seed):
+    """The tensor-core precisions on further seeds of the long causal stress
+    distribution (Q,K N(0,3^2)): 64 rows spread over the sequence."""
+    q_seq = 8192
+    rng = np.random.default_rng(seed)
+    rows = sorted(set(rng.integers(0, q_seq, 56).tolist()) | set(range(q_seq - 8, q_seq)))
+    check(cuda_lib, orc, q_seq, q_seq, 32, 8, 128, CAUSAL, prec, seed=seed, rows=rows, qk_sigma=3.0)
+
+
+@pytest.mark.parametrize("prec", [TF32, BF16])
+@pytest.mark.parametrize("qs,ks", [(1e-6, 1e6), (1e6, 1e-6), (2.0 ** 40, 2.0 ** -40), (2.0 ** -60, 2.0 ** 60)])
+def test_operand_range(cuda_lib, orc, prec, qs, ks):
+    """Scaling Q by qs and K by ks = 1/qs leaves every score, and so the result,
+    unchanged.  The 16-bit path's fp16 score operands carry powers of two that
+    keep them inside fp16's range whatever the fp32 magnitudes (plain fp16 would
+    overflow beyond 65504 or lose everything below 6e-8)."""
+    q_seq, H, G, D = 300, 8, 2, 128
+    q, k, v = synthetic.forward_inputs(q_seq, q_seq, H, G, D, seed=23)
+    ref, _ = run_forward(cuda_lib, q, k, v, q_seq, q_seq, H, G, D, CAUSAL, prec)
+    out, _ = run_forward(cuda_lib, q * qs, k * ks, v, q_seq, q_seq, H, G, D, CAUSAL, prec)
+    ro, _ = orc.forward(q.numpy(), k.numpy(), v.numpy(), q_seq, q_seq, H, G, D, CAUSAL)
+    vmax = float(v.abs().max())
+    assert_out_close(out, ro, prec, vmax, "scaled operands")
+    if math.frexp(qs)[0] == 0.5:  # exact powers of two change no operand bit
+        assert np.array_equal(out, ref)
+
+
+def test_bf16_mixed_magnitude_tile(cuda_lib, orc):
+    """One key row a million times larger than the others in its 128-key tile:
+    the tile's power of two follows that row, and the other keys' scores keep
+    their accuracy (fp16 subnormals only start far below their magnitude)."""
+    q_seq, H, G, D = 256, 4, 1, 64
+    q, k, v = synthetic.forward_inputs(q_seq, q_seq, H, G, D, seed=24)
+    k[200] *= 1e6
+    out, _ = run_forward(cuda_lib, q, k, v, q_seq, q_seq, H, G, D, FULL, BF16)
+    ro, _ = orc.forward(q.numpy(), k.numpy(), v.numpy(), q_seq, q_seq, H, G, D, FULL)
+    assert_out_close(out, ro, BF16, float(v.abs().max()), "mixed-magnitude tile")

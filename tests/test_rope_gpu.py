@@ -68,7 +68,7 @@ def test_rope_shapes(cuda_lib, orc, prec, q_seq, kv_seq, H, G, D, mask, window, 
     check(cuda_lib, orc, q_seq, kv_seq, H, G, D, mask, prec, seed=q_seq + D, window=window, base=base)
 
 
-@pytest.mark.parametrize("prec,qk_sigma", [(FP32, 3.0), (TF32, 3.0), (BF16, 1.0)])
+@pytest.mark.parametrize("prec,qk_sigma", [(FP32, 3.0), (TF32, 3.0), (BF16, 3.0)])
 def test_rope_long_causal(cuda_lib, orc, prec, qk_sigma):
     """q_seq 8193, 32 heads over 8 kv heads, D=128: sampled rows up to position 8192."""
     rng = np.random.default_rng(3)

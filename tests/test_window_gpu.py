@@ -69,20 +69,29 @@ def long_rows(q_seq, w):
                   set(rng.integers(0, q_seq, 12).tolist()))
 
 
-@pytest.mark.parametrize("prec,qk_sigma", [(FP32, 3.0), (TF32, 3.0), (BF16, 1.0)])
-def test_forward_window_long_causal(cuda_lib, orc, prec, qk_sigma):
-    """q_seq 8193, 32 heads over 8 kv heads, D=128, window 4096: sampled rows.  Q,K
-    N(0,3^2) for fp32 and TF32; N(0,1) for bf16 operands (see the next test)."""
+@pytest.mark.parametrize("prec", PRECS)
+def test_forward_window_long_causal(cuda_lib, orc, prec):
+    """q_seq 8193, 32 heads over 8 kv heads, D=128, window 4096, Q,K N(0,3^2): sampled rows."""
     q_seq, w = 8193, 4096
     check_forward(cuda_lib, orc, q_seq, q_seq, 32, 8, 128, CAUSAL, prec, w, seed=8, rows=long_rows(q_seq, w),
-                  qk_sigma=qk_sigma)
+                  qk_sigma=3.0)
 
 
-def test_forward_window_long_causal_bf16_wide_scores(cuda_lib, orc):
-    """bf16 operands with Q,K N(0,3^2) (scores of standard deviation 9): rounding Q and K
-    to bf16 alone moves this sample by about 2.2e-2 max|V| (computed below in fp64 from
-    the rounded operands), beyond the 2e-2 bf16 target.  The kernel must match that
-    rounding model closely and stay within 2.5e-2 of the exact result."""
+def f16_scaled(x, axis_max):
+    """x * 2^(14 - E) rounded to fp16 and scaled back, with E the binary exponent of
+    axis_max (the largest magnitude of x's set), as the 16-bit path stores its
+    Q K^T operands."""
+    e = np.clip(np.floor(np.log2(np.maximum(axis_max, 1e-38))), -100, 127)
+    up = np.exp2(14.0 - e)
+    return (x * up).astype(np.float16).astype(np.float64) / up
+
+
+def test_forward_window_long_causal_bf16_operand_model(cuda_lib, orc):
+    """The 16-bit path computes what it states: Q and each 128-key K tile rounded to
+    fp16 under their own power of two, P and V rounded to bf16, fp32 accumulation.
+    An fp64 evaluation of that rounding model on the windowed 8193-row case with
+    Q,K N(0,3^2) (scores of standard deviation 9) must sit close to the kernel,
+    and both within the 2e-2 bound of the exact result."""
     q_seq, w, H, G, D = 8193, 4096, 32, 8, 128
     rows = long_rows(q_seq, w)
     q, k, v = synthetic.forward_inputs(q_seq, q_seq, H, G, D, seed=8, qk_sigma=3.0)
@@ -90,22 +99,30 @@ def test_forward_window_long_causal_bf16_wide_scores(cuda_lib, orc):
     ro, _ = orc.forward(q.numpy(), k.numpy(), v.numpy(), q_seq, q_seq, H, G, D, CAUSAL, rows=rows, window=w)
     vmax = float(v.abs().max())
     sl2 = np.float32(1.0 / math.sqrt(D)) * np.float32(math.log2(math.e))
-    rnd = lambda x: x.to(torch.bfloat16).to(torch.float64)  # noqa: E731
-    kb, vb = rnd(k.double()), rnd(v.double())
+    kn, vn = k.numpy(), v.numpy()
+    vb = v.to(torch.bfloat16).to(torch.float64).numpy()
+    # K tiles of 128 keys per kv head, each under its own power of two.
+    kq = np.empty(kn.shape, np.float64)
+    for t0 in range(0, q_seq, 128):
+        blk = kn[t0:t0 + 128].reshape(-1, G, D)
+        m = np.abs(blk).max(axis=(0, 2))                    # per kv head
+        kq[t0:t0 + 128] = f16_scaled(blk.astype(np.float64), m[None, :, None]).reshape(-1, G * D)
     model_err = kernel_err = 0.0
     for r in rows:
         lo = max(0, r + 1 - w)
         for h in range(H):
             g = h // (H // G)
-            qs = rnd((q[r, h * D:(h + 1) * D] * sl2).double())
-            s = kb[lo:r + 1, g * D:(g + 1) * D] @ qs
-            p = torch.exp2(s - s.max())
-            o = ((rnd(p) @ vb[lo:r + 1, g * D:(g + 1) * D]) / p.sum()).numpy()
+            qs = (q[r, h * D:(h + 1) * D].numpy() * sl2).astype(np.float32).astype(np.float64)
+            qr = f16_scaled(qs, np.abs(qs).max())
+            s = kq[lo:r + 1, g * D:(g + 1) * D] @ qr
+            p = np.exp2(s - s.max())
+            pb = torch.from_numpy(p).to(torch.bfloat16).to(torch.float64).numpy()
+            o = (pb @ vb[lo:r + 1, g * D:(g + 1) * D]) / p.sum()
             model_err = max(model_err, np.abs(o - ro[r, h * D:(h + 1) * D]).max())
             kernel_err = max(kernel_err, np.abs(out[r, h * D:(h + 1) * D] - o).max())
-    assert model_err / vmax > 2e-2          # the sample really is beyond the target
+    assert model_err / vmax < 2e-2
     assert kernel_err / vmax < 3e-3, kernel_err / vmax
-    assert np.abs(out[rows] - ro[rows]).max() / vmax < 2.5e-2
+    assert np.abs(out[rows] - ro[rows]).max() / vmax < 2e-2
 
 
 @pytest.mark.parametrize("prec", PRECS)

@@ -1,4 +1,4 @@
-"""attn_decode_cached_noalloc through the C ABI, against attn_decode_cached.
+"""attn_decode_cached_noalloc through the C ABI, against attn_decode_cached and the oracle.
 
 The no-allocation decode is for callers that cannot give the library device
 scratch memory (a plugin inside a framework that owns every allocation, a
@@ -29,8 +29,9 @@ def c_noalloc(lib):
 @pytest.mark.parametrize("H,G,D,max_seq,positions", [
     (32, 8, 128, 16384, [16383, 511]),   # the decode benchmark shape, then a short window
     (16, 2, 64, 3000, [2999, 64]),
+    (32, 2, 128, 4096, [4095, 100]),     # 16 query heads per kv head: four head groups per kv head
 ])
-def test_noalloc_matches_workspace_decode(cuda_lib, H, G, D, max_seq, positions):
+def test_noalloc_matches_workspace_decode_and_oracle(cuda_lib, orc, H, G, D, max_seq, positions):
     lib = cuda_lib.load_library()
     noalloc = c_noalloc(lib)
     q, kc, vc = synthetic.decode_inputs(max_seq, H, G, D, seed=11)
@@ -43,6 +44,7 @@ def test_noalloc_matches_workspace_decode(cuda_lib, H, G, D, max_seq, positions)
         pos.fill_(kv_pos)
         ref = torch.full((1, H * D), float("nan"), device="cuda")
         cuda_lib.attn_decode_cached(dq, dk, dv, pos, ref, H, G, D, max_seq, ws)
+        exact = orc.decode(q.numpy(), kc.numpy(), vc.numpy(), kv_pos, H, G, D, max_seq)
         for call in range(2):  # two calls in a row share (and reuse) the fixed scratch
             out = torch.full((1, H * D), float("nan"), device="cuda")
             rc = noalloc(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), pos.data_ptr(), out.data_ptr(),
@@ -50,15 +52,28 @@ def test_noalloc_matches_workspace_decode(cuda_lib, H, G, D, max_seq, positions)
             assert rc == 0, cuda_lib.attn_status_string(rc)
             torch.cuda.synchronize()
             assert cuda_lib.attn_get_status() == 0
-            assert_out_close(out.cpu().numpy(), ref.cpu().numpy(), FP32, vmax,
-                             "noalloc call %d at kv_pos %d" % (call, kv_pos))
+            got = out.cpu().numpy()
+            where = "noalloc call %d at kv_pos %d" % (call, kv_pos)
+            assert_out_close(got, ref.cpu().numpy(), FP32, vmax, where + " vs workspace decode")
+            assert_out_close(got, exact, FP32, vmax, where + " vs oracle")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
+    """Real (small) buffers throughout, so that even a call that wrongly went
+    ahead would stay inside its allocations."""
     lib = cuda_lib.load_library()
     noalloc = c_noalloc(lib)
-    fake = 1 << 20  # aligned, never dereferenced: the call must refuse before launching
-    # 16384 heads over 4096 kv heads at D = 128 need about 8 MiB of scratch.
-    rc = noalloc(fake, fake, fake, fake, fake, 16384, 4096, 128, 1 << 16, None)
+    # 16384 heads over 4096 kv heads at D = 128 need about 8.5 MiB of scratch
+    # with a one-row cache (one split per head group).
+    H, G, D, max_seq = 16384, 4096, 128, 1
+    q = torch.zeros(H * D, device="cuda")
+    out = torch.zeros(H * D, device="cuda")
+    kc = torch.zeros(max_seq * G * D, device="cuda")
+    vc = torch.zeros(max_seq * G * D, device="cuda")
+    pos = torch.zeros(4, dtype=torch.int32, device="cuda")
+    ptrs = [x.data_ptr() for x in (q, kc, vc, pos, out)]
+    rc = noalloc(*ptrs, H, G, D, max_seq, None)
     assert rc == cuda_lib.ATTN_ERR_UNSUPPORTED
-    assert noalloc(0, fake, fake, fake, fake, 32, 8, 128, 16384, None) == cuda_lib.ATTN_ERR_INVALID_ARG
+    assert noalloc(0, *ptrs[1:], 32, 8, 128, max_seq, None) == cuda_lib.ATTN_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert cuda_lib.attn_get_status() == 0
