@@ -23,10 +23,12 @@
 // A pre-pass writes K as fp16 (with the tile factors) and V as bf16, in
 // their own layout; Q is converted inside the kernel.
 //
-// One CTA owns 128 packed rows of one kv head g: row r is (query i, head
-// g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs query
-// heads that share it.  Keys are walked in tiles of 128, from the tile holding
-// the block's first kept key to the one holding its last.  Three score buffers
+// One CTA owns the packed rows of 128/gs queries of one kv head g (rpb =
+// (128/gs)*gs of its 128 MMA rows; the rest idle when gs does not divide
+// 128): row r is (query i, head g*gs + j) with i*gs + j = rpb*block + r, so
+// each K/V tile feeds all gs query heads that share it.  Keys are walked in
+// tiles of 128, from the tile holding the block's first kept key to the one
+// holding its last.  Three score buffers
 // in tensor memory let Q K^T run up to three tiles ahead of P V, so the
 // softmax of one tile overlaps the products of the others.  The two softmax
 // warpgroups split every tile's columns (64 each) and swap their partial row
@@ -70,6 +72,7 @@ constexpr int kMaxRing = 12;
 constexpr int kSBuf = 3;                   // score buffers
 constexpr int kColO = 384;                 // S_b at 128 b; O at 384
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kFacCache = 512;             // K tile powers of two a CTA keeps in shared memory
 
 struct __align__(1024) Bf16Smem {
   unsigned char operands[kOperandBytes];  // [Q tile][ring slots]
@@ -83,7 +86,9 @@ struct __align__(1024) Bf16Smem {
   uint64_t o_final;        // every P V has completed
   uint64_t drain[2];
   float red_max[2][2][kRows];  // [tile parity][group][row] partial tile maxima
-  float red_l[2][kRows];       // [group][row] partial row sums (epilogue)
+  float red_l[2][kRows];       // [group][row] partial row maxima of Q, then partial row sums
+  float kfac[kFacCache];       // powers of two of the CTA's K tiles jt0, jt0 + 1, ...
+  long long row_off[kRows];    // output offset of each packed row (-1: no row)
   uint32_t tmem_base;
   int abort;
 };
@@ -92,7 +97,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_bf16_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
-                      const float* __restrict__ kfac) {
+                      const float* __restrict__ kfac, int early_q) {
   constexpr int kChunks = D / 64;                // 128-byte (64-element) column chunks of a K row
   constexpr int kChunkBytes = kKeys * 128;       // one K box: 128 keys x 128 bytes
   constexpr int kTileBytes = kChunks * kChunkBytes;
@@ -111,12 +116,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* const qstage = reinterpret_cast<const float*>(ring + 3 * kTileBytes);
 
   allow_dependent_launch();
-  grid_dependency_wait();
+  // With the pre-pass launched just before (early_q), everything up to the
+  // first K/V copy -- set-up and the Q block, which the pre-pass does not
+  // write -- overlaps its tail: the pre-pass lets this grid start only once it
+  // has itself waited for the kernels before it.  Each thread that reads what
+  // the pre-pass wrote, or writes the outputs, waits for it first.
+  if (!early_q) grid_dependency_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y;
   const int blk = gridDim.x - 1 - blockIdx.x;  // heaviest causal blocks first
   const int gs = a.H / a.G;
-  const int qpb = kRows / gs;
+  const int qpb = kRows / gs;                  // queries per block
+  const int rpb = qpb * gs;                    // packed rows used (rows rpb..127 idle when gs does not divide 128)
   const long long i0 = (long long)blk * qpb;
   auto window = [&](long long i) -> int {
     if (i < 0 || i >= a.n_q) return 0;
@@ -164,8 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(&sm.q_full, (unsigned)(kRows * D * 4));
+      mbar_arrive_expect_tx(&sm.q_full, (unsigned)(rpb * D * 4));
       tma_load_3d(ring + 3 * kTileBytes, &tm_q, 0, g * gs, (int)i0, &sm.q_full);
+      if (early_q) grid_dependency_wait();  // the K/V copies are the pre-pass's output
       int p = 0;  // copies issued; copy p goes to ring slot p % kRing
       auto load = [&](bool is_v, int j) {
         const int s = p % kRing, use = p / kRing;
@@ -261,12 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = (warp - 4) >> 2;           // column group 0 or 1
     const int r = 32 * (warp & 3) + lane;      // row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const long long packed = (long long)blk * kRows + r;
-    const long long qi = packed / gs;
-    const int h = g * gs + (int)(packed % gs);
-    const int n_r = window(qi);
+    const long long qi = i0 + r / gs;         // packed row blk * rpb + r
+    const int h = g * gs + r % gs;
+    const bool row_ok = r < rpb && qi < a.n_q;
+    if (grp == 0) sm.row_off[r] = row_ok ? qi * a.out_row_stride + (long long)h * D : -1;
+    const int n_r = row_ok ? window(qi) : 0;
     const int lo_r = first_key(n_r, a.window);
-    const bool row_ok = qi < a.n_q;
     const float sl2 = a.scale * kLog2e;
 
     // Q row, pre-scaled by scale * log2(e), as fp16 into the K-major operand
@@ -289,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < kQF4; ++i) {
         const int f = (i + r) % kQF4;
         const int e = grp * (D / 2) + 4 * f;  // first element of this float4
-        float4 x = *reinterpret_cast<const float4*>(qrow + e);
+        float4 x = r < rpb ? *reinterpret_cast<const float4*>(qrow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
         if (cs != nullptr) {
           const int dd = grp == 0 ? e : e - D / 2;  // pair index
           const float4 y = *reinterpret_cast<const float4*>(qrow + (grp == 0 ? e + D / 2 : dd));
@@ -322,18 +334,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.q_ready);
+    if (early_q) grid_dependency_wait();
+    // The K tiles' powers of two (the pre-pass's output), read once.
+    for (int i = 32 * (warp - 4) + lane; i < min(nt, kFacCache); i += kSoftmaxThreads)
+      sm.kfac[i] = kfac[(long long)(jt0 + i) * a.G + g];
+    named_barrier(2, kSoftmaxThreads);
 
     const uint32_t o_col = tmem + lane_base + kColO;
     constexpr int kHalfD = D / 2;  // O columns per group
     float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
-    // Power of two of K tile jt0 + j of this kv head, read one tile ahead.
-    float f_next = nt > 0 ? __ldg(kfac + (long long)jt0 * a.G + g) : 1.f;
+    // The power of two of K tile jt0 + j of this kv head, read one tile ahead.
+    auto tile_fac = [&](int j) {
+      return j < kFacCache ? sm.kfac[j] : __ldg(kfac + (long long)(jt0 + j) * a.G + g);
+    };
+    float f_next = nt > 0 ? tile_fac(0) : 1.f;
     for (int j = 0; j < nt; ++j) {
       const int b = j % kSBuf;
       const uint32_t s_col = tmem + lane_base + kKeys * b + 64 * grp;
       // Raw score -> base-2 units (at least FLT_MIN, so a masked -inf stays -inf).
       const float cf = fmaxf(f_row * f_next, FLT_MIN);
-      if (j + 1 < nt) f_next = __ldg(kfac + (long long)(jt0 + j + 1) * a.G + g);
       mbar_wait_bounded(&sm.s_full[b], (unsigned)((j / kSBuf) & 1), a.status, &sm.abort);
       tc::fence_after_sync();
       uint32_t s[2][32];
@@ -369,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sm.red_max[j & 1][grp][r] = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       named_barrier(1, kSoftmaxThreads);  // both halves of every row are read and maxed
       const float tmax = cf * fmaxf(sm.red_max[j & 1][0][r], sm.red_max[j & 1][1][r]);
+      if (j + 1 < nt) f_next = tile_fac(j + 1);
       m_true = fmaxf(m_true, tmax);
       const float m_prev = m_ref;
       if (tmax > m_ref + kRescaleThreshold) m_ref = tmax;  // also for the first finite tile max
@@ -456,17 +476,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       constexpr int kLanesPerRow = kHalfD / 4;
       constexpr int kRowsPerStore = 32 / kLanesPerRow;
-      const int lg = __ffs(gs) - 1;  // gs is a power of two
       const int u = lane % kLanesPerRow;
 #pragma unroll 4
       for (int i = 0; i < 32 / kRowsPerStore; ++i) {
         const int t = kRowsPerStore * i + lane / kLanesPerRow;  // row within the warp
-        const long long pk = (long long)blk * kRows + 32 * (warp & 3) + t;
-        const long long qq = pk >> lg;
-        if (qq < a.n_q) {
+        const long long off = sm.row_off[32 * (warp & 3) + t];
+        if (off >= 0) {
           const float4 v = *reinterpret_cast<const float4*>(stage + t * kHalfD + 4 * (u ^ (t & 7)));
-          *reinterpret_cast<float4*>(a.out + qq * a.out_row_stride + (long long)(g * gs + (int)(pk & (gs - 1))) * D +
-                                     grp * kHalfD + 4 * u) = v;
+          *reinterpret_cast<float4*>(a.out + off + grp * kHalfD + 4 * u) = v;
         }
       }
     }
@@ -490,8 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 int launch_d(const FlashArgs& a, cudaStream_t s) {
   const int gs = a.H / a.G;
-  const long long rows = (long long)a.n_q * gs;
-  const long long nb = (rows + kRows - 1) / kRows;
+  const int qpb = kRows / gs;  // queries per 128-row block
+  const long long nb = ((long long)a.n_q + qpb - 1) / qpb;
   if (nb == 0) return 0;
   // Rows of K/V any CTA may read: the largest window of the call.  Rows past
   // it are outside the tensor maps and arrive as zeros.
@@ -536,7 +553,6 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
     pa.page_rows = a.page_rows;
     pa.num_pages = a.num_pages;
     pa.status = a.status;
-    pa.mode = kPrepF16Scaled;
     const cudaError_t e = launch_kv_prep(pa, s);
     if (e != cudaSuccess) {
       scratch_free(scratch, s);
@@ -551,7 +567,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   // one CTA's block, D x gs heads x 128/gs queries; rows past n_q read as 0.
   const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)a.H, (uint64_t)a.n_q};
   const uint64_t qstrides[2] = {(uint64_t)D * 4, (uint64_t)a.q_row_stride * 4};
-  const uint32_t qbox[3] = {(uint32_t)D, (uint32_t)gs, (uint32_t)(kRows / gs)};
+  const uint32_t qbox[3] = {(uint32_t)D, (uint32_t)gs, (uint32_t)qpb};
   // K and V: [kv_rows][kv_row_stride] 16-bit, boxes of 64 elements x 128 keys.
   const uint64_t dims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
   const uint64_t strides[1] = {(uint64_t)a.kv_row_stride * 2};
@@ -569,7 +585,8 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
       rc = ATTN_ERR_CUDA;
     } else {
       FlashArgs aa = a;
-      void* args[] = {&aa, &tm_k, &tm_v, &tm_q, &kfac};
+      int early_q = kfac != nullptr ? 1 : 0;  // the pre-pass ran just before
+      void* args[] = {&aa, &tm_k, &tm_v, &tm_q, &kfac, &early_q};
       if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s,
                      args) != cudaSuccess)
         rc = ATTN_ERR_CUDA;

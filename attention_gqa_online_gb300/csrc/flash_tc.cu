@@ -12,29 +12,33 @@
 // Precision.  The scores enter the softmax through an exponential, so their
 // operand rounding dominates the error: with scores of standard deviation 9
 // (Q, K ~ N(0, 3^2), D = 128), TF32 Q and K (11 significant bits) move the
-// output by up to about 3.5e-3 max|V|.  Q K^T is therefore computed from a
-// split of both operands into bf16 pairs, x = hi + lo with hi = bf16(x) and
-// lo = bf16(x - hi) (16 or more significant bits), as the three products
-// Qhi Khi^T + Qhi Klo^T + Qlo Khi^T (the dropped Qlo Klo^T is below 2^-16 of
-// the score): about 1.5 times the tensor time of one TF32 product, and an
-// error near 5e-4 max|V|, set by P V.  P V uses TF32 operands: P (fp32 in
-// tensor memory) and the V tiles straight from the fp32 input.  A pre-pass
-// writes K's hi and lo parts (bf16, K's own layout); Q is split inside the
-// kernel.
+// output by up to about 3.5e-3 max|V|.  Q K^T is therefore computed with Q
+// kept to 22 significant bits: each query row, scaled by a power of two that
+// puts its largest magnitude in [2^14, 2^15), is split into fp16 hi + lo
+// (hi = fp16(x), lo = fp16(x - hi)), and K is one fp16 operand under a power
+// of two per 128-key tile of a kv head (the pre-pass); the two products
+// Qhi K^T + Qlo K^T accumulate in fp32 -- the tensor time of one TF32 product
+// -- and the two powers of two turn the raw score back in the softmax, as the
+// multiplier of the fma that subtracts the running max.  K's own rounding
+// (2^-11) leaves an error near 1.4e-3 max|V| on those inputs.  P V uses TF32
+// operands: P (fp32 in tensor memory) and the V tiles straight from the fp32
+// input.
 //
-// One CTA owns 128 packed rows of one kv head g: row r is (query i, head
-// g*gs + j) with i*gs + j = 128*block + r, so each K/V tile feeds all gs
-// query heads that share it.  Keys are walked in tiles of 128, from the tile
-// holding the block's first kept key to the one holding its last.
+// One CTA owns the packed rows of 128/gs queries of one kv head g (rpb =
+// (128/gs)*gs of its 128 MMA rows; the rest idle when gs does not divide
+// 128): row r is (query i, head g*gs + j) with i*gs + j = rpb*block + r, so
+// each K/V tile feeds all gs query heads that share it.  Keys are walked in
+// tiles of 128, from the tile holding the block's first kept key to the one
+// holding its last.
 //
 // Warp roles (384 threads):
-//   warp 0      TMA producer: K tile (hi then lo part, each 128 keys x D bf16,
-//               128-byte swizzle, K-major operand) and V tile (fp32, MN-major
+//   warp 0      TMA producer: K tile (128 keys x D fp16, 128-byte swizzle,
+//               K-major operand, in the first half of a slot) and V tile (fp32, MN-major
 //               operand, which for 32-bit elements needs the 128-byte swizzle
 //               of 32-byte atoms) into a 192 KB shared-memory ring three tiles
 //               deep, in the order the MMAs consume them.
 //   warp 1      tensor-memory allocation; issues S_(j%2) = Q K_j^T
-//               (A = Q hi / lo in TMEM, B = K hi / lo tile, M=128 N=128) once
+//               (A = Q hi / lo in TMEM, B = K tile, M=128 N=128) once
 //               P V of tile j-2 has released that buffer.
 //   warp 2      issues O += P_j V_j (A = P in TMEM over S_(j%2), B = V,
 //               M=128 N=D) in tile order once both softmax groups wrote P_j.
@@ -48,9 +52,9 @@
 //               half of O when the reference max moves, and finally writes its
 //               half of O / l; group 0 writes (max, log sum).
 // Tensor memory (512 columns): Q hi [0, D/2) and Q lo [D/2, D) as packed
-// bf16 pairs, two 128-column score buffers [128, 384), O [384, 384 + D).
-// Scores are in base-2 units: Q is pre-multiplied by scale * log2(e) before
-// it is split.  The reference max only moves when a row's tile max exceeds it
+// fp16 pairs, two 128-column score buffers [128, 384), O [384, 384 + D).
+// Scores are in base-2 units once scaled: Q is pre-multiplied by
+// scale * log2(e) before it is split.  The reference max only moves when a row's tile max exceeds it
 // by more than 8 (so P <= 256), which leaves the result exact and skips most
 // O rescales; the true max is tracked separately for the LSE.  Every wait is
 // bounded; a CTA whose pipeline breaks drains its copies and MMAs before it
@@ -75,6 +79,7 @@ constexpr int kColQ = 0, kColS0 = 128, kColO = 384;  // Q hi / lo in [0, 128); S
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 constexpr int kPageBox = 32;     // fewest key rows per TMA box of a paged cache (page_rows % 32 == 0)
 constexpr int kPageCache = 1024;  // block-table entries a CTA keeps in shared memory
+constexpr int kFacCache = 512;    // K tile powers of two a CTA keeps in shared memory
 
 // Key rows per TMA box of a paged cache with pages of page_rows rows.
 __host__ __device__ inline int page_box(int page_rows) {
@@ -94,22 +99,24 @@ struct __align__(1024) TcSmem {
   float red_max[2][2][kRows];  // [tile parity][group][row] partial tile maxima
   float red_l[2][kRows];       // [group][row] partial row sums (epilogue)
   uint32_t pages[kPageCache];  // block-table entries of the CTA's key range (paged caches)
+  long long row_off[kRows];    // output offset of each packed row (-1: no row)
+  float kfac[kFacCache];       // powers of two of the CTA's K tiles jt0, jt0 + 1, ...
   uint32_t tmem_base;
   int abort;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    flash_tc_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_kh,
-                    const __grid_constant__ CUtensorMap tm_kl, const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_q) {
+    flash_tc_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
+                    const float* __restrict__ kfac, int early_q) {
   constexpr int kEpr = 32;                     // fp32 elements per 128-byte row
   constexpr int kChunks = D / kEpr;            // 128-byte column chunks of an fp32 V (or Q) row
   constexpr int kChunkBytes = kKeys * 128;     // one TMA box: 128 keys x 128 bytes
   constexpr int kTileBytes = kChunks * kChunkBytes;
-  constexpr int kKChunks = D / 64;             // 128-byte column chunks of a bf16 K row
-  constexpr int kKHalf = kKChunks * kChunkBytes;  // the hi (then the lo) part of a K tile
-  static_assert(2 * kKHalf == kTileBytes, "a K tile (hi + lo) fills one ring slot");
+  constexpr int kKChunks = D / 64;             // 128-byte column chunks of an fp16 K row
+  constexpr int kKBytes = kKChunks * kChunkBytes;  // an fp16 K tile: the first half of a ring slot
+  static_assert(2 * kKBytes == kTileBytes, "ring slots hold an fp32 V tile");
   constexpr int kColQl = D / 2;                // Q lo after the D/2 columns of Q hi pairs
   constexpr int kRing = kRingBytes / kTileBytes;  // tiles in flight
   static_assert(kRing <= kMaxRing, "ring barriers");
@@ -126,12 +133,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Programmatic dependent launch: the next kernel may start launching; this
   // one touches no global memory before the previous kernel has completed.
   allow_dependent_launch();
-  grid_dependency_wait();
+  // With the pre-pass launched just before (early_q), everything up to the
+  // first K/V copy -- set-up and the Q block, which the pre-pass does not
+  // write -- overlaps its tail: the pre-pass lets this grid start only once it
+  // has itself waited for the kernels before it.  Each thread that reads what
+  // the pre-pass wrote, or writes the outputs, waits for it first.
+  if (!early_q) grid_dependency_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y;
   const int blk = gridDim.x - 1 - blockIdx.x;  // heaviest causal blocks first
   const int gs = a.H / a.G;
   const int qpb = kRows / gs;                  // queries per block
+  const int rpb = qpb * gs;                    // packed rows used (rows rpb..127 idle when gs does not divide 128)
   const long long i0 = (long long)blk * qpb;   // first query of the block
   const long long i1 = min((long long)a.n_q, i0 + qpb) - 1;  // last valid query
   auto window = [&](long long i) -> int {
@@ -182,12 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nt > 0) {
       prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_kh);
-      prefetch_tmap(&tm_kl);
+      prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(&sm.q_full, (unsigned)kTileBytes);
+      mbar_arrive_expect_tx(&sm.q_full, (unsigned)(rpb * D * 4));
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) tma_load_3d(qstage + c * kChunkBytes, &tm_q, kEpr * c, g * gs, (int)i0, &sm.q_full);
+      if (early_q) grid_dependency_wait();  // the K copies are the pre-pass's output
       // Copies go out in the order the MMA issuer consumes the tiles: K_0,
       // K_1, V_0, K_2, V_1, ..., K_(nt-1), V_(nt-2), V_(nt-1).  Ring slot
       // p % kRing holds copy p; it is refilled once its consumer completes.
@@ -196,17 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned char* dst = sm.ring + s * kTileBytes;
         if (p == 2) mbar_wait_bounded(&sm.q_ready, 0, a.status, &sm.abort);  // the staging slot is free again
         if (use >= 1) mbar_wait_bounded(&sm.kv_empty[s], (unsigned)((use - 1) & 1), a.status, &sm.abort);
-        mbar_arrive_expect_tx(&sm.kv_full[s], (unsigned)kTileBytes);
         const bool is_v = (p == 2 * nt - 1) || (p > 0 && (p & 1) == 0);
+        mbar_arrive_expect_tx(&sm.kv_full[s], (unsigned)(is_v ? kTileBytes : kKBytes));
         const int t0 = kKeys * (jt0 + (is_v ? (p == 2 * nt - 1 ? nt - 1 : p / 2 - 1) : (p + 1) / 2));
         if (!is_v) {
-          // K: the pre-pass's hi and lo parts (bf16, logical rows, also for a
-          // paged cache), 64-element column chunks.
+          // K: the pre-pass's fp16 copy (logical rows, also for a paged
+          // cache), 64-element column chunks.
 #pragma unroll
-          for (int c = 0; c < kKChunks; ++c) {
-            tma_load_2d(dst + c * kChunkBytes, &tm_kh, g * D + 64 * c, t0, &sm.kv_full[s]);
-            tma_load_2d(dst + kKHalf + c * kChunkBytes, &tm_kl, g * D + 64 * c, t0, &sm.kv_full[s]);
-          }
+          for (int c = 0; c < kKChunks; ++c) tma_load_2d(dst + c * kChunkBytes, &tm_k, g * D + 64 * c, t0, &sm.kv_full[s]);
         } else if (a.block_table == nullptr) {
 #pragma unroll
           for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, &tm_v, g * D + kEpr * c, t0, &sm.kv_full[s]);
@@ -246,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // runs its loop (warp-uniform values); one elected lane issues each MMA
     // and commit.
     if (nt > 0) {
-      constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtBF16, false, kRows, kKeys);
+      constexpr uint32_t idesc_qk = tc::idesc_f32acc(tc::kFmtF16, false, kRows, kKeys);
       constexpr uint32_t idesc_pv = tc::idesc_f32acc(tc::kFmtTF32, true, kRows, D);
       // V (MN-major B): the 32-byte-atom layout, 4-row K groups 512 bytes apart.
       constexpr uint32_t kVStep = kKStep * 128;  // bytes of V rows per K step
@@ -269,22 +279,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(&sm.kv_full[p % kRing], p / kRing)) return false;
         if (j >= kSBuf && !wait(&sm.pv_done[b], (j - kSBuf) / kSBuf)) return false;
         tc::fence_after_sync();
-        const uint64_t dkh = dk0 + slot_off(p);
-        const uint64_t dkl = dkh + (uint64_t)(kKHalf >> 4);
+        const uint64_t dk = dk0 + slot_off(p);
         const uint32_t ds = tmem + kColS0 + kKeys * b;
-        // Four K steps (16 bf16, 32 bytes each) per 128-byte chunk of the K
-        // tile; Q takes 8 TMEM columns (16 packed bf16) per step.  Per chunk:
-        // Qhi Khi, Qhi Klo, Qlo Khi, all accumulating into S.
+        // Four K steps (16 fp16, 32 bytes each) per 128-byte chunk of the K
+        // tile; Q takes 8 TMEM columns (16 packed fp16) per step.  Per chunk:
+        // Qhi K and Qlo K, both accumulating into S.
 #pragma unroll
         for (int c4 = 0; c4 < kKChunks; ++c4) {
           const uint64_t c = (uint64_t)((c4 * kChunkBytes) >> 4);
           const uint32_t qh = tmem + kColQ + 32 * c4, ql = qh + kColQl;
-          tc::mma4_f16_ts(ds, qh, qh + 8, qh + 16, qh + 24, dkh + c, dkh + c + 2, dkh + c + 4, dkh + c + 6, idesc_qk,
+          tc::mma4_f16_ts(ds, qh, qh + 8, qh + 16, qh + 24, dk + c, dk + c + 2, dk + c + 4, dk + c + 6, idesc_qk,
                           c4 > 0 ? 1u : 0u);
-          tc::mma4_f16_ts(ds, qh, qh + 8, qh + 16, qh + 24, dkl + c, dkl + c + 2, dkl + c + 4, dkl + c + 6, idesc_qk,
-                          1u);
-          tc::mma4_f16_ts(ds, ql, ql + 8, ql + 16, ql + 24, dkh + c, dkh + c + 2, dkh + c + 4, dkh + c + 6, idesc_qk,
-                          1u);
+          tc::mma4_f16_ts(ds, ql, ql + 8, ql + 16, ql + 24, dk + c, dk + c + 2, dk + c + 4, dk + c + 6, idesc_qk, 1u);
         }
         tc::commit_elect(&sm.s_full[b]);
         tc::commit_elect(&sm.kv_empty[p % kRing]);
@@ -332,17 +338,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = (warp - 4) >> 2;           // column group 0 or 1
     const int r = 32 * (warp & 3) + lane;      // row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const long long packed = (long long)blk * kRows + r;
-    const long long qi = packed / gs;
-    const int h = g * gs + (int)(packed % gs);
-    const int n_r = window(qi);
+    const long long qi = i0 + r / gs;         // packed row blk * rpb + r
+    const int h = g * gs + r % gs;
+    const bool row_ok = r < rpb && qi < a.n_q;
+    if (grp == 0) sm.row_off[r] = row_ok ? qi * a.out_row_stride + (long long)h * D : -1;
+    const int n_r = row_ok ? window(qi) : 0;
     const int lo_r = first_key(n_r, a.window);
-    const bool row_ok = qi < a.n_q;
     const float sl2 = a.scale * kLog2e;
 
-    // Q row -> TMEM (pre-scaled, then split into bf16 hi and lo parts), two
-    // values per column; each group stores half the row, read from the
-    // staging slot (rows past n_q arrived as zeros).
+    // Q row -> TMEM: pre-scaled by scale * log2(e) and by the row's power of
+    // two (its largest magnitude into [2^14, 2^15)), then split into fp16 hi
+    // and lo parts, two values per column; each group converts half the row,
+    // read from the staging slot (rows past n_q arrived as zeros), and the two
+    // halves agree on the power of two through shared memory.
+    float f_row = 1.f;  // 2^(E_r - 14): turns this row's raw scores back
     if (nt > 0) {
       constexpr int kQCols = D / 2;
       mbar_wait_bounded(&sm.q_full, 0, a.status, &sm.abort);
@@ -350,35 +359,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       // qi at position base_pos + qi; rows past n_q are zeros and stay so).
       const float* cs = (a.rope != nullptr && row_ok) ? a.rope + (a.base_pos + qi) * D : nullptr;
       const float sgn = grp == 0 ? -1.f : 1.f;
+      float v[kQCols / 32][32];
+      float qmax = 0.f;
 #pragma unroll
       for (int c = 0; c < kQCols / 32; ++c) {
         const unsigned char* src = qstage + (grp * (kQCols / 32) + c) * kChunkBytes + r * 128;
         const unsigned char* other = qstage + ((1 - grp) * (kQCols / 32) + c) * kChunkBytes + r * 128;
-        uint32_t v[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          float4 x = *reinterpret_cast<const float4*>(src + 16 * (u ^ (r & 7)));
+          float4 x = r < rpb ? *reinterpret_cast<const float4*>(src + 16 * (u ^ (r & 7))) : make_float4(0.f, 0.f, 0.f, 0.f);
           if (cs != nullptr) {
-            const float4 y = *reinterpret_cast<const float4*>(other + 16 * (u ^ (r & 7)));
+            const float4 y = r < rpb ? *reinterpret_cast<const float4*>(other + 16 * (u ^ (r & 7)))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
             const float4 cv = *reinterpret_cast<const float4*>(cs + 32 * c + 4 * u);
             const float4 sv = *reinterpret_cast<const float4*>(cs + kQCols + 32 * c + 4 * u);
             x = make_float4(fmaf(sgn * y.x, sv.x, x.x * cv.x), fmaf(sgn * y.y, sv.y, x.y * cv.y),
                             fmaf(sgn * y.z, sv.z, x.z * cv.z), fmaf(sgn * y.w, sv.w, x.w * cv.w));
           }
-          v[4 * u] = __float_as_uint(x.x * sl2);
-          v[4 * u + 1] = __float_as_uint(x.y * sl2);
-          v[4 * u + 2] = __float_as_uint(x.z * sl2);
-          v[4 * u + 3] = __float_as_uint(x.w * sl2);
+          v[c][4 * u] = x.x * sl2;
+          v[c][4 * u + 1] = x.y * sl2;
+          v[c][4 * u + 2] = x.z * sl2;
+          v[c][4 * u + 3] = x.w * sl2;
+          qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(v[c][4 * u]), fabsf(v[c][4 * u + 1])),
+                                   fmaxf(fabsf(v[c][4 * u + 2]), fabsf(v[c][4 * u + 3]))));
         }
-        // Element pairs (2i, 2i+1) of the chunk: hi = bf16 of each, lo = bf16
+      }
+      sm.red_l[grp][r] = qmax;
+      named_barrier(1, kSoftmaxThreads);
+      const int er = pow2_scale_exp(fmaxf(sm.red_l[0][r], sm.red_l[1][r]));
+      const float up = pow2f(14 - er);
+      f_row = pow2f(er - 14);
+#pragma unroll
+      for (int c = 0; c < kQCols / 32; ++c) {
+        // Element pairs (2i, 2i+1) of the chunk: hi = fp16 of each, lo = fp16
         // of what hi leaves (exact in fp32).  Pair i goes to column i.
         uint32_t hi[32], lo[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float x0 = __uint_as_float(v[2 * i]), x1 = __uint_as_float(v[2 * i + 1]);
-          const uint32_t h = tc::pack_bf16(x0, x1);
+          const float y0 = v[c][2 * i] * up, y1 = v[c][2 * i + 1] * up;
+          const uint32_t h = tc::pack_f16(y0, y1);
+          const float2 hf = tc::unpack_f16(h);
           hi[i] = h;
-          lo[i] = tc::pack_bf16(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xffff0000u));
+          lo[i] = tc::pack_f16(y0 - hf.x, y1 - hf.y);
         }
         const uint32_t qcol = tmem + lane_base + kColQ + (grp * kQCols + 32 * c) / 2;
         tc::tmem_st16(qcol, hi);
@@ -391,6 +413,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.q_ready);
     }
+    if (early_q) grid_dependency_wait();  // the pre-pass's output; before the outputs are written
+    // The K tiles' powers of two (the pre-pass's output), read once.
+    for (int i = 32 * (warp - 4) + lane; i < min(nt, kFacCache); i += kSoftmaxThreads)
+      sm.kfac[i] = kfac[(long long)(jt0 + i) * a.G + g];
+    named_barrier(2, kSoftmaxThreads);
+    auto tile_fac = [&](int j) {
+      return j < kFacCache ? sm.kfac[j] : __ldg(kfac + (long long)(jt0 + j) * a.G + g);
+    };
+    float f_next = nt > 0 ? tile_fac(0) : 1.f;
 
     constexpr int kCols = kKeys / 2;           // score columns per group per tile
     constexpr int kCC = kCols / 32;            // 32-column TMEM loads per group per tile
@@ -398,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nt; ++j) {
       const int b = j % kSBuf;
       const uint32_t s_col = tmem + lane_base + kColS0 + kKeys * b + kCols * grp;
+      // Raw score -> base-2 units (at least FLT_MIN, so a masked -inf stays -inf).
+      const float cf = fmaxf(f_row * f_next, FLT_MIN);
       mbar_wait_bounded(&sm.s_full[b], (unsigned)((j / kSBuf) & 1), a.status, &sm.abort);
       tc::fence_after_sync();
       uint32_t s[kCC][32];
@@ -434,7 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx[k] = max3(mx[k], __uint_as_float(s[i >> 5][(i & 31) + 2 * k]), __uint_as_float(s[i >> 5][(i & 31) + 2 * k + 1]));
       sm.red_max[j & 1][grp][r] = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       named_barrier(1, kSoftmaxThreads);
-      const float tmax = fmaxf(sm.red_max[j & 1][0][r], sm.red_max[j & 1][1][r]);
+      const float tmax = cf * fmaxf(sm.red_max[j & 1][0][r], sm.red_max[j & 1][1][r]);
+      if (j + 1 < nt) f_next = tile_fac(j + 1);
       m_true = fmaxf(m_true, tmax);
       float corr = 1.f;
       if (tmax > m_ref + kRescaleThreshold) {  // also true for the first finite tile max
@@ -451,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float x0 = __uint_as_float(s[c][e]), x1 = __uint_as_float(s[c][e + 1]);
-          add2(x0, x1, neg_m, neg_m);
+          fma2(x0, x1, cf, cf, neg_m, neg_m);
           const float p0 = ex2(x0), p1 = ex2(x1);
           const int k = (e >> 1) & 3;
           add2(sum[2 * k], sum[2 * k + 1], p0, p1);
@@ -526,17 +560,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       constexpr int kLanesPerRow = kHalfD / 4;
       constexpr int kRowsPerStore = 32 / kLanesPerRow;
-      const int lg = __ffs(gs) - 1;  // gs is a power of two
       const int u = lane % kLanesPerRow;
 #pragma unroll 4
       for (int i = 0; i < 32 / kRowsPerStore; ++i) {
         const int t = kRowsPerStore * i + lane / kLanesPerRow;  // row within the warp
-        const long long pk = (long long)blk * kRows + 32 * (warp & 3) + t;
-        const long long qq = pk >> lg;
-        if (qq < a.n_q) {
+        const long long off = sm.row_off[32 * (warp & 3) + t];
+        if (off >= 0) {
           const float4 v = *reinterpret_cast<const float4*>(stage + t * kHalfD + 4 * (u ^ (t & 7)));
-          *reinterpret_cast<float4*>(a.out + qq * a.out_row_stride + (long long)(g * gs + (int)(pk & (gs - 1))) * D +
-                                     grp * kHalfD + 4 * u) = v;
+          *reinterpret_cast<float4*>(a.out + off + grp * kHalfD + 4 * u) = v;
         }
       }
     }
@@ -557,13 +588,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
-
 template <int D>
 int launch_d(const FlashArgs& a, cudaStream_t s) {
   const int gs = a.H / a.G;
-  const long long rows = (long long)a.n_q * gs;
-  const long long nb = (rows + kRows - 1) / kRows;
+  const int qpb = kRows / gs;  // queries per 128-row block
+  const long long nb = ((long long)a.n_q + qpb - 1) / qpb;
   if (nb == 0) return 0;
   // Logical K/V rows any CTA may read: the largest window of the call.  Rows
   // past it are outside the tensor maps and arrive as zeros.  A paged V is
@@ -576,50 +605,54 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const long long v_rows = (paged && !no_keys) ? (long long)a.num_pages * a.page_rows : kv_rows;
   // An empty key set never reads K/V: any aligned base will do.
   const void* khp = a.q;
-  const void* klp = a.q;
   const void* vp = no_keys ? static_cast<const void*>(a.q) : a.v;
   void* scratch = nullptr;
+  uint16_t* kh16 = nullptr;
+  const float* kfac = nullptr;
   if (!no_keys) {
-    // K's bf16 hi and lo parts (turned by RoPE, gathered from pages) in
-    // stream-ordered scratch memory (library pool), released on the same
-    // stream once the attention kernel has run.  Only tiles from the first
-    // one any CTA reads are written.
+    // K as fp16 with one power of two per (tile, kv head) (turned by RoPE,
+    // gathered from pages) in stream-ordered scratch memory (library pool),
+    // released on the same stream once the attention kernel has run.  Only
+    // tiles from the first one any CTA reads are written.
     const long long elems = kv_rows * a.kv_row_stride;
     const int n_first = a.causal ? (int)min((long long)a.cap, a.base_pos + 1) : a.n_all;  // window of query 0
-    if (scratch_alloc(&scratch, (size_t)elems * 4, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    uint16_t* kh = static_cast<uint16_t*>(scratch);
+    const size_t fac_off = ((size_t)elems * 2 + 255) / 256 * 256;
+    const size_t fac_bytes = (size_t)((kv_rows + kKeys - 1) / kKeys) * a.G * sizeof(float);
+    if (scratch_alloc(&scratch, fac_off + fac_bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    const int n_tiles = (int)((kv_rows + kKeys - 1) / kKeys);
+    kh16 = static_cast<uint16_t*>(scratch);
+    kfac = reinterpret_cast<float*>(static_cast<char*>(scratch) + fac_off);
     PrepArgs pa{};
     pa.k = a.k;
     pa.v = a.v;
-    pa.out0 = kh;
-    pa.out1 = kh + elems;
+    pa.out0 = kh16;
+    pa.out1 = nullptr;  // V is read as it is
+    pa.kfac = const_cast<float*>(kfac);
     pa.stride = a.kv_row_stride;
     pa.G = a.G;
     pa.D = D;
     pa.tile0 = first_key(n_first, a.window) / kKeys;
-    pa.n_tiles = (int)((kv_rows + kKeys - 1) / kKeys);
+    pa.n_tiles = n_tiles;
     pa.rows_end = kv_rows;
     pa.rope = a.rope;
     pa.table = a.block_table;
     pa.page_rows = a.page_rows;
     pa.num_pages = a.num_pages;
     pa.status = a.status;
-    pa.mode = kPrepBf16Split;
     if (launch_kv_prep(pa, s) != cudaSuccess) {
       scratch_free(scratch, s);
       return ATTN_ERR_CUDA;
     }
-    khp = pa.out0;
-    klp = pa.out1;
+    khp = kh16;
   }
-  CUtensorMap tm_kh, tm_kl, tm_v, tm_q;
+  CUtensorMap tm_k, tm_v, tm_q;
   // Q: fp32 [n_q][H][D] (query rows q_row_stride floats apart); one CTA's
   // block is D/32 boxes of 32 floats x gs heads x 128/gs queries, rows past
   // n_q read as 0.
   const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)a.H, (uint64_t)a.n_q};
   const uint64_t qstrides[2] = {(uint64_t)D * 4, (uint64_t)a.q_row_stride * 4};
-  const uint32_t qbox[3] = {32, (uint32_t)gs, (uint32_t)(kRows / gs)};
-  // K hi / lo: [kv_rows][kv_row_stride] bf16, boxes of 64 elements x 128 keys.
+  const uint32_t qbox[3] = {32, (uint32_t)gs, (uint32_t)qpb};
+  // K: [kv_rows][kv_row_stride] fp16, boxes of 64 elements x 128 keys.
   const uint64_t kdims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
   const uint64_t kstrides[1] = {(uint64_t)a.kv_row_stride * 2};
   const uint32_t kbox[2] = {64, (uint32_t)kKeys};
@@ -628,8 +661,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   const uint64_t vstrides[1] = {(uint64_t)a.kv_row_stride * 4};
   const uint32_t vbox[2] = {32, (uint32_t)(paged ? page_box(a.page_rows) : kKeys)};
   int rc = ATTN_OK;
-  if (!make_tmap(&tm_kh, khp, 2, kdims, kstrides, kbox, true, kSwizzle128) ||
-      !make_tmap(&tm_kl, klp, 2, kdims, kstrides, kbox, true, kSwizzle128) ||
+  if (!make_tmap(&tm_k, khp, 2, kdims, kstrides, kbox, true, kSwizzle128) ||
       !make_tmap(&tm_v, vp, 2, vdims, vstrides, vbox, false, kSwizzle128Atom32) ||
       !make_tmap(&tm_q, a.q, 3, qdims, qstrides, qbox, false, kSwizzle128)) {
     rc = ATTN_ERR_UNSUPPORTED;
@@ -640,7 +672,8 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
       rc = ATTN_ERR_CUDA;
     } else {
       FlashArgs aa = a;
-      void* args[] = {&aa, &tm_kh, &tm_kl, &tm_v, &tm_q};
+      int early_q = scratch != nullptr ? 1 : 0;  // the pre-pass ran just before
+      void* args[] = {&aa, &tm_k, &tm_v, &tm_q, &kfac, &early_q};
       if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s,
                      args) != cudaSuccess)
         rc = ATTN_ERR_CUDA;
@@ -658,7 +691,7 @@ bool flash_tc_supported(const FlashArgs& a, int prec) {
   if (a.D != 64 && a.D != 128) return false;
   if (a.G > 65535) return false;
   const int gs = a.H / a.G;
-  if (!is_pow2(gs) || gs > kRows) return false;
+  if (gs < 1 || gs > kRows) return false;
   const uintptr_t al = reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.out) |
                        reinterpret_cast<uintptr_t>(a.k) | reinterpret_cast<uintptr_t>(a.v);
   if (al % 16 != 0) return false;

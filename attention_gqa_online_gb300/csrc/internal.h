@@ -98,13 +98,10 @@ bool make_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dim
 // K/V operand pre-pass of the tensor-core kernels (kv_prep.cu).  One block
 // per (128-key tile T in [tile0, n_tiles), kv head g); rows at or past
 // rows_end are not written.  Paged caches through table (as FlashArgs), RoPE
-// on K through rope (the table of launch_rope_table).
-//   kPrepF16Scaled  out0 = K as fp16 times 2^(14 - E_T) (E_T: binary exponent
-//                   of the tile's largest magnitude, per kv head), kfac[T * G +
-//                   g] = 2^(E_T - 14); out1 = V as bf16.
-//   kPrepBf16Split  out0 = bf16(K), out1 = bf16(K - out0) (V is not read).
+// on K through rope (the table of launch_rope_table).  out0 = K as fp16 times
+// 2^(14 - E_T) (E_T: binary exponent of the tile's largest magnitude, per kv
+// head), kfac[T * G + g] = 2^(E_T - 14); if out1 is set, out1 = V as bf16.
 // Outputs keep the inputs' layout: rows of `stride` elements, head g at g*D.
-enum { kPrepF16Scaled = 0, kPrepBf16Split = 1 };
 struct PrepArgs {
   const float* k;
   const float* v;
@@ -119,7 +116,6 @@ struct PrepArgs {
   const uint32_t* table;
   int page_rows, num_pages;
   unsigned* status;
-  int mode;
 };
 cudaError_t launch_kv_prep(const PrepArgs& p, cudaStream_t s);
 

@@ -9,14 +9,11 @@
 // (rope != nullptr): K row t is turned at position t first.  Outputs keep the
 // inputs' layout (rows of `stride` elements, head g at column g * D).
 //
-// kPrepF16Scaled (the 16-bit kernel's operands):
-//   z = 0  K as fp16 times 2^(14 - E_T), E_T the binary exponent of the
-//          tile's (this head's) largest magnitude, so its values lie below
-//          2^15, inside fp16's range; kfac[T * G + g] = 2^(E_T - 14).
-//   z = 1  V as bf16.
-// kPrepBf16Split (the TF32 kernel's exact Q K^T):
-//   z = 0  K = hi + lo with hi = bf16(K) and lo = bf16(K - hi), 16 or more
-//          significant bits between them (K - hi is exact in fp32).
+// Operands: K as fp16 times 2^(14 - E_T), E_T the binary exponent of the
+// tile's (this head's) largest magnitude, so its values lie below 2^15, inside
+// fp16's range; kfac[T * G + g] = 2^(E_T - 14).  With out1 set, blocks of the
+// second grid layer (z = 1) also write V as bf16 (the 16-bit kernel's P V
+// operand; the TF32-class kernel reads V as it is).
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -26,13 +23,16 @@ namespace {
 
 constexpr int kPrepThreads = 512;
 
-template <int D, int Mode>
+template <int D>
 __global__ void __launch_bounds__(kPrepThreads, 2) kv_prep_kernel(const PrepArgs p) {
   constexpr int kPerRow = D / 4;                       // float4 groups per row of one head
   constexpr int kRowsPerPass = kPrepThreads / kPerRow;  // rows of the tile per pass of the block
   constexpr int kPasses = 128 / kRowsPerPass;
-  allow_dependent_launch();
+  // The attention kernel that follows may start once every block is past this
+  // wait: it reads Q (and the RoPE table, a block table) before waiting for
+  // this grid, and those were written, if at all, by kernels this wait covers.
   grid_dependency_wait();
+  allow_dependent_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.y;
   const bool is_k = blockIdx.z == 0;
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) kv_prep_kernel(const PrepArgs
       if (row >= 0) x[i] = *reinterpret_cast<const float4*>(src + row * p.stride + col);
     }
   }
-  if (!is_k) {  // V as bf16 (kPrepF16Scaled only)
+  if (!is_k) {  // V as bf16
 #pragma unroll
     for (int i = 0; i < kPasses; ++i) {
       const long long t = t_first + i * kRowsPerPass + rsub;
@@ -82,23 +82,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) kv_prep_kernel(const PrepArgs
                            fmaf(sg * y.z, sv.z, x[i].z * cv.z), fmaf(sg * y.w, sv.w, x[i].w * cv.w));
       }
     }
-    if (Mode == kPrepF16Scaled)
-      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x[i].x), fabsf(x[i].y)), fmaxf(fabsf(x[i].z), fabsf(x[i].w))));
-  }
-  if (Mode == kPrepBf16Split) {
-#pragma unroll
-    for (int i = 0; i < kPasses; ++i) {
-      const long long t = t_first + i * kRowsPerPass + rsub;
-      if (t < p.rows_end) {
-        const uint32_t h01 = tc::pack_bf16(x[i].x, x[i].y), h23 = tc::pack_bf16(x[i].z, x[i].w);
-        const float4 h = make_float4(__uint_as_float(h01 << 16), __uint_as_float(h01 & 0xffff0000u),
-                                     __uint_as_float(h23 << 16), __uint_as_float(h23 & 0xffff0000u));
-        *reinterpret_cast<uint2*>(p.out0 + t * p.stride + col) = make_uint2(h01, h23);
-        *reinterpret_cast<uint2*>(p.out1 + t * p.stride + col) =
-            make_uint2(tc::pack_bf16(x[i].x - h.x, x[i].y - h.y), tc::pack_bf16(x[i].z - h.z, x[i].w - h.w));
-      }
-    }
-    return;
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x[i].x), fabsf(x[i].y)), fmaxf(fabsf(x[i].z), fabsf(x[i].w))));
   }
   // Largest magnitude of the tile: warp maxima, then the block's.
   __shared__ float wmax[kPrepThreads / 32];
@@ -121,22 +105,20 @@ __global__ void __launch_bounds__(kPrepThreads, 2) kv_prep_kernel(const PrepArgs
   }
 }
 
-template <int D, int Mode>
-cudaError_t launch_mode(const PrepArgs& p, cudaStream_t s) {
+template <int D>
+cudaError_t launch_d(const PrepArgs& p, cudaStream_t s) {
   PrepArgs pp = p;
   void* args[] = {&pp};
-  const dim3 grid((unsigned)(p.n_tiles - p.tile0), (unsigned)p.G, Mode == kPrepF16Scaled ? 2u : 1u);
-  return launch_pdl(reinterpret_cast<const void*>(kv_prep_kernel<D, Mode>), grid, dim3(kPrepThreads), 0, s, args);
+  const dim3 grid((unsigned)(p.n_tiles - p.tile0), (unsigned)p.G, p.out1 != nullptr ? 2u : 1u);
+  return launch_pdl(reinterpret_cast<const void*>(kv_prep_kernel<D>), grid, dim3(kPrepThreads), 0, s, args);
 }
 
 }  // namespace
 
 cudaError_t launch_kv_prep(const PrepArgs& p, cudaStream_t s) {
   if (p.n_tiles <= p.tile0) return cudaSuccess;
-  if (p.D == 128)
-    return p.mode == kPrepF16Scaled ? launch_mode<128, kPrepF16Scaled>(p, s) : launch_mode<128, kPrepBf16Split>(p, s);
-  if (p.D == 64)
-    return p.mode == kPrepF16Scaled ? launch_mode<64, kPrepF16Scaled>(p, s) : launch_mode<64, kPrepBf16Split>(p, s);
+  if (p.D == 128) return launch_d<128>(p, s);
+  if (p.D == 64) return launch_d<64>(p, s);
   return cudaErrorInvalidValue;
 }
 

@@ -163,6 +163,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
       : ATTN_R8(0), ATTN_R8(8), ATTN_R8(16), ATTN_R8(24)
       : "r"(taddr));
 }
+// The first 16 of v from 16 consecutive columns (v[16..31] are left as is).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : ATTN_R8(0), ATTN_R8(8)
+      : "r"(taddr));
+}
 #undef ATTN_R8
 #define ATTN_W8(i) "r"(v[i]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3]), "r"(v[i + 4]), "r"(v[i + 5]), \
                    "r"(v[i + 6]), "r"(v[i + 7])
@@ -190,6 +198,9 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void reg_fence(uint32_t (&v)[32]) {
   asm volatile("" : ATTN_F8(0), ATTN_F8(8), ATTN_F8(16), ATTN_F8(24)::"memory");
 }
+__device__ __forceinline__ void reg_fence16(uint32_t (&v)[32]) {
+  asm volatile("" : ATTN_F8(0), ATTN_F8(8)::"memory");
+}
 #undef ATTN_F8
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -199,6 +210,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// The two fp16 halves of a word as floats (lo = bits 0-15).
+__device__ __forceinline__ float2 unpack_f16(uint32_t v) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(v));
+  return make_float2(lo, hi);
 }
 
 // Two floats as round-to-nearest-even fp16 in one word: lo in bits 0-15.

@@ -23,12 +23,19 @@
  *   Data       fp32 in, fp32 out, row-major, all pointers are DEVICE memory
  *              owned by the caller.  The library keeps no pointer after a call
  *              returns.  The device memory it allocates is temporary scratch
- *              (the bf16 copies of the ATTN_BF16 paths, K turned for RoPE,
- *              the backward's per-row values): stream-ordered on the call's
- *              stream, from a memory pool the library creates per device and
- *              keeps (freed blocks stay reserved for later calls).  The
- *              backward also runs one of its kernels on a library-owned
- *              stream per device, forked from and joined back into `stream`.
+ *              (the 16-bit K/V operand copies of the tensor-core paths, K
+ *              turned for RoPE, the backward's per-row values): stream-ordered
+ *              on the call's stream, from a memory pool the library creates
+ *              per device and keeps (freed blocks stay reserved for later
+ *              calls).  Besides, every GPU that loads the library holds one
+ *              fixed 4 MiB array for attn_decode_cached_noalloc (shared by
+ *              all its calls on that device, kept until the process exits).
+ *              The backward also runs one of its kernels on a library-owned
+ *              stream per device, forked from and joined back into `stream`;
+ *              all callers on a device share that stream, so concurrent
+ *              backward calls on independent streams serialise there, and a
+ *              backward must not be captured into CUDA graphs from two
+ *              threads at once.
  *   Streams    every call is asynchronous on `stream` (a cudaStream_t; NULL is
  *              the legacy default stream).  Results are ready when the stream
  *              has reached the call.
@@ -44,15 +51,27 @@
  *              (-1e30, -1e30) to their LSE pair (attention.wgsl, fn main: the
  *              select() guards on sum_exp == 0).
  *   Precision  ATTN_FP32: fp32 CUDA-core arithmetic throughout.
- *              ATTN_TF32: QK^T and PV on tcgen05 tensor cores with TF32
- *              operands and fp32 accumulation; softmax in fp32.
- *              ATTN_BF16: as TF32 but with bf16 operands (K and V rounded to
- *              bf16 by a pre-pass, Q and the probabilities P on their way
- *              into tensor memory), fp32 accumulation and softmax.
+ *              ATTN_TF32: both products on tcgen05 tensor cores with fp32
+ *              accumulation and an fp32 softmax.  QK^T keeps Q to 22
+ *              significant bits (two fp16 parts, hi + lo, under a power of
+ *              two per query row) and K to 11 (fp16 under a power of two per
+ *              128-key tile of a kv head): two products, the tensor time of
+ *              one TF32 product.  PV takes TF32 operands (P and V with 11
+ *              significant bits).  The scores feed an exponential, so their
+ *              operand rounding sets the error: plain TF32 Q and K reach
+ *              3.5e-3 of max|V| on scores of standard deviation 9, this
+ *              scheme about 1.4e-3.
+ *              ATTN_BF16: 16-bit operands at the full 16-bit tensor rate.
+ *              QK^T takes fp16 operands (11 significant bits) under powers
+ *              of two, one per query row and one per 128-key tile of a kv
+ *              head, that keep every value below 2^15 whatever the fp32
+ *              magnitudes; PV takes bf16 operands (P <= 256 and V).  K and V
+ *              are converted by a pre-pass, Q and P on their way into the
+ *              tensor core.
  *              Tensor-core precisions need D in {64, 128}, gs a power of two
- *              <= 128, 16-byte aligned pointers and row strides that are
- *              multiples of 4 floats (K/V rows a multiple of 8 floats for
- *              ATTN_BF16); otherwise they return ATTN_ERR_UNSUPPORTED.
+ *              <= 128, 16-byte aligned pointers, Q/out row strides that are
+ *              multiples of 4 floats and K/V row strides that are multiples
+ *              of 8 floats; otherwise they return ATTN_ERR_UNSUPPORTED.
  *              ATTN_FP32 accepts any 1 <= D <= 128.
  */
 #ifndef ATTN_GQA_H

@@ -54,6 +54,11 @@ def test_small_config(cuda_lib, orc, prec, mask, kv):
     (5, 300, 2, 2, 100, CROSS),
     (1, 1, 4, 2, 64, CAUSAL),        # single query: window of one key
     (200, 200, 1, 1, 128, CAUSAL),
+    (67, 67, 6, 2, 128, CAUSAL),     # gs = 3: 42 queries (126 of 128 rows) per block
+    (150, 150, 12, 4, 64, FULL),     # gs = 3, D = 64
+    (90, 90, 10, 2, 128, CAUSAL),    # gs = 5
+    (61, 200, 14, 2, 64, CROSS),     # gs = 7
+    (40, 40, 48, 1, 128, CAUSAL),    # gs = 48: two queries per block
 ])
 def test_shapes(cuda_lib, orc, prec, q_seq, kv_seq, H, G, D, mask):
     if prec != FP32 and not tc_supported(H, G, D):

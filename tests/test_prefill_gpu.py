@@ -47,11 +47,13 @@ def test_prefill_config(cuda_lib, orc, prec):
     (1, 4, 2, 64, 128, 1, 0, 256, 256, 0),          # one query, one-row cache
     (129, 8, 1, 64, 96, 1000, 700, 520, 512, 3),    # gs = 8, kv_dim > G*D
     (50, 2, 2, 12, 30, 80, 25, 30, 24, 2),          # small odd head_dim
+    (37, 6, 2, 128, 256, 300, 100, 800, 776, 5),    # gs = 3 on the tensor cores
+    (70, 10, 2, 64, 136, 400, 250, 648, 640, 1),    # gs = 5, kv_dim > G*D
 ])
 def test_prefill_shapes(cuda_lib, orc, prec, n_queries, H, G, D, kv_dim, max_seq, start_pos, q_stride,
                         out_stride, q_base):
     if prec != FP32 and not tc_supported(H, G, D):
-        pytest.skip("tensor-core precisions need D in {64, 128} and a power-of-two group size")
+        pytest.skip("tensor-core precisions need D in {64, 128}")
     check(cuda_lib, orc, n_queries, H, G, D, kv_dim, max_seq, start_pos, q_stride, out_stride, q_base, prec,
           seed=n_queries)
 

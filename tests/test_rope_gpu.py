@@ -61,10 +61,11 @@ def test_rope_forward(cuda_lib, orc, prec, mask, kv):
     (45, 131, 8, 8, 64, CROSS, 0, 500.0),       # MHA, other base
     (200, 200, 4, 2, 128, CAUSAL, 77, 10000.0),  # sliding window
     (1, 1, 4, 2, 64, CAUSAL, 0, 10000.0),
+    (100, 100, 6, 2, 128, CAUSAL, 0, 10000.0),  # gs = 3 on the tensor cores
 ])
 def test_rope_shapes(cuda_lib, orc, prec, q_seq, kv_seq, H, G, D, mask, window, base):
     if prec != FP32 and not tc_supported(H, G, D):
-        pytest.skip("tensor-core precisions need D in {64, 128} and a power-of-two group size")
+        pytest.skip("tensor-core precisions need D in {64, 128}")
     check(cuda_lib, orc, q_seq, kv_seq, H, G, D, mask, prec, seed=q_seq + D, window=window, base=base)
 
 

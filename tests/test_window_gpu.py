@@ -55,10 +55,11 @@ def test_forward_window(cuda_lib, orc, prec, window, mask, kv):
     (45, 131, 8, 8, 64, CROSS, 100),     # MHA, ragged key tail
     (200, 200, 1, 1, 128, CAUSAL, 77),
     (20, 20, 2, 1, 12, FULL, 3),         # small odd head_dim (fp32 only)
+    (300, 300, 6, 2, 128, CAUSAL, 129),  # gs = 3 on the tensor cores
 ])
 def test_forward_window_shapes(cuda_lib, orc, prec, q_seq, kv_seq, H, G, D, mask, window):
     if prec != FP32 and not tc_supported(H, G, D):
-        pytest.skip("tensor-core precisions need D in {64, 128} and a power-of-two group size")
+        pytest.skip("tensor-core precisions need D in {64, 128}")
     check_forward(cuda_lib, orc, q_seq, kv_seq, H, G, D, mask, prec, window, seed=q_seq + window)
 
 
@@ -189,7 +190,7 @@ def test_prefill_window_config(cuda_lib, orc, prec, window):
 def test_prefill_window_shapes(cuda_lib, orc, prec, n_queries, H, G, D, kv_dim, max_seq, start_pos, q_stride,
                                out_stride, q_base, window):
     if prec != FP32 and not tc_supported(H, G, D):
-        pytest.skip("tensor-core precisions need D in {64, 128} and a power-of-two group size")
+        pytest.skip("tensor-core precisions need D in {64, 128}")
     check_prefill(cuda_lib, orc, n_queries, H, G, D, kv_dim, max_seq, start_pos, q_stride, out_stride, q_base, prec,
                   window, seed=n_queries + window)
 
