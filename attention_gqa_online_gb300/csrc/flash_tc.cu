@@ -99,7 +99,6 @@ struct __align__(1024) TcSmem {
   float red_max[2][2][kRows];  // [tile parity][group][row] partial tile maxima
   float red_l[2][kRows];       // [group][row] partial row sums (epilogue)
   uint32_t pages[kPageCache];  // block-table entries of the CTA's key range (paged caches)
-  long long row_off[kRows];    // output offset of each packed row (-1: no row)
   float kfac[kFacCache];       // powers of two of the CTA's K tiles jt0, jt0 + 1, ...
   uint32_t tmem_base;
   int abort;
@@ -109,7 +108,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_tc_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
-                    const float* __restrict__ kfac, int early_q) {
+                    const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ kfac, int early_q) {
   constexpr int kEpr = 32;                     // fp32 elements per 128-byte row
   constexpr int kChunks = D / kEpr;            // 128-byte column chunks of an fp32 V (or Q) row
   constexpr int kChunkBytes = kKeys * 128;     // one TMA box: 128 keys x 128 bytes
@@ -197,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_o);
       mbar_arrive_expect_tx(&sm.q_full, (unsigned)(rpb * D * 4));
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) tma_load_3d(qstage + c * kChunkBytes, &tm_q, kEpr * c, g * gs, (int)i0, &sm.q_full);
@@ -341,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long qi = i0 + r / gs;         // packed row blk * rpb + r
     const int h = g * gs + r % gs;
     const bool row_ok = r < rpb && qi < a.n_q;
-    if (grp == 0) sm.row_off[r] = row_ok ? qi * a.out_row_stride + (long long)h * D : -1;
     const int n_r = row_ok ? window(qi) : 0;
     const int lo_r = first_key(n_r, a.window);
     const float sl2 = a.scale * kLog2e;
@@ -531,14 +530,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_barrier(1, kSoftmaxThreads);
     const float l_row = sm.red_l[0][r] + sm.red_l[1][r];
     const float inv = (l_row == 0.f) ? 0.f : 1.f / l_row;
-    // O / l leaves through a per-warp staging area in the (now idle) K/V
-    // ring so that the global stores are whole row runs: each thread writes
-    // its row's kHalfD values (16-byte unit u at u ^ (row & 7), which spreads
-    // a warp's writes over all banks), then the warp stores rows out.
-    float* stage = reinterpret_cast<float*>(sm.ring) + (warp - 4) * 32 * kHalfD;
+    // O / l leaves by TMA tensor stores.  Each group stages its D/2 columns in
+    // the (now idle) K/V ring as 32-float chunks of 128 rows x 128 bytes, in
+    // the order of a 3-D box {32 floats, gs heads, 128/gs queries} (row r =
+    // query r / gs, head r % gs of the block) with the 128-byte swizzle
+    // (16-byte unit u of row r at u ^ (r & 7)); one thread then stores every
+    // chunk with one box each.  Rows past n_q fall outside the tensor and are
+    // not written, nor are the idle rows past (128/gs)*gs.
+    constexpr int kOChunks = kHalfD / 32;  // 32-float chunks per group
+    unsigned char* const ostage = sm.ring;   // [group][chunk][128 rows][128 bytes]
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the ring was last written by TMA
 #pragma unroll
-    for (int c = 0; c < kHalfD / 32; ++c) {
+    for (int c = 0; c < kOChunks; ++c) {
       uint32_t o[32];
       if (nt > 0) {
         tc::tmem_ld32(tmem + lane_base + kColO + grp * kHalfD + 32 * c, o);
@@ -548,28 +551,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
+      unsigned char* dst = ostage + (grp * kOChunks + c) * (kRows * 128) + r * 128;
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        const int u = (32 * c + e) / 4;
-        *reinterpret_cast<float4*>(stage + lane * kHalfD + 4 * (u ^ (lane & 7))) =
-            make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv, __uint_as_float(o[e + 2]) * inv,
-                        __uint_as_float(o[e + 3]) * inv);
-      }
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<float4*>(dst + 16 * (u ^ (r & 7))) =
+            make_float4(__uint_as_float(o[4 * u]) * inv, __uint_as_float(o[4 * u + 1]) * inv,
+                        __uint_as_float(o[4 * u + 2]) * inv, __uint_as_float(o[4 * u + 3]) * inv);
     }
-    __syncwarp();
-    {
-      constexpr int kLanesPerRow = kHalfD / 4;
-      constexpr int kRowsPerStore = 32 / kLanesPerRow;
-      const int u = lane % kLanesPerRow;
-#pragma unroll 4
-      for (int i = 0; i < 32 / kRowsPerStore; ++i) {
-        const int t = kRowsPerStore * i + lane / kLanesPerRow;  // row within the warp
-        const long long off = sm.row_off[32 * (warp & 3) + t];
-        if (off >= 0) {
-          const float4 v = *reinterpret_cast<const float4*>(stage + t * kHalfD + 4 * (u ^ (t & 7)));
-          *reinterpret_cast<float4*>(a.out + off + grp * kHalfD + 4 * u) = v;
-        }
-      }
+    // The tensor stores read the staging chunks through the async proxy.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    named_barrier(1, kSoftmaxThreads);
+    if (warp == 4 && lane == 0) {
+      for (int k = 0; k < 2 * kOChunks; ++k) tma_store_3d(&tm_o, ostage + k * (kRows * 128), 32 * k, g * gs, (int)i0);
+      bulk_commit();
+      bulk_wait_all();  // the staging memory stays live, and the stores complete, before the CTA exits
     }
     if (grp == 0 && row_ok && a.lse != nullptr) {
       float* l2 = a.lse + (qi * a.H + h) * 2;
@@ -645,13 +640,16 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
     }
     khp = kh16;
   }
-  CUtensorMap tm_k, tm_v, tm_q;
+  CUtensorMap tm_k, tm_v, tm_q, tm_o;
   // Q: fp32 [n_q][H][D] (query rows q_row_stride floats apart); one CTA's
   // block is D/32 boxes of 32 floats x gs heads x 128/gs queries, rows past
   // n_q read as 0.
   const uint64_t qdims[3] = {(uint64_t)D, (uint64_t)a.H, (uint64_t)a.n_q};
   const uint64_t qstrides[2] = {(uint64_t)D * 4, (uint64_t)a.q_row_stride * 4};
   const uint32_t qbox[3] = {32, (uint32_t)gs, (uint32_t)qpb};
+  // out: the same box over [n_q][H][D] (query rows out_row_stride floats apart).
+  const uint64_t odims[3] = {(uint64_t)D, (uint64_t)a.H, (uint64_t)a.n_q};
+  const uint64_t ostrides[2] = {(uint64_t)D * 4, (uint64_t)a.out_row_stride * 4};
   // K: [kv_rows][kv_row_stride] fp16, boxes of 64 elements x 128 keys.
   const uint64_t kdims[2] = {(uint64_t)a.kv_row_stride, (uint64_t)kv_rows};
   const uint64_t kstrides[1] = {(uint64_t)a.kv_row_stride * 2};
@@ -663,7 +661,8 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
   int rc = ATTN_OK;
   if (!make_tmap(&tm_k, khp, 2, kdims, kstrides, kbox, true, kSwizzle128) ||
       !make_tmap(&tm_v, vp, 2, vdims, vstrides, vbox, false, kSwizzle128Atom32) ||
-      !make_tmap(&tm_q, a.q, 3, qdims, qstrides, qbox, false, kSwizzle128)) {
+      !make_tmap(&tm_q, a.q, 3, qdims, qstrides, qbox, false, kSwizzle128) ||
+      !make_tmap(&tm_o, a.out, 3, odims, ostrides, qbox, false, kSwizzle128)) {
     rc = ATTN_ERR_UNSUPPORTED;
   } else {
     const size_t smem = sizeof(TcSmem) + 1024;
@@ -673,7 +672,7 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
     } else {
       FlashArgs aa = a;
       int early_q = scratch != nullptr ? 1 : 0;  // the pre-pass ran just before
-      void* args[] = {&aa, &tm_k, &tm_v, &tm_q, &kfac, &early_q};
+      void* args[] = {&aa, &tm_k, &tm_v, &tm_q, &tm_o, &kfac, &early_q};
       if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s,
                      args) != cudaSuccess)
         rc = ATTN_ERR_CUDA;

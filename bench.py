@@ -443,17 +443,21 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
     steps = max(3, min(args.steps, args.extra_steps))
 
     def timed(fn, n):
+        """Mean device time per call of n back-to-back calls between one event
+        pair (each call's kernels chain to the previous call's by programmatic
+        dependent launch, as in a stream of calls; an event between calls would
+        break that chain).  Inputs rotate over sets larger than L2 together."""
         for i in range(args.warmup):
             fn(i)
         torch.cuda.synchronize()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
         for i in range(n):
-            evs[i][0].record(stream)
             fn(i)
-            evs[i][1].record(stream)
+        e1.record(stream)
         torch.cuda.synchronize()
         res["_launches"] += n + args.warmup
-        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+        return e0.elapsed_time(e1) / n
 
     def roof(prec, tf, kernel):
         if prec == A.ATTN_BF16:
