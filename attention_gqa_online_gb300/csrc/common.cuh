@@ -210,6 +210,15 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float b0, float b1, f
       : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+// (a0, a1) += (x0 * y0, x1 * y1) as one paired fp32 fma (each result rounded
+// once, as fmaf).
+__device__ __forceinline__ void fma2_acc(float& a0, float& a1, float x0, float x1, float y0, float y1) {
+  asm("{\n\t.reg .b64 a, x, y;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "fma.rn.f32x2 a, x, y, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
+
 // Power-of-two range scaling of 16-bit tensor-core operands.  For the
 // largest magnitude m of a set of values, pow2_scale_exp gives E such that
 // m * 2^(14 - E) lies in [2^14, 2^15) (exactly representable range of fp16,

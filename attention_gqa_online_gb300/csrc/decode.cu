@@ -260,12 +260,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const float4 kv = *reinterpret_cast<const float4*>(&ks[pos * D + 4 * qc + 32 * u]);
+          if constexpr (GS % 2 == 0) {
+            // Two heads per paired fma: the same per-head order of products.
 #pragma unroll
-          for (int h = 0; h < GS; ++h) {
-            part[h] = fmaf(qr[h][u].x, kv.x, part[h]);
-            part[h] = fmaf(qr[h][u].y, kv.y, part[h]);
-            part[h] = fmaf(qr[h][u].z, kv.z, part[h]);
-            part[h] = fmaf(qr[h][u].w, kv.w, part[h]);
+            for (int h = 0; h < GS; h += 2) {
+              fma2_acc(part[h], part[h + 1], qr[h][u].x, qr[h + 1][u].x, kv.x, kv.x);
+              fma2_acc(part[h], part[h + 1], qr[h][u].y, qr[h + 1][u].y, kv.y, kv.y);
+              fma2_acc(part[h], part[h + 1], qr[h][u].z, qr[h + 1][u].z, kv.z, kv.z);
+              fma2_acc(part[h], part[h + 1], qr[h][u].w, qr[h + 1][u].w, kv.w, kv.w);
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < GS; ++h) {
+              part[h] = fmaf(qr[h][u].x, kv.x, part[h]);
+              part[h] = fmaf(qr[h][u].y, kv.y, part[h]);
+              part[h] = fmaf(qr[h][u].z, kv.z, part[h]);
+              part[h] = fmaf(qr[h][u].w, kv.w, part[h]);
+            }
           }
         }
 #pragma unroll
@@ -314,22 +325,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
           for (int h = 0; h < GS; ++h) wb[h] = __shfl_sync(0xffffffffu, w[grp][h], 8 * pp);
           if (ppos < valid && ppos >= first) {
+            // Two output dims per paired fma.
             if constexpr (VP == 4) {
               const float4 vv = *reinterpret_cast<const float4*>(&vs[ppos * D + 4 * lane]);
 #pragma unroll
               for (int h = 0; h < GS; ++h) {
-                acc[h][0] = fmaf(wb[h], vv.x, acc[h][0]);
-                acc[h][1] = fmaf(wb[h], vv.y, acc[h][1]);
-                acc[h][2] = fmaf(wb[h], vv.z, acc[h][2]);
-                acc[h][3] = fmaf(wb[h], vv.w, acc[h][3]);
+                fma2_acc(acc[h][0], acc[h][1], wb[h], wb[h], vv.x, vv.y);
+                fma2_acc(acc[h][2], acc[h][3], wb[h], wb[h], vv.z, vv.w);
               }
             } else {
               const float2 vv = *reinterpret_cast<const float2*>(&vs[ppos * D + 2 * lane]);
 #pragma unroll
-              for (int h = 0; h < GS; ++h) {
-                acc[h][0] = fmaf(wb[h], vv.x, acc[h][0]);
-                acc[h][1] = fmaf(wb[h], vv.y, acc[h][1]);
-              }
+              for (int h = 0; h < GS; ++h) fma2_acc(acc[h][0], acc[h][1], wb[h], wb[h], vv.x, vv.y);
             }
           }
         }
@@ -384,47 +391,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (!sm.is_last) return;
   __threadfence();
 
-  // Fast path: every split's partials of this kv head fit in the (now idle)
-  // stage buffers: one round of bulk copies brings them all in, then the
-  // merge runs from shared memory.
+  // Fast path: the splits' partials of as many heads as fit in the (now
+  // idle) stage buffers come in with one round of bulk copies, then the merge
+  // runs from shared memory; rounds repeat until every head is merged.
   const int S2 = even_splits(S);
   const unsigned ml_head_bytes = ((unsigned)s_eff * 8u + 15u) & ~15u;
-  const size_t merge_bytes = (size_t)GS * s_eff * D * 4 + (size_t)GS * ml_head_bytes;
-  if (merge_bytes <= sizeof(sm.k) + sizeof(sm.v)) {
-    float* so = &sm.k[0][0];                       // [GS][s_eff][D]
-    float* sml = so + (size_t)GS * s_eff * D;      // [GS][ml_head_bytes / 4]
-    if (tid == 0) {
-      asm volatile("fence.proxy.async;" ::: "memory");
-      mbar_arrive_expect_tx(&sm.merge_bar, (unsigned)merge_bytes);
-      for (int h = 0; h < GS; ++h) {
-        bulk_g2s(so + (size_t)h * s_eff * D, ws.o + (size_t)(g * GS + h) * S * D, (unsigned)(s_eff * D * 4),
-                 &sm.merge_bar);
-        bulk_g2s(sml + (size_t)h * (ml_head_bytes / 4), ws.ml + (size_t)(g * GS + h) * S2 * 2, ml_head_bytes,
-                 &sm.merge_bar);
+  const size_t head_bytes = (size_t)s_eff * D * 4 + ml_head_bytes;
+  const int hr = (int)min((size_t)GS, (sizeof(sm.k) + sizeof(sm.v)) / head_bytes);  // heads per round
+  if (hr > 0) {
+    for (int h0 = 0, round = 0; h0 < GS; h0 += hr, ++round) {
+      const int nh = min(hr, GS - h0);
+      float* so = &sm.k[0][0];                  // [nh][s_eff][D]
+      float* sml = so + (size_t)nh * s_eff * D;  // [nh][ml_head_bytes / 4]
+      if (tid == 0) {
+        asm volatile("fence.proxy.async;" ::: "memory");
+        mbar_arrive_expect_tx(&sm.merge_bar, (unsigned)(nh * head_bytes));
+        for (int h = 0; h < nh; ++h) {
+          bulk_g2s(so + (size_t)h * s_eff * D, ws.o + (size_t)(g * GS + h0 + h) * S * D, (unsigned)(s_eff * D * 4),
+                   &sm.merge_bar);
+          bulk_g2s(sml + (size_t)h * (ml_head_bytes / 4), ws.ml + (size_t)(g * GS + h0 + h) * S2 * 2, ml_head_bytes,
+                   &sm.merge_bar);
+        }
       }
-    }
-    mbar_wait_bounded(&sm.merge_bar, 0, a.status);
-    for (int idx = tid; idx < GS * (D / 4); idx += kThreads) {
-      const int h = idx / (D / 4), c = idx % (D / 4);
-      const float* mlh = sml + (size_t)h * (ml_head_bytes / 4);
-      float M = -INFINITY;
-      for (int s = 0; s < s_eff; ++s) M = fmaxf(M, mlh[2 * s]);
-      const float Mu = (M == -INFINITY) ? 0.f : M;
-      float L = 0.f;
-      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+      mbar_wait_bounded(&sm.merge_bar, (unsigned)(round & 1), a.status);
+      for (int idx = tid; idx < nh * (D / 4); idx += kThreads) {
+        const int h = idx / (D / 4), c = idx % (D / 4);
+        const float* mlh = sml + (size_t)h * (ml_head_bytes / 4);
+        float M = -INFINITY;
+        for (int s = 0; s < s_eff; ++s) M = fmaxf(M, mlh[2 * s]);
+        const float Mu = (M == -INFINITY) ? 0.f : M;
+        float L = 0.f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-      for (int s = 0; s < s_eff; ++s) {
-        const float f = ex2(mlh[2 * s] - Mu);
-        const float4 x = *reinterpret_cast<const float4*>(so + ((size_t)h * s_eff + s) * D + 4 * c);
-        L = fmaf(mlh[2 * s + 1], f, L);
-        O.x = fmaf(x.x, f, O.x);
-        O.y = fmaf(x.y, f, O.y);
-        O.z = fmaf(x.z, f, O.z);
-        O.w = fmaf(x.w, f, O.w);
+        for (int s = 0; s < s_eff; ++s) {
+          const float f = ex2(mlh[2 * s] - Mu);
+          const float4 x = *reinterpret_cast<const float4*>(so + ((size_t)h * s_eff + s) * D + 4 * c);
+          L = fmaf(mlh[2 * s + 1], f, L);
+          O.x = fmaf(x.x, f, O.x);
+          O.y = fmaf(x.y, f, O.y);
+          O.z = fmaf(x.z, f, O.z);
+          O.w = fmaf(x.w, f, O.w);
+        }
+        const float inv = (L == 0.f) ? 0.f : 1.f / L;
+        *reinterpret_cast<float4*>(a.out + (size_t)(g * GS + h0 + h) * D + 4 * c) =
+            make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
       }
-      const float inv = (L == 0.f) ? 0.f : 1.f / L;
-      *reinterpret_cast<float4*>(a.out + (size_t)(g * GS + h) * D + 4 * c) =
-          make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+      __syncthreads();  // the buffers are refilled by the next round
     }
     if (tid == 0) ws.tickets[g] = 0u;
     return;
