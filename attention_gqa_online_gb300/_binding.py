@@ -72,6 +72,20 @@ def load_library(path=None):
     lib.attn_backward_rope.argtypes = [_vp] * 9 + [_u32] * 5 + [ctypes.c_int, ctypes.c_int, _u32, _vp, _u32, _vp]
     lib.attn_get_status.restype = ctypes.c_int
     lib.attn_get_status.argtypes = [_vp]
+    lib.attn_set_workspace.restype = ctypes.c_int
+    lib.attn_set_workspace.argtypes = [_vp, ctypes.c_size_t]
+    lib.attn_forward_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_forward_workspace_bytes.argtypes = [_u32] * 5 + [ctypes.c_int, ctypes.c_int, _u32, ctypes.c_int]
+    lib.attn_prefill_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_prefill_workspace_bytes.argtypes = [_u32] * 8 + [ctypes.c_int, _u32]
+    lib.attn_backward_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_backward_workspace_bytes.argtypes = [_u32] * 5 + [ctypes.c_int, ctypes.c_int]
+    lib.attn_scratch_reserved_bytes.restype = ctypes.c_size_t
+    lib.attn_scratch_reserved_bytes.argtypes = []
+    lib.attn_scratch_peak_bytes.restype = ctypes.c_size_t
+    lib.attn_scratch_peak_bytes.argtypes = [ctypes.c_int]
+    lib.attn_release_scratch.restype = ctypes.c_int
+    lib.attn_release_scratch.argtypes = []
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_status_string.argtypes = [ctypes.c_int]
     _lib = lib
@@ -280,6 +294,45 @@ def attn_decode_cached_noalloc(q, k_cache, v_cache, kv_pos_dev, out, num_heads, 
     _check(fn(_addr(q, "q", f), _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f),
               _addr(kv_pos_dev, "kv_pos_dev"), _addr(out, "out", f), num_heads, num_kv_heads, head_dim, max_seq,
               _stream(stream)), "attn_decode_cached_noalloc")
+
+
+def attn_set_workspace(workspace, workspace_bytes=None):
+    """Bind a caller-owned device buffer (256-byte aligned) for the scratch of
+    this thread's later calls, or unbind with None; see attn_gqa.h."""
+    if workspace is None:
+        _check(load_library().attn_set_workspace(None, 0), "attn_set_workspace")
+        return
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load_library().attn_set_workspace(_addr(workspace, "workspace"), workspace_bytes), "attn_set_workspace")
+
+
+def attn_forward_workspace_bytes(q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask, prec, window=0, rope=False):
+    return int(load_library().attn_forward_workspace_bytes(q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask,
+                                                           prec, window, 1 if rope else 0))
+
+
+def attn_prefill_workspace_bytes(n_queries, n_heads, n_kv_heads, head_dim, kv_dim, max_seq, start_pos, q_base, prec,
+                                 window=0):
+    return int(load_library().attn_prefill_workspace_bytes(n_queries, n_heads, n_kv_heads, head_dim, kv_dim, max_seq,
+                                                           start_pos, q_base, prec, window))
+
+
+def attn_backward_workspace_bytes(q_seq, kv_seq, num_heads, num_kv_heads, head_dim, prec, rope=False):
+    return int(load_library().attn_backward_workspace_bytes(q_seq, kv_seq, num_heads, num_kv_heads, head_dim, prec,
+                                                            1 if rope else 0))
+
+
+def attn_scratch_reserved_bytes():
+    return int(load_library().attn_scratch_reserved_bytes())
+
+
+def attn_scratch_peak_bytes(reset=False):
+    return int(load_library().attn_scratch_peak_bytes(1 if reset else 0))
+
+
+def attn_release_scratch():
+    _check(load_library().attn_release_scratch(), "attn_release_scratch")
 
 
 def attn_selftest_wait_timeout(timeout_us=10000, stream=None):

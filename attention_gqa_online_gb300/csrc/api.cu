@@ -59,11 +59,28 @@ int window_arg(uint32_t window) { return window > 0x7fffffffu ? 0x7fffffff : (in
 
 bool valid_prec(int prec) { return prec == ATTN_FP32 || prec == ATTN_TF32 || prec == ATTN_BF16; }
 
+size_t flash_scratch_bytes(const FlashArgs& a, int prec) {
+  if (prec == ATTN_FP32) return flash_simt_scratch_bytes(a);
+  return prec == ATTN_BF16 ? flash_bf16_scratch_bytes(a) : flash_tc_scratch_bytes(a);
+}
+
+// A workspace bound to this thread must hold the call's whole scratch; this
+// is checked before anything is launched.
+bool workspace_too_small(size_t need) {
+  size_t have = 0;
+  return scratch_bound(&have) && need > have;
+}
+
 int run_flash(const FlashArgs& a, int prec, cudaStream_t s) {
+  scratch_begin_call();
+  if (prec != ATTN_FP32 && !flash_tc_supported(a, prec)) return ATTN_ERR_UNSUPPORTED;
+  if (workspace_too_small(flash_scratch_bytes(a, prec))) return ATTN_ERR_INVALID_ARG;
   if (prec == ATTN_FP32) return launch_flash_simt(a, s);
-  if (!flash_tc_supported(a, prec)) return ATTN_ERR_UNSUPPORTED;
   return launch_flash_tc(a, prec, s);
 }
+
+// Host-only stand-in for present K/V in size queries (never dereferenced).
+const float kPresent = 0.f;
 
 }  // namespace
 
@@ -75,7 +92,7 @@ using namespace attn;
 
 extern "C" int attn_forward_window(const float* q, const float* k, const float* v, float* out, float* lse,
                                    uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
-                                   uint32_t head_dim, int mask, int prec, uint32_t window, attn_stream_t stream) {
+                                   uint32_t head_dim, attn_mask_t mask, attn_prec_t prec, uint32_t window, attn_stream_t stream) {
   if (!heads_ok(num_heads, num_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
   if (mask != ATTN_CAUSAL && mask != ATTN_FULL && mask != ATTN_CROSS) return ATTN_ERR_INVALID_ARG;
   if (mask != ATTN_CROSS && kv_seq != q_seq) return ATTN_ERR_INVALID_ARG;
@@ -119,7 +136,7 @@ extern "C" int attn_rope_table(float* table, uint32_t max_pos, uint32_t head_dim
 
 extern "C" int attn_forward_rope(const float* q, const float* k, const float* v, float* out, float* lse,
                                  uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
-                                 uint32_t head_dim, int mask, int prec, uint32_t window, const float* rope_table,
+                                 uint32_t head_dim, attn_mask_t mask, attn_prec_t prec, uint32_t window, const float* rope_table,
                                  uint32_t table_rows, attn_stream_t stream) {
   if (!heads_ok(num_heads, num_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
   if (mask != ATTN_CAUSAL && mask != ATTN_FULL && mask != ATTN_CROSS) return ATTN_ERR_INVALID_ARG;
@@ -159,7 +176,7 @@ extern "C" int attn_forward_rope(const float* q, const float* k, const float* v,
 
 extern "C" int attn_forward(const float* q, const float* k, const float* v, float* out, float* lse,
                             uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
-                            uint32_t head_dim, int mask, int prec, attn_stream_t stream) {
+                            uint32_t head_dim, attn_mask_t mask, attn_prec_t prec, attn_stream_t stream) {
   return attn_forward_window(q, k, v, out, lse, q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask, prec, 0,
                              stream);
 }
@@ -292,7 +309,7 @@ extern "C" int attn_prefill_window(const float* q_batch, const float* k_cache, c
                                    float* out_batch, uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads,
                                    uint32_t head_dim, uint32_t kv_dim, uint32_t max_seq, float scale,
                                    uint32_t start_pos, uint32_t q_stride, uint32_t out_stride, uint32_t q_base,
-                                   int prec, uint32_t window, attn_stream_t stream) {
+                                   attn_prec_t prec, uint32_t window, attn_stream_t stream) {
   if (!heads_ok(n_heads, n_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
   if ((uint64_t)kv_dim < (uint64_t)n_kv_heads * head_dim) return ATTN_ERR_INVALID_ARG;
   if ((uint64_t)q_stride < (uint64_t)n_heads * head_dim || (uint64_t)out_stride < (uint64_t)n_heads * head_dim)
@@ -330,7 +347,7 @@ extern "C" int attn_prefill_window(const float* q_batch, const float* k_cache, c
 extern "C" int attn_prefill(const float* q_batch, const float* k_cache, const float* v_cache, float* out_batch,
                             uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads, uint32_t head_dim,
                             uint32_t kv_dim, uint32_t max_seq, float scale, uint32_t start_pos, uint32_t q_stride,
-                            uint32_t out_stride, uint32_t q_base, int prec, attn_stream_t stream) {
+                            uint32_t out_stride, uint32_t q_base, attn_prec_t prec, attn_stream_t stream) {
   return attn_prefill_window(q_batch, k_cache, v_cache, out_batch, n_queries, n_heads, n_kv_heads, head_dim, kv_dim,
                              max_seq, scale, start_pos, q_stride, out_stride, q_base, prec, 0, stream);
 }
@@ -415,7 +432,7 @@ extern "C" int attn_prefill_paged(const float* q_batch, const float* k_pages, co
                                   const uint32_t* block_table, float* out_batch, uint32_t n_queries, uint32_t n_heads,
                                   uint32_t n_kv_heads, uint32_t head_dim, uint32_t kv_dim, uint32_t page_rows,
                                   uint32_t num_pages, uint32_t max_blocks, float scale, uint32_t start_pos,
-                                  uint32_t q_stride, uint32_t out_stride, uint32_t q_base, int prec, uint32_t window,
+                                  uint32_t q_stride, uint32_t out_stride, uint32_t q_base, attn_prec_t prec, uint32_t window,
                                   attn_stream_t stream) {
   if (!heads_ok(n_heads, n_kv_heads, head_dim) || !valid_prec(prec)) return ATTN_ERR_INVALID_ARG;
   if (!paged_sizes_ok(page_rows, num_pages, max_blocks)) return ATTN_ERR_INVALID_ARG;
@@ -454,6 +471,13 @@ extern "C" int attn_prefill_paged(const float* q_batch, const float* k_pages, co
   a.page_rows = (int)page_rows;
   a.num_pages = (int)num_pages;
   return run_flash(a, prec, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Scratch of one backward call: q and k turned (RoPE), then the backward's own.
+static size_t backward_scratch_bytes(const BwdArgs& a, int prec, bool rope) {
+  const size_t turned = rope ? scratch_round(((size_t)a.n_q * a.H + (size_t)a.n_kv * a.G) * a.D * sizeof(float)) : 0;
+  if (a.n_kv == 0) return 0;
+  return turned + (prec == ATTN_BF16 ? backward_bf16_scratch_bytes(a) : backward_simt_scratch_bytes(a));
 }
 
 // The backward behind attn_backward and attn_backward_rope; rope_table (or
@@ -504,6 +528,8 @@ static int backward_impl(const float* q, const float* k, const float* v, const f
   a.status = status_ptr();
   if (a.status == nullptr) return ATTN_ERR_CUDA;
   if (prec == ATTN_BF16 && !backward_bf16_supported(a)) return ATTN_ERR_UNSUPPORTED;
+  scratch_begin_call();
+  if (workspace_too_small(backward_scratch_bytes(a, prec, rope))) return ATTN_ERR_INVALID_ARG;
   // RoPE: the gradient of the plain attention at the turned q and k, turned
   // back (the rotations are orthogonal); q and k are turned into scratch.
   void* scratch = nullptr;
@@ -531,7 +557,7 @@ static int backward_impl(const float* q, const float* k, const float* v, const f
 
 extern "C" int attn_backward(const float* q, const float* k, const float* v, const float* out, const float* dout,
                              const float* lse, float* dq, float* dk, float* dv, uint32_t q_seq, uint32_t kv_seq,
-                             uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,
+                             uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, attn_mask_t mask, attn_prec_t prec,
                              uint32_t window, attn_stream_t stream) {
   return backward_impl(q, k, v, out, dout, lse, dq, dk, dv, q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask,
                        prec, window, nullptr, 0, stream);
@@ -539,13 +565,82 @@ extern "C" int attn_backward(const float* q, const float* k, const float* v, con
 
 extern "C" int attn_backward_rope(const float* q, const float* k, const float* v, const float* out, const float* dout,
                                   const float* lse, float* dq, float* dk, float* dv, uint32_t q_seq, uint32_t kv_seq,
-                                  uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,
+                                  uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, attn_mask_t mask, attn_prec_t prec,
                                   uint32_t window, const float* rope_table, uint32_t table_rows,
                                   attn_stream_t stream) {
   if (rope_table == nullptr) return ATTN_ERR_INVALID_ARG;
   return backward_impl(q, k, v, out, dout, lse, dq, dk, dv, q_seq, kv_seq, num_heads, num_kv_heads, head_dim, mask,
                        prec, window, rope_table, table_rows, stream);
 }
+
+extern "C" int attn_set_workspace(void* workspace, size_t workspace_bytes) {
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) % 256) != 0) return ATTN_ERR_INVALID_ARG;
+  scratch_bind(workspace, workspace_bytes);
+  return ATTN_OK;
+}
+
+extern "C" size_t attn_forward_workspace_bytes(uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads,
+                                               uint32_t num_kv_heads, uint32_t head_dim, attn_mask_t mask,
+                                               attn_prec_t prec, uint32_t window, int rope) {
+  if (!heads_ok(num_heads, num_kv_heads, head_dim) || !valid_prec(prec)) return 0;
+  if (mask != ATTN_CAUSAL && mask != ATTN_FULL && mask != ATTN_CROSS) return 0;
+  if ((mask != ATTN_CROSS && kv_seq != q_seq) || q_seq > 0x7fffffffu || kv_seq > 0x7fffffffu) return 0;
+  FlashArgs a{};
+  a.k = a.v = kv_seq > 0 ? &kPresent : nullptr;
+  a.q_row_stride = a.out_row_stride = (long long)num_heads * head_dim;
+  a.kv_row_stride = (long long)num_kv_heads * head_dim;
+  a.n_q = (int)q_seq;
+  a.H = (int)num_heads;
+  a.G = (int)num_kv_heads;
+  a.D = (int)head_dim;
+  a.causal = (mask == ATTN_CAUSAL);
+  a.cap = a.n_all = (int)kv_seq;
+  a.window = window_arg(window);
+  a.rope = rope ? &kPresent : nullptr;
+  return flash_scratch_bytes(a, prec);
+}
+
+extern "C" size_t attn_prefill_workspace_bytes(uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads,
+                                               uint32_t head_dim, uint32_t kv_dim, uint32_t max_seq,
+                                               uint32_t start_pos, uint32_t q_base, attn_prec_t prec,
+                                               uint32_t window) {
+  if (!heads_ok(n_heads, n_kv_heads, head_dim) || !valid_prec(prec)) return 0;
+  if ((uint64_t)kv_dim < (uint64_t)n_kv_heads * head_dim || max_seq > 0x7fffffffu) return 0;
+  if ((uint64_t)start_pos + q_base + n_queries > max_seq) return 0;
+  FlashArgs a{};
+  a.k = a.v = &kPresent;
+  a.q_row_stride = a.out_row_stride = (long long)n_heads * head_dim;
+  a.kv_row_stride = kv_dim;
+  a.n_q = (int)n_queries;
+  a.H = (int)n_heads;
+  a.G = (int)n_kv_heads;
+  a.D = (int)head_dim;
+  a.causal = 1;
+  a.base_pos = (long long)start_pos + q_base;
+  a.cap = a.n_all = (int)max_seq;
+  a.window = window_arg(window);
+  return flash_scratch_bytes(a, prec);
+}
+
+extern "C" size_t attn_backward_workspace_bytes(uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads,
+                                                uint32_t num_kv_heads, uint32_t head_dim, attn_prec_t prec, int rope) {
+  if (!heads_ok(num_heads, num_kv_heads, head_dim) || !valid_prec(prec) || q_seq > 0x7fffffffu ||
+      kv_seq > 0x7fffffffu)
+    return 0;
+  BwdArgs a{};
+  a.n_q = (int)q_seq;
+  a.n_kv = (int)kv_seq;
+  a.H = (int)num_heads;
+  a.G = (int)num_kv_heads;
+  a.D = (int)head_dim;
+  return q_seq == 0 ? 0 : backward_scratch_bytes(a, prec, rope != 0);
+}
+
+extern "C" size_t attn_scratch_reserved_bytes(void) { return scratch_pool_stat(0, false); }
+
+extern "C" size_t attn_scratch_peak_bytes(int reset) { return scratch_pool_stat(1, reset != 0); }
+
+extern "C" int attn_release_scratch(void) { return scratch_trim() ? ATTN_OK : ATTN_ERR_CUDA; }
 
 extern "C" int attn_get_status(attn_stream_t stream) {
   unsigned* st = status_ptr();

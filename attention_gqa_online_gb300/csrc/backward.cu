@@ -429,12 +429,17 @@ cudaError_t launch_bwd_prep(const BwdArgs& a, float* delta, float* l2, cudaStrea
                     pargs);
 }
 
+// delta and the base-2 log-sum-exp per (row, head).
+size_t backward_simt_scratch_bytes(const BwdArgs& a) {
+  return scratch_round((size_t)a.n_q * a.H * 2 * sizeof(float));
+}
+
 int launch_backward_simt(const BwdArgs& a, cudaStream_t s) {
   const long long pairs = (long long)a.n_q * a.H;
   if (pairs == 0) return ATTN_OK;
   if (a.G > 65535 || (pairs + 7) / 8 > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   void* scratch = nullptr;
-  if (scratch_alloc(&scratch, (size_t)pairs * 2 * sizeof(float), s) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (scratch_alloc(&scratch, backward_simt_scratch_bytes(a), s) != cudaSuccess) return ATTN_ERR_CUDA;
   float* delta = static_cast<float*>(scratch);
   float* l2 = delta + pairs;
   int rc = launch_bwd_prep(a, delta, l2, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

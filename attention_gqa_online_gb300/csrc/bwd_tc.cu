@@ -585,6 +585,13 @@ bool backward_bf16_supported(const BwdArgs& a) {
   return al % 16 == 0;
 }
 
+// delta and the base-2 log-sum-exp per (row, head), then bf16 copies of q,
+// dout, k and v, each part 256-byte aligned.
+size_t backward_bf16_scratch_bytes(const BwdArgs& a) {
+  const size_t pairs = (size_t)a.n_q * a.H, qe = pairs * a.D, ke = (size_t)a.n_kv * a.G * a.D;
+  return 2 * align256(pairs * 4) + 2 * align256(qe * 2) + 2 * align256(ke * 2);
+}
+
 int launch_backward_bf16(const BwdArgs& a, cudaStream_t s) {
   const long long pairs = (long long)a.n_q * a.H;
   if (pairs == 0 || a.n_kv == 0) return ATTN_OK;
@@ -592,9 +599,8 @@ int launch_backward_bf16(const BwdArgs& a, cudaStream_t s) {
   const size_t qe = (size_t)pairs * a.D, ke = (size_t)a.n_kv * a.G * a.D;
   const size_t off_l2 = align256((size_t)pairs * 4), off_q = off_l2 + align256((size_t)pairs * 4);
   const size_t off_g = off_q + align256(qe * 2), off_k = off_g + align256(qe * 2), off_v = off_k + align256(ke * 2);
-  const size_t total = off_v + align256(ke * 2);
   void* scratch = nullptr;
-  if (scratch_alloc(&scratch, total, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (scratch_alloc(&scratch, backward_bf16_scratch_bytes(a), s) != cudaSuccess) return ATTN_ERR_CUDA;
   char* base = static_cast<char*>(scratch);
   float* delta = reinterpret_cast<float*>(base);
   float* l2 = reinterpret_cast<float*>(base + off_l2);

@@ -525,9 +525,8 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
     const int n_tiles = (int)((kv_rows + kKeys - 1) / kKeys);
     const int n_first = a.causal ? (int)min((long long)a.cap, a.base_pos + 1) : a.n_all;  // window of query 0
     const int tile0 = first_key(n_first, a.window) / kKeys;
-    const size_t fac_off = ((size_t)elems * 4 + 255) / 256 * 256;
-    if (scratch_alloc(&scratch, fac_off + (size_t)n_tiles * a.G * sizeof(float), s) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+    const size_t fac_off = scratch_round((size_t)elems * 4);
+    if (scratch_alloc(&scratch, flash_bf16_scratch_bytes(a), s) != cudaSuccess) return ATTN_ERR_CUDA;
     uint16_t* k16 = static_cast<uint16_t*>(scratch);
     uint16_t* v16 = k16 + elems;
     float* fac = reinterpret_cast<float*>(static_cast<char*>(scratch) + fac_off);
@@ -598,6 +597,16 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+// K as fp16 and V as bf16 (kv_rows x kv_row_stride each) and one float per
+// (128-key tile, kv head).
+size_t flash_bf16_scratch_bytes(const FlashArgs& a) {
+  long long kv_rows = a.causal ? a.base_pos + a.n_q : a.n_all;
+  if (kv_rows > a.cap) kv_rows = a.cap;
+  if (kv_rows < 1 || a.k == nullptr || a.v == nullptr || a.n_q == 0) return 0;
+  return scratch_round(scratch_round((size_t)kv_rows * a.kv_row_stride * 4) +
+                       (size_t)((kv_rows + kKeys - 1) / kKeys) * a.G * sizeof(float));
+}
 
 // Callers check flash_tc_supported(a, ATTN_BF16) first.
 int launch_flash_bf16(const FlashArgs& a, cudaStream_t s) {

@@ -350,6 +350,13 @@ int launch_one(const FlashArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// RoPE only: K turned (kv_rows x kv_row_stride floats).
+size_t flash_simt_scratch_bytes(const FlashArgs& a) {
+  const long long kv_rows = a.causal ? min((long long)a.cap, a.base_pos + a.n_q) : a.n_all;
+  if (a.rope == nullptr || kv_rows <= 0 || a.n_q == 0) return 0;
+  return scratch_round((size_t)kv_rows * a.kv_row_stride * sizeof(float));
+}
+
 int launch_flash_simt(const FlashArgs& a0, cudaStream_t s) {
   // RoPE: K is turned once into stream-ordered scratch (rows of G*D floats,
   // row t at position t) and the kernel turns Q.
@@ -357,8 +364,7 @@ int launch_flash_simt(const FlashArgs& a0, cudaStream_t s) {
   void* scratch = nullptr;
   const long long kv_rows = a.causal ? min((long long)a.cap, a.base_pos + a.n_q) : a.n_all;
   if (a.rope != nullptr && kv_rows > 0) {
-    if (scratch_alloc(&scratch, (size_t)kv_rows * a.kv_row_stride * sizeof(float), s) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+    if (scratch_alloc(&scratch, flash_simt_scratch_bytes(a), s) != cudaSuccess) return ATTN_ERR_CUDA;
     if (launch_rope_k(a.k, static_cast<float*>(scratch), a.rope, kv_rows, a.G, a.D, s) != cudaSuccess) {
       scratch_free(scratch, s);
       return ATTN_ERR_CUDA;

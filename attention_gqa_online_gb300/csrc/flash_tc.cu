@@ -611,9 +611,8 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
     // tiles from the first one any CTA reads are written.
     const long long elems = kv_rows * a.kv_row_stride;
     const int n_first = a.causal ? (int)min((long long)a.cap, a.base_pos + 1) : a.n_all;  // window of query 0
-    const size_t fac_off = ((size_t)elems * 2 + 255) / 256 * 256;
-    const size_t fac_bytes = (size_t)((kv_rows + kKeys - 1) / kKeys) * a.G * sizeof(float);
-    if (scratch_alloc(&scratch, fac_off + fac_bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    const size_t fac_off = scratch_round((size_t)elems * 2);
+    if (scratch_alloc(&scratch, flash_tc_scratch_bytes(a), s) != cudaSuccess) return ATTN_ERR_CUDA;
     const int n_tiles = (int)((kv_rows + kKeys - 1) / kKeys);
     kh16 = static_cast<uint16_t*>(scratch);
     kfac = reinterpret_cast<float*>(static_cast<char*>(scratch) + fac_off);
@@ -683,6 +682,23 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+// Logical K/V rows a call reads (at least 1) and whether it has no keys.
+static long long kv_rows_of(const FlashArgs& a, bool* no_keys) {
+  long long kv_rows = a.causal ? a.base_pos + a.n_q : a.n_all;
+  if (kv_rows > a.cap) kv_rows = a.cap;
+  *no_keys = kv_rows < 1 || a.k == nullptr || a.v == nullptr;
+  return kv_rows < 1 ? 1 : kv_rows;
+}
+
+// K as fp16 (kv_rows x kv_row_stride) and one float per (128-key tile, kv head).
+size_t flash_tc_scratch_bytes(const FlashArgs& a) {
+  bool no_keys = false;
+  const long long kv_rows = kv_rows_of(a, &no_keys);
+  if (no_keys || a.n_q == 0) return 0;
+  return scratch_round(scratch_round((size_t)kv_rows * a.kv_row_stride * 2) +
+                       (size_t)((kv_rows + kKeys - 1) / kKeys) * a.G * sizeof(float));
+}
 
 bool flash_tc_supported(const FlashArgs& a, int prec) {
   if (prec != ATTN_TF32 && prec != ATTN_BF16) return false;

@@ -214,9 +214,30 @@ size_t decode_ticket_bytes(int groups);
 // Device address of the current device's status word (nullptr on failure).
 unsigned* device_status_word();
 
-// Stream-ordered scratch memory from a library-owned pool on the current
-// device that keeps freed memory reserved between calls.
+// Temporary scratch memory of a call.  With a workspace bound to the calling
+// thread (scratch_bind; attn_set_workspace), allocations are carved from it
+// in order, each start rounded up to 256 bytes, from offset 0 at every
+// scratch_begin_call(); otherwise they are stream-ordered allocations from a
+// library-owned pool on the current device that keeps freed memory reserved
+// between calls.  scratch_free of workspace memory does nothing.
+inline size_t scratch_round(size_t b) { return (b + 255) & ~size_t(255); }
+void scratch_bind(void* ws, size_t bytes);
+bool scratch_bound(size_t* bytes);
+void scratch_begin_call();
 cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s);
 cudaError_t scratch_free(void* p, cudaStream_t s);
+// The pool's reserved bytes (which = 0) or its high-water mark of bytes in
+// use (which = 1; reset to 0 afterwards if `reset`); trimming returns the
+// reserved memory that is not in use.
+size_t scratch_pool_stat(int which, bool reset);
+bool scratch_trim();
+
+// Scratch bytes each launcher requests (a sum of scratch_round'ed sizes; 0
+// when it needs none).  The launchers allocate exactly these.
+size_t flash_tc_scratch_bytes(const FlashArgs& a);
+size_t flash_bf16_scratch_bytes(const FlashArgs& a);
+size_t flash_simt_scratch_bytes(const FlashArgs& a);
+size_t backward_simt_scratch_bytes(const BwdArgs& a);
+size_t backward_bf16_scratch_bytes(const BwdArgs& a);
 
 }  // namespace attn

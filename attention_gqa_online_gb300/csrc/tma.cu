@@ -94,15 +94,64 @@ cudaMemPool_t scratch_pool() {
   }
   return g_pool[dev];
 }
+
+// A caller-owned workspace bound to this thread (attn_set_workspace): every
+// call's scratch is carved from it, from offset 0 at the start of each call
+// (calls on one stream run in order, so they can reuse the same bytes).
+thread_local void* t_ws = nullptr;
+thread_local size_t t_ws_bytes = 0;
+thread_local size_t t_ws_used = 0;
+
 }  // namespace
 
+void scratch_bind(void* ws, size_t bytes) {
+  t_ws = ws;
+  t_ws_bytes = ws != nullptr ? bytes : 0;
+  t_ws_used = 0;
+}
+
+bool scratch_bound(size_t* bytes) {
+  if (bytes != nullptr) *bytes = t_ws_bytes;
+  return t_ws != nullptr;
+}
+
+void scratch_begin_call() { t_ws_used = 0; }
+
 cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t s) {
+  if (t_ws != nullptr) {
+    const size_t off = scratch_round(t_ws_used);
+    if (off > t_ws_bytes || bytes > t_ws_bytes - off) return cudaErrorMemoryAllocation;
+    *p = static_cast<char*>(t_ws) + off;
+    t_ws_used = off + bytes;
+    return cudaSuccess;
+  }
   cudaMemPool_t pool = scratch_pool();
   if (pool == nullptr) return cudaErrorMemoryAllocation;
   return cudaMallocFromPoolAsync(p, bytes, pool, s);
 }
 
-cudaError_t scratch_free(void* p, cudaStream_t s) { return cudaFreeAsync(p, s); }
+cudaError_t scratch_free(void* p, cudaStream_t s) {
+  if (t_ws != nullptr && p >= t_ws && p < static_cast<char*>(t_ws) + t_ws_bytes) return cudaSuccess;
+  return cudaFreeAsync(p, s);
+}
+
+size_t scratch_pool_stat(int which, bool reset) {
+  cudaMemPool_t pool = scratch_pool();
+  if (pool == nullptr) return 0;
+  cudaMemPoolAttr attr = which == 0 ? cudaMemPoolAttrReservedMemCurrent : cudaMemPoolAttrUsedMemHigh;
+  uint64_t v = 0;
+  if (cudaMemPoolGetAttribute(pool, attr, &v) != cudaSuccess) return 0;
+  if (reset && which == 1) {
+    uint64_t zero = 0;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &zero);
+  }
+  return (size_t)v;
+}
+
+bool scratch_trim() {
+  cudaMemPool_t pool = scratch_pool();
+  return pool != nullptr && cudaMemPoolTrimTo(pool, 0) == cudaSuccess;
+}
 
 cudaStream_t side_stream() {
   static cudaStream_t streams[kMaxDevices] = {};

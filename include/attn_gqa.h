@@ -22,12 +22,16 @@
  *              takes scale as an argument (the cera shader's params[5]).
  *   Data       fp32 in, fp32 out, row-major, all pointers are DEVICE memory
  *              owned by the caller.  The library keeps no pointer after a call
- *              returns.  The device memory it allocates is temporary scratch
- *              (the 16-bit K/V operand copies of the tensor-core paths, K
- *              turned for RoPE, the backward's per-row values): stream-ordered
- *              on the call's stream, from a memory pool the library creates
- *              per device and keeps (freed blocks stay reserved for later
- *              calls).  Besides, every GPU that loads the library holds one
+ *              returns.  Some calls need temporary scratch (the 16-bit K/V
+ *              operand copies of the tensor-core paths, K turned for RoPE,
+ *              the backward's per-row values; sizes from the
+ *              attn_*_workspace_bytes queries).  With a workspace bound to the
+ *              calling thread (attn_set_workspace) it is carved from that
+ *              caller-owned buffer and the library allocates nothing.
+ *              Otherwise it is stream-ordered on the call's stream, from a
+ *              memory pool the library creates per device and keeps (freed
+ *              blocks stay reserved for later calls; attn_release_scratch
+ *              returns them).  Besides, every GPU that loads the library holds one
  *              fixed 4 MiB array for attn_decode_cached_noalloc (shared by
  *              all its calls on that device, kept until the process exits).
  *              The backward also runs one of its kernels on a library-owned
@@ -131,7 +135,7 @@ enum {
  */
 ATTN_API int attn_forward(const float *q, const float *k, const float *v, float *out, float *lse,
                  uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
-                 uint32_t head_dim, int mask, int prec, attn_stream_t stream);
+                 uint32_t head_dim, attn_mask_t mask, attn_prec_t prec, attn_stream_t stream);
 
 /*
  * Bytes of device workspace attn_decode_cached needs for these sizes on the
@@ -210,7 +214,7 @@ ATTN_API int attn_prefill(const float *q_batch, const float *k_cache, const floa
                  float *out_batch, uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads,
                  uint32_t head_dim, uint32_t kv_dim, uint32_t max_seq, float scale,
                  uint32_t start_pos, uint32_t q_stride, uint32_t out_stride, uint32_t q_base,
-                 int prec, attn_stream_t stream);
+                 attn_prec_t prec, attn_stream_t stream);
 
 /*
  * Sliding-window (local) attention: the three calls above with one more
@@ -230,7 +234,7 @@ ATTN_API int attn_prefill(const float *q_batch, const float *k_cache, const floa
  */
 ATTN_API int attn_forward_window(const float *q, const float *k, const float *v, float *out, float *lse,
                                  uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
-                                 uint32_t head_dim, int mask, int prec, uint32_t window, attn_stream_t stream);
+                                 uint32_t head_dim, attn_mask_t mask, attn_prec_t prec, uint32_t window, attn_stream_t stream);
 ATTN_API int attn_decode_cached_window(const float *q, const float *k_cache, const float *v_cache,
                                        const uint32_t *kv_pos_dev, float *out, uint32_t num_heads,
                                        uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq,
@@ -240,7 +244,7 @@ ATTN_API int attn_prefill_window(const float *q_batch, const float *k_cache, con
                                  float *out_batch, uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads,
                                  uint32_t head_dim, uint32_t kv_dim, uint32_t max_seq, float scale,
                                  uint32_t start_pos, uint32_t q_stride, uint32_t out_stride, uint32_t q_base,
-                                 int prec, uint32_t window, attn_stream_t stream);
+                                 attn_prec_t prec, uint32_t window, attn_stream_t stream);
 
 /*
  * Rotary position embedding (RoPE) fused into the forward.  The forward page
@@ -266,7 +270,7 @@ ATTN_API int attn_prefill_window(const float *q_batch, const float *k_cache, con
 ATTN_API int attn_rope_table(float *table, uint32_t max_pos, uint32_t head_dim, double base, attn_stream_t stream);
 ATTN_API int attn_forward_rope(const float *q, const float *k, const float *v, float *out, float *lse,
                                uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads, uint32_t num_kv_heads,
-                               uint32_t head_dim, int mask, int prec, uint32_t window, const float *rope_table,
+                               uint32_t head_dim, attn_mask_t mask, attn_prec_t prec, uint32_t window, const float *rope_table,
                                uint32_t table_rows, attn_stream_t stream);
 
 /*
@@ -305,7 +309,7 @@ ATTN_API int attn_prefill_paged(const float *q_batch, const float *k_pages, cons
                                 const uint32_t *block_table, float *out_batch, uint32_t n_queries, uint32_t n_heads,
                                 uint32_t n_kv_heads, uint32_t head_dim, uint32_t kv_dim, uint32_t page_rows,
                                 uint32_t num_pages, uint32_t max_blocks, float scale, uint32_t start_pos,
-                                uint32_t q_stride, uint32_t out_stride, uint32_t q_base, int prec, uint32_t window,
+                                uint32_t q_stride, uint32_t out_stride, uint32_t q_base, attn_prec_t prec, uint32_t window,
                                 attn_stream_t stream);
 
 /*
@@ -334,14 +338,15 @@ ATTN_API int attn_prefill_paged(const float *q_batch, const float *k_pages, cons
  * element is computed by one thread block, without atomics, so repeated
  * calls give identical bits.  Needs D % 4 == 0 and 16-byte-aligned pointers,
  * else ATTN_ERR_UNSUPPORTED.  Scratch (8 bytes per (row, head); with
- * ATTN_BF16 also bf16 copies of q, dout, k and v) comes from the library's
- * per-device pool.  q_seq == 0 is a no-op; kv_seq == 0 zeroes
+ * ATTN_BF16 also bf16 copies of q, dout, k and v) comes from the bound
+ * workspace or the library pool (see the Data rule above).  q_seq == 0 is a
+ * no-op; kv_seq == 0 zeroes
  * dq.  Errors otherwise as attn_forward, plus NULL out, dout, lse or
  * gradient pointers.
  */
 ATTN_API int attn_backward(const float *q, const float *k, const float *v, const float *out, const float *dout,
                            const float *lse, float *dq, float *dk, float *dv, uint32_t q_seq, uint32_t kv_seq,
-                           uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,
+                           uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, attn_mask_t mask, attn_prec_t prec,
                            uint32_t window, attn_stream_t stream);
 
 /*
@@ -354,7 +359,7 @@ ATTN_API int attn_backward(const float *q, const float *k, const float *v, const
  */
 ATTN_API int attn_backward_rope(const float *q, const float *k, const float *v, const float *out, const float *dout,
                                 const float *lse, float *dq, float *dk, float *dv, uint32_t q_seq, uint32_t kv_seq,
-                                uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, int mask, int prec,
+                                uint32_t num_heads, uint32_t num_kv_heads, uint32_t head_dim, attn_mask_t mask, attn_prec_t prec,
                                 uint32_t window, const float *rope_table, uint32_t table_rows,
                                 attn_stream_t stream);
 
@@ -390,6 +395,53 @@ ATTN_API int attn_decode_cached_noalloc(const float *q, const float *k_cache, co
                                         const uint32_t *kv_pos_dev, float *out, uint32_t num_heads,
                                         uint32_t num_kv_heads, uint32_t head_dim, uint32_t max_seq,
                                         attn_stream_t stream);
+
+/*
+ * Caller-owned scratch.  attn_set_workspace binds a DEVICE buffer of
+ * workspace_bytes bytes (256-byte aligned) to the calling thread: from then
+ * on every call this thread makes takes its temporary scratch from it, from
+ * offset 0 each call, and allocates nothing; a call whose scratch does not
+ * fit returns ATTN_ERR_INVALID_ARG before launching anything.
+ * attn_set_workspace(NULL, 0) returns to the library pool.  The buffer is
+ * read and written on the calls' streams: calls that share it must be
+ * ordered on one stream (or synchronised), and it must stay allocated until
+ * the last of them has run.  Errors: INVALID_ARG for a misaligned buffer.
+ *
+ * The queries give the bytes one call needs (0: none, or arguments the call
+ * would reject); a bound workspace must hold the largest of the calls it
+ * serves.
+ *   attn_forward_workspace_bytes   attn_forward, attn_forward_window and, with
+ *                                  rope != 0, attn_forward_rope
+ *   attn_prefill_workspace_bytes   attn_prefill, attn_prefill_window and
+ *                                  attn_prefill_paged (max_seq = page_rows *
+ *                                  max_blocks)
+ *   attn_backward_workspace_bytes  attn_backward and, with rope != 0,
+ *                                  attn_backward_rope
+ * Decode takes its workspace as an argument (attn_decode_workspace_bytes).
+ */
+ATTN_API int attn_set_workspace(void *workspace, size_t workspace_bytes);
+ATTN_API size_t attn_forward_workspace_bytes(uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads,
+                                             uint32_t num_kv_heads, uint32_t head_dim, attn_mask_t mask,
+                                             attn_prec_t prec, uint32_t window, int rope);
+ATTN_API size_t attn_prefill_workspace_bytes(uint32_t n_queries, uint32_t n_heads, uint32_t n_kv_heads,
+                                             uint32_t head_dim, uint32_t kv_dim, uint32_t max_seq,
+                                             uint32_t start_pos, uint32_t q_base, attn_prec_t prec,
+                                             uint32_t window);
+ATTN_API size_t attn_backward_workspace_bytes(uint32_t q_seq, uint32_t kv_seq, uint32_t num_heads,
+                                              uint32_t num_kv_heads, uint32_t head_dim, attn_prec_t prec, int rope);
+
+/*
+ * The library pool on the current device (the scratch of calls made without
+ * a bound workspace): attn_scratch_reserved_bytes is the memory it holds;
+ * attn_scratch_peak_bytes the most it has had in use at once since the last
+ * reset (reset != 0 resets it to 0 after reading); attn_release_scratch
+ * returns the reserved memory not in use (call it after synchronising the
+ * streams that used the pool).  Errors: ATTN_ERR_CUDA if the pool is not
+ * available.
+ */
+ATTN_API size_t attn_scratch_reserved_bytes(void);
+ATTN_API size_t attn_scratch_peak_bytes(int reset);
+ATTN_API int attn_release_scratch(void);
 
 /*
  * Waits for `stream`, then returns and clears the current device's status

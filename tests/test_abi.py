@@ -213,3 +213,30 @@ def test_backward_rope_rejects(lib):
     assert lib.attn_backward_rope(*args, FAKE, 7, None) == 1          # table one row short
     odd = [FAKE] * 9 + [8, 8, 2, 1, 63, 0, 0, 0]
     assert lib.attn_backward_rope(*odd, FAKE, 8, None) == 1           # odd head_dim
+
+
+def test_workspace_queries(lib):
+    """Scratch sizes per call: what the tensor-core paths copy K/V into, the
+    RoPE-turned K of the fp32 path, the backward's per-row values."""
+    r = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    n, H, G, D = 300, 8, 2, 128
+    tiles = (n + 127) // 128
+    # ATTN_BF16: fp16 K and bf16 V (4 bytes per K/V element pair), one float per (tile, kv head)
+    assert lib.attn_forward_workspace_bytes(n, n, H, G, D, 0, 2, 0, 0) == r(r(n * G * D * 4) + tiles * G * 4)
+    # ATTN_TF32: fp16 K only
+    assert lib.attn_forward_workspace_bytes(n, n, H, G, D, 0, 1, 0, 0) == r(r(n * G * D * 2) + tiles * G * 4)
+    assert lib.attn_forward_workspace_bytes(n, n, H, G, D, 0, 0, 0, 0) == 0
+    assert lib.attn_forward_workspace_bytes(n, n, H, G, D, 0, 0, 0, 1) == r(n * G * D * 4)
+    assert lib.attn_forward_workspace_bytes(n, n + 1, H, G, D, 0, 2, 0, 0) == 0  # causal needs kv_seq == q_seq
+    # prefill 40 queries from position 100 of a 300-row cache: keys 0..139 are read
+    assert lib.attn_prefill_workspace_bytes(40, H, G, D, G * D, 300, 100, 0, 2, 0) == r(r(140 * G * D * 4) + 2 * G * 4)
+    assert lib.attn_prefill_workspace_bytes(40, H, G, D, G * D, 100, 100, 0, 2, 0) == 0  # past the cache
+    assert lib.attn_backward_workspace_bytes(n, n, H, G, D, 0, 0) == r(n * H * 8)
+    assert lib.attn_backward_workspace_bytes(n, n, H, G, D, 0, 1) == r((n * H + n * G) * D * 4) + r(n * H * 8)
+    qe, ke = n * H * D, n * G * D
+    assert lib.attn_backward_workspace_bytes(n, n, H, G, D, 2, 0) == 2 * r(n * H * 4) + 2 * r(qe * 2) + 2 * r(ke * 2)
+
+
+def test_set_workspace_rejects_misaligned(lib):
+    assert lib.attn_set_workspace(FAKE + 16, 4096) == 1
+    assert lib.attn_set_workspace(None, 0) == 0
