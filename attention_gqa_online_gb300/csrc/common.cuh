@@ -17,6 +17,7 @@ __device__ __forceinline__ void record_status(unsigned* status, unsigned code) {
 
 // Wall-clock limit of every spin-wait in the library's kernels.
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+constexpr unsigned kWaitSliceNs = 2000;  // longest sleep of one bounded-wait step
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
@@ -58,6 +59,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep for up to `hint_ns` while the
+// phase is incomplete; completing the phase wakes it at once.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, unsigned parity, unsigned hint_ns) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Non-blocking test: has phase `parity` of `bar` completed?
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, unsigned parity) {
   unsigned ok;
@@ -93,7 +108,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // Sleeps until the phase completes (or 2 us pass, for the checks below).
+    if (mbar_try_wait_for(bar, parity, kWaitSliceNs)) return true;
     if (abort_flag != nullptr && *abort_flag != 0) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       record_status(status, ATTN_ERR_TIMEOUT);

@@ -28,32 +28,41 @@
 // 128): row r is (query i, head g*gs + j) with i*gs + j = rpb*block + r, so
 // each K/V tile feeds all gs query heads that share it.  Keys are walked in
 // tiles of 128, from the tile holding the block's first kept key to the one
-// holding its last.  Three score buffers
-// in tensor memory let Q K^T run up to three tiles ahead of P V, so the
-// softmax of one tile overlaps the products of the others.  The two softmax
-// warpgroups split every tile's columns (64 each) and swap their partial row
-// maxima through shared memory, so both hold the same reference max; it only
-// moves when a row's tile max exceeds it by more than 8 (so P <= 256), and
-// when it moves each group rescales its half of the single O accumulator
-// once P V of the previous tile has landed.
+// holding its last.
 //
-// Warp roles (384 threads):
+// Two score buffers S_0, S_1 and two P buffers in tensor memory let Q K^T of
+// tile j + 2 start as soon as the softmax has read S_(j%2) (P_j has its own
+// columns), so the tensor core is not held up by P V.  The two softmax
+// warpgroups take alternate key tiles (group 0 the even ones, group 1 the
+// odd ones), each thread a whole 128-column row, so while one group waits
+// for its scores the other computes exponentials.  The reference max that P
+// is taken against is one chain through the tiles: the warp of tile j reads
+// the reference its counterpart (same 32 rows, other group) left at tile
+// j - 1, moves it to the tile max when that exceeds it by more than 24 (so P
+// <= 2^24; a wide gap between the two only makes P large, which fp32
+// accumulation and bf16's 8-bit exponent carry without loss), and hands it
+// on through shared memory and a per-warp barrier.  When the reference
+// moves, the warp rescales its rows of the single O accumulator once P V of
+// tile j - 1 has landed.  Each group keeps the row sum of its own tiles;
+// the two sums are combined at the end.
+//
+// Warp roles (352 threads):
 //   warp 0      TMA producer: K tile (128 keys x D, 128-byte swizzle, K-major)
 //               and V tile (the same boxes; read as the MN-major operand of
 //               P V) into a shared-memory ring, in the order they are consumed.
-//   warp 1      tensor-memory allocation; issues S_(j%3) = Q K_j^T
-//               (A = Q in shared memory, B = K tile) once P V of tile j-3
-//               has released that buffer.
-//   warp 2      issues O += P_j V_j (A = P in TMEM over S_(j%3), B = V
-//               tile) in tile order once P_j is written.
-//   warps 4-11  softmax, two warpgroups: warp w of group c covers rows
-//               32(w%4)..+31 (its TMEM lanes) and score columns 64c..64c+63.
+//   warp 1      tensor-memory allocation; issues S_(j%2) = Q K_j^T
+//               (A = Q in shared memory, B = K tile) once the softmax has
+//               read the scores of tile j - 2 from that buffer.
+//   warp 2      issues O += P_j V_j (A = P_(j%2) in TMEM, B = V tile) in
+//               tile order once P_j is written.
+//   warps 3-10  softmax, two groups of four warps (3-6 and 7-10): warp w
+//               covers rows 32(w%4)..+31 (its TMEM lanes).
 // The issuing warps run their loops warp-uniformly; one elected lane issues.
-// Tensor memory (512 columns): S_b [128 b, 128 b + 128) for b = 0..2, O
-// [384, 384 + D).  Scores are in base-2 units once scaled (Q carries
-// scale * log2(e)).  The true max is tracked apart for the LSE.  Every wait is
-// bounded; a CTA whose pipeline breaks drains its copies and MMAs before it
-// releases tensor memory.
+// Tensor memory (512 columns): S_b [128 b, 128 b + 128) and P_b [256 + 64 b,
+// 256 + 64 b + 64) for b = 0, 1, O [384, 384 + D).  Scores are in base-2
+// units once scaled (Q carries scale * log2(e)).  The true max is tracked
+// apart for the LSE.  Every wait is bounded; a CTA whose pipeline breaks
+// drains its copies and MMAs before it releases tensor memory.
 #include <cfloat>
 
 #include "common.cuh"
@@ -65,13 +74,14 @@ namespace {
 
 constexpr int kRows = 128;                 // packed rows per CTA (MMA M)
 constexpr int kKeys = 128;                 // keys per tile
-constexpr int kThreads = 384;
+constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kOperandBytes = 192 * 1024;  // Q tile + K/V ring
 constexpr int kMaxRing = 12;
-constexpr int kSBuf = 3;                   // score buffers
-constexpr int kColO = 384;                 // S_b at 128 b; O at 384
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kSBuf = 2;                   // score buffers (and P buffers)
+constexpr int kColP = 256;                 // S_b at 128 b, P_b at 256 + 64 b, O at 384
+constexpr int kColO = 384;
+constexpr float kRescaleThreshold = 24.0f;  // log2 units: P <= 2^24
 constexpr int kFacCache = 512;             // K tile powers of two a CTA keeps in shared memory
 
 struct __align__(1024) Bf16Smem {
@@ -79,13 +89,17 @@ struct __align__(1024) Bf16Smem {
   uint64_t kv_full[kMaxRing];
   uint64_t kv_empty[kMaxRing];
   uint64_t s_full[kSBuf];
+  uint64_t s_free[kSBuf];  // the softmax has read S_b of the tile
+  uint64_t mref_bar[4][2];  // [row quarter][tile parity]: the tile's reference max is in mref
   uint64_t p_ready[kSBuf];
   uint64_t pv_done[2];     // P V of tile j completes phase j/2 of pv_done[j & 1]
   uint64_t q_full;         // the fp32 Q block has landed in the staging area
   uint64_t q_ready;        // the bf16 Q tile is written
   uint64_t o_final;        // every P V has completed
   uint64_t drain[2];
-  float red_max[2][2][kRows];  // [tile parity][group][row] partial tile maxima
+  float mref[2][kRows];        // [tile parity][row] reference max handed from one tile's group to the next
+  float red_m[2][kRows];       // [group][row] the group's last reference max
+  float red_t[2][kRows];       // [group][row] the group's true max
   float red_l[2][kRows];       // [group][row] partial row maxima of Q, then partial row sums
   float kfac[kFacCache];       // powers of two of the CTA's K tiles jt0, jt0 + 1, ...
   uint32_t tmem_base;
@@ -150,7 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < kSBuf; ++b) {
       mbar_init(&sm.s_full[b], 1);
-      mbar_init(&sm.p_ready[b], 8);
+      mbar_init(&sm.s_free[b], 4);
+      for (int q4 = 0; q4 < 4; ++q4) mbar_init(&sm.mref_bar[q4][b], 32);
+      mbar_init(&sm.p_ready[b], 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.pv_done[b], 1);
@@ -226,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         for (int j = 0; ok && j < nt; ++j) {
           const int pk = k_pos(j), b = j % kSBuf;
-          ok = wait(&sm.kv_full[pk % kRing], pk / kRing) && (j < kSBuf || wait(&sm.pv_done[(j - 3) & 1], (j - 3) >> 1));
+          ok = wait(&sm.kv_full[pk % kRing], pk / kRing) && (j < kSBuf || wait(&sm.s_free[b], (j - kSBuf) / kSBuf));
           if (!ok) break;
           tc::fence_after_sync();
           const uint64_t dk = dk0 + slot_off(pk);
@@ -256,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c4 = 0; c4 < kKeys / 64; ++c4) {
             const uint64_t c = 4 * st * c4;
-            const uint32_t pa = tmem + kKeys * b + 32 * c4;  // P: 8 columns (16 keys) per K step
+            const uint32_t pa = tmem + kColP + 64 * b + 32 * c4;  // P: 8 columns (16 keys) per K step
             tc::mma4_f16_ts(tmem + kColO, pa, pa + 8, pa + 16, pa + 24, dv + c, dv + c + st, dv + c + 2 * st,
                             dv + c + 3 * st, idesc_pv, (j > 0 || c4 > 0) ? 1u : 0u);
           }
@@ -268,9 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(&sm.drain[1], 0, a.status);
       }
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------------------ softmax / epilogue
-    const int grp = (warp - 4) >> 2;           // column group 0 or 1
+    const int grp = (warp - 3) >> 2;           // group 0 (warps 3-6) or 1 (warps 7-10)
     const int r = 32 * (warp & 3) + lane;      // row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const long long qi = i0 + r / gs;         // packed row blk * rpb + r
@@ -335,71 +351,84 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(&sm.q_ready);
     if (early_q) grid_dependency_wait();
     // The K tiles' powers of two (the pre-pass's output), read once.
-    for (int i = 32 * (warp - 4) + lane; i < min(nt, kFacCache); i += kSoftmaxThreads)
+    for (int i = 32 * (warp - 3) + lane; i < min(nt, kFacCache); i += kSoftmaxThreads)
       sm.kfac[i] = kfac[(long long)(jt0 + i) * a.G + g];
     named_barrier(2, kSoftmaxThreads);
 
     const uint32_t o_col = tmem + lane_base + kColO;
-    constexpr int kHalfD = D / 2;  // O columns per group
+    // Group grp takes key tiles j = grp, grp + 2, ...: whole 128-column rows.
+    // Each group keeps its own row sum and true max against the reference it
+    // last used; the two are combined at the end.
     float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
-    // The power of two of K tile jt0 + j of this kv head, read one tile ahead.
     auto tile_fac = [&](int j) {
       return j < kFacCache ? sm.kfac[j] : __ldg(kfac + (long long)(jt0 + j) * a.G + g);
     };
-    float f_next = nt > 0 ? tile_fac(0) : 1.f;
-    for (int j = 0; j < nt; ++j) {
+    for (int j = grp; j < nt; j += 2) {
       const int b = j % kSBuf;
-      const uint32_t s_col = tmem + lane_base + kKeys * b + 64 * grp;
+      const uint32_t s_col = tmem + lane_base + kKeys * b;
       // Raw score -> base-2 units (at least FLT_MIN, so a masked -inf stays -inf).
-      const float cf = fmaxf(f_row * f_next, FLT_MIN);
+      const float cf = fmaxf(f_row * tile_fac(j), FLT_MIN);
       mbar_wait_bounded(&sm.s_full[b], (unsigned)((j / kSBuf) & 1), a.status, &sm.abort);
       tc::fence_after_sync();
-      uint32_t s[2][32];
+      uint32_t s[4][32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) tc::tmem_ld32(s_col + 32 * c, s[c]);
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_col + 32 * c, s[c]);
       tc::tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) tc::reg_fence(s[c]);
+      for (int c = 0; c < 4; ++c) tc::reg_fence(s[c]);
+      // S_b may take the scores of tile j + 2 now.
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.s_free[b]);
 
-      const int key0 = (jt0 + j) * kKeys + 64 * grp;  // key of this half's first column
-      if (key0 - 64 * grp + kKeys > n_min) {  // the tile crosses some row's window end
+      const int key0 = (jt0 + j) * kKeys;  // key of the tile's first column
+      if (key0 + kKeys > n_min) {          // the tile crosses some row's window end
         const int lim = n_r - key0;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (32 * c + e >= lim) s[c][e] = __float_as_uint(-INFINITY);
       }
-      if (key0 - 64 * grp < lo_max) {  // ... or some row's window start
+      if (key0 < lo_max) {  // ... or some row's window start
         const int lim = lo_r - key0;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (32 * c + e < lim) s[c][e] = __float_as_uint(-INFINITY);
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < 64; i += 8)
+      for (int i = 0; i < 128; i += 8)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mx[k] = max3(mx[k], __uint_as_float(s[i >> 5][(i & 31) + 2 * k]), __uint_as_float(s[i >> 5][(i & 31) + 2 * k + 1]));
-      sm.red_max[j & 1][grp][r] = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
-      named_barrier(1, kSoftmaxThreads);  // both halves of every row are read and maxed
-      const float tmax = cf * fmaxf(sm.red_max[j & 1][0][r], sm.red_max[j & 1][1][r]);
-      if (j + 1 < nt) f_next = tile_fac(j + 1);
+      const float tmax = cf * max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       m_true = fmaxf(m_true, tmax);
-      const float m_prev = m_ref;
-      if (tmax > m_ref + kRescaleThreshold) m_ref = tmax;  // also for the first finite tile max
-      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
-      // P = 2^(S - m) as bf16 pairs: this group's 64 values become 32
-      // columns at 32 grp of S_b (the other group has read its scores: the
-      // barrier above).  Chunk c's 32 values are packed in place into s[c]
-      // and stored at column 32 grp + 16 c.  The row sum is taken in fp32.
+      // The reference left by tile j-1, then this tile's, handed to tile j+1.
+      // Rows are handed over warp to warp: the warps of both groups that
+      // cover the same 32 rows share barrier mref_bar[warp & 3][parity].
+      float m_prev = m_ref;
+      if (j >= 1) {
+        mbar_wait_bounded(&sm.mref_bar[warp & 3][(j - 1) & 1], (unsigned)(((j - 1) >> 1) & 1), a.status, &sm.abort);
+        m_prev = sm.mref[(j - 1) & 1][r];
+      }
+      const float m_new = (tmax > m_prev + kRescaleThreshold) ? tmax : m_prev;  // also for the first finite tile max
+      if (j + 1 < nt) {
+        sm.mref[j & 1][r] = m_new;
+        mbar_arrive(&sm.mref_bar[warp & 3][j & 1]);
+      }
+      const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
+
+      // P = 2^(S - m) as bf16 pairs: chunk c's 32 values are packed in
+      // place into s[c], then stored at column 16 c of P_b once P V of tile
+      // j - 2 (the last reader of P_b) has completed.  The row sum is taken
+      // in fp32.
       float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float x0 = __uint_as_float(s[c][e]), x1 = __uint_as_float(s[c][e + 1]);
@@ -409,27 +438,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           add2(sum[2 * k], sum[2 * k + 1], p0, p1);
           s[c][e >> 1] = tc::pack_bf16(p0, p1);
         }
-        tc::tmem_st16(tmem + lane_base + kKeys * b + 32 * grp + 16 * c, s[c]);
       }
+      if (j >= kSBuf) {
+        mbar_wait_bounded(&sm.pv_done[j & 1], (unsigned)(((j - 2) >> 1) & 1), a.status, &sm.abort);
+        tc::fence_after_sync();
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_st16(tmem + lane_base + kColP + 64 * b + 16 * c, s[c]);
       const float tsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-      const float corr = (m_ref != m_prev) ? ex2(m_prev - m_ref) : 1.f;  // m_prev = -inf gives 0
-      l = l * corr + tsum;
+      // This group's sum moves to the new reference (m_ref = -inf: l is 0, the factor 0).
+      l = l * ((m_new != m_ref) ? ex2(m_ref - m_new) : 1.f) + tsum;
+      m_ref = m_new;
 
       // O holds tiles 0..j-1 against m_prev once P V of tile j-1 has landed;
-      // P V of tile j waits for p_ready.  Rescale this group's half of O when
-      // any row of the warp moved its reference.
-      if (j >= 1 && __any_sync(0xffffffffu, m_ref != m_prev)) {
+      // P V of tile j waits for p_ready.  Rescale the row's O when any row of
+      // the warp moved its reference at this tile.
+      if (j >= 1 && __any_sync(0xffffffffu, m_new != m_prev)) {
+        const float corr = (m_new != m_prev) ? ex2(m_prev - m_new) : 1.f;  // m_prev = -inf gives 0
         mbar_wait_bounded(&sm.pv_done[(j - 1) & 1], (unsigned)(((j - 1) >> 1) & 1), a.status, &sm.abort);
         tc::fence_after_sync();
 #pragma unroll
-        for (int c = 0; c < kHalfD / 32; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          tc::tmem_ld32(o_col + grp * kHalfD + 32 * c, o);
+          tc::tmem_ld32(o_col + 32 * c, o);
           tc::tmem_ld_wait();
           tc::reg_fence(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-          tc::tmem_st32(o_col + grp * kHalfD + 32 * c, o);
+          tc::tmem_st32(o_col + 32 * c, o);
         }
       }
       tc::tmem_st_wait();
@@ -438,13 +474,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sm.p_ready[b]);
     }
 
-    // Epilogue: out = O / l, lse = (max, log sum).
+    // Epilogue: out = O / l, lse = (max, log sum).  The row's reference is
+    // the larger of the two groups' last ones (it only grows along the
+    // chain); each group's sum is moved onto it.
     sm.red_l[grp][r] = l;
+    sm.red_m[grp][r] = m_ref;
+    sm.red_t[grp][r] = m_true;
     if (nt > 0) mbar_wait_bounded(&sm.o_final, 0, a.status, &sm.abort);
     tc::fence_before_sync();
     named_barrier(1, kSoftmaxThreads);
     tc::fence_after_sync();
-    const float l_row = sm.red_l[0][r] + sm.red_l[1][r];
+    const float m_fin = fmaxf(sm.red_m[0][r], sm.red_m[1][r]);
+    float l_row = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      if (sm.red_l[k][r] > 0.f) l_row += sm.red_l[k][r] * ex2(sm.red_m[k][r] - m_fin);
+    m_true = fmaxf(sm.red_t[0][r], sm.red_t[1][r]);
+    m_ref = m_fin;
     const float inv = (l_row == 0.f) ? 0.f : 1.f / l_row;
     // O / l leaves by TMA tensor stores.  Each group stages its D/2 columns in
     // the (now idle) K/V ring as 32-float chunks of 128 rows x 128 bytes, in
@@ -453,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (16-byte unit u of row r at u ^ (r & 7)); one thread then stores every
     // chunk with one box each.  Rows past n_q fall outside the tensor and are
     // not written, nor are the idle rows past (128/gs)*gs.
+    constexpr int kHalfD = D / 2;          // O columns per group
     constexpr int kOChunks = kHalfD / 32;  // 32-float chunks per group
     unsigned char* const ostage = ring;   // [group][chunk][128 rows][128 bytes]
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the ring was last written by TMA
