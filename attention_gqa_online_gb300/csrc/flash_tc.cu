@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 4 && lane == 0) {
       for (int k = 0; k < 2 * kOChunks; ++k) tma_store_3d(&tm_o, ostage + k * (kRows * 128), 32 * k, g * gs, (int)i0);
       bulk_commit();
-      bulk_wait_all();  // the staging memory stays live, and the stores complete, before the CTA exits
+      bulk_wait_read_all();  // the staging memory stays live until the stores have read it
     }
     if (grp == 0 && row_ok && a.lse != nullptr) {
       float* l2 = a.lse + (qi * a.H + h) * 2;
