@@ -368,7 +368,7 @@ def run_ours(args, world, rank, local):
 
     if rank == 0:
         sampler.stop()
-        traffic = profile_traffic("decode_split_kernel", "attention_gqa_online_gb300/csrc/decode.cu")
+        traffic = profile_traffic("decode_split_kernel_kvpos16383", "attention_gqa_online_gb300/csrc/decode.cu")
         line = {
             "metric": "decode K/V-stream bandwidth", "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -459,18 +459,33 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
         res["_launches"] += n + args.warmup
         return e0.elapsed_time(e1) / n
 
-    def roof(prec, tf, kernel):
+    # Committed ncu summaries per (precision, workload): profiles/<tag>.md and
+    # the kernel source it was captured from.
+    flash_src = {A.ATTN_BF16: ("flash_bf16_kernel", "attention_gqa_online_gb300/csrc/flash_bf16.cu"),
+                 A.ATTN_TF32: ("flash_tc_kernel", "attention_gqa_online_gb300/csrc/flash_tc.cu"),
+                 A.ATTN_FP32: ("flash_simt_kernel", "attention_gqa_online_gb300/csrc/flash_simt.cu")}
+
+    def roof(prec, tf, kernel, workload=None, prof=None):
+        """Roofline of the line's dominant kernel; `traffic` from profiles/<kernel>_<workload>.md
+        (or the (tag, source) pair `prof`) when that summary exists and matches the kernel's
+        current source."""
+        traffic = None
+        if prof is not None:
+            traffic = profile_traffic(*prof)
+        elif workload is not None and prec in flash_src:
+            tag, src = flash_src[prec]
+            traffic = profile_traffic(tag + "_" + workload, src)
         if prec == A.ATTN_BF16:
             pk = peaks["bf16_tflops"]
             return {"bound": "tensor", "achieved": tf, "peak": pk, "unit": "TFLOP/s", "frac": tf / pk,
-                    "traffic": None, "kernel": kernel, "peak_source": "%s bf16 dense, burst" % peak_src}
+                    "traffic": traffic, "kernel": kernel, "peak_source": "%s bf16 dense, burst" % peak_src}
         if prec == A.ATTN_TF32:
             pk = tf32_peak(peaks)
             return {"bound": "tensor", "achieved": tf, "peak": pk, "unit": "TFLOP/s", "frac": tf / pk,
-                    "traffic": None, "kernel": kernel,
+                    "traffic": traffic, "kernel": kernel,
                     "peak_source": "%s bf16 %.0f TFLOP/s x 1.1/2.25 (nominal TF32/bf16)" % (peak_src, peaks["bf16_tflops"])}
         return {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
-                "traffic": None, "kernel": kernel,
+                "traffic": traffic, "kernel": kernel,
                 "peak_source": "fp32 FMA: %d SMs x 128 lanes x 2 x %.0f MHz" % (sms, sm_mhz)}
 
     def forward_lines(prefix, window, what, rope=False, q_seq=None):
@@ -498,9 +513,10 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
                     raise RuntimeError("forward failed: %d" % rc)
             ms = timed(fwd_step, steps)
             tf = forward_flops(window, f["q_seq"]) / (ms * 1e-3) / 1e12
+            plain = not rope and not window and q_seq is None
             res[prefix + name] = {
                 "workload": what, "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "prec": name,
-                "roofline": roof(prec, tf, kern), "l2": "inputs 192 MiB > L2"}
+                "roofline": roof(prec, tf, kern, "forward_q8192" if plain else None), "l2": "inputs 192 MiB > L2"}
 
     variants = ((A.ATTN_TF32, "tf32", "flash_tc_kernel<128> (tf32)"),
                 (A.ATTN_BF16, "bf16", "flash_bf16_kernel<128> (fp16 QK, bf16 PV) + kv_prep16 pre-pass"),
@@ -527,7 +543,7 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
             res["prefill_" + name] = {
                 "workload": "prefill 512 queries start_pos=1536 max_seq=2048 32/8 heads D=128",
                 "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "prec": name,
-                "roofline": roof(prec, tf, kern), "l2": "rotating %d input sets" % n_rot}
+                "roofline": roof(prec, tf, kern, "prefill_512q"), "l2": "rotating %d input sets" % n_rot}
         del bufs
 
     if only in ("all", "forward"):
@@ -550,6 +566,8 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
             raise RuntimeError("attn_forward failed: %d" % rc)
         gout = torch.randn(qd.shape, device=dev, generator=torch.Generator(device=dev).manual_seed(3))
         dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        bwd_prof = {A.ATTN_BF16: ("bwd_dkdv_tc_kernel_backward_q8192", "attention_gqa_online_gb300/csrc/bwd_tc.cu"),
+                    A.ATTN_FP32: ("bwd_dkdv_kernel_backward_q8192", "attention_gqa_online_gb300/csrc/backward.cu")}
         for prec, name, kern, nsteps in (
                 (A.ATTN_BF16, "bf16", "bwd_dkdv_tc_kernel<128> + bwd_dq_tc_kernel<128> (+ prep, bf16 pre-passes)",
                  steps),
@@ -567,7 +585,7 @@ def run_extras(args, A, lib, synthetic, dev, stream, sh, l2, sms, peaks, peak_sr
                 "workload": "causal backward (dq, dk, dv) q_seq=8192 32/8 heads D=128, Q,K N(0,9)", "value": tf,
                 "unit": "TFLOP/s", "ms_per_step": ms, "prec": name,
                 "flops": "2.5x the forward's: 10 D per (row, head, kept key), the five products of the gradient",
-                "roofline": roof(prec, tf, kern), "l2": "inputs 320 MiB > L2"}
+                "roofline": roof(prec, tf, kern, prof=bwd_prof[prec]), "l2": "inputs 320 MiB > L2"}
         del qd, kd, vd, outf, gout, dq, dk, dv
 
     if only in ("all", "paged"):

@@ -69,13 +69,16 @@
  *              QK^T takes fp16 operands (11 significant bits) under powers
  *              of two, one per query row and one per 128-key tile of a kv
  *              head, that keep every value below 2^15 whatever the fp32
- *              magnitudes; PV takes bf16 operands (P <= 256 and V).  K and V
- *              are converted by a pre-pass, Q and P on their way into the
- *              tensor core.
- *              Tensor-core precisions need D in {64, 128}, gs a power of two
- *              <= 128, 16-byte aligned pointers, Q/out row strides that are
- *              multiples of 4 floats and K/V row strides that are multiples
- *              of 8 floats; otherwise they return ATTN_ERR_UNSUPPORTED.
+ *              magnitudes; PV takes bf16 operands (P <= 2^24 and V; the
+ *              fp32 accumulators carry |V| * keys * 2^24 below fp32's range
+ *              for any |V| < 2^70).  K and V are converted by a pre-pass, Q
+ *              and P on their way into the tensor core.
+ *              Tensor-core precisions need D in {64, 128}, 1 <= gs <= 128
+ *              (a thread block packs 128/gs queries of gs heads; when gs
+ *              does not divide 128 the remaining rows idle), 16-byte aligned
+ *              pointers, Q/out row strides that are multiples of 4 floats
+ *              and K/V row strides that are multiples of 8 floats; otherwise
+ *              they return ATTN_ERR_UNSUPPORTED.
  *              ATTN_FP32 accepts any 1 <= D <= 128.
  */
 #ifndef ATTN_GQA_H
