@@ -92,8 +92,10 @@ def load_library(path=None):
     return lib
 
 
-def _addr(x, name, dtype=None):
-    """Device address of a tensor (checked to be CUDA and of `dtype`), an int, or None."""
+def _addr(x, name, dtype=None, host_ok=False):
+    """Device address of a tensor (checked to be CUDA and of `dtype`), an int, or None.
+    With host_ok, a pinned host tensor is accepted too (its address is valid on
+    the device under unified addressing)."""
     if x is None:
         return None
     if isinstance(x, int):
@@ -101,8 +103,8 @@ def _addr(x, name, dtype=None):
     import torch
     if not isinstance(x, torch.Tensor):
         raise TypeError("%s must be a CUDA tensor, a device address or None" % name)
-    if not x.is_cuda:
-        raise ValueError("%s must be in device memory" % name)
+    if not x.is_cuda and not (host_ok and x.is_pinned()):
+        raise ValueError("%s must be in device memory%s" % (name, " or pinned host memory" if host_ok else ""))
     if dtype is not None and x.dtype != dtype:
         raise ValueError("%s must be %s, got %s" % (name, dtype, x.dtype))
     return x.data_ptr()
@@ -200,9 +202,9 @@ def attn_decode_cached(q, k_cache, v_cache, kv_pos_dev, out, num_heads, num_kv_h
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check(load_library().attn_decode_cached(
-        _addr(q, "q", f), _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f),
-        _addr(kv_pos_dev, "kv_pos_dev"),
-        _addr(out, "out", f), num_heads, num_kv_heads, head_dim, max_seq,
+        _addr(q, "q", f, True), _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f),
+        _addr(kv_pos_dev, "kv_pos_dev", None, True),
+        _addr(out, "out", f, True), num_heads, num_kv_heads, head_dim, max_seq,
         _addr(workspace, "workspace"), workspace_bytes, _stream(stream)), "attn_decode_cached")
 
 
@@ -248,8 +250,9 @@ def attn_decode_append(q, k_new, v_new, k_cache, v_cache, kv_pos_dev, out, num_h
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check(load_library().attn_decode_append(
-        _addr(q, "q", f), _addr(k_new, "k_new", f), _addr(v_new, "v_new", f), _addr(k_cache, "k_cache", f),
-        _addr(v_cache, "v_cache", f), _addr(kv_pos_dev, "kv_pos_dev"), _addr(out, "out", f), num_heads,
+        _addr(q, "q", f, True), _addr(k_new, "k_new", f, True), _addr(v_new, "v_new", f, True),
+        _addr(k_cache, "k_cache", f), _addr(v_cache, "v_cache", f), _addr(kv_pos_dev, "kv_pos_dev", None, True),
+        _addr(out, "out", f, True), num_heads,
         num_kv_heads, head_dim, max_seq, _addr(workspace, "workspace"), workspace_bytes, _stream(stream)),
         "attn_decode_append")
 

@@ -181,7 +181,7 @@ ATTN_API int attn_decode_cached(const float *q, const float *k_cache, const floa
 
 /*
  * Cached decode of a new token that first appends its own K and V row: the
- * [G*D] rows k_new and v_new (DEVICE memory) are written into row *kv_pos_dev
+ * [G*D] rows k_new and v_new are written into row *kv_pos_dev
  * of k_cache and v_cache, then the call is attn_decode_cached over positions
  * 0..kv_pos (the new row included).  The pages leave filling the cache to
  * the host framework; this entry point saves a serving step the separate
@@ -190,6 +190,15 @@ ATTN_API int attn_decode_cached(const float *q, const float *k_cache, const floa
  * max_seq writes nothing and records ATTN_ERR_INVALID_ARG, as in
  * attn_decode_cached.  Arguments, workspace and errors otherwise as
  * attn_decode_cached, plus NULL k_new / v_new.
+ *
+ * Step I/O in host memory.  On the shapes the split decode covers (D in
+ * {64, 128}, gs = H/G a power of two up to 32; the same holds for
+ * attn_decode_cached), q, k_new, v_new, kv_pos_dev and out may also be
+ * pinned host memory (cudaHostAlloc / cudaMallocHost, whose addresses are
+ * valid on the device under unified addressing): the kernel reads the
+ * step's inputs and writes its output across the host link itself, so a
+ * serving step needs no staging copies.  The caches and the workspace must
+ * be device memory.
  */
 ATTN_API int attn_decode_append(const float *q, const float *k_new, const float *v_new, float *k_cache,
                                 float *v_cache, const uint32_t *kv_pos_dev, float *out, uint32_t num_heads,

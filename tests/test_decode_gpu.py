@@ -118,3 +118,33 @@ def test_decode_append(cuda_lib, orc, H, G, D, max_seq):
                                 max_seq, ws)
     assert cuda_lib.attn_get_status() == cuda_lib.ATTN_ERR_INVALID_ARG
     assert np.array_equal(dk.cpu().numpy(), before)
+
+
+@pytest.mark.parametrize("H,G,D,max_seq", [(32, 8, 128, 4096), (16, 2, 64, 700)])
+def test_decode_append_pinned_host_io(cuda_lib, orc, H, G, D, max_seq):
+    """A serving step with its small inputs (q, the new K/V row, kv_pos) and its
+    output in pinned host memory, read and written by the split decode kernel
+    directly, against the oracle."""
+    q, kc, vc = synthetic.decode_inputs(max_seq, H, G, D, seed=max_seq + 5)
+    rng = np.random.default_rng(max_seq + 1)
+    kh, vh = kc.numpy().copy(), vc.numpy().copy()
+    dk, dv = dev(kc), dev(vc)
+    ws, _ = make_state(cuda_lib, H, G, D, max_seq)
+    qh = torch.empty((1, H * D)).pin_memory()
+    knh, vnh = torch.empty(G * D).pin_memory(), torch.empty(G * D).pin_memory()
+    posh = torch.zeros(4, dtype=torch.int32).pin_memory()
+    outh = torch.empty((1, H * D)).pin_memory()
+    for kv_pos in (0, 5, max_seq // 3, max_seq - 1):
+        kn = rng.standard_normal(G * D).astype(np.float32)
+        vn = rng.standard_normal(G * D).astype(np.float32)
+        qn = rng.standard_normal((1, H * D)).astype(np.float32)
+        qh.copy_(torch.from_numpy(qn)); knh.copy_(torch.from_numpy(kn)); vnh.copy_(torch.from_numpy(vn))
+        posh[0] = kv_pos
+        outh.fill_(float("nan"))
+        cuda_lib.attn_decode_append(qh, knh, vnh, dk, dv, posh, outh, H, G, D, max_seq, ws)
+        torch.cuda.synchronize()
+        assert cuda_lib.attn_get_status() == 0
+        kh[kv_pos], vh[kv_pos] = kn, vn
+        assert np.array_equal(dk.cpu().numpy(), kh) and np.array_equal(dv.cpu().numpy(), vh)
+        ref = orc.decode(qn, kh, vh, kv_pos, H, G, D, max_seq)
+        assert_out_close(outh.numpy(), ref, FP32, float(np.abs(vh).max()), "pinned append kv_pos=%d" % kv_pos)
