@@ -144,3 +144,33 @@ def test_bf16_mixed_magnitude_tile(cuda_lib, orc):
     out, _ = run_forward(cuda_lib, q, k, v, q_seq, q_seq, H, G, D, FULL, BF16)
     ro, _ = orc.forward(q.numpy(), k.numpy(), v.numpy(), q_seq, q_seq, H, G, D, FULL)
     assert_out_close(out, ro, BF16, float(v.abs().max()), "mixed-magnitude tile")
+
+
+@pytest.mark.parametrize("prec", PRECS)
+def test_reference_max_moves_at_every_tile(cuda_lib, orc, prec):
+    """Rows whose score max rises by 26 (base 2) at every 128-key tile, just
+    above the tensor kernels' rescale threshold of 24: every tile moves the
+    reference max, so O and the row sums are rescaled at every tile, and the
+    16-bit kernel's two softmax groups hand the reference over at every tile.
+    A skipped or wrong rescale leaves an earlier tile's value at weight ~1
+    instead of 2^-26: an error of order max|V|.  Q is the unit vector e_0 (plus
+    small noise); the last key of tile j is e_0 times the value that gives
+    score 26 (j + 1) in base 2; the other keys are N(0,1)."""
+    q_seq = kv_seq = 128 * 12
+    H, G, D = 8, 2, 128
+    gen = torch.Generator().manual_seed(17)
+    q = 0.01 * torch.randn((q_seq, H * D), generator=gen)
+    q.view(q_seq, H, D)[:, :, 0] += 1.0
+    k = torch.randn((kv_seq, G * D), generator=gen)
+    v = torch.randn((kv_seq, G * D), generator=gen)
+    scale_log2 = (1.0 / math.sqrt(D)) * 1.4426950408889634
+    for j in range(kv_seq // 128):
+        kv = k.view(kv_seq, G, D)[128 * j + 127]
+        kv.zero_()
+        kv[:, 0] = 26.0 * (j + 1) / scale_log2
+    out, lse = run_forward(cuda_lib, q, k, v, q_seq, kv_seq, H, G, D, CAUSAL, prec)
+    rows = list(range(0, q_seq, 37)) + [127, 128, 255, 256, q_seq - 1]
+    ro, rl = orc.forward(q.numpy(), k.numpy(), v.numpy(), q_seq, kv_seq, H, G, D, CAUSAL, rows=rows)
+    sel = np.asarray(rows)
+    assert_out_close(out[sel], ro[sel], prec, float(v.abs().max()), "score max rising 26 per tile")
+    assert_lse_close(lse[sel], rl[sel], prec, float(np.abs(rl[sel][..., 0]).max()), "score max rising 26 per tile")
