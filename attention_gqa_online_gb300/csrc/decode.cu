@@ -56,6 +56,7 @@ struct __align__(128) DecodeSmem {
   float red_m[kCWarps][GS];
   float red_l[kCWarps][GS];
   float red_o[kCWarps][GS][D];
+  float wts[kCWarps][kNg * 4 + 1][GS];  // per warp: P of its positions for every head, then the corrections
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t merge_bar;
@@ -201,15 +202,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   __syncthreads();
 
-  float m_run[GS], l_run[GS];
   float acc[GS][VP];
 #pragma unroll
-  for (int h = 0; h < GS; ++h) {
-    m_run[h] = -INFINITY;
-    l_run[h] = 0.f;
+  for (int h = 0; h < GS; ++h)
 #pragma unroll
     for (int e = 0; e < VP; ++e) acc[h][e] = 0.f;
-  }
 
   if (warp == kCWarps) {
     // ---------------- producer: one [kT x D] tile of K and of V per stage
@@ -241,6 +238,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         float4 x = *reinterpret_cast<const float4*>(a.q + (size_t)(g * GS + h) * D + 4 * qc + 32 * u);
         qr[h][u] = make_float4(x.x * sl2, x.y * sl2, x.z * sl2, x.w * sl2);
       }
+    // The eight lanes of a position reduce their GS partial dot products by
+    // recursive halving: at each level a lane keeps half of its heads and
+    // adds its partner's values for them, so after three levels it holds the
+    // full score of one head, h_own (lanes 8p + c, 8p + c' with equal h_own
+    // hold the same value).  The online softmax state of h_own lives in the
+    // lane; the weights and corrections every lane needs for P V go through
+    // the warp's slot of sm.wts.
+    int h_own = 0;
+    {
+      int n = GS;
+#pragma unroll
+      for (int o = 4; o >= 1; o >>= 1)
+        if (n > 1) {
+          n >>= 1;
+          if (qc & o) h_own += n;
+        }
+    }
+    float m_own = -INFINITY, l_own = 0.f;
+    // One writer per (position, head): the lowest lane c of each head.
+    const bool writer = ((qc & ((8 / (GS < 8 ? GS : 8)) - 1)) == 0);
+    float(*wts)[GS] = sm.wts[warp];
     for (int st = 0; st < n_st; ++st) {
       const int slot = st % kStages;
       mbar_wait_bounded(&sm.full[slot], (st / kStages) & 1, a.status, &sm.abort);
@@ -249,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const float* ks = sm.k[slot];
       const float* vs = sm.v[slot];
 
-      // Scores of this warp's kNg groups of four positions.
-      float sc[kNg][GS];
+      // Scores of this warp's kNg groups of four positions, head h_own.
+      float sc[kNg];
 #pragma unroll
       for (int grp = 0; grp < kNg; ++grp) {
         const int pos = kPpw * warp + 4 * grp + qp;
@@ -279,52 +297,80 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
           }
         }
+        int n = GS;
 #pragma unroll
-        for (int h = 0; h < GS; ++h) {
-          float x = part[h];
-          x += __shfl_xor_sync(0xffffffffu, x, 1);
-          x += __shfl_xor_sync(0xffffffffu, x, 2);
-          x += __shfl_xor_sync(0xffffffffu, x, 4);
-          sc[grp][h] = (pos < valid && pos >= first) ? x : -INFINITY;
+        for (int o = 4; o >= 1; o >>= 1) {
+          if (n > 1) {
+            const int half = n >> 1;
+            const bool upper = (qc & o) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+              const float keep = upper ? part[half + i] : part[i];
+              const float send = upper ? part[i] : part[half + i];
+              part[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+            n = half;
+          } else {
+            part[0] += __shfl_xor_sync(0xffffffffu, part[0], o);
+          }
         }
+        sc[grp] = (pos < valid && pos >= first) ? part[0] : -INFINITY;
       }
 
-      // Online softmax over the warp's kPpw positions, per head.
-      float w[kNg][GS];
+      // Online softmax of head h_own over the warp's kPpw positions.
+      float mx = sc[0];
 #pragma unroll
-      for (int h = 0; h < GS; ++h) {
-        float mx = sc[0][h];
+      for (int grp = 1; grp < kNg; ++grp) mx = fmaxf(mx, sc[grp]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_own, mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float corr = ex2(m_own - m_use);
+      float sum = 0.f;
 #pragma unroll
-        for (int grp = 1; grp < kNg; ++grp) mx = fmaxf(mx, sc[grp][h]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m_run[h], mx);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float corr = ex2(m_run[h] - m_use);
-        float sum = 0.f;
-#pragma unroll
-        for (int grp = 0; grp < kNg; ++grp) {
-          w[grp][h] = ex2(sc[grp][h] - m_use);
-          sum += w[grp][h];
-        }
-        sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-        l_run[h] = l_run[h] * corr + sum;
-        m_run[h] = m_new;
-#pragma unroll
-        for (int e = 0; e < VP; ++e) acc[h][e] *= corr;
+      for (int grp = 0; grp < kNg; ++grp) {
+        const float w = ex2(sc[grp] - m_use);
+        sum += w;
+        if (writer) wts[4 * grp + qp][h_own] = w;
       }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+      l_own = l_own * corr + sum;
+      m_own = m_new;
+      if (writer && qp == 0) wts[kNg * 4][h_own] = corr;
+      __syncwarp();
 
-      // acc += w * V over the warp's positions; lane owns dims VP*lane ..
+      // acc = acc * corr + w * V over the warp's positions; lane owns dims VP*lane ..
+      auto row = [&](int i, float* out) {
+        if constexpr (GS % 4 == 0) {
+#pragma unroll
+          for (int h = 0; h < GS; h += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(&wts[i][h]);
+            out[h] = x.x; out[h + 1] = x.y; out[h + 2] = x.z; out[h + 3] = x.w;
+          }
+        } else if constexpr (GS == 2) {
+          const float2 x = *reinterpret_cast<const float2*>(&wts[i][0]);
+          out[0] = x.x; out[1] = x.y;
+        } else {
+          out[0] = wts[i][0];
+        }
+      };
+      {
+        float cb[GS];
+        row(kNg * 4, cb);
+#pragma unroll
+        for (int h = 0; h < GS; ++h)
+#pragma unroll
+          for (int e = 0; e < VP; ++e) acc[h][e] *= cb[h];
+      }
 #pragma unroll
       for (int grp = 0; grp < kNg; ++grp)
 #pragma unroll
         for (int pp = 0; pp < 4; ++pp) {
           const int ppos = kPpw * warp + 4 * grp + pp;
-          float wb[GS];
-#pragma unroll
-          for (int h = 0; h < GS; ++h) wb[h] = __shfl_sync(0xffffffffu, w[grp][h], 8 * pp);
           if (ppos < valid && ppos >= first) {
+            float wb[GS];
+            row(4 * grp + pp, wb);
             // Two output dims per paired fma.
             if constexpr (VP == 4) {
               const float4 vv = *reinterpret_cast<const float4*>(&vs[ppos * D + 4 * lane]);
@@ -344,15 +390,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
 
+    if (writer && qp == 0) {
+      sm.red_m[warp][h_own] = m_own;
+      sm.red_l[warp][h_own] = l_own;
+    }
 #pragma unroll
-    for (int h = 0; h < GS; ++h) {
-      if (lane == 0) {
-        sm.red_m[warp][h] = m_run[h];
-        sm.red_l[warp][h] = l_run[h];
-      }
+    for (int h = 0; h < GS; ++h)
 #pragma unroll
       for (int e = 0; e < VP; ++e) sm.red_o[warp][h][VP * lane + e] = acc[h][e];
-    }
   }
   __syncthreads();
 
