@@ -85,6 +85,7 @@ const float kPresent = 0.f;
 }  // namespace
 
 unsigned* device_status_word() { return status_ptr(); }
+int device_sm_count() { return sm_count(); }
 
 }  // namespace attn
 

@@ -110,7 +110,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     flash_bf16_kernel(const FlashArgs a, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ kfac, int early_q) {
+                      const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ kfac, int early_q,
+                      int q_ahead) {
   constexpr int kChunks = D / 64;                // 128-byte (64-element) column chunks of a K row
   constexpr int kChunkBytes = kKeys * 128;       // one K box: 128 keys x 128 bytes
   constexpr int kTileBytes = kChunks * kChunkBytes;
@@ -193,6 +194,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_o);
       mbar_arrive_expect_tx(&sm.q_full, (unsigned)(rpb * D * 4));
       tma_load_3d(ring + 3 * kTileBytes, &tm_q, 0, g * gs, (int)i0, &sm.q_full);
+      // The CTA q_ahead places later in launch order (about one wave of the
+      // grid) finds its Q block in L2: its start then waits for L2, not HBM.
+      const long long la = (long long)blockIdx.y * gridDim.x + blockIdx.x + q_ahead;
+      if (q_ahead > 0 && la < (long long)gridDim.x * gridDim.y) {
+        const int xa = (int)(la % gridDim.x), ya = (int)(la / gridDim.x);
+        tma_prefetch_l2_3d(&tm_q, 0, ya * gs, (int)((long long)(gridDim.x - 1 - xa) * qpb));
+      }
       if (early_q) grid_dependency_wait();  // the K/V copies are the pre-pass's output
       int p = 0;  // copies issued; copy p goes to ring slot p % kRing
       auto load = [&](bool is_v, int j) {
@@ -633,7 +641,8 @@ int launch_d(const FlashArgs& a, cudaStream_t s) {
     } else {
       FlashArgs aa = a;
       int early_q = kfac != nullptr ? 1 : 0;  // the pre-pass ran just before
-      void* args[] = {&aa, &tm_k, &tm_v, &tm_q, &tm_o, &kfac, &early_q};
+      int q_ahead = device_sm_count();         // one CTA per SM: about one wave ahead
+      void* args[] = {&aa, &tm_k, &tm_v, &tm_q, &tm_o, &kfac, &early_q, &q_ahead};
       if (launch_pdl(reinterpret_cast<const void*>(kern), dim3((unsigned)nb, (unsigned)a.G), dim3(kThreads), smem, s,
                      args) != cudaSuccess)
         rc = ATTN_ERR_CUDA;

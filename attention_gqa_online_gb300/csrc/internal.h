@@ -128,6 +128,8 @@ int launch_flash_tc(const FlashArgs& a, int prec, cudaStream_t s);
 // bf16-operand kernel (flash_bf16.cu); the caller has checked
 // flash_tc_supported(a, ATTN_BF16).
 int launch_flash_bf16(const FlashArgs& a, cudaStream_t s);
+// SM count of the current device (0 if it cannot be read).
+int device_sm_count();
 
 // Backward of the forward attention (fp32, CUDA cores).  Contiguous
 // layouts: q, out, dout, dq [n_q][H*D]; k, v, dk, dv [n_kv][G*D]; lse
