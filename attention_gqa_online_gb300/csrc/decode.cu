@@ -425,16 +425,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   }
 
-  // The last split of this kv head to finish merges all of them.
-  __threadfence();
+  // The last split of this kv head to finish merges all of them.  One
+  // thread takes the ticket with an acquire-release atomic: the release
+  // orders the CTA's partial (written by all its threads, ordered before it
+  // by the barrier) before the ticket, and in the last CTA the acquire (with
+  // the barrier after it) orders the other splits' partials before the
+  // merge's reads.
   __syncthreads();
   if (tid == 0) {
-    const unsigned prev = atomicAdd(&ws.tickets[g], 1u);
+    unsigned prev;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(&ws.tickets[g]) : "memory");
     sm.is_last = (prev == (unsigned)(s_eff - 1));
   }
   __syncthreads();
   if (!sm.is_last) return;
-  __threadfence();
 
   // Fast path: the splits' partials of as many heads as fit in the (now
   // idle) stage buffers come in with one round of bulk copies, then the merge
