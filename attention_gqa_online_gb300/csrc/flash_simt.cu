@@ -46,13 +46,6 @@ struct SimtSmem {
   int row_lo[BM];
 };
 
-__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
-  acc = fmaf(a.x, b.x, acc);
-  acc = fmaf(a.y, b.y, acc);
-  acc = fmaf(a.z, b.z, acc);
-  return fmaf(a.w, b.w, acc);
-}
-
 // Issues the async copies of one (rows x DMAX) tile into shared memory, with
 // zero fill for rows >= valid_rows, columns >= D and rows whose src(r) is
 // nullptr.  src(r) is the global address of row r's first element; `any` is
@@ -217,7 +210,10 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
       for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
     // Each group of 8 products is summed on its own before it joins the
     // running dot product: 16 roundings of the large partial sum instead of
-    // 128 keeps fp32 scores within a few ulp for widely spread inputs.
+    // 128 keeps fp32 scores within a few ulp for widely spread inputs.  The
+    // group runs as two chains (even and odd elements) of paired fmas, one
+    // instruction for two products, on the register pairs the float4 loads
+    // fill.
     const float* kt = sm.k[buf];
 #pragma unroll 2
     for (int d = 0; d < DMAX; d += 8) {
@@ -235,7 +231,14 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) s[i][j] += dot4(qa[i][1], kb[j][1], dot4(qa[i][0], kb[j][0], 0.f));
+        for (int j = 0; j < 4; ++j) {
+          float e0 = 0.f, e1 = 0.f;
+          fma2_acc(e0, e1, qa[i][0].x, qa[i][0].y, kb[j][0].x, kb[j][0].y);
+          fma2_acc(e0, e1, qa[i][0].z, qa[i][0].w, kb[j][0].z, kb[j][0].w);
+          fma2_acc(e0, e1, qa[i][1].x, qa[i][1].y, kb[j][1].x, kb[j][1].y);
+          fma2_acc(e0, e1, qa[i][1].z, qa[i][1].w, kb[j][1].z, kb[j][1].w);
+          s[i][j] += e0 + e1;
+        }
     }
 
     // Mask, tile max, correction, exponentials, running sum.
@@ -289,11 +292,9 @@ __global__ void __launch_bounds__(NT, 1) flash_simt_kernel(const FlashArgs a) {
         float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
         if (DMAX >= 64 || col < DMAX) vv = *reinterpret_cast<const float4*>(&vt[kk * DMAX + col]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          t[i][4 * jj + 0] = fmaf(pr[i], vv.x, t[i][4 * jj + 0]);
-          t[i][4 * jj + 1] = fmaf(pr[i], vv.y, t[i][4 * jj + 1]);
-          t[i][4 * jj + 2] = fmaf(pr[i], vv.z, t[i][4 * jj + 2]);
-          t[i][4 * jj + 3] = fmaf(pr[i], vv.w, t[i][4 * jj + 3]);
+        for (int i = 0; i < 4; ++i) {  // two output columns per paired fma, same order per column
+          fma2_acc(t[i][4 * jj + 0], t[i][4 * jj + 1], pr[i], pr[i], vv.x, vv.y);
+          fma2_acc(t[i][4 * jj + 2], t[i][4 * jj + 3], pr[i], pr[i], vv.z, vv.w);
         }
       }
     }
