@@ -89,10 +89,19 @@ __device__ __forceinline__ void score_tile(const float* A, const float* B, int r
       y[j][0] = *reinterpret_cast<const float4*>(&B[(cl + 16 * j) * STRIDE + d]);
       y[j][1] = *reinterpret_cast<const float4*>(&B[(cl + 16 * j) * STRIDE + d + 4]);
     }
+    // Each 8-product group as two chains (even and odd elements) of paired
+    // fmas on the register pairs the float4 loads fill.
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) s[i][j] += dot4(x[i][1], y[j][1], dot4(x[i][0], y[j][0], 0.f));
+      for (int j = 0; j < 4; ++j) {
+        float e0 = 0.f, e1 = 0.f;
+        fma2_acc(e0, e1, x[i][0].x, x[i][0].y, y[j][0].x, y[j][0].y);
+        fma2_acc(e0, e1, x[i][0].z, x[i][0].w, y[j][0].z, y[j][0].w);
+        fma2_acc(e0, e1, x[i][1].x, x[i][1].y, y[j][1].x, y[j][1].y);
+        fma2_acc(e0, e1, x[i][1].z, x[i][1].w, y[j][1].z, y[j][1].w);
+        s[i][j] += e0 + e1;
+      }
   }
 }
 
@@ -233,14 +242,10 @@ __global__ void __launch_bounds__(NT, 1)
         const float4 qv = *reinterpret_cast<const float4*>(&sm.q[r * QS + col]);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          dv[i][4 * jj + 0] = fmaf(pk[i], gv.x, dv[i][4 * jj + 0]);
-          dv[i][4 * jj + 1] = fmaf(pk[i], gv.y, dv[i][4 * jj + 1]);
-          dv[i][4 * jj + 2] = fmaf(pk[i], gv.z, dv[i][4 * jj + 2]);
-          dv[i][4 * jj + 3] = fmaf(pk[i], gv.w, dv[i][4 * jj + 3]);
-          dk[i][4 * jj + 0] = fmaf(sk[i], qv.x, dk[i][4 * jj + 0]);
-          dk[i][4 * jj + 1] = fmaf(sk[i], qv.y, dk[i][4 * jj + 1]);
-          dk[i][4 * jj + 2] = fmaf(sk[i], qv.z, dk[i][4 * jj + 2]);
-          dk[i][4 * jj + 3] = fmaf(sk[i], qv.w, dk[i][4 * jj + 3]);
+          fma2_acc(dv[i][4 * jj + 0], dv[i][4 * jj + 1], pk[i], pk[i], gv.x, gv.y);  // same order per column
+          fma2_acc(dv[i][4 * jj + 2], dv[i][4 * jj + 3], pk[i], pk[i], gv.z, gv.w);
+          fma2_acc(dk[i][4 * jj + 0], dk[i][4 * jj + 1], sk[i], sk[i], qv.x, qv.y);
+          fma2_acc(dk[i][4 * jj + 2], dk[i][4 * jj + 3], sk[i], sk[i], qv.z, qv.w);
         }
       }
     }
@@ -372,10 +377,8 @@ __global__ void __launch_bounds__(NT, 1)
         const float4 kv = *reinterpret_cast<const float4*>(&sm.k[kk * QS + 4 * cl + 64 * jj]);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          dq[i][4 * jj + 0] = fmaf(sr[i], kv.x, dq[i][4 * jj + 0]);
-          dq[i][4 * jj + 1] = fmaf(sr[i], kv.y, dq[i][4 * jj + 1]);
-          dq[i][4 * jj + 2] = fmaf(sr[i], kv.z, dq[i][4 * jj + 2]);
-          dq[i][4 * jj + 3] = fmaf(sr[i], kv.w, dq[i][4 * jj + 3]);
+          fma2_acc(dq[i][4 * jj + 0], dq[i][4 * jj + 1], sr[i], sr[i], kv.x, kv.y);  // same order per column
+          fma2_acc(dq[i][4 * jj + 2], dq[i][4 * jj + 3], sr[i], sr[i], kv.z, kv.w);
         }
       }
     }
