@@ -59,7 +59,7 @@ struct __align__(128) DecodeSmem {
   float wts[kCWarps][kNg * 4 + 1][GS];  // per warp: P of its positions for every head, then the corrections
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t merge_bar;
+  uint64_t merge_bar[GS];  // per head of the round: its partials have landed
   int is_last;
   int abort;
 };
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kCWarps);
     }
-    mbar_init(&sm.merge_bar, 1);
+    for (int h = 0; h < GS; ++h) mbar_init(&sm.merge_bar[h], 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -442,7 +442,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   // Fast path: the splits' partials of as many heads as fit in the (now
   // idle) stage buffers come in with one round of bulk copies, then the merge
-  // runs from shared memory; rounds repeat until every head is merged.
+  // runs from shared memory; rounds repeat until every head is merged.  Each
+  // head's copies complete on its own barrier, so the threads of a head
+  // merge as soon as its partials have landed.
   const int S2 = even_splits(S);
   const unsigned ml_head_bytes = ((unsigned)s_eff * 8u + 15u) & ~15u;
   const size_t head_bytes = (size_t)s_eff * D * 4 + ml_head_bytes;
@@ -454,17 +456,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       float* sml = so + (size_t)nh * s_eff * D;  // [nh][ml_head_bytes / 4]
       if (tid == 0) {
         asm volatile("fence.proxy.async;" ::: "memory");
-        mbar_arrive_expect_tx(&sm.merge_bar, (unsigned)(nh * head_bytes));
         for (int h = 0; h < nh; ++h) {
+          mbar_arrive_expect_tx(&sm.merge_bar[h], (unsigned)head_bytes);
           bulk_g2s(so + (size_t)h * s_eff * D, ws.o + (size_t)(g * GS + h0 + h) * S * D, (unsigned)(s_eff * D * 4),
-                   &sm.merge_bar);
+                   &sm.merge_bar[h]);
           bulk_g2s(sml + (size_t)h * (ml_head_bytes / 4), ws.ml + (size_t)(g * GS + h0 + h) * S2 * 2, ml_head_bytes,
-                   &sm.merge_bar);
+                   &sm.merge_bar[h]);
         }
       }
-      mbar_wait_bounded(&sm.merge_bar, (unsigned)(round & 1), a.status);
       for (int idx = tid; idx < nh * (D / 4); idx += kThreads) {
         const int h = idx / (D / 4), c = idx % (D / 4);
+        mbar_wait_bounded(&sm.merge_bar[h], (unsigned)(round & 1), a.status);
         const float* mlh = sml + (size_t)h * (ml_head_bytes / 4);
         float M = -INFINITY;
         for (int s = 0; s < s_eff; ++s) M = fmaxf(M, mlh[2 * s]);
@@ -476,10 +478,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           const float f = ex2(mlh[2 * s] - Mu);
           const float4 x = *reinterpret_cast<const float4*>(so + ((size_t)h * s_eff + s) * D + 4 * c);
           L = fmaf(mlh[2 * s + 1], f, L);
-          O.x = fmaf(x.x, f, O.x);
-          O.y = fmaf(x.y, f, O.y);
-          O.z = fmaf(x.z, f, O.z);
-          O.w = fmaf(x.w, f, O.w);
+          fma2_acc(O.x, O.y, x.x, x.y, f, f);
+          fma2_acc(O.z, O.w, x.z, x.w, f, f);
         }
         const float inv = (L == 0.f) ? 0.f : 1.f / L;
         *reinterpret_cast<float4*>(a.out + (size_t)(g * GS + h0 + h) * D + 4 * c) =
