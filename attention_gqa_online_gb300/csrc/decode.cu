@@ -363,29 +363,39 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
           for (int e = 0; e < VP; ++e) acc[h][e] *= cb[h];
       }
+      // One position's weights times its V row; two output dims per paired fma.
+      auto pv = [&](int i) {
+        const int ppos = kPpw * warp + i;
+        float wb[GS];
+        row(i, wb);
+        if constexpr (VP == 4) {
+          const float4 vv = *reinterpret_cast<const float4*>(&vs[ppos * D + 4 * lane]);
 #pragma unroll
-      for (int grp = 0; grp < kNg; ++grp)
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-          const int ppos = kPpw * warp + 4 * grp + pp;
-          if (ppos < valid && ppos >= first) {
-            float wb[GS];
-            row(4 * grp + pp, wb);
-            // Two output dims per paired fma.
-            if constexpr (VP == 4) {
-              const float4 vv = *reinterpret_cast<const float4*>(&vs[ppos * D + 4 * lane]);
-#pragma unroll
-              for (int h = 0; h < GS; ++h) {
-                fma2_acc(acc[h][0], acc[h][1], wb[h], wb[h], vv.x, vv.y);
-                fma2_acc(acc[h][2], acc[h][3], wb[h], wb[h], vv.z, vv.w);
-              }
-            } else {
-              const float2 vv = *reinterpret_cast<const float2*>(&vs[ppos * D + 2 * lane]);
-#pragma unroll
-              for (int h = 0; h < GS; ++h) fma2_acc(acc[h][0], acc[h][1], wb[h], wb[h], vv.x, vv.y);
-            }
+          for (int h = 0; h < GS; ++h) {
+            fma2_acc(acc[h][0], acc[h][1], wb[h], wb[h], vv.x, vv.y);
+            fma2_acc(acc[h][2], acc[h][3], wb[h], wb[h], vv.z, vv.w);
           }
+        } else {
+          const float2 vv = *reinterpret_cast<const float2*>(&vs[ppos * D + 2 * lane]);
+#pragma unroll
+          for (int h = 0; h < GS; ++h) fma2_acc(acc[h][0], acc[h][1], wb[h], wb[h], vv.x, vv.y);
         }
+      };
+      if (valid == kT && first <= 0) {
+        // Every position of the stage is kept (all but a split's last stage
+        // and a window's first): no per-position test, so the loads of
+        // several positions can be in flight together.
+#pragma unroll
+        for (int i = 0; i < kNg * 4; ++i) pv(i);
+      } else {
+        // Skipped positions may hold any bits (a cache row past kv_pos), so
+        // they are left out rather than weighted by zero.
+#pragma unroll
+        for (int i = 0; i < kNg * 4; ++i) {
+          const int ppos = kPpw * warp + i;
+          if (ppos < valid && ppos >= first) pv(i);
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
