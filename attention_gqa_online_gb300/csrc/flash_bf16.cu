@@ -158,25 +158,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto k_pos = [&](int j) { return j < 3 ? j : 2 * j - 2; };
   auto v_pos = [&](int j) { return min(2 * j + 3, j + nt); };
 
-  if (tid == 0) {
-    for (int s = 0; s < kRing; ++s) {
+  if (warp == 0) {
+    // The Q block is copied first, so that it lands while the rest of the
+    // set-up runs; the other barriers are initialised across the warp.
+    if (lane == 0) {
+      mbar_init(&sm.q_full, 1);
+      fence_mbar_init();
+      if (nt > 0) {
+        prefetch_tmap(&tm_q);
+        mbar_arrive_expect_tx(&sm.q_full, (unsigned)(rpb * D * 4));
+        tma_load_3d(ring + 3 * kTileBytes, &tm_q, 0, g * gs, (int)i0, &sm.q_full);
+      }
+      sm.abort = 0;
+    }
+    for (int s = lane; s < kRing; s += 32) {
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    for (int b = 0; b < kSBuf; ++b) {
+    for (int b = lane; b < kSBuf; b += 32) {
       mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.s_free[b], 4);
-      for (int q4 = 0; q4 < 4; ++q4) mbar_init(&sm.mref_bar[q4][b], 32);
       mbar_init(&sm.p_ready[b], 4);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.pv_done[b], 1);
-      mbar_init(&sm.drain[b], 1);
+    for (int i = lane; i < 4 * kSBuf; i += 32) mbar_init(&sm.mref_bar[i / kSBuf][i % kSBuf], 32);
+    if (lane < 2) {
+      mbar_init(&sm.pv_done[lane], 1);
+      mbar_init(&sm.drain[lane], 1);
     }
-    mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_ready, 8);
-    mbar_init(&sm.o_final, 1);
-    sm.abort = 0;
+    if (lane == 2) {
+      mbar_init(&sm.q_ready, 8);
+      mbar_init(&sm.o_final, 1);
+    }
     fence_mbar_init();
   }
   if (warp == 1) tc::tmem_alloc(&sm.tmem_base, 512);
@@ -188,12 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nt > 0) {
-      prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_o);
-      mbar_arrive_expect_tx(&sm.q_full, (unsigned)(rpb * D * 4));
-      tma_load_3d(ring + 3 * kTileBytes, &tm_q, 0, g * gs, (int)i0, &sm.q_full);
       // The CTA q_ahead places later in launch order (about one wave of the
       // grid) finds its Q block in L2: its start then waits for L2, not HBM.
       const long long la = (long long)blockIdx.y * gridDim.x + blockIdx.x + q_ahead;

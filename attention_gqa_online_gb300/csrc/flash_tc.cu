@@ -158,21 +158,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int jt0 = first_key(n_min, a.window) / kKeys;  // first key tile of the block
   const int nt = (n_max + kKeys - 1) / kKeys - jt0;    // key tiles the block walks
 
-  if (tid == 0) {
-    for (int s = 0; s < kRing; ++s) {
+  if (warp == 0) {
+    // The Q block is copied first, so that it lands while the rest of the
+    // set-up runs; the other barriers are initialised across the warp.
+    if (lane == 0) {
+      mbar_init(&sm.q_full, 1);
+      fence_mbar_init();
+      if (nt > 0) {
+        prefetch_tmap(&tm_q);
+        mbar_arrive_expect_tx(&sm.q_full, (unsigned)(rpb * D * 4));
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_3d(qstage + c * kChunkBytes, &tm_q, kEpr * c, g * gs, (int)i0, &sm.q_full);
+      }
+      sm.abort = 0;
+    }
+    for (int s = lane; s < kRing; s += 32) {
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    for (int b = 0; b < kSBuf; ++b) {
+    for (int b = lane; b < kSBuf; b += 32) {
       mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.p_ready[b], 8);
       mbar_init(&sm.pv_done[b], 1);
     }
-    mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_ready, 8);
-    mbar_init(&sm.drain[0], 1);
-    mbar_init(&sm.drain[1], 1);
-    sm.abort = 0;
+    if (lane < 2) mbar_init(&sm.drain[lane], 1);
+    if (lane == 2) mbar_init(&sm.q_ready, 8);
     fence_mbar_init();
   }
   // Paged cache: the block-table entries of pages [page0, page0 + n_pages)
@@ -193,13 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nt > 0) {
-      prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_o);
-      mbar_arrive_expect_tx(&sm.q_full, (unsigned)(rpb * D * 4));
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) tma_load_3d(qstage + c * kChunkBytes, &tm_q, kEpr * c, g * gs, (int)i0, &sm.q_full);
       if (early_q) grid_dependency_wait();  // the K copies are the pre-pass's output
       // Copies go out in the order the MMA issuer consumes the tiles: K_0,
       // K_1, V_0, K_2, V_1, ..., K_(nt-1), V_(nt-2), V_(nt-1).  Ring slot
