@@ -203,13 +203,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_o);
-      // The CTA q_ahead places later in launch order (about one wave of the
-      // grid) finds its Q block in L2: its start then waits for L2, not HBM.
-      const long long la = (long long)blockIdx.y * gridDim.x + blockIdx.x + q_ahead;
-      if (q_ahead > 0 && la < (long long)gridDim.x * gridDim.y) {
-        const int xa = (int)(la % gridDim.x), ya = (int)(la / gridDim.x);
-        tma_prefetch_l2_3d(&tm_q, 0, ya * gs, (int)((long long)(gridDim.x - 1 - xa) * qpb));
-      }
       if (early_q) grid_dependency_wait();  // the K/V copies are the pre-pass's output
       int p = 0;  // copies issued; copy p goes to ring slot p % kRing
       auto load = [&](bool is_v, int j) {
@@ -225,6 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++p;
       };
       for (int t = 0; t < 3 && t < nt; ++t) load(false, t);
+      // After the first K copies: the CTA q_ahead places later in launch order (about one wave of the
+      // grid) finds its Q block in L2: its start then waits for L2, not HBM.
+      const long long la = (long long)blockIdx.y * gridDim.x + blockIdx.x + q_ahead;
+      if (q_ahead > 0 && la < (long long)gridDim.x * gridDim.y) {
+        const int xa = (int)(la % gridDim.x), ya = (int)(la / gridDim.x);
+        tma_prefetch_l2_3d(&tm_q, 0, ya * gs, (int)((long long)(gridDim.x - 1 - xa) * qpb));
+      }
       for (int j = 0; j < nt; ++j) {
         load(true, j);
         if (j + 3 < nt) load(false, j + 3);
@@ -327,23 +327,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* qrow = qstage + r * D;
       // RoPE: element e pairs with e +- D/2 (query qi at position base_pos + qi).
       const float* cs = (a.rope != nullptr && row_ok) ? a.rope + (a.base_pos + qi) * D : nullptr;
+      // All of the half row's loads are issued before any is used.
       float4 xq[kQF4];
-      float qmax = 0.f;
+      if (r < rpb) {
 #pragma unroll
-      for (int i = 0; i < kQF4; ++i) {
-        const int f = (i + r) % kQF4;
-        const int e = grp * (D / 2) + 4 * f;  // first element of this float4
-        float4 x = r < rpb ? *reinterpret_cast<const float4*>(qrow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-        if (cs != nullptr) {
-          const int dd = grp == 0 ? e : e - D / 2;  // pair index
+        for (int i = 0; i < kQF4; ++i)
+          xq[i] = *reinterpret_cast<const float4*>(qrow + grp * (D / 2) + 4 * ((i + r) % kQF4));
+      } else {
+#pragma unroll
+        for (int i = 0; i < kQF4; ++i) xq[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (cs != nullptr) {
+#pragma unroll
+        for (int i = 0; i < kQF4; ++i) {
+          const int e = grp * (D / 2) + 4 * ((i + r) % kQF4);  // first element of this float4
+          const int dd = grp == 0 ? e : e - D / 2;               // pair index
           const float4 y = *reinterpret_cast<const float4*>(qrow + (grp == 0 ? e + D / 2 : dd));
           const float4 cv = *reinterpret_cast<const float4*>(cs + dd);
           const float4 sv = *reinterpret_cast<const float4*>(cs + D / 2 + dd);
           const float sg = grp == 0 ? -1.f : 1.f;
-          x = make_float4(fmaf(sg * y.x, sv.x, x.x * cv.x), fmaf(sg * y.y, sv.y, x.y * cv.y),
-                          fmaf(sg * y.z, sv.z, x.z * cv.z), fmaf(sg * y.w, sv.w, x.w * cv.w));
+          const float4 x = xq[i];
+          xq[i] = make_float4(fmaf(sg * y.x, sv.x, x.x * cv.x), fmaf(sg * y.y, sv.y, x.y * cv.y),
+                              fmaf(sg * y.z, sv.z, x.z * cv.z), fmaf(sg * y.w, sv.w, x.w * cv.w));
         }
-        x = make_float4(x.x * sl2, x.y * sl2, x.z * sl2, x.w * sl2);
+      }
+      float qmax = 0.f;
+#pragma unroll
+      for (int i = 0; i < kQF4; ++i) {
+        const float4 x = make_float4(xq[i].x * sl2, xq[i].y * sl2, xq[i].z * sl2, xq[i].w * sl2);
         xq[i] = x;
         qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
       }
