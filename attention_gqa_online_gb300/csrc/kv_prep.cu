@@ -43,14 +43,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2) kv_prep_kernel(const PrepArgs
   const long long col = (long long)g * D + 4 * c4;
   float4 x[kPasses];
   float mx = 0.f;
+  if (p.table == nullptr && t_first + 128 <= p.rows_end) {
+    // A whole contiguous tile: every load is issued before any is used.
 #pragma unroll
-  for (int i = 0; i < kPasses; ++i) {
-    const long long t = t_first + i * kRowsPerPass + rsub;
-    x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t < p.rows_end) {
-      long long row = t;
-      if (p.table != nullptr) row = paged_row(p.table, p.page_rows, p.num_pages, (int)t, p.status);
-      if (row >= 0) x[i] = *reinterpret_cast<const float4*>(src + row * p.stride + col);
+    for (int i = 0; i < kPasses; ++i)
+      x[i] = *reinterpret_cast<const float4*>(src + (t_first + i * kRowsPerPass + rsub) * p.stride + col);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      const long long t = t_first + i * kRowsPerPass + rsub;
+      x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < p.rows_end) {
+        long long row = t;
+        if (p.table != nullptr) row = paged_row(p.table, p.page_rows, p.num_pages, (int)t, p.status);
+        if (row >= 0) x[i] = *reinterpret_cast<const float4*>(src + row * p.stride + col);
+      }
     }
   }
   if (!is_k) {  // V as bf16
