@@ -59,6 +59,7 @@ def test_small_config(cuda_lib, orc, prec, mask, kv):
     (90, 90, 10, 2, 128, CAUSAL),    # gs = 5
     (61, 200, 14, 2, 64, CROSS),     # gs = 7
     (40, 40, 48, 1, 128, CAUSAL),    # gs = 48: two queries per block
+    (5, 5, 128, 1, 64, FULL),        # gs = 128: one query per block
 ])
 def test_shapes(cuda_lib, orc, prec, q_seq, kv_seq, H, G, D, mask):
     if prec != FP32 and not tc_supported(H, G, D):
