@@ -412,20 +412,37 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   __syncthreads();
 
   // Merge the consumer warps' states into this split's partial.
-  const WsLayout ws = ws_layout(a.workspace, a.H, a.G * a.kv_div, D, S);
-  for (int idx = tid; idx < GS * D; idx += kThreads) {
-    const int h = idx / D, d = idx % D;
-    float M = -INFINITY;
+  auto cta_state = [&](int h, int d, float& M, float& L, float& O) {
+    M = -INFINITY;
 #pragma unroll
     for (int w2 = 0; w2 < kCWarps; ++w2) M = fmaxf(M, sm.red_m[w2][h]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f, O = 0.f;
+    L = 0.f;
+    O = 0.f;
 #pragma unroll
     for (int w2 = 0; w2 < kCWarps; ++w2) {
       const float f = ex2(sm.red_m[w2][h] - Mu);
       L += sm.red_l[w2][h] * f;
       O += sm.red_o[w2][h][d] * f;
     }
+  };
+  if (s_eff == 1) {
+    // The only split: its state is the result (merging one partial would
+    // reproduce it), so no partial, no ticket.
+    for (int idx = tid; idx < GS * D; idx += kThreads) {
+      const int h = idx / D, d = idx % D;
+      float M, L, O;
+      cta_state(h, d, M, L, O);
+      const float inv = (L == 0.f) ? 0.f : 1.f / L;
+      a.out[(size_t)(g * GS + h) * D + d] = O * inv;
+    }
+    return;
+  }
+  const WsLayout ws = ws_layout(a.workspace, a.H, a.G * a.kv_div, D, S);
+  for (int idx = tid; idx < GS * D; idx += kThreads) {
+    const int h = idx / D, d = idx % D;
+    float M, L, O;
+    cta_state(h, d, M, L, O);
     const size_t hs = (size_t)(g * GS + h) * S + j;
     ws.o[hs * D + d] = O;
     if (d == 0) {
