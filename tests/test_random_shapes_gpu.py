@@ -1,4 +1,4 @@
-"""Seeded random shapes through forward, prefill and decode, every precision, against the fp64 oracle.
+"""Seeded random shapes through forward, prefill, decode and backward, every precision, against the fp64 oracle.
 
 Each case draws its own sizes from a generator seeded by the case number:
 head_dim (64 and 128, and sizes only the fp32 path takes), kv heads, query
@@ -144,3 +144,45 @@ def test_random_decode(cuda_lib, orc, case):
             assert cuda_lib.attn_get_status() == 0
             assert_out_close(out.cpu().numpy(), ref, FP32, vmax, "case %d: H%d G%d D%d max_seq%d kv_pos%d window%d" % (
                 case, H, G, D, max_seq, kp, w))
+
+
+def backward_case(i):
+    rng = np.random.default_rng(10000 + i)
+    D = int(rng.choice([64, 128, 64, 48]))
+    G = int(rng.integers(1, 4))
+    gs = int(rng.choice([1, 2, 3, 4, 8]))
+    mask = int(rng.integers(0, 3))
+    q_seq = int(rng.integers(1, 200))
+    kv_seq = q_seq if mask != CROSS else int(rng.integers(1, 260))
+    window = 0 if rng.random() < 0.5 else int(rng.integers(1, kv_seq + 20))
+    return G * gs, G, D, mask, q_seq, kv_seq, window
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_random_backward(cuda_lib, orc, case):
+    """dq, dk, dv per gradient tensor: fp32 within 1e-5 + 1e-4 max|ref|; bf16 operands
+    (D in {64, 128}, power-of-two groups) within 2e-2 max|ref|."""
+    H, G, D, mask, q_seq, kv_seq, window = backward_case(case)
+    q, k, v = synthetic.forward_inputs(q_seq, kv_seq, H, G, D, seed=300 + case)
+    dout = torch.from_numpy(np.random.default_rng(400 + case).standard_normal((q_seq, H * D)).astype(np.float32))
+    ref = orc.backward(q.numpy(), k.numpy(), v.numpy(), dout.numpy(), q_seq, kv_seq, H, G, D, mask, window=window)
+    gs = H // G
+    precs = [FP32, BF16] if D in (64, 128) and gs & (gs - 1) == 0 else [FP32]
+    dq_, dk_, dv_, do_ = dev(q), dev(k), dev(v), dev(dout)
+    out = torch.empty((q_seq, H * D), device="cuda")
+    lse = torch.empty((q_seq, H, 2), device="cuda")
+    cuda_lib.attn_forward_window(dq_, dk_, dv_, out, lse, q_seq, kv_seq, H, G, D, mask, FP32, window)
+    for prec in precs:
+        grads = [torch.full(shape, float("nan"), device="cuda") for shape in
+                 ((q_seq, H * D), (kv_seq, G * D), (kv_seq, G * D))]
+        cuda_lib.attn_backward(dq_, dk_, dv_, out, do_, lse, *grads, q_seq, kv_seq, H, G, D, mask, prec, window)
+        torch.cuda.synchronize()
+        assert cuda_lib.attn_get_status() == 0
+        for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+            got = g.cpu().numpy()
+            where = "case %d: q%d kv%d H%d G%d D%d mask%d window%d prec%d %s" % (
+                case, q_seq, kv_seq, H, G, D, mask, window, prec, name)
+            assert np.all(np.isfinite(got)), where + ": non-finite gradient"
+            err = float(np.abs(got - r).max())
+            tol = (1e-5 + 1e-4 * float(np.abs(r).max())) if prec == FP32 else 2e-2 * float(np.abs(r).max())
+            assert err <= tol, "%s: max|err| = %.3g > %.3g" % (where, err, tol)
