@@ -59,9 +59,13 @@ int window_arg(uint32_t window) { return window > 0x7fffffffu ? 0x7fffffff : (in
 
 bool valid_prec(int prec) { return prec == ATTN_FP32 || prec == ATTN_TF32 || prec == ATTN_BF16; }
 
+// A tensor-core call that runs on the fp32 kernel instead (see run_flash)
+// needs that kernel's scratch, so a tensor-core precision reports the larger.
 size_t flash_scratch_bytes(const FlashArgs& a, int prec) {
-  if (prec == ATTN_FP32) return flash_simt_scratch_bytes(a);
-  return prec == ATTN_BF16 ? flash_bf16_scratch_bytes(a) : flash_tc_scratch_bytes(a);
+  const size_t simt = flash_simt_scratch_bytes(a);
+  if (prec == ATTN_FP32) return simt;
+  const size_t tc = prec == ATTN_BF16 ? flash_bf16_scratch_bytes(a) : flash_tc_scratch_bytes(a);
+  return tc > simt ? tc : simt;
 }
 
 // A workspace bound to this thread must hold the call's whole scratch; this
@@ -73,8 +77,14 @@ bool workspace_too_small(size_t need) {
 
 int run_flash(const FlashArgs& a, int prec, cudaStream_t s) {
   scratch_begin_call();
-  if (prec != ATTN_FP32 && !flash_tc_supported(a, prec)) return ATTN_ERR_UNSUPPORTED;
+  // The tensor-core precisions refuse only head_dim outside {64, 128}.  A
+  // layout their kernels do not take (pointers not 16-byte aligned, row
+  // strides off the TMA granule, more than 128 query heads per kv head, pages
+  // the tiles cannot follow) runs on the fp32 kernel, whose results lie within
+  // every precision's bound.
+  if (prec != ATTN_FP32 && a.D != 64 && a.D != 128) return ATTN_ERR_UNSUPPORTED;
   if (workspace_too_small(flash_scratch_bytes(a, prec))) return ATTN_ERR_INVALID_ARG;
+  if (prec != ATTN_FP32 && !flash_tc_supported(a, prec)) prec = ATTN_FP32;
   if (prec == ATTN_FP32) return launch_flash_simt(a, s);
   return launch_flash_tc(a, prec, s);
 }
@@ -478,7 +488,12 @@ extern "C" int attn_prefill_paged(const float* q_batch, const float* k_pages, co
 static size_t backward_scratch_bytes(const BwdArgs& a, int prec, bool rope) {
   const size_t turned = rope ? scratch_round(((size_t)a.n_q * a.H + (size_t)a.n_kv * a.G) * a.D * sizeof(float)) : 0;
   if (a.n_kv == 0) return 0;
-  return turned + (prec == ATTN_BF16 ? backward_bf16_scratch_bytes(a) : backward_simt_scratch_bytes(a));
+  const size_t simt = backward_simt_scratch_bytes(a);
+  if (prec != ATTN_BF16) return turned + simt;
+  // A bf16 call that runs on the fp32 backward (see backward_impl) needs that
+  // kernel's scratch: report the larger.
+  const size_t tc = backward_bf16_scratch_bytes(a);
+  return turned + (tc > simt ? tc : simt);
 }
 
 // The backward behind attn_backward and attn_backward_rope; rope_table (or
@@ -528,7 +543,12 @@ static int backward_impl(const float* q, const float* k, const float* v, const f
   a.scale = 1.0f / sqrtf((float)head_dim);
   a.status = status_ptr();
   if (a.status == nullptr) return ATTN_ERR_CUDA;
-  if (prec == ATTN_BF16 && !backward_bf16_supported(a)) return ATTN_ERR_UNSUPPORTED;
+  if (prec == ATTN_BF16 && !backward_bf16_supported(a)) {
+    // bf16 operands refuse only head_dim outside {64, 128}; other groups
+    // (not a power of two up to 128) run the fp32 backward.
+    if (a.D != 64 && a.D != 128) return ATTN_ERR_UNSUPPORTED;
+    prec = ATTN_FP32;
+  }
   scratch_begin_call();
   if (workspace_too_small(backward_scratch_bytes(a, prec, rope))) return ATTN_ERR_INVALID_ARG;
   // RoPE: the gradient of the plain attention at the turned q and k, turned

@@ -73,12 +73,15 @@
  *              fp32 accumulators carry |V| * keys * 2^24 below fp32's range
  *              for any |V| < 2^70).  K and V are converted by a pre-pass, Q
  *              and P on their way into the tensor core.
- *              Tensor-core precisions need D in {64, 128}, 1 <= gs <= 128
- *              (a thread block packs 128/gs queries of gs heads; when gs
- *              does not divide 128 the remaining rows idle), 16-byte aligned
- *              pointers, Q/out row strides that are multiples of 4 floats
- *              and K/V row strides that are multiples of 8 floats; otherwise
- *              they return ATTN_ERR_UNSUPPORTED.
+ *              Tensor-core precisions need D in {64, 128}, else they
+ *              return ATTN_ERR_UNSUPPORTED.  Their kernels take
+ *              1 <= gs <= 128 (a thread block packs 128/gs queries of gs
+ *              heads; when gs does not divide 128 the remaining rows idle),
+ *              16-byte aligned pointers, Q/out row strides that are
+ *              multiples of 4 floats and K/V row strides that are multiples
+ *              of 8 floats (paged caches: page_rows % 32 == 0); a call
+ *              outside that runs on the fp32 CUDA-core kernel instead, whose
+ *              results lie within every precision's bound.
  *              ATTN_FP32 accepts any 1 <= D <= 128.
  */
 #ifndef ATTN_GQA_H
@@ -304,9 +307,9 @@ ATTN_API int attn_forward_rope(const float *q, const float *k, const float *v, f
  * attn_decode_workspace_bytes(H, G, D, max_seq)).  Only the block-table
  * entries of pages inside a row's window are read; an entry >= num_pages
  * reads as zeros and records ATTN_ERR_INVALID_ARG in the status word.  The
- * split decode and the tensor-core precisions need page_rows % 32 == 0
- * (decode otherwise runs the fp32 CUDA-core kernel; the tensor-core prefill
- * returns ATTN_ERR_UNSUPPORTED).  The TF32 prefill reads named pages in
+ * split decode and the tensor-core kernels need page_rows % 32 == 0
+ * (otherwise decode, and a tensor-core prefill, run the fp32 CUDA-core
+ * kernel).  The TF32 prefill reads named pages in
  * 32-row groups, so rows of such a group past the last attended position
  * must hold finite values.  Further errors: INVALID_ARG for a NULL
  * block_table, page_rows, num_pages or max_blocks of 0, or a capacity or
@@ -344,7 +347,9 @@ ATTN_API int attn_prefill_paged(const float *q_batch, const float *k_pages, cons
  *   prec               ATTN_FP32: CUDA cores, fp32 arithmetic.
  *                      ATTN_BF16: tensor cores; q, k, v, dout and the
  *                      P and dS tiles rounded to bf16, fp32 accumulation
- *                      (D in {64, 128}, H/G a power of two up to 128).
+ *                      (D in {64, 128}, else ATTN_ERR_UNSUPPORTED; a group
+ *                      H/G that is not a power of two up to 128 runs the
+ *                      fp32 backward instead).
  *                      ATTN_TF32 returns ATTN_ERR_UNSUPPORTED.
  * dq, dk and dv are written in full (keys no row attends get zero).  Each
  * element is computed by one thread block, without atomics, so repeated

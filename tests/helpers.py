@@ -44,6 +44,6 @@ def assert_lse_close(got, ref, prec, smax=1.0, where=""):
 
 
 def tc_supported(H, G, D):
-    """Shapes the tensor-core forward and prefill accept (contiguous, aligned tensors)."""
-    gs = H // G
-    return D in (64, 128) and 1 <= gs <= 128
+    """Shapes the tensor-core precisions accept: D in {64, 128} (layouts their
+    kernels do not take run on the fp32 kernel)."""
+    return D in (64, 128)

@@ -119,12 +119,9 @@ def test_prefill_paged_ragged(cuda_lib, orc, prec):
     check_prefill_paged(cuda_lib, orc, 129, 8, 1, 64, 96, 64, 16, 700, 520, 3, prec, 0, seed=3)
 
 
-def test_prefill_paged_small_pages(cuda_lib, orc):
-    """16-row pages: the fp32 kernel takes them; the tensor-core precisions refuse."""
+@pytest.mark.parametrize("prec", [TF32, BF16])
+def test_prefill_paged_small_pages(cuda_lib, orc, prec):
+    """16-row pages: the fp32 kernel takes them; the tensor-core precisions, whose
+    tiles follow pages of 32 rows, run on that kernel too (within their bounds)."""
     check_prefill_paged(cuda_lib, orc, 37, 6, 2, 80, 200, 16, 20, 100, 500, 5, FP32, 0, seed=4)
-    kp, vp, table, num_pages = paged_pool(4, 16, 16, 128)
-    with pytest.raises(cuda_lib.AttnError) as e:
-        cuda_lib.attn_prefill_paged(torch.zeros((8, 256), device="cuda"), dev(torch.from_numpy(kp)),
-                                    dev(torch.from_numpy(vp)), table_dev(table), torch.zeros((8, 256), device="cuda"),
-                                    8, 4, 2, 64, 128, 16, num_pages, 16, 0.125, 0, 256, 256, 0, TF32, 0)
-    assert e.value.code == cuda_lib.ATTN_ERR_UNSUPPORTED
+    check_prefill_paged(cuda_lib, orc, 37, 6, 2, 64, 136, 16, 20, 100, 400, 5, prec, 0, seed=6)

@@ -92,19 +92,10 @@ def test_random_prefill(cuda_lib, orc, case):
     sentinel = 12345.0
     for prec in precisions(H, G, D):
         out = torch.full((q_rows, out_stride), sentinel, device="cuda")
-        call = lambda: cuda_lib.attn_prefill_window(dqb, dkc, dvc, out, n_queries, H, G, D, kv_dim, max_seq,
-                                                    float(scale), start_pos, q_stride, out_stride, q_base, prec,
-                                                    window)
-        if prec != FP32 and (kv_dim % 8 or q_stride % 4 or out_stride % 4):
-            # Documented: the tensor-core precisions need K/V row strides in
-            # multiples of 8 floats (Q/out: 4); the call writes nothing.
-            with pytest.raises(cuda_lib.AttnError) as e:
-                call()
-            assert e.value.code == cuda_lib.ATTN_ERR_UNSUPPORTED
-            torch.cuda.synchronize()
-            assert np.all(out.cpu().numpy() == sentinel)
-            continue
-        call()
+        # K/V row strides that are not multiples of 8 floats run the
+        # tensor-core precisions on the fp32 kernel.
+        cuda_lib.attn_prefill_window(dqb, dkc, dvc, out, n_queries, H, G, D, kv_dim, max_seq, float(scale),
+                                     start_pos, q_stride, out_stride, q_base, prec, window)
         torch.cuda.synchronize()
         assert cuda_lib.attn_get_status() == 0
         got = out.cpu().numpy()
@@ -186,3 +177,61 @@ def test_random_backward(cuda_lib, orc, case):
             err = float(np.abs(got - r).max())
             tol = (1e-5 + 1e-4 * float(np.abs(r).max())) if prec == FP32 else 2e-2 * float(np.abs(r).max())
             assert err <= tol, "%s: max|err| = %.3g > %.3g" % (where, err, tol)
+
+
+def offset_view(x, shape):
+    """x's values in a device buffer that starts one float past a 16-byte boundary."""
+    buf = torch.zeros(x.numel() + 4, device="cuda")
+    v = buf[1:1 + x.numel()].view(shape)
+    v.copy_(x.reshape(shape).to("cuda"))
+    assert v.data_ptr() % 16 == 4
+    return v
+
+
+@pytest.mark.parametrize("prec", [TF32, BF16])
+def test_tensor_core_precision_layouts_off_the_kernels(cuda_lib, orc, prec):
+    """Layouts the tensor-core kernels do not take run on the fp32 kernel and meet the
+    precision's bound: pointers 4 bytes past a 16-byte boundary, and 160 query heads
+    over one kv head (more than a thread block's 128 rows)."""
+    q_seq, H, G, D = 70, 6, 2, 64
+    q, k, v = synthetic.forward_inputs(q_seq, q_seq, H, G, D, seed=41, qk_sigma=3.0)
+    ro, rl = orc.forward(q.numpy(), k.numpy(), v.numpy(), q_seq, q_seq, H, G, D, CAUSAL)
+    out = offset_view(torch.full((q_seq, H * D), float("nan")), (q_seq, H * D))
+    lse = torch.full((q_seq, H, 2), float("nan"), device="cuda")
+    cuda_lib.attn_forward(offset_view(q, (q_seq, H * D)), offset_view(k, (q_seq, G * D)),
+                          offset_view(v, (q_seq, G * D)), out, lse, q_seq, q_seq, H, G, D, CAUSAL, prec)
+    torch.cuda.synchronize()
+    assert cuda_lib.attn_get_status() == 0
+    assert_out_close(out.cpu().numpy(), ro, prec, float(v.abs().max()), "offset pointers")
+    assert_lse_close(lse.cpu().numpy(), rl, prec, float(np.abs(rl[..., 0]).max()), "offset pointers")
+
+    q_seq, H, G, D = 9, 160, 1, 64
+    q, k, v = synthetic.forward_inputs(q_seq, q_seq, H, G, D, seed=42)
+    ro, rl = orc.forward(q.numpy(), k.numpy(), v.numpy(), q_seq, q_seq, H, G, D, FULL)
+    out = torch.full((q_seq, H * D), float("nan"), device="cuda")
+    lse = torch.full((q_seq, H, 2), float("nan"), device="cuda")
+    cuda_lib.attn_forward(dev(q), dev(k), dev(v), out, lse, q_seq, q_seq, H, G, D, FULL, prec)
+    torch.cuda.synchronize()
+    assert cuda_lib.attn_get_status() == 0
+    assert_out_close(out.cpu().numpy(), ro, prec, float(v.abs().max()), "160 query heads per kv head")
+    assert_lse_close(lse.cpu().numpy(), rl, prec, float(np.abs(rl[..., 0]).max()), "160 query heads per kv head")
+
+
+def test_bf16_backward_group_of_three(cuda_lib, orc):
+    """bf16 operands with 3 query heads per kv head (not a power of two) run the fp32
+    backward: within the bf16 bound (2e-2 max|ref|), indeed within fp32's."""
+    q_seq, H, G, D = 90, 6, 2, 64
+    q, k, v = synthetic.forward_inputs(q_seq, q_seq, H, G, D, seed=43)
+    dout = torch.from_numpy(np.random.default_rng(44).standard_normal((q_seq, H * D)).astype(np.float32))
+    ref = orc.backward(q.numpy(), k.numpy(), v.numpy(), dout.numpy(), q_seq, q_seq, H, G, D, CAUSAL)
+    dq_, dk_, dv_, do_ = dev(q), dev(k), dev(v), dev(dout)
+    out = torch.empty((q_seq, H * D), device="cuda")
+    lse = torch.empty((q_seq, H, 2), device="cuda")
+    cuda_lib.attn_forward(dq_, dk_, dv_, out, lse, q_seq, q_seq, H, G, D, CAUSAL, FP32)
+    grads = [torch.full(shape, float("nan"), device="cuda") for shape in ((q_seq, H * D), (q_seq, G * D), (q_seq, G * D))]
+    cuda_lib.attn_backward(dq_, dk_, dv_, out, do_, lse, *grads, q_seq, q_seq, H, G, D, CAUSAL, BF16)
+    torch.cuda.synchronize()
+    assert cuda_lib.attn_get_status() == 0
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        err = float(np.abs(g.cpu().numpy() - r).max())
+        assert err <= 1e-5 + 1e-4 * float(np.abs(r).max()), "%s: %.3g" % (name, err)
