@@ -370,22 +370,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kQCols / 32; ++c) {
         const unsigned char* src = qstage + (grp * (kQCols / 32) + c) * kChunkBytes + r * 128;
-        const unsigned char* other = qstage + ((1 - grp) * (kQCols / 32) + c) * kChunkBytes + r * 128;
+        // The chunk's eight loads are issued before any is used.
+        float4 x[8];
+        if (r < rpb) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          float4 x = r < rpb ? *reinterpret_cast<const float4*>(src + 16 * (u ^ (r & 7))) : make_float4(0.f, 0.f, 0.f, 0.f);
-          if (cs != nullptr) {
-            const float4 y = r < rpb ? *reinterpret_cast<const float4*>(other + 16 * (u ^ (r & 7)))
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int u = 0; u < 8; ++u) x[u] = *reinterpret_cast<const float4*>(src + 16 * (u ^ (r & 7)));
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (cs != nullptr) {  // rows with a table are rows below rpb
+          const unsigned char* other = qstage + ((1 - grp) * (kQCols / 32) + c) * kChunkBytes + r * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 y = *reinterpret_cast<const float4*>(other + 16 * (u ^ (r & 7)));
             const float4 cv = *reinterpret_cast<const float4*>(cs + 32 * c + 4 * u);
             const float4 sv = *reinterpret_cast<const float4*>(cs + kQCols + 32 * c + 4 * u);
-            x = make_float4(fmaf(sgn * y.x, sv.x, x.x * cv.x), fmaf(sgn * y.y, sv.y, x.y * cv.y),
-                            fmaf(sgn * y.z, sv.z, x.z * cv.z), fmaf(sgn * y.w, sv.w, x.w * cv.w));
+            x[u] = make_float4(fmaf(sgn * y.x, sv.x, x[u].x * cv.x), fmaf(sgn * y.y, sv.y, x[u].y * cv.y),
+                               fmaf(sgn * y.z, sv.z, x[u].z * cv.z), fmaf(sgn * y.w, sv.w, x[u].w * cv.w));
           }
-          v[c][4 * u] = x.x * sl2;
-          v[c][4 * u + 1] = x.y * sl2;
-          v[c][4 * u + 2] = x.z * sl2;
-          v[c][4 * u + 3] = x.w * sl2;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          v[c][4 * u] = x[u].x * sl2;
+          v[c][4 * u + 1] = x[u].y * sl2;
+          v[c][4 * u + 2] = x[u].z * sl2;
+          v[c][4 * u + 3] = x[u].w * sl2;
           qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(v[c][4 * u]), fabsf(v[c][4 * u + 1])),
                                    fmaxf(fabsf(v[c][4 * u + 2]), fabsf(v[c][4 * u + 3]))));
         }
