@@ -204,6 +204,13 @@ def time_oracle_decode(min_seconds, kv_pos=KV_POS):
     return calls, el
 
 
+def decode_config(world):
+    """The headline workload, the same for both arms."""
+    return {"workload": DECODE_WORKLOAD, "heads": H, "kv_heads": G, "head_dim": D,
+            "l2": "inputs larger than 2x L2 between steps (rotating caches)",
+            "parallelism": "independent decode per GPU" if world > 1 else "single GPU"}
+
+
 def reference_arm(args, world, rank):
     """The fp64 CPU oracle on the host cores, same metric and workload.  Each
     step is a bounded sample: the decode over the first n' cache positions,
@@ -227,7 +234,7 @@ def reference_arm(args, world, rank):
         "impl": "reference", "metric": "decode K/V-stream bandwidth", "value": val, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": DECODE_WORKLOAD, "l2": "n/a (host)"},
+        "config": decode_config(world),
         "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -379,9 +386,8 @@ def run_ours(args, world, rank, local):
             "metric": "decode K/V-stream bandwidth", "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": DECODE_WORKLOAD, "heads": H, "kv_heads": G, "head_dim": D,
-                       "l2": "inputs rotate over %d K/V caches (%d MiB) > 2x L2" % (n_rot, n_rot * 2 * cache_bytes >> 20),
-                       "parallelism": "independent decode per GPU" if world > 1 else "single GPU"},
+            "config": decode_config(world),
+            "l2": "inputs rotate over %d K/V caches (%d MiB) > 2x L2" % (n_rot, n_rot * 2 * cache_bytes >> 20),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": "decode_split_kernel<128,4>", "kernel_us": kern_ms * 1e3,
