@@ -1,6 +1,8 @@
 // kv_prep.cu -- K/V operand pre-pass of the tensor-core flash kernels.
 //
-// One block per (128-key tile T, kv head g, tensor z), 512 threads; a row of
+// One block per (128-key tile T, kv head g) for K and, on the 16-bit path, two
+// per tile for V (64 rows each: V needs no tile-wide reduction, and the
+// smaller blocks leave the SMs sooner), 512 threads; a row of
 // one head is D/4 consecutive threads' float4 groups, so every load and store
 // is a coalesced row run.  Rows [128 T, 128 T + 128) at or past `rows_end`
 // are not written (the attention kernels' tensor maps end there).  Paged
@@ -36,6 +38,38 @@ __global__ void __launch_bounds__(kPrepThreads, 2) kv_prep_kernel(const PrepArgs
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.y;
   const bool is_k = blockIdx.z == 0;
+  if (!is_k) {
+    // V as bf16, half a tile per block (no reduction over the tile).
+    constexpr int kHalf = kPasses / 2;
+    const long long t0 = (long long)(p.tile0 + blockIdx.x) * 128 + 64 * (blockIdx.z - 1);
+    const int c4v = tid % kPerRow, rsv = tid / kPerRow;
+    const long long colv = (long long)g * D + 4 * c4v;
+    float4 xv[kHalf];
+    if (p.table == nullptr && t0 + 64 <= p.rows_end) {
+#pragma unroll
+      for (int i = 0; i < kHalf; ++i)
+        xv[i] = *reinterpret_cast<const float4*>(p.v + (t0 + i * kRowsPerPass + rsv) * p.stride + colv);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kHalf; ++i) {
+        const long long t = t0 + i * kRowsPerPass + rsv;
+        xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < p.rows_end) {
+          long long row = t;
+          if (p.table != nullptr) row = paged_row(p.table, p.page_rows, p.num_pages, (int)t, p.status);
+          if (row >= 0) xv[i] = *reinterpret_cast<const float4*>(p.v + row * p.stride + colv);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kHalf; ++i) {
+      const long long t = t0 + i * kRowsPerPass + rsv;
+      if (t < p.rows_end)
+        *reinterpret_cast<uint2*>(p.out1 + t * p.stride + colv) =
+            make_uint2(tc::pack_bf16(xv[i].x, xv[i].y), tc::pack_bf16(xv[i].z, xv[i].w));
+    }
+    return;
+  }
   const long long t_first = (long long)(p.tile0 + blockIdx.x) * 128;
   const int c4 = tid % kPerRow;  // float4 group within the row
   const int rsub = tid / kPerRow;
@@ -116,7 +150,7 @@ template <int D>
 cudaError_t launch_d(const PrepArgs& p, cudaStream_t s) {
   PrepArgs pp = p;
   void* args[] = {&pp};
-  const dim3 grid((unsigned)(p.n_tiles - p.tile0), (unsigned)p.G, p.out1 != nullptr ? 2u : 1u);
+  const dim3 grid((unsigned)(p.n_tiles - p.tile0), (unsigned)p.G, p.out1 != nullptr ? 3u : 1u);
   return launch_pdl(reinterpret_cast<const void*>(kv_prep_kernel<D>), grid, dim3(kPrepThreads), 0, s, args);
 }
 
