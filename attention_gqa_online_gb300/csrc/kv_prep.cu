@@ -37,8 +37,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) kv_prep_kernel(const PrepArgs
   allow_dependent_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.y;
-  const bool is_k = blockIdx.z == 0;
-  if (!is_k) {
+  if (blockIdx.z > 0) {
     // V as bf16, half a tile per block (no reduction over the tile).
     constexpr int kHalf = kPasses / 2;
     const long long t0 = (long long)(p.tile0 + blockIdx.x) * 128 + 64 * (blockIdx.z - 1);
@@ -73,7 +72,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) kv_prep_kernel(const PrepArgs
   const long long t_first = (long long)(p.tile0 + blockIdx.x) * 128;
   const int c4 = tid % kPerRow;  // float4 group within the row
   const int rsub = tid / kPerRow;
-  const float* src = is_k ? p.k : p.v;
+  const float* src = p.k;
   const long long col = (long long)g * D + 4 * c4;
   float4 x[kPasses];
   float mx = 0.f;
@@ -93,16 +92,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) kv_prep_kernel(const PrepArgs
         if (row >= 0) x[i] = *reinterpret_cast<const float4*>(src + row * p.stride + col);
       }
     }
-  }
-  if (!is_k) {  // V as bf16
-#pragma unroll
-    for (int i = 0; i < kPasses; ++i) {
-      const long long t = t_first + i * kRowsPerPass + rsub;
-      if (t < p.rows_end)
-        *reinterpret_cast<uint2*>(p.out1 + t * p.stride + col) =
-            make_uint2(tc::pack_bf16(x[i].x, x[i].y), tc::pack_bf16(x[i].z, x[i].w));
-    }
-    return;
   }
 #pragma unroll
   for (int i = 0; i < kPasses; ++i) {
