@@ -155,8 +155,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const unsigned kp_hint = *static_cast<const volatile uint32_t*>(a.kv_pos_dev);
     const SplitRange h = split_range(kp_hint, a.max_seq, a.window, S, j);
     // Twice as deep when one CTA serves all the query heads of its kv head;
-    // with several head groups, their duplicate hints cost more than they gain.
-    const int n_pf = a.kv_div == 1 ? 2 * kPrefetchStages : kPrefetchStages;
+    // with several head groups, whose CTAs hint the same rows, only the first
+    // two stages.
+    const int n_pf = a.kv_div == 1 ? 2 * kPrefetchStages : 2;
     for (int st = 0; st < n_pf && j < h.s_eff && h.p_begin + st * kT < h.p_end; ++st) {
       const int row = cache_row(a, h.p_begin + st * kT, true);
       tma_prefetch_l2_2d(&tm_k, kvh * D, row);
