@@ -235,6 +235,13 @@ def test_workspace_queries(lib):
     assert lib.attn_backward_workspace_bytes(n, n, H, G, D, 0, 1) == r((n * H + n * G) * D * 4) + r(n * H * 8)
     qe, ke = n * H * D, n * G * D
     assert lib.attn_backward_workspace_bytes(n, n, H, G, D, 2, 0) == 2 * r(n * H * 4) + 2 * r(qe * 2) + 2 * r(ke * 2)
+    # A tensor-core call whose layout runs on the fp32 kernel needs that kernel's
+    # scratch: the tensor-core precisions report at least the fp32 size.
+    for rope in (0, 1):
+        fp32 = lib.attn_forward_workspace_bytes(n, n, H, G, D, 0, 0, 0, rope)
+        for prec in (1, 2):
+            assert lib.attn_forward_workspace_bytes(n, n, H, G, D, 0, prec, 0, rope) >= fp32
+    assert lib.attn_backward_workspace_bytes(n, n, 6, 2, D, 2, 0) >= lib.attn_backward_workspace_bytes(n, n, 6, 2, D, 0, 0)
 
 
 def test_set_workspace_rejects_misaligned(lib):
